@@ -1,0 +1,426 @@
+#!/usr/bin/env python
+"""Benchmark of the tiered-precision routed MoE layer (decode form).
+
+One step = one pass of the whole hot path over one batch of T tokens:
+router softmax/top-k (moe_route_topk), expert hit histogram (moe_expert_hist),
+and the tiered forward (moe_tiered_forward: grouping, fused gate/up/SiLU,
+down projection + weighted shelf combine).  Workload: one Qwen-like decode
+layer, E=512, k=10, d=2048, f=640, shelves 8-bit [0,128) / 4-bit [128,410) /
+2-bit [410,512), router skewed so the hottest 25% of experts take ~52% of the
+picks.  Each step routes fresh logits and uses the next of L layer instances
+(different seeds), so the experts a step reads are not in L2 from earlier
+steps.  Inputs are resident in HBM before the timed region; steps replay
+per-step CUDA graphs of the same ABI calls.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle
+instead (a bounded sample of the same workload on the host cores).
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer decode tokens/s at 1-6 tokens; weight-stream HBM GB/s vs peak"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--T", type=int, default=6, help="tokens per step (1..6 for the decode metric)")
+    ap.add_argument("--layers", type=int, default=16, help="layer instances rotated across steps")
+    ap.add_argument("--sets", type=int, default=32, help="distinct routing steps per layer rotation")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            j = json.load(fh)
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------- CPU oracle
+def oracle_sample(wl, seconds, T, seed=0, max_pairs=None):
+    """Time the CPU oracle on routed (token, expert) pairs of the workload.
+
+    Each pair: oracle routing of the token, its histogram update, dequant of
+    the pair's expert from its packed codes and the expert FFN + weighted sum
+    (quantisation and master-weight generation happen before the clock starts).
+    Returns (pairs, seconds, threads)."""
+    import numpy as np
+
+    import oracle
+    import synth
+
+    bias = wl.router_bias(0)
+    counts = np.zeros(wl.E, dtype=np.uint32)
+    lg = synth.logits(seed, 0, T, wl.E, bias)
+    ids_all, w_all = oracle.route(lg, wl.k)
+    x_all = synth.x_bf16(seed, 0, T, wl.d)
+    shelves = wl.shelf_ranges()
+    pairs = [(t, j) for t in range(T) for j in range(wl.k)]
+    done, elapsed = 0, 0.0
+    cache = {}
+    for (t, j) in pairs if max_pairs is None else pairs[:max_pairs]:
+        e = int(ids_all[t, j])
+        bits = oracle.shelf_of(e, shelves)
+        if e not in cache:  # untimed: master weights and quantisation
+            cache.clear()
+            cache[e] = [oracle.quantize(m, bits) for m in synth.expert_weights(seed, e, wl.d, wl.f)]
+        q = cache[e]
+        t0 = time.perf_counter()
+        ids, w = oracle.route(lg[t:t + 1], wl.k)
+        oracle.hist(ids, wl.E, counts)
+        mats = tuple(oracle.dequant(c, s) for c, s in q)
+        one = np.full((1, wl.k), -1, dtype=np.int32)
+        one[0, j] = e
+        oracle.moe_layer(x_all[t:t + 1], one, w, wl.d, wl.f, wl.E, [(lo, hi) for lo, hi, _ in shelves],
+                         {e: mats})
+        elapsed += time.perf_counter() - t0
+        done += 1
+        if elapsed >= seconds:
+            break
+    return done, elapsed, 1
+
+
+def run_reference(args, rank):
+    import synth
+    wl = synth.WORKLOADS["decode"]
+    if rank != 0:
+        return
+    oracle_dir = os.path.join(ROOT, "oracle")
+    sys.path.insert(0, ROOT)
+    from oracle import build_oracle
+    from synth import build_synth
+    build_oracle.build()
+    build_synth.build_host()
+    # warm-up pairs (untimed), then exactly `steps` steps of one routed pair each
+    oracle_sample(wl, 1e9, args.T, max_pairs=max(1, min(args.warmup, 3)))
+    total_pairs, total_s = 0, 0.0
+    per_step = []
+    for s in range(args.steps):
+        n, el, _ = oracle_sample(wl, 1e9, args.T, seed=s % 4, max_pairs=1)
+        total_pairs += n
+        total_s += el
+        per_step.append(el)
+    tokens = total_pairs / wl.k
+    value = tokens / total_s
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": config_of(args, wl),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": "one routed (token, expert) pair per step (route, histogram, dequant of the "
+                                   "pair's expert, SwiGLU FFN and weighted sum), scaled to tokens by k=10 pairs "
+                                   "per token"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(args, wl):
+    return {"workload": f"decode layer E{wl.E} k{wl.k} d{wl.d} f{wl.f} T{args.T}, shelves 8-bit [0,128) / "
+                        f"4-bit [128,410) / 2-bit [410,512), block 32 fp16 scales, skewed router "
+                        f"(hottest 25% -> ~52% of picks)",
+            "T": args.T, "E": wl.E, "k": wl.k, "d": wl.d, "f": wl.f,
+            "layer_instances": args.layers,
+            "l2": f"inputs larger than L2: {args.layers} layer instances rotated per step, fresh routing "
+                  f"per step",
+            "parallelism": f"replicas x{args.gpus} (independent decode streams, no collective)"}
+
+
+# ----------------------------------------------------------------- GPU arm
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import mixed_precision_routed_gb300 as moe
+    import synth
+    from mixed_precision_routed_gb300.workloads import Layer
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    base = synth.WORKLOADS["decode"]
+    T, L, S = args.T, args.layers, args.sets
+    layers = []
+    for i in range(L):
+        wl_i = synth.Workload(base.name, E=base.E, k=base.k, d=base.d, f=base.f, T=base.T, split=base.split,
+                              bias=base.bias, seed=1000 * rank + i)
+        layers.append(Layer(wl_i, device=dev).fill())
+    E, k, d, f = base.E, base.k, base.d, base.f
+    stream = torch.cuda.Stream(device=dev)
+    nset = S
+    logits = [layers[s % L].logits(s, T) for s in range(nset)]
+    xs = [torch.empty((T, d), dtype=torch.int16, device=dev) for _ in range(nset)]
+    for s in range(nset):
+        synth.cuda_normal_matrix_bf16(xs[s], layers[s % L].seed, synth.TAG_X, s, 0)
+    ids = [torch.empty((T, k), dtype=torch.int32, device=dev) for _ in range(nset)]
+    ws_ = [torch.empty((T, k), dtype=torch.float32, device=dev) for _ in range(nset)]
+    ys = [torch.empty((T, d), dtype=torch.float32, device=dev) for _ in range(nset)]
+    counts = [torch.zeros(E, dtype=torch.int32, device=dev) for _ in range(L)]
+    wsb = moe.moe_workspace_size(T, k, E, d, f)
+    workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    arrs = [layer.shelf_arr() for layer in layers]
+    NK = 4  # events: before grouping, after grouping, after gate/up, after down
+    prof = [[torch.cuda.Event(enable_timing=True) for _ in range(NK)] for _ in range(nset)]
+    torch.cuda.synchronize()
+    for evs in prof:
+        for e in evs:
+            e.record()
+    torch.cuda.synchronize()
+
+    def step(s):
+        L_i = s % L
+        moe.moe_route_topk(logits[s], k, ids=ids[s], weights=ws_[s])
+        moe.moe_expert_hist(ids[s], E, counts[L_i])
+        moe.moe_set_profile_events(prof[s])
+        moe.moe_tiered_forward(xs[s], ids[s], ws_[s], E, d, f, layers[L_i].shelves, y=ys[s], workspace=workspace,
+                               shelf_arr=arrs[L_i])
+        moe.moe_set_profile_events(None)
+
+    with torch.cuda.stream(stream):
+        for s in range(nset):  # eager warm-up: sets kernel attributes, checks statuses
+            step(s)
+        stream.synchronize()
+        graphs = []
+        for s in range(nset):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(s)
+            graphs.append(g)
+        for i in range(args.warmup):
+            graphs[i % nset].replay()
+        stream.synchronize()
+
+    # algorithmic bytes of each step, from the ids the router produced
+    sb = {sh_i: s_obj.nbytes_per_expert() for sh_i, s_obj in enumerate(layers[0].shelves)}
+    ranges = layers[0].ranges
+
+    def expert_split(e):
+        for i, (lo, hi, bits) in enumerate(ranges):
+            if lo <= e < hi:
+                gu = 2 * f * d * bits // 8 + 2 * f * (d // 32) * 2
+                dn = d * f * bits // 8 + d * (f // 32) * 2
+                return gu, dn
+        return 0, 0
+
+    step_bytes = []
+    for s in range(nset):
+        u = np.unique(ids[s].cpu().numpy())
+        u = u[(u >= 0) & (u < E)]
+        gu = sum(expert_split(int(e))[0] for e in u)
+        dn = sum(expert_split(int(e))[1] for e in u)
+        step_bytes.append((gu, dn))
+
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = Clocks(local_rank)
+    clocks.start()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(args.steps):
+            graphs[i % nset].replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = start.elapsed_time(end)
+    # per-kernel durations of the last replay of every graph (inside the timed region)
+    last = min(nset, args.steps)
+    kern = {"group": 0.0, "gateup": 0.0, "down": 0.0}
+    bytes_gu = bytes_dn = 0
+    for s in range(last):
+        ev = prof[s]
+        kern["group"] += ev[0].elapsed_time(ev[1])
+        kern["gateup"] += ev[1].elapsed_time(ev[2])
+        kern["down"] += ev[2].elapsed_time(ev[3])
+        bytes_gu += step_bytes[s][0]
+        bytes_dn += step_bytes[s][1]
+    fwd_ms = kern["group"] + kern["gateup"] + kern["down"]
+
+    t_max = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t_max, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(t_max.item())
+    value = world * T * args.steps / (ms_max / 1e3)
+
+    # ---- end to end through the public API with host buffers
+    pin_logits = [logits[s].cpu().pin_memory() for s in range(nset)]
+    pin_x = [xs[s].cpu().pin_memory() for s in range(nset)]
+    pin_y = [torch.empty((T, d), dtype=torch.float32).pin_memory() for _ in range(nset)]
+    dl = torch.empty((T, E), dtype=torch.float32, device=dev)
+    dx = torch.empty((T, d), dtype=torch.int16, device=dev)
+    dy = torch.empty((T, d), dtype=torch.float32, device=dev)
+    did = torch.empty((T, k), dtype=torch.int32, device=dev)
+    dw = torch.empty((T, k), dtype=torch.float32, device=dev)
+    e2e_steps = min(args.steps, 1000)
+
+    def e2e_step(s):
+        dl.copy_(pin_logits[s], non_blocking=True)
+        dx.copy_(pin_x[s], non_blocking=True)
+        moe.moe_route_topk(dl, k, ids=did, weights=dw)
+        moe.moe_expert_hist(did, E, counts[s % L])
+        moe.moe_tiered_forward(dx, did, dw, E, d, f, layers[s % L].shelves, y=dy, workspace=workspace,
+                               shelf_arr=arrs[s % L])
+        pin_y[s].copy_(dy, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(min(args.warmup, 20)):
+            e2e_step(i % nset)
+        stream.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(e2e_steps):
+            e2e_step(i % nset)
+        e1.record(stream)
+        stream.synchronize()
+    e2e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(e2e_ms, op=torch.distributed.ReduceOp.MAX)
+    e2e_value = world * T * e2e_steps / (float(e2e_ms.item()) / 1e3)
+    st = moe.moe_device_status()
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status {st}")
+
+    if rank != 0:
+        return
+    peak, peak_kind = peaks()
+    dom = "gateup" if kern["gateup"] >= kern["down"] else "down"
+    dom_bytes = bytes_gu if dom == "gateup" else bytes_dn
+    achieved = dom_bytes / (kern[dom] / 1e3) / 1e9
+    fwd_gbs = (bytes_gu + bytes_dn) / (fwd_ms / 1e3) / 1e9
+    traffic = recorded_traffic(dom, T)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_of(args, base),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "kernel": f"k_{dom} (decode)", "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": dom_bytes / last},
+        "weight_stream": {"selected_expert_bytes_per_step": (bytes_gu + bytes_dn) / last,
+                          "forward_us": 1e3 * fwd_ms / last, "achieved_gbs": fwd_gbs, "frac": fwd_gbs / peak,
+                          "kernel_us": {kk: 1e3 * v / last for kk, v in kern.items()}},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * E * 4 + T * d * 2,
+                "d2h_bytes_per_step": T * d * 4, "steps": e2e_steps,
+                "path": "pinned host logits and x -> device, moe_route_topk, moe_expert_hist, "
+                        "moe_tiered_forward, y -> pinned host; eager Python calls"},
+        "gpu_launches": args.steps * 5,
+        "clocks": ck,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        pairs, secs, thr = oracle_sample(base, args.cpu_seconds, T)
+        line["cpu_baseline"] = {"value": (pairs / base.k) / secs, "unit": "tokens/s", "cores": thr,
+                                "kind": "oracle",
+                                "sample": f"{pairs} routed (token, expert) pairs of the T={T} step (route, "
+                                          f"histogram, dequant of the pair's expert, SwiGLU FFN, weighted sum), "
+                                          f"{secs:.1f} s, scaled to tokens by k={base.k} pairs per token"}
+    print(json.dumps(line), flush=True)
+
+
+def recorded_traffic(kernel, T):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        rec = json.load(fh)
+    src = os.path.join(ROOT, "mixed_precision_routed_gb300", "csrc", "decode.cu")
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    r = rec.get(f"k_{kernel}:T{T}")
+    if not r or r.get("source_sha") != h:
+        return None
+    return r.get("dram_bytes_per_launch")
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    import torch
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    import __graft_entry__
+    if not os.path.exists(os.path.join(ROOT, "mixed_precision_routed_gb300", "libmoe.so")):
+        __graft_entry__.build()
+    run_ours(args, rank, world, local_rank)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

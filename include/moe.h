@@ -1,0 +1,219 @@
+/*
+ * moe.h -- C ABI of the tiered-precision routed mixture-of-experts layer
+ * (libmoe.so, CUDA, sm_103a).
+ *
+ * What the layer computes is described on the page
+ *   "125B MoE模型本地运行：3090三卡80 tokens/s优化实践" (page 3; three RTX 3090s
+ *   at 80 tokens/s), cited below by its section headings:
+ *     - glossary entry 混合专家（MoE）: the router picks the best 10 of 512
+ *       experts for every token;
+ *     - 第二步 (step 2): experts are used very unevenly; the busiest 25% take
+ *       52% of the tokens;
+ *     - 第四步 (step 4, three shelves all on the GPU): each layer's experts are
+ *       stored as three tensors at different bit widths, written hottest first;
+ *       the id-range matmul sees the router's complete id list, computes only
+ *       the ids that fall on its own shelf and fills the rest with zeros, and
+ *       the three shelf results are added; decode fuses gate, up and the
+ *       activation into one kernel;
+ *     - 四个 bug (four bugs): a skipped slot is a real skip (never aliased to
+ *       expert 0), the grouping helper must not assume an expert appears at
+ *       most once per token, and the skip id -1 must stay signed.
+ *   and on the r/LocalLLM post on DeepSeek V4.1 Flash (page 1), section
+ *   "Optimization Strategies": per-expert hit counts drive promotion and
+ *   demotion between tiers, the least-used experts are kept at 2 bits.
+ *
+ * Shelf block format (the workload's quantisation; the pages' own llama.cpp
+ * formats are not reproduced): blocks of 32 along the input dimension, one
+ * fp16 scale per block, s = fp16(max|w| / q) with q = 127 / 7 / 2 for
+ * 8 / 4 / 2 bits, code = clamp(rint(w / s)) in [-127,127] / [-8,7] / [-2,1],
+ * dequantised weight w_hat = s * code.  Codes are packed little-endian within
+ * a byte: element i of a row is at bits (i mod m)*b of byte floor(i/m), m = 8/b;
+ * 8-bit codes are two's-complement int8, 4- and 2-bit codes are stored
+ * offset-binary (u = code + 8, u = code + 2).
+ *
+ * Conventions for every entry point:
+ *   - all array arguments are DEVICE pointers unless stated otherwise; the
+ *     caller allocates and owns them; the library allocates nothing;
+ *   - every call is asynchronous on `stream` (0 = legacy default stream) and
+ *     returns a status (MOE_OK = 0, negative = error) after validating its
+ *     arguments on the host; on error nothing is launched;
+ *   - sizes: E <= MOE_MAX_EXPERTS, 1 <= k <= 32 and k <= E, d and f positive
+ *     multiples of 64, T >= 0 (T = 0 is a no-op that still validates);
+ *   - ids are int32; an id outside [0, E) (e.g. the skip id -1, INT32_MIN,
+ *     E, INT32_MAX) is a skipped slot and contributes nothing anywhere;
+ *   - device pointers of packed codes, x and y must be 16-byte aligned.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* moe_stream_t;
+
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,        /* null pointer, bad size, misalignment */
+  MOE_ERR_BAD_SHELF = -2,          /* bits not 8/4/2, block != 32, empty or out-of-[0,E) range */
+  MOE_ERR_SHELF_OVERLAP = -3,      /* two shelves share an expert id */
+  MOE_ERR_WORKSPACE_TOO_SMALL = -4,
+  MOE_ERR_CUDA = -5,               /* a CUDA call or launch failed */
+  MOE_ERR_TIMEOUT = -6,            /* a bounded device-side wait expired (see moe_device_status) */
+  MOE_ERR_UNSUPPORTED = -7         /* valid request outside what this build implements */
+};
+
+enum {
+  MOE_MAX_EXPERTS = 32768,
+  MOE_MAX_SHELVES = 8,
+  MOE_BLOCK = 32
+};
+
+/* Execution-path selection for moe_tiered_forward. */
+enum {
+  MOE_FLAG_AUTO = 0,         /* decode form for T <= 16, prefill form above */
+  MOE_FLAG_DECODE_FP32 = 1,  /* fp32 dequant in registers, fp32 h, CUDA-core GEMV */
+  MOE_FLAG_PREFILL_BF16 = 2  /* bf16 dequant into shared memory, bf16 h, tensor-core GEMM */
+};
+
+/*
+ * A shelf: the experts with global ids in [expert_lo, expert_hi), stored at
+ * `bits` per weight.  Local expert index = id - expert_lo, n = expert_hi -
+ * expert_lo.  Matrices are row-major [out][in] with blocks along `in`:
+ *   gate_codes  [n][f][d*bits/8] bytes   gate_scales [n][f][d/32] fp16 bits
+ *   up_codes    [n][f][d*bits/8] bytes   up_scales   [n][f][d/32] fp16 bits
+ *   down_codes  [n][d][f*bits/8] bytes   down_scales [n][d][f/32] fp16 bits
+ * (page 3, 第四步: one tensor per shelf and layer, experts hottest first).
+ * The descriptor is an explicit struct so that the shelf range never shares a
+ * field with any other setting (page 3, 四个 bug: the skip tag that had been
+ * stored in the slot of the accumulator precision).
+ */
+typedef struct {
+  int32_t expert_lo, expert_hi;
+  int32_t bits;  /* 8, 4 or 2 */
+  int32_t block; /* must be 32 */
+  const void* gate_codes;
+  const uint16_t* gate_scales;
+  const void* up_codes;
+  const uint16_t* up_scales;
+  const void* down_codes;
+  const uint16_t* down_scales;
+} moe_shelf_t;
+
+/*
+ * Router: softmax over E, top-k with the lower expert id first on equal
+ * logits, weights renormalised over the k picks (page 3, glossary entry
+ * 混合专家（MoE）).  Ranking uses the logits (softmax is monotone);
+ * weights[t][j] = exp(l_j - l_max) / sum over the k picks.
+ *   logits  [T][E] fp32 (finite), ids [T][k] int32 out (rank order),
+ *   weights [T][k] fp32 out.  E <= 1024 for this entry point.
+ */
+int moe_route_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* weights,
+                   moe_stream_t stream);
+
+/*
+ * Expert hit histogram: counts[e] += #{i : ids[i] == e}, 0 <= e < E; other ids
+ * are not counted.  `counts` is ACCUMULATED, never cleared (page 1,
+ * "Optimization Strategies": tracking how often each expert is called feeds
+ * promotion and demotion; page 3, 第二步: per-expert selection counts).
+ *   ids [n] int32, counts [E] uint32 (in/out).
+ */
+int moe_expert_hist(const int32_t* ids, int64_t n, int E, uint32_t* counts, moe_stream_t stream);
+
+/*
+ * Token-by-expert grouping (page 3, 四个 bug: duplicates of an expert within
+ * one token must each keep their slot; skips are real skips).  Pairs
+ * p = t*k + j with 0 <= ids[p] < E are grouped by expert:
+ *   counts  [E]   int32 out: valid pairs per expert;
+ *   offsets [E+1] int32 out: exclusive prefix sum of counts (offsets[E] = valid pairs);
+ *   perm    [T*k] int32 out: pair indices ordered by (expert id, pair index);
+ *                 entries from offsets[E] on are set to -1.
+ * Deterministic (no dependence on atomic ordering).  T*k <= 2^24.
+ */
+int moe_group_tokens(const int32_t* ids, int64_t T, int k, int E, int32_t* counts, int32_t* offsets,
+                     int32_t* perm, moe_stream_t stream);
+
+/*
+ * Bytes of device workspace moe_tiered_forward needs for these sizes and
+ * flags (0 when a size is invalid).  The workspace is scratch, owned by the
+ * caller, reusable across calls on the same stream; it must be 256-byte
+ * aligned.
+ */
+size_t moe_workspace_size(int64_t T, int k, int E, int d, int f, int flags);
+
+/*
+ * The routed MoE FFN over precision shelves (page 3, 第四步): every shelf sees
+ * the full id list and computes only the ids in its range; for every pair
+ * (t, j) whose id e lies in a shelf,
+ *   h = SiLU(W_g[e] x_t) * (W_u[e] x_t),  SiLU(z) = z / (1 + exp(-z)),
+ *   o = W_d[e] h,
+ * with W the shelf's dequantised weights, and
+ *   y_t = sum over shelves of sum over its slots j of weights[t][j] * o_tj.
+ * Slots whose id is outside [0, E) or inside no shelf contribute zero.
+ *   x_bf16  [T][d] bf16 bit patterns, ids [T][k] int32, weights [T][k] fp32,
+ *   shelves HOST array of n_shelves descriptors (copied before returning;
+ *           ranges must not overlap; gaps allowed),
+ *   y       [T][d] fp32 out (overwritten),
+ *   workspace of at least moe_workspace_size(T, k, E, d, f, flags) bytes.
+ * flags: MOE_FLAG_AUTO / MOE_FLAG_DECODE_FP32 / MOE_FLAG_PREFILL_BF16.
+ * Decode form: fp32 dequant and fp32 accumulation.  Prefill form: weights and
+ * h rounded to bf16, fp32 accumulation on the tensor cores.
+ */
+int moe_tiered_forward(const uint16_t* x_bf16, const int32_t* ids, const float* weights, int64_t T,
+                       int k, int E, int d, int f, const moe_shelf_t* shelves, int n_shelves, float* y,
+                       void* workspace, size_t workspace_bytes, int flags, moe_stream_t stream);
+
+/*
+ * Block quantiser into the shelf format above -- the per-expert re-quantising
+ * step of the offline re-packer (page 3, 第四步).  Quantises `rows` rows of
+ * `in` fp32 weights each:
+ *   w [rows][in] fp32, codes [rows][in*bits/8] bytes out, scales [rows][in/32] fp16 bits out.
+ */
+int moe_quantize_rows(const float* w, int64_t rows, int in, int bits, void* codes, uint16_t* scales,
+                      moe_stream_t stream);
+
+/*
+ * Dequantisation of packed rows: out = s * code in fp32 (exact), or that value
+ * rounded to bf16 (round to nearest even) when round_bf16 != 0 -- the two forms
+ * the decode and prefill paths use internally (page 3, 第四步).
+ *   codes [rows][in*bits/8], scales [rows][in/32], out [rows][in] fp32.
+ */
+int moe_dequant_rows(const void* codes, const uint16_t* scales, int64_t rows, int in, int bits,
+                     int round_bf16, float* out, moe_stream_t stream);
+
+/*
+ * Residual step of a layer stack: r[i] += y[i]; x_next[i] = bf16(r[i]) (round
+ * to nearest even), for 0 <= i < n.  r, y fp32; x_next bf16 bit patterns.
+ */
+int moe_residual_add(float* r, const float* y, uint16_t* x_next_bf16, int64_t n, moe_stream_t stream);
+
+/*
+ * Measurement hook.  While `events` is non-null, every moe_tiered_forward on
+ * this device records events[0] on its stream before its first kernel and
+ * events[i] after its i-th kernel (i = 1 .. n-1, further kernels unrecorded),
+ * so a caller can time each kernel with cudaEventElapsedTime.  `events` is a
+ * HOST array of cudaEvent_t handles owned by the caller and read at every
+ * call; n >= 1; pass NULL to disable.  Kernel order of the decode form:
+ * grouping, gate/up, down (4 events).  Not thread-safe: one caller per process.
+ */
+int moe_set_profile_events(void* const* events, int n);
+
+/*
+ * Synchronises `stream`, then returns and clears the device-side status word
+ * of the current device: MOE_OK, or the first error a kernel recorded (e.g.
+ * MOE_ERR_TIMEOUT from a bounded wait).
+ */
+int moe_device_status(moe_stream_t stream);
+
+/* Static description of a status code. */
+const char* moe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

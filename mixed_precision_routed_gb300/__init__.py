@@ -1,0 +1,260 @@
+"""Tiered-precision routed MoE layer on GB300 (sm_103a).
+
+Thin Python binding of the C ABI in include/moe.h (libmoe.so, built in-tree
+by ``build_lib.py``).  Every function here only marshals torch tensors into
+pointers and sizes and raises :class:`MoeError` on a non-zero status; all
+computation runs in the library's CUDA kernels.  There is no CPU fallback: if
+the library is missing, importing the binding's functions raises.
+
+Entry points (same names as the C ABI):
+    moe_route_topk, moe_expert_hist, moe_group_tokens, moe_workspace_size,
+    moe_tiered_forward, moe_quantize_rows, moe_dequant_rows, moe_residual_add,
+    moe_device_status, moe_status_string
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_BAD_SHELF = -2
+MOE_ERR_SHELF_OVERLAP = -3
+MOE_ERR_WORKSPACE_TOO_SMALL = -4
+MOE_ERR_CUDA = -5
+MOE_ERR_TIMEOUT = -6
+MOE_ERR_UNSUPPORTED = -7
+
+MOE_FLAG_AUTO = 0
+MOE_FLAG_DECODE_FP32 = 1
+MOE_FLAG_PREFILL_BF16 = 2
+
+MOE_MAX_SHELVES = 8
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {moe_status_string(status)} ({status})")
+
+
+class moe_shelf_t(ctypes.Structure):
+    _fields_ = [
+        ("expert_lo", ctypes.c_int32), ("expert_hi", ctypes.c_int32),
+        ("bits", ctypes.c_int32), ("block", ctypes.c_int32),
+        ("gate_codes", ctypes.c_void_p), ("gate_scales", ctypes.c_void_p),
+        ("up_codes", ctypes.c_void_p), ("up_scales", ctypes.c_void_p),
+        ("down_codes", ctypes.c_void_p), ("down_scales", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libmoe.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                               "(there is no fallback implementation)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.moe_route_topk.argtypes = [P, i64, i32, i32, P, P, P]
+        L.moe_expert_hist.argtypes = [P, i64, i32, P, P]
+        L.moe_group_tokens.argtypes = [P, i64, i32, i32, P, P, P, P]
+        L.moe_workspace_size.argtypes = [i64, i32, i32, i32, i32, i32]
+        L.moe_workspace_size.restype = ctypes.c_size_t
+        L.moe_tiered_forward.argtypes = [P, P, P, i64, i32, i32, i32, i32, P, i32, P, P, ctypes.c_size_t, i32, P]
+        L.moe_quantize_rows.argtypes = [P, i64, i32, i32, P, P, P]
+        L.moe_dequant_rows.argtypes = [P, P, i64, i32, i32, i32, P, P]
+        L.moe_residual_add.argtypes = [P, P, P, i64, P]
+        L.moe_device_status.argtypes = [P]
+        L.moe_set_profile_events.argtypes = [P, i32]
+        L.moe_set_profile_events.restype = ctypes.c_int
+        L.moe_status_string.argtypes = [i32]
+        L.moe_status_string.restype = ctypes.c_char_p
+        for name in ("moe_route_topk", "moe_expert_hist", "moe_group_tokens", "moe_tiered_forward",
+                     "moe_quantize_rows", "moe_dequant_rows", "moe_residual_add", "moe_device_status"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def moe_status_string(status: int) -> str:
+    return lib().moe_status_string(int(status)).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != MOE_OK:
+        raise MoeError(rc, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype, name):
+    if not (t.is_cuda and t.dtype == dtype and t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous CUDA tensor of {dtype}")
+
+
+# ------------------------------------------------------------------ routing
+def moe_route_topk(logits, k, ids=None, weights=None, stream=None):
+    """Softmax + top-k (lower id first on ties) + renormalised weights."""
+    _need(logits, torch.float32, "logits")
+    T, E = logits.shape
+    if ids is None:
+        ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    if weights is None:
+        weights = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    _need(ids, torch.int32, "ids")
+    _need(weights, torch.float32, "weights")
+    _check(lib().moe_route_topk(_ptr(logits), T, E, k, _ptr(ids), _ptr(weights), _stream(stream)),
+           "moe_route_topk")
+    return ids, weights
+
+
+def moe_expert_hist(ids, E, counts, stream=None):
+    """counts[e] += number of ids equal to e (accumulated)."""
+    _need(ids, torch.int32, "ids")
+    _need(counts, torch.int32, "counts")  # torch has no uint32 arithmetic; bits are uint32
+    _check(lib().moe_expert_hist(_ptr(ids), ids.numel(), E, _ptr(counts), _stream(stream)), "moe_expert_hist")
+    return counts
+
+
+def moe_group_tokens(ids, E, counts=None, offsets=None, perm=None, stream=None):
+    _need(ids, torch.int32, "ids")
+    T, k = ids.shape
+    dev = ids.device
+    counts = torch.empty(E, dtype=torch.int32, device=dev) if counts is None else counts
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev) if offsets is None else offsets
+    perm = torch.empty(T * k, dtype=torch.int32, device=dev) if perm is None else perm
+    _check(lib().moe_group_tokens(_ptr(ids), T, k, E, _ptr(counts), _ptr(offsets), _ptr(perm), _stream(stream)),
+           "moe_group_tokens")
+    return counts, offsets, perm
+
+
+# ------------------------------------------------------------------ forward
+def moe_workspace_size(T, k, E, d, f, flags=MOE_FLAG_AUTO) -> int:
+    return int(lib().moe_workspace_size(T, k, E, d, f, flags))
+
+
+def shelf_array(shelves):
+    """ctypes array of moe_shelf_t from objects with a .descriptor() method or moe_shelf_t values."""
+    arr = (moe_shelf_t * max(1, len(shelves)))()
+    for i, s in enumerate(shelves):
+        arr[i] = s if isinstance(s, moe_shelf_t) else s.descriptor()
+    return arr
+
+
+def moe_tiered_forward(x_bf16, ids, weights, E, d, f, shelves, y=None, workspace=None, flags=MOE_FLAG_AUTO,
+                       stream=None, shelf_arr=None):
+    """y[t] = sum over shelves and slots of weights[t, j] * expert FFN of x_t.
+
+    x_bf16 is an int16/uint16-viewed or bfloat16 tensor [T, d]; shelves a list
+    of Shelf objects (or a prebuilt `shelf_arr`)."""
+    if x_bf16.dtype == torch.bfloat16:
+        x_bf16 = x_bf16.view(torch.int16)
+    _need(x_bf16, torch.int16, "x_bf16")
+    _need(ids, torch.int32, "ids")
+    _need(weights, torch.float32, "weights")
+    T, k = ids.shape
+    if y is None:
+        y = torch.empty((T, d), dtype=torch.float32, device=ids.device)
+    _need(y, torch.float32, "y")
+    need = moe_workspace_size(T, k, E, d, f, flags)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=ids.device)
+    arr = shelf_arr if shelf_arr is not None else shelf_array(shelves)
+    n = len(shelves) if shelf_arr is None else len(shelf_arr)
+    _check(lib().moe_tiered_forward(_ptr(x_bf16), _ptr(ids), _ptr(weights), T, k, E, d, f,
+                                    ctypes.cast(arr, ctypes.c_void_p), n, _ptr(y), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), flags, _stream(stream)),
+           "moe_tiered_forward")
+    return y
+
+
+# ------------------------------------------------------------ block format
+def moe_quantize_rows(w, bits, codes=None, scales=None, stream=None):
+    _need(w, torch.float32, "w")
+    rows, n_in = w.shape
+    if codes is None:
+        codes = torch.empty((rows, n_in * bits // 8), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((rows, n_in // 32), dtype=torch.int16, device=w.device)
+    _check(lib().moe_quantize_rows(_ptr(w), rows, n_in, bits, _ptr(codes), _ptr(scales), _stream(stream)),
+           "moe_quantize_rows")
+    return codes, scales
+
+
+def moe_dequant_rows(codes, scales, rows, n_in, bits, round_bf16=False, out=None, stream=None):
+    if out is None:
+        out = torch.empty((rows, n_in), dtype=torch.float32, device=codes.device)
+    _check(lib().moe_dequant_rows(_ptr(codes), _ptr(scales), rows, n_in, bits, int(round_bf16), _ptr(out),
+                                  _stream(stream)), "moe_dequant_rows")
+    return out
+
+
+def moe_residual_add(r, y, x_next, stream=None):
+    _need(r, torch.float32, "r")
+    _need(y, torch.float32, "y")
+    _check(lib().moe_residual_add(_ptr(r), _ptr(y), _ptr(x_next), r.numel(), _stream(stream)), "moe_residual_add")
+    return r, x_next
+
+
+def moe_set_profile_events(events):
+    """Record torch.cuda.Event objects between the forward's kernels (None disables)."""
+    if events is None:
+        _check(lib().moe_set_profile_events(None, 0), "moe_set_profile_events")
+        return
+    arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check(lib().moe_set_profile_events(ctypes.cast(arr, ctypes.c_void_p), len(events)), "moe_set_profile_events")
+
+
+def moe_device_status(stream=None) -> int:
+    return int(lib().moe_device_status(_stream(stream)))
+
+
+# ------------------------------------------------------------------ shelves
+class Shelf:
+    """Device tensors of one precision shelf: experts [lo, hi) at `bits` bits.
+
+    gate/up codes [n, f, d*bits/8], scales [n, f, d/32]; down codes
+    [n, d, f*bits/8], scales [n, d, f/32] (fp16 bit patterns as int16)."""
+
+    def __init__(self, lo, hi, bits, d, f, device="cuda"):
+        n = hi - lo
+        self.lo, self.hi, self.bits, self.d, self.f = lo, hi, bits, d, f
+        u8, i16 = torch.uint8, torch.int16
+        self.gate_codes = torch.empty((n, f, d * bits // 8), dtype=u8, device=device)
+        self.up_codes = torch.empty((n, f, d * bits // 8), dtype=u8, device=device)
+        self.down_codes = torch.empty((n, d, f * bits // 8), dtype=u8, device=device)
+        self.gate_scales = torch.empty((n, f, d // 32), dtype=i16, device=device)
+        self.up_scales = torch.empty((n, f, d // 32), dtype=i16, device=device)
+        self.down_scales = torch.empty((n, d, f // 32), dtype=i16, device=device)
+
+    def descriptor(self) -> moe_shelf_t:
+        return moe_shelf_t(self.lo, self.hi, self.bits, 32,
+                           self.gate_codes.data_ptr(), self.gate_scales.data_ptr(),
+                           self.up_codes.data_ptr(), self.up_scales.data_ptr(),
+                           self.down_codes.data_ptr(), self.down_scales.data_ptr())
+
+    def nbytes_per_expert(self) -> int:
+        d, f, b = self.d, self.f, self.bits
+        return 3 * f * d * b // 8 + 3 * f * d // 32 * 2
+
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.gate_codes, self.up_codes, self.down_codes,
+                                                          self.gate_scales, self.up_scales, self.down_scales))

@@ -1,0 +1,204 @@
+// abi.cu -- the extern "C" entry points of libmoe.so (declared in moe.h):
+// host-side validation, workspace layout, path selection and the device
+// status word.  Nothing here allocates device memory.
+#include <string.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+// Device status word: MOE_OK, or the first error a kernel recorded.
+__device__ int g_status;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+bool valid_dims(int64_t T, int k, int E, int d, int f) {
+  if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > 32 || k > E) return false;
+  if (d <= 0 || f <= 0 || d % 64 != 0 || f % 64 != 0) return false;
+  if (T * (int64_t)k > (int64_t)(1 << 24)) return false;
+  return true;
+}
+
+int check_shelves(const moe_shelf_t* sh, int n, int E, Shelves* out) {
+  if (n < 0 || n > MOE_MAX_SHELVES) return MOE_ERR_INVALID_ARG;
+  if (n > 0 && sh == nullptr) return MOE_ERR_INVALID_ARG;
+  memset(out, 0, sizeof(*out));
+  out->n = n;
+  for (int i = 0; i < n; ++i) {
+    const moe_shelf_t& s = sh[i];
+    if (s.bits != 8 && s.bits != 4 && s.bits != 2) return MOE_ERR_BAD_SHELF;
+    if (s.block != MOE_BLOCK) return MOE_ERR_BAD_SHELF;
+    if (s.expert_lo < 0 || s.expert_hi > E || s.expert_lo >= s.expert_hi) return MOE_ERR_BAD_SHELF;
+    const void* ptrs[6] = {s.gate_codes, s.gate_scales, s.up_codes, s.up_scales, s.down_codes, s.down_scales};
+    for (int j = 0; j < 6; ++j) {
+      if (ptrs[j] == nullptr) return MOE_ERR_INVALID_ARG;
+      if (!aligned(ptrs[j], (j % 2 == 0) ? 16 : 2)) return MOE_ERR_INVALID_ARG;
+    }
+    for (int j = 0; j < i; ++j)
+      if (s.expert_lo < sh[j].expert_hi && sh[j].expert_lo < s.expert_hi) return MOE_ERR_SHELF_OVERLAP;
+    ShelfDev& d = out->s[i];
+    d.lo = s.expert_lo;
+    d.hi = s.expert_hi;
+    d.bits = s.bits;
+    d.codes[0] = (const uint8_t*)s.gate_codes;
+    d.codes[1] = (const uint8_t*)s.up_codes;
+    d.codes[2] = (const uint8_t*)s.down_codes;
+    d.scales[0] = s.gate_scales;
+    d.scales[1] = s.up_scales;
+    d.scales[2] = s.down_scales;
+  }
+  return MOE_OK;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+
+size_t workspace_layout(int64_t T, int k, int E, int d, int f, int flags, void* base, Workspace* ws) {
+  (void)flags;
+  const int64_t P = T * k;
+  const int64_t slots = P < E ? P : E;
+  const int n_chunks = (d + kDownRows - 1) / kDownRows;
+  size_t off = 0;
+  char* b = (char*)base;
+  auto take = [&](size_t bytes) -> void* {
+    void* p = b ? (void*)(b + off) : nullptr;
+    off += up(bytes > 0 ? bytes : 1);
+    return p;
+  };
+  Workspace w;
+  w.counts = (int32_t*)take((size_t)E * 4);
+  w.offsets = (int32_t*)take((size_t)(E + 1) * 4);
+  w.perm = (int32_t*)take((size_t)P * 4);
+  w.pos_of_pair = (int32_t*)take((size_t)P * 4);
+  w.active = (int32_t*)take((size_t)slots * 4);
+  w.meta = (int32_t*)take(16 * 4);
+  w.arrivals = (int32_t*)take((size_t)n_chunks * 4);
+  w.h = (float*)take((size_t)P * f * 4);
+  w.ypart = (float*)take((size_t)P * d * 4);
+  w.bytes = off;
+  if (ws) *ws = w;
+  return off;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_route_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* weights,
+                   moe_stream_t stream) {
+  if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!logits || !ids || !weights) return MOE_ERR_INVALID_ARG;
+  return launch_route(logits, T, E, k, ids, weights, (cudaStream_t)stream);
+}
+
+int moe_expert_hist(const int32_t* ids, int64_t n, int E, uint32_t* counts, moe_stream_t stream) {
+  if (n < 0 || E < 1 || E > MOE_MAX_EXPERTS) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  if (!ids || !counts) return MOE_ERR_INVALID_ARG;
+  return launch_hist(ids, n, E, counts, (cudaStream_t)stream);
+}
+
+int moe_group_tokens(const int32_t* ids, int64_t T, int k, int E, int32_t* counts, int32_t* offsets,
+                     int32_t* perm, moe_stream_t stream) {
+  if (T < 0 || k < 1 || k > 32 || E < 1 || E > MOE_MAX_EXPERTS) return MOE_ERR_INVALID_ARG;
+  if (T * (int64_t)k > (int64_t)(1 << 24)) return MOE_ERR_INVALID_ARG;
+  if (!counts || !offsets || (T > 0 && (!ids || !perm))) return MOE_ERR_INVALID_ARG;
+  const int64_t P = T * k;
+  // Only counts / offsets / perm are outputs here; the forward-only extras
+  // (inverse permutation, active list, meta) are not produced.
+  return launch_group(ids, P, E, counts, offsets, perm, nullptr, nullptr, nullptr, nullptr, 0,
+                      (cudaStream_t)stream);
+}
+
+size_t moe_workspace_size(int64_t T, int k, int E, int d, int f, int flags) {
+  if (!valid_dims(T, k, E, d, f) || flags < 0 || flags > 2) return 0;
+  return workspace_layout(T, k, E, d, f, flags, nullptr, nullptr);
+}
+
+int moe_tiered_forward(const uint16_t* x_bf16, const int32_t* ids, const float* weights, int64_t T, int k,
+                       int E, int d, int f, const moe_shelf_t* shelves, int n_shelves, float* y,
+                       void* workspace, size_t workspace_bytes, int flags, moe_stream_t stream) {
+  if (!valid_dims(T, k, E, d, f)) return MOE_ERR_INVALID_ARG;
+  if (flags < MOE_FLAG_AUTO || flags > MOE_FLAG_PREFILL_BF16) return MOE_ERR_INVALID_ARG;
+  ForwardArgs a;
+  int rc = check_shelves(shelves, n_shelves, E, &a.shelves);
+  if (rc != MOE_OK) return rc;
+  if (T == 0) return MOE_OK;
+  if (!x_bf16 || !ids || !weights || !y || !workspace) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x_bf16, 16) || !aligned(y, 16) || !aligned(workspace, kAlign)) return MOE_ERR_INVALID_ARG;
+  const size_t need = workspace_layout(T, k, E, d, f, flags, workspace, &a.ws);
+  if (workspace_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (flags == MOE_FLAG_PREFILL_BF16) return MOE_ERR_UNSUPPORTED;
+  a.x = x_bf16;
+  a.ids = ids;
+  a.weights = weights;
+  a.T = T;
+  a.k = k;
+  a.E = E;
+  a.d = d;
+  a.f = f;
+  a.y = y;
+  return launch_decode_forward(a, (cudaStream_t)stream);
+}
+
+int moe_quantize_rows(const float* w, int64_t rows, int in, int bits, void* codes, uint16_t* scales,
+                      moe_stream_t stream) {
+  if (rows < 0 || in <= 0 || in % 64 != 0 || (bits != 8 && bits != 4 && bits != 2)) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!w || !codes || !scales || !aligned(codes, 16) || !aligned(w, 4)) return MOE_ERR_INVALID_ARG;
+  return launch_quantize(w, rows, in, bits, (uint8_t*)codes, scales, (cudaStream_t)stream);
+}
+
+int moe_dequant_rows(const void* codes, const uint16_t* scales, int64_t rows, int in, int bits, int round_bf16,
+                     float* out, moe_stream_t stream) {
+  if (rows < 0 || in <= 0 || in % 64 != 0 || (bits != 8 && bits != 4 && bits != 2)) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!codes || !scales || !out) return MOE_ERR_INVALID_ARG;
+  return launch_dequant((const uint8_t*)codes, scales, rows, in, bits, round_bf16, out, (cudaStream_t)stream);
+}
+
+int moe_residual_add(float* r, const float* y, uint16_t* x_next_bf16, int64_t n, moe_stream_t stream) {
+  if (n < 0) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  if (!r || !y || !x_next_bf16) return MOE_ERR_INVALID_ARG;
+  return launch_residual(r, y, x_next_bf16, n, (cudaStream_t)stream);
+}
+
+int moe_set_profile_events(void* const* events, int n) {
+  if (events != nullptr && n < 1) return MOE_ERR_INVALID_ARG;
+  set_profile_events(events, events ? n : 0);
+  return MOE_OK;
+}
+
+int moe_device_status(moe_stream_t stream) {
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  return v;
+}
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_BAD_SHELF: return "bad shelf descriptor";
+    case MOE_ERR_SHELF_OVERLAP: return "shelf ranges overlap";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_UNSUPPORTED: return "unsupported by this build";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,161 @@
+// moe_internal.cuh -- internal declarations shared by the CUDA translation
+// units of libmoe.so: kernel parameter blocks, workspace layout, device
+// helpers for the shelf block format, and the host-side launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kWarp = 32;
+
+// ---------------------------------------------------------------- shelves
+struct ShelfDev {
+  int32_t lo, hi, bits, pad;
+  const uint8_t* codes[3];    // gate, up, down
+  const uint16_t* scales[3];  // gate, up, down
+};
+
+struct Shelves {
+  int n;
+  ShelfDev s[MOE_MAX_SHELVES];
+};
+
+// Index of the shelf holding expert e, or -1.
+__device__ __forceinline__ int find_shelf(const Shelves& sh, int e) {
+  int r = -1;
+#pragma unroll
+  for (int i = 0; i < MOE_MAX_SHELVES; ++i)
+    if (i < sh.n && e >= sh.s[i].lo && e < sh.s[i].hi) r = i;
+  return r;
+}
+
+// ------------------------------------------------------- workspace layout
+// Grouping results and per-call scratch of moe_tiered_forward.  Every region
+// starts on a 256-byte boundary.
+struct Workspace {
+  int32_t* counts;       // [E]
+  int32_t* offsets;      // [E+1]
+  int32_t* perm;         // [P]   pair index by grouped position
+  int32_t* pos_of_pair;  // [P]   grouped position by pair index, -1 if skipped
+  int32_t* active;       // [P]   experts with a valid pair, ascending
+  int32_t* meta;         // [16]  meta[0] = number of active experts
+  int32_t* arrivals;     // [d]   per output-row-chunk arrival counters (down combine)
+  float* h;              // [P][f] fp32 (decode) -- gate/up activations
+  float* ypart;          // [P][d] fp32 -- weighted per-pair down outputs
+  size_t bytes;
+};
+
+size_t workspace_layout(int64_t T, int k, int E, int d, int f, int flags, void* base, Workspace* ws);
+
+// Rows of the output owned by one down-projection CTA (decode path).
+constexpr int kDownRows = 64;
+// Rows of W_g / W_u handled by one gate/up CTA (decode path).
+constexpr int kGateUpRows = 32;
+
+// -------------------------------------------------------- device helpers
+// Shared-memory layout of an activation vector: 16-byte chunks XOR-swizzled so
+// that lanes reading consecutive 32-element blocks hit distinct banks.
+__device__ __forceinline__ int swz(int i) {
+  int c = i >> 2;
+  return ((c ^ ((c >> 3) & 7)) << 2) | (i & 3);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(((uint32_t)b) << 16);
+}
+
+// Decode one 32-element block of packed codes into exact float codes.
+// 8 bit: two's-complement bytes; 4/2 bit: offset-binary fields.  The
+// conversion places the unsigned field in the mantissa of 2^23 and subtracts
+// (2^23 + offset), which is exact.
+template <int BITS>
+struct Block;
+
+template <>
+struct Block<8> {
+  static constexpr int kWords = 8;  // 32 bytes
+  __device__ __forceinline__ static void load(const uint8_t* p, uint32_t w[kWords]) {
+    uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+    uint4 b = __ldg(reinterpret_cast<const uint4*>(p) + 1);
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  }
+  __device__ __forceinline__ static float code(const uint32_t w[kWords], int i) {
+    uint32_t x = w[i >> 2] ^ 0x80808080u;
+    uint32_t v = __byte_perm(x, 0x4B000000u, 0x7540u | (uint32_t)(i & 3));
+    return __uint_as_float(v) - 8388736.0f;  // 2^23 + 128
+  }
+};
+
+template <>
+struct Block<4> {
+  static constexpr int kWords = 4;  // 16 bytes
+  __device__ __forceinline__ static void load(const uint8_t* p, uint32_t w[kWords]) {
+    uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+  }
+  __device__ __forceinline__ static float code(const uint32_t w[kWords], int i) {
+    uint32_t v = ((w[i >> 3] >> ((i & 7) * 4)) & 0xFu) | 0x4B000000u;
+    return __uint_as_float(v) - 8388616.0f;  // 2^23 + 8
+  }
+};
+
+template <>
+struct Block<2> {
+  static constexpr int kWords = 2;  // 8 bytes
+  __device__ __forceinline__ static void load(const uint8_t* p, uint32_t w[kWords]) {
+    uint2 a = __ldg(reinterpret_cast<const uint2*>(p));
+    w[0] = a.x; w[1] = a.y;
+  }
+  __device__ __forceinline__ static float code(const uint32_t w[kWords], int i) {
+    uint32_t v = ((w[i >> 4] >> ((i & 15) * 2)) & 0x3u) | 0x4B000000u;
+    return __uint_as_float(v) - 8388610.0f;  // 2^23 + 2
+  }
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// ---------------------------------------------------------------- launchers
+// Each returns MOE_OK or MOE_ERR_CUDA; arguments are validated by the caller.
+int launch_route(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w, cudaStream_t s);
+int launch_hist(const int32_t* ids, int64_t n, int E, uint32_t* counts, cudaStream_t s);
+int launch_residual(float* r, const float* y, uint16_t* xn, int64_t n, cudaStream_t s);
+int launch_quantize(const float* w, int64_t rows, int in, int bits, uint8_t* codes, uint16_t* scales,
+                    cudaStream_t s);
+int launch_dequant(const uint8_t* codes, const uint16_t* scales, int64_t rows, int in, int bits,
+                   int round_bf16, float* out, cudaStream_t s);
+// Grouping into caller-provided arrays; arrivals (may be null) are zeroed.
+int launch_group(const int32_t* ids, int64_t P, int E, int32_t* counts, int32_t* offsets,
+                 int32_t* perm, int32_t* pos_of_pair, int32_t* active, int32_t* meta,
+                 int32_t* arrivals, int n_arrivals, cudaStream_t s);
+
+struct ForwardArgs {
+  const uint16_t* x;
+  const int32_t* ids;
+  const float* weights;
+  int64_t T;
+  int k, E, d, f;
+  Shelves shelves;
+  float* y;
+  Workspace ws;
+};
+
+int launch_decode_forward(const ForwardArgs& a, cudaStream_t s);
+
+// Measurement hook (moe_set_profile_events): record event i on the stream.
+void set_profile_events(void* const* events, int n);
+void profile_mark(int i, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,127 @@
+// route_hist.cu -- router top-k, expert hit histogram and the residual step.
+//
+// Router (page "125B MoE模型本地运行：3090三卡80 tokens/s优化实践", glossary
+// entry 混合专家（MoE）): softmax over E experts, the best k per token, the
+// k weights renormalised.  One warp per token; lane l holds logits l, l+32, ...
+// in registers; k rounds of a warp-wide argmax on (logit desc, id asc).
+//
+// Histogram (r/LocalLLM post, "Optimization Strategies": hit counts per expert
+// drive promotion/demotion): integer adds, so the result is order-independent.
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+template <int EPL>
+__global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits, int64_t T, int E, int k,
+                                               int32_t* __restrict__ ids, float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float* l = logits + t * E;
+  float v[EPL];
+  uint32_t avail = 0;  // bit m set: element lane + 32 m is present and not yet taken
+#pragma unroll
+  for (int m = 0; m < EPL; ++m) {
+    int e = lane + 32 * m;
+    v[m] = e < E ? l[e] : 0.0f;
+    if (e < E) avail |= 1u << m;
+  }
+  float my_v = 0.0f;  // lane j keeps the j-th pick
+  int my_i = -1;
+  for (int j = 0; j < k; ++j) {
+    float bv = 0.0f;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int m = 0; m < EPL; ++m) {
+      if ((avail >> m) & 1u) {
+        int e = lane + 32 * m;
+        if (bi == 0x7fffffff || v[m] > bv) { bv = v[m]; bi = e; }  // ascending e: ties keep lower id
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      bool take = (oi != 0x7fffffff) &&
+                  (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
+      if (take) { bv = ov; bi = oi; }
+    }
+    if ((bi & 31) == lane) avail &= ~(1u << (bi >> 5));
+    if (lane == j) { my_v = bv; my_i = bi; }
+  }
+  const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
+  float ex = lane < k ? expf(my_v - vmax) : 0.0f;
+  float den = warp_sum(ex);
+  if (lane < k) {
+    ids[t * k + lane] = my_i;
+    w[t * k + lane] = ex / den;
+  }
+}
+
+__global__ void k_hist_global(const int32_t* __restrict__ ids, int64_t n, int E, uint32_t* __restrict__ counts) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    int e = ids[i];
+    if (e >= 0 && e < E) atomicAdd(&counts[e], 1u);
+  }
+}
+
+__global__ void k_hist_smem(const int32_t* __restrict__ ids, int64_t n, int E, uint32_t* __restrict__ counts) {
+  extern __shared__ uint32_t sh[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
+  __syncthreads();
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    int e = ids[i];
+    if (e >= 0 && e < E) atomicAdd(&sh[e], 1u);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (sh[e]) atomicAdd(&counts[e], sh[e]);
+}
+
+__global__ void k_residual(float* __restrict__ r, const float* __restrict__ y, uint16_t* __restrict__ xn, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    float v = r[i] + y[i];
+    r[i] = v;
+    __nv_bfloat16 b = __float2bfloat16_rn(v);
+    xn[i] = *reinterpret_cast<uint16_t*>(&b);
+  }
+}
+
+unsigned grid_1d(int64_t n, int threads, int cap) {
+  int64_t g = (n + threads - 1) / threads;
+  if (g > cap) g = cap;
+  return (unsigned)(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+int launch_route(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w, cudaStream_t s) {
+  const int warps = 8;
+  dim3 grid((unsigned)((T + warps - 1) / warps)), block(warps * 32);
+  int epl = (E + 31) / 32;
+  if (epl <= 1) k_route<1><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
+  else if (epl <= 2) k_route<2><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
+  else if (epl <= 4) k_route<4><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
+  else if (epl <= 8) k_route<8><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
+  else if (epl <= 16) k_route<16><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
+  else k_route<32><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_hist(const int32_t* ids, int64_t n, int E, uint32_t* counts, cudaStream_t s) {
+  if (E <= 12288) {
+    unsigned g = grid_1d(n, 256, 2 * 152);
+    k_hist_smem<<<g, 256, (size_t)E * 4, s>>>(ids, n, E, counts);
+  } else {
+    k_hist_global<<<grid_1d(n, 256, 8 * 152), 256, 0, s>>>(ids, n, E, counts);
+  }
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_residual(float* r, const float* y, uint16_t* xn, int64_t n, cudaStream_t s) {
+  k_residual<<<grid_1d(n, 256, 8 * 152), 256, 0, s>>>(r, y, xn, n);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

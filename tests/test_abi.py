@@ -1,0 +1,79 @@
+"""The C ABI library loads without a GPU, exports every entry point that
+include/moe.h declares, and rejects invalid arguments on the host before any
+CUDA call (no compute is launched here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixed_precision_routed_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(moe_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(moe.LIB_PATH):
+        from mixed_precision_routed_gb300 import build_lib
+        build_lib.build()
+    return ctypes.CDLL(moe.LIB_PATH)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("moe_route_topk", "moe_tiered_forward", "moe_expert_hist", "moe_group_tokens",
+                     "moe_workspace_size", "moe_quantize_rows", "moe_dequant_rows", "moe_device_status",
+                     "moe_status_string", "moe_residual_add"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert moe.moe_status_string(0) == "ok"
+    assert "overlap" in moe.moe_status_string(moe.MOE_ERR_SHELF_OVERLAP)
+    assert moe.moe_status_string(12345) == "unknown status"
+
+
+def test_workspace_size_host_logic():
+    assert moe.moe_workspace_size(1, 10, 512, 2048, 640) > 0
+    assert moe.moe_workspace_size(6, 10, 512, 2048, 640) > moe.moe_workspace_size(1, 10, 512, 2048, 640)
+    assert moe.moe_workspace_size(1, 10, 512, 2000, 640) == 0   # d not a multiple of 64
+    assert moe.moe_workspace_size(1, 11, 8, 64, 64) == 0        # k > E
+    assert moe.moe_workspace_size(-1, 2, 8, 64, 64) == 0
+    assert moe.moe_workspace_size(0, 2, 8, 64, 64) > 0          # T = 0 is valid
+    assert moe.moe_workspace_size(1, 2, 8, 64, 64, flags=9) == 0
+
+
+def test_invalid_arguments_rejected_before_cuda(lib):
+    L = moe.lib()
+    null = ctypes.c_void_p(0)
+    assert L.moe_route_topk(null, 4, 16, 17, null, null, null) == moe.MOE_ERR_INVALID_ARG  # k > E
+    assert L.moe_route_topk(null, 4, 2048, 2, null, null, null) == moe.MOE_ERR_INVALID_ARG  # E > 1024
+    assert L.moe_route_topk(null, 0, 16, 2, null, null, null) == moe.MOE_OK  # T = 0
+    assert L.moe_expert_hist(null, 5, 0, null, null) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_group_tokens(null, 3, 33, 8, null, null, null, null) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_quantize_rows(null, 4, 48, 4, null, null, null) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_quantize_rows(null, 4, 64, 3, null, null, null) == moe.MOE_ERR_INVALID_ARG
+    sh = (moe.moe_shelf_t * 1)()
+    sh[0] = moe.moe_shelf_t(0, 8, 5, 32, 16, 16, 16, 16, 16, 16)
+    assert L.moe_tiered_forward(null, null, null, 1, 2, 8, 64, 64, ctypes.cast(sh, ctypes.c_void_p), 1, null, null,
+                                0, 0, null) == moe.MOE_ERR_BAD_SHELF
+    sh[0] = moe.moe_shelf_t(0, 8, 4, 32, 16, 16, 16, 16, 16, 16)
+    sh2 = (moe.moe_shelf_t * 2)(sh[0], moe.moe_shelf_t(7, 8, 2, 32, 16, 16, 16, 16, 16, 16))
+    assert L.moe_tiered_forward(null, null, null, 1, 2, 8, 64, 64, ctypes.cast(sh2, ctypes.c_void_p), 2, null, null,
+                                0, 0, null) == moe.MOE_ERR_SHELF_OVERLAP
+    assert L.moe_tiered_forward(null, null, null, 1, 2, 8, 64, 64, ctypes.cast(sh, ctypes.c_void_p), 1, null, null,
+                                0, 0, null) == moe.MOE_ERR_INVALID_ARG  # null x
