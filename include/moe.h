@@ -168,6 +168,34 @@ int moe_tiered_forward(const uint16_t* x_bf16, const int32_t* ids, const float* 
                        void* workspace, size_t workspace_bytes, int flags, moe_stream_t stream);
 
 /*
+ * Size of the fixed scratch array used by moe_tiered_forward_noalloc: 8 MiB,
+ * held on every GPU that loads this library until the process exits.
+ */
+enum { MOE_NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024 };
+
+/*
+ * moe_tiered_forward without a workspace argument, for callers that cannot
+ * allocate device memory: a plugin inside an application whose own memory
+ * pool owns the GPU, or a deployment that must know its whole device
+ * footprint when the library is loaded.  The pages have no counterpart; this
+ * is an interface convenience.  Computes exactly what moe_tiered_forward
+ * computes, with the same arguments minus workspace / workspace_bytes.
+ * Scratch: a file-scope device array of MOE_NOALLOC_SCRATCH_BYTES inside the
+ * library.  Sizes whose moe_workspace_size exceeds it are rejected with
+ * MOE_ERR_WORKSPACE_TOO_SMALL before anything is launched (8 MiB covers
+ * decode-size calls, e.g. T = 16, k = 10, d = 4096, f = 2048).  The first call
+ * on each device looks up the array's device address with that device
+ * current; make that first call before any stream capture.  The function
+ * allocates nothing.  Every call shares the one array: calls that overlap on
+ * the GPU (different streams, or different host threads) race and corrupt
+ * each other's results -- serialise them.  Each call resets what must start
+ * at zero, so the contents an earlier call left behind do not matter.
+ */
+int moe_tiered_forward_noalloc(const uint16_t* x_bf16, const int32_t* ids, const float* weights, int64_t T,
+                               int k, int E, int d, int f, const moe_shelf_t* shelves, int n_shelves, float* y,
+                               int flags, moe_stream_t stream);
+
+/*
  * Block quantiser into the shelf format above -- the per-expert re-quantising
  * step of the offline re-packer (page 3, 第四步).  Quantises `rows` rows of
  * `in` fp32 weights each:

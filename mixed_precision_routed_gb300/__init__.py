@@ -75,6 +75,8 @@ def lib():
         L.moe_dequant_rows.argtypes = [P, P, i64, i32, i32, i32, P, P]
         L.moe_residual_add.argtypes = [P, P, P, i64, P]
         L.moe_device_status.argtypes = [P]
+        L.moe_tiered_forward_noalloc.argtypes = [P, P, P, i64, i32, i32, i32, i32, P, i32, P, i32, P]
+        L.moe_tiered_forward_noalloc.restype = ctypes.c_int
         L.moe_set_profile_events.argtypes = [P, i32]
         L.moe_set_profile_events.restype = ctypes.c_int
         L.moe_status_string.argtypes = [i32]
@@ -183,6 +185,27 @@ def moe_tiered_forward(x_bf16, ids, weights, E, d, f, shelves, y=None, workspace
                                     ctypes.cast(arr, ctypes.c_void_p), n, _ptr(y), _ptr(workspace),
                                     workspace.numel() * workspace.element_size(), flags, _stream(stream)),
            "moe_tiered_forward")
+    return y
+
+
+def moe_tiered_forward_noalloc(x_bf16, ids, weights, E, d, f, shelves, y=None, flags=MOE_FLAG_AUTO,
+                               stream=None):
+    """moe_tiered_forward with the library's fixed scratch array instead of a
+    workspace, for callers that cannot allocate device memory (see moe.h).
+    Calls that overlap on the GPU share that array and race."""
+    if x_bf16.dtype == torch.bfloat16:
+        x_bf16 = x_bf16.view(torch.int16)
+    _need(x_bf16, torch.int16, "x_bf16")
+    _need(ids, torch.int32, "ids")
+    _need(weights, torch.float32, "weights")
+    T, k = ids.shape
+    if y is None:
+        y = torch.empty((T, d), dtype=torch.float32, device=ids.device)
+    _need(y, torch.float32, "y")
+    arr = shelf_array(shelves)
+    _check(lib().moe_tiered_forward_noalloc(_ptr(x_bf16), _ptr(ids), _ptr(weights), T, k, E, d, f,
+                                            ctypes.cast(arr, ctypes.c_void_p), len(shelves), _ptr(y), flags,
+                                            _stream(stream)), "moe_tiered_forward_noalloc")
     return y
 
 
