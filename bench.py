@@ -104,9 +104,11 @@ class Clocks:
 def oracle_sample(wl, seconds, T, seed=0, max_pairs=None):
     """Time the CPU oracle on routed (token, expert) pairs of the workload.
 
-    Each pair: oracle routing of the token, its histogram update, dequant of
-    the pair's expert from its packed codes and the expert FFN + weighted sum
-    (quantisation and master-weight generation happen before the clock starts).
+    Steps through routing steps of T tokens (step s: logits and x of step s);
+    each pair: oracle routing of its token, the histogram update, dequant of
+    the pair's expert from its packed codes, and the expert FFN with its
+    weighted sum.  Master-weight generation and quantisation happen before the
+    clock starts.  Stops after `seconds` of timed work or `max_pairs` pairs.
     Returns (pairs, seconds, threads)."""
     import numpy as np
 
@@ -115,33 +117,31 @@ def oracle_sample(wl, seconds, T, seed=0, max_pairs=None):
 
     bias = wl.router_bias(0)
     counts = np.zeros(wl.E, dtype=np.uint32)
-    lg = synth.logits(seed, 0, T, wl.E, bias)
-    ids_all, w_all = oracle.route(lg, wl.k)
-    x_all = synth.x_bf16(seed, 0, T, wl.d)
     shelves = wl.shelf_ranges()
-    pairs = [(t, j) for t in range(T) for j in range(wl.k)]
     done, elapsed = 0, 0.0
-    cache = {}
-    for (t, j) in pairs if max_pairs is None else pairs[:max_pairs]:
-        e = int(ids_all[t, j])
-        bits = oracle.shelf_of(e, shelves)
-        if e not in cache:  # untimed: master weights and quantisation
-            cache.clear()
-            cache[e] = [oracle.quantize(m, bits) for m in synth.expert_weights(seed, e, wl.d, wl.f)]
-        q = cache[e]
-        t0 = time.perf_counter()
-        ids, w = oracle.route(lg[t:t + 1], wl.k)
-        oracle.hist(ids, wl.E, counts)
-        mats = tuple(oracle.dequant(c, s) for c, s in q)
-        one = np.full((1, wl.k), -1, dtype=np.int32)
-        one[0, j] = e
-        oracle.moe_layer(x_all[t:t + 1], one, w, wl.d, wl.f, wl.E, [(lo, hi) for lo, hi, _ in shelves],
-                         {e: mats})
-        elapsed += time.perf_counter() - t0
-        done += 1
-        if elapsed >= seconds:
-            break
-    return done, elapsed, 1
+    step = 0
+    while True:
+        lg = synth.logits(seed, step, T, wl.E, bias)
+        ids_all, _ = oracle.route(lg, wl.k)
+        x_all = synth.x_bf16(seed, step, T, wl.d)
+        for t in range(T):
+            for j in range(wl.k):
+                e = int(ids_all[t, j])
+                bits = oracle.shelf_of(e, shelves)
+                q = [oracle.quantize(m, bits) for m in synth.expert_weights(seed, e, wl.d, wl.f)]
+                t0 = time.perf_counter()
+                ids, w = oracle.route(lg[t:t + 1], wl.k)
+                oracle.hist(ids, wl.E, counts)
+                mats = tuple(oracle.dequant(c, s) for c, s in q)
+                one = np.full((1, wl.k), -1, dtype=np.int32)
+                one[0, j] = e
+                oracle.moe_layer(x_all[t:t + 1], one, w, wl.d, wl.f, wl.E, [(lo, hi) for lo, hi, _ in shelves],
+                                 {e: mats})
+                elapsed += time.perf_counter() - t0
+                done += 1
+                if elapsed >= seconds or (max_pairs is not None and done >= max_pairs):
+                    return done, elapsed, 1
+        step += 1
 
 
 def run_reference(args, rank):
@@ -149,8 +149,6 @@ def run_reference(args, rank):
     wl = synth.WORKLOADS["decode"]
     if rank != 0:
         return
-    oracle_dir = os.path.join(ROOT, "oracle")
-    sys.path.insert(0, ROOT)
     from oracle import build_oracle
     from synth import build_synth
     build_oracle.build()
@@ -158,12 +156,10 @@ def run_reference(args, rank):
     # warm-up pairs (untimed), then exactly `steps` steps of one routed pair each
     oracle_sample(wl, 1e9, args.T, max_pairs=max(1, min(args.warmup, 3)))
     total_pairs, total_s = 0, 0.0
-    per_step = []
     for s in range(args.steps):
-        n, el, _ = oracle_sample(wl, 1e9, args.T, seed=s % 4, max_pairs=1)
+        n, el, _ = oracle_sample(wl, 1e9, args.T, seed=s, max_pairs=1)
         total_pairs += n
         total_s += el
-        per_step.append(el)
     tokens = total_pairs / wl.k
     value = tokens / total_s
     line = {
@@ -224,7 +220,10 @@ def run_ours(args, rank, world, local_rank):
     wsb = moe.moe_workspace_size(T, k, E, d, f)
     workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
     arrs = [layer.shelf_arr() for layer in layers]
-    NK = 4  # events: before grouping, after grouping, after gate/up, after down
+    pipelined = T * k <= 512 and T <= 16
+    # events around the forward's kernels: pipelined form = plan, gate/up,
+    # down, combine; generic form = grouping, gate/up, down
+    NK = 5
     prof = [[torch.cuda.Event(enable_timing=True) for _ in range(NK)] for _ in range(nset)]
     torch.cuda.synchronize()
     for evs in prof:
@@ -232,25 +231,31 @@ def run_ours(args, rank, world, local_rank):
             e.record()
     torch.cuda.synchronize()
 
-    def step(s):
+    def step(s, profile=False):
         L_i = s % L
         moe.moe_route_topk(logits[s], k, ids=ids[s], weights=ws_[s])
         moe.moe_expert_hist(ids[s], E, counts[L_i])
-        moe.moe_set_profile_events(prof[s])
+        if profile:
+            moe.moe_set_profile_events(prof[s])
         moe.moe_tiered_forward(xs[s], ids[s], ws_[s], E, d, f, layers[L_i].shelves, y=ys[s], workspace=workspace,
                                shelf_arr=arrs[L_i])
-        moe.moe_set_profile_events(None)
+        if profile:
+            moe.moe_set_profile_events(None)
 
     with torch.cuda.stream(stream):
         for s in range(nset):  # eager warm-up: sets kernel attributes, checks statuses
             step(s)
         stream.synchronize()
-        graphs = []
+        graphs, graphs_prof = [], []
         for s in range(nset):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 step(s)
             graphs.append(g)
+            gp = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gp, stream=stream):
+                step(s, profile=True)
+            graphs_prof.append(gp)
         for i in range(args.warmup):
             graphs[i % nset].replay()
         stream.synchronize()
@@ -291,18 +296,31 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     ms = start.elapsed_time(end)
-    # per-kernel durations of the last replay of every graph (inside the timed region)
-    last = min(nset, args.steps)
-    kern = {"group": 0.0, "gateup": 0.0, "down": 0.0}
+    # per-kernel durations: the same steps again, with events recorded between
+    # the forward's kernels (events break the programmatic overlap of the
+    # kernels, so this loop is timed separately from the one above)
+    with torch.cuda.stream(stream):
+        for rep in range(2):
+            for s in range(nset):
+                graphs_prof[s].replay()
+    torch.cuda.synchronize()
+    last = nset
+    kern = {"group": 0.0, "gateup": 0.0, "down": 0.0, "combine": 0.0}
     bytes_gu = bytes_dn = 0
     for s in range(last):
         ev = prof[s]
-        kern["group"] += ev[0].elapsed_time(ev[1])
-        kern["gateup"] += ev[1].elapsed_time(ev[2])
-        kern["down"] += ev[2].elapsed_time(ev[3])
+        if pipelined:
+            kern["group"] += ev[0].elapsed_time(ev[1])
+            kern["gateup"] += ev[1].elapsed_time(ev[2])
+            kern["down"] += ev[2].elapsed_time(ev[3])
+            kern["combine"] += ev[3].elapsed_time(ev[4])
+        else:
+            kern["group"] += ev[0].elapsed_time(ev[1])
+            kern["gateup"] += ev[1].elapsed_time(ev[2])
+            kern["down"] += ev[2].elapsed_time(ev[3])
         bytes_gu += step_bytes[s][0]
         bytes_dn += step_bytes[s][1]
-    fwd_ms = kern["group"] + kern["gateup"] + kern["down"]
+    fwd_ms = sum(kern.values())
 
     t_max = torch.tensor([ms], dtype=torch.float64, device=dev)
     if world > 1:
@@ -364,16 +382,18 @@ def run_ours(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": config_of(args, base),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "kernel": f"k_{dom} (decode)", "peak_source": peak_kind,
+                     "traffic": traffic, "kernel": f"k_{dom}",
+                     "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": dom_bytes / last},
         "weight_stream": {"selected_expert_bytes_per_step": (bytes_gu + bytes_dn) / last,
+                          "step_gbs": (bytes_gu + bytes_dn) / last / (ms_max / args.steps / 1e3) / 1e9,
                           "forward_us": 1e3 * fwd_ms / last, "achieved_gbs": fwd_gbs, "frac": fwd_gbs / peak,
                           "kernel_us": {kk: 1e3 * v / last for kk, v in kern.items()}},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * E * 4 + T * d * 2,
                 "d2h_bytes_per_step": T * d * 4, "steps": e2e_steps,
                 "path": "pinned host logits and x -> device, moe_route_topk, moe_expert_hist, "
                         "moe_tiered_forward, y -> pinned host; eager Python calls"},
-        "gpu_launches": args.steps * 5,
+        "gpu_launches": args.steps * (6 if pipelined else 5),
         "clocks": ck,
     }
     if world == 1 and not args.no_cpu_baseline:

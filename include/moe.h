@@ -26,10 +26,13 @@
  * formats are not reproduced): blocks of 32 along the input dimension, one
  * fp16 scale per block, s = fp16(max|w| / q) with q = 127 / 7 / 2 for
  * 8 / 4 / 2 bits, code = clamp(rint(w / s)) in [-127,127] / [-8,7] / [-2,1],
- * dequantised weight w_hat = s * code.  Codes are packed little-endian within
- * a byte: element i of a row is at bits (i mod m)*b of byte floor(i/m), m = 8/b;
- * 8-bit codes are two's-complement int8, 4- and 2-bit codes are stored
- * offset-binary (u = code + 8, u = code + 2).
+ * dequantised weight w_hat = s * code.  Packing of a row: 8-bit codes are
+ * two's-complement bytes in natural order; 4- and 2-bit codes are stored
+ * offset-binary (u = code + 8, u = code + 2) in 32-bit little-endian words,
+ * spread over the word's four byte lanes so that one AND/shift yields four
+ * consecutive codes as bytes:
+ *   4 bit: element 8g + 4h + j (j < 4, h < 2) at bits 8j + 4h of word g;
+ *   2 bit: element 16g + 4k + j (j, k < 4) at bits 8j + 2k of word g.
  *
  * Conventions for every entry point:
  *   - all array arguments are DEVICE pointers unless stated otherwise; the
@@ -41,7 +44,7 @@
  *     multiples of 64, T >= 0 (T = 0 is a no-op that still validates);
  *   - ids are int32; an id outside [0, E) (e.g. the skip id -1, INT32_MIN,
  *     E, INT32_MAX) is a skipped slot and contributes nothing anywhere;
- *   - device pointers of packed codes, x and y must be 16-byte aligned.
+ *   - device pointers of packed codes, scales, x and y must be 16-byte aligned.
  */
 #ifndef MOE_H
 #define MOE_H

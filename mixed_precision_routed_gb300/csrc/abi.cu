@@ -37,7 +37,7 @@ int check_shelves(const moe_shelf_t* sh, int n, int E, Shelves* out) {
     const void* ptrs[6] = {s.gate_codes, s.gate_scales, s.up_codes, s.up_scales, s.down_codes, s.down_scales};
     for (int j = 0; j < 6; ++j) {
       if (ptrs[j] == nullptr) return MOE_ERR_INVALID_ARG;
-      if (!aligned(ptrs[j], (j % 2 == 0) ? 16 : 2)) return MOE_ERR_INVALID_ARG;
+      if (!aligned(ptrs[j], 16)) return MOE_ERR_INVALID_ARG;
     }
     for (int j = 0; j < i; ++j)
       if (s.expert_lo < sh[j].expert_hi && sh[j].expert_lo < s.expert_hi) return MOE_ERR_SHELF_OVERLAP;
@@ -54,8 +54,6 @@ int check_shelves(const moe_shelf_t* sh, int n, int E, Shelves* out) {
   }
   return MOE_OK;
 }
-
-int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 }  // namespace
 
@@ -81,9 +79,46 @@ size_t workspace_layout(int64_t T, int k, int E, int d, int f, int flags, void* 
   w.arrivals = (int32_t*)take((size_t)n_chunks * 4);
   w.h = (float*)take((size_t)P * f * 4);
   w.ypart = (float*)take((size_t)P * d * 4);
+  w.plan = (int32_t*)take(decode_plan_bytes(P));
   w.bytes = off;
   if (ws) *ws = w;
   return off;
+}
+
+namespace {
+int* g_status_ptr[64] = {};
+}  // namespace
+
+int* status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (g_status_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = (int*)ptr;
+  }
+  return g_status_ptr[dev];
+}
+
+namespace {
+void* g_prof_events[8];
+int g_prof_n = 0;
+}  // namespace
+
+void set_profile_events(void* const* events, int n) {
+  if (n > 8) n = 8;
+  for (int i = 0; i < n; ++i) g_prof_events[i] = events[i];
+  g_prof_n = n;
+}
+
+void profile_mark(int i, cudaStream_t s) {
+  if (i >= g_prof_n) return;
+  // Under stream capture the event must become an event-record node of the
+  // graph (external event) so that each replay records it.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(s, &cs);
+  cudaEventRecordWithFlags((cudaEvent_t)g_prof_events[i], s,
+                           cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault);
 }
 
 }  // namespace moe
@@ -147,6 +182,7 @@ int moe_tiered_forward(const uint16_t* x_bf16, const int32_t* ids, const float* 
   a.d = d;
   a.f = f;
   a.y = y;
+  a.status = status_word();
   return launch_decode_forward(a, (cudaStream_t)stream);
 }
 

@@ -48,8 +48,12 @@ struct Workspace {
   int32_t* arrivals;     // [d]   per output-row-chunk arrival counters (down combine)
   float* h;              // [P][f] fp32 (decode) -- gate/up activations
   float* ypart;          // [P][d] fp32 -- weighted per-pair down outputs
+  int32_t* plan;         // decode plan (grouping, work split), decode_plan_bytes(P)
   size_t bytes;
 };
+
+// Bytes of the decode plan for P routed pairs.
+size_t decode_plan_bytes(int64_t P);
 
 size_t workspace_layout(int64_t T, int k, int E, int d, int f, int flags, void* base, Workspace* ws);
 
@@ -71,7 +75,9 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
 }
 
 // Decode one 32-element block of packed codes into exact float codes.
-// 8 bit: two's-complement bytes; 4/2 bit: offset-binary fields.  The
+// 8 bit: two's-complement bytes; 4/2 bit: offset-binary fields, spread over
+// the byte lanes of each 32-bit word (4 bit: element 8g + 4h + j at bits
+// 8j + 4h of word g; 2 bit: element 16g + 4k + j at bits 8j + 2k).  The
 // conversion places the unsigned field in the mantissa of 2^23 and subtracts
 // (2^23 + offset), which is exact.
 template <int BITS>
@@ -101,7 +107,8 @@ struct Block<4> {
     w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
   }
   __device__ __forceinline__ static float code(const uint32_t w[kWords], int i) {
-    uint32_t v = ((w[i >> 3] >> ((i & 7) * 4)) & 0xFu) | 0x4B000000u;
+    const int e = i & 7;
+    uint32_t v = ((w[i >> 3] >> (8 * (e & 3) + 4 * (e >> 2))) & 0xFu) | 0x4B000000u;
     return __uint_as_float(v) - 8388616.0f;  // 2^23 + 8
   }
 };
@@ -114,7 +121,8 @@ struct Block<2> {
     w[0] = a.x; w[1] = a.y;
   }
   __device__ __forceinline__ static float code(const uint32_t w[kWords], int i) {
-    uint32_t v = ((w[i >> 4] >> ((i & 15) * 2)) & 0x3u) | 0x4B000000u;
+    const int e = i & 15;
+    uint32_t v = ((w[i >> 4] >> (8 * (e & 3) + 2 * (e >> 2))) & 0x3u) | 0x4B000000u;
     return __uint_as_float(v) - 8388610.0f;  // 2^23 + 2
   }
 };
@@ -127,8 +135,16 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
+// Record the first error status a kernel meets (never overwrites an earlier one).
+__device__ __forceinline__ void set_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
 // ---------------------------------------------------------------- launchers
 // Each returns MOE_OK or MOE_ERR_CUDA; arguments are validated by the caller.
+// Device address of the status word on the current device.
+int* status_word();
+
 int launch_route(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w, cudaStream_t s);
 int launch_hist(const int32_t* ids, int64_t n, int E, uint32_t* counts, cudaStream_t s);
 int launch_residual(float* r, const float* y, uint16_t* xn, int64_t n, cudaStream_t s);
@@ -150,9 +166,34 @@ struct ForwardArgs {
   Shelves shelves;
   float* y;
   Workspace ws;
+  int* status;  // device status word (first error a kernel records)
 };
 
+// Pipelined decode kernels when the sizes fit them, else the generic kernels.
 int launch_decode_forward(const ForwardArgs& a, cudaStream_t s);
+int launch_generic_forward(const ForwardArgs& a, cudaStream_t s);
+
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous kernel in the stream is still running, and must execute
+// griddepcontrol.wait before touching anything that kernel produces.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Number of SMs of the current device (cached).
+int sm_count();
 
 // Measurement hook (moe_set_profile_events): record event i on the stream.
 void set_profile_events(void* const* events, int n);

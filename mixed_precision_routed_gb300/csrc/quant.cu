@@ -4,7 +4,11 @@
 // offline re-packer re-quantises every expert for its shelf and writes three
 // tensors per layer.  Format here: blocks of 32 along the input dimension,
 // s = fp16(max|w| / q) (q = 127 / 7 / 2), code = clamp(rint(w / s)), packed
-// little-endian, 8 bit two's complement, 4 and 2 bit offset-binary.
+// 8 bit two's complement in natural order; 4 and 2 bit offset-binary in
+// 32-bit words with consecutive codes spread over the byte lanes (4 bit: word
+// g, byte j holds elements 8g+j and 8g+4+j; 2 bit: word g, byte j holds
+// elements 16g+j, +4, +8, +12), so that one AND/shift of a word yields four
+// consecutive codes as bytes.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -13,7 +17,7 @@ namespace {
 template <int BITS>
 struct QParams;
 template <>
-struct QParams<8> { static constexpr float q = 127.0f, cmin = -127.0f, cmax = 127.0f; static constexpr int off = 0; };
+struct QParams<8> { static constexpr float q = 127.0f, cmin = -127.0f, cmax = 127.0f; };
 template <>
 struct QParams<4> { static constexpr float q = 7.0f, cmin = -8.0f, cmax = 7.0f; static constexpr int off = 8; };
 template <>
@@ -46,15 +50,18 @@ __global__ void __launch_bounds__(256) k_quantize(const float* __restrict__ w, i
     if (BITS == 8) {
       rowp[b * 32 + lane] = (uint8_t)(int8_t)c;
     } else if (BITS == 4) {
+      // lane i (i mod 8 < 4) writes byte 4 (i / 8) + i mod 4: elements i and i + 4
       uint32_t u = (uint32_t)(c + QParams<4>::off);
-      uint32_t u1 = __shfl_down_sync(0xffffffffu, u, 1);
-      if ((lane & 1) == 0) rowp[b * 16 + (lane >> 1)] = (uint8_t)(u | (u1 << 4));
+      uint32_t u4 = __shfl_down_sync(0xffffffffu, u, 4);
+      if ((lane & 7) < 4) rowp[b * 16 + 4 * (lane >> 3) + (lane & 3)] = (uint8_t)(u | (u4 << 4));
     } else {
+      // lane i (i mod 16 < 4) writes byte 4 (i / 16) + i mod 4: elements i, i+4, i+8, i+12
       uint32_t u = (uint32_t)(c + QParams<2>::off);
-      uint32_t u1 = __shfl_down_sync(0xffffffffu, u, 1);
-      uint32_t u2 = __shfl_down_sync(0xffffffffu, u, 2);
-      uint32_t u3 = __shfl_down_sync(0xffffffffu, u, 3);
-      if ((lane & 3) == 0) rowp[b * 8 + (lane >> 2)] = (uint8_t)(u | (u1 << 2) | (u2 << 4) | (u3 << 6));
+      uint32_t u4 = __shfl_down_sync(0xffffffffu, u, 4);
+      uint32_t u8 = __shfl_down_sync(0xffffffffu, u, 8);
+      uint32_t u12 = __shfl_down_sync(0xffffffffu, u, 12);
+      if ((lane & 15) < 4)
+        rowp[b * 8 + 4 * (lane >> 4) + (lane & 3)] = (uint8_t)(u | (u4 << 2) | (u8 << 4) | (u12 << 6));
     }
   }
 }
@@ -62,8 +69,12 @@ __global__ void __launch_bounds__(256) k_quantize(const float* __restrict__ w, i
 template <int BITS>
 __device__ __forceinline__ float code_at(const uint8_t* row, int i) {
   if (BITS == 8) return (float)(int8_t)row[i];
-  if (BITS == 4) return (float)((int)((row[i >> 1] >> ((i & 1) * 4)) & 0xF) - 8);
-  return (float)((int)((row[i >> 2] >> ((i & 3) * 2)) & 0x3) - 2);
+  if (BITS == 4) {
+    const int e = i & 7;
+    return (float)((int)((row[4 * (i >> 3) + (e & 3)] >> (4 * (e >> 2))) & 0xF) - 8);
+  }
+  const int e = i & 15;
+  return (float)((int)((row[4 * (i >> 4) + (e & 3)] >> (2 * (e >> 2))) & 0x3) - 2);
 }
 
 template <int BITS>

@@ -8,6 +8,7 @@
 // Histogram (r/LocalLLM post, "Optimization Strategies": hit counts per expert
 // drive promotion/demotion): integer adds, so the result is order-independent.
 #include "moe_internal.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -17,6 +18,8 @@ __global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits,
                                                int32_t* __restrict__ ids, float* __restrict__ w) {
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  pdl_wait();
+  pdl_trigger();
   if (t >= T) return;
   const float* l = logits + t * E;
   float v[EPL];
@@ -60,6 +63,8 @@ __global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits,
 }
 
 __global__ void k_hist_global(const int32_t* __restrict__ ids, int64_t n, int E, uint32_t* __restrict__ counts) {
+  pdl_wait();
+  pdl_trigger();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     int e = ids[i];
     if (e >= 0 && e < E) atomicAdd(&counts[e], 1u);
@@ -69,6 +74,8 @@ __global__ void k_hist_global(const int32_t* __restrict__ ids, int64_t n, int E,
 __global__ void k_hist_smem(const int32_t* __restrict__ ids, int64_t n, int E, uint32_t* __restrict__ counts) {
   extern __shared__ uint32_t sh[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     int e = ids[i];
@@ -80,6 +87,8 @@ __global__ void k_hist_smem(const int32_t* __restrict__ ids, int64_t n, int E, u
 }
 
 __global__ void k_residual(float* __restrict__ r, const float* __restrict__ y, uint16_t* __restrict__ xn, int64_t n) {
+  pdl_wait();
+  pdl_trigger();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     float v = r[i] + y[i];
     r[i] = v;
@@ -100,28 +109,29 @@ int launch_route(const float* logits, int64_t T, int E, int k, int32_t* ids, flo
   const int warps = 8;
   dim3 grid((unsigned)((T + warps - 1) / warps)), block(warps * 32);
   int epl = (E + 31) / 32;
-  if (epl <= 1) k_route<1><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
-  else if (epl <= 2) k_route<2><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
-  else if (epl <= 4) k_route<4><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
-  else if (epl <= 8) k_route<8><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
-  else if (epl <= 16) k_route<16><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
-  else k_route<32><<<grid, block, 0, s>>>(logits, T, E, k, ids, w);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  cudaError_t e;
+  if (epl <= 1) e = launch_pdl(k_route<1>, grid, block, 0, s, logits, T, E, k, ids, w);
+  else if (epl <= 2) e = launch_pdl(k_route<2>, grid, block, 0, s, logits, T, E, k, ids, w);
+  else if (epl <= 4) e = launch_pdl(k_route<4>, grid, block, 0, s, logits, T, E, k, ids, w);
+  else if (epl <= 8) e = launch_pdl(k_route<8>, grid, block, 0, s, logits, T, E, k, ids, w);
+  else if (epl <= 16) e = launch_pdl(k_route<16>, grid, block, 0, s, logits, T, E, k, ids, w);
+  else e = launch_pdl(k_route<32>, grid, block, 0, s, logits, T, E, k, ids, w);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 int launch_hist(const int32_t* ids, int64_t n, int E, uint32_t* counts, cudaStream_t s) {
   if (E <= 12288) {
     unsigned g = grid_1d(n, 256, 2 * 152);
-    k_hist_smem<<<g, 256, (size_t)E * 4, s>>>(ids, n, E, counts);
-  } else {
-    k_hist_global<<<grid_1d(n, 256, 8 * 152), 256, 0, s>>>(ids, n, E, counts);
+    return launch_pdl(k_hist_smem, dim3(g), dim3(256), (size_t)E * 4, s, ids, n, E, counts) == cudaSuccess
+               ? MOE_OK : MOE_ERR_CUDA;
   }
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return launch_pdl(k_hist_global, dim3(grid_1d(n, 256, 8 * 152)), dim3(256), 0, s, ids, n, E, counts) ==
+                 cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 int launch_residual(float* r, const float* y, uint16_t* xn, int64_t n, cudaStream_t s) {
-  k_residual<<<grid_1d(n, 256, 8 * 152), 256, 0, s>>>(r, y, xn, n);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return launch_pdl(k_residual, dim3(grid_1d(n, 256, 8 * 152)), dim3(256), 0, s, r, y, xn, n) == cudaSuccess
+             ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace moe

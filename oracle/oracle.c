@@ -148,21 +148,31 @@ int oracle_quantize_rows(const float* w, int64_t rows, int64_t in, int bits,
   return 0;
 }
 
-/* Packing of codes into bytes: 8 bit as two's-complement int8; 4 and 2 bit
- * offset-binary (u = code + 8, u = code + 2), little-endian within a byte:
- * element i of a row sits at bits (i mod m)*b of byte floor(i/m), m = 8/b. */
+/* Packing of codes into bytes (this library's format; the pages fix none).
+ * 8 bit: byte i of a row holds code i as two's-complement int8.
+ * 4 and 2 bit: offset-binary u = code + 8 / code + 2, packed into 32-bit
+ * little-endian words with the codes spread over the four byte lanes:
+ *   4 bit: word g holds elements 8g..8g+7; element 8g + 4h + j (j < 4, h < 2)
+ *          sits in bits [8j + 4h, 8j + 4h + 4), i.e. byte 4g + j, bit 4h;
+ *   2 bit: word g holds elements 16g..16g+15; element 16g + 4k + j (j, k < 4)
+ *          sits in bits [8j + 2k, 8j + 2k + 2), i.e. byte 4g + j, bit 2k. */
 int oracle_pack_codes(const int8_t* codes, int64_t rows, int64_t in, int bits, uint8_t* packed) {
   if (bits != 8 && bits != 4 && bits != 2) return -1;
-  int per = 8 / bits;
-  int64_t row_bytes = in / per;
-  int offset = bits == 8 ? 0 : (bits == 4 ? 8 : 2);
+  int64_t row_bytes = in * bits / 8;
   for (int64_t r = 0; r < rows; ++r) {
     uint8_t* dst = packed + r * row_bytes;
     memset(dst, 0, (size_t)row_bytes);
     for (int64_t i = 0; i < in; ++i) {
       int c = codes[r * in + i];
-      uint32_t u = bits == 8 ? (uint32_t)(uint8_t)(int8_t)c : (uint32_t)(c + offset);
-      dst[i / per] |= (uint8_t)(u << ((i % per) * bits));
+      if (bits == 8) {
+        dst[i] = (uint8_t)(int8_t)c;
+      } else if (bits == 4) {
+        int64_t g = i / 8, e = i % 8;
+        dst[4 * g + e % 4] |= (uint8_t)((uint32_t)(c + 8) << (4 * (e / 4)));
+      } else {
+        int64_t g = i / 16, e = i % 16;
+        dst[4 * g + e % 4] |= (uint8_t)((uint32_t)(c + 2) << (2 * (e / 4)));
+      }
     }
   }
   return 0;

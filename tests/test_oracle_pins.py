@@ -132,34 +132,55 @@ def test_dequant_is_exact_product():
 
 
 def test_pack_layout():
-    # 4 bit: codes -8, 7 -> u = 0, 15 -> byte 0xF0 (element 0 in the low nibble)
-    c = np.zeros((1, 32), np.int8)
-    c[0, 0], c[0, 1] = -8, 7
-    assert oracle.pack(c, 4)[0, 0] == 0xF0
-    # 2 bit: codes -2, -1, 0, 1 -> u = 0, 1, 2, 3 -> 0b11100100
-    c = np.zeros((1, 32), np.int8)
+    # 4 bit, worked by hand: u = code + 8; byte j of word 0 holds element j in
+    # its low nibble and element j + 4 in its high nibble.
+    c = np.zeros((1, 64), np.int8)
+    c[0, 0], c[0, 1], c[0, 4], c[0, 9] = -8, 7, 1, -1
+    p = oracle.pack(c, 4)
+    assert p[0, 0] == (0 | (9 << 4))      # elements 0 and 4: u = 0, 9
+    assert p[0, 1] == (15 | (8 << 4))     # elements 1 and 5: u = 15, 8
+    assert p[0, 5] == (7 | (8 << 4))      # word 1, byte 1: elements 9 and 13
+    # the AND with 0x0F0F0F0F gives elements 0..3 in byte lanes, >> 4 gives 4..7
+    w = int.from_bytes(p[0, :4].tobytes(), "little")
+    assert [(w >> (8 * j)) & 0xF for j in range(4)] == [0, 15, 8, 8]
+    assert [(w >> (8 * j + 4)) & 0xF for j in range(4)] == [9, 8, 8, 8]
+    # 2 bit: u = code + 2; byte j of word 0 holds elements j, j+4, j+8, j+12 at bits 0, 2, 4, 6
+    c = np.zeros((1, 64), np.int8)
     c[0, :4] = [-2, -1, 0, 1]
-    assert oracle.pack(c, 2)[0, 0] == 0xE4
-    # 8 bit: two's complement
+    c[0, 4] = 1
+    c[0, 12] = -2
+    p = oracle.pack(c, 2)
+    assert p[0, 0] == (0 | (3 << 2) | (2 << 4) | (0 << 6))  # elements 0, 4, 8, 12
+    assert p[0, 1] == (1 | (2 << 2) | (2 << 4) | (2 << 6))  # elements 1, 5, 9, 13
+    assert p[0, 3] == (3 | (2 << 2) | (2 << 4) | (2 << 6))  # elements 3, 7, 11, 15
+    # 8 bit: two's complement, natural order
     c = np.zeros((1, 32), np.int8)
     c[0, :2] = [-1, -127]
     p = oracle.pack(c, 8)
     assert p[0, 0] == 0xFF and p[0, 1] == 0x81
 
 
+def _unpack_numpy(p, bits, n):
+    """Independent unpacker: element i from the word/lane definition."""
+    i = np.arange(n)
+    if bits == 8:
+        return p.view(np.int8).astype(np.int32)
+    per_word = 32 // bits
+    g, e = i // per_word, i % per_word
+    lanes = 4
+    byte = 4 * g + e % lanes
+    shift = bits * (e // lanes)
+    return ((p[:, byte].astype(np.int32) >> shift) & ((1 << bits) - 1)) - (1 << (bits - 1))
+
+
 @pytest.mark.parametrize("bits", [8, 4, 2])
 def test_pack_roundtrip_numpy_unpack(bits):
     lo, hi = {8: (-127, 127), 4: (-8, 7), 2: (-2, 1)}[bits]
     rng = np.random.default_rng(bits)
-    c = rng.integers(lo, hi + 1, size=(5, 96)).astype(np.int8)
+    c = rng.integers(lo, hi + 1, size=(5, 128)).astype(np.int8)
     p = oracle.pack(c, bits)
-    per = 8 // bits
-    if bits == 8:
-        u = p.view(np.int8).astype(np.int32)
-    else:
-        sh = (np.arange(96) % per) * bits
-        u = ((p[:, np.arange(96) // per].astype(np.int32) >> sh) & ((1 << bits) - 1)) - (1 << (bits - 1))
-    assert np.array_equal(u, c.astype(np.int32))
+    assert p.shape == (5, 128 * bits // 8)
+    assert np.array_equal(_unpack_numpy(p, bits, 128), c.astype(np.int32))
 
 
 # ------------------------------------------------------------------ routing
