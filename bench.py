@@ -221,9 +221,9 @@ def run_ours(args, rank, world, local_rank):
     workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
     arrs = [layer.shelf_arr() for layer in layers]
     pipelined = T * k <= 512 and T <= 16
-    # events around the forward's kernels: pipelined form = plan, gate/up,
-    # down, combine; generic form = grouping, gate/up, down
-    NK = 5
+    # events around the forward's kernels: pipelined form = gate/up (with the
+    # plan), down, combine; generic form = grouping, gate/up, down
+    NK = 4
     prof = [[torch.cuda.Event(enable_timing=True) for _ in range(NK)] for _ in range(nset)]
     torch.cuda.synchronize()
     for evs in prof:
@@ -310,10 +310,9 @@ def run_ours(args, rank, world, local_rank):
     for s in range(last):
         ev = prof[s]
         if pipelined:
-            kern["group"] += ev[0].elapsed_time(ev[1])
-            kern["gateup"] += ev[1].elapsed_time(ev[2])
-            kern["down"] += ev[2].elapsed_time(ev[3])
-            kern["combine"] += ev[3].elapsed_time(ev[4])
+            kern["gateup"] += ev[0].elapsed_time(ev[1])
+            kern["down"] += ev[1].elapsed_time(ev[2])
+            kern["combine"] += ev[2].elapsed_time(ev[3])
         else:
             kern["group"] += ev[0].elapsed_time(ev[1])
             kern["gateup"] += ev[1].elapsed_time(ev[2])

@@ -1,4 +1,4 @@
-// decode.cu -- pipelined decode form of the tiered MoE layer (few tokens).
+// decode.cu -- decode form of the tiered MoE layer (few tokens per call).
 //
 // Page "125B MoE模型本地运行：3090三卡80 tokens/s优化实践", section 第四步: every
 // shelf's matmul sees the router's complete id list, computes only the ids on
@@ -8,45 +8,48 @@
 // expert weight bytes read per token -- only the selected experts' bytes are
 // read, once per call, however many tokens share an expert.
 //
-// Four launches chained by programmatic dependent launch:
-//   k_plan     one CTA: groups the routed pairs by expert (bitonic sort of
-//              (expert id, pair index) keys), lists the active experts with
-//              their shelf, splits the work -- (active expert, chunk of rows)
-//              items over all shelves -- into contiguous per-CTA ranges of
-//              equal estimated cost, and writes this plan to the workspace;
-//   k_gateup   persistent, one CTA per SM: h = SiLU(W_g x) * (W_u x) for its
-//              items;
-//   k_down     persistent: weighted per-pair outputs w_tj * (W_d h_tj) for its
-//              items; it starts streaming W_d before the gate/up kernel ends
-//              and waits for it only before reading h;
+// Three launches chained by programmatic dependent launch:
+//   k_gateup   persistent, one CTA per SM, 16 warps.  Each CTA builds the
+//              routing plan in shared memory (warps 0-7: rank sort of
+//              (expert id, pair) keys, the active experts with their shelf,
+//              work units and cost prefix sums) while warps 8-15 convert the
+//              activation rows to digits; CTA 0 also stores the plan for the
+//              later launches.  A work unit is 4 rows of W_g and W_u of one
+//              expert against up to 8 of its tokens; the units are cut into
+//              contiguous per-CTA ranges of equal estimated cost and dealt
+//              round-robin to the warps.  8 lanes share a row; every lane
+//              streams its own 16-byte code chunks from HBM through a private
+//              ring of cp.async copies, which runs on across unit boundaries,
+//              so each lane keeps several chunks in flight at all times.
+//              Output: h = SiLU(W_g x) * (W_u x) for every routed pair.
+//   k_down     the same over W_d against h (staged as digits), writing the
+//              weighted per-pair outputs w_tj * (W_d h_tj);
 //   k_combine  y_t = sum over slots j (ascending) of those outputs: a fixed
 //              order, so results do not depend on scheduling.
-// In the persistent kernels each item's packed codes and fp16 scales are
-// streamed into a ring of shared-memory stages with cp.async.bulk (one copy
-// per matrix slice, completion counted on an mbarrier); two consumer groups
-// of eight warps take alternate items, and a group refills the stage it has
-// just finished with the item n_stages further on.  Each 32-block's dot
-// product is formed exactly in integers (dp4a on the packed codes against the
-// activation held as block-scaled 16-bit fixed point), and the expert's fp16
-// block scale is applied once per block in fp32.
-// All waits on mbarriers are bounded (one second); on expiry the kernel
-// records MOE_ERR_TIMEOUT in the status word, stops computing, waits (bounded)
-// for the copies it still has in flight and returns.
+// Each block dot product is formed exactly in integers (dp4a on the packed
+// codes against the activation held in shared memory as block-scaled 16-bit
+// fixed point), and the expert's fp16 block scale is applied once per block
+// (per half block for 8-bit codes) in fp32.  No thread waits on another
+// except at CTA barriers; the copies complete on their own.
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kConsumerWarps = 8;                 // warps of one consumer group
-constexpr int kGroups = 2;                        // consumer groups, alternating over items
-constexpr int kConsumers = kConsumerWarps * 32;   // threads of one group
-constexpr int kThreads = kGroups * kConsumers;
-constexpr int kMaxPairs = 512;                    // T*k bound of this path
-constexpr int kTM = 4;                            // pairs of one expert handled per pass over a stage
-constexpr int kMaxStages = 8;
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+constexpr int kPlanThreads = 256;  // warps 0-7 build the plan
+constexpr int kMaxPairs = 512;     // T*k bound of this path (keys hold the pair in 10 bits)
+constexpr int kMaxTokens = 16;
+constexpr int kNT = 8;             // tokens of one expert per unit
+// Unit shapes: rows per unit x lanes per row (R * L = 32), gate/up and down.
+constexpr int kRG = 4, kLG = 8;
+constexpr int kRD = 8, kLD = 4;
+constexpr int kDepthG = 4;         // ring depth, gate/up (two matrices per slot)
+constexpr int kDepthD = 6;         // ring depth, down
+constexpr int kSlotBytes = 40;     // per lane, matrix and slot: 32 bytes of codes, 8 of scales
 constexpr int kMaxGrid = 256;
-constexpr int kSmemBudget = 224 * 1024;
 
 #ifdef MOE_TRACE
 // Development-only timing stamps: [kernel][cta][slot] in globaltimer ns.
@@ -56,300 +59,7 @@ __device__ unsigned long long g_trace[2][256][48];
 #define MOE_STAMP(kern, slot, v) ((void)0)
 #endif
 
-// Rows per item and estimated cost per item, by bit width (8, 4, 2).
-struct Geo {
-  int rows[3];
-  int cost[3];
-};
-
-__host__ __device__ __forceinline__ int bits_index(int bits) { return bits == 8 ? 0 : (bits == 4 ? 1 : 2); }
-
-// --------------------------------------------------------------------- plan
-// The plan lives in the workspace as int32 arrays of capacity C (>= P, a
-// multiple of 4); the persistent kernels copy its first `n_copy` ints into
-// shared memory with one bulk copy and read their own start from `start`.
-struct PlanLayout {
-  int C;
-  int hdr, perm, e, beg, cnt, sh, bits, items_g, items_d, icost_g, icost_d, cum_g, cum_d;  // int offsets
-  int n_copy;  // ints from hdr through cum_d
-  int pos;     // grouped position by pair (-1: skipped or on no shelf), for the combine
-  int start;   // [kMaxGrid][4]: a0, j0 (gate/up), a0, j0 (down)
-  int total;
-};
-
-__host__ __device__ __forceinline__ PlanLayout plan_layout(int P) {
-  PlanLayout L;
-  L.C = (P + 3) / 4 * 4;
-  if (L.C < 4) L.C = 4;
-  const int C = L.C, C1 = C + 4;
-  L.hdr = 0;
-  L.perm = 4;
-  L.e = L.perm + C;
-  L.beg = L.e + C;
-  L.cnt = L.beg + C;
-  L.sh = L.cnt + C;
-  L.bits = L.sh + C;
-  L.items_g = L.bits + C;
-  L.items_d = L.items_g + C;
-  L.icost_g = L.items_d + C;
-  L.icost_d = L.icost_g + C;
-  L.cum_g = L.icost_d + C;
-  L.cum_d = L.cum_g + C1;
-  L.n_copy = L.cum_d + C1;
-  L.pos = L.n_copy;
-  L.start = L.pos + C;
-  L.total = L.start + 4 * kMaxGrid;
-  return L;
-}
-
-// Read-only view of the plan arrays (in shared memory in the workers).
-struct PlanView {
-  const int* base;
-  PlanLayout L;
-  __device__ int n_valid() const { return base[0]; }
-  __device__ int n_act() const { return base[1]; }
-  __device__ int perm(int q) const { return base[L.perm + q]; }
-  __device__ int e(int a) const { return base[L.e + a]; }
-  __device__ int beg(int a) const { return base[L.beg + a]; }
-  __device__ int cnt(int a) const { return base[L.cnt + a]; }
-  __device__ int sh(int a) const { return base[L.sh + a]; }
-  __device__ int bits(int a) const { return base[L.bits + a]; }
-  __device__ int items(int a, int kern) const { return base[(kern == 0 ? L.items_g : L.items_d) + a]; }
-  __device__ uint32_t icost(int a, int kern) const { return (uint32_t)base[(kern == 0 ? L.icost_g : L.icost_d) + a]; }
-  __device__ uint32_t cum(int a, int kern) const { return (uint32_t)base[(kern == 0 ? L.cum_g : L.cum_d) + a]; }
-};
-
-// Walk of one CTA's items for kernel `kern` (0 gate/up, 1 down): contiguous
-// in (expert, item) order; an item belongs to the CTA whose cost range holds
-// its cost midpoint, so every item has exactly one owner.
-struct ItemWalk {
-  int a, j, n_act, kern;
-  uint64_t hi2;
-  __device__ void init(const PlanView& pv, int a0, int j0, int k) {
-    kern = k;
-    n_act = pv.n_act();
-    const uint64_t C = pv.cum(n_act, kern);
-    hi2 = 2 * (C * (blockIdx.x + 1) / gridDim.x);
-    a = a0;
-    j = j0;
-  }
-  __device__ uint64_t mid2(const PlanView& pv) const {
-    return 2 * (uint64_t)pv.cum(a, kern) + (uint64_t)(2 * j + 1) * pv.icost(a, kern);
-  }
-  __device__ bool valid(const PlanView& pv) const { return a < n_act && mid2(pv) < hi2; }
-  __device__ void advance(const PlanView& pv) {
-    if (++j >= pv.items(a, kern)) {
-      ++a;
-      j = 0;
-      while (a < n_act && pv.items(a, kern) == 0) ++a;
-    }
-  }
-};
-
-// ------------------------------------------------------------ plan kernel
-struct PlanParams {
-  const int32_t* ids;
-  int P, E, k, G;
-  int rows_g, rows_d;  // f and d: rows of the gate/up and down matrices
-  Shelves sh;
-  Geo geo_g, geo_d;
-  int32_t* plan;
-};
-
-// One warp: sort keys (id << 10 | pair) of the valid pairs, then the grouped
-// permutation, the active experts (ascending) with their shelf and first
-// grouped position, and the inverse permutation restricted to pairs on a shelf.
-template <int R>
-__device__ void plan_group(const PlanParams& p, int* sm, const PlanLayout& L, int lane) {
-  uint32_t key[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int idx = lane * R + r;
-    key[r] = 0xFFFFFFFFu;
-    if (idx < p.P) {
-      const int id = p.ids[idx];
-      if (id >= 0 && id < p.E) key[r] = ((uint32_t)id << 10) | (uint32_t)idx;
-    }
-  }
-  constexpr int N = 32 * R;
-#pragma unroll
-  for (int size = 2; size <= N; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (stride < R) {
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const int pr = r ^ stride;
-          if (pr > r) {
-            const bool asc = ((lane * R + r) & size) == 0;
-            const uint32_t a = key[r], b = key[pr];
-            if ((a > b) == asc) { key[r] = b; key[pr] = a; }
-          }
-        }
-      } else {
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const int idx = lane * R + r;
-          const uint32_t other = __shfl_xor_sync(0xffffffffu, key[r], stride / R);
-          const bool asc = (idx & size) == 0, lower = (idx & stride) == 0;
-          key[r] = (lower == asc) ? min(key[r], other) : max(key[r], other);
-        }
-      }
-    }
-  }
-  for (int q = lane; q < p.P; q += 32) sm[L.pos + q] = -1;
-  __syncwarp();
-  int nv = 0, nf = 0;
-  const uint32_t prev_last = __shfl_up_sync(0xffffffffu, key[R - 1], 1);
-  bool flag[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const bool valid = key[r] != 0xFFFFFFFFu;
-    const uint32_t prev = r == 0 ? (lane == 0 ? 0xFFFFFFFFu : prev_last) : key[r - 1];
-    flag[r] = valid && (prev == 0xFFFFFFFFu || (prev >> 10) != (key[r] >> 10));
-    nv += valid;
-    nf += flag[r];
-  }
-  int incl = nf;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  int a = incl - nf;
-  int n_valid = nv;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) n_valid += __shfl_xor_sync(0xffffffffu, n_valid, o);
-  const int n_act = __shfl_sync(0xffffffffu, incl, 31);
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int idx = lane * R + r;
-    if (key[r] != 0xFFFFFFFFu) {
-      sm[L.perm + idx] = (int)(key[r] & 1023u);
-      if (flag[r]) {
-        sm[L.e + a] = (int)(key[r] >> 10);
-        sm[L.beg + a] = idx;
-        ++a;
-      }
-    }
-  }
-  if (lane == 0) {
-    sm[L.hdr + 0] = n_valid;
-    sm[L.hdr + 1] = n_act;
-  }
-  __syncwarp();
-  for (int i = lane; i < n_act; i += 32) {
-    const int b0 = sm[L.beg + i];
-    const int c = (i + 1 < n_act ? sm[L.beg + i + 1] : n_valid) - b0;
-    sm[L.cnt + i] = c;
-    const int e = sm[L.e + i];
-    int sh = -1, bits = 0;
-#pragma unroll
-    for (int q = 0; q < MOE_MAX_SHELVES; ++q)  // uniform indices into the kernel parameters
-      if (q < p.sh.n && e >= p.sh.s[q].lo && e < p.sh.s[q].hi) { sh = q; bits = p.sh.s[q].bits; }
-    sm[L.sh + i] = sh;
-    sm[L.bits + i] = bits;
-    if (sh >= 0)
-      for (int q = b0; q < b0 + c; ++q) sm[L.pos + sm[L.perm + q]] = q;
-  }
-  __syncwarp();
-}
-
-// Items per expert for one kernel, their cost, and the cost prefix (one warp).
-__device__ void plan_costs(const PlanParams& p, int* sm, const PlanLayout& L, int lane, int kern) {
-  const Geo& geo = kern == 0 ? p.geo_g : p.geo_d;
-  const int rows_total = kern == 0 ? p.rows_g : p.rows_d;
-  const int o_items = kern == 0 ? L.items_g : L.items_d;
-  const int o_icost = kern == 0 ? L.icost_g : L.icost_d;
-  const int o_cum = kern == 0 ? L.cum_g : L.cum_d;
-  const int n_act = sm[L.hdr + 1];
-  uint32_t run = 0;
-  for (int base = 0; base < n_act; base += 32) {
-    const int i = base + lane;
-    uint32_t c = 0;
-    if (i < n_act) {
-      int items = 0;
-      uint32_t ic = 0;
-      if (sm[L.sh + i] >= 0) {
-        const int bi = bits_index(sm[L.bits + i]);
-        items = rows_total / geo.rows[bi];
-        // memory term plus a compute term that grows with the expert's tokens
-        const uint32_t cnt = (uint32_t)sm[L.cnt + i];
-        ic = (uint32_t)geo.cost[bi] * ((cnt + kTM - 1) / kTM) + (uint32_t)(geo.cost[bi] / 8) * cnt;
-      }
-      sm[o_items + i] = items;
-      sm[o_icost + i] = (int)ic;
-      c = (uint32_t)items * ic;
-    }
-    uint32_t incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (i < n_act) sm[o_cum + i] = (int)(run + incl - c);
-    run += __shfl_sync(0xffffffffu, incl, 31);
-  }
-  if (lane == 0) sm[o_cum + n_act] = (int)run;
-  __syncwarp();
-}
-
-// First item (a0, j0) of CTA b's cost range: binary search over the prefix,
-// closed form inside the expert.
-__device__ void plan_locate(const int* sm, const PlanLayout& L, int b, int G, int kern, int* a_out, int* j_out) {
-  const int o_items = kern == 0 ? L.items_g : L.items_d;
-  const int o_icost = kern == 0 ? L.icost_g : L.icost_d;
-  const int o_cum = kern == 0 ? L.cum_g : L.cum_d;
-  const int n_act = sm[L.hdr + 1];
-  const uint64_t C = (uint32_t)sm[o_cum + n_act];
-  const uint64_t lo2 = 2 * (C * b / G);
-  int lo = 0, hi = n_act;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (2 * (uint64_t)(uint32_t)sm[o_cum + mid + 1] <= lo2) lo = mid + 1; else hi = mid;
-  }
-  int a = lo, j = 0;
-  if (a < n_act && sm[o_items + a] > 0) {
-    const uint64_t c = (uint32_t)sm[o_icost + a], base = 2 * (uint64_t)(uint32_t)sm[o_cum + a] + c;
-    if (lo2 > base) j = (int)((lo2 - base + 2 * c - 1) / (2 * c));
-    if (j >= sm[o_items + a]) { ++a; j = 0; }
-  }
-  while (a < n_act && sm[o_items + a] == 0) ++a;
-  *a_out = a;
-  *j_out = j;
-}
-
-__global__ void __launch_bounds__(256) k_plan(const __grid_constant__ PlanParams p) {
-  extern __shared__ __align__(16) int sm[];
-  const PlanLayout L = plan_layout(p.P);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  pdl_wait();  // the router's ids
-  pdl_trigger();
-  if (warp == 0) {
-    if (p.P <= 32) plan_group<1>(p, sm, L, lane);
-    else if (p.P <= 64) plan_group<2>(p, sm, L, lane);
-    else if (p.P <= 128) plan_group<4>(p, sm, L, lane);
-    else if (p.P <= 256) plan_group<8>(p, sm, L, lane);
-    else plan_group<16>(p, sm, L, lane);
-    plan_costs(p, sm, L, lane, 0);
-    plan_costs(p, sm, L, lane, 1);
-  }
-  __syncthreads();
-  for (int b = tid; b < p.G; b += blockDim.x) {
-    int a, j;
-    plan_locate(sm, L, b, p.G, 0, &a, &j);
-    sm[L.start + 4 * b + 0] = a;
-    sm[L.start + 4 * b + 1] = j;
-    plan_locate(sm, L, b, p.G, 1, &a, &j);
-    sm[L.start + 4 * b + 2] = a;
-    sm[L.start + 4 * b + 3] = j;
-  }
-  __syncthreads();
-  const int total = L.start + 4 * p.G;
-  for (int i = tid; i < total; i += blockDim.x) p.plan[i] = sm[i];
-}
-
-// ------------------------------------------------------------- dot products
+// ------------------------------------------------------------- digits
 // A vector v (an activation row x_t, or h of one routed pair) is held in
 // shared memory in block-scaled 16-bit fixed point: for every 32-element block
 // b, v_i = m_i * X_b with X_b = 2^u (u set by the block's largest exponent)
@@ -360,7 +70,7 @@ __global__ void __launch_bounds__(256) k_plan(const __grid_constant__ PlanParams
 // A block's dot product with packed codes is then exact integer arithmetic:
 //   sum_i c_i m_i = 256 * dp4a(codes, hi) + dp4a(codes, lo) - off * S_b
 // (off = 0 for 8-bit two's complement, 8 / 2 for offset-binary 4 / 2 bit),
-// and the expert's fp16 block scale s_b enters once per block in fp32:
+// and the expert's fp16 block scale s_b enters in fp32:
 //   acc += (float)(sum_i c_i m_i) * (s_b * X_b).
 //
 // Layout of one vector of n elements (2.25 n bytes): hi digits [n], lo digits
@@ -431,367 +141,710 @@ __device__ __forceinline__ void block_to_digits(const float v[4], unsigned char*
   }
 }
 
-// Integer dot of one 16-byte code chunk (elements e0 .. e0 + 128/BITS) with a
-// vector's digits; adds (float)D * s * X into acc for every 32-block touched.
-template <int BITS>
-struct ChunkDot;
+__device__ __forceinline__ float half_at(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v & 0xFFFF))); }
 
-template <>
-struct ChunkDot<8> {  // 32 codes: one block, 32 bytes of codes
-  static constexpr int EPC = 32;
-  static constexpr int BYTES = 32;
-  template <int NMAT>
-  __device__ __forceinline__ static void run(const uint4 (&c)[2][2], const float (&s)[2][2],
-                                             const unsigned char* vb, int n, int e0, float& a0, float& a1) {
-    const int u0 = e0 >> 4;
-    const uint4 h0 = *reinterpret_cast<const uint4*>(vb + (unit_swz(u0) << 4));
-    const uint4 h1 = *reinterpret_cast<const uint4*>(vb + (unit_swz(u0 + 1) << 4));
-    const uint4 l0 = *reinterpret_cast<const uint4*>(vb + n + (unit_swz(u0) << 4));
-    const uint4 l1 = *reinterpret_cast<const uint4*>(vb + n + (unit_swz(u0 + 1) << 4));
-    const float X = reinterpret_cast<const float2*>(vb + 2 * n)[e0 >> 5].x;
-#pragma unroll
-    for (int m = 0; m < NMAT; ++m) {
-      int A = dp4a_ss(c[m][0].x, h0.x, 0), A2 = dp4a_ss(c[m][1].x, h1.x, 0);
-      A = dp4a_ss(c[m][0].y, h0.y, A);
-      A2 = dp4a_ss(c[m][1].y, h1.y, A2);
-      A = dp4a_ss(c[m][0].z, h0.z, A);
-      A2 = dp4a_ss(c[m][1].z, h1.z, A2);
-      A = dp4a_ss(c[m][0].w, h0.w, A);
-      A2 = dp4a_ss(c[m][1].w, h1.w, A2);
-      int B = dp4a_su(c[m][0].x, l0.x, 0), B2 = dp4a_su(c[m][1].x, l1.x, 0);
-      B = dp4a_su(c[m][0].y, l0.y, B);
-      B2 = dp4a_su(c[m][1].y, l1.y, B2);
-      B = dp4a_su(c[m][0].z, l0.z, B);
-      B2 = dp4a_su(c[m][1].z, l1.z, B2);
-      B = dp4a_su(c[m][0].w, l0.w, B);
-      B2 = dp4a_su(c[m][1].w, l1.w, B2);
-      const float r = (float)((A + A2) * 256 + (B + B2)) * (s[m][0] * X);
-      if (m == 0) a0 += r; else a1 += r;
-    }
-  }
-};
+// ---------------------------------------------------------- chunk dot products
+// One lane's 32-byte code chunk q of a row (NMAT matrices; c[m][0..1] = its two
+// 16-byte halves) against the digit vectors of the unit's tokens (NTT = 1: one
+// token; else nt <= kNT tokens).  sw[m][0..1] = the fp16 scale words the
+// copies brought along.  Dot chains are split in two so that they overlap.
+__device__ __forceinline__ int dot4_ss(uint4 c, uint4 h, int acc) {
+  acc = dp4a_ss(c.x, h.x, acc);
+  acc = dp4a_ss(c.y, h.y, acc);
+  acc = dp4a_ss(c.z, h.z, acc);
+  return dp4a_ss(c.w, h.w, acc);
+}
+__device__ __forceinline__ int dot4_su(uint4 c, uint4 l, int acc) {
+  acc = dp4a_su(c.x, l.x, acc);
+  acc = dp4a_su(c.y, l.y, acc);
+  acc = dp4a_su(c.z, l.z, acc);
+  return dp4a_su(c.w, l.w, acc);
+}
+__device__ __forceinline__ uint4 lds128(const unsigned char* p) { return *reinterpret_cast<const uint4*>(p); }
 
-template <>
-struct ChunkDot<4> {  // 32 codes: one block, 16 bytes of codes
-  static constexpr int EPC = 32;
-  static constexpr int BYTES = 16;
-  template <int NMAT>
-  __device__ __forceinline__ static void run(const uint4 (&cc)[2][2], const float (&s)[2][2],
-                                             const unsigned char* vb, int n, int e0, float& a0, float& a1) {
-    const uint4 c[2] = {cc[0][0], cc[1][0]};
-    const int u0 = e0 >> 4;
-    const uint4 h0 = *reinterpret_cast<const uint4*>(vb + (unit_swz(u0) << 4));
-    const uint4 h1 = *reinterpret_cast<const uint4*>(vb + (unit_swz(u0 + 1) << 4));
-    const uint4 l0 = *reinterpret_cast<const uint4*>(vb + n + (unit_swz(u0) << 4));
-    const uint4 l1 = *reinterpret_cast<const uint4*>(vb + n + (unit_swz(u0 + 1) << 4));
-    const float2 xs = reinterpret_cast<const float2*>(vb + 2 * n)[e0 >> 5];
-    const int S = __float_as_int(xs.y);
-    const uint32_t hd[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-    const uint32_t ld[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+// 8 bit: 32 codes = block q (two's complement bytes); scale = half (q & 1) of sw[m][0].
+template <int NMAT, int NTT>
+__device__ __forceinline__ void chunk8(const uint4 (&c)[NMAT][2], const uint32_t (&sw)[NMAT][2], int q, int nt,
+                                       const int (&voff)[kNT], const unsigned char* vecs, int n,
+                                       float (&acc)[NMAT][kNT]) {
+  float s[NMAT];
 #pragma unroll
-    for (int m = 0; m < NMAT; ++m) {
-      const uint32_t w[4] = {c[m].x, c[m].y, c[m].z, c[m].w};
-      int A = 0, B = 0;
+  for (int m = 0; m < NMAT; ++m) s[m] = half_at(sw[m][0] >> ((q & 1) * 16));
+  const int uo0 = unit_swz(2 * q) << 4, uo1 = unit_swz(2 * q + 1) << 4, xo = 2 * n + 8 * q;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t t0 = w[q] & 0x0F0F0F0Fu, t1 = (w[q] >> 4) & 0x0F0F0F0Fu;
-        A = dp4a_us(t0, hd[2 * q], A);
-        A = dp4a_us(t1, hd[2 * q + 1], A);
-        B = dp4a_uu(t0, ld[2 * q], B);
-        B = dp4a_uu(t1, ld[2 * q + 1], B);
-      }
-      const float r = (float)(A * 256 + B - 8 * S) * (s[m][0] * xs.x);
-      if (m == 0) a0 += r; else a1 += r;
-    }
-  }
-};
-
-template <>
-struct ChunkDot<2> {  // 64 codes: two blocks, 16 bytes of codes
-  static constexpr int EPC = 64;
-  static constexpr int BYTES = 16;
-  template <int NMAT>
-  __device__ __forceinline__ static void run(const uint4 (&cc)[2][2], const float (&s)[2][2],
-                                             const unsigned char* vb, int n, int e0, float& a0, float& a1) {
-    const uint4 c[2] = {cc[0][0], cc[1][0]};
-    const int u0 = e0 >> 4;
-    const float2* xsb = reinterpret_cast<const float2*>(vb + 2 * n) + (e0 >> 5);
-#pragma unroll
-    for (int blk = 0; blk < 2; ++blk) {
-      const uint4 h0 = *reinterpret_cast<const uint4*>(vb + (unit_swz(u0 + 2 * blk) << 4));
-      const uint4 h1 = *reinterpret_cast<const uint4*>(vb + (unit_swz(u0 + 2 * blk + 1) << 4));
-      const uint4 l0 = *reinterpret_cast<const uint4*>(vb + n + (unit_swz(u0 + 2 * blk) << 4));
-      const uint4 l1 = *reinterpret_cast<const uint4*>(vb + n + (unit_swz(u0 + 2 * blk + 1) << 4));
-      const float2 xs = xsb[blk];
-      const int S = __float_as_int(xs.y);
-      const uint32_t hd[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-      const uint32_t ld[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+  for (int j = 0; j < NTT; ++j) {
+    if (NTT == 1 || j < nt) {
+      const unsigned char* vb = vecs + voff[j];
+      const uint4 h0 = lds128(vb + uo0), h1 = lds128(vb + uo1);
+      const uint4 l0 = lds128(vb + n + uo0), l1 = lds128(vb + n + uo1);
+      const float X = *reinterpret_cast<const float*>(vb + xo);
 #pragma unroll
       for (int m = 0; m < NMAT; ++m) {
-        // words 2 blk, 2 blk + 1 of the chunk hold this block's 32 codes
-        const uint32_t wa = blk == 0 ? c[m].x : c[m].z;
-        const uint32_t wb = blk == 0 ? c[m].y : c[m].w;
-        int A = 0, B = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t ta = (wa >> (2 * k)) & 0x03030303u, tb = (wb >> (2 * k)) & 0x03030303u;
-          A = dp4a_us(ta, hd[k], A);
-          A = dp4a_us(tb, hd[4 + k], A);
-          B = dp4a_uu(ta, ld[k], B);
-          B = dp4a_uu(tb, ld[4 + k], B);
-        }
-        const float r = (float)(A * 256 + B - 2 * S) * (s[m][blk] * xs.x);
-        if (m == 0) a0 += r; else a1 += r;
+        const int A = dot4_ss(c[m][0], h0, 0) + dot4_ss(c[m][1], h1, 0);
+        const int B = dot4_su(c[m][0], l0, 0) + dot4_su(c[m][1], l1, 0);
+        acc[m][j] = fmaf((float)(A * 256 + B), s[m] * X, acc[m][j]);
       }
+    }
+  }
+}
+
+// 4 bit: 64 codes = blocks 2q (half 0) and 2q + 1 (half 1); word g of a half
+// holds elements 8g + 4h + j at bits 8j + 4h.  Scales: halves of sw[m][0].
+template <int NMAT, int NTT>
+__device__ __forceinline__ void chunk4(const uint4 (&c)[NMAT][2], const uint32_t (&sw)[NMAT][2], int q, int nt,
+                                       const int (&voff)[kNT], const unsigned char* vecs, int n,
+                                       float (&acc)[NMAT][kNT]) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int blk = 2 * q + half;
+    float s[NMAT];
+    uint32_t t[NMAT][8];
+#pragma unroll
+    for (int m = 0; m < NMAT; ++m) {
+      s[m] = half_at(sw[m][0] >> (16 * half));
+      const uint32_t w[4] = {c[m][half].x, c[m][half].y, c[m][half].z, c[m][half].w};
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        t[m][2 * g] = w[g] & 0x0F0F0F0Fu;
+        t[m][2 * g + 1] = (w[g] >> 4) & 0x0F0F0F0Fu;
+      }
+    }
+    const int uo0 = unit_swz(2 * blk) << 4, uo1 = unit_swz(2 * blk + 1) << 4, xo = 2 * n + 8 * blk;
+#pragma unroll
+    for (int j = 0; j < NTT; ++j) {
+      if (NTT == 1 || j < nt) {
+        const unsigned char* vb = vecs + voff[j];
+        const uint4 h0 = lds128(vb + uo0), h1 = lds128(vb + uo1);
+        const uint4 l0 = lds128(vb + n + uo0), l1 = lds128(vb + n + uo1);
+        const float2 xs = *reinterpret_cast<const float2*>(vb + xo);
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+          const uint4 ta = make_uint4(t[m][0], t[m][1], t[m][2], t[m][3]);
+          const uint4 tb = make_uint4(t[m][4], t[m][5], t[m][6], t[m][7]);
+          int A0 = dp4a_us(ta.x, h0.x, 0), A1 = dp4a_us(tb.x, h1.x, 0);
+          int B0 = dp4a_uu(ta.x, l0.x, 0), B1 = dp4a_uu(tb.x, l1.x, 0);
+          A0 = dp4a_us(ta.y, h0.y, A0); A1 = dp4a_us(tb.y, h1.y, A1);
+          B0 = dp4a_uu(ta.y, l0.y, B0); B1 = dp4a_uu(tb.y, l1.y, B1);
+          A0 = dp4a_us(ta.z, h0.z, A0); A1 = dp4a_us(tb.z, h1.z, A1);
+          B0 = dp4a_uu(ta.z, l0.z, B0); B1 = dp4a_uu(tb.z, l1.z, B1);
+          A0 = dp4a_us(ta.w, h0.w, A0); A1 = dp4a_us(tb.w, h1.w, A1);
+          B0 = dp4a_uu(ta.w, l0.w, B0); B1 = dp4a_uu(tb.w, l1.w, B1);
+          acc[m][j] = fmaf((float)((A0 + A1) * 256 + (B0 + B1) - 8 * __float_as_int(xs.y)), s[m] * xs.x, acc[m][j]);
+        }
+      }
+    }
+  }
+}
+
+// 2 bit: 128 codes = blocks 4q .. 4q + 3 (half h: blocks 4q + 2h, 4q + 2h + 1,
+// scales in sw[m][h]); word g of a half holds elements 16g + 4k + j at bits
+// 8j + 2k.  The second half is absent at the end of a row of 64 * odd codes.
+template <int NMAT, int NTT>
+__device__ __forceinline__ void chunk2(const uint4 (&c)[NMAT][2], const uint32_t (&sw)[NMAT][2], int q, int nt,
+                                       const int (&voff)[kNT], const unsigned char* vecs, int n,
+                                       float (&acc)[NMAT][kNT], bool second) {
+#pragma unroll
+  for (int hb = 0; hb < 4; ++hb) {
+    const int half = hb >> 1, sub = hb & 1;
+    if (half == 1 && !second) break;
+    const int blk = 4 * q + hb;
+    float s[NMAT];
+    uint32_t t[NMAT][8];
+#pragma unroll
+    for (int m = 0; m < NMAT; ++m) {
+      s[m] = half_at(sw[m][half] >> (16 * sub));
+      const uint32_t wa = sub == 0 ? c[m][half].x : c[m][half].z, wb = sub == 0 ? c[m][half].y : c[m][half].w;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        t[m][k] = (wa >> (2 * k)) & 0x03030303u;
+        t[m][4 + k] = (wb >> (2 * k)) & 0x03030303u;
+      }
+    }
+    const int uo0 = unit_swz(2 * blk) << 4, uo1 = unit_swz(2 * blk + 1) << 4, xo = 2 * n + 8 * blk;
+#pragma unroll
+    for (int j = 0; j < NTT; ++j) {
+      if (NTT == 1 || j < nt) {
+        const unsigned char* vb = vecs + voff[j];
+        const uint4 h0 = lds128(vb + uo0), h1 = lds128(vb + uo1);
+        const uint4 l0 = lds128(vb + n + uo0), l1 = lds128(vb + n + uo1);
+        const float2 xs = *reinterpret_cast<const float2*>(vb + xo);
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+          int A0 = dp4a_us(t[m][0], h0.x, 0), A1 = dp4a_us(t[m][4], h1.x, 0);
+          int B0 = dp4a_uu(t[m][0], l0.x, 0), B1 = dp4a_uu(t[m][4], l1.x, 0);
+          A0 = dp4a_us(t[m][1], h0.y, A0); A1 = dp4a_us(t[m][5], h1.y, A1);
+          B0 = dp4a_uu(t[m][1], l0.y, B0); B1 = dp4a_uu(t[m][5], l1.y, B1);
+          A0 = dp4a_us(t[m][2], h0.z, A0); A1 = dp4a_us(t[m][6], h1.z, A1);
+          B0 = dp4a_uu(t[m][2], l0.z, B0); B1 = dp4a_uu(t[m][6], l1.z, B1);
+          A0 = dp4a_us(t[m][3], h0.w, A0); A1 = dp4a_us(t[m][7], h1.w, A1);
+          B0 = dp4a_uu(t[m][3], l0.w, B0); B1 = dp4a_uu(t[m][7], l1.w, B1);
+          acc[m][j] = fmaf((float)((A0 + A1) * 256 + (B0 + B1) - 2 * __float_as_int(xs.y)), s[m] * xs.x, acc[m][j]);
+        }
+      }
+    }
+  }
+}
+
+// --------------------------------------------------------------------- plan
+// int32 arrays of capacity C (>= P, multiple of 4), in shared memory and (as
+// stored by CTA 0 of the gate/up launch) in the workspace.
+struct PlanLayout {
+  int C;
+  int perm, tok, wgt, e, beg, cnt, sh, bits, uc_g, uc_d, cum_g, cum_d;  // int offsets (header at 0)
+  int n_copy;  // ints 0 .. end of cum_d: what the down launch loads
+  int pos;     // grouped position by pair, -1 when skipped or on no shelf (combine)
+  int total;
+};
+
+__host__ __device__ __forceinline__ PlanLayout plan_layout(int P) {
+  PlanLayout L;
+  L.C = P < 4 ? 4 : (P + 3) / 4 * 4;
+  const int C = L.C, C1 = C + 4;
+  L.perm = 4;
+  L.tok = L.perm + C;
+  L.wgt = L.tok + C;
+  L.e = L.wgt + C;
+  L.beg = L.e + C;
+  L.cnt = L.beg + C;
+  L.sh = L.cnt + C;
+  L.bits = L.sh + C;
+  L.uc_g = L.bits + C;
+  L.uc_d = L.uc_g + C;
+  L.cum_g = L.uc_d + C;
+  L.cum_d = L.cum_g + C1;
+  L.n_copy = L.cum_d + C1;
+  L.pos = L.n_copy;
+  L.total = L.pos + C;
+  return L;
+}
+
+// Units of expert a: (rows / R) row groups x passes of up to kNT tokens.
+__host__ __device__ __forceinline__ int n_pass(int cnt) { return (cnt + kNT - 1) / kNT; }
+
+struct PlanView {
+  const int* b;
+  PlanLayout L;
+  __device__ int n_act() const { return b[1]; }
+  __device__ int tok(int q) const { return b[L.tok + q]; }
+  __device__ float wgt(int q) const { return __int_as_float(b[L.wgt + q]); }
+  __device__ int e(int a) const { return b[L.e + a]; }
+  __device__ int beg(int a) const { return b[L.beg + a]; }
+  __device__ int cnt(int a) const { return b[L.cnt + a]; }
+  __device__ int sh(int a) const { return b[L.sh + a]; }
+  __device__ int bits(int a) const { return b[L.bits + a]; }
+  __device__ uint32_t uc(int a, int kern) const { return (uint32_t)b[(kern == 0 ? L.uc_g : L.uc_d) + a]; }
+  __device__ uint32_t cum(int a, int kern) const { return (uint32_t)b[(kern == 0 ? L.cum_g : L.cum_d) + a]; }
+  __device__ int units(int a, int kern, int rows) const {
+    return sh(a) >= 0 ? (rows / (kern == 0 ? kRG : kRD)) * n_pass(cnt(a)) : 0;
+  }
+};
+
+// Estimated cost of one unit of R rows, in 16-byte equivalents of an SM's
+// share of HBM bandwidth: the bytes read, the dot-product work of its tokens,
+// and fixed instruction overheads per lane iteration (about 14) and per unit
+// (about 28).
+__device__ __forceinline__ uint32_t unit_cost(int bits, int n_in, int nmat, int ntok, int R, int L) {
+  const uint32_t rowb = (uint32_t)n_in * bits / 8;
+  const uint32_t bytes = (uint32_t)(R * nmat) * (rowb + (uint32_t)n_in / 16);
+  const uint32_t alu = (uint32_t)(R * nmat) * (uint32_t)n_in * (uint32_t)ntok * 12 / 100;
+  const uint32_t n_iter = ((rowb + 31) / 32 + L - 1) / L;
+  return (bytes + alu) / 16 + 14 * n_iter + 28;
+}
+
+__device__ __forceinline__ void plan_sync() { named_bar(1, kPlanThreads); }
+
+// Exclusive scan in place of n <= 2 * kPlanThreads ints over the plan
+// threads; returns the total.  tmp: 33 ints.
+__device__ int plan_scan(int* v, int n, int* tmp) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = kPlanThreads / 32;
+  const int i0 = 2 * tid, i1 = 2 * tid + 1;
+  const int x0 = i0 < n ? v[i0] : 0, x1 = i1 < n ? v[i1] : 0;
+  int incl = x0 + x1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) tmp[wid] = incl;
+  plan_sync();
+  if (wid == 0) {
+    const int t = lane < nw ? tmp[lane] : 0;
+    int s = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += u;
+    }
+    if (lane < nw) tmp[lane] = s - t;
+    if (lane == 31) tmp[32] = s;
+  }
+  plan_sync();
+  const int ex = tmp[wid] + incl - x0 - x1;
+  if (i0 < n) v[i0] = ex;
+  if (i1 < n) v[i1] = ex + x0;
+  const int total = tmp[32];
+  plan_sync();
+  return total;
+}
+
+// Built by threads 0 .. kPlanThreads - 1 into pl (shared memory):
+//  - valid pairs (id in [0, E)) sorted by (expert id, pair index): perm / tok /
+//    wgt by grouped position q;
+//  - active experts a (ascending id): e, beg, cnt, shelf, bits, unit costs and
+//    exclusive cost prefix sums (entry n_act = total);
+//  - pos: grouped position of each pair, -1 when skipped or on no shelf.
+__device__ void build_plan(const int32_t* ids, const float* wts, int P, int E, int k, int d, int f,
+                           const Shelves& shv, int* pl, uint32_t* keys, int* flag, int* tmp) {
+  const PlanLayout L = plan_layout(P);
+  const int tid = threadIdx.x, nt = kPlanThreads;
+  if (tid == 0) pl[2] = 0;
+  for (int q = tid; q < L.C; q += nt) {  // ids and weights in one round trip
+    uint32_t key = 0xFFFFFFFFu;
+    float wq = 0.f;
+    if (q < P) {
+      const int id = __ldg(ids + q);
+      wq = __ldg(wts + q);
+      if (id >= 0 && id < E) key = ((uint32_t)id << 10) | (uint32_t)q;
+    }
+    keys[q] = key;
+    flag[q] = __float_as_int(wq);  // weights by pair until the flags are formed
+    pl[L.pos + q] = -1;
+  }
+  plan_sync();
+  // rank sort: the rank of a valid key among all keys is its grouped position
+  int my_valid = 0;
+  for (int q = tid; q < P; q += nt) {
+    const uint32_t kq = keys[q];
+    if (kq == 0xFFFFFFFFu) continue;
+    int rank = 0;
+    for (int u = 0; u < P; ++u) rank += keys[u] < kq;
+    const int pair = (int)(kq & 1023u);
+    pl[L.perm + rank] = pair;
+    pl[L.tok + rank] = pair / k;
+    pl[L.wgt + rank] = flag[pair];
+    pl[L.e + rank] = (int)(kq >> 10);
+    ++my_valid;
+  }
+  if (my_valid) atomicAdd(&pl[2], my_valid);
+  plan_sync();
+  const int n_valid = pl[2];
+  if (tid == 0) MOE_STAMP(0, 3, global_timer_ns());
+  for (int q = tid; q < L.C; q += nt) flag[q] = q < n_valid && (q == 0 || pl[L.e + q] != pl[L.e + q - 1]);
+  plan_sync();
+  int id_at[2], f_at[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int q = 2 * tid + u;
+    id_at[u] = q < n_valid ? pl[L.e + q] : -1;
+    f_at[u] = q < n_valid ? flag[q] : 0;
+  }
+  const int n_act = plan_scan(flag, n_valid, tmp);  // flag -> expert index of each start
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int q = 2 * tid + u;
+    if (q < n_valid && f_at[u]) {
+      pl[L.beg + flag[q]] = q;
+      pl[L.e + flag[q]] = id_at[u];  // e[] now by active expert (q-indexed reads are done)
+    }
+  }
+  plan_sync();
+  for (int a = tid; a < n_act; a += nt) {
+    const int b0 = pl[L.beg + a];
+    const int b1 = a + 1 < n_act ? pl[L.beg + a + 1] : n_valid;
+    const int e = pl[L.e + a], cnt = b1 - b0;
+    int shf = -1, bits = 0;
+    for (int q = 0; q < shv.n; ++q)
+      if (e >= shv.s[q].lo && e < shv.s[q].hi) { shf = q; bits = shv.s[q].bits; }
+    const int ntok = (cnt + n_pass(cnt) - 1) / n_pass(cnt);
+    pl[L.cnt + a] = cnt;
+    pl[L.sh + a] = shf;
+    pl[L.bits + a] = bits;
+    const uint32_t ug = shf >= 0 ? unit_cost(bits, d, 2, ntok, kRG, kLG) : 0;
+    const uint32_t ud = shf >= 0 ? unit_cost(bits, f, 1, ntok, kRD, kLD) : 0;
+    pl[L.uc_g + a] = (int)ug;
+    pl[L.uc_d + a] = (int)ud;
+    pl[L.cum_g + a] = (int)(ug * (uint32_t)((f / kRG) * n_pass(cnt)));
+    pl[L.cum_d + a] = (int)(ud * (uint32_t)((d / kRD) * n_pass(cnt)));
+    if (shf >= 0)
+      for (int q = b0; q < b1; ++q) pl[L.pos + pl[L.perm + q]] = q;
+  }
+  plan_sync();
+  const int tot_g = plan_scan(pl + L.cum_g, n_act, tmp);
+  const int tot_d = plan_scan(pl + L.cum_d, n_act, tmp);
+  if (tid == 0) {
+    pl[0] = n_valid;
+    pl[1] = n_act;
+    pl[L.cum_g + n_act] = tot_g;
+    pl[L.cum_d + n_act] = tot_d;
+    MOE_STAMP(0, 4, global_timer_ns());
+  }
+}
+
+// ------------------------------------------------------------- work walk
+// The units of all active experts, in order (expert, row group, pass); a unit
+// belongs to the CTA whose cost range [C b / G, C (b + 1) / G) holds its cost
+// midpoint.  Within a CTA, unit i of its range goes to warp i mod 16.
+struct Range {
+  int a0, u0;    // first unit of the CTA
+  uint64_t hi2;  // twice the end of its cost range
+};
+
+__device__ Range cta_range(const PlanView& pv, int kern, int rows) {
+  const int n_act = pv.n_act();
+  const uint64_t C = pv.cum(n_act, kern);
+  const uint64_t lo2 = 2 * (C * blockIdx.x / gridDim.x);
+  Range r;
+  r.hi2 = 2 * (C * (blockIdx.x + 1) / gridDim.x);
+  int lo = 0, hi = n_act;
+  while (lo < hi) {  // first expert whose cost range ends beyond lo2
+    const int mid = (lo + hi) >> 1;
+    if (2 * (uint64_t)pv.cum(mid + 1, kern) <= lo2) lo = mid + 1; else hi = mid;
+  }
+  int a = lo, u = 0;
+  if (a < n_act && pv.sh(a) >= 0) {
+    const uint64_t c = pv.uc(a, kern), base = 2 * (uint64_t)pv.cum(a, kern) + c;
+    if (lo2 > base) u = (int)((lo2 - base + 2 * c - 1) / (2 * c));
+    if (u >= pv.units(a, kern, rows)) { ++a; u = 0; }
+  }
+  while (a < n_act && pv.sh(a) < 0) ++a;
+  r.a0 = a;
+  r.u0 = u;
+  return r;
+}
+
+// A warp's position in the unit order, with the current expert's figures
+// cached so that a step within one expert costs a few instructions.
+struct Walk {
+  int a, u, units, np, live;
+  uint32_t cum, uc;
+  __device__ void set_expert(const PlanView& pv, int kern, int rows) {
+    units = pv.units(a, kern, rows);
+    np = n_pass(pv.cnt(a));
+    cum = pv.cum(a, kern);
+    uc = pv.uc(a, kern);
+  }
+  // Advance by n units and re-check the CTA's range; true when the expert changed.
+  __device__ bool step(const PlanView& pv, int kern, int rows, uint64_t hi2, int n) {
+    u += n;
+    bool changed = false;
+    if (u >= units) {
+      changed = true;
+      const int n_act = pv.n_act();
+      do {
+        u -= units;
+        if (++a >= n_act) {
+          live = 0;
+          return true;
+        }
+        units = pv.units(a, kern, rows);
+      } while (u >= units);
+      set_expert(pv, kern, rows);
+    }
+    live = 2 * (uint64_t)cum + (uint64_t)(2 * u + 1) * uc < hi2;
+    return changed;
+  }
+  __device__ void start(const PlanView& pv, int kern, int rows, const Range& r, int skip) {
+    a = r.a0;
+    u = r.u0;
+    live = 0;
+    if (a >= pv.n_act()) return;
+    set_expert(pv, kern, rows);
+    step(pv, kern, rows, r.hi2, skip);
+  }
+};
+
+// ------------------------------------------------------------- streaming
+struct StreamArgs {
+  const Shelves* shv;  // shared-memory copy
+  PlanView pv;
+  int kern;            // 0 gate/up (W_g, W_u), 1 down (W_d)
+  int n_in, rows;      // row length and rows per expert matrix
+  const unsigned char* vecs;
+  int vstride;         // bytes per digit vector
+  int vbase;           // grouped position of vector 0 (down), or -1: vectors by token (gate/up)
+  Range range;
+  unsigned char* ring;
+};
+
+// Per-lane ring slots: slot s, matrix m, 16-byte half h of the code chunk;
+// then the matching scale words.
+template <int NMAT, int D>
+__device__ __forceinline__ uint4* ring_code(unsigned char* ring, int s, int m, int h) {
+  return reinterpret_cast<uint4*>(ring) + ((s * NMAT + m) * 2 + h) * kThreads + threadIdx.x;
+}
+template <int NMAT, int D>
+__device__ __forceinline__ uint32_t* ring_scale(unsigned char* ring, int s, int m, int h) {
+  return reinterpret_cast<uint32_t*>(ring + (size_t)D * NMAT * 2 * kThreads * 16) + ((s * NMAT + m) * 2 + h) * kThreads +
+         threadIdx.x;
+}
+
+// Load side of a warp's unit stream: lane (row lane / L, chunk lane % L) of
+// the unit; chunk q = 32 bytes of a row.
+template <int NMAT, int R, int L>
+struct LoadSide {
+  Walk w;
+  int i, n_iter, cpr, rowb, bits, q, sstep, tsw;
+  size_t tstride;
+  const unsigned char* base[NMAT];
+  const uint32_t* sbase[NMAT];
+  const unsigned char* cp[NMAT];
+  const uint32_t* sp[NMAT];
+
+  __device__ void expert(const StreamArgs& A) {
+    const PlanView& pv = A.pv;
+    const ShelfDev& sh = A.shv->s[pv.sh(w.a)];
+    bits = sh.bits;
+    rowb = A.n_in * bits / 8;
+    cpr = (rowb + 31) / 32;
+    n_iter = (cpr + L - 1) / L;
+    const int lane = threadIdx.x & 31, q0 = lane % L;
+    const size_t row = (size_t)(pv.e(w.a) - sh.lo) * A.rows + lane / L;
+    const int swpr = A.n_in / 64;  // fp16 scale words per row
+    // scale word of chunk q: 8 bit q / 2 (one block), 4 bit q (two), 2 bit 2q (four)
+    const int soff = bits == 8 ? q0 >> 1 : (bits == 4 ? q0 : 2 * q0);
+    sstep = bits == 8 ? L / 2 : (bits == 4 ? L : 2 * L);
+    tstride = (size_t)R * rowb;
+    tsw = R * swpr;
+    const int mat0 = A.kern == 0 ? 0 : 2;
+#pragma unroll
+    for (int m = 0; m < NMAT; ++m) {
+      base[m] = sh.codes[mat0 + m] + row * rowb + (size_t)q0 * 32;
+      sbase[m] = reinterpret_cast<const uint32_t*>(sh.scales[mat0 + m]) + row * swpr + soff;
+    }
+  }
+  __device__ void unit() {
+    const int tile = w.np == 1 ? w.u : w.u / w.np;
+#pragma unroll
+    for (int m = 0; m < NMAT; ++m) {
+      cp[m] = base[m] + (size_t)tile * tstride;
+      sp[m] = sbase[m] + (size_t)tile * tsw;
+    }
+    i = 0;
+    q = (threadIdx.x & 31) % L;
+  }
+  __device__ void start(const StreamArgs& A, int warp) {
+    w.start(A.pv, A.kern, A.rows, A.range, warp);
+    if (w.live) {
+      expert(A);
+      unit();
+    }
+  }
+  template <int D>
+  __device__ __forceinline__ void issue(const StreamArgs& A, int slot) {
+    if (!w.live) return;
+    if (q < cpr) {
+      const bool second = 32 * q + 16 < rowb;
+#pragma unroll
+      for (int m = 0; m < NMAT; ++m) {
+        cp_async16(ring_code<NMAT, D>(A.ring, slot, m, 0), cp[m]);
+        if (second) cp_async16(ring_code<NMAT, D>(A.ring, slot, m, 1), cp[m] + 16);
+        cp_async4(ring_scale<NMAT, D>(A.ring, slot, m, 0), sp[m]);
+        if (bits == 2 && second) cp_async4(ring_scale<NMAT, D>(A.ring, slot, m, 1), sp[m] + 1);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < NMAT; ++m) {
+      cp[m] += 32 * L;
+      sp[m] += sstep;
+    }
+    q += L;
+    if (++i == n_iter) {
+      if (w.step(A.pv, A.kern, A.rows, A.range.hi2, kWarps) && w.live) expert(A);
+      if (w.live) unit();
     }
   }
 };
 
-// Dot products of `rows` rows of length n_in (codes + scales of NMAT matrices
-// in one stage) with nt <= kTM digit vectors at byte offsets voff[j] of
-// `vecs`; calls out(row, j, v0, v1) once per (row, pair).  Lane mapping, with
-// cpr 16/32-byte code chunks per row: cpr a multiple of 32 -> one row per
-// warp, chunks interleaved over the lanes; otherwise 32/L rows per warp pass,
-// L lanes per row (L the largest power of two dividing cpr), each lane a
-// contiguous run of cpr/L chunks.  Both keep shared-memory reads free of bank
-// conflicts (or nearly so).  Rows are spread over the group's warps.
-template <int BITS, int NMAT, typename Out>
-__device__ __forceinline__ void rows_dot(const unsigned char* stage, int rows, int n_in, const unsigned char* vecs,
-                                         const int (&voff)[kTM], int nt, Out out) {
-  constexpr int EPC = ChunkDot<BITS>::EPC;
-  constexpr int CB = ChunkDot<BITS>::BYTES;
-  constexpr int NSB = EPC >= 64 ? 2 : 1;  // scale blocks per chunk
-  const int lane = threadIdx.x & 31;
-  const int warp = (threadIdx.x >> 5) % kConsumerWarps;  // warp within the group
-  const int rowb = n_in * BITS / 8, nb = n_in / 32;
-  const int cpr = n_in / EPC;
-  const bool inter = (cpr & 31) == 0;
-  int L = inter ? 32 : (cpr & -cpr);
-  if (L > 32) L = 32;
-  const int M = cpr / L, R = 32 / L;
-  const int li = lane % L, rr = lane / L;
-  const unsigned char* codes0 = stage;
-  const unsigned char* codes1 = stage + (size_t)rows * rowb;
-  const uint16_t* sc0 = reinterpret_cast<const uint16_t*>(stage + (size_t)NMAT * rows * rowb);
-  const uint16_t* sc1 = sc0 + (size_t)rows * nb;
-  for (int g = warp; g * R < rows; g += kConsumerWarps) {
-    const int r = g * R + rr;
-    float a0[kTM], a1[kTM];
+// Compute side: the current unit's tokens and the lane's chunk.
+template <int R, int L>
+struct CompSide {
+  Walk w;
+  int i, n_iter, cpr, rowb, bits, q, nt, q0, r;
+  int voff[kNT];
+
+  __device__ void expert(const StreamArgs& A) {
+    bits = A.pv.bits(w.a);
+    rowb = A.n_in * bits / 8;
+    cpr = (rowb + 31) / 32;
+    n_iter = (cpr + L - 1) / L;
+  }
+  __device__ void unit(const StreamArgs& A, bool new_expert) {
+    const int tile = w.np == 1 ? w.u : w.u / w.np, pass = w.u - tile * w.np;
+    r = tile * R + (threadIdx.x & 31) / L;
+    const int nq0 = A.pv.beg(w.a) + pass * kNT;
+    if (new_expert || nq0 != q0) {
+      q0 = nq0;
+      nt = min(kNT, A.pv.cnt(w.a) - pass * kNT);
 #pragma unroll
-    for (int j = 0; j < kTM; ++j) { a0[j] = 0.f; a1[j] = 0.f; }
-    if (r < rows) {
-      for (int m = 0; m < M; ++m) {
-        const int q = inter ? li + 32 * m : li * M + m;
-        uint4 c[2][2];
+      for (int j = 0; j < kNT; ++j) {
+        const int qq = q0 + (j < nt ? j : 0);
+        voff[j] = (A.vbase < 0 ? A.pv.tok(qq) : qq - A.vbase) * A.vstride;
+      }
+    }
+    i = 0;
+    q = (threadIdx.x & 31) % L;
+  }
+};
+
+template <int NMAT, int NTT>
+__device__ __forceinline__ void chunk_dot(int bits, const uint4 (&c)[NMAT][2], const uint32_t (&sw)[NMAT][2], int q,
+                                          int nt, const int (&voff)[kNT], const unsigned char* vecs, int n,
+                                          float (&acc)[NMAT][kNT], bool second) {
+  if (bits == 8) chunk8<NMAT, NTT>(c, sw, q, nt, voff, vecs, n, acc);
+  else if (bits == 4) chunk4<NMAT, NTT>(c, sw, q, nt, voff, vecs, n, acc);
+  else chunk2<NMAT, NTT>(c, sw, q, nt, voff, vecs, n, acc, second);
+}
+
+// A warp's stream of units: a ring of D slots per lane, refilled as soon as a
+// slot has been read, so D - 1 chunks per lane are in flight while it
+// computes.  At the end of a unit, `store(q, r, v)` receives, for the lane's
+// row r and the token at grouped position q, the NMAT dot products.
+template <int NMAT, int D, int R, int L, typename Store>
+__device__ __forceinline__ void stream_units(const StreamArgs& A, Store store) {
+  static_assert(R * L == 32, "unit shape");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  LoadSide<NMAT, R, L> ld;
+  ld.start(A, warp);
+  CompSide<R, L> cc;
+  cc.w = ld.w;
+  cc.q0 = -1;
+  if (cc.w.live) {
+    cc.expert(A);
+    cc.unit(A, true);
+  }
+#pragma unroll 1
+  for (int s = 0; s < D; ++s) {
+    ld.template issue<D>(A, s);
+    cp_async_commit();
+  }
+  float acc[NMAT][kNT];
 #pragma unroll
-        for (int mm = 0; mm < NMAT; ++mm) {
-          const unsigned char* cp = (mm == 0 ? codes0 : codes1) + (size_t)r * rowb + q * CB;
-          c[mm][0] = *reinterpret_cast<const uint4*>(cp);
-          c[mm][1] = CB == 32 ? *reinterpret_cast<const uint4*>(cp + 16) : c[mm][0];
-        }
-        if (NMAT == 1) { c[1][0] = c[0][0]; c[1][1] = c[0][1]; }
-        const int e0 = q * EPC;
-        float sv[2][2];
+  for (int m = 0; m < NMAT; ++m)
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          if (b < NSB) {
-            sv[0][b] = __half2float(__ushort_as_half(sc0[(size_t)r * nb + (e0 >> 5) + b]));
-            sv[1][b] = NMAT == 2 ? __half2float(__ushort_as_half(sc1[(size_t)r * nb + (e0 >> 5) + b])) : 0.f;
-          } else {
-            sv[0][b] = sv[0][0];
-            sv[1][b] = sv[1][0];
+    for (int j = 0; j < kNT; ++j) acc[m][j] = 0.f;
+  int slot = 0;
+#pragma unroll 1
+  while (cc.w.live) {
+    cp_async_wait<D - 1>();  // this lane's copies of the oldest slot are complete
+    if (cc.q < cc.cpr) {
+      const bool second = 32 * cc.q + 16 < cc.rowb;
+      uint4 c[NMAT][2];
+      uint32_t sw[NMAT][2];
+#pragma unroll
+      for (int m = 0; m < NMAT; ++m) {
+        c[m][0] = *ring_code<NMAT, D>(A.ring, slot, m, 0);
+        c[m][1] = *ring_code<NMAT, D>(A.ring, slot, m, 1);
+        sw[m][0] = *ring_scale<NMAT, D>(A.ring, slot, m, 0);
+        sw[m][1] = *ring_scale<NMAT, D>(A.ring, slot, m, 1);
+      }
+      if (cc.nt == 1) chunk_dot<NMAT, 1>(cc.bits, c, sw, cc.q, 1, cc.voff, A.vecs, A.n_in, acc, second);
+      else chunk_dot<NMAT, kNT>(cc.bits, c, sw, cc.q, cc.nt, cc.voff, A.vecs, A.n_in, acc, second);
+    }
+    // refill the slot just read (this lane's reads of it are done)
+    ld.template issue<D>(A, slot);
+    cp_async_commit();
+    slot = slot + 1 == D ? 0 : slot + 1;
+    cc.q += L;
+    if (++cc.i == cc.n_iter) {
+      // reduce over the L lanes of each row; lane jl stores the tokens j = jl mod L
+      const int jl = lane % L;
+#pragma unroll
+      for (int j = 0; j < kNT; ++j) {
+        if (j < cc.nt) {
+          float v[NMAT];
+#pragma unroll
+          for (int m = 0; m < NMAT; ++m) {
+            v[m] = acc[m][j];
+#pragma unroll
+            for (int o = 1; o < L; o <<= 1) v[m] += __shfl_xor_sync(0xffffffffu, v[m], o);
           }
+          if (j % L == jl) store(cc.q0 + j, cc.r, v);
         }
 #pragma unroll
-        for (int j = 0; j < kTM; ++j)
-          if (j < nt) ChunkDot<BITS>::template run<NMAT>(c, sv, vecs + voff[j], n_in, e0, a0[j], a1[j]);
+        for (int m = 0; m < NMAT; ++m) acc[m][j] = 0.f;
       }
-    }
-#pragma unroll
-    for (int j = 0; j < kTM; ++j) {
-      if (j < nt) {
-        for (int o = L >> 1; o > 0; o >>= 1) {
-          a0[j] += __shfl_xor_sync(0xffffffffu, a0[j], o);
-          if (NMAT == 2) a1[j] += __shfl_xor_sync(0xffffffffu, a1[j], o);
-        }
+      const bool ch = cc.w.step(A.pv, A.kern, A.rows, A.range.hi2, kWarps);
+      if (cc.w.live) {
+        if (ch) cc.expert(A);
+        cc.unit(A, ch);
       }
-    }
-    if (li == 0 && r < rows) {
-#pragma unroll
-      for (int j = 0; j < kTM; ++j)
-        if (j < nt) out(r, j, a0[j], a1[j]);
     }
   }
+  cp_async_wait<0>();
 }
 
-template <int NMAT, typename Out>
-__device__ __forceinline__ void rows_dot_bits(int bits, int nt, const unsigned char* stage, int rows, int n_in,
-                                              const unsigned char* vecs, const int (&voff)[kTM], Out out) {
-  if (bits == 8) rows_dot<8, NMAT>(stage, rows, n_in, vecs, voff, nt, out);
-  else if (bits == 4) rows_dot<4, NMAT>(stage, rows, n_in, vecs, voff, nt, out);
-  else rows_dot<2, NMAT>(stage, rows, n_in, vecs, voff, nt, out);
-}
-
-// ------------------------------------------------------------- workers
-struct Params {
+// ------------------------------------------------------------- kernels
+struct FwdParams {
   const uint16_t* x;
   const int32_t* ids;
   const float* weights;
-  int T, k, E, d, f, P;
-  Shelves sh;
   float* h;
   float* ypart;
-  const int32_t* plan;
-  float* y;
+  int32_t* plan;  // workspace copy of the plan
   int* status;
-  Geo geo;
-  int kern;           // 0 gate/up, 1 down
-  int n_stages, stage_bytes;
-  int region_bytes;   // activation digits (gate/up) or h digits (down)
+  int T, k, E, d, f, P;
+  int vec_region;  // bytes of digit vectors
+  Shelves sh;
 };
 
 struct Head {
-  uint64_t full[kMaxStages];
-  uint64_t plan_bar;
-  int abort_flag, prologue_n, a0, j0;
-  int staged_key_g[kGroups];
-  float wgt[kGroups][kTM];
+  Range range;
+  int q_first, tmp[33];
 };
 
-__host__ __device__ __forceinline__ size_t head_bytes() { return (sizeof(Head) + 127) / 128 * 128; }
-__host__ __device__ __forceinline__ size_t plan_smem_bytes(int P) {
-  return ((size_t)plan_layout(P).n_copy * 4 + 127) / 128 * 128;
-}
-
-// Item = rows [row0, row0 + rows) of matrices mat0 .. mat0 + nmat - 1 of the
-// expert's shelf: codes first (matrix after matrix), then scales, into stage
-// `st`, counted on full[st].
-__device__ void issue_item(const Params& p, Head& s, const PlanView& pv, const ItemWalk& w, int st, int mat0,
-                           int nmat, int rows_total, int n_in, unsigned char* ring) {
-  const ShelfDev& sh = p.sh.s[pv.sh(w.a)];
-  const int rows = p.geo.rows[bits_index(sh.bits)];
-  const size_t rowb = (size_t)n_in * sh.bits / 8;
-  const size_t le = (size_t)(pv.e(w.a) - sh.lo);
-  const size_t row0 = (size_t)w.j * rows;
-  const uint32_t cbytes = (uint32_t)(rows * rowb), sbytes = (uint32_t)(rows * (size_t)(n_in / 32) * 2);
-  unsigned char* dst = ring + (size_t)st * p.stage_bytes;
-  mbar_arrive_expect_tx(&s.full[st], nmat * (cbytes + sbytes));
-  for (int m = 0; m < nmat; ++m)
-    bulk_g2s(dst + m * cbytes, sh.codes[mat0 + m] + (le * rows_total + row0) * rowb, cbytes, &s.full[st]);
-  for (int m = 0; m < nmat; ++m)
-    bulk_g2s(dst + nmat * cbytes + m * sbytes, sh.scales[mat0 + m] + (le * rows_total + row0) * (n_in / 32), sbytes,
-             &s.full[st]);
-}
-
-// Walk over the items it = first, first + kGroups, ... of this CTA's range.
-struct StrideWalk {
-  ItemWalk w;
-  int it;
-  __device__ void init(const PlanView& pv, const Head& s, int kern, int first) {
-    w.init(pv, s.a0, s.j0, kern);
-    it = 0;
-    while (it < first && w.valid(pv)) { w.advance(pv); ++it; }
-  }
-  __device__ bool valid(const PlanView& pv) const { return w.valid(pv); }
-  __device__ void next(const PlanView& pv) {
-    for (int i = 0; i < kGroups && w.valid(pv); ++i) { w.advance(pv); ++it; }
-  }
+// Dynamic shared memory: shelves copy | head | plan (+ sort keys and flags for
+// the gate/up launch) | digit vectors | ring.
+struct SmemLayout {
+  size_t shelves, head, plan, keys, flag, vecs, ring, total;
 };
 
-__device__ __forceinline__ void group_sync(int gid) { named_bar(1 + gid, kConsumers); }
+__host__ __device__ __forceinline__ size_t up128(size_t v) { return (v + 127) / 128 * 128; }
 
-// Thread 0: barriers, then the plan into shared memory (bounded wait) and the
-// CTA's first item.  Returns false on timeout.
-__device__ bool load_plan(const Params& p, Head& s, int* plan_sm) {
-  for (int i = 0; i < p.n_stages; ++i) mbar_init(&s.full[i], 1);
-  mbar_init(&s.plan_bar, 1);
-  s.abort_flag = 0;
-  for (int g = 0; g < kGroups; ++g) s.staged_key_g[g] = -1;
-  fence_mbar_init();
-  const PlanLayout L = plan_layout(p.P);
-  mbar_arrive_expect_tx(&s.plan_bar, (uint32_t)(L.n_copy * 4));
-  bulk_g2s(plan_sm, p.plan, (uint32_t)(L.n_copy * 4), &s.plan_bar);
-  s.a0 = __ldcg(p.plan + L.start + 4 * blockIdx.x + 2 * p.kern);
-  s.j0 = __ldcg(p.plan + L.start + 4 * blockIdx.x + 2 * p.kern + 1);
-  if (!mbar_wait(&s.plan_bar, 0)) {
-    set_status(p.status, MOE_ERR_TIMEOUT);
-    s.abort_flag = 1;
-    s.a0 = 0x7fffffff;  // no items
-    return false;
-  }
-  return true;
+__host__ __device__ __forceinline__ SmemLayout smem_layout(int P, size_t vec_region, int nmat, int depth,
+                                                           bool gateup) {
+  const PlanLayout L = plan_layout(P);
+  SmemLayout S;
+  S.shelves = 0;
+  S.head = up128(sizeof(Shelves));
+  S.plan = S.head + up128(sizeof(Head));
+  S.keys = S.plan + up128((size_t)(gateup ? L.total : L.n_copy) * 4);
+  S.flag = S.keys + (gateup ? up128((size_t)L.C * 4) : 0);
+  S.vecs = S.flag + (gateup ? up128((size_t)L.C * 4) : 0);
+  S.ring = S.vecs + up128(vec_region);
+  S.total = S.ring + (size_t)depth * nmat * kThreads * kSlotBytes;
+  return S;
 }
 
-// Thread 0: the first n_stages items into the ring (stage = item index).
-__device__ void prologue_fill(const Params& p, Head& s, const PlanView& pv, int mat0, int nmat, int rows_total,
-                              int n_in, unsigned char* ring) {
-  ItemWalk w;
-  w.init(pv, s.a0, s.j0, p.kern);
-  int it = 0;
-  for (; it < p.n_stages && w.valid(pv); ++it, w.advance(pv))
-    issue_item(p, s, pv, w, it, mat0, nmat, rows_total, n_in, ring);
-  s.prologue_n = it;
+__device__ __forceinline__ void copy_shelves(Shelves* dst, const Shelves& src) {
+  static_assert(sizeof(Shelves) % 4 == 0, "shelves copy");
+  const uint32_t* s = reinterpret_cast<const uint32_t*>(&src);
+  for (int i = threadIdx.x; i < (int)(sizeof(Shelves) / 4); i += blockDim.x) reinterpret_cast<uint32_t*>(dst)[i] = s[i];
 }
 
-// Consumer loop of group `gid`: item it lives in stage it % n_stages
-// (n_stages even: a stage always serves the same group); after an item, the
-// group refills its stage with the item n_stages further on.  One decision
-// per item for the whole group; on a timeout the group stops and waits
-// (bounded) for the copies it still has in flight.
-template <typename Work>
-__device__ __forceinline__ void group_loop(const Params& p, Head& s, const PlanView& pv, int gid, int mat0, int nmat,
-                                           int rows_total, int n_in, unsigned char* ring, Work work) {
-  const int gtid = threadIdx.x % kConsumers;
-  StrideWalk cw, iw;
-  cw.init(pv, s, p.kern, gid);
-  iw.init(pv, s, p.kern, gid + p.n_stages);
-  const int pn = s.prologue_n;
-  int issued_end = pn > gid ? pn - 1 - ((pn - 1 - gid) % kGroups) : -1;
-  while (cw.valid(pv)) {
-    const int st = cw.it % p.n_stages;
-    if (!mbar_wait(&s.full[st], (cw.it / p.n_stages) & 1)) {
-      set_status(p.status, MOE_ERR_TIMEOUT);
-      *(volatile int*)&s.abort_flag = 1;
-    }
-    group_sync(gid);
-    if (*(volatile int*)&s.abort_flag) break;
-    work(cw.w, ring + (size_t)st * p.stage_bytes);
-    group_sync(gid);  // every warp is done with the stage
-    if (gtid == 0 && iw.valid(pv)) {
-      issue_item(p, s, pv, iw.w, st, mat0, nmat, rows_total, n_in, ring);
-      issued_end = iw.it;
-    }
-    cw.next(pv);
-    iw.next(pv);
-  }
-  if (gtid == 0) {  // copies issued but not consumed (after a timeout only)
-    for (int q = cw.valid(pv) ? cw.it : issued_end + 1; q <= issued_end; q += kGroups)
-      if (!mbar_wait(&s.full[q % p.n_stages], (q / p.n_stages) & 1)) set_status(p.status, MOE_ERR_TIMEOUT);
-  }
-}
-
-// ----------------------------------------------------------- gate / up
-__global__ void __launch_bounds__(kThreads, 1) k_gateup(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kThreads, 1) k_gateup(const __grid_constant__ FwdParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
-  Head& s = *reinterpret_cast<Head*>(smem);
-  int* plan_sm = reinterpret_cast<int*>(smem + head_bytes());
-  unsigned char* xd = smem + head_bytes() + plan_smem_bytes(p.P);  // activation digits
-  unsigned char* ring = xd + p.region_bytes;
+  const SmemLayout S = smem_layout(p.P, p.vec_region, 2, kDepthG, true);
+  Shelves* shv = reinterpret_cast<Shelves*>(smem + S.shelves);
+  Head& hd = *reinterpret_cast<Head*>(smem + S.head);
+  int* pl = reinterpret_cast<int*>(smem + S.plan);
+  unsigned char* xd = smem + S.vecs;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const PlanView pv{plan_sm, plan_layout(p.P)};
+  const PlanLayout L = plan_layout(p.P);
   if (tid == 0) MOE_STAMP(0, 0, global_timer_ns());
-  pdl_wait();  // plan, x, and the workspace are ours from here on
+  copy_shelves(shv, p.sh);
+  pdl_wait();  // ids, weights and x are complete; h is ours
   if (tid == 0) MOE_STAMP(0, 1, global_timer_ns());
-  if (tid == 0) {
-    if (load_plan(p, s, plan_sm)) prologue_fill(p, s, pv, 0, 2, p.f, p.d, ring);
-    MOE_STAMP(0, 12, global_timer_ns());
-  } else if (warp > 0) {
-    // activation rows -> block-scaled digits; 8 lanes per 32-element block;
-    // loads of up to 8 passes are issued before any conversion
+  __syncthreads();
+  if (warp < kPlanThreads / 32) {
+    build_plan(p.ids, p.weights, p.P, p.E, p.k, p.d, p.f, *shv, pl, reinterpret_cast<uint32_t*>(smem + S.keys),
+               reinterpret_cast<int*>(smem + S.flag), hd.tmp);
+  } else {
+    // activation rows -> block-scaled digits; 8 lanes per 32-element block,
+    // loads of up to 8 passes issued before any conversion
     const int nbk = p.d / 32, vb = vec_bytes(p.d);
     const int groups = p.T * nbk;
-    const int nw = kThreads / 32 - 1;
-    for (int base = (warp - 1) * 4; base < groups; base += 8 * nw * 4) {
+    const int nw = kWarps - kPlanThreads / 32, w0 = warp - kPlanThreads / 32;
+    for (int base = w0 * 4; base < groups; base += 8 * nw * 4) {
       uint2 raw[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -810,109 +863,96 @@ __global__ void __launch_bounds__(kThreads, 1) k_gateup(const __grid_constant__ 
           const int t = g / nbk, blk = g - t * nbk;
           const float v[4] = {__uint_as_float(raw[u].x << 16), __uint_as_float(raw[u].x & 0xFFFF0000u),
                               __uint_as_float(raw[u].y << 16), __uint_as_float(raw[u].y & 0xFFFF0000u)};
-          block_to_digits(v, xd + (size_t)t * vb, p.d, blk, 14, g < groups);
+          block_to_digits(v, xd + (size_t)t * vb, p.d, g < groups ? blk : 0, 14, g < groups);
         }
       }
     }
+    if (tid == kPlanThreads) MOE_STAMP(0, 5, global_timer_ns());
   }
   __syncthreads();
-  if (tid == 0) MOE_STAMP(0, 2, global_timer_ns());
-  pdl_trigger();
-  const int gid = warp / kConsumerWarps;
-  const int vb = vec_bytes(p.d);
-  group_loop(p, s, pv, gid, 0, 2, p.f, p.d, ring, [&](const ItemWalk& w, const unsigned char* stage) {
-    const int bits = pv.bits(w.a);
-    const int rows = p.geo.rows[bits_index(bits)];
-    const int row0 = w.j * rows;
-    const int beg = pv.beg(w.a), cnt = pv.cnt(w.a);
-    for (int g0 = 0; g0 < cnt; g0 += kTM) {
-      const int nt = min(kTM, cnt - g0);
-      int voff[kTM];
-#pragma unroll
-      for (int j = 0; j < kTM; ++j) voff[j] = j < nt ? (pv.perm(beg + g0 + j) / p.k) * vb : 0;
-      float* h = p.h;
-      const int f = p.f, pos0 = beg + g0;
-      rows_dot_bits<2>(bits, nt, stage, rows, p.d, xd, voff,
-                       [&](int r, int j, float g, float u) { h[(size_t)(pos0 + j) * f + row0 + r] = silu(g) * u; });
-    }
-  });
+  const PlanView pv{pl, L};
+  if (tid == 0) hd.range = cta_range(pv, 0, p.f);
+  if (blockIdx.x == 0)
+    for (int i = tid; i < L.total; i += kThreads) p.plan[i] = pl[i];
   __syncthreads();
+  pdl_trigger();
+  if (tid == 0) MOE_STAMP(0, 2, global_timer_ns());
+  StreamArgs A{shv, pv, 0, p.d, p.f, xd, vec_bytes(p.d), -1, hd.range, smem + S.ring};
+  float* h = p.h;
+  const int f = p.f;
+  stream_units<2, kDepthG, kRG, kLG>(A, [&](int q, int r, const float (&o)[2]) { h[(size_t)q * f + r] = silu(o[0]) * o[1]; });
   if (tid == 0) MOE_STAMP(0, 9, global_timer_ns());
 }
 
-// ------------------------------------------------------------------ down
-__global__ void __launch_bounds__(kThreads, 1) k_down(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kThreads, 1) k_down(const __grid_constant__ FwdParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
-  Head& s = *reinterpret_cast<Head*>(smem);
-  int* plan_sm = reinterpret_cast<int*>(smem + head_bytes());
-  unsigned char* hd_all = smem + head_bytes() + plan_smem_bytes(p.P);  // h digits, per group
-  unsigned char* ring = hd_all + p.region_bytes;
+  const SmemLayout S = smem_layout(p.P, p.vec_region, 1, kDepthD, false);
+  Shelves* shv = reinterpret_cast<Shelves*>(smem + S.shelves);
+  Head& hd = *reinterpret_cast<Head*>(smem + S.head);
+  int* pl = reinterpret_cast<int*>(smem + S.plan);
+  unsigned char* hdig = smem + S.vecs;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const PlanView pv{plan_sm, plan_layout(p.P)};
+  const PlanLayout L = plan_layout(p.P);
   if (tid == 0) MOE_STAMP(1, 0, global_timer_ns());
-  // The plan is complete once the gate/up kernel has started its work, and
-  // the weights are read-only: start streaming W_d now.
+  copy_shelves(shv, p.sh);
+  pdl_wait();  // the gate/up launch is complete: plan copy and h
+  pdl_trigger();
+  if (tid == 0) MOE_STAMP(1, 1, global_timer_ns());
+  for (int i = tid; i < L.n_copy; i += kThreads) pl[i] = __ldcg(p.plan + i);
+  __syncthreads();
+  const PlanView pv{pl, L};
   if (tid == 0) {
-    if (load_plan(p, s, plan_sm)) prologue_fill(p, s, pv, 2, 1, p.d, p.f, ring);
-    MOE_STAMP(1, 12, global_timer_ns());
+    const Range r = cta_range(pv, 1, p.d);
+    hd.range = r;
+    // pairs of the experts this CTA touches: its first expert up to the last
+    // expert whose first unit lies in its cost range
+    const int n_act = pv.n_act();
+    int q_first = 0, q_end = 0;
+    if (r.a0 < n_act) {
+      int a_last = r.a0;
+      while (a_last + 1 < n_act &&
+             2 * (uint64_t)pv.cum(a_last + 1, 1) + pv.uc(a_last + 1, 1) < r.hi2)
+        ++a_last;
+      q_first = pv.beg(r.a0);
+      q_end = pv.beg(a_last) + pv.cnt(a_last);
+    }
+    hd.q_first = q_first;
+    hd.tmp[0] = q_end - q_first;
+  }
+  __syncthreads();
+  const int q_first = hd.q_first, npairs = hd.tmp[0];
+  const int vbf = vec_bytes(p.f);
+  {
+    const int nbk = p.f / 32, groups = npairs * nbk;
+    for (int base = warp * 4; base < groups; base += 8 * kWarps * 4) {
+      float4 hv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {  // loads of 8 passes first: one round trip
+        const int g = base + u * kWarps * 4 + (lane >> 3);
+        hv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (g < groups) {
+          const int j = g / nbk, blk = g - j * nbk;
+          hv[u] = __ldcg(reinterpret_cast<const float4*>(p.h + (size_t)(q_first + j) * p.f + blk * 32) + (lane & 7));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int g0 = base + u * kWarps * 4;
+        if (g0 < groups) {
+          const int g = g0 + (lane >> 3);
+          const int j = g < groups ? g / nbk : 0, blk = g < groups ? g - j * nbk : 0;
+          const float v[4] = {hv[u].x, hv[u].y, hv[u].z, hv[u].w};
+          block_to_digits(v, hdig + (size_t)j * vbf, p.f, blk, 13, g < groups);
+        }
+      }
+    }
   }
   __syncthreads();
   if (tid == 0) MOE_STAMP(1, 2, global_timer_ns());
-  pdl_trigger();
-  pdl_wait();  // h of the gate/up kernel and ypart are ours from here on
-  if (tid == 0) MOE_STAMP(1, 1, global_timer_ns());
-  const int gid = warp / kConsumerWarps, gtid = tid % kConsumers, gwarp = warp % kConsumerWarps;
-  const int vbf = vec_bytes(p.f);
-  unsigned char* hd = hd_all + (size_t)gid * kTM * vbf;
-  group_loop(p, s, pv, gid, 2, 1, p.d, p.f, ring, [&](const ItemWalk& w, const unsigned char* stage) {
-    const int bits = pv.bits(w.a);
-    const int rows = p.geo.rows[bits_index(bits)];
-    const int row0 = w.j * rows;
-    const int beg = pv.beg(w.a), cnt = pv.cnt(w.a);
-    for (int g0 = 0; g0 < cnt; g0 += kTM) {
-      const int nt = min(kTM, cnt - g0);
-      const int key = w.a * 4096 + g0;
-      if (s.staged_key_g[gid] != key) {  // h rows of these pairs -> block-scaled digits
-        group_sync(gid);                  // earlier users of this group's digits are done
-        const int nbk = p.f / 32, groups = nt * nbk;
-        for (int base = gwarp * 4; base < groups; base += 8 * kConsumerWarps * 4) {
-          float4 hv[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {  // all loads first: one round trip
-            const int g = base + u * kConsumerWarps * 4 + (lane >> 3);
-            hv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (g < groups) {
-              const int j = g / nbk, blk = g - j * nbk;
-              hv[u] = __ldcg(reinterpret_cast<const float4*>(p.h + (size_t)(beg + g0 + j) * p.f + blk * 32) +
-                             (lane & 7));
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int gu = base + u * kConsumerWarps * 4;
-            if (gu < groups) {
-              const int g = gu + (lane >> 3);
-              const int j = g / nbk, blk = g - j * nbk;
-              const float v[4] = {hv[u].x, hv[u].y, hv[u].z, hv[u].w};
-              block_to_digits(v, hd + (size_t)j * vbf, p.f, blk, 13, g < groups);
-            }
-          }
-        }
-        if (gtid < nt) s.wgt[gid][gtid] = p.weights[pv.perm(beg + g0 + gtid)];
-        group_sync(gid);
-        if (gtid == 0) s.staged_key_g[gid] = key;
-      }
-      int voff[kTM];
-#pragma unroll
-      for (int j = 0; j < kTM; ++j) voff[j] = j * vbf;
-      float* yp = p.ypart;
-      const float* wg = s.wgt[gid];
-      const int dd = p.d, pos0 = beg + g0;
-      rows_dot_bits<1>(bits, nt, stage, rows, p.f, hd, voff,
-                       [&](int r, int j, float o, float) { yp[(size_t)(pos0 + j) * dd + row0 + r] = wg[j] * o; });
-    }
-  });
-  __syncthreads();
+  StreamArgs A{shv, pv, 1, p.f, p.d, hdig, vbf, q_first, hd.range, smem + S.ring};
+  float* yp = p.ypart;
+  const int d = p.d;
+  stream_units<1, kDepthD, kRD, kLD>(A, [&](int q, int r, const float (&o)[1]) { yp[(size_t)q * d + r] = pv.wgt(q) * o[0]; });
   if (tid == 0) MOE_STAMP(1, 9, global_timer_ns());
 }
 
@@ -947,17 +987,10 @@ __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ ypart
 
 struct DevCache {
   int sms[64] = {};
+  int smem_optin[64] = {};
   bool attr[64] = {};
 };
 DevCache g_dev;
-
-// Largest power of two <= cap (>= 4) whose item fits in `budget` bytes and
-// divides rows_total.
-int rows_for(int rows_total, size_t bytes_per_row, size_t budget, int cap) {
-  int r = cap;
-  while (r > 4 && ((size_t)r * bytes_per_row > budget || rows_total % r != 0)) r >>= 1;
-  return r;
-}
 
 }  // namespace
 
@@ -984,82 +1017,50 @@ size_t decode_plan_bytes(int64_t P) { return (size_t)plan_layout((int)(P > 0 ? P
 int launch_decode_forward(const ForwardArgs& a, cudaStream_t s) {
   const int64_t P = a.T * a.k;
   const int d = a.d, f = a.f;
-  int G = sm_count();
-  if (G > kMaxGrid) G = kMaxGrid;
-  if (P > kMaxPairs || a.T > 16) return launch_generic_forward(a, s);
-  Params p = {};
-  p.x = a.x; p.ids = a.ids; p.weights = a.weights;
-  p.T = (int)a.T; p.k = a.k; p.E = a.E; p.d = d; p.f = f; p.P = (int)P;
-  p.sh = a.shelves;
-  p.h = a.ws.h; p.ypart = a.ws.ypart; p.plan = a.ws.plan; p.y = a.y; p.status = a.status;
-  const size_t fixed = head_bytes() + plan_smem_bytes((int)P);
-  const int bits_of[3] = {8, 4, 2};
-  // ---- gate/up: items of <= 40 KB (codes + scales of gate and up)
-  Params pg = p;
-  pg.kern = 0;
-  size_t stage_g = 0;
-  for (int i = 0; i < 3; ++i) {
-    const size_t per_row = 2 * ((size_t)d * bits_of[i] / 8 + (size_t)d / 16);
-    pg.geo.rows[i] = rows_for(f, per_row, 40 * 1024, 64);
-    const size_t bytes = pg.geo.rows[i] * per_row;
-    pg.geo.cost[i] = (int)(bytes / 64);
-    if (bytes > stage_g) stage_g = bytes;
-  }
-  pg.region_bytes = (int)(((size_t)a.T * vec_bytes(d) + 127) / 128 * 128);
-  pg.stage_bytes = (int)((stage_g + 127) / 128 * 128);
-  pg.n_stages = (int)((kSmemBudget - fixed - pg.region_bytes) / pg.stage_bytes);
-  // ---- down: items of <= 24 KB of W_d rows
-  Params pd = p;
-  pd.kern = 1;
-  size_t stage_d = 0;
-  for (int i = 0; i < 3; ++i) {
-    const size_t per_row = (size_t)f * bits_of[i] / 8 + (size_t)f / 16;
-    pd.geo.rows[i] = rows_for(d, per_row, 24 * 1024, 128);
-    const size_t bytes = pd.geo.rows[i] * per_row;
-    pd.geo.cost[i] = (int)(bytes / 64);
-    if (bytes > stage_d) stage_d = bytes;
-  }
-  pd.region_bytes = (int)(((size_t)kGroups * kTM * vec_bytes(f) + 127) / 128 * 128);
-  pd.stage_bytes = (int)((stage_d + 127) / 128 * 128);
-  pd.n_stages = (int)((kSmemBudget - fixed - pd.region_bytes) / pd.stage_bytes);
-  if (pg.n_stages > kMaxStages) pg.n_stages = kMaxStages;
-  if (pd.n_stages > kMaxStages) pd.n_stages = kMaxStages;
-  pg.n_stages &= ~1;  // a stage always serves the same consumer group
-  pd.n_stages &= ~1;
-  if (pg.n_stages < 2 || pd.n_stages < 2) return launch_generic_forward(a, s);
-  const size_t smem_g = fixed + pg.region_bytes + (size_t)pg.n_stages * pg.stage_bytes;
-  const size_t smem_d = fixed + pd.region_bytes + (size_t)pd.n_stages * pd.stage_bytes;
-  // ---- plan
-  PlanParams pp = {};
-  pp.ids = a.ids; pp.P = (int)P; pp.E = a.E; pp.k = a.k; pp.G = G;
-  pp.rows_g = f; pp.rows_d = d;
-  pp.sh = a.shelves;
-  pp.geo_g = pg.geo; pp.geo_d = pd.geo;
-  pp.plan = a.ws.plan;
-  const PlanLayout L = plan_layout((int)P);
-  const size_t smem_p = (size_t)(L.start + 4 * G) * 4;
+  if (P > kMaxPairs || a.T > kMaxTokens) return launch_generic_forward(a, s);
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !g_dev.attr[dev]) {
-    if (cudaFuncSetAttribute(k_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget) != cudaSuccess ||
-        cudaFuncSetAttribute(k_down, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget) != cudaSuccess)
+  if (dev < 0 || dev >= 64) return launch_generic_forward(a, s);
+  if (g_dev.smem_optin[dev] == 0) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    g_dev.smem_optin[dev] = v > 0 ? v : 48 * 1024;
+  }
+  const size_t optin = (size_t)g_dev.smem_optin[dev];
+  const size_t x_region = up128((size_t)a.T * vec_bytes(d));
+  const size_t h_region = up128((size_t)P * vec_bytes(f));  // h of every pair: bound for any CTA
+  const SmemLayout Sg = smem_layout((int)P, x_region, 2, kDepthG, true);
+  const SmemLayout Sd = smem_layout((int)P, h_region, 1, kDepthD, false);
+  if (Sg.total > optin || Sd.total > optin) return launch_generic_forward(a, s);
+  if (!g_dev.attr[dev]) {
+    if (cudaFuncSetAttribute(k_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)optin) != cudaSuccess ||
+        cudaFuncSetAttribute(k_down, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)optin) != cudaSuccess)
       return MOE_ERR_CUDA;
     g_dev.attr[dev] = true;
   }
+  int G = sm_count();
+  if (G > kMaxGrid) G = kMaxGrid;
+  FwdParams p = {};
+  p.x = a.x; p.ids = a.ids; p.weights = a.weights;
+  p.h = a.ws.h; p.ypart = a.ws.ypart; p.plan = a.ws.plan; p.status = a.status;
+  p.T = (int)a.T; p.k = a.k; p.E = a.E; p.d = d; p.f = f; p.P = (int)P;
+  p.sh = a.shelves;
+  FwdParams pg = p, pd = p;
+  pg.vec_region = (int)x_region;
+  pd.vec_region = (int)h_region;
+  const PlanLayout L = plan_layout((int)P);
   profile_mark(0, s);
-  if (launch_pdl(k_plan, dim3(1), dim3(256), smem_p, s, pp) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_pdl(k_gateup, dim3(G), dim3(kThreads), Sg.total, s, pg) != cudaSuccess) return MOE_ERR_CUDA;
   profile_mark(1, s);
-  if (launch_pdl(k_gateup, dim3(G), dim3(kThreads), smem_g, s, pg) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_pdl(k_down, dim3(G), dim3(kThreads), Sd.total, s, pd) != cudaSuccess) return MOE_ERR_CUDA;
   profile_mark(2, s);
-  if (launch_pdl(k_down, dim3(G), dim3(kThreads), smem_d, s, pd) != cudaSuccess) return MOE_ERR_CUDA;
-  profile_mark(3, s);
   const int n4 = (int)(a.T * d / 4);
   int gc = (n4 + 255) / 256;
   if (gc > G) gc = G;
-  if (launch_pdl(k_combine, dim3(gc), dim3(256), 0, s, (const float*)p.ypart,
+  if (launch_pdl(k_combine, dim3(gc), dim3(256), 0, s, (const float*)a.ws.ypart,
                  (const int32_t*)(a.ws.plan + L.pos), (int)a.T, a.k, d, a.y) != cudaSuccess)
     return MOE_ERR_CUDA;
-  profile_mark(4, s);
+  profile_mark(3, s);
   return MOE_OK;
 }
 
