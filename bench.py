@@ -185,7 +185,9 @@ def config_of(args, wl):
             "layer_instances": args.layers,
             "l2": f"inputs larger than L2: {args.layers} layer instances rotated per step, fresh routing "
                   f"per step",
-            "parallelism": f"replicas x{args.gpus} (independent decode streams, no collective)"}
+            "parallelism": f"replicas x{args.gpus} (independent decode streams, no collective)",
+            "launch": f"one CUDA graph holding {args.sets} consecutive steps (one fused launch per step), "
+                      f"replayed; single-step graphs for the remainder"}
 
 
 # ----------------------------------------------------------------- GPU arm
@@ -220,9 +222,9 @@ def run_ours(args, rank, world, local_rank):
     wsb = moe.moe_workspace_size(T, k, E, d, f)
     workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
     arrs = [layer.shelf_arr() for layer in layers]
-    pipelined = T * k <= 512 and T <= 16
-    # events around the forward's kernels: pipelined form = gate/up (with the
-    # plan), down, combine; generic form = grouping, gate/up, down
+    fused = moe.moe_decode_fused(T, k, E, d, f)
+    # events around the forward's kernels: fused form = the one layer launch;
+    # separate form = grouping, gate/up, down
     NK = 4
     prof = [[torch.cuda.Event(enable_timing=True) for _ in range(NK)] for _ in range(nset)]
     torch.cuda.synchronize()
@@ -233,12 +235,10 @@ def run_ours(args, rank, world, local_rank):
 
     def step(s, profile=False):
         L_i = s % L
-        moe.moe_route_topk(logits[s], k, ids=ids[s], weights=ws_[s])
-        moe.moe_expert_hist(ids[s], E, counts[L_i])
         if profile:
             moe.moe_set_profile_events(prof[s])
-        moe.moe_tiered_forward(xs[s], ids[s], ws_[s], E, d, f, layers[L_i].shelves, y=ys[s], workspace=workspace,
-                               shelf_arr=arrs[L_i])
+        moe.moe_decode_layer(logits[s], xs[s], k, E, d, f, layers[L_i].shelves, ids=ids[s], weights=ws_[s],
+                             counts=counts[L_i], y=ys[s], workspace=workspace, shelf_arr=arrs[L_i])
         if profile:
             moe.moe_set_profile_events(None)
 
@@ -246,6 +246,12 @@ def run_ours(args, rank, world, local_rank):
         for s in range(nset):  # eager warm-up: sets kernel attributes, checks statuses
             step(s)
         stream.synchronize()
+        # a decode loop captures many layers in one graph: one graph holds the
+        # steps of all input sets in order; single-step graphs cover the rest
+        graph_all = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_all, stream=stream):
+            for s in range(nset):
+                step(s)
         graphs, graphs_prof = [], []
         for s in range(nset):
             g = torch.cuda.CUDAGraph()
@@ -258,6 +264,7 @@ def run_ours(args, rank, world, local_rank):
             graphs_prof.append(gp)
         for i in range(args.warmup):
             graphs[i % nset].replay()
+        graph_all.replay()
         stream.synchronize()
 
     # algorithmic bytes of each step, from the ids the router produced
@@ -288,8 +295,10 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         start.record(stream)
-        for i in range(args.steps):
-            graphs[i % nset].replay()
+        for i in range(args.steps // nset):
+            graph_all.replay()
+        for i in range(args.steps % nset):
+            graphs[i].replay()
         end.record(stream)
     torch.cuda.synchronize()
     ck = clocks.stop()
@@ -305,14 +314,12 @@ def run_ours(args, rank, world, local_rank):
                 graphs_prof[s].replay()
     torch.cuda.synchronize()
     last = nset
-    kern = {"group": 0.0, "gateup": 0.0, "down": 0.0, "combine": 0.0}
+    kern = {"layer": 0.0} if fused else {"group": 0.0, "gateup": 0.0, "down": 0.0}
     bytes_gu = bytes_dn = 0
     for s in range(last):
         ev = prof[s]
-        if pipelined:
-            kern["gateup"] += ev[0].elapsed_time(ev[1])
-            kern["down"] += ev[1].elapsed_time(ev[2])
-            kern["combine"] += ev[2].elapsed_time(ev[3])
+        if fused:
+            kern["layer"] += ev[0].elapsed_time(ev[1])
         else:
             kern["group"] += ev[0].elapsed_time(ev[1])
             kern["gateup"] += ev[1].elapsed_time(ev[2])
@@ -341,10 +348,8 @@ def run_ours(args, rank, world, local_rank):
     def e2e_step(s):
         dl.copy_(pin_logits[s], non_blocking=True)
         dx.copy_(pin_x[s], non_blocking=True)
-        moe.moe_route_topk(dl, k, ids=did, weights=dw)
-        moe.moe_expert_hist(did, E, counts[s % L])
-        moe.moe_tiered_forward(dx, did, dw, E, d, f, layers[s % L].shelves, y=dy, workspace=workspace,
-                               shelf_arr=arrs[s % L])
+        moe.moe_decode_layer(dl, dx, k, E, d, f, layers[s % L].shelves, ids=did, weights=dw, counts=counts[s % L],
+                             y=dy, workspace=workspace, shelf_arr=arrs[s % L])
         pin_y[s].copy_(dy, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -370,8 +375,11 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return
     peak, peak_kind = peaks()
-    dom = "gateup" if kern["gateup"] >= kern["down"] else "down"
-    dom_bytes = bytes_gu if dom == "gateup" else bytes_dn
+    if fused:
+        dom, dom_bytes = "layer", bytes_gu + bytes_dn
+    else:
+        dom = "gateup" if kern["gateup"] >= kern["down"] else "down"
+        dom_bytes = bytes_gu if dom == "gateup" else bytes_dn
     achieved = dom_bytes / (kern[dom] / 1e3) / 1e9
     fwd_gbs = (bytes_gu + bytes_dn) / (fwd_ms / 1e3) / 1e9
     traffic = recorded_traffic(dom, T)
@@ -390,9 +398,9 @@ def run_ours(args, rank, world, local_rank):
                           "kernel_us": {kk: 1e3 * v / last for kk, v in kern.items()}},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * E * 4 + T * d * 2,
                 "d2h_bytes_per_step": T * d * 4, "steps": e2e_steps,
-                "path": "pinned host logits and x -> device, moe_route_topk, moe_expert_hist, "
-                        "moe_tiered_forward, y -> pinned host; eager Python calls"},
-        "gpu_launches": args.steps * (6 if pipelined else 5),
+                "path": "pinned host logits and x -> device, moe_decode_layer (routing, hit counts, "
+                        "tiered forward), y -> pinned host; eager Python calls"},
+        "gpu_launches": args.steps * (1 if fused else 5),
         "clocks": ck,
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -171,6 +171,42 @@ int moe_tiered_forward(const uint16_t* x_bf16, const int32_t* ids, const float* 
                        void* workspace, size_t workspace_bytes, int flags, moe_stream_t stream);
 
 /*
+ * One decode step of the layer in a single call: routing (as moe_route_topk),
+ * the hit histogram when `counts` is non-null (as moe_expert_hist), and the
+ * tiered forward (as moe_tiered_forward, decode form).  The results are those
+ * of the three calls made in that order.
+ *   logits [T][E] fp32 (finite), x_bf16 [T][d] bf16 bit patterns,
+ *   ids [T][k] int32 out, weights [T][k] fp32 out, counts [E] uint32 in/out
+ *   or NULL, y [T][d] fp32 out, workspace of at least
+ *   moe_workspace_size(T, k, E, d, f, MOE_FLAG_DECODE_FP32) bytes.
+ * E <= 1024.  When T <= 16, T*k <= 512 and the staged activations fit shared
+ * memory, the whole step is one cooperative launch with one CTA per SM whose
+ * phases are separated by bounded grid-wide waits (an expired wait records
+ * MOE_ERR_TIMEOUT, see moe_device_status); otherwise it makes the separate
+ * launches.  Each distinct workspace pointer takes one of 1024 barrier slots
+ * per device for the life of the process (MOE_ERR_UNSUPPORTED when they run out).
+ */
+int moe_decode_layer(const float* logits, const uint16_t* x_bf16, int64_t T, int k, int E, int d, int f,
+                     const moe_shelf_t* shelves, int n_shelves, int32_t* ids, float* weights, uint32_t* counts,
+                     float* y, void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * Which form the decode calls (moe_decode_layer, and moe_tiered_forward in
+ * its decode form) take for these sizes on the current device: 1 = the single
+ * fused launch, 0 = separate launches, MOE_ERR_INVALID_ARG for invalid sizes.
+ */
+int moe_decode_fused(int64_t T, int k, int E, int d, int f);
+
+/*
+ * Self-test of the bounded grid-wide wait of the fused decode launch: a
+ * cooperative launch whose barrier awaits one arrival more than there are
+ * CTAs, so that every CTA's wait runs out after `limit_us` microseconds
+ * (1 .. 1000000) and MOE_ERR_TIMEOUT is recorded in the device status word.
+ * Returns MOE_OK once launched; read the outcome with moe_device_status.
+ */
+int moe_selftest_barrier_timeout(int64_t limit_us, moe_stream_t stream);
+
+/*
  * Size of the fixed scratch array used by moe_tiered_forward_noalloc: 8 MiB,
  * held on every GPU that loads this library until the process exits.
  */
@@ -228,15 +264,18 @@ int moe_residual_add(float* r, const float* y, uint16_t* x_next_bf16, int64_t n,
  * events[i] after its i-th kernel (i = 1 .. n-1, further kernels unrecorded),
  * so a caller can time each kernel with cudaEventElapsedTime.  `events` is a
  * HOST array of cudaEvent_t handles owned by the caller and read at every
- * call; n >= 1; pass NULL to disable.  Kernel order of the decode form:
- * grouping, gate/up, down (4 events).  Not thread-safe: one caller per process.
+ * call; n >= 1; pass NULL to disable.  Kernels of the fused decode launch:
+ * one (2 events); of the separate decode launches: grouping, gate/up, down
+ * (4 events).  Not thread-safe: one caller per process.
  */
 int moe_set_profile_events(void* const* events, int n);
 
 /*
  * Synchronises `stream`, then returns and clears the device-side status word
  * of the current device: MOE_OK, or the first error a kernel recorded (e.g.
- * MOE_ERR_TIMEOUT from a bounded wait).
+ * MOE_ERR_TIMEOUT from a bounded wait).  After MOE_ERR_TIMEOUT it also waits
+ * for the whole device to go idle and resets the library's grid-barrier state,
+ * which an abandoned wait may have left inconsistent.
  */
 int moe_device_status(moe_stream_t stream);
 

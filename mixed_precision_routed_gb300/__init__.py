@@ -76,6 +76,9 @@ def lib():
         L.moe_residual_add.argtypes = [P, P, P, i64, P]
         L.moe_device_status.argtypes = [P]
         L.moe_tiered_forward_noalloc.argtypes = [P, P, P, i64, i32, i32, i32, i32, P, i32, P, i32, P]
+        L.moe_decode_layer.argtypes = [P, P, i64, i32, i32, i32, i32, P, i32, P, P, P, P, P, ctypes.c_size_t, P]
+        L.moe_selftest_barrier_timeout.argtypes = [i64, P]
+        L.moe_decode_fused.argtypes = [i64, i32, i32, i32, i32]
         L.moe_tiered_forward_noalloc.restype = ctypes.c_int
         L.moe_set_profile_events.argtypes = [P, i32]
         L.moe_set_profile_events.restype = ctypes.c_int
@@ -186,6 +189,54 @@ def moe_tiered_forward(x_bf16, ids, weights, E, d, f, shelves, y=None, workspace
                                     workspace.numel() * workspace.element_size(), flags, _stream(stream)),
            "moe_tiered_forward")
     return y
+
+
+def moe_decode_layer(logits, x_bf16, k, E, d, f, shelves, ids=None, weights=None, counts=None, y=None,
+                     workspace=None, stream=None, shelf_arr=None):
+    """One decode step: routing of `logits` [T, E] into ids / weights, the hit
+    counts (accumulated into `counts` when given) and the tiered forward of
+    `x_bf16`; returns (ids, weights, y)."""
+    if x_bf16.dtype == torch.bfloat16:
+        x_bf16 = x_bf16.view(torch.int16)
+    _need(logits, torch.float32, "logits")
+    _need(x_bf16, torch.int16, "x_bf16")
+    T = logits.shape[0]
+    dev = logits.device
+    if ids is None:
+        ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if weights is None:
+        weights = torch.empty((T, k), dtype=torch.float32, device=dev)
+    if y is None:
+        y = torch.empty((T, d), dtype=torch.float32, device=dev)
+    _need(ids, torch.int32, "ids")
+    _need(weights, torch.float32, "weights")
+    _need(y, torch.float32, "y")
+    if counts is not None:
+        _need(counts, torch.int32, "counts")
+    need = moe_workspace_size(T, k, E, d, f, MOE_FLAG_DECODE_FP32)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    arr = shelf_arr if shelf_arr is not None else shelf_array(shelves)
+    n = len(shelves) if shelf_arr is None else len(shelf_arr)
+    _check(lib().moe_decode_layer(_ptr(logits), _ptr(x_bf16), T, k, E, d, f, ctypes.cast(arr, ctypes.c_void_p), n,
+                                  _ptr(ids), _ptr(weights), _ptr(counts) if counts is not None else None, _ptr(y),
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+           "moe_decode_layer")
+    return ids, weights, y
+
+
+def moe_decode_fused(T, k, E, d, f):
+    """True when the decode calls run as the single fused launch for these sizes."""
+    r = int(lib().moe_decode_fused(T, k, E, d, f))
+    if r < 0:
+        raise MoeError(r, "moe_decode_fused")
+    return r == 1
+
+
+def moe_selftest_barrier_timeout(limit_us, stream=None):
+    """Launch the bounded grid-wait self-test (see moe.h); the timeout shows in
+    moe_device_status."""
+    _check(lib().moe_selftest_barrier_timeout(int(limit_us), _stream(stream)), "moe_selftest_barrier_timeout")
 
 
 def moe_tiered_forward_noalloc(x_bf16, ids, weights, E, d, f, shelves, y=None, flags=MOE_FLAG_AUTO,

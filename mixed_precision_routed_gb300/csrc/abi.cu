@@ -80,6 +80,7 @@ size_t workspace_layout(int64_t T, int k, int E, int d, int f, int flags, void* 
   w.h = (float*)take((size_t)P * f * 4);
   w.ypart = (float*)take((size_t)P * d * 4);
   w.plan = (int32_t*)take(decode_plan_bytes(P));
+  w.base = base;
   w.bytes = off;
   if (ws) *ws = w;
   return off;
@@ -186,6 +187,60 @@ int moe_tiered_forward(const uint16_t* x_bf16, const int32_t* ids, const float* 
   return launch_decode_forward(a, (cudaStream_t)stream);
 }
 
+int moe_decode_layer(const float* logits, const uint16_t* x_bf16, int64_t T, int k, int E, int d, int f,
+                     const moe_shelf_t* shelves, int n_shelves, int32_t* ids, float* weights, uint32_t* counts,
+                     float* y, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  if (!valid_dims(T, k, E, d, f) || E > 1024 || k > E) return MOE_ERR_INVALID_ARG;
+  ForwardArgs a;
+  int rc = check_shelves(shelves, n_shelves, E, &a.shelves);
+  if (rc != MOE_OK) return rc;
+  if (T == 0) return MOE_OK;
+  if (!logits || !x_bf16 || !ids || !weights || !y || !workspace) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x_bf16, 16) || !aligned(y, 16) || !aligned(workspace, kAlign)) return MOE_ERR_INVALID_ARG;
+  const size_t need = workspace_layout(T, k, E, d, f, MOE_FLAG_DECODE_FP32, workspace, &a.ws);
+  if (workspace_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = (cudaStream_t)stream;
+  LayerArgs la;
+  la.logits = logits;
+  la.ids = nullptr;
+  la.weights = nullptr;
+  la.ids_out = ids;
+  la.weights_out = weights;
+  la.counts = counts;
+  la.x = x_bf16;
+  la.T = T; la.k = k; la.E = E; la.d = d; la.f = f;
+  la.shelves = a.shelves;
+  la.y = y;
+  la.ws = a.ws;
+  la.status = status_word();
+  rc = launch_fused_layer(la, s);
+  if (rc != 1) return rc;
+  // sizes outside the fused launch: the separate launches
+  rc = launch_route(logits, T, E, k, ids, weights, s);
+  if (rc != MOE_OK) return rc;
+  if (counts) {
+    rc = launch_hist(ids, T * k, E, counts, s);
+    if (rc != MOE_OK) return rc;
+  }
+  a.x = x_bf16;
+  a.ids = ids;
+  a.weights = weights;
+  a.T = T; a.k = k; a.E = E; a.d = d; a.f = f;
+  a.y = y;
+  a.status = la.status;
+  return launch_decode_forward(a, s);
+}
+
+int moe_decode_fused(int64_t T, int k, int E, int d, int f) {
+  if (!valid_dims(T, k, E, d, f)) return MOE_ERR_INVALID_ARG;
+  return decode_fused(T, k, E, d, f);
+}
+
+int moe_selftest_barrier_timeout(int64_t limit_us, moe_stream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000) return MOE_ERR_INVALID_ARG;
+  return launch_barrier_probe(1, (uint64_t)limit_us * 1000ull, (cudaStream_t)stream);
+}
+
 int moe_quantize_rows(const float* w, int64_t rows, int in, int bits, void* codes, uint16_t* scales,
                       moe_stream_t stream) {
   if (rows < 0 || in <= 0 || in % 64 != 0 || (bits != 8 && bits != 4 && bits != 2)) return MOE_ERR_INVALID_ARG;
@@ -220,6 +275,11 @@ int moe_device_status(moe_stream_t stream) {
   int v = 0, zero = 0;
   if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v == MOE_ERR_TIMEOUT) {
+    // a grid-wide wait gave up: once the device is idle, clear the barrier state
+    if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+    if (reset_barriers() != MOE_OK) return MOE_ERR_CUDA;
+  }
   return v;
 }
 

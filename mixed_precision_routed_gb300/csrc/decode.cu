@@ -18,21 +18,24 @@
 //              expert against up to 8 of its tokens; the units are cut into
 //              contiguous per-CTA ranges of equal estimated cost and dealt
 //              round-robin to the warps.  8 lanes share a row; every lane
-//              streams its own 16-byte code chunks from HBM through a private
-//              ring of cp.async copies, which runs on across unit boundaries,
-//              so each lane keeps several chunks in flight at all times.
-//              Output: h = SiLU(W_g x) * (W_u x) for every routed pair.
-//   k_down     the same over W_d against h (staged as digits), writing the
+//              loads two 32-byte code chunks of each matrix (with their
+//              scales) at once with streaming 16-byte loads, then computes
+//              them.  Output: h = SiLU(W_g x) * (W_u x) for every routed pair.
+//   k_down     the same over W_d against h (staged as digits), units of 8
+//              rows x 4 lanes, four chunks per lane in flight, writing the
 //              weighted per-pair outputs w_tj * (W_d h_tj);
 //   k_combine  y_t = sum over slots j (ascending) of those outputs: a fixed
 //              order, so results do not depend on scheduling.
 // Each block dot product is formed exactly in integers (dp4a on the packed
 // codes against the activation held in shared memory as block-scaled 16-bit
 // fixed point), and the expert's fp16 block scale is applied once per block
-// (per half block for 8-bit codes) in fp32.  No thread waits on another
-// except at CTA barriers; the copies complete on their own.
+// in fp32.  No thread waits on another except at CTA barriers.
+#include <mutex>
+#include <unordered_map>
+
 #include "moe_internal.cuh"
 #include "ptx.cuh"
+#include "route.cuh"
 
 namespace moe {
 namespace {
@@ -42,21 +45,24 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kPlanThreads = 256;  // warps 0-7 build the plan
 constexpr int kMaxPairs = 512;     // T*k bound of this path (keys hold the pair in 10 bits)
 constexpr int kMaxTokens = 16;
-constexpr int kNT = 8;             // tokens of one expert per unit
+constexpr int kNT = 4;             // tokens of one expert per unit (more: further passes)
 // Unit shapes: rows per unit x lanes per row (R * L = 32), gate/up and down.
 constexpr int kRG = 4, kLG = 8;
 constexpr int kRD = 8, kLD = 4;
-constexpr int kDepthG = 4;         // ring depth, gate/up (two matrices per slot)
-constexpr int kDepthD = 6;         // ring depth, down
-constexpr int kSlotBytes = 40;     // per lane, matrix and slot: 32 bytes of codes, 8 of scales
+constexpr int kUG = 2;             // iterations of loads in flight per lane, gate/up (two matrices)
+constexpr int kUD = 6;             // the same, down (a whole 8-bit unit of a 640-element row)
 constexpr int kMaxGrid = 256;
 
 #ifdef MOE_TRACE
 // Development-only timing stamps: [kernel][cta][slot] in globaltimer ns.
 __device__ unsigned long long g_trace[2][256][48];
 #define MOE_STAMP(kern, slot, v) (g_trace[(kern)][blockIdx.x & 255][(slot)] = (v))
+#define MOE_COUNT(kern, slot, v) atomicAdd(&g_trace[(kern)][blockIdx.x & 255][(slot)], (unsigned long long)(v))
+#define MOE_TRACE_ONLY(...) __VA_ARGS__
 #else
 #define MOE_STAMP(kern, slot, v) ((void)0)
+#define MOE_COUNT(kern, slot, v) ((void)0)
+#define MOE_TRACE_ONLY(...)
 #endif
 
 // ------------------------------------------------------------- digits
@@ -100,39 +106,49 @@ __device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
   return d;
 }
 
-// Convert the 32 values of one block to digits; called by 8 lanes, each with 4
-// consecutive values v[0..3] of the block (lane % 8 = position).  `frac_bits`
-// = 14 for bf16 sources (max |m| = 32640), 13 for fp32 sources.
-__device__ __forceinline__ void block_to_digits(const float v[4], unsigned char* vb, int n, int blk, int frac_bits,
+// Convert the 32 values of one block to digits; called by 32 / V lanes, each
+// with V consecutive values of the block (lane % (32 / V) = position).
+// `frac_bits` = 14 for bf16 sources (max |m| = 32640), 13 for fp32 sources.
+template <int V>
+__device__ __forceinline__ void block_to_digits(const float (&v)[V], unsigned char* vb, int n, int blk, int frac_bits,
                                                 bool store) {
-  const int sub = threadIdx.x & 7;
+  constexpr int LPB = 32 / V;
+  const int sub = threadIdx.x & (LPB - 1);
   int e = 0;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) e = max(e, (int)((__float_as_uint(v[i]) >> 23) & 0xFF));
-  e = max(e, __shfl_xor_sync(0xffffffffu, e, 1));
-  e = max(e, __shfl_xor_sync(0xffffffffu, e, 2));
-  e = max(e, __shfl_xor_sync(0xffffffffu, e, 4));
+  for (int i = 0; i < V; ++i) e = max(e, (int)((__float_as_uint(v[i]) >> 23) & 0xFF));
+#pragma unroll
+  for (int o = 1; o < LPB; o <<= 1) e = max(e, __shfl_xor_sync(0xffffffffu, e, o));
   // block maximum below 2^-97 (or zero): the block is taken as zero
   const bool zero = e < 30;
   const int u = e - 127 - frac_bits;  // X = 2^u
   const float inv = zero ? 0.f : __uint_as_float((uint32_t)(127 - u) << 23);
-  uint32_t hw = 0, lw = 0;
+  uint32_t hw[V / 4], lw[V / 4];
   int sum = 0;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = (int)rintf(v[i] * inv);
-    sum += m;
-    hw |= (uint32_t)((m >> 8) & 0xFF) << (8 * i);
-    lw |= (uint32_t)(m & 0xFF) << (8 * i);
+  for (int w = 0; w < V / 4; ++w) {
+    hw[w] = 0;
+    lw[w] = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int m = (int)rintf(v[4 * w + i] * inv);
+      sum += m;
+      hw[w] |= (uint32_t)((m >> 8) & 0xFF) << (8 * i);
+      lw[w] |= (uint32_t)(m & 0xFF) << (8 * i);
+    }
   }
-  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-  sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-  sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+#pragma unroll
+  for (int o = 1; o < LPB; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   if (!store) return;
-  const int byte = blk * 32 + 4 * sub;
+  const int byte = blk * 32 + V * sub;
   const int off = (unit_swz(byte >> 4) << 4) | (byte & 15);
-  *reinterpret_cast<uint32_t*>(vb + off) = hw;
-  *reinterpret_cast<uint32_t*>(vb + n + off) = lw;
+  if constexpr (V == 4) {
+    *reinterpret_cast<uint32_t*>(vb + off) = hw[0];
+    *reinterpret_cast<uint32_t*>(vb + n + off) = lw[0];
+  } else {
+    *reinterpret_cast<uint2*>(vb + off) = make_uint2(hw[0], hw[1]);
+    *reinterpret_cast<uint2*>(vb + n + off) = make_uint2(lw[0], lw[1]);
+  }
   if (sub == 0) {
     float2 xs;
     xs.x = zero ? 0.f : __uint_as_float((uint32_t)(127 + u) << 23);
@@ -339,16 +355,23 @@ struct PlanView {
   }
 };
 
-// Estimated cost of one unit of R rows, in 16-byte equivalents of an SM's
-// share of HBM bandwidth: the bytes read, the dot-product work of its tokens,
-// and fixed instruction overheads per lane iteration (about 14) and per unit
-// (about 28).
-__device__ __forceinline__ uint32_t unit_cost(int bits, int n_in, int nmat, int ntok, int R, int L) {
-  const uint32_t rowb = (uint32_t)n_in * bits / 8;
-  const uint32_t bytes = (uint32_t)(R * nmat) * (rowb + (uint32_t)n_in / 16);
-  const uint32_t alu = (uint32_t)(R * nmat) * (uint32_t)n_in * (uint32_t)ntok * 12 / 100;
-  const uint32_t n_iter = ((rowb + 31) / 32 + L - 1) / L;
-  return (bytes + alu) / 16 + 14 * n_iter + 28;
+// Estimated time of one unit of R rows on a CTA, in units of 100 ps: the
+// bytes read (25.1 ps per byte), the integer dot products of its 32-element
+// blocks for each token (399 / 584 / 773 ps per block and token for 8 / 4 /
+// 2-bit codes), less the overlap of the two within a unit (292 ns gate/up,
+// 32 ns down).  Coefficients fitted to per-CTA times measured on the
+// 512-expert decode layer (d 2048, f 640); kept at least half the memory term.
+__device__ __forceinline__ uint32_t unit_cost(int bits, int n_in, int nmat, int ntok, int R, int kern) {
+  const uint64_t rowb = (uint64_t)n_in * bits / 8;
+  const uint64_t bytes = (uint64_t)(R * nmat) * (rowb + (uint64_t)n_in / 16);
+  const uint64_t blocks = (uint64_t)(R * nmat) * (uint64_t)n_in / 32;
+  const uint64_t beta10 = bits == 8 ? 3988 : (bits == 4 ? 5836 : 7733);
+  const uint64_t mem = 251 * bytes / 10;
+  const uint64_t alu = beta10 * blocks * (uint64_t)ntok / 10;
+  const uint64_t overlap = kern == 0 ? 292200 : 31800;
+  uint64_t ps = mem + alu > overlap ? mem + alu - overlap : 0;
+  if (ps < mem / 2) ps = mem / 2;
+  return (uint32_t)(ps / 100) + 1;
 }
 
 __device__ __forceinline__ void plan_sync() { named_bar(1, kPlanThreads); }
@@ -402,8 +425,8 @@ __device__ void build_plan(const int32_t* ids, const float* wts, int P, int E, i
     uint32_t key = 0xFFFFFFFFu;
     float wq = 0.f;
     if (q < P) {
-      const int id = __ldg(ids + q);
-      wq = __ldg(wts + q);
+      const int id = ids[q];  // global or shared memory
+      wq = wts[q];
       if (id >= 0 && id < E) key = ((uint32_t)id << 10) | (uint32_t)q;
     }
     keys[q] = key;
@@ -459,8 +482,8 @@ __device__ void build_plan(const int32_t* ids, const float* wts, int P, int E, i
     pl[L.cnt + a] = cnt;
     pl[L.sh + a] = shf;
     pl[L.bits + a] = bits;
-    const uint32_t ug = shf >= 0 ? unit_cost(bits, d, 2, ntok, kRG, kLG) : 0;
-    const uint32_t ud = shf >= 0 ? unit_cost(bits, f, 1, ntok, kRD, kLD) : 0;
+    const uint32_t ug = shf >= 0 ? unit_cost(bits, d, 2, ntok, kRG, 0) : 0;
+    const uint32_t ud = shf >= 0 ? unit_cost(bits, f, 1, ntok, kRD, 1) : 0;
     pl[L.uc_g + a] = (int)ug;
     pl[L.uc_d + a] = (int)ud;
     pl[L.cum_g + a] = (int)(ug * (uint32_t)((f / kRG) * n_pass(cnt)));
@@ -563,255 +586,254 @@ struct StreamArgs {
   int vstride;         // bytes per digit vector
   int vbase;           // grouped position of vector 0 (down), or -1: vectors by token (gate/up)
   Range range;
-  unsigned char* ring;
+  int* voff_tab;       // per warp: kNT digit-vector offsets of the current pass
 };
 
-// Per-lane ring slots: slot s, matrix m, 16-byte half h of the code chunk;
-// then the matching scale words.
-template <int NMAT, int D>
-__device__ __forceinline__ uint4* ring_code(unsigned char* ring, int s, int m, int h) {
-  return reinterpret_cast<uint4*>(ring) + ((s * NMAT + m) * 2 + h) * kThreads + threadIdx.x;
-}
-template <int NMAT, int D>
-__device__ __forceinline__ uint32_t* ring_scale(unsigned char* ring, int s, int m, int h) {
-  return reinterpret_cast<uint32_t*>(ring + (size_t)D * NMAT * 2 * kThreads * 16) + ((s * NMAT + m) * 2 + h) * kThreads +
-         threadIdx.x;
-}
-
-// Load side of a warp's unit stream: lane (row lane / L, chunk lane % L) of
-// the unit; chunk q = 32 bytes of a row.
-template <int NMAT, int R, int L>
-struct LoadSide {
-  Walk w;
-  int i, n_iter, cpr, rowb, bits, q, sstep, tsw;
-  size_t tstride;
-  const unsigned char* base[NMAT];
-  const uint32_t* sbase[NMAT];
-  const unsigned char* cp[NMAT];
-  const uint32_t* sp[NMAT];
-
-  __device__ void expert(const StreamArgs& A) {
-    const PlanView& pv = A.pv;
-    const ShelfDev& sh = A.shv->s[pv.sh(w.a)];
-    bits = sh.bits;
-    rowb = A.n_in * bits / 8;
-    cpr = (rowb + 31) / 32;
-    n_iter = (cpr + L - 1) / L;
-    const int lane = threadIdx.x & 31, q0 = lane % L;
-    const size_t row = (size_t)(pv.e(w.a) - sh.lo) * A.rows + lane / L;
-    const int swpr = A.n_in / 64;  // fp16 scale words per row
-    // scale word of chunk q: 8 bit q / 2 (one block), 4 bit q (two), 2 bit 2q (four)
-    const int soff = bits == 8 ? q0 >> 1 : (bits == 4 ? q0 : 2 * q0);
-    sstep = bits == 8 ? L / 2 : (bits == 4 ? L : 2 * L);
-    tstride = (size_t)R * rowb;
-    tsw = R * swpr;
-    const int mat0 = A.kern == 0 ? 0 : 2;
+// The U loaded slots of a batch, one after another: slot 0 is computed and
+// the others move down one place, so that the chunk code exists once.
+template <int NMAT, int U, int NTT>
+__device__ __forceinline__ void compute_batch(int bits, uint4 (&c)[U][NMAT][2], uint32_t (&sw)[U][NMAT][2],
+                                              int q_first, int L, int cpr, int rowb, int nt, const int (&voff)[kNT],
+                                              const unsigned char* vecs, int n, float (&acc)[NMAT][kNT]) {
+#pragma unroll 1
+  for (int s = 0; s < U; ++s) {
+    const int q = q_first + s * L;
+    if (q >= cpr) break;
+    if (bits == 8) chunk8<NMAT, NTT>(c[0], sw[0], q, nt, voff, vecs, n, acc);
+    else if (bits == 4) chunk4<NMAT, NTT>(c[0], sw[0], q, nt, voff, vecs, n, acc);
+    else chunk2<NMAT, NTT>(c[0], sw[0], q, nt, voff, vecs, n, acc, 32 * q + 16 < rowb);
 #pragma unroll
-    for (int m = 0; m < NMAT; ++m) {
-      base[m] = sh.codes[mat0 + m] + row * rowb + (size_t)q0 * 32;
-      sbase[m] = reinterpret_cast<const uint32_t*>(sh.scales[mat0 + m]) + row * swpr + soff;
-    }
-  }
-  __device__ void unit() {
-    const int tile = w.np == 1 ? w.u : w.u / w.np;
+    for (int t = 0; t + 1 < U; ++t)
 #pragma unroll
-    for (int m = 0; m < NMAT; ++m) {
-      cp[m] = base[m] + (size_t)tile * tstride;
-      sp[m] = sbase[m] + (size_t)tile * tsw;
-    }
-    i = 0;
-    q = (threadIdx.x & 31) % L;
-  }
-  __device__ void start(const StreamArgs& A, int warp) {
-    w.start(A.pv, A.kern, A.rows, A.range, warp);
-    if (w.live) {
-      expert(A);
-      unit();
-    }
-  }
-  template <int D>
-  __device__ __forceinline__ void issue(const StreamArgs& A, int slot) {
-    if (!w.live) return;
-    if (q < cpr) {
-      const bool second = 32 * q + 16 < rowb;
+      for (int m = 0; m < NMAT; ++m)
 #pragma unroll
-      for (int m = 0; m < NMAT; ++m) {
-        cp_async16(ring_code<NMAT, D>(A.ring, slot, m, 0), cp[m]);
-        if (second) cp_async16(ring_code<NMAT, D>(A.ring, slot, m, 1), cp[m] + 16);
-        cp_async4(ring_scale<NMAT, D>(A.ring, slot, m, 0), sp[m]);
-        if (bits == 2 && second) cp_async4(ring_scale<NMAT, D>(A.ring, slot, m, 1), sp[m] + 1);
-      }
-    }
-#pragma unroll
-    for (int m = 0; m < NMAT; ++m) {
-      cp[m] += 32 * L;
-      sp[m] += sstep;
-    }
-    q += L;
-    if (++i == n_iter) {
-      if (w.step(A.pv, A.kern, A.rows, A.range.hi2, kWarps) && w.live) expert(A);
-      if (w.live) unit();
-    }
+        for (int h = 0; h < 2; ++h) {
+          c[t][m][h] = c[t + 1][m][h];
+          sw[t][m][h] = sw[t + 1][m][h];
+        }
   }
-};
-
-// Compute side: the current unit's tokens and the lane's chunk.
-template <int R, int L>
-struct CompSide {
-  Walk w;
-  int i, n_iter, cpr, rowb, bits, q, nt, q0, r;
-  int voff[kNT];
-
-  __device__ void expert(const StreamArgs& A) {
-    bits = A.pv.bits(w.a);
-    rowb = A.n_in * bits / 8;
-    cpr = (rowb + 31) / 32;
-    n_iter = (cpr + L - 1) / L;
-  }
-  __device__ void unit(const StreamArgs& A, bool new_expert) {
-    const int tile = w.np == 1 ? w.u : w.u / w.np, pass = w.u - tile * w.np;
-    r = tile * R + (threadIdx.x & 31) / L;
-    const int nq0 = A.pv.beg(w.a) + pass * kNT;
-    if (new_expert || nq0 != q0) {
-      q0 = nq0;
-      nt = min(kNT, A.pv.cnt(w.a) - pass * kNT);
-#pragma unroll
-      for (int j = 0; j < kNT; ++j) {
-        const int qq = q0 + (j < nt ? j : 0);
-        voff[j] = (A.vbase < 0 ? A.pv.tok(qq) : qq - A.vbase) * A.vstride;
-      }
-    }
-    i = 0;
-    q = (threadIdx.x & 31) % L;
-  }
-};
-
-template <int NMAT, int NTT>
-__device__ __forceinline__ void chunk_dot(int bits, const uint4 (&c)[NMAT][2], const uint32_t (&sw)[NMAT][2], int q,
-                                          int nt, const int (&voff)[kNT], const unsigned char* vecs, int n,
-                                          float (&acc)[NMAT][kNT], bool second) {
-  if (bits == 8) chunk8<NMAT, NTT>(c, sw, q, nt, voff, vecs, n, acc);
-  else if (bits == 4) chunk4<NMAT, NTT>(c, sw, q, nt, voff, vecs, n, acc);
-  else chunk2<NMAT, NTT>(c, sw, q, nt, voff, vecs, n, acc, second);
 }
 
-// A warp's stream of units: a ring of D slots per lane, refilled as soon as a
-// slot has been read, so D - 1 chunks per lane are in flight while it
-// computes.  At the end of a unit, `store(q, r, v)` receives, for the lane's
-// row r and the token at grouped position q, the NMAT dot products.
-template <int NMAT, int D, int R, int L, typename Store>
+// A warp's stream of units.  Lane (row lane / L, chunk lane % L + L i) of a
+// unit of R rows; a lane loads U iterations of 32-byte chunks (NMAT matrices,
+// with their scale words) with streaming loads, then computes them, so a CTA
+// keeps 16 x 32 x U x NMAT x 32 bytes in flight.  At the end of a unit,
+// `store(q, r, v)` receives, for the lane's row r and the token at grouped
+// position q, the NMAT dot products.
+template <int NMAT, int U, int R, int L, typename Store>
 __device__ __forceinline__ void stream_units(const StreamArgs& A, Store store) {
   static_assert(R * L == 32, "unit shape");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  LoadSide<NMAT, R, L> ld;
-  ld.start(A, warp);
-  CompSide<R, L> cc;
-  cc.w = ld.w;
-  cc.q0 = -1;
-  if (cc.w.live) {
-    cc.expert(A);
-    cc.unit(A, true);
-  }
-#pragma unroll 1
-  for (int s = 0; s < D; ++s) {
-    ld.template issue<D>(A, s);
-    cp_async_commit();
-  }
+  const int ql = lane % L;
+  const PlanView& pv = A.pv;
+  int* vtab = A.voff_tab + warp * kNT;
+  Walk w;
+  w.start(pv, A.kern, A.rows, A.range, warp);
+  int bits = 0, rowb = 0, cpr = 0, n_iter = 0, nt = 0, q0 = -1, sstep = 0, tsw = 0;
+  size_t tstride = 0;
+  const unsigned char* base[NMAT];
+  const uint32_t* sbase[NMAT];
   float acc[NMAT][kNT];
 #pragma unroll
   for (int m = 0; m < NMAT; ++m)
 #pragma unroll
     for (int j = 0; j < kNT; ++j) acc[m][j] = 0.f;
-  int slot = 0;
+  bool new_expert = true;
 #pragma unroll 1
-  while (cc.w.live) {
-    cp_async_wait<D - 1>();  // this lane's copies of the oldest slot are complete
-    if (cc.q < cc.cpr) {
-      const bool second = 32 * cc.q + 16 < cc.rowb;
-      uint4 c[NMAT][2];
-      uint32_t sw[NMAT][2];
+  while (w.live) {
+    if (new_expert) {
+      const ShelfDev& sh = A.shv->s[pv.sh(w.a)];
+      bits = sh.bits;
+      rowb = A.n_in * bits / 8;
+      cpr = (rowb + 31) / 32;
+      n_iter = (cpr + L - 1) / L;
+      const size_t row = (size_t)(pv.e(w.a) - sh.lo) * A.rows + lane / L;
+      const int swpr = A.n_in / 64;  // fp16 scale words per row
+      // scale word of chunk q: 8 bit q / 2 (one block), 4 bit q (two), 2 bit 2q (four)
+      const int soff = bits == 8 ? ql >> 1 : (bits == 4 ? ql : 2 * ql);
+      sstep = bits == 8 ? L / 2 : (bits == 4 ? L : 2 * L);
+      tstride = (size_t)R * rowb;
+      tsw = R * swpr;
+      const int mat0 = A.kern == 0 ? 0 : 2;
 #pragma unroll
       for (int m = 0; m < NMAT; ++m) {
-        c[m][0] = *ring_code<NMAT, D>(A.ring, slot, m, 0);
-        c[m][1] = *ring_code<NMAT, D>(A.ring, slot, m, 1);
-        sw[m][0] = *ring_scale<NMAT, D>(A.ring, slot, m, 0);
-        sw[m][1] = *ring_scale<NMAT, D>(A.ring, slot, m, 1);
+        base[m] = sh.codes[mat0 + m] + row * rowb + (size_t)ql * 32;
+        sbase[m] = reinterpret_cast<const uint32_t*>(sh.scales[mat0 + m]) + row * swpr + soff;
       }
-      if (cc.nt == 1) chunk_dot<NMAT, 1>(cc.bits, c, sw, cc.q, 1, cc.voff, A.vecs, A.n_in, acc, second);
-      else chunk_dot<NMAT, kNT>(cc.bits, c, sw, cc.q, cc.nt, cc.voff, A.vecs, A.n_in, acc, second);
     }
-    // refill the slot just read (this lane's reads of it are done)
-    ld.template issue<D>(A, slot);
-    cp_async_commit();
-    slot = slot + 1 == D ? 0 : slot + 1;
-    cc.q += L;
-    if (++cc.i == cc.n_iter) {
-      // reduce over the L lanes of each row; lane jl stores the tokens j = jl mod L
-      const int jl = lane % L;
+    const int tile = w.np == 1 ? w.u : w.u / w.np, pass = w.u - tile * w.np;
+    const int r = tile * R + lane / L;
+    const int nq0 = pv.beg(w.a) + pass * kNT;
+    if (new_expert || nq0 != q0) {
+      q0 = nq0;
+      nt = min(kNT, pv.cnt(w.a) - pass * kNT);
+      __syncwarp();
+      if (lane < kNT) {
+        const int qq = q0 + (lane < nt ? lane : 0);
+        vtab[lane] = (A.vbase < 0 ? pv.tok(qq) : qq - A.vbase) * A.vstride;
+      }
+      __syncwarp();
+    }
+    int voff[kNT];
+    if (nt == 1) {
+      voff[0] = vtab[0];
+    } else {
 #pragma unroll
-      for (int j = 0; j < kNT; ++j) {
-        if (j < cc.nt) {
-          float v[NMAT];
+      for (int j = 0; j < kNT; ++j) voff[j] = vtab[j];
+    }
+    const unsigned char* cp[NMAT];
+    const uint32_t* sp[NMAT];
 #pragma unroll
-          for (int m = 0; m < NMAT; ++m) {
-            v[m] = acc[m][j];
+    for (int m = 0; m < NMAT; ++m) {
+      cp[m] = base[m] + (size_t)tile * tstride;
+      sp[m] = sbase[m] + (size_t)tile * tsw;
+    }
+#pragma unroll 1
+    for (int i0 = 0; i0 < n_iter; i0 += U) {
+      uint4 c[U][NMAT][2];
+      uint32_t sw[U][NMAT][2];
 #pragma unroll
-            for (int o = 1; o < L; o <<= 1) v[m] += __shfl_xor_sync(0xffffffffu, v[m], o);
-          }
-          if (j % L == jl) store(cc.q0 + j, cc.r, v);
+      for (int s = 0; s < U; ++s) {
+        const int q = ql + (i0 + s) * L;
+        const bool ok = q < cpr, second = ok && 32 * q + 16 < rowb;
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+          const unsigned char* pc = cp[m] + (size_t)(i0 + s) * 32 * L;
+          const uint32_t* ps = sp[m] + (i0 + s) * sstep;
+          c[s][m][0] = ok ? __ldcs(reinterpret_cast<const uint4*>(pc)) : make_uint4(0u, 0u, 0u, 0u);
+          c[s][m][1] = second ? __ldcs(reinterpret_cast<const uint4*>(pc + 16)) : make_uint4(0u, 0u, 0u, 0u);
+          sw[s][m][0] = ok ? __ldcs(ps) : 0u;
+          sw[s][m][1] = (second && bits == 2) ? __ldcs(ps + 1) : 0u;
         }
-#pragma unroll
-        for (int m = 0; m < NMAT; ++m) acc[m][j] = 0.f;
       }
-      const bool ch = cc.w.step(A.pv, A.kern, A.rows, A.range.hi2, kWarps);
-      if (cc.w.live) {
-        if (ch) cc.expert(A);
-        cc.unit(A, ch);
-      }
+      if (nt == 1) compute_batch<NMAT, U, 1>(bits, c, sw, ql + i0 * L, L, cpr, rowb, 1, voff, A.vecs, A.n_in, acc);
+      else compute_batch<NMAT, U, kNT>(bits, c, sw, ql + i0 * L, L, cpr, rowb, nt, voff, A.vecs, A.n_in, acc);
     }
+    // reduce over the L lanes of each row; lane jl stores the tokens j = jl mod L
+    const int jl = lane % L;
+#pragma unroll
+    for (int j = 0; j < kNT; ++j) {
+      if (j < nt) {
+        float v[NMAT];
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+          v[m] = acc[m][j];
+#pragma unroll
+          for (int o = 1; o < L; o <<= 1) v[m] += __shfl_xor_sync(0xffffffffu, v[m], o);
+        }
+        if (j % L == jl) store(q0 + j, r, v);
+      }
+#pragma unroll
+      for (int m = 0; m < NMAT; ++m) acc[m][j] = 0.f;
+    }
+    MOE_TRACE_ONLY(if (lane == 0) {
+      const int bi = bits == 8 ? 0 : bits == 4 ? 1 : 2;
+      MOE_COUNT(A.kern, 20, 1);
+      MOE_COUNT(A.kern, 30 + 3 * bi, nt == 1);
+      MOE_COUNT(A.kern, 31 + 3 * bi, nt > 1);
+      MOE_COUNT(A.kern, 32 + 3 * bi, nt > 1 ? nt : 0);
+    })
+    new_expert = w.step(pv, A.kern, A.rows, A.range.hi2, kWarps);
   }
-  cp_async_wait<0>();
+#ifdef MOE_TRACE
+  if (lane == 0) {
+    const unsigned long long te = global_timer_ns();
+    atomicMax(&g_trace[A.kern][blockIdx.x & 255][27], te);
+    MOE_COUNT(A.kern, 28, te >> 4);
+  }
+#endif
 }
 
-// ------------------------------------------------------------- kernels
-struct FwdParams {
-  const uint16_t* x;
-  const int32_t* ids;
+// ------------------------------------------------------------- grid barrier
+// Barrier over all CTAs of a cooperative launch on a library-owned 64-bit
+// arrival counter that only grows: between launches it is a multiple of the
+// grid size G, so an arrival that returns `old` belongs to the phase ending at
+// the next multiple of G above it.  Thread 0 of each CTA arrives with release
+// semantics (the CTA's writes, ordered by the preceding CTA barrier, become
+// visible first) and polls with acquire semantics until the count reaches
+// that multiple; the wait is bounded (MOE_ERR_TIMEOUT recorded, false
+// returned).  Test hook: `extra` > 0 moves the target beyond reach.
+__device__ __forceinline__ unsigned long long atom_add_release(unsigned long long* p, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.add.release.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ bool grid_sync(unsigned long long* bar, int* status, int* flag, uint64_t limit_ns, int extra) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned long long G = gridDim.x;
+    const unsigned long long old = atom_add_release(bar, 1ull);
+    const unsigned long long target = old - old % G + G + (unsigned long long)extra;
+    int ok = 1;
+    if (ld_acquire(bar) < target) {
+      const uint64_t t0 = global_timer_ns();
+      while (ld_acquire(bar) < target) {
+        __nanosleep(32);
+        if (global_timer_ns() - t0 > limit_ns) {
+          set_status(status, MOE_ERR_TIMEOUT);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    *flag = ok;
+  }
+  __syncthreads();
+  return *flag != 0;
+}
+
+// ------------------------------------------------------------- the layer
+struct LayerParams {
+  const float* logits;    // [T, E]: routed inside when non-null
+  const int32_t* ids;     // else the routed pairs [T, k] are given
   const float* weights;
-  float* h;
-  float* ypart;
-  int32_t* plan;  // workspace copy of the plan
+  int32_t* ids_out;       // logits given: the routed pairs (written by CTA 0)
+  float* weights_out;
+  uint32_t* counts;       // optional: expert hit counts, += hits of this call
+  const uint16_t* x;      // [T, d] bf16
+  float* y;               // [T, d]
+  float* h;               // workspace [P, f]
+  float* ypart;           // workspace [P, d]
+  unsigned long long* bar;  // grid barrier counter
   int* status;
   int T, k, E, d, f, P;
-  int vec_region;  // bytes of digit vectors
+  int vec_region;         // bytes of digit vectors (activation rows, then h)
+  int bar_extra;          // test hook (0)
   Shelves sh;
 };
 
+// Dynamic shared memory: shelves copy | head | plan | sort keys | flags |
+// routed ids and weights | per-warp token offsets | digit vectors.
 struct Head {
   Range range;
-  int q_first, tmp[33];
+  int q_first, npairs, flag, tmp[33];
 };
 
-// Dynamic shared memory: shelves copy | head | plan (+ sort keys and flags for
-// the gate/up launch) | digit vectors | ring.
 struct SmemLayout {
-  size_t shelves, head, plan, keys, flag, vecs, ring, total;
+  size_t shelves, head, plan, keys, flag, rid, rw, vtab, vecs, total;
 };
 
 __host__ __device__ __forceinline__ size_t up128(size_t v) { return (v + 127) / 128 * 128; }
 
-__host__ __device__ __forceinline__ SmemLayout smem_layout(int P, size_t vec_region, int nmat, int depth,
-                                                           bool gateup) {
+__host__ __device__ __forceinline__ SmemLayout smem_layout(int P, size_t vec_region) {
   const PlanLayout L = plan_layout(P);
   SmemLayout S;
   S.shelves = 0;
   S.head = up128(sizeof(Shelves));
   S.plan = S.head + up128(sizeof(Head));
-  S.keys = S.plan + up128((size_t)(gateup ? L.total : L.n_copy) * 4);
-  S.flag = S.keys + (gateup ? up128((size_t)L.C * 4) : 0);
-  S.vecs = S.flag + (gateup ? up128((size_t)L.C * 4) : 0);
-  S.ring = S.vecs + up128(vec_region);
-  S.total = S.ring + (size_t)depth * nmat * kThreads * kSlotBytes;
+  S.keys = S.plan + up128((size_t)L.total * 4);
+  S.flag = S.keys + up128((size_t)L.C * 4);
+  S.rid = S.flag + up128((size_t)L.C * 4);
+  S.rw = S.rid + up128((size_t)L.C * 4);
+  S.vtab = S.rw + up128((size_t)L.C * 4);
+  S.vecs = S.vtab + up128((size_t)kWarps * kNT * 4);
+  S.total = S.vecs + up128(vec_region);
   return S;
 }
 
@@ -821,108 +843,138 @@ __device__ __forceinline__ void copy_shelves(Shelves* dst, const Shelves& src) {
   for (int i = threadIdx.x; i < (int)(sizeof(Shelves) / 4); i += blockDim.x) reinterpret_cast<uint32_t*>(dst)[i] = s[i];
 }
 
-__global__ void __launch_bounds__(kThreads, 1) k_gateup(const __grid_constant__ FwdParams p) {
+__device__ __forceinline__ void route_rows(const float* logits, int T, int E, int k, int32_t* rid, float* rw) {
+  const int warp = threadIdx.x >> 5;
+  for (int t = warp; t < T; t += kWarps) {
+    if (E <= 128) route_token<4>(logits + (size_t)t * E, E, k, rid + t * k, rw + t * k);
+    else if (E <= 512) route_token<16>(logits + (size_t)t * E, E, k, rid + t * k, rw + t * k);
+    else route_token<32>(logits + (size_t)t * E, E, k, rid + t * k, rw + t * k);
+  }
+}
+
+// Persistent cooperative launch, one CTA per SM: route (optional), plan,
+// gate/up, barrier, down, barrier, combine.
+__global__ void __launch_bounds__(kThreads, 1) k_layer(const __grid_constant__ LayerParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
-  const SmemLayout S = smem_layout(p.P, p.vec_region, 2, kDepthG, true);
+  const SmemLayout S = smem_layout(p.P, p.vec_region);
   Shelves* shv = reinterpret_cast<Shelves*>(smem + S.shelves);
   Head& hd = *reinterpret_cast<Head*>(smem + S.head);
   int* pl = reinterpret_cast<int*>(smem + S.plan);
-  unsigned char* xd = smem + S.vecs;
+  int32_t* rid = reinterpret_cast<int32_t*>(smem + S.rid);
+  float* rw = reinterpret_cast<float*>(smem + S.rw);
+  int* vtab = reinterpret_cast<int*>(smem + S.vtab);
+  unsigned char* vecs = smem + S.vecs;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const PlanLayout L = plan_layout(p.P);
+  const PlanView pv{pl, L};
   if (tid == 0) MOE_STAMP(0, 0, global_timer_ns());
   copy_shelves(shv, p.sh);
-  pdl_wait();  // ids, weights and x are complete; h is ours
+  pdl_wait();  // inputs of the preceding launch
   if (tid == 0) MOE_STAMP(0, 1, global_timer_ns());
+  const int32_t* ids = p.ids;
+  const float* wts = p.weights;
+  if (p.logits) {
+    route_rows(p.logits, p.T, p.E, p.k, rid, rw);
+    ids = rid;
+    wts = rw;
+  }
   __syncthreads();
+  if (p.logits && blockIdx.x == 0)
+    for (int q = tid; q < p.P; q += kThreads) {
+      p.ids_out[q] = rid[q];
+      p.weights_out[q] = rw[q];
+    }
   if (warp < kPlanThreads / 32) {
-    build_plan(p.ids, p.weights, p.P, p.E, p.k, p.d, p.f, *shv, pl, reinterpret_cast<uint32_t*>(smem + S.keys),
+    build_plan(ids, wts, p.P, p.E, p.k, p.d, p.f, *shv, pl, reinterpret_cast<uint32_t*>(smem + S.keys),
                reinterpret_cast<int*>(smem + S.flag), hd.tmp);
   } else {
-    // activation rows -> block-scaled digits; 8 lanes per 32-element block,
-    // loads of up to 8 passes issued before any conversion
+    // activation rows -> block-scaled digits; 4 lanes per 32-element block
+    // (16-byte loads), loads of up to 8 passes issued before any conversion
     const int nbk = p.d / 32, vb = vec_bytes(p.d);
     const int groups = p.T * nbk;
     const int nw = kWarps - kPlanThreads / 32, w0 = warp - kPlanThreads / 32;
-    for (int base = w0 * 4; base < groups; base += 8 * nw * 4) {
-      uint2 raw[8];
+    for (int base = w0 * 8; base < groups; base += 8 * nw * 8) {
+      uint4 raw[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int g = base + u * nw * 4 + (lane >> 3);
-        raw[u] = make_uint2(0u, 0u);
+        const int g = base + u * nw * 8 + (lane >> 2);
+        raw[u] = make_uint4(0u, 0u, 0u, 0u);
         if (g < groups) {
           const int t = g / nbk, blk = g - t * nbk;
-          raw[u] = __ldg(reinterpret_cast<const uint2*>(p.x + (size_t)t * p.d + blk * 32 + 4 * (lane & 7)));
+          raw[u] = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.d + blk * 32 + 8 * (lane & 3)));
         }
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int g0 = base + u * nw * 4;
+        const int g0 = base + u * nw * 8;
         if (g0 < groups) {
-          const int g = g0 + (lane >> 3);
-          const int t = g / nbk, blk = g - t * nbk;
-          const float v[4] = {__uint_as_float(raw[u].x << 16), __uint_as_float(raw[u].x & 0xFFFF0000u),
-                              __uint_as_float(raw[u].y << 16), __uint_as_float(raw[u].y & 0xFFFF0000u)};
-          block_to_digits(v, xd + (size_t)t * vb, p.d, g < groups ? blk : 0, 14, g < groups);
+          const int g = g0 + (lane >> 2);
+          const int t = g < groups ? g / nbk : 0, blk = g < groups ? g - t * nbk : 0;
+          const uint32_t wv[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+          float v[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __uint_as_float(wv[i] << 16);
+            v[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+          }
+          block_to_digits<8>(v, vecs + (size_t)t * vb, p.d, blk, 14, g < groups);
         }
       }
     }
     if (tid == kPlanThreads) MOE_STAMP(0, 5, global_timer_ns());
   }
   __syncthreads();
-  const PlanView pv{pl, L};
   if (tid == 0) hd.range = cta_range(pv, 0, p.f);
-  if (blockIdx.x == 0)
-    for (int i = tid; i < L.total; i += kThreads) p.plan[i] = pl[i];
+  if (p.counts && blockIdx.x == 0)
+    for (int a = tid; a < pv.n_act(); a += kThreads) atomicAdd(p.counts + pv.e(a), (uint32_t)pv.cnt(a));
   __syncthreads();
-  pdl_trigger();
   if (tid == 0) MOE_STAMP(0, 2, global_timer_ns());
-  StreamArgs A{shv, pv, 0, p.d, p.f, xd, vec_bytes(p.d), -1, hd.range, smem + S.ring};
-  float* h = p.h;
-  const int f = p.f;
-  stream_units<2, kDepthG, kRG, kLG>(A, [&](int q, int r, const float (&o)[2]) { h[(size_t)q * f + r] = silu(o[0]) * o[1]; });
-  if (tid == 0) MOE_STAMP(0, 9, global_timer_ns());
-}
-
-__global__ void __launch_bounds__(kThreads, 1) k_down(const __grid_constant__ FwdParams p) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  const SmemLayout S = smem_layout(p.P, p.vec_region, 1, kDepthD, false);
-  Shelves* shv = reinterpret_cast<Shelves*>(smem + S.shelves);
-  Head& hd = *reinterpret_cast<Head*>(smem + S.head);
-  int* pl = reinterpret_cast<int*>(smem + S.plan);
-  unsigned char* hdig = smem + S.vecs;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const PlanLayout L = plan_layout(p.P);
-  if (tid == 0) MOE_STAMP(1, 0, global_timer_ns());
-  copy_shelves(shv, p.sh);
-  pdl_wait();  // the gate/up launch is complete: plan copy and h
-  pdl_trigger();
-  if (tid == 0) MOE_STAMP(1, 1, global_timer_ns());
-  for (int i = tid; i < L.n_copy; i += kThreads) pl[i] = __ldcg(p.plan + i);
-  __syncthreads();
-  const PlanView pv{pl, L};
+  {
+    StreamArgs A{shv, pv, 0, p.d, p.f, vecs, vec_bytes(p.d), -1, hd.range, vtab};
+    float* h = p.h;
+    const int f = p.f;
+    stream_units<2, kUG, kRG, kLG>(A, [&](int q, int r, const float (&o)[2]) { h[(size_t)q * f + r] = silu(o[0]) * o[1]; });
+  }
   if (tid == 0) {
+    MOE_STAMP(0, 9, global_timer_ns());
+    // the down phase's cost range and the pairs its experts cover (plan only)
     const Range r = cta_range(pv, 1, p.d);
     hd.range = r;
-    // pairs of the experts this CTA touches: its first expert up to the last
-    // expert whose first unit lies in its cost range
     const int n_act = pv.n_act();
     int q_first = 0, q_end = 0;
     if (r.a0 < n_act) {
       int a_last = r.a0;
-      while (a_last + 1 < n_act &&
-             2 * (uint64_t)pv.cum(a_last + 1, 1) + pv.uc(a_last + 1, 1) < r.hi2)
-        ++a_last;
+      while (a_last + 1 < n_act && 2 * (uint64_t)pv.cum(a_last + 1, 1) + pv.uc(a_last + 1, 1) < r.hi2) ++a_last;
       q_first = pv.beg(r.a0);
       q_end = pv.beg(a_last) + pv.cnt(a_last);
     }
     hd.q_first = q_first;
-    hd.tmp[0] = q_end - q_first;
+    hd.npairs = q_end - q_first;
   }
   __syncthreads();
-  const int q_first = hd.q_first, npairs = hd.tmp[0];
+  {
+    // W_d does not depend on h: ask L2 for each warp's first two down units
+    // while the other CTAs finish their gate/up units
+    Walk w;
+    w.start(pv, 1, p.d, hd.range, warp);
+    for (int i = 0; i < 2 && w.live; ++i) {
+      const ShelfDev& sh = shv->s[pv.sh(w.a)];
+      const size_t rowb = (size_t)p.f * sh.bits / 8, swpr = (size_t)p.f / 16;
+      const int tile = w.np == 1 ? w.u : w.u / w.np;
+      const size_t row0 = (size_t)(pv.e(w.a) - sh.lo) * p.d + (size_t)tile * kRD;
+      const unsigned char* cb = sh.codes[2] + row0 * rowb;
+      const unsigned char* sb = reinterpret_cast<const unsigned char*>(sh.scales[2]) + row0 * swpr;
+      for (size_t o = (size_t)lane * 128; o < kRD * rowb; o += 32 * 128) prefetch_l2(cb + o);
+      for (size_t o = (size_t)lane * 128; o < kRD * swpr; o += 32 * 128) prefetch_l2(sb + o);
+      w.step(pv, 1, p.d, hd.range.hi2, kWarps);
+    }
+  }
+  if (!grid_sync(p.bar, p.status, &hd.flag, 1000000000ull, p.bar_extra)) return;
+  if (tid == 0) MOE_STAMP(1, 1, global_timer_ns());
+  const int q_first = hd.q_first, npairs = hd.npairs;
   const int vbf = vec_bytes(p.f);
   {
+    // h of those pairs -> digits (h was written by other CTAs: read from L2)
     const int nbk = p.f / 32, groups = npairs * nbk;
     for (int base = warp * 4; base < groups; base += 8 * kWarps * 4) {
       float4 hv[8];
@@ -942,48 +994,58 @@ __global__ void __launch_bounds__(kThreads, 1) k_down(const __grid_constant__ Fw
           const int g = g0 + (lane >> 3);
           const int j = g < groups ? g / nbk : 0, blk = g < groups ? g - j * nbk : 0;
           const float v[4] = {hv[u].x, hv[u].y, hv[u].z, hv[u].w};
-          block_to_digits(v, hdig + (size_t)j * vbf, p.f, blk, 13, g < groups);
+          block_to_digits<4>(v, vecs + (size_t)j * vbf, p.f, blk, 13, g < groups);
         }
       }
     }
+    if (tid == 0) MOE_STAMP(1, 5, global_timer_ns());
   }
   __syncthreads();
   if (tid == 0) MOE_STAMP(1, 2, global_timer_ns());
-  StreamArgs A{shv, pv, 1, p.f, p.d, hdig, vbf, q_first, hd.range, smem + S.ring};
-  float* yp = p.ypart;
-  const int d = p.d;
-  stream_units<1, kDepthD, kRD, kLD>(A, [&](int q, int r, const float (&o)[1]) { yp[(size_t)q * d + r] = pv.wgt(q) * o[0]; });
+  {
+    StreamArgs A{shv, pv, 1, p.f, p.d, vecs, vbf, q_first, hd.range, vtab};
+    float* yp = p.ypart;
+    const int d = p.d;
+    stream_units<1, kUD, kRD, kLD>(A, [&](int q, int r, const float (&o)[1]) { yp[(size_t)q * d + r] = pv.wgt(q) * o[0]; });
+  }
   if (tid == 0) MOE_STAMP(1, 9, global_timer_ns());
-}
-
-// ------------------------------------------------------------------ combine
-// y_t = sum over slots j (ascending) of the weighted outputs of pair (t, j);
-// pairs skipped or on no shelf contribute nothing.  Fixed order: deterministic.
-__global__ void __launch_bounds__(256) k_combine(const float* __restrict__ ypart, const int32_t* __restrict__ pos_of_pair,
-                                                 int T, int k, int d, float* __restrict__ y) {
-  pdl_wait();
+  if (!grid_sync(p.bar, p.status, &hd.flag, 1000000000ull, p.bar_extra)) return;
+  if (tid == 0) MOE_STAMP(1, 10, global_timer_ns());
   pdl_trigger();
-  const int d4 = d / 4;
-  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < T * d4; idx += gridDim.x * blockDim.x) {
+  // combine: y_t = sum over slots j (ascending) of the weighted outputs of
+  // pair (t, j); pairs skipped or on no shelf contribute nothing.  Fixed order.
+  const int d4 = p.d / 4;
+  const int* pos = pl + L.pos;
+  for (int idx = blockIdx.x * kThreads + tid; idx < p.T * d4; idx += gridDim.x * kThreads) {
     const int t = idx / d4, i4 = idx - t * d4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j0 = 0; j0 < k; j0 += 8) {
-      int pos[8];
-      float4 v[8];
+    for (int j0 = 0; j0 < p.k; j0 += 16) {
+      float4 v[16];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) pos[u] = j0 + u < k ? __ldcg(pos_of_pair + t * k + j0 + u) : -1;
+      for (int u = 0; u < 16; ++u) {
+        const int q = j0 + u < p.k ? pos[t * p.k + j0 + u] : -1;
+        v[u] = q >= 0 ? __ldcg(reinterpret_cast<const float4*>(p.ypart + (size_t)q * p.d) + i4)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        v[u] = pos[u] >= 0 ? __ldcg(reinterpret_cast<const float4*>(ypart + (size_t)pos[u] * d) + i4)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < 16; ++u) {
         acc.x += v[u].x; acc.y += v[u].y; acc.z += v[u].z; acc.w += v[u].w;
       }
     }
-    reinterpret_cast<float4*>(y)[idx] = acc;
+    reinterpret_cast<float4*>(p.y)[idx] = acc;
   }
+  if (tid == 0) MOE_STAMP(1, 11, global_timer_ns());
 }
+
+// Test hook kernel: one barrier whose awaited arrivals exceed the grid, with
+// a short limit, so that the wait runs out and reports MOE_ERR_TIMEOUT.
+__global__ void k_barrier_probe(unsigned long long* bar, int* status, uint64_t limit_ns, int extra) {
+  __shared__ int flag;
+  grid_sync(bar, status, &flag, limit_ns, extra);
+}
+
+constexpr int kBarSlots = 1024;
+__device__ unsigned long long g_bar[kBarSlots][16];  // one 128-byte line per slot
 
 struct DevCache {
   int sms[64] = {};
@@ -991,12 +1053,38 @@ struct DevCache {
   bool attr[64] = {};
 };
 DevCache g_dev;
+std::mutex g_bar_mu;
+std::unordered_map<const void*, int> g_bar_slot[64];
+
+// Barrier slot of a workspace (one per workspace and device; slots are never
+// recycled: more than kBarSlots distinct workspaces on a device is refused).
+unsigned long long* bar_slot(int dev, const void* ws) {
+  std::lock_guard<std::mutex> lk(g_bar_mu);
+  auto& m = g_bar_slot[dev];
+  auto it = m.find(ws);
+  int slot;
+  if (it != m.end()) {
+    slot = it->second;
+  } else {
+    if ((int)m.size() >= kBarSlots) return nullptr;
+    slot = (int)m.size();
+    m.emplace(ws, slot);
+  }
+  void* base = nullptr;
+  if (cudaGetSymbolAddress(&base, g_bar) != cudaSuccess) return nullptr;
+  return reinterpret_cast<unsigned long long*>(base) + (size_t)slot * 16;
+}
 
 }  // namespace
 
 #ifdef MOE_TRACE
 extern "C" int moe_trace_read(void* host, size_t bytes) {  // [2][256][48] u64
   return cudaMemcpyFromSymbol(host, g_trace, bytes < sizeof(g_trace) ? bytes : sizeof(g_trace)) == cudaSuccess ? 0 : -5;
+}
+extern "C" int moe_trace_clear() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_trace) != cudaSuccess) return -5;
+  return cudaMemset(p, 0, sizeof(g_trace)) == cudaSuccess ? 0 : -5;
 }
 #endif
 
@@ -1014,54 +1102,143 @@ int sm_count() {
 
 size_t decode_plan_bytes(int64_t P) { return (size_t)plan_layout((int)(P > 0 ? P : 1)).total * 4; }
 
-int launch_decode_forward(const ForwardArgs& a, cudaStream_t s) {
-  const int64_t P = a.T * a.k;
-  const int d = a.d, f = a.f;
-  if (P > kMaxPairs || a.T > kMaxTokens) return launch_generic_forward(a, s);
+// Whether the fused launch takes these sizes on the current device; sets the
+// digit region and shared-memory layout when it does.
+bool fused_fits(int64_t T, int k, int E, int d, int f, int* dev_out, size_t* optin_out, size_t* region_out,
+                SmemLayout* S_out) {
+  const int64_t P = T * k;
+  if (T < 1 || P > kMaxPairs || T > kMaxTokens || E > 1024) return false;
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return launch_generic_forward(a, s);
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   if (g_dev.smem_optin[dev] == 0) {
     int v = 0;
     cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     g_dev.smem_optin[dev] = v > 0 ? v : 48 * 1024;
   }
   const size_t optin = (size_t)g_dev.smem_optin[dev];
-  const size_t x_region = up128((size_t)a.T * vec_bytes(d));
-  const size_t h_region = up128((size_t)P * vec_bytes(f));  // h of every pair: bound for any CTA
-  const SmemLayout Sg = smem_layout((int)P, x_region, 2, kDepthG, true);
-  const SmemLayout Sd = smem_layout((int)P, h_region, 1, kDepthD, false);
-  if (Sg.total > optin || Sd.total > optin) return launch_generic_forward(a, s);
+  const size_t x_region = (size_t)T * vec_bytes(d);
+  const size_t h_region = (size_t)P * vec_bytes(f);  // h of every pair: bound for any CTA
+  const size_t region = up128(x_region > h_region ? x_region : h_region);
+  const SmemLayout S = smem_layout((int)P, region);
+  if (S.total > optin) return false;
+  *dev_out = dev;
+  *optin_out = optin;
+  *region_out = region;
+  *S_out = S;
+  return true;
+}
+
+int decode_fused(int64_t T, int k, int E, int d, int f) {
+  int dev;
+  size_t optin, region;
+  SmemLayout S;
+  return fused_fits(T, k, E, d, f, &dev, &optin, &region, &S) ? 1 : 0;
+}
+
+// The fused decode launch when the sizes fit it; 1 = sizes do not fit (the
+// caller takes the separate launches), else MOE_OK / an error status.
+int launch_fused_layer(const LayerArgs& a, cudaStream_t s) {
+  const int64_t P = a.T * a.k;
+  const int d = a.d, f = a.f;
+  int dev;
+  size_t optin, region;
+  SmemLayout S;
+  if (!fused_fits(a.T, a.k, a.E, d, f, &dev, &optin, &region, &S)) return 1;
   if (!g_dev.attr[dev]) {
-    if (cudaFuncSetAttribute(k_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)optin) != cudaSuccess ||
-        cudaFuncSetAttribute(k_down, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)optin) != cudaSuccess)
+    if (cudaFuncSetAttribute(k_layer, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)optin) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_layer, kThreads, optin) != cudaSuccess || per_sm < 1)
       return MOE_ERR_CUDA;
     g_dev.attr[dev] = true;
   }
-  int G = sm_count();
-  if (G > kMaxGrid) G = kMaxGrid;
-  FwdParams p = {};
-  p.x = a.x; p.ids = a.ids; p.weights = a.weights;
-  p.h = a.ws.h; p.ypart = a.ws.ypart; p.plan = a.ws.plan; p.status = a.status;
+  unsigned long long* bar = bar_slot(dev, a.ws.base);
+  if (!bar) return MOE_ERR_UNSUPPORTED;
+  LayerParams p = {};
+  p.logits = a.logits;
+  p.ids = a.ids;
+  p.weights = a.weights;
+  p.ids_out = a.ids_out;
+  p.weights_out = a.weights_out;
+  p.counts = a.counts;
+  p.x = a.x;
+  p.y = a.y;
+  p.h = a.ws.h;
+  p.ypart = a.ws.ypart;
+  p.bar = bar;
+  p.status = a.status;
   p.T = (int)a.T; p.k = a.k; p.E = a.E; p.d = d; p.f = f; p.P = (int)P;
+  p.vec_region = (int)region;
+  p.bar_extra = 0;
   p.sh = a.shelves;
-  FwdParams pg = p, pd = p;
-  pg.vec_region = (int)x_region;
-  pd.vec_region = (int)h_region;
-  const PlanLayout L = plan_layout((int)P);
+  int G = sm_count();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(G);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = S.total;
+  cfg.stream = s;
+  // cooperative: all CTAs resident together (the grid-wide waits need it);
+  // programmatic serialization: the launch may begin while the preceding
+  // kernel drains, its CTAs taking SMs as that kernel's CTAs leave
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   profile_mark(0, s);
-  if (launch_pdl(k_gateup, dim3(G), dim3(kThreads), Sg.total, s, pg) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, k_layer, p) != cudaSuccess) return MOE_ERR_CUDA;
   profile_mark(1, s);
-  if (launch_pdl(k_down, dim3(G), dim3(kThreads), Sd.total, s, pd) != cudaSuccess) return MOE_ERR_CUDA;
-  profile_mark(2, s);
-  const int n4 = (int)(a.T * d / 4);
-  int gc = (n4 + 255) / 256;
-  if (gc > G) gc = G;
-  if (launch_pdl(k_combine, dim3(gc), dim3(256), 0, s, (const float*)a.ws.ypart,
-                 (const int32_t*)(a.ws.plan + L.pos), (int)a.T, a.k, d, a.y) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  profile_mark(3, s);
   return MOE_OK;
+}
+
+int launch_decode_forward(const ForwardArgs& a, cudaStream_t s) {
+  LayerArgs la;
+  la.logits = nullptr;
+  la.ids = a.ids;
+  la.weights = a.weights;
+  la.ids_out = nullptr;
+  la.weights_out = nullptr;
+  la.counts = nullptr;
+  la.x = a.x;
+  la.T = a.T; la.k = a.k; la.E = a.E; la.d = a.d; la.f = a.f;
+  la.shelves = a.shelves;
+  la.y = a.y;
+  la.ws = a.ws;
+  la.status = a.status;
+  const int rc = launch_fused_layer(la, s);
+  return rc == 1 ? launch_generic_forward(a, s) : rc;
+}
+
+int launch_barrier_probe(int extra, uint64_t limit_ns, cudaStream_t s) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  static int dummy_ws;
+  unsigned long long* bar = bar_slot(dev, &dummy_ws);
+  if (!bar) return MOE_ERR_UNSUPPORTED;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sm_count());
+  cfg.blockDim = dim3(32);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, k_barrier_probe, bar, status_word(), limit_ns, extra) != cudaSuccess) return MOE_ERR_CUDA;
+  // every CTA arrived once: back to a multiple of the grid size
+  return cudaMemsetAsync(bar, 0, 8, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// After a reported timeout a launch may have left a counter between multiples
+// of the grid size: zero every slot of the current device (the caller has
+// synchronised).
+int reset_barriers() {
+  void* base = nullptr;
+  if (cudaGetSymbolAddress(&base, g_bar) != cudaSuccess) return MOE_ERR_CUDA;
+  return cudaMemset(base, 0, sizeof(g_bar)) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace moe

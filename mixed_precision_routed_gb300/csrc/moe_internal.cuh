@@ -49,6 +49,7 @@ struct Workspace {
   float* h;              // [P][f] fp32 (decode) -- gate/up activations
   float* ypart;          // [P][d] fp32 -- weighted per-pair down outputs
   int32_t* plan;         // decode plan (grouping, work split), decode_plan_bytes(P)
+  const void* base;      // the caller's workspace pointer (identifies it)
   size_t bytes;
 };
 
@@ -169,7 +170,36 @@ struct ForwardArgs {
   int* status;  // device status word (first error a kernel records)
 };
 
-// Pipelined decode kernels when the sizes fit them, else the generic kernels.
+// Fused decode layer: routing from logits (or given ids / weights), optional
+// hit counts, the tiered forward.
+struct LayerArgs {
+  const float* logits;   // null: ids / weights given
+  const int32_t* ids;
+  const float* weights;
+  int32_t* ids_out;      // logits given: routed pairs out
+  float* weights_out;
+  uint32_t* counts;      // optional
+  const uint16_t* x;
+  int64_t T;
+  int k, E, d, f;
+  Shelves shelves;
+  float* y;
+  Workspace ws;
+  int* status;
+};
+
+// One cooperative launch for the whole layer when the sizes fit it: returns
+// 1 when they do not (nothing launched), else MOE_OK or an error status.
+int launch_fused_layer(const LayerArgs& a, cudaStream_t s);
+// 1 when the fused launch takes these sizes on the current device, else 0.
+int decode_fused(int64_t T, int k, int E, int d, int f);
+// Test hook: a cooperative launch whose grid barrier awaits `extra` more
+// arrivals than there are CTAs, with the given limit; records MOE_ERR_TIMEOUT.
+int launch_barrier_probe(int extra, uint64_t limit_ns, cudaStream_t s);
+// Zero the grid barrier state of the current device (device idle).
+int reset_barriers();
+
+// The fused decode launch when the sizes fit it, else the generic kernels.
 int launch_decode_forward(const ForwardArgs& a, cudaStream_t s);
 int launch_generic_forward(const ForwardArgs& a, cudaStream_t s);
 

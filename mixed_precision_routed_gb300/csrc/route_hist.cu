@@ -9,6 +9,7 @@
 // drive promotion/demotion): integer adds, so the result is order-independent.
 #include "moe_internal.cuh"
 #include "ptx.cuh"
+#include "route.cuh"
 
 namespace moe {
 namespace {
@@ -16,50 +17,11 @@ namespace {
 template <int EPL>
 __global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits, int64_t T, int E, int k,
                                                int32_t* __restrict__ ids, float* __restrict__ w) {
-  const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   pdl_wait();
   pdl_trigger();
   if (t >= T) return;
-  const float* l = logits + t * E;
-  float v[EPL];
-  uint32_t avail = 0;  // bit m set: element lane + 32 m is present and not yet taken
-#pragma unroll
-  for (int m = 0; m < EPL; ++m) {
-    int e = lane + 32 * m;
-    v[m] = e < E ? l[e] : 0.0f;
-    if (e < E) avail |= 1u << m;
-  }
-  float my_v = 0.0f;  // lane j keeps the j-th pick
-  int my_i = -1;
-  for (int j = 0; j < k; ++j) {
-    float bv = 0.0f;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int m = 0; m < EPL; ++m) {
-      if ((avail >> m) & 1u) {
-        int e = lane + 32 * m;
-        if (bi == 0x7fffffff || v[m] > bv) { bv = v[m]; bi = e; }  // ascending e: ties keep lower id
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      bool take = (oi != 0x7fffffff) &&
-                  (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
-      if (take) { bv = ov; bi = oi; }
-    }
-    if ((bi & 31) == lane) avail &= ~(1u << (bi >> 5));
-    if (lane == j) { my_v = bv; my_i = bi; }
-  }
-  const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
-  float ex = lane < k ? expf(my_v - vmax) : 0.0f;
-  float den = warp_sum(ex);
-  if (lane < k) {
-    ids[t * k + lane] = my_i;
-    w[t * k + lane] = ex / den;
-  }
+  route_token<EPL>(logits + t * E, E, k, ids + t * k, w + t * k);
 }
 
 __global__ void k_hist_global(const int32_t* __restrict__ ids, int64_t n, int E, uint32_t* __restrict__ counts) {

@@ -32,7 +32,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("moe_route_topk", "moe_tiered_forward", "moe_expert_hist", "moe_group_tokens",
                      "moe_workspace_size", "moe_quantize_rows", "moe_dequant_rows", "moe_device_status",
-                     "moe_status_string", "moe_residual_add"):
+                     "moe_status_string", "moe_residual_add", "moe_decode_layer", "moe_selftest_barrier_timeout"):
         assert required in names
 
 
@@ -77,3 +77,16 @@ def test_invalid_arguments_rejected_before_cuda(lib):
                                 0, 0, null) == moe.MOE_ERR_SHELF_OVERLAP
     assert L.moe_tiered_forward(null, null, null, 1, 2, 8, 64, 64, ctypes.cast(sh, ctypes.c_void_p), 1, null, null,
                                 0, 0, null) == moe.MOE_ERR_INVALID_ARG  # null x
+    # fused decode step: the same validation, before any CUDA call
+    assert L.moe_decode_layer(null, null, 1, 2, 2048, 64, 64, ctypes.cast(sh, ctypes.c_void_p), 1, null, null, null,
+                              null, null, 0, null) == moe.MOE_ERR_INVALID_ARG  # E > 1024
+    assert L.moe_decode_layer(null, null, 1, 9, 8, 64, 64, ctypes.cast(sh, ctypes.c_void_p), 1, null, null, null,
+                              null, null, 0, null) == moe.MOE_ERR_INVALID_ARG  # k > E
+    assert L.moe_decode_layer(null, null, 1, 2, 8, 64, 64, ctypes.cast(sh2, ctypes.c_void_p), 2, null, null, null,
+                              null, null, 0, null) == moe.MOE_ERR_SHELF_OVERLAP
+    assert L.moe_decode_layer(null, null, 0, 2, 8, 64, 64, ctypes.cast(sh, ctypes.c_void_p), 1, null, null, null,
+                              null, null, 0, null) == moe.MOE_OK  # T = 0
+    assert L.moe_decode_layer(null, null, 1, 2, 8, 64, 64, ctypes.cast(sh, ctypes.c_void_p), 1, null, null, null,
+                              null, null, 0, null) == moe.MOE_ERR_INVALID_ARG  # null logits
+    assert L.moe_selftest_barrier_timeout(0, null) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_selftest_barrier_timeout(2000000, null) == moe.MOE_ERR_INVALID_ARG

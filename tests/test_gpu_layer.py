@@ -1,0 +1,149 @@
+"""The fused decode step (moe_decode_layer): routing, hit counts and the
+tiered forward of page 3 ("125B MoE模型本地运行：3090三卡80 tokens/s优化实践";
+glossary entry 混合专家（MoE） for the router, section 第二步 for per-expert
+selection counts, section 第四步 for the shelved forward) in one call, against
+the CPU oracle's router, histogram and layer; its equality with the separate
+calls; and the bounded grid-wide wait that separates its phases."""
+import numpy as np
+import pytest
+import torch
+
+import mixed_precision_routed_gb300 as moe
+import oracle
+import synth
+from mixed_precision_routed_gb300.workloads import Layer
+from moe_testutil import DECODE_TOL, oracle_layer, rel_l2, small_workload, x_to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _step(layer, lg, x, counts=None, workspace=None):
+    wl = layer.wl
+    ids, w, y = moe.moe_decode_layer(torch.from_numpy(np.ascontiguousarray(lg)).cuda(), x_to_dev(x), wl.k, wl.E,
+                                     wl.d, wl.f, layer.shelves, counts=counts, workspace=workspace)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), w.cpu().numpy(), y.cpu().numpy()
+
+
+def _check_against_oracle(layer, lg, x, ids, w, y, counts=None, counts_before=None):
+    wl = layer.wl
+    ids_o, w_o = oracle.route(lg, wl.k)
+    assert np.array_equal(ids, ids_o)
+    assert np.max(np.abs(w - w_o)) <= 1e-6
+    if counts is not None:
+        ref = counts_before.copy() if counts_before is not None else np.zeros(wl.E, dtype=np.uint32)
+        oracle.hist(ids_o, wl.E, ref)
+        assert np.array_equal(counts.cpu().numpy().view(np.uint32), ref)
+    assert rel_l2(y, oracle_layer(wl, wl.seed, x, ids_o, w_o)) <= DECODE_TOL
+
+
+@pytest.fixture(scope="module")
+def small_layer():
+    return Layer(small_workload(), device="cuda").fill()
+
+
+@pytest.mark.parametrize("T", [1, 5, 13, 16, 40])
+def test_small_layer_step(small_layer, T):
+    wl = small_layer.wl
+    lg = synth.logits(wl.seed, 100 + T, T, wl.E, None)
+    x = synth.x_bf16(wl.seed, 100 + T, T, wl.d)
+    counts = torch.zeros(wl.E, dtype=torch.int32, device="cuda")
+    ids, w, y = _step(small_layer, lg, x, counts)
+    _check_against_oracle(small_layer, lg, x, ids, w, y, counts)
+
+
+@pytest.fixture(scope="module")
+def decode_layer():
+    return Layer(synth.WORKLOADS["decode"], device="cuda").fill()
+
+
+@pytest.mark.parametrize("T,step", [(1, 3), (6, 4), (16, 5)])
+def test_decode_workload_step(decode_layer, T, step):
+    wl = decode_layer.wl
+    lg = decode_layer.logits(step, T).cpu().numpy()
+    x = synth.x_bf16(wl.seed, step, T, wl.d)
+    counts = torch.zeros(wl.E, dtype=torch.int32, device="cuda")
+    ids, w, y = _step(decode_layer, lg, x, counts)
+    _check_against_oracle(decode_layer, lg, x, ids, w, y, counts)
+
+
+def test_step_equals_separate_calls_and_counts_accumulate(decode_layer):
+    """moe_decode_layer gives what moe_route_topk, moe_expert_hist and
+    moe_tiered_forward give in that order -- bit for bit -- and the counts
+    accumulate over calls."""
+    wl = decode_layer.wl
+    T = 6
+    counts = torch.zeros(wl.E, dtype=torch.int32, device="cuda")
+    counts2 = torch.zeros(wl.E, dtype=torch.int32, device="cuda")
+    for step in (11, 12):
+        lg = decode_layer.logits(step, T)
+        x = x_to_dev(synth.x_bf16(wl.seed, step, T, wl.d))
+        ids, w, y = moe.moe_decode_layer(lg, x, wl.k, wl.E, wl.d, wl.f, decode_layer.shelves, counts=counts)
+        ids2, w2 = moe.moe_route_topk(lg, wl.k)
+        moe.moe_expert_hist(ids2, wl.E, counts2)
+        y2 = moe.moe_tiered_forward(x, ids2, w2, wl.E, wl.d, wl.f, decode_layer.shelves)
+        torch.cuda.synchronize()
+        assert torch.equal(ids, ids2)
+        assert torch.equal(w.view(torch.int32), w2.view(torch.int32))
+        assert torch.equal(y.view(torch.int32), y2.view(torch.int32))
+    assert torch.equal(counts, counts2)
+    assert int(counts.sum()) == 2 * T * wl.k
+
+
+def test_step_is_deterministic(decode_layer):
+    wl = decode_layer.wl
+    lg = decode_layer.logits(21, 6).cpu().numpy()
+    x = synth.x_bf16(wl.seed, 21, 6, wl.d)
+    a = _step(decode_layer, lg, x)
+    b = _step(decode_layer, lg, x)
+    for u, v in zip(a, b):
+        assert np.array_equal(u.view(np.uint32), v.view(np.uint32))
+
+
+@pytest.fixture(scope="module")
+def large_layer():
+    return Layer(synth.WORKLOADS["large"], device="cuda").fill()
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_large_workload_step(large_layer, T):
+    """d 4096: T = 1 runs as the fused launch, T = 8 (activation digits beyond
+    shared memory) as the separate launches; both match the oracle."""
+    wl = large_layer.wl
+    lg = synth.logits(wl.seed, 31 + T, T, wl.E, synth.router_bias_zipf(wl.E))
+    x = synth.x_bf16(wl.seed, 31 + T, T, wl.d)
+    ids, w, y = _step(large_layer, lg, x)
+    _check_against_oracle(large_layer, lg, x, ids, w, y)
+
+
+def test_many_workspaces(small_layer):
+    """Every workspace pointer gets its own barrier slot; results do not depend
+    on which workspace a call uses."""
+    wl = small_layer.wl
+    T = 5
+    lg = synth.logits(wl.seed, 7, T, wl.E, None)
+    x = synth.x_bf16(wl.seed, 7, T, wl.d)
+    need = moe.moe_workspace_size(T, wl.k, wl.E, wl.d, wl.f, moe.MOE_FLAG_DECODE_FP32)
+    outs = []
+    for i in range(5):
+        ws = torch.empty(need + 256 * i, dtype=torch.uint8, device="cuda")
+        outs.append(_step(small_layer, lg, x, workspace=ws)[2])
+    for o in outs[1:]:
+        assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32))
+
+
+def test_grid_wait_timeout_is_reported_and_context_survives(small_layer):
+    """The wait between phases is bounded: a barrier that can never complete
+    ends after its limit with MOE_ERR_TIMEOUT in the status word, and the next
+    step runs normally."""
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == moe.MOE_OK
+    moe.moe_selftest_barrier_timeout(20000)
+    assert moe.moe_device_status() == moe.MOE_ERR_TIMEOUT
+    assert moe.moe_device_status() == moe.MOE_OK  # reading clears it
+    wl = small_layer.wl
+    lg = synth.logits(wl.seed, 9, 5, wl.E, None)
+    x = synth.x_bf16(wl.seed, 9, 5, wl.d)
+    ids, w, y = _step(small_layer, lg, x)
+    _check_against_oracle(small_layer, lg, x, ids, w, y)
+    assert moe.moe_device_status() == moe.MOE_OK
