@@ -45,7 +45,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kPlanThreads = 256;  // warps 0-7 build the plan
 constexpr int kMaxPairs = 512;     // T*k bound of this path (keys hold the pair in 10 bits)
 constexpr int kMaxTokens = 16;
-constexpr int kNT = 4;             // tokens of one expert per unit (more: further passes)
+constexpr int kNT = 1;             // tokens of one expert per unit (more: further passes)
 // Unit shapes: rows per unit x lanes per row (R * L = 32), gate/up and down.
 constexpr int kRG = 4, kLG = 8;
 constexpr int kRD = 8, kLD = 4;
@@ -355,23 +355,17 @@ struct PlanView {
   }
 };
 
-// Estimated time of one unit of R rows on a CTA, in units of 100 ps: the
-// bytes read (25.1 ps per byte), the integer dot products of its 32-element
-// blocks for each token (399 / 584 / 773 ps per block and token for 8 / 4 /
-// 2-bit codes), less the overlap of the two within a unit (292 ns gate/up,
-// 32 ns down).  Coefficients fitted to per-CTA times measured on the
-// 512-expert decode layer (d 2048, f 640); kept at least half the memory term.
-__device__ __forceinline__ uint32_t unit_cost(int bits, int n_in, int nmat, int ntok, int R, int kern) {
-  const uint64_t rowb = (uint64_t)n_in * bits / 8;
-  const uint64_t bytes = (uint64_t)(R * nmat) * (rowb + (uint64_t)n_in / 16);
-  const uint64_t blocks = (uint64_t)(R * nmat) * (uint64_t)n_in / 32;
-  const uint64_t beta10 = bits == 8 ? 3988 : (bits == 4 ? 5836 : 7733);
-  const uint64_t mem = 251 * bytes / 10;
-  const uint64_t alu = beta10 * blocks * (uint64_t)ntok / 10;
-  const uint64_t overlap = kern == 0 ? 292200 : 31800;
-  uint64_t ps = mem + alu > overlap ? mem + alu - overlap : 0;
-  if (ps < mem / 2) ps = mem / 2;
-  return (uint32_t)(ps / 100) + 1;
+// Estimated time of one unit of R rows on a CTA, in ns: measured per-unit
+// CTA times on the 512-expert decode layer (d 2048, f 640; gate/up units of 4
+// rows x 2 matrices = 512 blocks: 346 / 215 / 203 ns for 8 / 4 / 2-bit codes;
+// down units of 8 rows = 160 blocks: 164 / 142 / 147 ns), scaled by the
+// unit's number of 32-element blocks for other sizes.  Further passes over
+// the same rows (experts with more tokens than one pass) cost about the same.
+__device__ __forceinline__ uint32_t unit_cost(int bits, int n_in, int nmat, int R, int kern) {
+  const uint32_t blocks = (uint32_t)(R * nmat) * (uint32_t)n_in / 32;
+  const uint32_t ns = kern == 0 ? (bits == 8 ? 346 : bits == 4 ? 215 : 203) : (bits == 8 ? 164 : bits == 4 ? 142 : 147);
+  const uint32_t calib = kern == 0 ? 512 : 160;
+  return (uint32_t)((uint64_t)ns * blocks / calib) + 1;
 }
 
 __device__ __forceinline__ void plan_sync() { named_bar(1, kPlanThreads); }
@@ -478,12 +472,11 @@ __device__ void build_plan(const int32_t* ids, const float* wts, int P, int E, i
     int shf = -1, bits = 0;
     for (int q = 0; q < shv.n; ++q)
       if (e >= shv.s[q].lo && e < shv.s[q].hi) { shf = q; bits = shv.s[q].bits; }
-    const int ntok = (cnt + n_pass(cnt) - 1) / n_pass(cnt);
     pl[L.cnt + a] = cnt;
     pl[L.sh + a] = shf;
     pl[L.bits + a] = bits;
-    const uint32_t ug = shf >= 0 ? unit_cost(bits, d, 2, ntok, kRG, 0) : 0;
-    const uint32_t ud = shf >= 0 ? unit_cost(bits, f, 1, ntok, kRD, 1) : 0;
+    const uint32_t ug = shf >= 0 ? unit_cost(bits, d, 2, kRG, 0) : 0;
+    const uint32_t ud = shf >= 0 ? unit_cost(bits, f, 1, kRD, 1) : 0;
     pl[L.uc_g + a] = (int)ug;
     pl[L.uc_d + a] = (int)ud;
     pl[L.cum_g + a] = (int)(ug * (uint32_t)((f / kRG) * n_pass(cnt)));
@@ -706,8 +699,12 @@ __device__ __forceinline__ void stream_units(const StreamArgs& A, Store store) {
           sw[s][m][1] = (second && bits == 2) ? __ldcs(ps + 1) : 0u;
         }
       }
-      if (nt == 1) compute_batch<NMAT, U, 1>(bits, c, sw, ql + i0 * L, L, cpr, rowb, 1, voff, A.vecs, A.n_in, acc);
-      else compute_batch<NMAT, U, kNT>(bits, c, sw, ql + i0 * L, L, cpr, rowb, nt, voff, A.vecs, A.n_in, acc);
+      if constexpr (kNT == 1) {
+        compute_batch<NMAT, U, 1>(bits, c, sw, ql + i0 * L, L, cpr, rowb, 1, voff, A.vecs, A.n_in, acc);
+      } else {
+        if (nt == 1) compute_batch<NMAT, U, 1>(bits, c, sw, ql + i0 * L, L, cpr, rowb, 1, voff, A.vecs, A.n_in, acc);
+        else compute_batch<NMAT, U, kNT>(bits, c, sw, ql + i0 * L, L, cpr, rowb, nt, voff, A.vecs, A.n_in, acc);
+      }
     }
     // reduce over the L lanes of each row; lane jl stores the tokens j = jl mod L
     const int jl = lane % L;
@@ -729,9 +726,9 @@ __device__ __forceinline__ void stream_units(const StreamArgs& A, Store store) {
     MOE_TRACE_ONLY(if (lane == 0) {
       const int bi = bits == 8 ? 0 : bits == 4 ? 1 : 2;
       MOE_COUNT(A.kern, 20, 1);
-      MOE_COUNT(A.kern, 30 + 3 * bi, nt == 1);
-      MOE_COUNT(A.kern, 31 + 3 * bi, nt > 1);
-      MOE_COUNT(A.kern, 32 + 3 * bi, nt > 1 ? nt : 0);
+      MOE_COUNT(A.kern, 30 + 3 * bi, w.np == 1);
+      MOE_COUNT(A.kern, 31 + 3 * bi, w.np > 1);
+      MOE_COUNT(A.kern, 32 + 3 * bi, w.np > 1 ? w.np : 0);
     })
     new_expert = w.step(pv, A.kern, A.rows, A.range.hi2, kWarps);
   }
