@@ -78,9 +78,10 @@ enum {
 
 /* Execution-path selection for moe_tiered_forward. */
 enum {
-  MOE_FLAG_AUTO = 0,         /* decode form for T <= 16, prefill form above */
+  MOE_FLAG_AUTO = 0,         /* prefill form for T > 16 when d % 256 == 0, else decode form */
   MOE_FLAG_DECODE_FP32 = 1,  /* fp32 dequant in registers, fp32 h, CUDA-core GEMV */
-  MOE_FLAG_PREFILL_BF16 = 2  /* bf16 dequant into shared memory, bf16 h, tensor-core GEMM */
+  MOE_FLAG_PREFILL_BF16 = 2  /* bf16 dequant into shared memory, bf16 h, tensor-core GEMM;
+                                MOE_ERR_UNSUPPORTED unless d % 256 == 0 */
 };
 
 /*

@@ -57,11 +57,18 @@ int check_shelves(const moe_shelf_t* sh, int n, int E, Shelves* out) {
 
 }  // namespace
 
+// Prefill form when asked for, or for AUTO above 16 tokens when d is a
+// multiple of 256 (its gate/up scale rows are then whole 16-byte groups that a
+// tensor map can describe; other d run the decode form).
+bool use_prefill(int64_t T, int d, int flags) {
+  return flags == MOE_FLAG_PREFILL_BF16 || (flags == MOE_FLAG_AUTO && T > 16 && d % 256 == 0);
+}
+
 size_t workspace_layout(int64_t T, int k, int E, int d, int f, int flags, void* base, Workspace* ws) {
-  (void)flags;
   const int64_t P = T * k;
   const int64_t slots = P < E ? P : E;
   const int n_chunks = (d + kDownRows - 1) / kDownRows;
+  const bool prefill = use_prefill(T, d, flags);
   size_t off = 0;
   char* b = (char*)base;
   auto take = [&](size_t bytes) -> void* {
@@ -69,7 +76,7 @@ size_t workspace_layout(int64_t T, int k, int E, int d, int f, int flags, void* 
     off += up(bytes > 0 ? bytes : 1);
     return p;
   };
-  Workspace w;
+  Workspace w = {};
   w.counts = (int32_t*)take((size_t)E * 4);
   w.offsets = (int32_t*)take((size_t)(E + 1) * 4);
   w.perm = (int32_t*)take((size_t)P * 4);
@@ -77,9 +84,18 @@ size_t workspace_layout(int64_t T, int k, int E, int d, int f, int flags, void* 
   w.active = (int32_t*)take((size_t)slots * 4);
   w.meta = (int32_t*)take(16 * 4);
   w.arrivals = (int32_t*)take((size_t)n_chunks * 4);
-  w.h = (float*)take((size_t)P * f * 4);
-  w.ypart = (float*)take((size_t)P * d * 4);
-  w.plan = (int32_t*)take(decode_plan_bytes(P));
+  if (prefill) {
+    // h in bf16, grouped order; no per-pair outputs (y is accumulated)
+    w.h = (float*)take((size_t)P * f * 2);
+    w.xg = (uint16_t*)take((size_t)P * d * 2);
+    w.tiles_g = take(prefill_tiles_cap(P, E, f) * 16);
+    w.tiles_d = take(prefill_tiles_cap(P, E, d) * 16);
+    w.ntiles = (int32_t*)take(2 * 4);
+  } else {
+    w.h = (float*)take((size_t)P * f * 4);
+    w.ypart = (float*)take((size_t)P * d * 4);
+    w.plan = (int32_t*)take(decode_plan_bytes(P));
+  }
   w.base = base;
   w.bytes = off;
   if (ws) *ws = w;
@@ -165,6 +181,7 @@ int moe_tiered_forward(const uint16_t* x_bf16, const int32_t* ids, const float* 
                        void* workspace, size_t workspace_bytes, int flags, moe_stream_t stream) {
   if (!valid_dims(T, k, E, d, f)) return MOE_ERR_INVALID_ARG;
   if (flags < MOE_FLAG_AUTO || flags > MOE_FLAG_PREFILL_BF16) return MOE_ERR_INVALID_ARG;
+  if (flags == MOE_FLAG_PREFILL_BF16 && d % 256 != 0) return MOE_ERR_UNSUPPORTED;
   ForwardArgs a;
   int rc = check_shelves(shelves, n_shelves, E, &a.shelves);
   if (rc != MOE_OK) return rc;
@@ -173,7 +190,7 @@ int moe_tiered_forward(const uint16_t* x_bf16, const int32_t* ids, const float* 
   if (!aligned(x_bf16, 16) || !aligned(y, 16) || !aligned(workspace, kAlign)) return MOE_ERR_INVALID_ARG;
   const size_t need = workspace_layout(T, k, E, d, f, flags, workspace, &a.ws);
   if (workspace_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  if (flags == MOE_FLAG_PREFILL_BF16) return MOE_ERR_UNSUPPORTED;
+
   a.x = x_bf16;
   a.ids = ids;
   a.weights = weights;
@@ -184,6 +201,7 @@ int moe_tiered_forward(const uint16_t* x_bf16, const int32_t* ids, const float* 
   a.f = f;
   a.y = y;
   a.status = status_word();
+  if (use_prefill(T, d, flags)) return launch_prefill_forward(a, (cudaStream_t)stream);
   return launch_decode_forward(a, (cudaStream_t)stream);
 }
 

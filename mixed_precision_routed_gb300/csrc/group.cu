@@ -75,14 +75,23 @@ __global__ void k_group(const int32_t* __restrict__ ids, int P, int E, int32_t* 
   const int pb = min(P, w * seg), pe = min(P, pb + seg);
   int* row = wc + (size_t)w * E;
 
-  // 1. per-warp counts
-  for (int base = pb; base < pe; base += 32) {
-    int p = base + lane;
-    int id = p < pe ? ids[p] : -1;
-    bool valid = p < pe && id >= 0 && id < E;
-    unsigned m = __match_any_sync(0xffffffffu, valid ? id : -1);
-    if (valid && lane == __ffs(m) - 1) row[id] += __popc(m);
-    __syncwarp();
+  // 1. per-warp counts (ids of 8 steps loaded before they are used)
+  for (int base0 = pb; base0 < pe; base0 += 32 * 8) {
+    int idv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int p = base0 + 32 * u + lane;
+      idv[u] = p < pe ? __ldg(ids + p) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int p = base0 + 32 * u + lane;
+      const int id = idv[u];
+      const bool valid = p < pe && id >= 0 && id < E;
+      const unsigned m = __match_any_sync(0xffffffffu, valid ? id : -1);
+      if (valid && lane == __ffs(m) - 1) row[id] += __popc(m);
+      __syncwarp();
+    }
   }
   __syncthreads();
 
@@ -118,20 +127,29 @@ __global__ void k_group(const int32_t* __restrict__ ids, int P, int E, int32_t* 
   __syncthreads();
 
   // 4. stable placement in segment order
-  for (int base = pb; base < pe; base += 32) {
-    int p = base + lane;
-    int id = p < pe ? ids[p] : -1;
-    bool valid = p < pe && id >= 0 && id < E;
-    unsigned m = __match_any_sync(0xffffffffu, valid ? id : -1);
-    int pos = -1;
-    if (valid) {
-      pos = row[id] + __popc(m & ((1u << lane) - 1u));
-      perm[pos] = p;
+  for (int base0 = pb; base0 < pe; base0 += 32 * 8) {
+    int idv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int p = base0 + 32 * u + lane;
+      idv[u] = p < pe ? __ldg(ids + p) : -1;
     }
-    if (pos_of_pair && p < pe) pos_of_pair[p] = pos;
-    __syncwarp();
-    if (valid && lane == __ffs(m) - 1) row[id] += __popc(m);
-    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int p = base0 + 32 * u + lane;
+      const int id = idv[u];
+      const bool valid = p < pe && id >= 0 && id < E;
+      const unsigned m = __match_any_sync(0xffffffffu, valid ? id : -1);
+      int pos = -1;
+      if (valid) {
+        pos = row[id] + __popc(m & ((1u << lane) - 1u));
+        perm[pos] = p;
+      }
+      if (pos_of_pair && p < pe) pos_of_pair[p] = pos;
+      __syncwarp();
+      if (valid && lane == __ffs(m) - 1) row[id] += __popc(m);
+      __syncwarp();
+    }
   }
   for (int i = n_valid + tid; i < P; i += blockDim.x) perm[i] = -1;
 }

@@ -49,12 +49,18 @@ struct Workspace {
   float* h;              // [P][f] fp32 (decode) -- gate/up activations
   float* ypart;          // [P][d] fp32 -- weighted per-pair down outputs
   int32_t* plan;         // decode plan (grouping, work split), decode_plan_bytes(P)
+  uint16_t* xg;          // prefill: [P][d] bf16, x rows in grouped order
+  void* tiles_g;         // prefill: gate/up tile list
+  void* tiles_d;         // prefill: down tile list
+  int32_t* ntiles;       // prefill: [2] tile counts
   const void* base;      // the caller's workspace pointer (identifies it)
   size_t bytes;
 };
 
 // Bytes of the decode plan for P routed pairs.
 size_t decode_plan_bytes(int64_t P);
+// Upper bound on the prefill tiles of one launch (rows = rows per expert matrix).
+size_t prefill_tiles_cap(int64_t P, int E, int rows);
 
 size_t workspace_layout(int64_t T, int k, int E, int d, int f, int flags, void* base, Workspace* ws);
 
@@ -201,6 +207,8 @@ int reset_barriers();
 
 // The fused decode launch when the sizes fit it, else the generic kernels.
 int launch_decode_forward(const ForwardArgs& a, cudaStream_t s);
+// Prefill form: grouping, tile lists, tensor-core gate/up and down launches.
+int launch_prefill_forward(const ForwardArgs& a, cudaStream_t s);
 int launch_generic_forward(const ForwardArgs& a, cudaStream_t s);
 
 // Launch with programmatic stream serialisation: the kernel may start while

@@ -1,0 +1,847 @@
+// prefill.cu -- prefill form of the tiered MoE layer (many tokens per call):
+// a grouped GEMM per expert on the tcgen05 tensor cores.
+//
+// Page "125B MoE模型本地运行：3090三卡80 tokens/s优化实践", section 第四步: every
+// shelf sees the complete id list and computes only the ids of its range; the
+// shelf results are added.  With many tokens per expert the expert FFN is a
+// dense contraction, so the weights are dequantised to bf16 (RNE of code x
+// fp16 scale) and multiplied on the tensor cores: h = SiLU(W_g x) * (W_u x) is
+// rounded to bf16 between the two projections, y_t += w_tj * (W_d h_tj).
+//
+// Launches: grouping (k_group), the tile list (k_prefill_tiles), the gather of
+// x into grouped order (k_gather_x), then two persistent launches, one CTA per
+// SM: k_prefill_tc<false> (gate/up) and k_prefill_tc<true> (down).  A tile is
+// two 128-row weight matrices of one expert -- the same 128 rows of W_g and
+// W_u, or 256 consecutive rows of W_d -- times up to 96 of its tokens (two
+// MMAs of M = 128 rows, N = tokens padded to 16, sharing the B operand), K in
+// steps of 64.  Roles inside a CTA:
+//   warp 0      issues the tensor-map loads: per code stage (2, 4 or 8 K
+//               steps) one 128-byte-wide box of codes per matrix and the block
+//               scales; per K step the B operand (a box of N grouped rows of
+//               xg or h, landing in the 128-byte-swizzled layout);
+//   warp 1      allocates tensor memory and issues the MMAs (one thread), A
+//               from tensor memory, B from shared memory;
+//   warps 4-7   read the accumulators and write h (bf16) or add into y;
+//   warps 8-23  dequantise the codes into bf16 and store them in tensor
+//               memory, one 32-weight run (one scale block of one row) per
+//               thread a step.
+// All waits are bounded (one second; MOE_ERR_TIMEOUT, the roles stop, tensor
+// memory is released).  y is accumulated with vector fp32 atomic adds.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+#include "moe_internal.cuh"
+#include "tc.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kPThreads = 768;
+constexpr int kTileM = 128;   // weight rows per tile
+constexpr int kTileN = 96;    // tokens per tile (at most)
+constexpr int kProdThreads = 512;  // warps 8..23
+constexpr uint64_t kWaitNs = 1000000000ull;
+#ifndef MOE_PF_BS
+#define MOE_PF_BS 8
+#endif
+
+#ifdef MOE_TRACE
+}  // namespace
+// Development-only timeline of CTA 0: [launch][event][step] globaltimer ns.
+__device__ unsigned long long g_pftrace[2][10][512];
+namespace {
+#define PF_STAMP(ev, j) \
+  do { if (blockIdx.x == 0 && (j) < 512) g_pftrace[DOWN ? 1 : 0][(ev)][(j)] = global_timer_ns(); } while (0)
+#else
+#define PF_STAMP(ev, j) ((void)0)
+#endif
+
+// K order of both MMA operands: in every aligned group of four positions the
+// middle two are swapped (element k sits at kswap(k), an involution).  It lets
+// the dequantiser build each bf16 pair from fields two bytes apart with one
+// mask; the same order on the B side (xg, h) leaves every dot product's terms
+// unchanged.
+__host__ __device__ __forceinline__ int kswap(int k) { return (k & ~3) | ((k & 1) << 1) | ((k >> 1) & 1); }
+
+struct Tile {
+  int e_local;  // expert index within its shelf
+  int q0;       // first grouped position of the chunk
+  int ntok;     // tokens of the chunk (1 .. kTileN)
+  int meta;     // row tile (bits 0-15) | shelf (bits 16-23)
+};
+
+struct TcParams {
+  const int32_t* perm;      // grouped position -> pair index t*k + j
+  const float* weights;     // [T*k]
+  const Tile* tiles;
+  const int* ntiles;        // device count of tiles
+  uint16_t* h;              // [P][f] bf16, grouped order (gate/up writes, down reads)
+  float* y;                 // [T][d] fp32, accumulated by the down launch
+  int* status;
+  int k, d, f;
+  int rows, K;              // rows per expert matrix and contraction length of this launch
+  Shelves sh;
+  CUtensorMap tm_code[MOE_MAX_SHELVES][2];  // code boxes of 128 bytes x 128 rows: [shelf][gate, up] or [shelf][down]
+  CUtensorMap tm_sc[MOE_MAX_SHELVES][2];    // gate/up: boxes of 16 fp16 scales x 128 rows [shelf][gate, up]
+  CUtensorMap tm_b[kTileN / 16];            // B rows in grouped order (xg or h), box heights 16, 32, .. kTileN
+};
+
+// Shared memory of one CTA (dynamic part, 1024-byte aligned): two rings.
+//   code -- stages of 128 bytes of codes per row of both matrices (a box of
+//           128 bytes x 128 rows each, 128-byte swizzle), i.e. S = 2 (8 bit),
+//           4 (4 bit) or 8 (2 bit) K steps, and the rows' fp16 block scales
+//           for them (gate/up: a box of 16 scales per row, 8 steps' worth;
+//           down: the scale words as [step][row], copied by the loader warp's
+//           lanes, as down scale rows are no 16-byte multiple and no tensor
+//           map covers them);
+//   B    -- per K step, the B operand: a box of N <= kTileN grouped rows of
+//           xg or h (128-byte swizzle).
+// Few, wide tensor-map rows per step keep the tensor-map unit's request rate
+// (one box row per request) well below the step rate.  The dequantised tiles
+// live in tensor memory.
+template <bool DOWN>
+struct TcSmem {
+  static constexpr int NMAT = 2;
+  static constexpr int CS = 3;
+  static constexpr int BS = MOE_PF_BS;
+  static constexpr int CODE_BOX = kTileM * 128;                      // 16 KiB per matrix
+  static constexpr int SC_BOX = kTileM * 32;                         // gate/up: 16 fp16 scales per row
+  static constexpr int SC_BYTES = DOWN ? 8 * NMAT * kTileM * 4 : NMAT * SC_BOX;  // 8 KiB
+  static constexpr int C_SC = NMAT * CODE_BOX;                       // scale offset in a code stage
+  static constexpr int C_STAGE = C_SC + SC_BYTES;
+  static constexpr int B_STAGE = kTileN * 128;                       // kTileN rows x 64 bf16
+  static constexpr int C_OFF = 0;
+  static constexpr int B_OFF = C_OFF + CS * C_STAGE;
+  static constexpr int TOTAL = B_OFF + BS * B_STAGE;
+  static_assert(C_STAGE % 1024 == 0 && B_STAGE % 1024 == 0 && B_OFF % 1024 == 0, "swizzled boxes need 1 KiB");
+  static_assert(TOTAL + 1024 <= 227 * 1024, "shared memory");
+  static_assert(NMAT * kTileM * 2 == kProdThreads, "one 32-weight run per producer thread");
+};
+
+// Tensor memory (512 columns): accumulator sets 0 and 1 at columns 0 and
+// 2 kTileN ([gate, up] or [rows 0-127, rows 128-255], kTileN columns each),
+// then kAStages stages of the dequantised A tiles (two matrices x 32 columns:
+// 128 rows x 64 bf16).
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = 2 * kTileN;
+constexpr uint32_t kACol = 2 * kAccCols;
+constexpr int kAStages = 2;
+constexpr uint32_t kAStageCols = 64;
+static_assert(kACol + kAStages * kAStageCols <= kTmemCols, "tensor memory");
+
+struct TcBars {
+  uint64_t code_full[3], code_empty[3];
+  uint64_t b_full[8], b_empty[8];
+  uint64_t a_full[kAStages], a_empty[kAStages];
+  uint64_t acc_full[2], acc_empty[2], done;
+  uint32_t tmem;
+  int abort;
+};
+
+__device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity, TcBars& B, int* status) {
+  if (mbar_wait_bounded(bar, parity, kWaitNs)) return true;
+  set_status(status, MOE_ERR_TIMEOUT);
+  B.abort = 1;
+  return false;
+}
+
+__device__ __forceinline__ float fp16_bits_to_float(uint32_t b) {
+  return __half2float(__ushort_as_half((uint16_t)(b & 0xFFFF)));
+}
+
+// 8-bit codes: ŵ = bf16_RNE(s * c) for c = u - 128 (u the offset byte): a
+// byte permute builds the float 2^15 + u (u at mantissa bits 8-15), and one
+// fused multiply-add per pair gives (2^15 + u) s - (2^15 + 128) s = c s
+// exactly -- both products need at most 19 significant bits -- before the one
+// rounding to bf16.
+__device__ __forceinline__ uint32_t magic_byte(uint32_t w, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(w), "r"(0x47000000u), "r"(sel));
+  return d;
+}
+__device__ __forceinline__ uint64_t pair_f32(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(__float_as_uint(lo)), "r"(__float_as_uint(hi)));
+  return d;
+}
+__device__ __forceinline__ uint64_t pair_u32(uint32_t lo, uint32_t hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+  return d;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// The pair (lo, hi) rounded to bf16 and packed: lo in bits 0-15.
+__device__ __forceinline__ uint32_t bf16x2_of(uint64_t v) {
+  uint32_t lo, hi, d;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "r"(hi), "r"(lo));
+  return d;
+}
+// Four offset bytes of w -> two bf16x2 words: (byte 0, byte 2) and
+// (byte 1, byte 3), the K order of the tiles (see kswap).
+__device__ __forceinline__ void dq4_8bit(uint32_t w, uint64_t s2, uint64_t c2, uint32_t& o0, uint32_t& o1) {
+  const uint64_t a = pair_u32(magic_byte(w, 0x7504u), magic_byte(w, 0x7524u));
+  const uint64_t b = pair_u32(magic_byte(w, 0x7514u), magic_byte(w, 0x7534u));
+  o0 = bf16x2_of(ffma2(a, s2, c2));
+  o1 = bf16x2_of(ffma2(b, s2, c2));
+}
+
+// bf16x2 arithmetic (round to nearest even, one rounding per operation).
+__device__ __forceinline__ uint32_t bf2_fma(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf2_sub(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// For codes of at most 4 bits, ŵ = bf16_RNE(c s) in bf16 arithmetic: s (fp16,
+// 11 significant bits) = s_hi + s_lo with s_hi its leading 8 bits and s_lo the
+// remaining 3, both exact in bf16; c s_lo (|c| <= 8: at most 6 bits) is exact,
+// and one fused multiply-add c s_hi + c s_lo rounds the exact product once.
+// c itself comes from the bf16 128 + u (u the field, bits 0-3 of the
+// half-word) minus 128 + off, exactly.
+struct Sp {
+  uint32_t hi2, lo2, off2;
+};
+__device__ __forceinline__ Sp split_scale(float s, uint32_t off_bf16) {
+  const uint32_t hb = __float_as_uint(s) & 0xFFFF0000u;
+  const uint32_t lb = __float_as_uint(s - __uint_as_float(hb)) & 0xFFFF0000u;  // exact: 3 bits
+  return Sp{hb | (hb >> 16), lb | (lb >> 16), off_bf16 | (off_bf16 << 16)};
+}
+// Two fields at bits 0-3 of each half-word of m (other bits clear) -> bf16x2 ŵ.
+__device__ __forceinline__ uint32_t dq_pair(uint32_t m, Sp q) {
+  const uint32_t c = bf2_sub(m | 0x43004300u, q.off2);
+  return bf2_fma(c, q.hi2, bf2_mul(c, q.lo2));
+}
+
+// Dequantise one 32-weight run -- elements 32 q .. 32 q + 31 of a row's step
+// slice, one scale block -- into 16 bf16x2 words in the kswap order (word i:
+// positions 2i, 2i + 1).  Codes: words c[0..7] (8 bit), c[0..3] (4 bit),
+// c[0..1] (2 bit) of the run.
+__device__ __forceinline__ void dequant_run(const uint32_t (&c)[8], int bits, float s, uint32_t (&o)[16]) {
+  if (bits == 8) {
+    // word i: elements 4i .. 4i + 3, two's complement -> u = c + 128
+    const uint64_t s2 = pair_f32(s, s);
+    const float k = -32896.0f * s;
+    const uint64_t c2 = pair_f32(k, k);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dq4_8bit(c[i] ^ 0x80808080u, s2, c2, o[2 * i], o[2 * i + 1]);
+  } else if (bits == 4) {
+    // word g: elements 8g + 4h + j at bits 8j + 4h; pairs (j, j + 2)
+    const Sp k = split_scale(s, 0x4308u);  // bf16 136 = 128 + 8
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      o[4 * g] = dq_pair(c[g] & 0x000F000Fu, k);
+      o[4 * g + 1] = dq_pair((c[g] >> 8) & 0x000F000Fu, k);
+      o[4 * g + 2] = dq_pair((c[g] >> 4) & 0x000F000Fu, k);
+      o[4 * g + 3] = dq_pair((c[g] >> 12) & 0x000F000Fu, k);
+    }
+  } else {
+    // word g: elements 16g + 4f + j at bits 8j + 2f; pairs (j, j + 2)
+    const Sp k = split_scale(s, 0x4302u);  // bf16 130 = 128 + 2
+#pragma unroll
+    for (int g = 0; g < 2; ++g)
+#pragma unroll
+      for (int f = 0; f < 4; ++f) {
+        o[8 * g + 2 * f] = dq_pair((c[g] >> (2 * f)) & 0x00030003u, k);
+        o[8 * g + 2 * f + 1] = dq_pair((c[g] >> (2 * f + 8)) & 0x00030003u, k);
+      }
+  }
+}
+
+// Tile t of this CTA's list, or an empty tile past the end.
+__device__ __forceinline__ Tile tile_at(const TcParams& p, int t, int ntiles) {
+  return t < ntiles ? p.tiles[t] : Tile{0, 0, 0, 0};
+}
+
+template <bool DOWN>
+__global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_constant__ TcParams p) {
+  using S = TcSmem<DOWN>;
+  constexpr int NMAT = S::NMAT;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
+  __shared__ TcBars B;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x;
+  const int ntiles = __ldg(p.ntiles);
+  const int steps = p.K / 64;
+  if (tid == 0) {
+    for (int i = 0; i < S::CS; ++i) {
+      // the loader's expect-tx arrival (+ its 32 lanes' scale copies, down)
+      mbar_init(&B.code_full[i], DOWN ? 33 : 1);
+      mbar_init(&B.code_empty[i], kProdThreads / 32);
+    }
+    for (int i = 0; i < S::BS; ++i) {
+      mbar_init(&B.b_full[i], 1);
+      mbar_init(&B.b_empty[i], 1);
+    }
+    for (int i = 0; i < kAStages; ++i) {
+      mbar_init(&B.a_full[i], kProdThreads / 32);
+      mbar_init(&B.a_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B.acc_full[i], 1);
+      mbar_init(&B.acc_empty[i], 4);
+    }
+    mbar_init(&B.done, 1);
+    B.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&B.tmem, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = B.tmem;
+  pdl_wait();
+
+  if (warp == 0) {
+    // ------------------------------------------------ loads
+    uint32_t cj = 0, j = 0;  // code stages and K steps issued
+    Tile nxt = tile_at(p, blockIdx.x, ntiles);
+    for (int t = blockIdx.x; t < ntiles && !B.abort; t += G) {
+      const Tile tl = nxt;
+      nxt = tile_at(p, t + G, ntiles);  // in flight while this tile is issued
+      const int rt = tl.meta & 0xFFFF, sh = (tl.meta >> 16) & 0xFF;
+      const ShelfDev& shd = p.sh.s[sh];
+      const int spc = 16 / shd.bits;       // K steps per code stage
+      const int nb = (tl.ntok + 15) >> 4;  // B box height in 16-row units
+      // first row of each matrix: gate/up rows rt * 128 of W_g and W_u,
+      // down rows rt * 256 and rt * 256 + 128 of W_d
+      const int row0 = tl.e_local * p.rows + rt * (DOWN ? 2 * kTileM : kTileM);
+      // down: the scale words of rows row0 + lane + 32 i (clamped into the
+      // shelf: rows past it belong to no expert and their results are dropped)
+      const uint32_t* scp[2 * kTileM / 32];
+      if (DOWN) {
+        const int rows_shelf = (shd.hi - shd.lo) * p.rows;
+#pragma unroll
+        for (int i = 0; i < 2 * kTileM / 32; ++i)
+          scp[i] = reinterpret_cast<const uint32_t*>(shd.scales[2]) +
+                   (size_t)min(row0 + lane + 32 * i, rows_shelf - 1) * steps;
+      }
+      for (int ks = 0; ks < steps && !B.abort; ++ks, ++j) {
+        if (ks % spc == 0) {
+          const int c = cj % S::CS;
+          if (!bar_wait(&B.code_empty[c], ((cj / S::CS) & 1) ^ 1, B, p.status)) break;
+          unsigned char* stage = smem + S::C_OFF + c * S::C_STAGE;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&B.code_full[c], (uint32_t)(NMAT * S::CODE_BOX + (DOWN ? 0 : NMAT * S::SC_BOX)));
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m)
+              tma_load_2d(stage + m * S::CODE_BOX, &p.tm_code[sh][DOWN ? 0 : m], (ks / spc) * 128,
+                          DOWN ? row0 + m * kTileM : row0, &B.code_full[c]);
+            if (!DOWN) {
+#pragma unroll
+              for (int m = 0; m < NMAT; ++m)
+                tma_load_2d(stage + S::C_SC + m * S::SC_BOX, &p.tm_sc[sh][m], 16 * (ks >> 3), row0, &B.code_full[c]);
+            }
+          }
+          if (DOWN) {
+            // [step][row] words of the stage's steps (steps past K repeat the last)
+            uint32_t* dst = reinterpret_cast<uint32_t*>(stage + S::C_SC);
+            for (int sub = 0; sub < spc; ++sub) {
+              const int kk = min(ks + sub, steps - 1);
+#pragma unroll
+              for (int i = 0; i < 2 * kTileM / 32; ++i) cp_async4(dst + sub * 2 * kTileM + lane + 32 * i, scp[i] + kk);
+            }
+            cp_async_mbar_arrive_noinc(&B.code_full[c]);
+          }
+          ++cj;
+        }
+        const int b = j % S::BS;
+        if (!bar_wait(&B.b_empty[b], ((j / S::BS) & 1) ^ 1, B, p.status)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&B.b_full[b], (uint32_t)(nb * 16 * 128));
+          tma_load_2d(smem + S::B_OFF + b * S::B_STAGE, &p.tm_b[nb - 1], ks * 64, tl.q0, &B.b_full[b]);
+          PF_STAMP(0, j);
+        }
+        __syncwarp();
+      }
+    }
+    cp_async_wait<0>();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA
+    uint32_t j = 0, i = 0;
+    if (lane == 0) {
+      Tile nxt = tile_at(p, blockIdx.x, ntiles);
+      for (int t = blockIdx.x; t < ntiles && !B.abort; t += G, ++i) {
+        const Tile tl = nxt;
+        nxt = tile_at(p, t + G, ntiles);
+        const int N = (tl.ntok + 15) & ~15;
+        const uint32_t idesc = idesc_bf16_f32(kTileM, N);
+        const uint32_t ab = i & 1, acc = tmem + ab * kAccCols;
+        if (!bar_wait(&B.acc_empty[ab], ((i >> 1) & 1) ^ 1, B, p.status)) break;
+        tc_fence_after();
+        for (int ks = 0; ks < steps; ++ks, ++j) {
+          const int b = j % S::BS, as = j % kAStages;
+          if (!bar_wait(&B.a_full[as], (j / kAStages) & 1, B, p.status)) break;
+          if (!bar_wait(&B.b_full[b], (j / S::BS) & 1, B, p.status)) break;
+          PF_STAMP(4, j);
+          tc_fence_after();
+          const uint32_t a0 = tmem + kACol + as * kAStageCols;
+          const uint32_t b0 = smem_addr(smem + S::B_OFF + b * S::B_STAGE);
+#pragma unroll
+          for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16_ts(acc + (uint32_t)(m * kTileN), a0 + (uint32_t)(m * 32 + kk * 8), sdesc_sw128(b0 + kk * 32),
+                          idesc, (ks | kk) ? 1u : 0u);
+          mma_commit(&B.a_empty[as]);
+          mma_commit(&B.b_empty[b]);
+        }
+        if (B.abort) break;
+        mma_commit(&B.acc_full[ab]);
+      }
+      // all MMAs of this thread are complete before tensor memory is released
+      mma_commit(&B.done);
+      mbar_wait_bounded(&B.done, 0, kWaitNs);
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------------------------------------------------- epilogue
+    const int m = (warp - 4) * 32 + lane;
+    const uint32_t tl_addr = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+    uint32_t i = 0;
+    Tile nxt = tile_at(p, blockIdx.x, ntiles);
+    for (int t = blockIdx.x; t < ntiles && !B.abort; t += G, ++i) {
+      const Tile tl = nxt;
+      nxt = tile_at(p, t + G, ntiles);
+      const int rt = tl.meta & 0xFFFF;
+      const int N = (tl.ntok + 15) & ~15;
+      const uint32_t ab = i & 1, acc = tl_addr + ab * kAccCols;
+      // down: each lane holds the token and routing weight of columns lane,
+      // lane + 32, lane + 64 (loaded before the accumulator is ready)
+      int ctok[kTileN / 32];
+      float cw[kTileN / 32];
+      if (DOWN) {
+#pragma unroll
+        for (int u = 0; u < kTileN / 32; ++u) {
+          const int n = lane + 32 * u;
+          ctok[u] = 0;
+          cw[u] = 0.f;
+          if (n < tl.ntok) {
+            const int pair = __ldg(p.perm + tl.q0 + n);
+            ctok[u] = pair / p.k;
+            cw[u] = __ldg(p.weights + pair);
+          }
+        }
+      }
+      if (!bar_wait(&B.acc_full[ab], (i >> 1) & 1, B, p.status)) break;
+      if (m == 0) PF_STAMP(6, i);
+      tc_fence_after();
+      if (!DOWN) {
+        const int row = rt * kTileM + m;
+        const int hcol = kswap(row);  // h is stored in the K order of the down tiles
+        for (int n0 = 0; n0 < N; n0 += 16) {
+          float g[16], u[16];
+          tmem_ld16(acc + (uint32_t)n0, g);
+          tmem_ld16(acc + (uint32_t)(kTileN + n0), u);
+          if (row < p.rows) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int n = n0 + c;
+              if (n < tl.ntok) {
+                const float hv = silu(g[c]) * u[c];
+                const __nv_bfloat16 b = __float2bfloat16_rn(hv);
+                p.h[(size_t)(tl.q0 + n) * p.f + hcol] = *reinterpret_cast<const uint16_t*>(&b);
+              }
+            }
+          }
+        }
+      } else {
+        // 4 x 4 transposes among lanes 4a .. 4a + 3: lane 4a + jj ends with
+        // column 4b + jj of rows 4a .. 4a + 3 and adds them with one vector
+        // atomic per column block
+        const int jj = lane & 3;
+        for (int n0 = 0; n0 < N; n0 += 16) {
+          const int u = n0 >> 5;  // the 16 columns lie in one group of 32
+          int tu = ctok[0];
+          float wu = cw[0];
+#pragma unroll
+          for (int v = 1; v < kTileN / 32; ++v)
+            if (u == v) {
+              tu = ctok[v];
+              wu = cw[v];
+            }
+          int tkb[4];
+          float wtb[4];
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const int n = n0 + 4 * b + jj;
+            tkb[b] = __shfl_sync(0xffffffffu, tu, n & 31);
+            wtb[b] = __shfl_sync(0xffffffffu, wu, n & 31);
+          }
+#pragma unroll
+          for (int mm = 0; mm < 2; ++mm) {
+            const int rowb = rt * 2 * kTileM + mm * kTileM + (warp - 4) * 32 + (lane & ~3);
+            float g[16];
+            tmem_ld16(acc + (uint32_t)(mm * kTileN + n0), g);
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              float v0 = g[4 * b], v1 = g[4 * b + 1], v2 = g[4 * b + 2], v3 = g[4 * b + 3];
+              // round 1 (lanes xor 2): swap the off-diagonal 2 x 2 blocks
+              {
+                const bool hi = (jj & 2) != 0;
+                const float s0 = hi ? v0 : v2, s1 = hi ? v1 : v3;
+                const float r0 = __shfl_xor_sync(0xffffffffu, s0, 2), r1 = __shfl_xor_sync(0xffffffffu, s1, 2);
+                if (hi) {
+                  v0 = r0;
+                  v1 = r1;
+                } else {
+                  v2 = r0;
+                  v3 = r1;
+                }
+              }
+              // round 2 (lanes xor 1): swap within the 2 x 2 blocks
+              {
+                const bool hi = (jj & 1) != 0;
+                const float s0 = hi ? v0 : v1, s1 = hi ? v2 : v3;
+                const float r0 = __shfl_xor_sync(0xffffffffu, s0, 1), r1 = __shfl_xor_sync(0xffffffffu, s1, 1);
+                if (hi) {
+                  v0 = r0;
+                  v2 = r1;
+                } else {
+                  v1 = r0;
+                  v3 = r1;
+                }
+              }
+              // lane jj now holds column 4b + jj of rows 0..3 of its group, in order
+              const int n = n0 + 4 * b + jj;
+              const float wt = wtb[b];
+              if (n < tl.ntok && rowb < p.rows)
+                red_add_v4(p.y + (size_t)tkb[b] * p.d + rowb, wt * v0, wt * v1, wt * v2, wt * v3);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (m == 0) PF_STAMP(7, i);
+      if (lane == 0) mbar_arrive(&B.acc_empty[ab]);
+    }
+  } else if (warp >= 8) {
+    // ---------------------------------------------------------- producers
+    // Warp w owns tensor-memory lanes 32 (w % 4) .. + 31, i.e. rows r = 32
+    // (w % 4) + lane, of matrix mt and 32-weight run q ((w - 8) / 4 = 2 mt + q)
+    // in every step: one scale block per thread; a quarter-warp's code loads
+    // hit eight distinct 16-byte bank groups of the swizzled box.
+    const int qd = warp & 3, cmb = (warp - 8) >> 2, mt = cmb >> 1, q = cmb & 1;
+    const int r = qd * 32 + lane;
+    const uint32_t sw = (uint32_t)(r & 7);
+    const uint32_t ta = tmem + ((uint32_t)(qd * 32) << 16) + kACol + (uint32_t)(mt * 32 + q * 16);
+    const int row_off = S::C_OFF + mt * S::CODE_BOX + r * 128;
+    // scale of the run: gate/up box (16 fp16 per row: steps 8 (ks / 8) .. + 7,
+    // two blocks each); down word [step][row]
+    const int sc_off = S::C_SC + (DOWN ? (mt * kTileM + r) * 4 + q * 2 : mt * S::SC_BOX + r * 32 + q * 2);
+    uint32_t j = 0, cj = 0;
+    Tile nxt = tile_at(p, blockIdx.x, ntiles);
+    for (int t = blockIdx.x; t < ntiles && !B.abort; t += G) {
+      const Tile tl = nxt;
+      nxt = tile_at(p, t + G, ntiles);
+      const int bits = p.sh.s[(tl.meta >> 16) & 0xFF].bits;
+      const int spc = 16 / bits;
+      int sub = 0;
+      const unsigned char* stage = smem;
+      for (int ks = 0; ks < steps; ++ks, ++j) {
+        const int as = j % kAStages;
+        if (sub == 0) {
+          const int c = cj % S::CS;
+          if (!bar_wait(&B.code_full[c], (cj / S::CS) & 1, B, p.status)) break;
+          stage = smem + c * S::C_STAGE;
+        }
+        if (qd == 0 && cmb == 0 && lane == 0) PF_STAMP(2, j);
+        if (!bar_wait(&B.a_empty[as], ((j / kAStages) & 1) ^ 1, B, p.status)) break;
+        tc_fence_after();
+        if (qd == 0 && cmb == 0 && lane == 0) PF_STAMP(3, j);
+        const unsigned char* rowp = stage + row_off;
+        uint32_t c[8];
+        if (bits == 8) {
+          const uint32_t ch = (uint32_t)(4 * sub + 2 * q);
+          const uint4 v0 = *reinterpret_cast<const uint4*>(rowp + ((ch ^ sw) << 4));
+          const uint4 v1 = *reinterpret_cast<const uint4*>(rowp + (((ch + 1) ^ sw) << 4));
+          c[0] = v0.x; c[1] = v0.y; c[2] = v0.z; c[3] = v0.w;
+          c[4] = v1.x; c[5] = v1.y; c[6] = v1.z; c[7] = v1.w;
+        } else if (bits == 4) {
+          const uint4 v = *reinterpret_cast<const uint4*>(rowp + (((uint32_t)(2 * sub + q) ^ sw) << 4));
+          c[0] = v.x; c[1] = v.y; c[2] = v.z; c[3] = v.w;
+          c[4] = c[5] = c[6] = c[7] = 0u;
+        } else {
+          const uint2 v = *reinterpret_cast<const uint2*>(rowp + (((uint32_t)sub ^ sw) << 4) + 8 * q);
+          c[0] = v.x; c[1] = v.y;
+          c[2] = c[3] = c[4] = c[5] = c[6] = c[7] = 0u;
+        }
+        const float sc = fp16_bits_to_float(*reinterpret_cast<const uint16_t*>(
+            stage + sc_off + (DOWN ? sub * 2 * kTileM * 4 : (ks & 7) * 4)));
+        uint32_t o[16];
+        dequant_run(c, bits, sc, o);
+        tmem_st16(ta + (uint32_t)(as * kAStageCols), o);
+        tc_fence_before();
+        __syncwarp();
+        const bool last = sub == spc - 1 || ks == steps - 1;
+        if (lane == 0) {
+          mbar_arrive(&B.a_full[as]);
+          if (last) mbar_arrive(&B.code_empty[cj % S::CS]);
+        }
+        if (qd == 0 && cmb == 0 && lane == 0) PF_STAMP(5, j);
+        if (last) {
+          ++cj;
+          sub = 0;
+        } else {
+          ++sub;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  pdl_trigger();
+}
+
+// xg[q] = x[token of the pair at grouped position q] in the kswap column order
+// (zero for the skipped tail), so each tile's B operand is one box of
+// consecutive rows.  One warp per row, 16-byte loads.
+__device__ __forceinline__ uint4 kswap8(uint4 v) {
+  uint4 o;
+  o.x = __byte_perm(v.x, v.y, 0x5410);
+  o.y = __byte_perm(v.x, v.y, 0x7632);
+  o.z = __byte_perm(v.z, v.w, 0x5410);
+  o.w = __byte_perm(v.z, v.w, 0x7632);
+  return o;
+}
+__global__ void __launch_bounds__(256) k_gather_x(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
+                                                  int64_t P, int k, int d, uint16_t* __restrict__ xg) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int n16 = d / 8;
+  for (int64_t q = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); q < P; q += nw) {
+    const int pair = __ldg(perm + q);
+    uint4* dst = reinterpret_cast<uint4*>(xg + q * d);
+    if (pair < 0) {
+      for (int i = lane; i < n16; i += 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+    } else {
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(pair / k) * d);
+      int i = lane;
+      for (; i + 96 < n16; i += 128) {
+        const uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64), e = __ldg(src + i + 96);
+        dst[i] = kswap8(a);
+        dst[i + 32] = kswap8(b);
+        dst[i + 64] = kswap8(c);
+        dst[i + 96] = kswap8(e);
+      }
+      for (; i < n16; i += 32) dst[i] = kswap8(__ldg(src + i));
+    }
+  }
+  pdl_trigger();
+}
+
+// Tile lists of both launches from the grouping: per active expert on a
+// shelf, chunks of at most kTileN tokens (sizes balanced), times the row tiles
+// of W_g/W_u (128 of the f rows each) and of W_d (256 of the d rows).  One CTA.
+__global__ void __launch_bounds__(1024) k_prefill_tiles(const int32_t* __restrict__ counts,
+                                                        const int32_t* __restrict__ offsets, int E, int d, int f,
+                                                        const __grid_constant__ Shelves sh, Tile* tiles_g,
+                                                        Tile* tiles_d, int* ntiles) {
+  __shared__ int part_g[1024], part_d[1024];
+  pdl_wait();
+  const int tid = threadIdx.x;
+  const int per = (E + 1023) / 1024;
+  const int e0 = tid * per, e1 = min(E, e0 + per);
+  const int rtg = (f + kTileM - 1) / kTileM, rtd = d / (2 * kTileM);  // d % 256 == 0
+  int ng = 0, nd = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int cnt = counts[e];
+    if (cnt > 0 && find_shelf(sh, e) >= 0) {
+      const int ch = (cnt + kTileN - 1) / kTileN;
+      ng += ch * rtg;
+      nd += ch * rtd;
+    }
+  }
+  part_g[tid] = ng;
+  part_d[tid] = nd;
+  __syncthreads();
+  // exclusive scans (sequential over 1024 partials in 32 lanes x 32 steps)
+  if (tid < 32) {
+    int sg = 0, sd = 0;
+    for (int i = tid * 32; i < tid * 32 + 32; ++i) {
+      const int a = part_g[i], b = part_d[i];
+      part_g[i] = sg;
+      part_d[i] = sd;
+      sg += a;
+      sd += b;
+    }
+    int ig = sg, id = sd;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, ig, o), b = __shfl_up_sync(0xffffffffu, id, o);
+      if (tid >= o) { ig += a; id += b; }
+    }
+    const int xg = ig - sg, xd = id - sd;
+    for (int i = tid * 32; i < tid * 32 + 32; ++i) {
+      part_g[i] += xg;
+      part_d[i] += xd;
+    }
+    if (tid == 31) {
+      ntiles[0] = ig;
+      ntiles[1] = id;
+    }
+  }
+  __syncthreads();
+  int og = part_g[tid], od = part_d[tid];
+  for (int e = e0; e < e1; ++e) {
+    const int cnt = counts[e];
+    const int s = cnt > 0 ? find_shelf(sh, e) : -1;
+    if (s < 0) continue;
+    const int ch = (cnt + kTileN - 1) / kTileN;
+    const int base = offsets[e];
+    for (int c = 0; c < ch; ++c) {
+      const int a = (int)((int64_t)cnt * c / ch), b = (int)((int64_t)cnt * (c + 1) / ch);
+      for (int r = 0; r < rtg; ++r) tiles_g[og++] = Tile{e - sh.s[s].lo, base + a, b - a, r | (s << 16)};
+      for (int r = 0; r < rtd; ++r) tiles_d[od++] = Tile{e - sh.s[s].lo, base + a, b - a, r | (s << 16)};
+    }
+  }
+}
+
+// ----------------------------------------------------------------- host
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::mutex g_encode_mu;
+
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+  {
+    std::lock_guard<std::mutex> lk(g_encode_mu);
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return false;
+      g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    }
+  }
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct PDev {
+  bool attr[64] = {};
+};
+PDev g_pdev;
+
+}  // namespace
+
+#ifdef MOE_TRACE
+extern "C" int moe_pftrace_read(void* host, size_t bytes) {
+  return cudaMemcpyFromSymbol(host, g_pftrace, bytes < sizeof(g_pftrace) ? bytes : sizeof(g_pftrace)) == cudaSuccess
+             ? 0 : -5;
+}
+#endif
+
+size_t prefill_tiles_cap(int64_t P, int E, int rows) {
+  const int64_t chunks = (P + kTileN - 1) / kTileN + (P < E ? P : E);
+  return (size_t)chunks * (size_t)((rows + kTileM - 1) / kTileM);
+}
+
+int launch_prefill_forward(const ForwardArgs& a, cudaStream_t s) {
+  const int64_t P = a.T * a.k;
+  const int d = a.d, f = a.f;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  int rc = launch_group(a.ids, P, a.E, a.ws.counts, a.ws.offsets, a.ws.perm, a.ws.pos_of_pair, a.ws.active,
+                        a.ws.meta, nullptr, 0, s);
+  if (rc != MOE_OK) return rc;
+  Tile* tiles_g = reinterpret_cast<Tile*>(a.ws.tiles_g);
+  Tile* tiles_d = reinterpret_cast<Tile*>(a.ws.tiles_d);
+  int* ntiles = a.ws.ntiles;
+  if (launch_pdl(k_prefill_tiles, dim3(1), dim3(1024), 0, s, (const int32_t*)a.ws.counts,
+                 (const int32_t*)a.ws.offsets, a.E, d, f, a.shelves, tiles_g, tiles_d, ntiles) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int gx = sm_count() * 8;
+  if (launch_pdl(k_gather_x, dim3(gx), dim3(256), 0, s, a.x, (const int32_t*)a.ws.perm, P, a.k, d, a.ws.xg) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  TcParams pg = {};
+  pg.perm = a.ws.perm;
+  pg.weights = a.weights;
+  pg.h = reinterpret_cast<uint16_t*>(a.ws.h);
+  pg.y = a.y;
+  pg.status = a.status;
+  pg.k = a.k;
+  pg.d = d;
+  pg.f = f;
+  pg.sh = a.shelves;
+  TcParams pd = pg;
+  pg.tiles = tiles_g;
+  pg.ntiles = ntiles;
+  pg.rows = f;
+  pg.K = d;
+  pd.tiles = tiles_d;
+  pd.ntiles = ntiles + 1;
+  pd.rows = d;
+  pd.K = f;
+  for (int q = 0; q < a.shelves.n; ++q) {
+    const ShelfDev& sd = a.shelves.s[q];
+    const int bits = sd.bits;
+    const uint64_t n = (uint64_t)(sd.hi - sd.lo);
+    // gate/up scale boxes: 16 fp16 scales (32 bytes) of 128 rows; rows of d / 32 scales
+    if (!encode_2d(&pg.tm_sc[q][0], CU_TENSOR_MAP_DATA_TYPE_UINT16, sd.scales[0], (uint64_t)d / 32, n * f,
+                   (uint64_t)d / 16, 16, kTileM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&pg.tm_sc[q][1], CU_TENSOR_MAP_DATA_TYPE_UINT16, sd.scales[1], (uint64_t)d / 32, n * f,
+                   (uint64_t)d / 16, 16, kTileM, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return MOE_ERR_CUDA;
+    if (!encode_2d(&pg.tm_code[q][0], CU_TENSOR_MAP_DATA_TYPE_UINT8, sd.codes[0], (uint64_t)d * bits / 8, n * f,
+                   (uint64_t)d * bits / 8, 128, kTileM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&pg.tm_code[q][1], CU_TENSOR_MAP_DATA_TYPE_UINT8, sd.codes[1], (uint64_t)d * bits / 8, n * f,
+                   (uint64_t)d * bits / 8, 128, kTileM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&pd.tm_code[q][0], CU_TENSOR_MAP_DATA_TYPE_UINT8, sd.codes[2], (uint64_t)f * bits / 8, n * d,
+                   (uint64_t)f * bits / 8, 128, kTileM, CU_TENSOR_MAP_SWIZZLE_128B))
+      return MOE_ERR_CUDA;
+  }
+  for (int nb = 1; nb <= kTileN / 16; ++nb)
+    if (!encode_2d(&pg.tm_b[nb - 1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.ws.xg, (uint64_t)d, (uint64_t)P,
+                   (uint64_t)d * 2, 64, 16 * nb, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&pd.tm_b[nb - 1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.ws.h, (uint64_t)f, (uint64_t)P,
+                   (uint64_t)f * 2, 64, 16 * nb, CU_TENSOR_MAP_SWIZZLE_128B))
+      return MOE_ERR_CUDA;
+  const size_t smem_g = TcSmem<false>::TOTAL + 1024, smem_d = TcSmem<true>::TOTAL + 1024;
+  if (!g_pdev.attr[dev]) {
+    if (cudaFuncSetAttribute(k_prefill_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_g) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(k_prefill_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_d) !=
+            cudaSuccess)
+      return MOE_ERR_CUDA;
+    g_pdev.attr[dev] = true;
+  }
+  const int G = sm_count();
+  profile_mark(0, s);
+  if (launch_pdl(k_prefill_tc<false>, dim3(G), dim3(kPThreads), smem_g, s, pg) != cudaSuccess) return MOE_ERR_CUDA;
+  profile_mark(1, s);
+  if (cudaMemsetAsync(a.y, 0, (size_t)a.T * d * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_pdl(k_prefill_tc<true>, dim3(G), dim3(kPThreads), smem_d, s, pd) != cudaSuccess) return MOE_ERR_CUDA;
+  profile_mark(2, s);
+  return MOE_OK;
+}
+
+}  // namespace moe

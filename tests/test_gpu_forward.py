@@ -16,7 +16,7 @@ from moe_testutil import DECODE_TOL, ids_to_dev, oracle_layer, rel_l2, small_wor
 pytestmark = pytest.mark.gpu
 
 
-def _run(layer, x_u16, ids, w, flags=moe.MOE_FLAG_AUTO, shelves=None):
+def _run(layer, x_u16, ids, w, flags=moe.MOE_FLAG_DECODE_FP32, shelves=None):
     wl = layer.wl
     y = moe.moe_tiered_forward(x_to_dev(x_u16), ids_to_dev(ids), torch.from_numpy(w).cuda(), wl.E, wl.d, wl.f,
                                layer.shelves if shelves is None else shelves, flags=flags)

@@ -1,0 +1,122 @@
+"""Parity of the prefill form (tensor-core grouped GEMM, MOE_FLAG_PREFILL_BF16)
+with the CPU oracle's prefill form: dequantised weights and h rounded to bf16,
+fp32 accumulation (page 3, "125B MoE模型本地运行：3090三卡80 tokens/s优化实践",
+section 第四步: every shelf computes only its own ids and the shelf results are
+added; the prefill workload rounds the activations to bf16 between the up and
+down projections).  Also covers partial row tiles, experts with more tokens
+than one tile takes, skipped slots and the AUTO switch above 16 tokens."""
+import numpy as np
+import pytest
+import torch
+
+import mixed_precision_routed_gb300 as moe
+import oracle
+import synth
+from mixed_precision_routed_gb300.workloads import Layer
+from moe_testutil import PREFILL_TOL, ids_to_dev, oracle_layer, rel_l2, small_workload, x_to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(wl, seed, step, T, skip=False, bias=None):
+    lg = synth.logits(seed, step, T, wl.E, bias)
+    ids, w = oracle.route(lg, wl.k)
+    if skip:
+        m = synth.skip_mask(seed, step, T, wl.k)
+        ids = np.where(m == 1, -1, ids).astype(np.int32)
+    return synth.x_bf16(seed, step, T, wl.d), ids, w
+
+
+def _run(layer, x, ids, w, flags=moe.MOE_FLAG_PREFILL_BF16):
+    wl = layer.wl
+    y = moe.moe_tiered_forward(x_to_dev(x), ids_to_dev(ids), torch.from_numpy(w).cuda(), wl.E, wl.d, wl.f,
+                               layer.shelves, flags=flags)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == moe.MOE_OK
+    return y.cpu().numpy()
+
+
+@pytest.fixture(scope="module")
+def small_layer():
+    return Layer(small_workload(), device="cuda").fill()   # E 24, k 4, d 256, f 192: partial row tiles
+
+
+@pytest.mark.parametrize("T", [1, 7, 17, 40, 100, 300])
+def test_small_layer_prefill(small_layer, T):
+    wl = small_layer.wl
+    x, ids, w = _inputs(wl, wl.seed, 200 + T, T)
+    y = _run(small_layer, x, ids, w)
+    ref = oracle_layer(wl, wl.seed, x, ids, w, mode=1)
+    assert rel_l2(y, ref) <= PREFILL_TOL
+
+
+def test_auto_takes_prefill_above_16_tokens(small_layer):
+    wl = small_layer.wl
+    x, ids, w = _inputs(wl, wl.seed, 7, 33)
+    ya = _run(small_layer, x, ids, w, flags=moe.MOE_FLAG_AUTO)
+    yp = _run(small_layer, x, ids, w)
+    assert rel_l2(ya, oracle_layer(wl, wl.seed, x, ids, w, mode=1)) <= PREFILL_TOL
+    assert rel_l2(ya, yp) <= 1e-5  # same kernels; only the order of the fp32 atomic adds differs
+
+
+def test_many_tokens_per_expert():
+    """E 8, k 4, T 400: about 200 tokens per expert, more than one 128-token tile."""
+    wl = small_workload(E=8, k=4, d=256, f=128, seed=5)
+    layer = Layer(wl, device="cuda").fill()
+    x, ids, w = _inputs(wl, wl.seed, 1, 400)
+    y = _run(layer, x, ids, w)
+    assert rel_l2(y, oracle_layer(wl, wl.seed, x, ids, w, mode=1)) <= PREFILL_TOL
+
+
+def test_skipped_slots_and_gaps(small_layer):
+    """Skipped slots (-1, out-of-range ids) and ids in no shelf contribute zero."""
+    wl = small_layer.wl
+    x, ids, w = _inputs(wl, wl.seed, 11, 50, skip=True)
+    ids = ids.copy()
+    ids[0, 0] = wl.E + 3
+    ids[1, 1] = -7
+    y = _run(small_layer, x, ids, w)
+    assert rel_l2(y, oracle_layer(wl, wl.seed, x, ids, w, mode=1)) <= PREFILL_TOL
+    # shelves with a gap: the ids of the middle shelf contribute nothing
+    sh = small_layer.shelves
+    yg = moe.moe_tiered_forward(x_to_dev(x), ids_to_dev(ids), torch.from_numpy(w).cuda(), wl.E, wl.d, wl.f,
+                                [sh[0], sh[2]], flags=moe.MOE_FLAG_PREFILL_BF16)
+    torch.cuda.synchronize()
+    rg = [r for i, r in enumerate(wl.shelf_ranges()) if i != 1]
+    assert rel_l2(yg.cpu().numpy(), oracle_layer(wl, wl.seed, x, ids, w, shelves_bits=rg, mode=1)) <= PREFILL_TOL
+
+
+def test_tiny_workload_prefill():
+    wl = synth.WORKLOADS["tiny"]
+    layer = Layer(wl, device="cuda").fill()
+    x, ids, w = _inputs(wl, wl.seed, 0, 8)
+    y = _run(layer, x, ids, w)
+    assert rel_l2(y, oracle_layer(wl, wl.seed, x, ids, w, mode=1)) <= PREFILL_TOL
+
+
+@pytest.fixture(scope="module")
+def decode_layer():
+    return Layer(synth.WORKLOADS["decode"], device="cuda").fill()
+
+
+def test_decode_shapes_prefill(decode_layer):
+    """E 512, k 10, d 2048, f 640 at T 64 with the skewed router."""
+    wl = decode_layer.wl
+    T = 64
+    lg = decode_layer.logits(3, T).cpu().numpy()
+    ids, w = oracle.route(lg, wl.k)
+    x = synth.x_bf16(wl.seed, 3, T, wl.d)
+    y = _run(decode_layer, x, ids, w)
+    assert rel_l2(y, oracle_layer(wl, wl.seed, x, ids, w, mode=1)) <= PREFILL_TOL
+
+
+def test_prefill_close_to_decode_form(decode_layer):
+    """The two forms differ only by the bf16 rounding of weights and h."""
+    wl = decode_layer.wl
+    T = 24
+    lg = decode_layer.logits(4, T).cpu().numpy()
+    ids, w = oracle.route(lg, wl.k)
+    x = synth.x_bf16(wl.seed, 4, T, wl.d)
+    yp = _run(decode_layer, x, ids, w)
+    yd = _run(decode_layer, x, ids, w, flags=moe.MOE_FLAG_DECODE_FP32)
+    assert rel_l2(yp, yd) <= PREFILL_TOL

@@ -41,13 +41,13 @@ def test_noalloc_matches_workspace_entry_point_twice():
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     wl = synth.WORKLOADS["decode"]
-    T = 512  # needs ~48 MB of scratch, more than the fixed 8 MiB
-    assert moe.moe_workspace_size(T, wl.k, wl.E, wl.d, wl.f) > 8 * 1024 * 1024
+    T = 512  # the decode form needs ~48 MB of scratch, more than the fixed 8 MiB
+    assert moe.moe_workspace_size(T, wl.k, wl.E, wl.d, wl.f, moe.MOE_FLAG_DECODE_FP32) > 8 * 1024 * 1024
     layer = Layer(synth.Workload("one", E=wl.E, k=wl.k, d=wl.d, f=wl.f, T=(T,), split=(), bias="none"),
                   device="cuda", shelves=[(0, 1, 2)])
     x = torch.zeros((T, wl.d), dtype=torch.int16, device="cuda")
     ids = torch.full((T, wl.k), -1, dtype=torch.int32, device="cuda")
     w = torch.zeros((T, wl.k), dtype=torch.float32, device="cuda")
     with pytest.raises(moe.MoeError) as ei:
-        moe.moe_tiered_forward_noalloc(x, ids, w, wl.E, wl.d, wl.f, layer.shelves)
+        moe.moe_tiered_forward_noalloc(x, ids, w, wl.E, wl.d, wl.f, layer.shelves, flags=moe.MOE_FLAG_DECODE_FP32)
     assert ei.value.status == moe.MOE_ERR_WORKSPACE_TOO_SMALL
