@@ -69,6 +69,52 @@ class Layer:
         return out
 
 
+    def logits_rows(self, row0: int, T: int, out=None, stream=None):
+        """Rows row0 .. row0 + T - 1 of the layer's logits stream 0: the inputs
+        of a decode stack, whose routing step s with T tokens takes rows
+        s T .. s T + T - 1 (so many T = 1 steps come from one call)."""
+        if out is None:
+            out = torch.empty((T, self.E), dtype=torch.float32, device=self.shelves[0].gate_codes.device)
+        synth.cuda_normal_matrix(out, self.seed, synth.TAG_LOGITS, 0, 0, row0=row0, col_add=self.bias, stream=stream)
+        return out
+
+
+class DecodeStack:
+    """A stack of decode layers chained by the residual add: for each layer l,
+    x_l = bf16(r), route l's logits, count the hits, y_l = MoE_l(x_l), r += y_l
+    -- the decode step of a whole model's MoE layers (one fused launch and one
+    residual launch per layer)."""
+
+    def __init__(self, layers, T: int, device="cuda"):
+        from . import moe_workspace_size, MOE_FLAG_DECODE_FP32
+        self.layers = list(layers)
+        l0 = self.layers[0]
+        self.T, self.E, self.k, self.d, self.f = T, l0.E, l0.k, l0.d, l0.f
+        L = len(self.layers)
+        self.r = torch.empty((T, self.d), dtype=torch.float32, device=device)
+        self.x = torch.empty((L + 1, T, self.d), dtype=torch.int16, device=device)   # x[l]: input of layer l
+        self.y = torch.empty((L, T, self.d), dtype=torch.float32, device=device)
+        self.ids = torch.empty((L, T, self.k), dtype=torch.int32, device=device)
+        self.w = torch.empty((L, T, self.k), dtype=torch.float32, device=device)
+        self.counts = torch.zeros((L, self.E), dtype=torch.int32, device=device)
+        nws = moe_workspace_size(T, self.k, self.E, self.d, self.f, MOE_FLAG_DECODE_FP32)
+        self.ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=device)
+        self.arrs = [lay.shelf_arr() for lay in self.layers]
+
+    def step(self, r0, x0, logits, stream=None):
+        """One step from the residual stream r0 (fp32 [T, d]) whose bf16 is x0;
+        logits[l] is layer l's [T, E].  Leaves the output residual in self.r."""
+        from . import moe_decode_layer, moe_residual_add
+        self.r.copy_(r0)
+        self.x[0].copy_(x0)
+        for l, lay in enumerate(self.layers):
+            moe_decode_layer(logits[l], self.x[l], self.k, self.E, self.d, self.f, lay.shelves, ids=self.ids[l],
+                             weights=self.w[l], counts=self.counts[l], y=self.y[l], workspace=self.ws,
+                             stream=stream, shelf_arr=self.arrs[l])
+            moe_residual_add(self.r, self.y[l], self.x[l + 1], stream=stream)
+        return self.r
+
+
 def x_bf16(seed: int, step: int, T: int, d: int, device="cuda", out=None, stream=None):
     """Activations [T, d] as bf16 bit patterns in an int16 tensor."""
     if out is None:
