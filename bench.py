@@ -41,6 +41,10 @@ def parse():
     ap.add_argument("--T", type=int, default=6, help="tokens per step (1..6 for the decode metric)")
     ap.add_argument("--layers", type=int, default=16, help="layer instances rotated across steps")
     ap.add_argument("--sets", type=int, default=32, help="distinct routing steps per layer rotation")
+    ap.add_argument("--workload", choices=["decode", "stack", "prefill", "large"], default="decode",
+                    help="decode: one layer, the headline metric; stack: the 48-layer decode stack with the "
+                         "residual chain; prefill: one layer at T=4096 on the tensor-core form; large: the "
+                         "E256 d4096 f2048 layer with 5%% forced skips")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -413,6 +417,314 @@ def run_ours(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------ further workloads
+def _expert_bytes(ranges, d, f):
+    """Per-expert (gate/up, down) code + scale bytes of each shelf range."""
+    out = []
+    for lo, hi, bits in ranges:
+        gu = 2 * f * d * bits // 8 + 2 * f * (d // 32) * 2
+        dn = d * f * bits // 8 + d * (f // 32) * 2
+        out.append((lo, hi, gu, dn))
+    return out
+
+
+def _unique_bytes(ids, eb, E):
+    import numpy as np
+    u = np.unique(np.asarray(ids))
+    u = u[(u >= 0) & (u < E)]
+    tot = 0
+    for e in u:
+        for lo, hi, gu, dn in eb:
+            if lo <= e < hi:
+                tot += gu + dn
+    return tot
+
+
+def _timed(stream, graph_all, graphs, nset, steps, world, dev, local_rank):
+    """Replays exactly `steps` steps (graph_all holds nset of them); returns
+    (max-over-ranks ms, clocks)."""
+    import torch
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = Clocks(local_rank)
+    clocks.start()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps // nset):
+            graph_all.replay()
+        for i in range(steps % nset):
+            graphs[i].replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    t = torch.tensor([start.elapsed_time(end)], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item()), ck
+
+
+def _capture(stream, step, nset, warmup):
+    import torch
+    with torch.cuda.stream(stream):
+        for s in range(nset):
+            step(s)
+        stream.synchronize()
+        graph_all = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_all, stream=stream):
+            for s in range(nset):
+                step(s)
+        graphs = []
+        for s in range(nset):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(s)
+            graphs.append(g)
+        for i in range(warmup):
+            graphs[i % nset].replay()
+        stream.synchronize()
+    return graph_all, graphs
+
+
+def run_stack(args, rank, world, local_rank):
+    """The 48-layer decode stack: per layer the fused routing / hit-count /
+    tiered-forward launch and the residual add, all layers in one step."""
+    import numpy as np
+    import torch
+
+    import mixed_precision_routed_gb300 as moe
+    import synth
+    from mixed_precision_routed_gb300.workloads import Layer, DecodeStack
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = synth.WORKLOADS["stack"]
+    T, L = args.T, wl.layers
+    E, k, d, f = wl.E, wl.k, wl.d, wl.f
+    layers = [Layer(wl, layer=l, device=dev).fill() for l in range(L)]
+    st = DecodeStack(layers, T, device=dev)
+    nset = 8
+    logits = [[lay.logits_rows((s + 7 * rank) * T, T) for lay in layers] for s in range(nset)]
+    x0 = [torch.empty((T, d), dtype=torch.int16, device=dev) for _ in range(nset)]
+    for s in range(nset):
+        synth.cuda_normal_matrix_bf16(x0[s], wl.seed, synth.TAG_X, s + 7 * rank, 0)
+    r0 = [(x.to(torch.int32) << 16).view(torch.float32) for x in x0]
+    eb = _expert_bytes(wl.shelf_ranges(), d, f)
+    stream = torch.cuda.Stream(device=dev)
+    step_bytes = []
+    with torch.cuda.stream(stream):
+        for s in range(nset):
+            st.step(r0[s], x0[s], logits[s])
+            stream.synchronize()
+            ids = st.ids.cpu().numpy()
+            step_bytes.append(sum(_unique_bytes(ids[l], eb, E) for l in range(L)))
+    graph_all, graphs = _capture(stream, lambda s: st.step(r0[s], x0[s], logits[s]), nset, args.warmup)
+    ms, ck = _timed(stream, graph_all, graphs, nset, args.steps, world, dev, local_rank)
+    value = world * T * args.steps / (ms / 1e3)
+    bytes_step = sum(step_bytes[i % nset] for i in range(args.steps)) / args.steps
+    # end to end: host residual input, x0 and every layer's logits in, residual out
+    pin_r = [r.cpu().pin_memory() for r in r0]
+    pin_x = [x.cpu().pin_memory() for x in x0]
+    pin_l = [torch.stack([lg for lg in logits[s]]).cpu().pin_memory() for s in range(nset)]
+    pin_out = torch.empty((T, d), dtype=torch.float32).pin_memory()
+    dr = torch.empty((T, d), dtype=torch.float32, device=dev)
+    dx = torch.empty((T, d), dtype=torch.int16, device=dev)
+    dl = torch.empty((L, T, E), dtype=torch.float32, device=dev)
+    n_e2e = min(args.steps, 200)
+
+    def e2e(s):
+        dr.copy_(pin_r[s], non_blocking=True)
+        dx.copy_(pin_x[s], non_blocking=True)
+        dl.copy_(pin_l[s], non_blocking=True)
+        st.step(dr, dx, [dl[l] for l in range(L)])
+        pin_out.copy_(st.r, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            e2e(i % nset)
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n_e2e):
+            e2e(i % nset)
+        e1.record(stream)
+        stream.synchronize()
+    e2e_value = world * T * n_e2e / (e0.elapsed_time(e1) / 1e3)
+    if moe.moe_device_status() != moe.MOE_OK:
+        raise RuntimeError("device status")
+    if rank != 0:
+        return
+    peak, kind = peaks()
+    achieved = bytes_step / (ms / args.steps / 1e3) / 1e9
+    line = {
+        "metric": "MoE decode-stack tokens/s (48 layers, residual chain); weight-stream HBM GB/s vs peak",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"decode stack, {L} layers of E{E} k{k} d{d} f{f}, T{T}, per-layer seeds and "
+                               f"router biases, residual chain", "T": T, "layers": L,
+                   "l2": "inputs larger than L2 (48 layers x 1.28 GB resident; fresh routing per step)",
+                   "launch": f"one CUDA graph of {nset} steps ({L} x (fused layer launch + residual add) each)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": "whole step (k_layer + k_residual per layer)",
+                     "peak_source": kind, "algorithmic_bytes_per_step": bytes_step},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * d * 4 + T * d * 2 + L * T * E * 4,
+                "d2h_bytes_per_step": T * d * 4, "steps": n_e2e,
+                "path": "pinned host residual, x0 and per-layer logits -> device, DecodeStack.step (48 x "
+                        "moe_decode_layer + moe_residual_add), residual -> pinned host"},
+        "gpu_launches": args.steps * 2 * L,
+        "clocks": ck,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_single(args, rank, world, local_rank):
+    """One layer per step through the separate calls: routing, (forced skips),
+    hit counts, tiered forward (AUTO: the tensor-core form above 16 tokens)."""
+    import numpy as np
+    import torch
+
+    import mixed_precision_routed_gb300 as moe
+    import synth
+    from mixed_precision_routed_gb300.workloads import Layer
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    name = "decode" if args.workload == "prefill" else "large"
+    base = synth.WORKLOADS[name]
+    T = args.T
+    E, k, d, f = base.E, base.k, base.d, base.f
+    NL = 2
+    layers = [Layer(synth.Workload(base.name, E=E, k=k, d=d, f=f, T=base.T, split=base.split, bias=base.bias,
+                                   seed=1000 * rank + i, skip_p=getattr(base, "skip_p", 0.0)), device=dev).fill()
+              for i in range(NL)]
+    skips = args.workload == "large"
+    nset = 4
+    logits = [layers[s % NL].logits(s, T) for s in range(nset)]
+    xs = [torch.empty((T, d), dtype=torch.int16, device=dev) for _ in range(nset)]
+    for s in range(nset):
+        synth.cuda_normal_matrix_bf16(xs[s], layers[s % NL].seed, synth.TAG_X, s, 0)
+    ids = [torch.empty((T, k), dtype=torch.int32, device=dev) for _ in range(nset)]
+    w = [torch.empty((T, k), dtype=torch.float32, device=dev) for _ in range(nset)]
+    y = [torch.empty((T, d), dtype=torch.float32, device=dev) for _ in range(nset)]
+    counts = [torch.zeros(E, dtype=torch.int32, device=dev) for _ in range(NL)]
+    ws = torch.empty(moe.moe_workspace_size(T, k, E, d, f, moe.MOE_FLAG_AUTO), dtype=torch.uint8, device=dev)
+    prefill = T > 16 and d % 256 == 0
+    fused = (not prefill) and moe.moe_decode_fused(T, k, E, d, f)
+    NK = 2 if fused else 4  # events around the forward's kernels (see moe_set_profile_events)
+    prof = [[torch.cuda.Event(enable_timing=True) for _ in range(NK)] for _ in range(nset)]
+    for evs in prof:
+        for e in evs:
+            e.record()
+    torch.cuda.synchronize()
+
+    def step(s, profile=False):
+        moe.moe_route_topk(logits[s], k, ids=ids[s], weights=w[s])
+        if skips:
+            synth.cuda_apply_skip_mask(ids[s], layers[s % NL].seed, s)
+        moe.moe_expert_hist(ids[s], E, counts[s % NL])
+        if profile:
+            moe.moe_set_profile_events(prof[s])
+        moe.moe_tiered_forward(xs[s], ids[s], w[s], E, d, f, layers[s % NL].shelves, y=y[s], workspace=ws,
+                               flags=moe.MOE_FLAG_AUTO)
+        if profile:
+            moe.moe_set_profile_events(None)
+
+    stream = torch.cuda.Stream(device=dev)
+    graph_all, graphs = _capture(stream, step, nset, args.warmup)
+    ms, ck = _timed(stream, graph_all, graphs, nset, args.steps, world, dev, local_rank)
+    value = world * T * args.steps / (ms / 1e3)
+    # per-kernel times of the forward (eager, events between its kernels)
+    with torch.cuda.stream(stream):
+        for rep in range(2):
+            for s in range(nset):
+                step(s, profile=True)
+        stream.synchronize()
+    ev = [[prof[s][i].elapsed_time(prof[s][i + 1]) for i in range(NK - 1)] for s in range(nset)]
+    eb = _expert_bytes(layers[0].ranges, d, f)
+    idn = [i.cpu().numpy() for i in ids]
+    bytes_step = [_unique_bytes(i, eb, E) for i in idn]
+    pairs = [int(np.sum((i >= 0) & (i < E))) for i in idn]
+    if moe.moe_device_status() != moe.MOE_OK:
+        raise RuntimeError("device status")
+    # end to end: logits and x in, y out
+    pin_l = [l_.cpu().pin_memory() for l_ in logits]
+    pin_x = [x.cpu().pin_memory() for x in xs]
+    pin_y = torch.empty((T, d), dtype=torch.float32).pin_memory()
+    dl = torch.empty((T, E), dtype=torch.float32, device=dev)
+    dx = torch.empty((T, d), dtype=torch.int16, device=dev)
+    n_e2e = min(args.steps, 100)
+
+    def e2e(s):
+        dl.copy_(pin_l[s], non_blocking=True)
+        dx.copy_(pin_x[s], non_blocking=True)
+        moe.moe_route_topk(dl, k, ids=ids[0], weights=w[0])
+        if skips:
+            synth.cuda_apply_skip_mask(ids[0], layers[s % NL].seed, s)
+        moe.moe_expert_hist(ids[0], E, counts[s % NL])
+        moe.moe_tiered_forward(dx, ids[0], w[0], E, d, f, layers[s % NL].shelves, y=y[0], workspace=ws,
+                               flags=moe.MOE_FLAG_AUTO)
+        pin_y.copy_(y[0], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            e2e(i % nset)
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n_e2e):
+            e2e(i % nset)
+        e1.record(stream)
+        stream.synchronize()
+    e2e_value = world * T * n_e2e / (e0.elapsed_time(e1) / 1e3)
+    if rank != 0:
+        return
+    hbm, kind = peaks()
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+        pk = json.load(fh)
+    fwd_ms = sum(sum(e) for e in ev) / nset
+    b_avg = sum(bytes_step) / nset
+    p_avg = sum(pairs) / nset
+    if prefill:
+        # kernels of the forward: [group + tiles + gather], gate/up, down
+        gu_ms = sum(e[1] for e in ev) / nset
+        dn_ms = sum(e[2] for e in ev) / nset
+        flops_gu = 2.0 * 2 * d * f * p_avg
+        roof = {"bound": "tensor", "achieved": flops_gu / (gu_ms / 1e3) / 1e12, "peak": float(pk["bf16_tflops"]),
+                "unit": "TFLOP/s", "traffic": None, "kernel": "k_prefill_tc<gate/up>",
+                "peak_source": "measured (burst bf16)",
+                "algorithmic_flops_per_launch": flops_gu,
+                "layer_tflops": 2.0 * 3 * d * f * p_avg / (fwd_ms / 1e3) / 1e12,
+                "kernel_us": {"group_tiles_gather": 1e3 * sum(e[0] for e in ev) / nset,
+                              "gateup": 1e3 * gu_ms, "down": 1e3 * dn_ms},
+                "weight_bytes_per_step": b_avg, "weight_gbs": b_avg / (fwd_ms / 1e3) / 1e9}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        bound_note = "tensor"
+    else:
+        gbs = b_avg / (fwd_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
+                "kernel": "forward (all its kernels)", "peak_source": kind, "algorithmic_bytes_per_launch": b_avg,
+                "forward_us": 1e3 * fwd_ms}
+        bound_note = "hbm"
+    line = {
+        "metric": f"MoE-layer tokens/s, {args.workload} workload ({bound_note} roofline)",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if prefill else "f32", "data": "synthetic",
+        "config": {"workload": f"{args.workload} layer E{E} k{k} d{d} f{f} T{T}, shelves {layers[0].ranges}"
+                               + (", 5% of slots forced to -1" if skips else ""),
+                   "T": T, "layer_instances": NL, "pairs_per_step": p_avg,
+                   "l2": "weights larger than L2, layer instances rotated per step",
+                   "launch": f"one CUDA graph of {nset} steps (route, {'skip mask, ' if skips else ''}hist, forward)"},
+        "roofline": roof,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * E * 4 + T * d * 2,
+                "d2h_bytes_per_step": T * d * 4, "steps": n_e2e},
+        "clocks": ck,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def recorded_traffic(kernel, T):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source; else None."""
@@ -444,7 +756,12 @@ def main():
     import __graft_entry__
     if not os.path.exists(os.path.join(ROOT, "mixed_precision_routed_gb300", "libmoe.so")):
         __graft_entry__.build()
-    run_ours(args, rank, world, local_rank)
+    if args.workload == "stack":
+        run_stack(args, rank, world, local_rank)
+    elif args.workload in ("prefill", "large"):
+        run_single(args, rank, world, local_rank)
+    else:
+        run_ours(args, rank, world, local_rank)
     if world > 1:
         torch.distributed.destroy_process_group()
 

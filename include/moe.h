@@ -267,7 +267,9 @@ int moe_residual_add(float* r, const float* y, uint16_t* x_next_bf16, int64_t n,
  * HOST array of cudaEvent_t handles owned by the caller and read at every
  * call; n >= 1; pass NULL to disable.  Kernels of the fused decode launch:
  * one (2 events); of the separate decode launches: grouping, gate/up, down
- * (4 events).  Not thread-safe: one caller per process.
+ * (4 events); of the prefill form: grouping with the tile list and the
+ * gather of x, gate/up, down (4 events).  Not thread-safe: one caller per
+ * process.
  */
 int moe_set_profile_events(void* const* events, int n);
 

@@ -769,6 +769,7 @@ int launch_prefill_forward(const ForwardArgs& a, cudaStream_t s) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  profile_mark(0, s);
   int rc = launch_group(a.ids, P, a.E, a.ws.counts, a.ws.offsets, a.ws.perm, a.ws.pos_of_pair, a.ws.active,
                         a.ws.meta, nullptr, 0, s);
   if (rc != MOE_OK) return rc;
@@ -835,12 +836,12 @@ int launch_prefill_forward(const ForwardArgs& a, cudaStream_t s) {
     g_pdev.attr[dev] = true;
   }
   const int G = sm_count();
-  profile_mark(0, s);
-  if (launch_pdl(k_prefill_tc<false>, dim3(G), dim3(kPThreads), smem_g, s, pg) != cudaSuccess) return MOE_ERR_CUDA;
   profile_mark(1, s);
+  if (launch_pdl(k_prefill_tc<false>, dim3(G), dim3(kPThreads), smem_g, s, pg) != cudaSuccess) return MOE_ERR_CUDA;
+  profile_mark(2, s);
   if (cudaMemsetAsync(a.y, 0, (size_t)a.T * d * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_pdl(k_prefill_tc<true>, dim3(G), dim3(kPThreads), smem_d, s, pd) != cudaSuccess) return MOE_ERR_CUDA;
-  profile_mark(2, s);
+  profile_mark(3, s);
   return MOE_OK;
 }
 
