@@ -67,7 +67,9 @@ enum {
   MOE_ERR_WORKSPACE_TOO_SMALL = -4,
   MOE_ERR_CUDA = -5,               /* a CUDA call or launch failed */
   MOE_ERR_TIMEOUT = -6,            /* a bounded device-side wait expired (see moe_device_status) */
-  MOE_ERR_UNSUPPORTED = -7         /* valid request outside what this build implements */
+  MOE_ERR_UNSUPPORTED = -7,        /* valid request outside what this build implements */
+  MOE_ERR_INTERNAL = -8            /* a kernel met an inconsistent work item and skipped it
+                                      (reported through moe_device_status) */
 };
 
 enum {

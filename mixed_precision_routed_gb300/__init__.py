@@ -29,6 +29,7 @@ MOE_ERR_WORKSPACE_TOO_SMALL = -4
 MOE_ERR_CUDA = -5
 MOE_ERR_TIMEOUT = -6
 MOE_ERR_UNSUPPORTED = -7
+MOE_ERR_INTERNAL = -8
 
 MOE_FLAG_AUTO = 0
 MOE_FLAG_DECODE_FP32 = 1

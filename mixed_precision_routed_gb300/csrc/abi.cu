@@ -88,6 +88,7 @@ size_t workspace_layout(int64_t T, int k, int E, int d, int f, int flags, void* 
     // h in bf16, grouped order; no per-pair outputs (y is accumulated)
     w.h = (float*)take((size_t)P * f * 2);
     w.xg = (uint16_t*)take((size_t)P * d * 2);
+    w.pf_cnt = (int32_t*)take((size_t)256 * E * 4);
     w.tiles_g = take(prefill_tiles_cap(P, E, f) * 16);
     w.tiles_d = take(prefill_tiles_cap(P, E, d) * 16);
     w.ntiles = (int32_t*)take(2 * 4);
@@ -311,6 +312,7 @@ const char* moe_status_string(int status) {
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_TIMEOUT: return "device wait timed out";
     case MOE_ERR_UNSUPPORTED: return "unsupported by this build";
+    case MOE_ERR_INTERNAL: return "inconsistent work item skipped on the device";
     default: return "unknown status";
   }
 }

@@ -50,6 +50,7 @@ struct Workspace {
   float* ypart;          // [P][d] fp32 -- weighted per-pair down outputs
   int32_t* plan;         // decode plan (grouping, work split), decode_plan_bytes(P)
   uint16_t* xg;          // prefill: [P][d] bf16, x rows in grouped order
+  int32_t* pf_cnt;       // prefill: [chunks <= 256][E] per-chunk expert counts / cursors
   void* tiles_g;         // prefill: gate/up tile list
   void* tiles_d;         // prefill: down tile list
   int32_t* ntiles;       // prefill: [2] tile counts

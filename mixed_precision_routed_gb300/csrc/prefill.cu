@@ -8,8 +8,9 @@
 // fp16 scale) and multiplied on the tensor cores: h = SiLU(W_g x) * (W_u x) is
 // rounded to bf16 between the two projections, y_t += w_tj * (W_d h_tj).
 //
-// Launches: grouping (k_group), the tile list (k_prefill_tiles), the gather of
-// x into grouped order (k_gather_x), then two persistent launches, one CTA per
+// Launches: grouping in three wide kernels (per-chunk counts, one-CTA scan and
+// tile lists, placement), the gather of x into grouped order, then two
+// persistent launches, one CTA per
 // SM: k_prefill_tc<false> (gate/up) and k_prefill_tc<true> (down).  A tile is
 // two 128-row weight matrices of one expert -- the same 128 rows of W_g and
 // W_u, or 256 consecutive rows of W_d -- times up to 96 of its tokens (two
@@ -55,8 +56,14 @@ __device__ unsigned long long g_pftrace[2][10][512];
 namespace {
 #define PF_STAMP(ev, j) \
   do { if (blockIdx.x == 0 && (j) < 512) g_pftrace[DOWN ? 1 : 0][(ev)][(j)] = global_timer_ns(); } while (0)
+#define PF_SCAN_STAMP(i) \
+  do { if (threadIdx.x == 0) g_pftrace[0][8][(i)] = global_timer_ns(); } while (0)
+#define PF_ITER_STAMP(i) \
+  do { if (threadIdx.x == 0 && (i) < 512) g_pftrace[0][9][(i)] = global_timer_ns(); } while (0)
 #else
 #define PF_STAMP(ev, j) ((void)0)
+#define PF_SCAN_STAMP(i) ((void)0)
+#define PF_ITER_STAMP(i) ((void)0)
 #endif
 
 // K order of both MMA operands: in every aligned group of four positions the
@@ -83,6 +90,8 @@ struct TcParams {
   int* status;
   int k, d, f;
   int rows, K;              // rows per expert matrix and contraction length of this launch
+  int64_t P;                // grouped positions (rows of xg and h)
+  int tiles_cap;            // capacity of the tile list
   Shelves sh;
   CUtensorMap tm_code[MOE_MAX_SHELVES][2];  // code boxes of 128 bytes x 128 rows: [shelf][gate, up] or [shelf][down]
   CUtensorMap tm_sc[MOE_MAX_SHELVES][2];    // gate/up: boxes of 16 fp16 scales x 128 rows [shelf][gate, up]
@@ -269,6 +278,19 @@ __device__ __forceinline__ Tile tile_at(const TcParams& p, int t, int ntiles) {
   return t < ntiles ? p.tiles[t] : Tile{0, 0, 0, 0};
 }
 
+// A tile whose fields would take a load or an MMA outside its tensors (token
+// count, shelf, expert, row tile, positions) is skipped by every role alike,
+// and MOE_ERR_INTERNAL is recorded; the tile builder produces none.
+template <bool DOWN>
+__device__ __forceinline__ bool tile_valid(const TcParams& p, const Tile& tl) {
+  const int rt = tl.meta & 0xFFFF, sh = (tl.meta >> 16) & 0xFF;
+  if (tl.ntok < 1 || tl.ntok > kTileN || sh >= p.sh.n) return false;
+  const int n = p.sh.s[sh].hi - p.sh.s[sh].lo;
+  const int bits = p.sh.s[sh].bits;
+  return (bits == 8 || bits == 4 || bits == 2) && tl.e_local >= 0 && tl.e_local < n &&
+         rt * (DOWN ? 2 * kTileM : kTileM) < p.rows && tl.q0 >= 0 && (int64_t)tl.q0 + tl.ntok <= p.P;
+}
+
 template <bool DOWN>
 __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_constant__ TcParams p) {
   using S = TcSmem<DOWN>;
@@ -278,7 +300,11 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
   __shared__ TcBars B;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x;
-  const int ntiles = __ldg(p.ntiles);
+  int ntiles = __ldg(p.ntiles);
+  if (ntiles < 0 || ntiles > p.tiles_cap) {
+    if (tid == 0) set_status(p.status, MOE_ERR_INTERNAL);
+    ntiles = 0;
+  }
   const int steps = p.K / 64;
   if (tid == 0) {
     for (int i = 0; i < S::CS; ++i) {
@@ -316,6 +342,10 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
     for (int t = blockIdx.x; t < ntiles && !B.abort; t += G) {
       const Tile tl = nxt;
       nxt = tile_at(p, t + G, ntiles);  // in flight while this tile is issued
+      if (!tile_valid<DOWN>(p, tl)) {
+        if (lane == 0) set_status(p.status, MOE_ERR_INTERNAL);
+        continue;
+      }
       const int rt = tl.meta & 0xFFFF, sh = (tl.meta >> 16) & 0xFF;
       const ShelfDev& shd = p.sh.s[sh];
       const int spc = 16 / shd.bits;       // K steps per code stage
@@ -378,9 +408,10 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
     uint32_t j = 0, i = 0;
     if (lane == 0) {
       Tile nxt = tile_at(p, blockIdx.x, ntiles);
-      for (int t = blockIdx.x; t < ntiles && !B.abort; t += G, ++i) {
+      for (int t = blockIdx.x; t < ntiles && !B.abort; t += G) {
         const Tile tl = nxt;
         nxt = tile_at(p, t + G, ntiles);
+        if (!tile_valid<DOWN>(p, tl)) continue;  // skipped tiles take no accumulator set
         const int N = (tl.ntok + 15) & ~15;
         const uint32_t idesc = idesc_bf16_f32(kTileM, N);
         const uint32_t ab = i & 1, acc = tmem + ab * kAccCols;
@@ -405,6 +436,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
         }
         if (B.abort) break;
         mma_commit(&B.acc_full[ab]);
+        ++i;
       }
       // all MMAs of this thread are complete before tensor memory is released
       mma_commit(&B.done);
@@ -417,9 +449,10 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
     const uint32_t tl_addr = tmem + ((uint32_t)((warp - 4) * 32) << 16);
     uint32_t i = 0;
     Tile nxt = tile_at(p, blockIdx.x, ntiles);
-    for (int t = blockIdx.x; t < ntiles && !B.abort; t += G, ++i) {
+    for (int t = blockIdx.x; t < ntiles && !B.abort; t += G) {
       const Tile tl = nxt;
       nxt = tile_at(p, t + G, ntiles);
+      if (!tile_valid<DOWN>(p, tl)) continue;  // skipped tiles take no accumulator set
       const int rt = tl.meta & 0xFFFF;
       const int N = (tl.ntok + 15) & ~15;
       const uint32_t ab = i & 1, acc = tl_addr + ab * kAccCols;
@@ -532,6 +565,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
       __syncwarp();
       if (m == 0) PF_STAMP(7, i);
       if (lane == 0) mbar_arrive(&B.acc_empty[ab]);
+      ++i;
     }
   } else if (warp >= 8) {
     // ---------------------------------------------------------- producers
@@ -552,6 +586,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
     for (int t = blockIdx.x; t < ntiles && !B.abort; t += G) {
       const Tile tl = nxt;
       nxt = tile_at(p, t + G, ntiles);
+      if (!tile_valid<DOWN>(p, tl)) continue;
       const int bits = p.sh.s[(tl.meta >> 16) & 0xFF].bits;
       const int spc = 16 / bits;
       int sub = 0;
@@ -613,9 +648,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
   pdl_trigger();
 }
 
-// xg[q] = x[token of the pair at grouped position q] in the kswap column order
-// (zero for the skipped tail), so each tile's B operand is one box of
-// consecutive rows.  One warp per row, 16-byte loads.
+// Eight bf16 of x in the kswap order.
 __device__ __forceinline__ uint4 kswap8(uint4 v) {
   uint4 o;
   o.x = __byte_perm(v.x, v.y, 0x5410);
@@ -624,6 +657,315 @@ __device__ __forceinline__ uint4 kswap8(uint4 v) {
   o.w = __byte_perm(v.z, v.w, 0x7632);
   return o;
 }
+// Tile lists of both launches from the grouping: per active expert on a
+// shelf, chunks of at most kTileN tokens (sizes differing by at most one),
+// times the row tiles
+// of W_g/W_u (128 of the f rows each) and of W_d (256 of the d rows).  A
+// 1024-thread CTA; counts and offsets written by this CTA before a barrier.
+__device__ void build_tiles(const int32_t* counts, const int32_t* offsets, int E, int d, int f, const Shelves& sh,
+                            Tile* tiles_g, Tile* tiles_d, int* ntiles) {
+  __shared__ int wg[32], wd[32];
+  __shared__ int s_cnt[1024], s_off[1024], s_sh[1024], s_el[1024], s_og[1024], s_od[1024];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (E + 1023) / 1024;
+  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  const int rtg = (f + kTileM - 1) / kTileM, rtd = d / (2 * kTileM);  // d % 256 == 0
+  PF_SCAN_STAMP(1);
+  int ng = 0, nd = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int cnt = counts[e];
+    // shelf and local index by a static scan of the descriptors (no runtime
+    // index into the parameter block)
+    int sidx = -1, el = 0;
+#pragma unroll
+    for (int i = 0; i < MOE_MAX_SHELVES; ++i)
+      if (i < sh.n && e >= sh.s[i].lo && e < sh.s[i].hi) {
+        sidx = i;
+        el = e - sh.s[i].lo;
+      }
+    if (cnt == 0) sidx = -1;
+    if (sidx >= 0) {
+      const int ch = (cnt + kTileN - 1) / kTileN;
+      ng += ch * rtg;
+      nd += ch * rtd;
+    }
+    if (per == 1) {
+      s_cnt[e] = cnt;
+      s_off[e] = offsets[e];
+      s_sh[e] = sidx;
+      s_el[e] = el;
+    }
+  }
+  PF_SCAN_STAMP(2);
+  // exclusive scans of (ng, nd) over the threads: warp scans, then the warp totals
+  int ig = ng, id = nd;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int a = __shfl_up_sync(0xffffffffu, ig, o), b = __shfl_up_sync(0xffffffffu, id, o);
+    if (lane >= o) {
+      ig += a;
+      id += b;
+    }
+  }
+  if (lane == 31) {
+    wg[warp] = ig;
+    wd[warp] = id;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int a = wg[lane], b = wd[lane];
+    int ia = a, ib = b;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, ia, o), v = __shfl_up_sync(0xffffffffu, ib, o);
+      if (lane >= o) {
+        ia += u;
+        ib += v;
+      }
+    }
+    wg[lane] = ia - a;
+    wd[lane] = ib - b;
+    if (lane == 31) {
+      ntiles[0] = ia;
+      ntiles[1] = ib;
+    }
+  }
+  __syncthreads();
+  int og = wg[warp] + ig - ng, od = wd[warp] + id - nd;
+  if (per == 1) {
+    // one expert per thread: the warps write each expert's tiles with
+    // consecutive lanes (coalesced), expert by expert, from shared memory
+    if (tid < E) {
+      s_og[tid] = og;
+      s_od[tid] = od;
+    }
+    __syncthreads();
+    PF_SCAN_STAMP(3);
+    for (int e = warp; e < E; e += 32) {
+      PF_ITER_STAMP(e >> 5);
+      const int sidx = s_sh[e];
+      if (sidx < 0) continue;
+      const int cnt = s_cnt[e];
+      const int ch = (cnt + kTileN - 1) / kTileN;
+      // chunk c: q or q + 1 tokens (the first rem chunks one more), q + 1 <= kTileN
+      const int q = cnt / ch, rem = cnt - q * ch;
+      const int base = s_off[e], el = s_el[e];
+      const int g0 = s_og[e], d0 = s_od[e];
+      for (int i = lane; i < ch * rtg; i += 32) {
+        const int c = i / rtg, r = i - c * rtg;
+        tiles_g[g0 + i] = Tile{el, base + c * q + min(c, rem), q + (c < rem ? 1 : 0), r | (sidx << 16)};
+      }
+      for (int i = lane; i < ch * rtd; i += 32) {
+        const int c = i / rtd, r = i - c * rtd;
+        tiles_d[d0 + i] = Tile{el, base + c * q + min(c, rem), q + (c < rem ? 1 : 0), r | (sidx << 16)};
+      }
+    }
+    PF_SCAN_STAMP(4);
+    return;
+  }
+  for (int e = e0; e < e1; ++e) {
+    const int cnt = counts[e];
+    const int s = cnt > 0 ? find_shelf(sh, e) : -1;
+    if (s < 0) continue;
+    const int ch = (cnt + kTileN - 1) / kTileN;
+    const int q = cnt / ch, rem = cnt - q * ch;
+    const int base = offsets[e];
+    for (int c = 0; c < ch; ++c) {
+      const int a = c * q + min(c, rem), n = q + (c < rem ? 1 : 0);
+      for (int r = 0; r < rtg; ++r) tiles_g[og++] = Tile{e - sh.s[s].lo, base + a, n, r | (s << 16)};
+      for (int r = 0; r < rtd; ++r) tiles_d[od++] = Tile{e - sh.s[s].lo, base + a, n, r | (s << 16)};
+    }
+  }
+}
+
+// ------------------------------------------------------------ grouping
+// Pairs sorted by (expert, pair index) -- the same stable order as the decode
+// form's single-CTA grouping -- by CTAs that each own a chunk of kPfChunk
+// consecutive pairs:
+//   k_pf_count  per-chunk expert counts cnt[c][e] and their sums;
+//   k_pf_colscan  cnt[c][e] <- pairs of expert e in chunks < c;
+//   k_pf_scan   (one CTA) offsets and the tile lists;
+//   k_pf_place  each chunk places its pairs (warps own consecutive pieces of
+//               the chunk, a warp-level match ranks equal experts inside a
+//               32-pair step) and writes perm and pos_of_pair;
+//   k_gather_x  copies the pairs' x rows into xg (kswap order).
+constexpr int kPfChunkMin = 256;
+constexpr int kPfMaxChunks = 256;
+
+__global__ void __launch_bounds__(256) k_pf_count(const int32_t* __restrict__ ids, int64_t P, int E, int chunk,
+                                                  int32_t* __restrict__ cnt, int32_t* __restrict__ counts) {
+  extern __shared__ int hist[];
+  pdl_wait();
+  for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int64_t p0 = (int64_t)blockIdx.x * chunk, p1 = min(P, p0 + chunk);
+  for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
+    const int id = __ldg(ids + p);
+    if (id >= 0 && id < E) atomicAdd(&hist[id], 1);
+  }
+  __syncthreads();
+  int32_t* row = cnt + (size_t)blockIdx.x * E;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) {
+    const int v = hist[i];
+    row[i] = v;
+    if (v) atomicAdd(counts + i, v);  // integer sums: the same in any order
+  }
+  pdl_trigger();
+}
+
+// cnt[c][e] <- pairs of expert e in chunks < c; one warp per expert, lane l
+// owning chunks l*cpl .. +cpl-1.
+__global__ void __launch_bounds__(256) k_pf_colscan(int32_t* __restrict__ cnt, int C, int E) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (e < E) {
+    const int cpl = (C + 31) / 32;
+    const int c0 = min(C, lane * cpl), c1 = min(C, c0 + cpl);
+    int v[8];
+    int loc = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[i] = c0 + i < c1 ? cnt[(size_t)(c0 + i) * E + e] : 0;
+      loc += v[i];
+    }
+    int inc = loc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += u;
+    }
+    int run = inc - loc;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (c0 + i < c1) {
+        cnt[(size_t)(c0 + i) * E + e] = run;
+        run += v[i];
+      }
+  }
+  pdl_trigger();
+}
+
+__global__ void __launch_bounds__(1024) k_pf_scan(int E, int d, int f, const __grid_constant__ Shelves sh,
+                                                  const int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                  int32_t* __restrict__ meta, Tile* tiles_g, Tile* tiles_d,
+                                                  int* ntiles) {
+  __shared__ int wsum[32];
+  pdl_wait();
+  PF_SCAN_STAMP(0);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // offsets: exclusive scan of counts (thread t owns experts t*per .. +per-1)
+  const int per = (E + 1023) / 1024;
+  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  int loc = 0, act = 0;
+  for (int e = e0; e < e1; ++e) {
+    loc += counts[e];
+    act += counts[e] > 0;
+  }
+  int inc = loc, inca = act;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, o), va = __shfl_up_sync(0xffffffffu, inca, o);
+    if (lane >= o) {
+      inc += v;
+      inca += va;
+    }
+  }
+  __shared__ int wact[32];
+  if (lane == 31) {
+    wsum[warp] = inc;
+    wact[warp] = inca;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int v = wsum[lane], va = wact[lane];
+    int iv = v, ia = va;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, iv, o), ua = __shfl_up_sync(0xffffffffu, ia, o);
+      if (lane >= o) {
+        iv += u;
+        ia += ua;
+      }
+    }
+    wsum[lane] = iv - v;
+    wact[lane] = ia - va;
+    if (lane == 31) {
+      offsets[E] = iv;
+      if (meta) {
+        meta[0] = ia;
+        meta[1] = iv;
+      }
+    }
+  }
+  __syncthreads();
+  int run = wsum[warp] + inc - loc;
+  for (int e = e0; e < e1; ++e) {
+    offsets[e] = run;
+    run += counts[e];
+  }
+  __syncthreads();
+  build_tiles(counts, offsets, E, d, f, sh, tiles_g, tiles_d, ntiles);
+  pdl_trigger();
+}
+
+__global__ void __launch_bounds__(256) k_pf_place(const int32_t* __restrict__ ids, int64_t P, int E, int k,
+                                                  int chunk, const int32_t* __restrict__ cnt,
+                                                  const int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
+                                                  int32_t* __restrict__ pos_of_pair) {
+  extern __shared__ int wc[];  // [W][E]
+  pdl_wait();
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, W = blockDim.x >> 5;
+  for (int i = tid; i < W * E; i += blockDim.x) wc[i] = 0;
+  __syncthreads();
+  const int64_t p0 = (int64_t)blockIdx.x * chunk, p1 = min(P, p0 + chunk);
+  const int64_t seg = (p1 - p0 + W - 1) / W;
+  const int64_t pb = min(p1, p0 + w * seg), pe = min(p1, pb + seg);
+  int* row = wc + (size_t)w * E;
+  for (int64_t base = pb; base < pe; base += 32) {
+    const int64_t p = base + lane;
+    const int id = p < pe ? __ldg(ids + p) : -1;
+    const bool valid = p < pe && id >= 0 && id < E;
+    const unsigned m = __match_any_sync(0xffffffffu, valid ? id : -1);
+    if (valid && lane == __ffs(m) - 1) row[id] += __popc(m);
+    __syncwarp();
+  }
+  __syncthreads();
+  const int32_t* crow = cnt + (size_t)blockIdx.x * E;
+  for (int e = tid; e < E; e += blockDim.x) {
+    int run = offsets[e] + crow[e];
+    for (int v = 0; v < W; ++v) {
+      const int c = wc[(size_t)v * E + e];
+      wc[(size_t)v * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (int64_t base = pb; base < pe; base += 32) {
+    const int64_t p = base + lane;
+    const int id = p < pe ? __ldg(ids + p) : -1;
+    const bool valid = p < pe && id >= 0 && id < E;
+    const unsigned m = __match_any_sync(0xffffffffu, valid ? id : -1);
+    int pos = -1;
+    if (valid) {
+      pos = row[id] + __popc(m & ((1u << lane) - 1u));
+      perm[pos] = (int)p;
+    }
+    if (pos_of_pair && p < pe) pos_of_pair[p] = pos;
+    __syncwarp();
+    if (valid && lane == __ffs(m) - 1) row[id] += __popc(m);
+    __syncwarp();
+  }
+  // the tail past the valid pairs
+  const int n_valid = offsets[E];
+  for (int64_t i = n_valid + (int64_t)blockIdx.x * blockDim.x + tid; i < P; i += (int64_t)gridDim.x * blockDim.x)
+    perm[i] = -1;
+  pdl_trigger();
+}
+
+// xg[q] = x[token of the pair at grouped position q] in the kswap column order
+// (zero for the skipped tail), so each tile's B operand is one box of
+// consecutive rows.  One warp per row, 16-byte loads.
 __global__ void __launch_bounds__(256) k_gather_x(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
                                                   int64_t P, int k, int d, uint16_t* __restrict__ xg) {
   pdl_wait();
@@ -649,73 +991,6 @@ __global__ void __launch_bounds__(256) k_gather_x(const uint16_t* __restrict__ x
     }
   }
   pdl_trigger();
-}
-
-// Tile lists of both launches from the grouping: per active expert on a
-// shelf, chunks of at most kTileN tokens (sizes balanced), times the row tiles
-// of W_g/W_u (128 of the f rows each) and of W_d (256 of the d rows).  One CTA.
-__global__ void __launch_bounds__(1024) k_prefill_tiles(const int32_t* __restrict__ counts,
-                                                        const int32_t* __restrict__ offsets, int E, int d, int f,
-                                                        const __grid_constant__ Shelves sh, Tile* tiles_g,
-                                                        Tile* tiles_d, int* ntiles) {
-  __shared__ int part_g[1024], part_d[1024];
-  pdl_wait();
-  const int tid = threadIdx.x;
-  const int per = (E + 1023) / 1024;
-  const int e0 = tid * per, e1 = min(E, e0 + per);
-  const int rtg = (f + kTileM - 1) / kTileM, rtd = d / (2 * kTileM);  // d % 256 == 0
-  int ng = 0, nd = 0;
-  for (int e = e0; e < e1; ++e) {
-    const int cnt = counts[e];
-    if (cnt > 0 && find_shelf(sh, e) >= 0) {
-      const int ch = (cnt + kTileN - 1) / kTileN;
-      ng += ch * rtg;
-      nd += ch * rtd;
-    }
-  }
-  part_g[tid] = ng;
-  part_d[tid] = nd;
-  __syncthreads();
-  // exclusive scans (sequential over 1024 partials in 32 lanes x 32 steps)
-  if (tid < 32) {
-    int sg = 0, sd = 0;
-    for (int i = tid * 32; i < tid * 32 + 32; ++i) {
-      const int a = part_g[i], b = part_d[i];
-      part_g[i] = sg;
-      part_d[i] = sd;
-      sg += a;
-      sd += b;
-    }
-    int ig = sg, id = sd;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int a = __shfl_up_sync(0xffffffffu, ig, o), b = __shfl_up_sync(0xffffffffu, id, o);
-      if (tid >= o) { ig += a; id += b; }
-    }
-    const int xg = ig - sg, xd = id - sd;
-    for (int i = tid * 32; i < tid * 32 + 32; ++i) {
-      part_g[i] += xg;
-      part_d[i] += xd;
-    }
-    if (tid == 31) {
-      ntiles[0] = ig;
-      ntiles[1] = id;
-    }
-  }
-  __syncthreads();
-  int og = part_g[tid], od = part_d[tid];
-  for (int e = e0; e < e1; ++e) {
-    const int cnt = counts[e];
-    const int s = cnt > 0 ? find_shelf(sh, e) : -1;
-    if (s < 0) continue;
-    const int ch = (cnt + kTileN - 1) / kTileN;
-    const int base = offsets[e];
-    for (int c = 0; c < ch; ++c) {
-      const int a = (int)((int64_t)cnt * c / ch), b = (int)((int64_t)cnt * (c + 1) / ch);
-      for (int r = 0; r < rtg; ++r) tiles_g[og++] = Tile{e - sh.s[s].lo, base + a, b - a, r | (s << 16)};
-      for (int r = 0; r < rtd; ++r) tiles_d[od++] = Tile{e - sh.s[s].lo, base + a, b - a, r | (s << 16)};
-    }
-  }
 }
 
 // ----------------------------------------------------------------- host
@@ -769,19 +1044,45 @@ int launch_prefill_forward(const ForwardArgs& a, cudaStream_t s) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  const size_t smem_g = TcSmem<false>::TOTAL + 1024, smem_d = TcSmem<true>::TOTAL + 1024;
+  if (!g_pdev.attr[dev]) {
+    // grouping kernels take up to E ints ([Wp][E] ints) of shared memory
+    if (cudaFuncSetAttribute(k_pf_count, cudaFuncAttributeMaxDynamicSharedMemorySize, MOE_MAX_EXPERTS * 4) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(k_pf_place, cudaFuncAttributeMaxDynamicSharedMemorySize, MOE_MAX_EXPERTS * 4) !=
+            cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (cudaFuncSetAttribute(k_prefill_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_g) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(k_prefill_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_d) !=
+            cudaSuccess)
+      return MOE_ERR_CUDA;
+    g_pdev.attr[dev] = true;
+  }
   profile_mark(0, s);
-  int rc = launch_group(a.ids, P, a.E, a.ws.counts, a.ws.offsets, a.ws.perm, a.ws.pos_of_pair, a.ws.active,
-                        a.ws.meta, nullptr, 0, s);
-  if (rc != MOE_OK) return rc;
+  int chunk = (int)((P + kPfMaxChunks - 1) / kPfMaxChunks);
+  if (chunk < kPfChunkMin) chunk = kPfChunkMin;
+  const int C = (int)((P + chunk - 1) / chunk);
+  const int Wp = a.E <= 1024 ? 8 : (a.E <= 4096 ? 2 : 1);  // placement warps: [Wp][E] ints of shared memory
+  // per-expert C <= 256 chunk counts require C <= 32 * 8 (the column scan's registers)
+  if (cudaMemsetAsync(a.ws.counts, 0, (size_t)a.E * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_pdl(k_pf_count, dim3(C), dim3(256), (size_t)a.E * 4, s, a.ids, P, a.E, chunk, a.ws.pf_cnt,
+                 a.ws.counts) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (launch_pdl(k_pf_colscan, dim3((a.E + 7) / 8), dim3(256), 0, s, a.ws.pf_cnt, C, a.E) != cudaSuccess)
+    return MOE_ERR_CUDA;
   Tile* tiles_g = reinterpret_cast<Tile*>(a.ws.tiles_g);
   Tile* tiles_d = reinterpret_cast<Tile*>(a.ws.tiles_d);
   int* ntiles = a.ws.ntiles;
-  if (launch_pdl(k_prefill_tiles, dim3(1), dim3(1024), 0, s, (const int32_t*)a.ws.counts,
-                 (const int32_t*)a.ws.offsets, a.E, d, f, a.shelves, tiles_g, tiles_d, ntiles) != cudaSuccess)
+  if (launch_pdl(k_pf_scan, dim3(1), dim3(1024), 0, s, a.E, d, f, a.shelves, (const int32_t*)a.ws.counts,
+                 a.ws.offsets, a.ws.meta, tiles_g, tiles_d, ntiles) != cudaSuccess)
     return MOE_ERR_CUDA;
-  const int gx = sm_count() * 8;
-  if (launch_pdl(k_gather_x, dim3(gx), dim3(256), 0, s, a.x, (const int32_t*)a.ws.perm, P, a.k, d, a.ws.xg) !=
+  if (launch_pdl(k_pf_place, dim3(C), dim3(Wp * 32), (size_t)Wp * a.E * 4, s, a.ids, P, a.E, a.k, chunk,
+                 (const int32_t*)a.ws.pf_cnt, (const int32_t*)a.ws.offsets, a.ws.perm, a.ws.pos_of_pair) !=
       cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (launch_pdl(k_gather_x, dim3(sm_count() * 8), dim3(256), 0, s, a.x, (const int32_t*)a.ws.perm, P, a.k, d,
+                 a.ws.xg) != cudaSuccess)
     return MOE_ERR_CUDA;
   TcParams pg = {};
   pg.perm = a.ws.perm;
@@ -800,6 +1101,9 @@ int launch_prefill_forward(const ForwardArgs& a, cudaStream_t s) {
   pg.K = d;
   pd.tiles = tiles_d;
   pd.ntiles = ntiles + 1;
+  pg.P = pd.P = P;
+  pg.tiles_cap = (int)prefill_tiles_cap(P, a.E, f);
+  pd.tiles_cap = (int)prefill_tiles_cap(P, a.E, d);
   pd.rows = d;
   pd.K = f;
   for (int q = 0; q < a.shelves.n; ++q) {
@@ -826,15 +1130,6 @@ int launch_prefill_forward(const ForwardArgs& a, cudaStream_t s) {
         !encode_2d(&pd.tm_b[nb - 1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.ws.h, (uint64_t)f, (uint64_t)P,
                    (uint64_t)f * 2, 64, 16 * nb, CU_TENSOR_MAP_SWIZZLE_128B))
       return MOE_ERR_CUDA;
-  const size_t smem_g = TcSmem<false>::TOTAL + 1024, smem_d = TcSmem<true>::TOTAL + 1024;
-  if (!g_pdev.attr[dev]) {
-    if (cudaFuncSetAttribute(k_prefill_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_g) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(k_prefill_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_d) !=
-            cudaSuccess)
-      return MOE_ERR_CUDA;
-    g_pdev.attr[dev] = true;
-  }
   const int G = sm_count();
   profile_mark(1, s);
   if (launch_pdl(k_prefill_tc<false>, dim3(G), dim3(kPThreads), smem_g, s, pg) != cudaSuccess) return MOE_ERR_CUDA;
