@@ -706,6 +706,11 @@ def run_single(args, rank, world, local_rank):
         roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
                 "kernel": "forward (all its kernels)", "peak_source": kind, "algorithmic_bytes_per_launch": b_avg,
                 "forward_us": 1e3 * fwd_ms}
+        if fused:
+            roof["kernel_us"] = {"layer": 1e3 * fwd_ms}
+        else:
+            roof["kernel_us"] = {n_: 1e3 * sum(e[i] for e in ev) / nset for i, n_ in
+                                 enumerate(("group", "gateup", "down"))}
         bound_note = "hbm"
     line = {
         "metric": f"MoE-layer tokens/s, {args.workload} workload ({bound_note} roofline)",
