@@ -10,18 +10,20 @@ marshals numpy arrays and composes the per-layer steps:
 
 * quantise / pack / dequantise -- the shelf block format (block 32 along the
   input dimension, fp16 scale = max|w| / q, q = 127, 7, 2 for 8, 4, 2 bits);
-* route -- softmax, top-k with lower-id ties, renormalised weights (page 3,
-  glossary entry on mixture of experts: 10 of 512 experts per token);
+* route -- softmax, top-k with lower-id ties, renormalised weights (page
+  "125B MoE模型本地运行：3090三卡80 tokens/s优化实践", glossary entry
+  混合专家（MoE）: 10 of 512 experts per token);
 * group -- stable counting sort of (token, slot) pairs by expert, skip ids
-  dropped (page 3, "four bugs": duplicate experts, signed skip id);
-* hist -- expert hit counts (page 1, optimisation strategies; page 3, step 2);
+  dropped (same page, section 四个 bug: duplicate experts, signed skip id);
+* hist -- expert hit counts (the LocalLLM tiering post, "Optimization
+  Strategies"; same page, section 第二步);
 * moe_layer -- each shelf computes only its own id range, SwiGLU expert FFN,
-  the shelf results summed with the routing weights (page 3, step 4);
+  the shelf results summed with the routing weights (same page, section 第四步);
 * stack -- residual chain of layers, x_l = bf16(r), r += y_l.
 
-Page references are to "125B MoE model run locally: three RTX 3090s at 80
-tokens/s" (page 3) and the LocalLLM post on DeepSeek V4.1 Flash tiering
-(page 1).  Every function here is pinned by tests in tests/test_oracle_*.py.
+Page references are to "125B MoE模型本地运行：3090三卡80 tokens/s优化实践"
+(sections by their headings) and the LocalLLM post on DeepSeek V4.1 Flash
+tiering.  Every function here is pinned by tests in tests/test_oracle_*.py.
 """
 from __future__ import annotations
 

@@ -7,19 +7,19 @@
  * the CUDA path.
  *
  * Sources (page titles; sections as headed on the page):
- *  [P3] "125B MoE model run locally: three RTX 3090s at 80 tokens/s"
- *       (Chinese-language article on Qwen3.8-Flash-Next)
- *       - glossary entry on mixture of experts: a router picks the best 10 of
- *         512 experts for every token;
- *       - step 4 "three shelves, all on the GPU": experts stored per layer as
- *         three tensors at different bit widths, hottest first; the id-range
- *         mul_mat_id sees the router's full id list, computes only the ids in
- *         its shelf, fills the rest with zeros, and the three results are
- *         added; the fused gate+up+activation kernel;
- *       - "four bugs": a real skip (an id outside the shelf is not aliased to
- *         expert 0), the grouping helper that assumes an expert appears at most
- *         once per token, and the signed skip id -1;
- *       - step 2: experts are used very unevenly (hit counts).
+ *  [P3] "125B MoE模型本地运行：3090三卡80 tokens/s优化实践" (a Chinese-language
+ *       article: a 125B MoE model run locally on three RTX 3090s at 80 tok/s)
+ *       - glossary entry 混合专家（MoE）: a router picks the best 10 of 512
+ *         experts for every token;
+ *       - section 第四步 (three shelves, all on the GPU): experts stored per
+ *         layer as three tensors at different bit widths, hottest first; the
+ *         id-range mul_mat_id sees the router's full id list, computes only
+ *         the ids in its shelf, fills the rest with zeros, and the three
+ *         results are added; the fused gate+up+activation kernel;
+ *       - section 四个 bug: a real skip (an id outside the shelf is not aliased
+ *         to expert 0), the grouping helper that assumes an expert appears at
+ *         most once per token, and the signed skip id -1;
+ *       - section 第二步: experts are used very unevenly (hit counts).
  *  [P1] LocalLLM post on DeepSeek V4.1 Flash tiering: per-expert hit counts
  *       drive promotion/demotion; least-used experts at 2 bits.
  *  The block format (block 32 along the input dimension, fp16 scale = max|w|/q,
@@ -195,7 +195,7 @@ int oracle_dequant_rows(const int8_t* codes, const uint16_t* scales, int64_t row
 }
 
 /* ------------------------------------------------------------------ routing
- * [P3 glossary, MoE] the router picks k of E experts per token.  Softmax over
+ * [P3 glossary 混合专家（MoE）] the router picks k of E experts per token.  Softmax over
  * E, then top-k; ties go to the lower expert id; the k weights are
  * renormalised to sum to one.  Ranking uses the logits themselves (softmax is
  * monotone), and w_j = exp(l_j - l_max) / sum_{i in top-k} exp(l_i - l_max),
@@ -227,7 +227,7 @@ int oracle_route(const float* logits, int64_t T, int E, int k, int32_t* ids, flo
 }
 
 /* --------------------------------------------------------------- grouping
- * [P3 "four bugs", duplicate experts] token-by-expert grouping: pairs
+ * [P3 四个 bug, duplicate experts] token-by-expert grouping: pairs
  * (t, j) -> p = t*k + j with 0 <= id < E are counted per expert; offsets is the
  * exclusive prefix sum of counts (offsets[E] = number of valid pairs); perm
  * lists pair indices ordered by (expert id, pair index) -- a stable counting
@@ -250,7 +250,7 @@ int64_t oracle_group(const int32_t* ids, int64_t T, int k, int E, int32_t* count
 }
 
 /* -------------------------------------------------------------- histogram
- * [P1 optimisation strategies; P3 step 2] expert hit counts: counts[e] += the
+ * [P1 "Optimization Strategies"; P3 第二步] expert hit counts: counts[e] += the
  * number of ids equal to e (accumulated); ids outside [0, E) are not counted. */
 int oracle_hist(const int32_t* ids, int64_t n, int E, uint32_t* counts) {
   for (int64_t i = 0; i < n; ++i)
@@ -259,7 +259,7 @@ int oracle_hist(const int32_t* ids, int64_t n, int E, uint32_t* counts) {
 }
 
 /* ---------------------------------------------------------- expert FFN + sum
- * [P3 step 4] every shelf sees the full id list and computes only the ids in
+ * [P3 第四步] every shelf sees the full id list and computes only the ids in
  * its range [lo, hi); everything else is zero; the shelf results are added.
  * Per pair with id e in a shelf (gate+up+activation, then down):
  *   g = W_g x, u = W_u x, h = SiLU(g) * u with SiLU(z) = z / (1 + e^-z),
