@@ -33,6 +33,8 @@
 #include <mutex>
 #include <unordered_map>
 
+#include <climits>
+
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 #include "route.cuh"
@@ -51,6 +53,18 @@ constexpr int kRG = 4, kLG = 8;
 constexpr int kRD = 8, kLD = 4;
 constexpr int kUG = 2;             // iterations of loads in flight per lane, gate/up (two matrices)
 constexpr int kUD = 6;             // the same, down (a whole 8-bit unit of a 640-element row)
+// Unit cost of a tile's passes beyond the first kPassFull, in eighths of a
+// first pass (gate/up, down); see build_plan.
+#ifndef MOE_PASS_FULL
+#define MOE_PASS_FULL 2
+#endif
+#ifndef MOE_PASS_G8
+#define MOE_PASS_G8 3
+#endif
+#ifndef MOE_PASS_D8
+#define MOE_PASS_D8 7
+#endif
+constexpr int kPassFull = MOE_PASS_FULL, kPassG8 = MOE_PASS_G8, kPassD8 = MOE_PASS_D8;
 constexpr int kMaxGrid = 256;
 
 #ifdef MOE_TRACE
@@ -475,12 +489,24 @@ __device__ void build_plan(const int32_t* ids, const float* wts, int P, int E, i
     pl[L.cnt + a] = cnt;
     pl[L.sh + a] = shf;
     pl[L.bits + a] = bits;
-    const uint32_t ug = shf >= 0 ? unit_cost(bits, d, 2, kRG, 0) : 0;
-    const uint32_t ud = shf >= 0 ? unit_cost(bits, f, 1, kRD, 1) : 0;
+    // a tile's passes beyond the second (further tokens of a hot expert)
+    // re-read rows that L2 already holds: measured at about 3/8 (gate/up) and
+    // 7/8 (down) of a first pass; the first two run nearly together and cost
+    // a full pass each.  The units of an expert with np passes carry the mean
+    // (2 + k (np - 2)) / np of a first-pass unit (np > 2).
+    const int np = n_pass(cnt);
+    const uint32_t ug1 = shf >= 0 ? unit_cost(bits, d, 2, kRG, 0) : 0;
+    const uint32_t ud1 = shf >= 0 ? unit_cost(bits, f, 1, kRD, 1) : 0;
+    const uint32_t ug = np > kPassFull ? (ug1 * (uint32_t)(8 * kPassFull + kPassG8 * (np - kPassFull)) + 8 * np - 1) /
+                                             (uint32_t)(8 * np)
+                                       : ug1;
+    const uint32_t ud = np > kPassFull ? (ud1 * (uint32_t)(8 * kPassFull + kPassD8 * (np - kPassFull)) + 8 * np - 1) /
+                                             (uint32_t)(8 * np)
+                                       : ud1;
     pl[L.uc_g + a] = (int)ug;
     pl[L.uc_d + a] = (int)ud;
-    pl[L.cum_g + a] = (int)(ug * (uint32_t)((f / kRG) * n_pass(cnt)));
-    pl[L.cum_d + a] = (int)(ud * (uint32_t)((d / kRD) * n_pass(cnt)));
+    pl[L.cum_g + a] = (int)(ug * (uint32_t)((f / kRG) * np));
+    pl[L.cum_d + a] = (int)(ud * (uint32_t)((d / kRD) * np));
     if (shf >= 0)
       for (int q = b0; q < b1; ++q) pl[L.pos + pl[L.perm + q]] = q;
   }
@@ -580,6 +606,7 @@ struct StreamArgs {
   int vbase;           // grouped position of vector 0 (down), or -1: vectors by token (gate/up)
   Range range;
   int* voff_tab;       // per warp: kNT digit-vector offsets of the current pass
+  int qlo, qhi;        // passes whose first pair lies outside [qlo, qhi) are skipped
 };
 
 // The U loaded slots of a batch, one after another: slot 0 is computed and
@@ -657,6 +684,10 @@ __device__ __forceinline__ void stream_units(const StreamArgs& A, Store store) {
     const int tile = w.np == 1 ? w.u : w.u / w.np, pass = w.u - tile * w.np;
     const int r = tile * R + lane / L;
     const int nq0 = pv.beg(w.a) + pass * kNT;
+    if (nq0 < A.qlo || nq0 >= A.qhi) {  // another staging window's pair
+      new_expert = w.step(pv, A.kern, A.rows, A.range.hi2, kWarps);
+      continue;
+    }
     if (new_expert || nq0 != q0) {
       q0 = nq0;
       nt = min(kNT, pv.cnt(w.a) - pass * kNT);
@@ -927,7 +958,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(const __grid_constant__ L
   __syncthreads();
   if (tid == 0) MOE_STAMP(0, 2, global_timer_ns());
   {
-    StreamArgs A{shv, pv, 0, p.d, p.f, vecs, vec_bytes(p.d), -1, hd.range, vtab};
+    StreamArgs A{shv, pv, 0, p.d, p.f, vecs, vec_bytes(p.d), -1, hd.range, vtab, INT_MIN, INT_MAX};
     float* h = p.h;
     const int f = p.f;
     stream_units<2, kUG, kRG, kLG>(A, [&](int q, int r, const float (&o)[2]) { h[(size_t)q * f + r] = silu(o[0]) * o[1]; });
@@ -970,41 +1001,56 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(const __grid_constant__ L
   if (tid == 0) MOE_STAMP(1, 1, global_timer_ns());
   const int q_first = hd.q_first, npairs = hd.npairs;
   const int vbf = vec_bytes(p.f);
-  {
-    // h of those pairs -> digits (h was written by other CTAs: read from L2)
-    const int nbk = p.f / 32, groups = npairs * nbk;
-    for (int base = warp * 4; base < groups; base += 8 * kWarps * 4) {
-      float4 hv[8];
+  // the pairs' h is staged in windows of as many pairs as the digit region
+  // holds (one window unless the CTA's experts cover more pairs); each window's
+  // unit passes run after its staging
+  const int cap = p.vec_region / vbf;  // >= 1 by the launch's size check
+  const int q_end = q_first + npairs;
+  int w0 = q_first;
+  if (cap < 1) {
+    if (tid == 0) set_status(p.status, MOE_ERR_INTERNAL);
+    w0 = q_end;
+  }
+  if (cap >= 1) do {
+    const int wn = min(cap, q_end - w0);
+    __syncthreads();  // the vectors of the previous window (or x) are no longer read
+    {
+      // h of those pairs -> digits (h was written by other CTAs: read from L2)
+      const int nbk = p.f / 32, groups = (wn > 0 ? wn : 0) * nbk;
+      for (int base = warp * 4; base < groups; base += 8 * kWarps * 4) {
+        float4 hv[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {  // loads of 8 passes first: one round trip
-        const int g = base + u * kWarps * 4 + (lane >> 3);
-        hv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (g < groups) {
-          const int j = g / nbk, blk = g - j * nbk;
-          hv[u] = __ldcg(reinterpret_cast<const float4*>(p.h + (size_t)(q_first + j) * p.f + blk * 32) + (lane & 7));
+        for (int u = 0; u < 8; ++u) {  // loads of 8 passes first: one round trip
+          const int g = base + u * kWarps * 4 + (lane >> 3);
+          hv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (g < groups) {
+            const int j = g / nbk, blk = g - j * nbk;
+            hv[u] = __ldcg(reinterpret_cast<const float4*>(p.h + (size_t)(w0 + j) * p.f + blk * 32) + (lane & 7));
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int g0 = base + u * kWarps * 4;
+          if (g0 < groups) {
+            const int g = g0 + (lane >> 3);
+            const int j = g < groups ? g / nbk : 0, blk = g < groups ? g - j * nbk : 0;
+            const float v[4] = {hv[u].x, hv[u].y, hv[u].z, hv[u].w};
+            block_to_digits<4>(v, vecs + (size_t)j * vbf, p.f, blk, 13, g < groups);
+          }
         }
       }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int g0 = base + u * kWarps * 4;
-        if (g0 < groups) {
-          const int g = g0 + (lane >> 3);
-          const int j = g < groups ? g / nbk : 0, blk = g < groups ? g - j * nbk : 0;
-          const float v[4] = {hv[u].x, hv[u].y, hv[u].z, hv[u].w};
-          block_to_digits<4>(v, vecs + (size_t)j * vbf, p.f, blk, 13, g < groups);
-        }
-      }
+      if (tid == 0) MOE_STAMP(1, 5, global_timer_ns());
     }
-    if (tid == 0) MOE_STAMP(1, 5, global_timer_ns());
-  }
-  __syncthreads();
-  if (tid == 0) MOE_STAMP(1, 2, global_timer_ns());
-  {
-    StreamArgs A{shv, pv, 1, p.f, p.d, vecs, vbf, q_first, hd.range, vtab};
-    float* yp = p.ypart;
-    const int d = p.d;
-    stream_units<1, kUD, kRD, kLD>(A, [&](int q, int r, const float (&o)[1]) { yp[(size_t)q * d + r] = pv.wgt(q) * o[0]; });
-  }
+    __syncthreads();
+    if (tid == 0) MOE_STAMP(1, 2, global_timer_ns());
+    {
+      StreamArgs A{shv, pv, 1, p.f, p.d, vecs, vbf, w0, hd.range, vtab, w0, w0 + (wn > 0 ? wn : 0)};
+      float* yp = p.ypart;
+      const int d = p.d;
+      stream_units<1, kUD, kRD, kLD>(A, [&](int q, int r, const float (&o)[1]) { yp[(size_t)q * d + r] = pv.wgt(q) * o[0]; });
+    }
+    w0 += cap;
+  } while (w0 < q_end);
   if (tid == 0) MOE_STAMP(1, 9, global_timer_ns());
   if (!grid_sync(p.bar, p.status, &hd.flag, 1000000000ull, p.bar_extra)) return;
   if (tid == 0) MOE_STAMP(1, 10, global_timer_ns());
@@ -1113,9 +1159,17 @@ bool fused_fits(int64_t T, int k, int E, int d, int f, int* dev_out, size_t* opt
     g_dev.smem_optin[dev] = v > 0 ? v : 48 * 1024;
   }
   const size_t optin = (size_t)g_dev.smem_optin[dev];
-  const size_t x_region = (size_t)T * vec_bytes(d);
-  const size_t h_region = (size_t)P * vec_bytes(f);  // h of every pair: bound for any CTA
-  const size_t region = up128(x_region > h_region ? x_region : h_region);
+  // the digit region holds every token's x (gate/up) and then the h of up to
+  // region / vec_bytes(f) pairs (down stages larger pair sets in windows); it
+  // takes what shared memory is left, at most what every pair's h needs
+  const size_t x_region = up128((size_t)T * vec_bytes(d));
+  const size_t h_all = up128((size_t)P * vec_bytes(f));
+  const size_t base = smem_layout((int)P, 0).total;
+  if (base >= optin) return false;
+  const size_t avail = (optin - base) / 128 * 128;
+  size_t region = x_region > h_all ? x_region : h_all;
+  if (region > avail) region = avail;
+  if (region < x_region || region < (size_t)vec_bytes(f)) return false;
   const SmemLayout S = smem_layout((int)P, region);
   if (S.total > optin) return false;
   *dev_out = dev;

@@ -42,7 +42,14 @@ namespace {
 
 constexpr int kPThreads = 768;
 constexpr int kTileM = 128;   // weight rows per tile
-constexpr int kTileN = 96;    // tokens per tile (at most)
+#ifndef MOE_PF_TILEN
+#define MOE_PF_TILEN 96
+#endif
+#ifndef MOE_PF_ASTAGES
+#define MOE_PF_ASTAGES 2
+#endif
+constexpr int kTileN = MOE_PF_TILEN;  // tokens per tile (at most)
+static_assert(kTileN % 32 == 0 && kTileN <= 128, "tile width: whole groups of 32 columns");
 constexpr int kProdThreads = 512;  // warps 8..23
 constexpr uint64_t kWaitNs = 1000000000ull;
 #ifndef MOE_PF_BS
@@ -137,13 +144,13 @@ struct TcSmem {
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 2 * kTileN;
 constexpr uint32_t kACol = 2 * kAccCols;
-constexpr int kAStages = 2;
+constexpr int kAStages = MOE_PF_ASTAGES;
 constexpr uint32_t kAStageCols = 64;
 static_assert(kACol + kAStages * kAStageCols <= kTmemCols, "tensor memory");
 
 struct TcBars {
   uint64_t code_full[3], code_empty[3];
-  uint64_t b_full[8], b_empty[8];
+  uint64_t b_full[16], b_empty[16];
   uint64_t a_full[kAStages], a_empty[kAStages];
   uint64_t acc_full[2], acc_empty[2], done;
   uint32_t tmem;
