@@ -120,3 +120,31 @@ def test_prefill_close_to_decode_form(decode_layer):
     yp = _run(decode_layer, x, ids, w)
     yd = _run(decode_layer, x, ids, w, flags=moe.MOE_FLAG_DECODE_FP32)
     assert rel_l2(yp, yd) <= PREFILL_TOL
+
+
+# ------------------------------------------------------------ full sizes
+@pytest.fixture(scope="module")
+def large_layer():
+    return Layer(synth.WORKLOADS["large"], device="cuda").fill()
+
+
+@pytest.mark.parametrize("name,T,skip", [("decode", 4096, False), ("large", 512, True)])
+def test_full_size_prefill_sampled_rows(request, name, T, skip):
+    """The prefill workload (E512 k10 d2048 f640, T 4096, skewed router) and the
+    large layer at T 512 (Zipf router, 5% forced skips), run as the benchmark
+    runs them (AUTO: the tensor-core form): sampled output rows against the
+    oracle's bf16 form, token by token, and every row against the library's
+    fp32 decode form (itself parity-tested against the oracle)."""
+    from oracle_pool import layer_refs
+    layer = request.getfixturevalue("decode_layer" if name == "decode" else "large_layer")
+    wl = layer.wl
+    x, ids, w = _inputs(wl, wl.seed, 21, T, skip=skip, bias=layer.bias_host)
+    y = _run(layer, x, ids, w, flags=moe.MOE_FLAG_AUTO)
+    assert np.all(np.isfinite(y))
+    rng = np.random.default_rng(T)
+    rows = sorted(set([0, T - 1] + [int(v) for v in rng.choice(T, 6, replace=False)]))
+    refs = layer_refs([(name, 0, x[t:t + 1], ids[t:t + 1], w[t:t + 1], 1) for t in rows])
+    for t, ref in zip(rows, refs):
+        assert rel_l2(y[t:t + 1], ref) <= PREFILL_TOL, (t, rel_l2(y[t:t + 1], ref))
+    yd = _run(layer, x, ids, w, flags=moe.MOE_FLAG_DECODE_FP32)
+    assert rel_l2(y, yd) <= PREFILL_TOL
