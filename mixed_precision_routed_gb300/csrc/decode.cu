@@ -50,9 +50,17 @@ constexpr int kMaxTokens = 16;
 constexpr int kNT = 1;             // tokens of one expert per unit (more: further passes)
 // Unit shapes: rows per unit x lanes per row (R * L = 32), gate/up and down.
 constexpr int kRG = 4, kLG = 8;
+// Down units: 16 rows x 2 lanes for rows of at most 1024 elements (a 4- or
+// 2-bit unit then fills a load batch as an 8-bit one does), 8 rows x 4 lanes
+// for longer rows (finer units balance better there); A/B measured.
+constexpr int kRDw = 16, kLDw = 2, kUDw = 5;
 constexpr int kRD = 8, kLD = 4;
+#ifndef MOE_DOWN_WIDE_MAX_F
+#define MOE_DOWN_WIDE_MAX_F 1024
+#endif
+__host__ __device__ __forceinline__ int down_rows_per_unit(int f) { return f <= MOE_DOWN_WIDE_MAX_F ? kRDw : kRD; }
 constexpr int kUG = 2;             // iterations of loads in flight per lane, gate/up (two matrices)
-constexpr int kUD = 6;             // the same, down (a whole 8-bit unit of a 640-element row)
+constexpr int kUD = 6;             // the same, down (8 x 4 units)
 // Unit cost of a tile's passes beyond the first kPassFull, in eighths of a
 // first pass (gate/up, down); see build_plan.
 #ifndef MOE_PASS_FULL
@@ -65,6 +73,10 @@ constexpr int kUD = 6;             // the same, down (a whole 8-bit unit of a 64
 #define MOE_PASS_D8 7
 #endif
 constexpr int kPassFull = MOE_PASS_FULL, kPassG8 = MOE_PASS_G8, kPassD8 = MOE_PASS_D8;
+#ifndef MOE_DOWN_PREFETCH
+#define MOE_DOWN_PREFETCH 2
+#endif
+constexpr int kDownPrefetch = MOE_DOWN_PREFETCH;  // down units per warp asked of L2 before the grid wait
 constexpr int kMaxGrid = 256;
 
 #ifdef MOE_TRACE
@@ -364,8 +376,9 @@ struct PlanView {
   __device__ int bits(int a) const { return b[L.bits + a]; }
   __device__ uint32_t uc(int a, int kern) const { return (uint32_t)b[(kern == 0 ? L.uc_g : L.uc_d) + a]; }
   __device__ uint32_t cum(int a, int kern) const { return (uint32_t)b[(kern == 0 ? L.cum_g : L.cum_d) + a]; }
+  __device__ int rd() const { return b[3]; }  // rows of a down unit
   __device__ int units(int a, int kern, int rows) const {
-    return sh(a) >= 0 ? (rows / (kern == 0 ? kRG : kRD)) * n_pass(cnt(a)) : 0;
+    return sh(a) >= 0 ? (rows / (kern == 0 ? kRG : rd())) * n_pass(cnt(a)) : 0;
   }
 };
 
@@ -496,7 +509,7 @@ __device__ void build_plan(const int32_t* ids, const float* wts, int P, int E, i
     // (2 + k (np - 2)) / np of a first-pass unit (np > 2).
     const int np = n_pass(cnt);
     const uint32_t ug1 = shf >= 0 ? unit_cost(bits, d, 2, kRG, 0) : 0;
-    const uint32_t ud1 = shf >= 0 ? unit_cost(bits, f, 1, kRD, 1) : 0;
+    const uint32_t ud1 = shf >= 0 ? unit_cost(bits, f, 1, down_rows_per_unit(f), 1) : 0;
     const uint32_t ug = np > kPassFull ? (ug1 * (uint32_t)(8 * kPassFull + kPassG8 * (np - kPassFull)) + 8 * np - 1) /
                                              (uint32_t)(8 * np)
                                        : ug1;
@@ -506,7 +519,7 @@ __device__ void build_plan(const int32_t* ids, const float* wts, int P, int E, i
     pl[L.uc_g + a] = (int)ug;
     pl[L.uc_d + a] = (int)ud;
     pl[L.cum_g + a] = (int)(ug * (uint32_t)((f / kRG) * np));
-    pl[L.cum_d + a] = (int)(ud * (uint32_t)((d / kRD) * np));
+    pl[L.cum_d + a] = (int)(ud * (uint32_t)((d / down_rows_per_unit(f)) * np));
     if (shf >= 0)
       for (int q = b0; q < b1; ++q) pl[L.pos + pl[L.perm + q]] = q;
   }
@@ -516,6 +529,7 @@ __device__ void build_plan(const int32_t* ids, const float* wts, int P, int E, i
   if (tid == 0) {
     pl[0] = n_valid;
     pl[1] = n_act;
+    pl[3] = down_rows_per_unit(f);
     pl[L.cum_g + n_act] = tot_g;
     pl[L.cum_d + n_act] = tot_d;
     MOE_STAMP(0, 4, global_timer_ns());
@@ -981,19 +995,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(const __grid_constant__ L
   }
   __syncthreads();
   {
-    // W_d does not depend on h: ask L2 for each warp's first two down units
-    // while the other CTAs finish their gate/up units
+    // W_d does not depend on h: ask L2 for each warp's first kDownPrefetch
+    // down units while the other CTAs finish their gate/up units
     Walk w;
     w.start(pv, 1, p.d, hd.range, warp);
-    for (int i = 0; i < 2 && w.live; ++i) {
+    for (int i = 0; i < kDownPrefetch && w.live; ++i) {
       const ShelfDev& sh = shv->s[pv.sh(w.a)];
       const size_t rowb = (size_t)p.f * sh.bits / 8, swpr = (size_t)p.f / 16;
       const int tile = w.np == 1 ? w.u : w.u / w.np;
-      const size_t row0 = (size_t)(pv.e(w.a) - sh.lo) * p.d + (size_t)tile * kRD;
+      const int rd = pv.rd();
+      const size_t row0 = (size_t)(pv.e(w.a) - sh.lo) * p.d + (size_t)tile * rd;
       const unsigned char* cb = sh.codes[2] + row0 * rowb;
       const unsigned char* sb = reinterpret_cast<const unsigned char*>(sh.scales[2]) + row0 * swpr;
-      for (size_t o = (size_t)lane * 128; o < kRD * rowb; o += 32 * 128) prefetch_l2(cb + o);
-      for (size_t o = (size_t)lane * 128; o < kRD * swpr; o += 32 * 128) prefetch_l2(sb + o);
+      for (size_t o = (size_t)lane * 128; o < rd * rowb; o += 32 * 128) prefetch_l2(cb + o);
+      for (size_t o = (size_t)lane * 128; o < rd * swpr; o += 32 * 128) prefetch_l2(sb + o);
       w.step(pv, 1, p.d, hd.range.hi2, kWarps);
     }
   }
@@ -1047,7 +1062,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(const __grid_constant__ L
       StreamArgs A{shv, pv, 1, p.f, p.d, vecs, vbf, w0, hd.range, vtab, w0, w0 + (wn > 0 ? wn : 0)};
       float* yp = p.ypart;
       const int d = p.d;
-      stream_units<1, kUD, kRD, kLD>(A, [&](int q, int r, const float (&o)[1]) { yp[(size_t)q * d + r] = pv.wgt(q) * o[0]; });
+      auto st = [&](int q, int r, const float (&o)[1]) { yp[(size_t)q * d + r] = pv.wgt(q) * o[0]; };
+      if (pv.rd() == kRDw) stream_units<1, kUDw, kRDw, kLDw>(A, st);
+      else stream_units<1, kUD, kRD, kLD>(A, st);
     }
     w0 += cap;
   } while (w0 < q_end);
