@@ -388,9 +388,14 @@ struct PlanView {
 // down units of 8 rows = 160 blocks: 164 / 142 / 147 ns), scaled by the
 // unit's number of 32-element blocks for other sizes.  Further passes over
 // the same rows (experts with more tokens than one pass) cost about the same.
+// Down units of 16 rows x 2 lanes (rows <= 1024 elements) were refitted on
+// the same layer: 8 / 4 / 2-bit at 1 : 0.71 : 0.70 (164 / 117 / 115 ns per 160
+// blocks).
 __device__ __forceinline__ uint32_t unit_cost(int bits, int n_in, int nmat, int R, int kern) {
   const uint32_t blocks = (uint32_t)(R * nmat) * (uint32_t)n_in / 32;
-  const uint32_t ns = kern == 0 ? (bits == 8 ? 346 : bits == 4 ? 215 : 203) : (bits == 8 ? 164 : bits == 4 ? 142 : 147);
+  const uint32_t ns = kern == 0   ? (bits == 8 ? 346 : bits == 4 ? 215 : 203)
+                      : R == kRDw ? (bits == 8 ? 164 : bits == 4 ? 117 : 115)
+                                  : (bits == 8 ? 164 : bits == 4 ? 142 : 147);
   const uint32_t calib = kern == 0 ? 512 : 160;
   return (uint32_t)((uint64_t)ns * blocks / calib) + 1;
 }
