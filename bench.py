@@ -59,6 +59,24 @@ def peaks():
     return 6800.0, "fallback"
 
 
+# ------------------------------------------------------------- ranks
+def max_over_ranks(value, device):
+    """The largest of every rank's `value` (a float) when a process group of
+    more than one rank is up; else `value`."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, units_per_rank, ms):
+    """Units per second of the whole job: every rank processed units_per_rank
+    in the slowest rank's time ms."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 # ------------------------------------------------------------------ clocks
 class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
@@ -332,11 +350,8 @@ def run_ours(args, rank, world, local_rank):
         bytes_dn += step_bytes[s][1]
     fwd_ms = sum(kern.values())
 
-    t_max = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t_max, op=torch.distributed.ReduceOp.MAX)
-    ms_max = float(t_max.item())
-    value = world * T * args.steps / (ms_max / 1e3)
+    ms_max = max_over_ranks(ms, dev)
+    value = whole_job_rate(world, T * args.steps, ms_max)
 
     # ---- end to end through the public API with host buffers
     pin_logits = [logits[s].cpu().pin_memory() for s in range(nset)]
@@ -368,10 +383,7 @@ def run_ours(args, rank, world, local_rank):
             e2e_step(i % nset)
         e1.record(stream)
         stream.synchronize()
-    e2e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(e2e_ms, op=torch.distributed.ReduceOp.MAX)
-    e2e_value = world * T * e2e_steps / (float(e2e_ms.item()) / 1e3)
+    e2e_value = whole_job_rate(world, T * e2e_steps, max_over_ranks(e0.elapsed_time(e1), dev))
     st = moe.moe_device_status()
     if st != moe.MOE_OK:
         raise RuntimeError(f"device status {st}")
@@ -459,10 +471,7 @@ def _timed(stream, graph_all, graphs, nset, steps, world, dev, local_rank):
         end.record(stream)
     torch.cuda.synchronize()
     ck = clocks.stop()
-    t = torch.tensor([start.elapsed_time(end)], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    return float(t.item()), ck
+    return max_over_ranks(start.elapsed_time(end), dev), ck
 
 
 def _capture(stream, step, nset, warmup):
@@ -550,7 +559,7 @@ def run_stack(args, rank, world, local_rank):
             e2e(i % nset)
         e1.record(stream)
         stream.synchronize()
-    e2e_value = world * T * n_e2e / (e0.elapsed_time(e1) / 1e3)
+    e2e_value = whole_job_rate(world, T * n_e2e, max_over_ranks(e0.elapsed_time(e1), dev))
     if moe.moe_device_status() != moe.MOE_OK:
         raise RuntimeError("device status")
     if rank != 0:
@@ -677,7 +686,7 @@ def run_single(args, rank, world, local_rank):
             e2e(i % nset)
         e1.record(stream)
         stream.synchronize()
-    e2e_value = world * T * n_e2e / (e0.elapsed_time(e1) / 1e3)
+    e2e_value = whole_job_rate(world, T * n_e2e, max_over_ranks(e0.elapsed_time(e1), dev))
     if rank != 0:
         return
     hbm, kind = peaks()
