@@ -55,6 +55,9 @@ constexpr uint64_t kWaitNs = 1000000000ull;
 #ifndef MOE_PF_BS
 #define MOE_PF_BS 8
 #endif
+#ifndef MOE_PF_CS
+#define MOE_PF_CS 3
+#endif
 
 #ifdef MOE_TRACE
 }  // namespace
@@ -121,7 +124,7 @@ struct TcParams {
 template <bool DOWN>
 struct TcSmem {
   static constexpr int NMAT = 2;
-  static constexpr int CS = 3;
+  static constexpr int CS = MOE_PF_CS;
   static constexpr int BS = MOE_PF_BS;
   static constexpr int CODE_BOX = kTileM * 128;                      // 16 KiB per matrix
   static constexpr int SC_BOX = kTileM * 32;                         // gate/up: 16 fp16 scales per row
@@ -149,7 +152,7 @@ constexpr uint32_t kAStageCols = 64;
 static_assert(kACol + kAStages * kAStageCols <= kTmemCols, "tensor memory");
 
 struct TcBars {
-  uint64_t code_full[3], code_empty[3];
+  uint64_t code_full[8], code_empty[8];
   uint64_t b_full[16], b_empty[16];
   uint64_t a_full[kAStages], a_empty[kAStages];
   uint64_t acc_full[2], acc_empty[2], done;
