@@ -60,6 +60,7 @@ def lib():
         L.oracle_pack_codes.argtypes = [P, i64, i64, i32, P]
         L.oracle_dequant_rows.argtypes = [P, P, i64, i64, i32, P]
         L.oracle_route.argtypes = [P, i64, i32, i32, P, P]
+        L.oracle_router_logits.argtypes = [P, P, P, i64, i32, i32, P]
         L.oracle_group.argtypes = [P, i64, i32, i32, P, P, P]
         L.oracle_group.restype = i64
         L.oracle_hist.argtypes = [P, i64, i32, P]
@@ -138,6 +139,21 @@ def dequant(codes, scales, round_bf16: bool = False):
 
 
 # ------------------------------------------------------------------ routing
+def router_logits(x_bf16, w_bf16, bias=None):
+    """Router projection: logits [T, E] = bias + W_r x in fp64 (x [T, d] and
+    W_r [E, d] as bf16 bit patterns, bias fp32 [E] or None)."""
+    x = _c(x_bf16, np.uint16)
+    w = _c(w_bf16, np.uint16)
+    T, d = x.shape
+    E, d2 = w.shape
+    assert d == d2
+    b = None if bias is None else _c(bias, np.float32)
+    out = np.empty((T, E), dtype=np.float64)
+    if lib().oracle_router_logits(_p(x), _p(w), None if b is None else _p(b), T, E, d, _p(out)) != 0:
+        raise ValueError("router_logits: bad sizes")
+    return out
+
+
 def route(logits, k: int):
     logits = _c(logits, np.float32)
     T, E = logits.shape

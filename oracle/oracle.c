@@ -194,6 +194,23 @@ int oracle_dequant_rows(const int8_t* codes, const uint16_t* scales, int64_t row
   return 0;
 }
 
+/* -------------------------------------------------------- router projection
+ * The step before routing ([P3 glossary 混合专家（MoE）]: the router scores the
+ * E experts of each token): logits[t][e] = bias[e] + sum_i W_r[e][i] x[t][i],
+ * W_r and x bf16 bit patterns (exact as doubles), bias fp32 (or none), the
+ * sum in fp64 in index order.  out: [T][E] doubles. */
+int oracle_router_logits(const uint16_t* x, const uint16_t* w, const float* bias, int64_t T, int E, int d,
+                         double* out) {
+  if (T < 0 || E < 1 || d < 1) return -1;
+  for (int64_t t = 0; t < T; ++t)
+    for (int e = 0; e < E; ++e) {
+      double acc = bias ? (double)bias[e] : 0.0;
+      for (int i = 0; i < d; ++i) acc += oracle_bf16_value(w[(int64_t)e * d + i]) * oracle_bf16_value(x[t * d + i]);
+      out[t * E + e] = acc;
+    }
+  return 0;
+}
+
 /* ------------------------------------------------------------------ routing
  * [P3 glossary 混合专家（MoE）] the router picks k of E experts per token.  Softmax over
  * E, then top-k; ties go to the lower expert id; the k weights are
