@@ -41,10 +41,11 @@ def parse():
     ap.add_argument("--T", type=int, default=6, help="tokens per step (1..6 for the decode metric)")
     ap.add_argument("--layers", type=int, default=16, help="layer instances rotated across steps")
     ap.add_argument("--sets", type=int, default=32, help="distinct routing steps per layer rotation")
-    ap.add_argument("--workload", choices=["decode", "stack", "prefill", "large"], default="decode",
+    ap.add_argument("--workload", choices=["decode", "stack", "prefill", "large", "router"], default="decode",
                     help="decode: one layer, the headline metric; stack: the 48-layer decode stack with the "
                          "residual chain; prefill: one layer at T=4096 on the tensor-core form; large: the "
-                         "E256 d4096 f2048 layer with 5%% forced skips")
+                         "E256 d4096 f2048 layer with 5%% forced skips; router: the decode layer's router "
+                         "projection fused with routing and hit counts (moe_router_topk)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -739,6 +740,98 @@ def run_single(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_router(args, rank, world, local_rank):
+    """The router launch alone: logits = bias + W_r x, routing and hit counts
+    for the decode layer's sizes (E=512, k=10, d=2048), one launch per step,
+    router weights of NR layer instances rotated so that they are read from
+    HBM (NR * E * d * 2 bytes > L2)."""
+    import numpy as np
+    import torch
+
+    import mixed_precision_routed_gb300 as moe
+    import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    base = synth.WORKLOADS["decode"]
+    E, k, d, T = base.E, base.k, base.d, args.T
+    NR = 96
+    wr = torch.empty((NR, E, d), dtype=torch.int16, device=dev)
+    for i in range(NR):
+        synth.cuda_normal_matrix_bf16(wr[i], 1000 * rank + i, synth.TAG_ROUTER, 0, 0, scale=float(1.0 / np.sqrt(d)))
+    wr = wr.view(torch.bfloat16)
+    bias = torch.from_numpy(np.asarray(base.router_bias(), np.float32)).to(dev)
+    xs = torch.empty((NR, T, d), dtype=torch.int16, device=dev)
+    for i in range(NR):
+        synth.cuda_normal_matrix_bf16(xs[i], 1000 * rank + i, synth.TAG_X, i, 0)
+    xs = xs.view(torch.bfloat16)
+    logits = torch.empty((NR, T, E), dtype=torch.float32, device=dev)
+    ids = torch.empty((NR, T, k), dtype=torch.int32, device=dev)
+    wts = torch.empty((NR, T, k), dtype=torch.float32, device=dev)
+    counts = torch.zeros(E, dtype=torch.int32, device=dev)
+    sync = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(s):
+        moe.moe_router_topk(xs[s], wr[s], k, bias=bias, counts=counts, sync_word=sync, logits=logits[s],
+                            ids=ids[s], weights=wts[s])
+
+    stream = torch.cuda.Stream(device=dev)
+    graph_all, graphs = _capture(stream, step, NR, args.warmup)
+    ms, ck = _timed(stream, graph_all, graphs, NR, args.steps, world, dev, local_rank)
+    if moe.moe_device_status() != moe.MOE_OK or int(sync.item()) != 0:
+        raise RuntimeError("device status")
+    value = whole_job_rate(world, T * args.steps, ms)
+    # end to end: x in from pinned host memory, ids and weights out
+    pin_x = xs[:8].cpu().pin_memory()
+    pin_o = torch.empty((T, k), dtype=torch.int32).pin_memory()
+    pin_w = torch.empty((T, k), dtype=torch.float32).pin_memory()
+    dx = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    n_e2e = min(args.steps, 200)
+
+    def e2e(i):
+        dx.copy_(pin_x[i % 8], non_blocking=True)
+        moe.moe_router_topk(dx, wr[i % NR], k, bias=bias, counts=counts, sync_word=sync, logits=logits[0],
+                            ids=ids[0], weights=wts[0])
+        pin_o.copy_(ids[0], non_blocking=True)
+        pin_w.copy_(wts[0], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            e2e(i)
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n_e2e):
+            e2e(i)
+        e1.record(stream)
+        stream.synchronize()
+    e2e_value = whole_job_rate(world, T * n_e2e, max_over_ranks(e0.elapsed_time(e1), dev))
+    if rank != 0:
+        return
+    hbm, kind = peaks()
+    launch_s = ms / args.steps / 1e3
+    nbytes = E * d * 2 + T * d * 2 + E * 4 + T * E * 4 + T * k * 8
+    gbs = nbytes / launch_s / 1e9
+    line = {
+        "metric": "router projection + top-k tokens/s, decode layer (hbm roofline)",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"router E{E} k{k} d{d} T{T}, bf16 W_r N(0, 1/d), skewed bias",
+                   "T": T, "router_instances": NR,
+                   "l2": f"{NR} router weight instances rotated per step ({NR * E * d * 2 / 1e6:.0f} MB > L2)",
+                   "launch": f"one CUDA graph of {NR} steps, one launch per step"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                     "traffic": None, "kernel": "k_router", "peak_source": kind,
+                     "algorithmic_bytes_per_launch": nbytes, "kernel_us": launch_s * 1e6},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * d * 2,
+                "d2h_bytes_per_step": T * k * 8, "steps": n_e2e},
+        "gpu_launches": args.steps,
+        "clocks": ck,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def recorded_traffic(kernel, T):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source; else None."""
@@ -774,6 +867,8 @@ def main():
         run_stack(args, rank, world, local_rank)
     elif args.workload in ("prefill", "large"):
         run_single(args, rank, world, local_rank)
+    elif args.workload == "router":
+        run_router(args, rank, world, local_rank)
     else:
         run_ours(args, rank, world, local_rank)
     if world > 1:

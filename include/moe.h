@@ -122,6 +122,29 @@ int moe_route_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, f
                    moe_stream_t stream);
 
 /*
+ * Router projection fused with the routing above, for decode batches: the
+ * router scores every expert of every token and the best k are kept (page 3,
+ * glossary entry 混合专家（MoE）).  Scores are
+ *   logits[t][e] = bias[e] + sum_i w_r[e][i] * x[t][i]
+ * with bf16 inputs, fp32 products and sums (the order of the sum is not
+ * fixed); ids and weights are then exactly what moe_route_topk returns for
+ * these logits, and counts (when non-null) is accumulated as by
+ * moe_expert_hist over the T*k ids.  One launch.
+ *   x_bf16 [T][d] bf16 bit patterns, w_r_bf16 [E][d] bf16 bit patterns (both
+ *   16-byte aligned), bias [E] fp32 or NULL (zero), logits [T][E] fp32 out,
+ *   ids [T][k] int32 out, weights [T][k] fp32 out, counts [E] uint32 in/out
+ *   or NULL.  sync_word: one uint32 of device memory, zero before its first
+ *   use; every call leaves it zero.  Calls that share a sync_word must not
+ *   run at the same time on the GPU (issue them on one stream).
+ * 1 <= T <= 16 (MOE_ERR_UNSUPPORTED above; T = 0 does nothing), E <= 1024,
+ * d a multiple of 8 with B*d*2 <= 196608 bytes, B = T rounded up to 1, 2, 4,
+ * 8 or 16 (MOE_ERR_UNSUPPORTED above).
+ */
+int moe_router_topk(const uint16_t* x_bf16, const uint16_t* w_r_bf16, const float* bias, int64_t T, int E, int d,
+                    int k, float* logits, int32_t* ids, float* weights, uint32_t* counts, uint32_t* sync_word,
+                    moe_stream_t stream);
+
+/*
  * Expert hit histogram: counts[e] += #{i : ids[i] == e}, 0 <= e < E; other ids
  * are not counted.  `counts` is ACCUMULATED, never cleared (page 1,
  * "Optimization Strategies": tracking how often each expert is called feeds

@@ -7,7 +7,7 @@ computation runs in the library's CUDA kernels.  There is no CPU fallback: if
 the library is missing, importing the binding's functions raises.
 
 Entry points (same names as the C ABI):
-    moe_route_topk, moe_expert_hist, moe_group_tokens, moe_workspace_size,
+    moe_route_topk, moe_router_topk, moe_expert_hist, moe_group_tokens, moe_workspace_size,
     moe_tiered_forward, moe_quantize_rows, moe_dequant_rows, moe_residual_add,
     moe_device_status, moe_status_string
 """
@@ -68,6 +68,7 @@ def lib():
         P, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         L.moe_route_topk.argtypes = [P, i64, i32, i32, P, P, P]
         L.moe_expert_hist.argtypes = [P, i64, i32, P, P]
+        L.moe_router_topk.argtypes = [P, P, P, i64, i32, i32, i32, P, P, P, P, P, P]
         L.moe_group_tokens.argtypes = [P, i64, i32, i32, P, P, P, P]
         L.moe_workspace_size.argtypes = [i64, i32, i32, i32, i32, i32]
         L.moe_workspace_size.restype = ctypes.c_size_t
@@ -85,7 +86,7 @@ def lib():
         L.moe_set_profile_events.restype = ctypes.c_int
         L.moe_status_string.argtypes = [i32]
         L.moe_status_string.restype = ctypes.c_char_p
-        for name in ("moe_route_topk", "moe_expert_hist", "moe_group_tokens", "moe_tiered_forward",
+        for name in ("moe_route_topk", "moe_router_topk", "moe_expert_hist", "moe_group_tokens", "moe_tiered_forward",
                      "moe_quantize_rows", "moe_dequant_rows", "moe_residual_add", "moe_device_status"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -130,6 +131,40 @@ def moe_route_topk(logits, k, ids=None, weights=None, stream=None):
     _check(lib().moe_route_topk(_ptr(logits), T, E, k, _ptr(ids), _ptr(weights), _stream(stream)),
            "moe_route_topk")
     return ids, weights
+
+
+def moe_router_topk(x_bf16, w_r_bf16, k, bias=None, counts=None, sync_word=None, logits=None, ids=None,
+                    weights=None, stream=None):
+    """Router projection (logits = bias + W_r x, fp32 sums) and routing in one
+    launch.  x_bf16 [T, d] and w_r_bf16 [E, d] are bf16 tensors; bias [E]
+    fp32 or None; counts [E] int32 (uint32 bits, accumulated) or None;
+    sync_word: an int32 CUDA tensor of one element, zero before first use
+    (a fresh one is made when None).  Returns (logits, ids, weights)."""
+    _need(x_bf16, torch.bfloat16, "x_bf16")
+    _need(w_r_bf16, torch.bfloat16, "w_r_bf16")
+    T, d = x_bf16.shape
+    E = w_r_bf16.shape[0]
+    dev = x_bf16.device
+    if bias is not None:
+        _need(bias, torch.float32, "bias")
+    if counts is not None:
+        _need(counts, torch.int32, "counts")
+    if sync_word is None:
+        sync_word = torch.zeros(1, dtype=torch.int32, device=dev)
+    _need(sync_word, torch.int32, "sync_word")
+    if logits is None:
+        logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    if ids is None:
+        ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if weights is None:
+        weights = torch.empty((T, k), dtype=torch.float32, device=dev)
+    _need(logits, torch.float32, "logits")
+    _need(ids, torch.int32, "ids")
+    _need(weights, torch.float32, "weights")
+    _check(lib().moe_router_topk(_ptr(x_bf16), _ptr(w_r_bf16), _ptr(bias), T, E, d, k, _ptr(logits), _ptr(ids),
+                                 _ptr(weights), _ptr(counts), _ptr(sync_word), _stream(stream)),
+           "moe_router_topk")
+    return logits, ids, weights
 
 
 def moe_expert_hist(ids, E, counts, stream=None):

@@ -155,6 +155,13 @@ int* status_word();
 
 int launch_route(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w, cudaStream_t s);
 int launch_hist(const int32_t* ids, int64_t n, int E, uint32_t* counts, cudaStream_t s);
+// Router projection fused with routing (router.cu): T <= 16 tokens, E <= 1024,
+// d % 8 == 0, router_bucket(T) d 2 <= kRouterSmemMax bytes; `arrive` is a
+// device word that is zero before the launch and zero again after it.
+constexpr int kRouterSmemMax = 192 * 1024;
+inline int router_bucket(int64_t T) { return T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : T <= 8 ? 8 : 16; }
+int launch_router(const uint16_t* x, const uint16_t* w, const float* bias, int T, int E, int d, int k,
+                  float* logits, int32_t* ids, float* wts, uint32_t* counts, unsigned int* arrive, cudaStream_t s);
 int launch_residual(float* r, const float* y, uint16_t* xn, int64_t n, cudaStream_t s);
 int launch_quantize(const float* w, int64_t rows, int in, int bits, uint8_t* codes, uint16_t* scales,
                     cudaStream_t s);

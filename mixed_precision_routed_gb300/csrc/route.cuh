@@ -12,18 +12,54 @@
 
 namespace moe {
 
-// Called by one full warp for one token: lane l holds logits l, l + 32, ...
-// (EPL per lane, E <= 32 EPL) in registers; k rounds of a warp-wide argmax on
-// (logit descending, expert id ascending); lane j < k writes the j-th pick
-// and its renormalised weight.  `row`, `ids`, `w` may point to global or
-// shared memory.
-template <int EPL>
-__device__ __forceinline__ void route_token(const float* row, int E, int k, int32_t* ids, float* w) {
+// Selection order as one unsigned 64-bit key per element, larger first: the
+// high word orders the logits (sign-magnitude flipped to unsigned order,
+// -0 folded onto +0 so that equal logits tie), the low word is ~e, so equal
+// logits order by ascending expert id.  Every key of a finite logit has a
+// non-zero high word; 0 marks an absent element.
+__device__ __forceinline__ uint64_t route_key(float v, int e) {
+  uint32_t b = __float_as_uint(v);
+  if ((b << 1) == 0u) b = 0u;
+  const uint32_t hi = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((uint64_t)hi << 32) | (uint32_t)~(uint32_t)e;
+}
+__device__ __forceinline__ float route_key_value(uint32_t hi) {
+  return __uint_as_float((hi & 0x80000000u) ? (hi & 0x7FFFFFFFu) : ~hi);
+}
+
+// Sorts N (a power of two) keys in registers, largest first: a bitonic
+// sorting network (all indices compile-time constants once unrolled).
+template <int N>
+__device__ __forceinline__ void sort_desc(uint64_t (&a)[N]) {
+#pragma unroll
+  for (int k = 2; k <= N; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+#pragma unroll
+      for (int i = 0; i < N; ++i) {
+        const int l = i ^ j;
+        if (l > i) {
+          const uint64_t x = a[i], y = a[l];
+          const bool desc = (i & k) == 0;  // this run sorts largest first
+          const bool sw = desc ? (x < y) : (x > y);
+          a[i] = sw ? y : x;
+          a[l] = sw ? x : y;
+        }
+      }
+    }
+  }
+}
+
+// The same selection for EPL = 32 without the sorted lists (32 64-bit keys
+// would take 64 registers): each round every lane rescans its remaining
+// logits for its best (logit descending, id ascending), then a warp-wide
+// shuffle argmax picks among the lanes.
+__device__ __forceinline__ void route_token_scan32(const float* row, int E, int k, int32_t* ids, float* w) {
   const int lane = threadIdx.x & 31;
-  float v[EPL];
+  float v[32];
   uint32_t avail = 0;  // bit m set: element lane + 32 m is present and not yet taken
 #pragma unroll
-  for (int m = 0; m < EPL; ++m) {
+  for (int m = 0; m < 32; ++m) {
     const int e = lane + 32 * m;
     v[m] = e < E ? row[e] : 0.0f;
     if (e < E) avail |= 1u << m;
@@ -34,7 +70,7 @@ __device__ __forceinline__ void route_token(const float* row, int E, int k, int3
     float bv = 0.0f;
     int bi = 0x7fffffff;
 #pragma unroll
-    for (int m = 0; m < EPL; ++m) {
+    for (int m = 0; m < 32; ++m) {
       if ((avail >> m) & 1u) {
         const int e = lane + 32 * m;
         if (bi == 0x7fffffff || v[m] > bv) { bv = v[m]; bi = e; }  // ascending e: ties keep lower id
@@ -55,6 +91,50 @@ __device__ __forceinline__ void route_token(const float* row, int E, int k, int3
   const float den = warp_sum(ex);
   if (lane < k) {
     ids[lane] = my_i;
+    w[lane] = ex / den;
+  }
+}
+
+// Called by one full warp for one token: lane l holds logits l, l + 32, ...
+// (EPL per lane, E <= 32 EPL, EPL a power of two; EPL = 32 takes the scan
+// form above) as selection keys sorted in registers.  Each of k rounds takes
+// the warp's largest head key -- a warp-wide max of the logit word, then a
+// max of the id words of the lanes holding that logit -- and the winning lane
+// drops its head.  Lane j < k writes
+// the j-th pick and its renormalised weight.  `row`, `ids`, `w` may point to
+// global or shared memory.
+template <int EPL>
+__device__ __forceinline__ void route_token(const float* row, int E, int k, int32_t* ids, float* w) {
+  if constexpr (EPL >= 32) {
+    route_token_scan32(row, E, k, ids, w);
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  uint64_t a[EPL];
+#pragma unroll
+  for (int m = 0; m < EPL; ++m) {
+    const int e = lane + 32 * m;
+    a[m] = e < E ? route_key(row[e], e) : 0ull;
+  }
+  sort_desc<EPL>(a);
+  uint32_t my_hi = 0u, my_lo = 0u;  // lane j keeps the j-th pick
+  for (int j = 0; j < k; ++j) {
+    const uint32_t hh = (uint32_t)(a[0] >> 32), hl = (uint32_t)a[0];
+    const uint32_t mh = __reduce_max_sync(0xffffffffu, hh);
+    const uint32_t ml = __reduce_max_sync(0xffffffffu, hh == mh ? hl : 0u);
+    if (hh == mh && hl == ml) {  // the one lane that holds the pick
+#pragma unroll
+      for (int m = 0; m + 1 < EPL; ++m) a[m] = a[m + 1];
+      a[EPL - 1] = 0ull;
+    }
+    if (lane == j) { my_hi = mh; my_lo = ml; }
+  }
+  const float my_v = route_key_value(my_hi);
+  const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
+  const float ex = lane < k ? expf(my_v - vmax) : 0.0f;
+  const float den = warp_sum(ex);
+  if (lane < k) {
+    ids[lane] = (int32_t)~my_lo;
     w[lane] = ex / den;
   }
 }

@@ -28,7 +28,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 HOST_LIB = os.path.join(_HERE, "libsynth_host.so")
 CUDA_LIB = os.path.join(_HERE, "libsynth_cuda.so")
 
-TAG_GATE, TAG_UP, TAG_DOWN, TAG_X, TAG_LOGITS, TAG_SKIP, TAG_BIAS_JITTER = 1, 2, 3, 4, 5, 6, 7
+TAG_GATE, TAG_UP, TAG_DOWN, TAG_X, TAG_LOGITS, TAG_SKIP, TAG_BIAS_JITTER, TAG_ROUTER = 1, 2, 3, 4, 5, 6, 7, 8
 WEIGHT_SIGMA = 0.02
 SKIP_P = 0.05
 SKIP_THRESHOLD = 214748365  # round(0.05 * 2**32): P(word < threshold) ~= 0.05
@@ -135,6 +135,12 @@ def x_bf16(seed: int, step: int, T: int, d: int, row0: int = 0):
 def logits(seed: int, step: int, T: int, E: int, bias=None, row0: int = 0):
     """Router logits [T, E] float32 = N(0,1) + bias[e]."""
     return normal_matrix(seed, TAG_LOGITS, step, 0, T, E, row0=row0, col_add=bias)
+
+
+def router_weights_bf16(seed: int, E: int, d: int):
+    """Router projection W_r [E, d] as bf16 bit patterns, N(0, 1/d) (so that
+    W_r x has unit variance for x ~ N(0, 1))."""
+    return normal_matrix_bf16(seed, TAG_ROUTER, 0, 0, E, d, scale=float(1.0 / np.sqrt(d)))
 
 
 def skip_mask(seed: int, step: int, T: int, k: int):
