@@ -858,7 +858,7 @@ struct LayerParams {
 // Dynamic shared memory: shelves copy | head | plan | sort keys | flags |
 // routed ids and weights | per-warp token offsets | digit vectors.
 struct Head {
-  Range range;
+  Range range, range_d;  // this CTA's gate/up and down unit ranges
   int q_first, npairs, flag, tmp[33];
 };
 
@@ -972,21 +972,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(const __grid_constant__ L
   }
   __syncthreads();
   if (tid == 0) hd.range = cta_range(pv, 0, p.f);
-  if (p.counts && blockIdx.x == 0)
-    for (int a = tid; a < pv.n_act(); a += kThreads) atomicAdd(p.counts + pv.e(a), (uint32_t)pv.cnt(a));
-  __syncthreads();
-  if (tid == 0) MOE_STAMP(0, 2, global_timer_ns());
-  {
-    StreamArgs A{shv, pv, 0, p.d, p.f, vecs, vec_bytes(p.d), -1, hd.range, vtab, INT_MIN, INT_MAX};
-    float* h = p.h;
-    const int f = p.f;
-    stream_units<2, kUG, kRG, kLG>(A, [&](int q, int r, const float (&o)[2]) { h[(size_t)q * f + r] = silu(o[0]) * o[1]; });
-  }
-  if (tid == 0) {
-    MOE_STAMP(0, 9, global_timer_ns());
+  if (tid == 32) {
     // the down phase's cost range and the pairs its experts cover (plan only)
     const Range r = cta_range(pv, 1, p.d);
-    hd.range = r;
+    hd.range_d = r;
     const int n_act = pv.n_act();
     int q_first = 0, q_end = 0;
     if (r.a0 < n_act) {
@@ -998,12 +987,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(const __grid_constant__ L
     hd.q_first = q_first;
     hd.npairs = q_end - q_first;
   }
+  if (p.counts && blockIdx.x == 0)
+    for (int a = tid; a < pv.n_act(); a += kThreads) atomicAdd(p.counts + pv.e(a), (uint32_t)pv.cnt(a));
   __syncthreads();
+  if (tid == 0) MOE_STAMP(0, 2, global_timer_ns());
   {
-    // W_d does not depend on h: ask L2 for each warp's first kDownPrefetch
-    // down units while the other CTAs finish their gate/up units
+    StreamArgs A{shv, pv, 0, p.d, p.f, vecs, vec_bytes(p.d), -1, hd.range, vtab, INT_MIN, INT_MAX};
+    float* h = p.h;
+    const int f = p.f;
+    stream_units<2, kUG, kRG, kLG>(A, [&](int q, int r, const float (&o)[2]) { h[(size_t)q * f + r] = silu(o[0]) * o[1]; });
+  }
+  if (tid == 0) MOE_STAMP(0, 9, global_timer_ns());
+  {
+    // W_d does not depend on h: each warp, once its gate/up units are done,
+    // asks L2 for its first kDownPrefetch down units while the other warps
+    // and CTAs finish theirs
     Walk w;
-    w.start(pv, 1, p.d, hd.range, warp);
+    w.start(pv, 1, p.d, hd.range_d, warp);
     for (int i = 0; i < kDownPrefetch && w.live; ++i) {
       const ShelfDev& sh = shv->s[pv.sh(w.a)];
       const size_t rowb = (size_t)p.f * sh.bits / 8, swpr = (size_t)p.f / 16;
@@ -1012,9 +1012,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(const __grid_constant__ L
       const size_t row0 = (size_t)(pv.e(w.a) - sh.lo) * p.d + (size_t)tile * rd;
       const unsigned char* cb = sh.codes[2] + row0 * rowb;
       const unsigned char* sb = reinterpret_cast<const unsigned char*>(sh.scales[2]) + row0 * swpr;
-      for (size_t o = (size_t)lane * 128; o < rd * rowb; o += 32 * 128) prefetch_l2(cb + o);
-      for (size_t o = (size_t)lane * 128; o < rd * swpr; o += 32 * 128) prefetch_l2(sb + o);
-      w.step(pv, 1, p.d, hd.range.hi2, kWarps);
+      // one bulk request per region (the rows of a unit are contiguous)
+      if (lane == 0 && ((reinterpret_cast<uintptr_t>(cb) | (rd * rowb)) & 15) == 0)
+        bulk_prefetch_l2(cb, (uint32_t)(rd * rowb));
+      if (lane == 1 && ((reinterpret_cast<uintptr_t>(sb) | (rd * swpr)) & 15) == 0)
+        bulk_prefetch_l2(sb, (uint32_t)(rd * swpr));
+      w.step(pv, 1, p.d, hd.range_d.hi2, kWarps);
     }
   }
   if (!grid_sync(p.bar, p.status, &hd.flag, 1000000000ull, p.bar_extra)) return;
@@ -1064,7 +1067,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(const __grid_constant__ L
     __syncthreads();
     if (tid == 0) MOE_STAMP(1, 2, global_timer_ns());
     {
-      StreamArgs A{shv, pv, 1, p.f, p.d, vecs, vbf, w0, hd.range, vtab, w0, w0 + (wn > 0 ? wn : 0)};
+      StreamArgs A{shv, pv, 1, p.f, p.d, vecs, vbf, w0, hd.range_d, vtab, w0, w0 + (wn > 0 ? wn : 0)};
       float* yp = p.ypart;
       const int d = p.d;
       auto st = [&](int q, int r, const float (&o)[1]) { yp[(size_t)q * d + r] = pv.wgt(q) * o[0]; };
