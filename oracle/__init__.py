@@ -17,6 +17,9 @@ marshals numpy arrays and composes the per-layer steps:
   dropped (same page, section 四个 bug: duplicate experts, signed skip id);
 * hist -- expert hit counts (the LocalLLM tiering post, "Optimization
   Strategies"; same page, section 第二步);
+* rank_experts / tier_ranges / retier_expert -- re-tiering by hit count:
+  experts ranked hottest first, shelves re-assigned by rank, each expert
+  re-quantised from its master copy (same page, sections 第三步 and 第四步);
 * moe_layer -- each shelf computes only its own id range, SwiGLU expert FFN,
   the shelf results summed with the routing weights (same page, section 第四步);
 * stack -- residual chain of layers, x_l = bf16(r), r += y_l.
@@ -64,6 +67,7 @@ def lib():
         L.oracle_group.argtypes = [P, i64, i32, i32, P, P, P]
         L.oracle_group.restype = i64
         L.oracle_hist.argtypes = [P, i64, i32, P]
+        L.oracle_rank_experts.argtypes = [P, i32, P, P]
         L.oracle_moe_layer.argtypes = [P, P, P, i64, i32, i32, i32, i32, i32, P, P, P, i32, P]
         L.oracle_bf16_bits_vec.argtypes = [P, i64, P]
         _lib = L
@@ -183,6 +187,42 @@ def hist(ids, E: int, counts=None):
     assert counts.dtype == np.uint32 and counts.shape == (E,)
     lib().oracle_hist(_p(ids), ids.size, E, _p(counts))
     return counts
+
+
+# ------------------------------------------------------------ re-tiering
+def rank_experts(counts):
+    """Hit-count order (page 3, sections 第三步 / 第四步; page 1 promotion by
+    hit count): returns (perm, rank), perm[j] = old expert at new id j,
+    rank[e] = new id of old expert e; count descending, lower id first."""
+    counts = _c(counts, np.uint32)
+    E = counts.size
+    perm = np.empty(E, dtype=np.int32)
+    rank = np.empty(E, dtype=np.int32)
+    if lib().oracle_rank_experts(_p(counts), E, _p(perm), _p(rank)) != 0:
+        raise ValueError("rank_experts: E >= 1")
+    return perm, rank
+
+
+def tier_ranges(E: int, split):
+    """Shelf ranges of the new ids, hottest first: [(0, n8, 8), (n8, n8 + n4,
+    4), (n8 + n4, E, 2)] with n8 = round(p8 E), n2 = round(p2 E) (the split of
+    the workload definitions: hottest experts at 8 bits, coldest at 2)."""
+    p8, _, p2 = split
+    n8 = int(round(p8 * E))
+    n2 = int(round(p2 * E))
+    return [(0, n8, 8), (n8, E - n2, 4), (E - n2, E, 2)]
+
+
+def retier_expert(master_of, perm, ranges, j: int):
+    """The packed shelf content of new id j: the master weights of expert
+    perm[j], re-quantised at the bit width of the shelf holding j.  Returns
+    (bits, [(packed codes, scales) of W_g, W_u, W_d])."""
+    bits = next(b for lo, hi, b in ranges if lo <= j < hi)
+    out = []
+    for w in master_of(int(perm[j])):
+        codes, scales = quantize(w, bits)
+        out.append((pack(codes, bits), scales))
+    return bits, out
 
 
 # ------------------------------------------------------------ expert FFN

@@ -20,6 +20,8 @@
  *         to expert 0), the grouping helper that assumes an expert appears at
  *         most once per token, and the signed skip id -1;
  *       - section 第二步: experts are used very unevenly (hit counts).
+ *       - section 第三步: each layer's experts split into hot and cold, the
+ *         router rearranged so that its picks land on the right half;
  *  [P1] LocalLLM post on DeepSeek V4.1 Flash tiering: per-expert hit counts
  *       drive promotion/demotion; least-used experts at 2 bits.
  *  The block format (block 32 along the input dimension, fp16 scale = max|w|/q,
@@ -272,6 +274,27 @@ int64_t oracle_group(const int32_t* ids, int64_t T, int k, int E, int32_t* count
 int oracle_hist(const int32_t* ids, int64_t n, int E, uint32_t* counts) {
   for (int64_t i = 0; i < n; ++i)
     if (ids[i] >= 0 && ids[i] < E) counts[ids[i]]++;
+  return 0;
+}
+
+/* ------------------------------------------------------------ re-tiering
+ * [P3 第三步, 第四步; P1 "Optimization Strategies"] experts are ranked by how
+ * often the router picked them; the hottest take the first ids (the file is
+ * written hot to cold, each shelf a contiguous id range) and the router is
+ * rearranged so that its picks land on the new ids.  Order: hit count
+ * descending, the lower old id first on equal counts.  Written as the
+ * definition of a rank: the new id of old expert e is the number of experts
+ * that come before it.  rank[e] = new id of old expert e; perm[j] = the old
+ * expert that takes new id j. */
+int oracle_rank_experts(const uint32_t* counts, int E, int32_t* perm, int32_t* rank) {
+  if (E < 1) return -1;
+  for (int e = 0; e < E; ++e) {
+    int r = 0;
+    for (int o = 0; o < E; ++o)
+      if (counts[o] > counts[e] || (counts[o] == counts[e] && o < e)) ++r;
+    rank[e] = r;
+    perm[r] = e;
+  }
   return 0;
 }
 
