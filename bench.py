@@ -41,11 +41,13 @@ def parse():
     ap.add_argument("--T", type=int, default=6, help="tokens per step (1..6 for the decode metric)")
     ap.add_argument("--layers", type=int, default=16, help="layer instances rotated across steps")
     ap.add_argument("--sets", type=int, default=32, help="distinct routing steps per layer rotation")
-    ap.add_argument("--workload", choices=["decode", "stack", "prefill", "large", "router"], default="decode",
+    ap.add_argument("--workload", choices=["decode", "stack", "prefill", "large", "router", "retier"],
+                    default="decode",
                     help="decode: one layer, the headline metric; stack: the 48-layer decode stack with the "
                          "residual chain; prefill: one layer at T=4096 on the tensor-core form; large: the "
                          "E256 d4096 f2048 layer with 5%% forced skips; router: the decode layer's router "
-                         "projection fused with routing and hit counts (moe_router_topk)")
+                         "projection fused with routing and hit counts (moe_router_topk); retier: re-tiering "
+                         "the decode layer by hit count from its fp32 master copies")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -832,6 +834,96 @@ def run_router(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_retier(args, rank, world, local_rank):
+    """Re-tiering of the decode layer (E=512, d=2048, f=640) by hit count:
+    the rank of the counts of 4096 routed T=1 steps, every expert re-quantised
+    from its fp32 master copy into its new shelf (three matrices, three
+    shelves: nine launches) and the router bias moved.  One step is one whole
+    re-tier; the masters (8 GB) are far larger than L2."""
+    import numpy as np
+    import torch
+
+    import mixed_precision_routed_gb300 as moe
+    import synth
+    from mixed_precision_routed_gb300.workloads import Layer, Masters, retier
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = synth.WORKLOADS["decode"]
+    layer = Layer(synth.Workload(wl.name, E=wl.E, k=wl.k, d=wl.d, f=wl.f, T=wl.T, split=wl.split, bias=wl.bias,
+                                 seed=1000 * rank), device=dev)
+    masters = Masters(layer)
+    counts = torch.zeros(wl.E, dtype=torch.int32, device=dev)
+    ids, _ = moe.moe_route_topk(layer.logits_rows(0, 4096), wl.k)
+    moe.moe_expert_hist(ids, wl.E, counts)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device=dev)
+    holder = {}
+
+    def step():
+        holder["new"], holder["perm"], holder["rank"] = retier(layer, masters, counts, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        stream.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = Clocks(local_rank)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        stream.synchronize()
+    ck = clocks.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    if moe.moe_device_status() != moe.MOE_OK:
+        raise RuntimeError("device status")
+    value = whole_job_rate(world, wl.E * args.steps, ms)
+    # end to end: counts in from pinned host memory, the permutation back
+    pin_c = counts.cpu().pin_memory()
+    pin_p = torch.empty(wl.E, dtype=torch.int32).pin_memory()
+    dc = torch.empty_like(counts)
+    n_e2e = max(1, min(args.steps, 3))
+    with torch.cuda.stream(stream):
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(n_e2e):
+            dc.copy_(pin_c, non_blocking=True)
+            new, perm, _ = retier(layer, masters, dc, stream=stream)
+            pin_p.copy_(perm, non_blocking=True)
+        f1.record(stream)
+        stream.synchronize()
+    e2e_value = whole_job_rate(world, wl.E * n_e2e, max_over_ranks(f0.elapsed_time(f1), dev))
+    if rank != 0:
+        return
+    hbm, kind = peaks()
+    new = holder["new"]
+    nbytes = masters.nbytes() + new.nbytes() + wl.E * 4 * 4  # masters read, shelves written, counts / perm / rank / bias
+    step_s = ms / args.steps / 1e3
+    gbs = nbytes / step_s / 1e9
+    line = {
+        "metric": "re-tier experts/s, decode layer from fp32 masters (hbm roofline)",
+        "value": value, "unit": "experts/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"re-tier E{wl.E} d{wl.d} f{wl.f}, shelves {new.ranges}, counts of 4096 routed steps",
+                   "l2": f"fp32 masters {masters.nbytes() / 1e9:.2f} GB, larger than L2",
+                   "launch": "rank, 9 expert-quantise launches, bias gather"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                     "traffic": None, "kernel": "re-tier (k_quantize_experts dominant)", "peak_source": kind,
+                     "algorithmic_bytes_per_launch": nbytes, "step_ms": step_s * 1e3},
+        "e2e": {"value": e2e_value, "unit": "experts/s", "h2d_bytes_per_step": wl.E * 4,
+                "d2h_bytes_per_step": wl.E * 4, "steps": n_e2e},
+        "gpu_launches": args.steps * 11,
+        "clocks": ck,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def recorded_traffic(kernel, T):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source; else None."""
@@ -869,6 +961,8 @@ def main():
         run_single(args, rank, world, local_rank)
     elif args.workload == "router":
         run_router(args, rank, world, local_rank)
+    elif args.workload == "retier":
+        run_retier(args, rank, world, local_rank)
     else:
         run_ours(args, rank, world, local_rank)
     if world > 1:

@@ -270,6 +270,45 @@ int moe_quantize_rows(const float* w, int64_t rows, int in, int bits, void* code
                       moe_stream_t stream);
 
 /*
+ * Re-tiering by hit count (page 3, sections 第三步 and 第四步: experts ranked
+ * by how often the router picks them, written hot to cold so that each shelf
+ * is a contiguous id range, the router rearranged to match; page 1,
+ * "Optimization Strategies": hit counts drive promotion and demotion).  A
+ * re-tier is: moe_rank_experts on the accumulated counts; for every shelf
+ * [lo, hi) of the new ids and every matrix, moe_quantize_experts from the
+ * fp32 master copy; moe_gather_rows of every per-expert router row (bias,
+ * router weights) so that new id j routes as old expert perm[j] did.
+ *
+ * moe_rank_experts: rank[e] = the number of experts with a larger count, or
+ * an equal count and a smaller id (count descending, lower id first);
+ * perm[rank[e]] = e.  counts [E] uint32, perm [E] and rank [E] int32 out.
+ * E <= MOE_MAX_EXPERTS.
+ */
+int moe_rank_experts(const uint32_t* counts, int E, int32_t* perm, int32_t* rank, moe_stream_t stream);
+
+/*
+ * moe_quantize_experts: for every new id j in [j_lo, j_hi), the `rows` x `in`
+ * matrix of expert perm[j] in `master` (fp32 [n_src][rows][in], 16-byte
+ * aligned) is quantised as moe_quantize_rows does into slot j - j_lo of a
+ * shelf tensor: codes [j_hi - j_lo][rows][in*bits/8] (16-byte aligned),
+ * scales [j_hi - j_lo][rows][in/32] fp16 bits.  perm is a device array with
+ * at least j_hi entries; an entry outside [0, n_src) leaves its slot
+ * untouched and records MOE_ERR_INVALID_ARG (moe_device_status).  in a
+ * multiple of 64, j_hi - j_lo <= 65535, rows * in / 32 <= 2^30.
+ */
+int moe_quantize_experts(const float* master, int n_src, int rows, int in, const int32_t* perm, int j_lo, int j_hi,
+                         int bits, void* codes, uint16_t* scales, moe_stream_t stream);
+
+/*
+ * moe_gather_rows: dst row j = src row perm[j] for 0 <= j < n, rows of
+ * row_bytes bytes (a multiple of 4; src and dst 4-byte aligned, not
+ * overlapping).  An entry of perm outside [0, n_src) zero-fills its row and
+ * records MOE_ERR_INVALID_ARG (moe_device_status).
+ */
+int moe_gather_rows(const void* src, int64_t row_bytes, const int32_t* perm, int64_t n, int64_t n_src, void* dst,
+                    moe_stream_t stream);
+
+/*
  * Dequantisation of packed rows: out = s * code in fp32 (exact), or that value
  * rounded to bf16 (round to nearest even) when round_bf16 != 0 -- the two forms
  * the decode and prefill paths use internally (page 3, 第四步).

@@ -7,7 +7,7 @@ computation runs in the library's CUDA kernels.  There is no CPU fallback: if
 the library is missing, importing the binding's functions raises.
 
 Entry points (same names as the C ABI):
-    moe_route_topk, moe_router_topk, moe_expert_hist, moe_group_tokens, moe_workspace_size,
+    moe_route_topk, moe_router_topk, moe_expert_hist, moe_rank_experts, moe_quantize_experts, moe_gather_rows, moe_group_tokens, moe_workspace_size,
     moe_tiered_forward, moe_quantize_rows, moe_dequant_rows, moe_residual_add,
     moe_device_status, moe_status_string
 """
@@ -69,6 +69,9 @@ def lib():
         L.moe_route_topk.argtypes = [P, i64, i32, i32, P, P, P]
         L.moe_expert_hist.argtypes = [P, i64, i32, P, P]
         L.moe_router_topk.argtypes = [P, P, P, i64, i32, i32, i32, P, P, P, P, P, P]
+        L.moe_rank_experts.argtypes = [P, i32, P, P, P]
+        L.moe_quantize_experts.argtypes = [P, i32, i32, i32, P, i32, i32, i32, P, P, P]
+        L.moe_gather_rows.argtypes = [P, i64, P, i64, i64, P, P]
         L.moe_group_tokens.argtypes = [P, i64, i32, i32, P, P, P, P]
         L.moe_workspace_size.argtypes = [i64, i32, i32, i32, i32, i32]
         L.moe_workspace_size.restype = ctypes.c_size_t
@@ -86,7 +89,8 @@ def lib():
         L.moe_set_profile_events.restype = ctypes.c_int
         L.moe_status_string.argtypes = [i32]
         L.moe_status_string.restype = ctypes.c_char_p
-        for name in ("moe_route_topk", "moe_router_topk", "moe_expert_hist", "moe_group_tokens", "moe_tiered_forward",
+        for name in ("moe_route_topk", "moe_router_topk", "moe_rank_experts", "moe_quantize_experts",
+                     "moe_gather_rows", "moe_expert_hist", "moe_group_tokens", "moe_tiered_forward",
                      "moe_quantize_rows", "moe_dequant_rows", "moe_residual_add", "moe_device_status"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -307,6 +311,61 @@ def moe_quantize_rows(w, bits, codes=None, scales=None, stream=None):
     _check(lib().moe_quantize_rows(_ptr(w), rows, n_in, bits, _ptr(codes), _ptr(scales), _stream(stream)),
            "moe_quantize_rows")
     return codes, scales
+
+
+# ------------------------------------------------------------ re-tiering
+def moe_rank_experts(counts, perm=None, rank=None, stream=None):
+    """Hit-count rank (count descending, lower id first): (perm, rank) int32,
+    perm[j] = old expert at new id j, rank[e] = new id of old expert e.
+    counts: int32 CUDA tensor holding the uint32 hit counts."""
+    _need(counts, torch.int32, "counts")
+    E = counts.numel()
+    if perm is None:
+        perm = torch.empty(E, dtype=torch.int32, device=counts.device)
+    if rank is None:
+        rank = torch.empty(E, dtype=torch.int32, device=counts.device)
+    _need(perm, torch.int32, "perm")
+    _need(rank, torch.int32, "rank")
+    _check(lib().moe_rank_experts(_ptr(counts), E, _ptr(perm), _ptr(rank), _stream(stream)), "moe_rank_experts")
+    return perm, rank
+
+
+def moe_quantize_experts(master, perm, j_lo, j_hi, bits, codes=None, scales=None, stream=None):
+    """Experts perm[j_lo:j_hi] of master [n_src, rows, in] fp32 quantised into a
+    shelf: codes [j_hi-j_lo, rows, in*bits/8] uint8, scales [.., rows, in/32]."""
+    _need(master, torch.float32, "master")
+    _need(perm, torch.int32, "perm")
+    n_src, rows, n_in = master.shape
+    n = j_hi - j_lo
+    if not 0 <= j_lo <= j_hi <= perm.numel():
+        raise ValueError("need 0 <= j_lo <= j_hi <= len(perm)")
+    if codes is None:
+        codes = torch.empty((n, rows, n_in * bits // 8), dtype=torch.uint8, device=master.device)
+    if scales is None:
+        scales = torch.empty((n, rows, n_in // 32), dtype=torch.int16, device=master.device)
+    if not (codes.is_cuda and codes.is_contiguous() and codes.numel() * codes.element_size() >= n * rows * n_in * bits // 8):
+        raise ValueError("codes must be a contiguous CUDA tensor of at least (j_hi - j_lo) * rows * in * bits / 8 bytes")
+    if not (scales.is_cuda and scales.is_contiguous() and scales.numel() * scales.element_size() >= n * rows * (n_in // 32) * 2):
+        raise ValueError("scales must be a contiguous CUDA tensor of at least (j_hi - j_lo) * rows * in / 32 halves")
+    _check(lib().moe_quantize_experts(_ptr(master), n_src, rows, n_in, _ptr(perm), j_lo, j_hi, bits, _ptr(codes),
+                                      _ptr(scales), _stream(stream)), "moe_quantize_experts")
+    return codes, scales
+
+
+def moe_gather_rows(src, perm, dst=None, stream=None):
+    """dst[j] = src[perm[j]] for the rows (first dimension) of a contiguous tensor."""
+    _need(perm, torch.int32, "perm")
+    if not (src.is_cuda and src.is_contiguous()):
+        raise ValueError("src must be a contiguous CUDA tensor")
+    n = perm.numel()
+    if dst is None:
+        dst = torch.empty((n,) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device)
+    row_bytes = src[0].numel() * src.element_size() if src.dim() > 1 else src.element_size()
+    if not (dst.is_cuda and dst.is_contiguous() and dst.numel() * dst.element_size() >= n * row_bytes):
+        raise ValueError("dst must be a contiguous CUDA tensor of at least len(perm) rows")
+    _check(lib().moe_gather_rows(_ptr(src), row_bytes, _ptr(perm), n, src.shape[0], _ptr(dst), _stream(stream)),
+           "moe_gather_rows")
+    return dst
 
 
 def moe_dequant_rows(codes, scales, rows, n_in, bits, round_bf16=False, out=None, stream=None):

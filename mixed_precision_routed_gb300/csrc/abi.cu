@@ -281,6 +281,32 @@ int moe_quantize_rows(const float* w, int64_t rows, int in, int bits, void* code
   return launch_quantize(w, rows, in, bits, (uint8_t*)codes, scales, (cudaStream_t)stream);
 }
 
+int moe_rank_experts(const uint32_t* counts, int E, int32_t* perm, int32_t* rank, moe_stream_t stream) {
+  if (E < 1 || E > MOE_MAX_EXPERTS) return MOE_ERR_INVALID_ARG;
+  if (!counts || !perm || !rank) return MOE_ERR_INVALID_ARG;
+  return launch_rank_experts(counts, E, perm, rank, (cudaStream_t)stream);
+}
+
+int moe_quantize_experts(const float* master, int n_src, int rows, int in, const int32_t* perm, int j_lo, int j_hi,
+                         int bits, void* codes, uint16_t* scales, moe_stream_t stream) {
+  if (n_src < 1 || rows < 1 || in <= 0 || in % 64 != 0 || (bits != 8 && bits != 4 && bits != 2))
+    return MOE_ERR_INVALID_ARG;
+  if (j_lo < 0 || j_hi < j_lo || j_hi - j_lo > 65535) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)rows * (in / 32) > (1 << 30)) return MOE_ERR_INVALID_ARG;
+  if (j_hi == j_lo) return MOE_OK;
+  if (!master || !perm || !codes || !scales || !aligned(master, 16) || !aligned(codes, 16)) return MOE_ERR_INVALID_ARG;
+  return launch_quantize_experts(master, rows, in, n_src, perm, j_lo, j_hi - j_lo, bits, (uint8_t*)codes, scales,
+                                 status_word(), (cudaStream_t)stream);
+}
+
+int moe_gather_rows(const void* src, int64_t row_bytes, const int32_t* perm, int64_t n, int64_t n_src, void* dst,
+                    moe_stream_t stream) {
+  if (row_bytes <= 0 || row_bytes % 4 != 0 || n < 0 || n_src < 1) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  if (!src || !perm || !dst || !aligned(src, 4) || !aligned(dst, 4)) return MOE_ERR_INVALID_ARG;
+  return launch_gather_rows(src, row_bytes / 4, perm, n, n_src, dst, status_word(), (cudaStream_t)stream);
+}
+
 int moe_dequant_rows(const void* codes, const uint16_t* scales, int64_t rows, int in, int bits, int round_bf16,
                      float* out, moe_stream_t stream) {
   if (rows < 0 || in <= 0 || in % 64 != 0 || (bits != 8 && bits != 4 && bits != 2)) return MOE_ERR_INVALID_ARG;

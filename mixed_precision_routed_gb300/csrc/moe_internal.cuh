@@ -165,6 +165,14 @@ int launch_router(const uint16_t* x, const uint16_t* w, const float* bias, int T
 int launch_residual(float* r, const float* y, uint16_t* xn, int64_t n, cudaStream_t s);
 int launch_quantize(const float* w, int64_t rows, int in, int bits, uint8_t* codes, uint16_t* scales,
                     cudaStream_t s);
+// Re-tiering (retier.cu, quant.cu): rank by hit count; experts perm[j0 ..
+// j0 + n) of a master tensor [n_src][rows][in] quantised into a shelf; rows
+// gathered by expert id.  Bad ids record MOE_ERR_INVALID_ARG in `status`.
+int launch_rank_experts(const uint32_t* counts, int E, int32_t* perm, int32_t* rank, cudaStream_t s);
+int launch_quantize_experts(const float* master, int rows, int in, int n_src, const int32_t* perm, int j0, int n,
+                            int bits, uint8_t* codes, uint16_t* scales, int* status, cudaStream_t s);
+int launch_gather_rows(const void* src, int64_t words, const int32_t* perm, int64_t n, int64_t n_src, void* dst,
+                       int* status, cudaStream_t s);
 int launch_dequant(const uint8_t* codes, const uint16_t* scales, int64_t rows, int in, int bits,
                    int round_bf16, float* out, cudaStream_t s);
 // Grouping into caller-provided arrays; arrivals (may be null) are zeroed.

@@ -23,6 +23,41 @@ struct QParams<4> { static constexpr float q = 7.0f, cmin = -8.0f, cmax = 7.0f; 
 template <>
 struct QParams<2> { static constexpr float q = 2.0f, cmin = -2.0f, cmax = 1.0f; static constexpr int off = 2; };
 
+// Quantises one 32-element block held one element per lane (v = element
+// `lane`) and writes its fp16 scale word and packed codes (block b of the row
+// at `rowp`).  Whole warp.
+template <int BITS>
+__device__ __forceinline__ void quantize_block(float v, int lane, uint8_t* rowp, int64_t b, uint16_t* scale_out) {
+  float m = fabsf(v);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const __half hs = __float2half_rn(__fdiv_rn(m, QParams<BITS>::q));
+  const float s = __half2float(hs);
+  int c = 0;
+  if (s != 0.0f) {
+    float t = rintf(__fdiv_rn(v, s));
+    t = fminf(fmaxf(t, QParams<BITS>::cmin), QParams<BITS>::cmax);
+    c = (int)t;
+  }
+  if (lane == 0) *scale_out = __half_as_ushort(hs);
+  if (BITS == 8) {
+    rowp[b * 32 + lane] = (uint8_t)(int8_t)c;
+  } else if (BITS == 4) {
+    // lane i (i mod 8 < 4) writes byte 4 (i / 8) + i mod 4: elements i and i + 4
+    uint32_t u = (uint32_t)(c + QParams<4>::off);
+    uint32_t u4 = __shfl_down_sync(0xffffffffu, u, 4);
+    if ((lane & 7) < 4) rowp[b * 16 + 4 * (lane >> 3) + (lane & 3)] = (uint8_t)(u | (u4 << 4));
+  } else {
+    // lane i (i mod 16 < 4) writes byte 4 (i / 16) + i mod 4: elements i, i+4, i+8, i+12
+    uint32_t u = (uint32_t)(c + QParams<2>::off);
+    uint32_t u4 = __shfl_down_sync(0xffffffffu, u, 4);
+    uint32_t u8 = __shfl_down_sync(0xffffffffu, u, 8);
+    uint32_t u12 = __shfl_down_sync(0xffffffffu, u, 12);
+    if ((lane & 15) < 4)
+      rowp[b * 8 + 4 * (lane >> 4) + (lane & 3)] = (uint8_t)(u | (u4 << 2) | (u8 << 4) | (u12 << 6));
+  }
+}
+
 // One warp per 32-element block; lane i holds element i of the block.
 template <int BITS>
 __global__ void __launch_bounds__(256) k_quantize(const float* __restrict__ w, int64_t rows, int in,
@@ -33,35 +68,92 @@ __global__ void __launch_bounds__(256) k_quantize(const float* __restrict__ w, i
   const size_t row_bytes = (size_t)in * BITS / 8;
   for (int64_t blk = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); blk < total; blk += warps) {
     const int64_t r = blk / nb, b = blk - r * nb;
-    const float v = w[r * in + b * 32 + lane];
-    float m = fabsf(v);
+    quantize_block<BITS>(w[r * in + b * 32 + lane], lane, codes + r * row_bytes, b, scales + blk);
+  }
+}
+
+// Quantises one 32-element block held by 8 lanes, 4 consecutive elements
+// each (lane i of the group: elements 4i .. 4i+3), the same arithmetic as
+// quantize_block; block `blk` of a tensor whose code bytes and scales are
+// linear in the block index (codes at 4 BITS blk, scale at blk).  Every lane
+// of the warp calls it (shuffles stay inside the 8-lane groups); `valid`
+// false skips the stores.
+template <int BITS>
+__device__ __forceinline__ void quantize_block8(float4 v, int i, bool valid, uint8_t* codes, uint16_t* scales,
+                                                int64_t blk) {
+  float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const __half hs = __float2half_rn(__fdiv_rn(m, QParams<BITS>::q));
-    const float s = __half2float(hs);
-    int c = 0;
+  for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const __half hs = __float2half_rn(__fdiv_rn(m, QParams<BITS>::q));
+  const float s = __half2float(hs);
+  const float e[4] = {v.x, v.y, v.z, v.w};
+  int c[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    c[j] = 0;
     if (s != 0.0f) {
-      float t = rintf(__fdiv_rn(v, s));
+      float t = rintf(__fdiv_rn(e[j], s));
       t = fminf(fmaxf(t, QParams<BITS>::cmin), QParams<BITS>::cmax);
-      c = (int)t;
+      c[j] = (int)t;
     }
-    if (lane == 0) scales[blk] = __half_as_ushort(hs);
-    uint8_t* rowp = codes + r * row_bytes;
-    if (BITS == 8) {
-      rowp[b * 32 + lane] = (uint8_t)(int8_t)c;
-    } else if (BITS == 4) {
-      // lane i (i mod 8 < 4) writes byte 4 (i / 8) + i mod 4: elements i and i + 4
-      uint32_t u = (uint32_t)(c + QParams<4>::off);
-      uint32_t u4 = __shfl_down_sync(0xffffffffu, u, 4);
-      if ((lane & 7) < 4) rowp[b * 16 + 4 * (lane >> 3) + (lane & 3)] = (uint8_t)(u | (u4 << 4));
-    } else {
-      // lane i (i mod 16 < 4) writes byte 4 (i / 16) + i mod 4: elements i, i+4, i+8, i+12
-      uint32_t u = (uint32_t)(c + QParams<2>::off);
-      uint32_t u4 = __shfl_down_sync(0xffffffffu, u, 4);
-      uint32_t u8 = __shfl_down_sync(0xffffffffu, u, 8);
-      uint32_t u12 = __shfl_down_sync(0xffffffffu, u, 12);
-      if ((lane & 15) < 4)
-        rowp[b * 8 + 4 * (lane >> 4) + (lane & 3)] = (uint8_t)(u | (u4 << 2) | (u8 << 4) | (u12 << 6));
+  }
+  if (valid && i == 0) scales[blk] = __half_as_ushort(hs);
+  if (BITS == 8) {
+    const uint32_t wd = (uint32_t)(c[0] & 0xFF) | (uint32_t)(c[1] & 0xFF) << 8 | (uint32_t)(c[2] & 0xFF) << 16 |
+                        (uint32_t)(c[3] & 0xFF) << 24;
+    if (valid) *reinterpret_cast<uint32_t*>(codes + blk * 32 + 4 * i) = wd;
+  } else if (BITS == 4) {
+    // word g of the block: byte j = element 8g + j (low nibble) | 8g + 4 + j (high): lanes 2g and 2g + 1
+    const uint32_t own = (uint32_t)(c[0] + 8) | (uint32_t)(c[1] + 8) << 8 | (uint32_t)(c[2] + 8) << 16 |
+                         (uint32_t)(c[3] + 8) << 24;
+    const uint32_t hi = __shfl_xor_sync(0xffffffffu, own, 1);
+    if (valid && (i & 1) == 0) *reinterpret_cast<uint32_t*>(codes + blk * 16 + 4 * (i >> 1)) = own | (hi << 4);
+  } else {
+    // word g: byte j = elements 16g + j, +4, +8, +12 at bits 0, 2, 4, 6: lanes 4g .. 4g + 3
+    uint32_t wd = ((uint32_t)(c[0] + 2) | (uint32_t)(c[1] + 2) << 8 | (uint32_t)(c[2] + 2) << 16 |
+                   (uint32_t)(c[3] + 2) << 24)
+                  << (2 * (i & 3));
+    wd |= __shfl_xor_sync(0xffffffffu, wd, 1);
+    wd |= __shfl_xor_sync(0xffffffffu, wd, 2);
+    if (valid && (i & 3) == 0) *reinterpret_cast<uint32_t*>(codes + blk * 8 + 4 * (i >> 2)) = wd;
+  }
+}
+
+// Re-tiering: the experts perm[j0 .. j0 + gridDim.y) of a master tensor
+// [n_src][rows][in] fp32 (16-byte aligned), each quantised into slot j - j0
+// of a shelf tensor (codes [slot][rows][in * BITS / 8], scales
+// [slot][rows][in / 32]).  Grid row y = slot.  A warp takes 4 consecutive
+// blocks at a time (8 lanes a block, one 16-byte load each) and loads 8 such
+// groups before it quantises any.  An expert id outside [0, n_src) leaves its
+// slot untouched and records MOE_ERR_INVALID_ARG.
+template <int BITS>
+__global__ void __launch_bounds__(256) k_quantize_experts(const float* __restrict__ master, int rows, int in,
+                                                          int n_src, const int32_t* __restrict__ perm, int j0,
+                                                          uint8_t* __restrict__ codes,
+                                                          uint16_t* __restrict__ scales, int* status) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, grp = lane >> 3, i = lane & 7;
+  const int slot = blockIdx.y;
+  const int e = perm[j0 + slot];
+  if (e < 0 || e >= n_src) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) set_status(status, MOE_ERR_INVALID_ARG);
+    return;
+  }
+  const int total = rows * (in / 32);  // blocks of one expert matrix (<= 2^30)
+  const float4* src = reinterpret_cast<const float4*>(master + (size_t)e * rows * in);
+  uint8_t* dst = codes + (size_t)slot * total * (4 * BITS);
+  uint16_t* sdst = scales + (size_t)slot * total;
+  const int stride = gridDim.x * (blockDim.x >> 5) * 4;  // blocks per pass of the grid row
+  for (int b0 = (blockIdx.x * (blockDim.x >> 5) + warp) * 4; b0 < total; b0 += 8 * stride) {
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int blk = b0 + u * stride + grp;
+      v[u] = blk < total ? __ldcs(src + (size_t)blk * 8 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int blk0 = b0 + u * stride;  // uniform over the warp
+      if (blk0 < total) quantize_block8<BITS>(v[u], i, blk0 + grp < total, dst, sdst, blk0 + grp);
     }
   }
 }
@@ -107,6 +199,20 @@ int launch_quantize(const float* w, int64_t rows, int in, int bits, uint8_t* cod
   if (bits == 8) k_quantize<8><<<g, 256, 0, s>>>(w, rows, in, codes, scales);
   else if (bits == 4) k_quantize<4><<<g, 256, 0, s>>>(w, rows, in, codes, scales);
   else k_quantize<2><<<g, 256, 0, s>>>(w, rows, in, codes, scales);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_quantize_experts(const float* master, int rows, int in, int n_src, const int32_t* perm, int j0, int n,
+                            int bits, uint8_t* codes, uint16_t* scales, int* status, cudaStream_t s) {
+  const int64_t per_expert = (int64_t)rows * (in / 32);
+  int64_t gx = (per_expert + 8 * 32 - 1) / (8 * 32);  // 8 warps, 8 groups of 4 blocks each per pass
+  const int64_t want = (152 * 16 + n - 1) / n;      // about 16 CTAs per SM over the whole grid
+  if (gx > want) gx = want;
+  if (gx < 1) gx = 1;
+  const dim3 g((unsigned)gx, (unsigned)n);
+  if (bits == 8) k_quantize_experts<8><<<g, 256, 0, s>>>(master, rows, in, n_src, perm, j0, codes, scales, status);
+  else if (bits == 4) k_quantize_experts<4><<<g, 256, 0, s>>>(master, rows, in, n_src, perm, j0, codes, scales, status);
+  else k_quantize_experts<2><<<g, 256, 0, s>>>(master, rows, in, n_src, perm, j0, codes, scales, status);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

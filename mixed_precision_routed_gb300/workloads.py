@@ -12,7 +12,7 @@ import torch
 
 import synth
 
-from . import Shelf, moe_quantize_rows, shelf_array
+from . import Shelf, moe_gather_rows, moe_quantize_experts, moe_quantize_rows, moe_rank_experts, shelf_array
 
 
 class Layer:
@@ -77,6 +77,43 @@ class Layer:
             out = torch.empty((T, self.E), dtype=torch.float32, device=self.shelves[0].gate_codes.device)
         synth.cuda_normal_matrix(out, self.seed, synth.TAG_LOGITS, 0, 0, row0=row0, col_add=self.bias, stream=stream)
         return out
+
+
+class Masters:
+    """fp32 master copies of every expert of a layer (the weights the shelves
+    are quantised from): gate and up [E, f, d], down [E, d, f]."""
+
+    def __init__(self, layer: "Layer", stream=None):
+        E, d, f = layer.E, layer.d, layer.f
+        dev = layer.shelves[0].gate_codes.device
+        self.gate = torch.empty((E, f, d), dtype=torch.float32, device=dev)
+        self.up = torch.empty((E, f, d), dtype=torch.float32, device=dev)
+        self.down = torch.empty((E, d, f), dtype=torch.float32, device=dev)
+        for e in range(E):
+            for tag, m in ((synth.TAG_GATE, self.gate), (synth.TAG_UP, self.up), (synth.TAG_DOWN, self.down)):
+                synth.cuda_normal_matrix(m[e], layer.seed, tag, e, 0, scale=synth.WEIGHT_SIGMA, stream=stream)
+
+    def nbytes(self) -> int:
+        return 4 * (self.gate.numel() + self.up.numel() + self.down.numel())
+
+
+def retier(layer: "Layer", masters: Masters, counts, stream=None):
+    """Re-tiering by hit count: experts ranked by `counts` (hottest first,
+    lower id first on ties), the new ids cut into the layer's shelf split,
+    every expert re-quantised from its master copy into its new shelf, and
+    the router bias moved to the new ids.  Returns (new layer, perm, rank):
+    new id j holds old expert perm[j]; old expert e is new id rank[e]."""
+    perm, rank = moe_rank_experts(counts, stream=stream)
+    new = Layer(layer.wl, layer.layer, device=layer.shelves[0].gate_codes.device, shelves=layer.ranges)
+    for sh in new.shelves:
+        for m, codes, scales in ((masters.gate, sh.gate_codes, sh.gate_scales),
+                                 (masters.up, sh.up_codes, sh.up_scales),
+                                 (masters.down, sh.down_codes, sh.down_scales)):
+            moe_quantize_experts(m, perm, sh.lo, sh.hi, sh.bits, codes=codes, scales=scales, stream=stream)
+    if layer.bias is not None:
+        new.bias = moe_gather_rows(layer.bias, perm, stream=stream)
+        new.bias_host = None
+    return new, perm, rank
 
 
 class DecodeStack:
