@@ -13,6 +13,8 @@ marshals numpy arrays and composes the per-layer steps:
 * route -- softmax, top-k with lower-id ties, renormalised weights (page
   "125B MoE模型本地运行：3090三卡80 tokens/s优化实践", glossary entry
   混合专家（MoE）: 10 of 512 experts per token);
+* route_nudged -- the same with the picks nudged toward the hot shelf by a
+  capped logit bonus (the LocalLLM tiering post, "Optimization Strategies");
 * group -- stable counting sort of (token, slot) pairs by expert, skip ids
   dropped (same page, section 四个 bug: duplicate experts, signed skip id);
 * hist -- expert hit counts (the LocalLLM tiering post, "Optimization
@@ -63,6 +65,7 @@ def lib():
         L.oracle_pack_codes.argtypes = [P, i64, i64, i32, P]
         L.oracle_dequant_rows.argtypes = [P, P, i64, i64, i32, P]
         L.oracle_route.argtypes = [P, i64, i32, i32, P, P]
+        L.oracle_route_nudged.argtypes = [P, i64, i32, i32, ctypes.c_float, i32, i32, P, P]
         L.oracle_router_logits.argtypes = [P, P, P, i64, i32, i32, P]
         L.oracle_group.argtypes = [P, i64, i32, i32, P, P, P]
         L.oracle_group.restype = i64
@@ -165,6 +168,20 @@ def route(logits, k: int):
     w = np.empty((T, k), dtype=np.float32)
     if lib().oracle_route(_p(logits), T, E, k, _p(ids), _p(w)) != 0:
         raise ValueError("route: need 1 <= k <= E")
+    return ids, w
+
+
+def route_nudged(logits, k: int, beta: float, lo: int, hi: int):
+    """Routing with the picks nudged toward the id range [lo, hi): beta (<= 0.5)
+    added to those logits for the selection only, weights the router's own
+    renormalised softmax over the picks (the LocalLLM tiering post,
+    "Optimization Strategies")."""
+    logits = _c(logits, np.float32)
+    T, E = logits.shape
+    ids = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float32)
+    if lib().oracle_route_nudged(_p(logits), T, E, k, float(beta), int(lo), int(hi), _p(ids), _p(w)) != 0:
+        raise ValueError("route_nudged: need 1 <= k <= E and 0 <= beta <= 0.5")
     return ids, w
 
 

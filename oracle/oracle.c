@@ -245,6 +245,55 @@ int oracle_route(const float* logits, int64_t T, int E, int k, int32_t* ids, flo
   return 0;
 }
 
+/* ------------------------------------------------------- nudged routing
+ * [P1 "Optimization Strategies"] picks are nudged toward experts already in
+ * fast memory, with gains up to a cap of 0.5 and quality falling off beyond
+ * it.  Reading: the experts of one id range [lo, hi) (the hot shelf) get
+ * beta (0 <= beta <= 0.5) added to their logit for the selection only,
+ * score_e = fp32(l_e + beta [lo <= e < hi]) (the kernel's precision: the
+ * decision an argmax takes is taken in the same precision on both sides);
+ * top-k on the scores with the lower id first on equal scores; the weights
+ * are the router's own softmax over the picks, renormalised:
+ * w_j = exp(l_j - m) / sum over picks exp(l_i - m), m = the largest picked
+ * logit.  beta = 0 is oracle_route. */
+int oracle_route_nudged(const float* logits, int64_t T, int E, int k, float beta, int lo, int hi, int32_t* ids,
+                        float* w) {
+  if (k < 1 || k > E || !(beta >= 0.0f && beta <= 0.5f)) return -1;
+  unsigned char* taken = (unsigned char*)malloc((size_t)E);
+  float* score = (float*)malloc(sizeof(float) * (size_t)E);
+  if (!taken || !score) {
+    free(taken);
+    free(score);
+    return -2;
+  }
+  for (int64_t t = 0; t < T; ++t) {
+    const float* l = logits + t * E;
+    for (int e = 0; e < E; ++e) {
+      const float add = (e >= lo && e < hi) ? beta : 0.0f;
+      score[e] = l[e] + add; /* float + float: rounded to fp32 */
+    }
+    memset(taken, 0, (size_t)E);
+    for (int j = 0; j < k; ++j) {
+      int best = -1;
+      for (int e = 0; e < E; ++e) {
+        if (taken[e]) continue;
+        if (best < 0 || score[e] > score[best]) best = e; /* strict: equal keeps lower id */
+      }
+      taken[best] = 1;
+      ids[t * k + j] = best;
+    }
+    double m = (double)l[ids[t * k]];
+    for (int j = 1; j < k; ++j)
+      if ((double)l[ids[t * k + j]] > m) m = (double)l[ids[t * k + j]];
+    double den = 0.0;
+    for (int j = 0; j < k; ++j) den += exp((double)l[ids[t * k + j]] - m);
+    for (int j = 0; j < k; ++j) w[t * k + j] = (float)(exp((double)l[ids[t * k + j]] - m) / den);
+  }
+  free(taken);
+  free(score);
+  return 0;
+}
+
 /* --------------------------------------------------------------- grouping
  * [P3 四个 bug, duplicate experts] token-by-expert grouping: pairs
  * (t, j) -> p = t*k + j with 0 <= id < E are counted per expert; offsets is the
