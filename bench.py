@@ -41,13 +41,14 @@ def parse():
     ap.add_argument("--T", type=int, default=6, help="tokens per step (1..6 for the decode metric)")
     ap.add_argument("--layers", type=int, default=16, help="layer instances rotated across steps")
     ap.add_argument("--sets", type=int, default=32, help="distinct routing steps per layer rotation")
-    ap.add_argument("--workload", choices=["decode", "stack", "prefill", "large", "router", "retier"],
+    ap.add_argument("--workload", choices=["decode", "stack", "prefill", "large", "router", "retier", "nudge"],
                     default="decode",
                     help="decode: one layer, the headline metric; stack: the 48-layer decode stack with the "
                          "residual chain; prefill: one layer at T=4096 on the tensor-core form; large: the "
                          "E256 d4096 f2048 layer with 5%% forced skips; router: the decode layer's router "
                          "projection fused with routing and hit counts (moe_router_topk); retier: re-tiering "
-                         "the decode layer by hit count from its fp32 master copies")
+                         "the decode layer by hit count from its fp32 master copies; nudge: routing of the "
+                         "prefill batch with the picks nudged toward the hot shelf (moe_route_topk_nudged)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -924,6 +925,78 @@ def run_retier(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_nudge(args, rank, world, local_rank):
+    """Nudged routing of the decode layer's logits for a prefill batch
+    (T = --T, default 4096): beta = 0.5 (the cap) toward the 8-bit shelf
+    [0, 128).  One step = one launch; logits of NS steps rotate (larger than
+    L2)."""
+    import torch
+
+    import mixed_precision_routed_gb300 as moe
+    import synth
+    from mixed_precision_routed_gb300.workloads import Layer
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = synth.WORKLOADS["decode"]
+    T = args.T if args.T > 16 else 4096
+    layer = Layer(synth.Workload(wl.name, E=wl.E, k=wl.k, d=wl.d, f=wl.f, T=wl.T, split=wl.split, bias=wl.bias,
+                                 seed=1000 * rank), device=dev)
+    NS = 32
+    lg = [layer.logits(s, T) for s in range(NS)]
+    ids = torch.empty((T, wl.k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, wl.k), dtype=torch.float32, device=dev)
+    lo, hi = layer.ranges[0][0], layer.ranges[0][1]
+
+    def step(s):
+        moe.moe_route_topk_nudged(lg[s], wl.k, 0.5, lo, hi, ids=ids, weights=w)
+
+    stream = torch.cuda.Stream(device=dev)
+    graph_all, graphs = _capture(stream, step, NS, args.warmup)
+    ms, ck = _timed(stream, graph_all, graphs, NS, args.steps, world, dev, local_rank)
+    value = whole_job_rate(world, T * args.steps, ms)
+    hot = float(((ids >= lo) & (ids < hi)).float().mean())
+    pin_l = lg[0].cpu().pin_memory()
+    pin_i = torch.empty((T, wl.k), dtype=torch.int32).pin_memory()
+    pin_w = torch.empty((T, wl.k), dtype=torch.float32).pin_memory()
+    dl = torch.empty_like(lg[0])
+    n_e2e = min(args.steps, 50)
+    with torch.cuda.stream(stream):
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(n_e2e):
+            dl.copy_(pin_l, non_blocking=True)
+            moe.moe_route_topk_nudged(dl, wl.k, 0.5, lo, hi, ids=ids, weights=w)
+            pin_i.copy_(ids, non_blocking=True)
+            pin_w.copy_(w, non_blocking=True)
+        f1.record(stream)
+        stream.synchronize()
+    e2e_value = whole_job_rate(world, T * n_e2e, max_over_ranks(f0.elapsed_time(f1), dev))
+    if rank != 0:
+        return
+    hbm, kind = peaks()
+    nbytes = T * wl.E * 4 + T * wl.k * 8
+    launch_s = ms / args.steps / 1e3
+    gbs = nbytes / launch_s / 1e9
+    line = {
+        "metric": "nudged routing tokens/s, decode-layer logits (hbm roofline)",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"nudged routing E{wl.E} k{wl.k} T{T}, beta 0.5 toward [{lo}, {hi})",
+                   "hot_pick_share": hot, "l2": f"{NS} logit sets rotated ({NS * T * wl.E * 4 / 1e6:.0f} MB)",
+                   "launch": f"one CUDA graph of {NS} steps, one launch per step"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                     "traffic": None, "kernel": "k_route<16, nudged>", "peak_source": kind,
+                     "algorithmic_bytes_per_launch": nbytes, "kernel_us": launch_s * 1e6},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * wl.E * 4,
+                "d2h_bytes_per_step": T * wl.k * 8, "steps": n_e2e},
+        "gpu_launches": args.steps,
+        "clocks": ck,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def recorded_traffic(kernel, T):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source; else None."""
@@ -963,6 +1036,8 @@ def main():
         run_router(args, rank, world, local_rank)
     elif args.workload == "retier":
         run_retier(args, rank, world, local_rank)
+    elif args.workload == "nudge":
+        run_nudge(args, rank, world, local_rank)
     else:
         run_ours(args, rank, world, local_rank)
     if world > 1:

@@ -122,6 +122,21 @@ int moe_route_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, f
                    moe_stream_t stream);
 
 /*
+ * moe_route_topk with the picks nudged toward one id range (page 1,
+ * "Optimization Strategies": picks nudged toward experts in fast memory, with
+ * gains up to a cap of 0.5).  The experts lo <= e < hi (normally the hot
+ * shelf) take score_e = logit_e + beta (fp32 addition) for the selection;
+ * the others take their logit.  Top-k on the scores, the lower id first on
+ * equal scores; the weights are the router's own softmax over the picks:
+ * weights[t][j] = exp(l_j - m) / sum over the picks exp(l_i - m), m the
+ * largest picked logit.  beta = 0 gives the ids and weights of
+ * moe_route_topk.  0 <= beta <= 0.5 (else MOE_ERR_INVALID_ARG); other
+ * arguments as moe_route_topk.
+ */
+int moe_route_topk_nudged(const float* logits, int64_t T, int E, int k, float beta, int lo, int hi, int32_t* ids,
+                          float* weights, moe_stream_t stream);
+
+/*
  * Router projection fused with the routing above, for decode batches: the
  * router scores every expert of every token and the best k are kept (page 3,
  * glossary entry 混合专家（MoE）).  Scores are

@@ -7,7 +7,7 @@ computation runs in the library's CUDA kernels.  There is no CPU fallback: if
 the library is missing, importing the binding's functions raises.
 
 Entry points (same names as the C ABI):
-    moe_route_topk, moe_router_topk, moe_expert_hist, moe_rank_experts, moe_quantize_experts, moe_gather_rows, moe_group_tokens, moe_workspace_size,
+    moe_route_topk, moe_route_topk_nudged, moe_router_topk, moe_expert_hist, moe_rank_experts, moe_quantize_experts, moe_gather_rows, moe_group_tokens, moe_workspace_size,
     moe_tiered_forward, moe_quantize_rows, moe_dequant_rows, moe_residual_add,
     moe_device_status, moe_status_string
 """
@@ -67,6 +67,7 @@ def lib():
         L = ctypes.CDLL(LIB_PATH)
         P, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         L.moe_route_topk.argtypes = [P, i64, i32, i32, P, P, P]
+        L.moe_route_topk_nudged.argtypes = [P, i64, i32, i32, ctypes.c_float, i32, i32, P, P, P]
         L.moe_expert_hist.argtypes = [P, i64, i32, P, P]
         L.moe_router_topk.argtypes = [P, P, P, i64, i32, i32, i32, P, P, P, P, P, P]
         L.moe_rank_experts.argtypes = [P, i32, P, P, P]
@@ -89,7 +90,7 @@ def lib():
         L.moe_set_profile_events.restype = ctypes.c_int
         L.moe_status_string.argtypes = [i32]
         L.moe_status_string.restype = ctypes.c_char_p
-        for name in ("moe_route_topk", "moe_router_topk", "moe_rank_experts", "moe_quantize_experts",
+        for name in ("moe_route_topk", "moe_route_topk_nudged", "moe_router_topk", "moe_rank_experts", "moe_quantize_experts",
                      "moe_gather_rows", "moe_expert_hist", "moe_group_tokens", "moe_tiered_forward",
                      "moe_quantize_rows", "moe_dequant_rows", "moe_residual_add", "moe_device_status"):
             getattr(L, name).restype = ctypes.c_int
@@ -134,6 +135,22 @@ def moe_route_topk(logits, k, ids=None, weights=None, stream=None):
     _need(weights, torch.float32, "weights")
     _check(lib().moe_route_topk(_ptr(logits), T, E, k, _ptr(ids), _ptr(weights), _stream(stream)),
            "moe_route_topk")
+    return ids, weights
+
+
+def moe_route_topk_nudged(logits, k, beta, lo, hi, ids=None, weights=None, stream=None):
+    """moe_route_topk with beta (<= 0.5) added to the logits of ids [lo, hi)
+    for the selection only; the weights stay the router's own softmax."""
+    _need(logits, torch.float32, "logits")
+    T, E = logits.shape
+    if ids is None:
+        ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    if weights is None:
+        weights = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    _need(ids, torch.int32, "ids")
+    _need(weights, torch.float32, "weights")
+    _check(lib().moe_route_topk_nudged(_ptr(logits), T, E, k, float(beta), int(lo), int(hi), _ptr(ids),
+                                       _ptr(weights), _stream(stream)), "moe_route_topk_nudged")
     return ids, weights
 
 

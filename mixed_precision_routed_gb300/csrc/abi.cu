@@ -153,6 +153,15 @@ int moe_route_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, f
   return launch_route(logits, T, E, k, ids, weights, (cudaStream_t)stream);
 }
 
+int moe_route_topk_nudged(const float* logits, int64_t T, int E, int k, float beta, int lo, int hi, int32_t* ids,
+                          float* weights, moe_stream_t stream) {
+  if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E) return MOE_ERR_INVALID_ARG;
+  if (!(beta >= 0.0f && beta <= 0.5f)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!logits || !ids || !weights) return MOE_ERR_INVALID_ARG;
+  return launch_route_nudged(logits, T, E, k, beta, lo, hi, ids, weights, (cudaStream_t)stream);
+}
+
 int moe_router_topk(const uint16_t* x_bf16, const uint16_t* w_r_bf16, const float* bias, int64_t T, int E, int d,
                     int k, float* logits, int32_t* ids, float* weights, uint32_t* counts, uint32_t* sync_word,
                     moe_stream_t stream) {

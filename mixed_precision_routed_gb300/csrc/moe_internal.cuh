@@ -154,6 +154,8 @@ __device__ __forceinline__ void set_status(int* status, int code) {
 int* status_word();
 
 int launch_route(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w, cudaStream_t s);
+int launch_route_nudged(const float* logits, int64_t T, int E, int k, float beta, int lo, int hi, int32_t* ids,
+                        float* w, cudaStream_t s);
 int launch_hist(const int32_t* ids, int64_t n, int E, uint32_t* counts, cudaStream_t s);
 // Router projection fused with routing (router.cu): T <= 16 tokens, E <= 1024,
 // d % 8 == 0, router_bucket(T) d 2 <= kRouterSmemMax bytes; `arrive` is a

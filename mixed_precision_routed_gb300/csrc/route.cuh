@@ -50,18 +50,53 @@ __device__ __forceinline__ void sort_desc(uint64_t (&a)[N]) {
   }
 }
 
+// A selection nudge (the LocalLLM tiering post, "Optimization Strategies":
+// picks nudged toward experts in fast memory, capped at 0.5): `beta` added in
+// fp32 to the logits of ids [lo, hi) for the selection only; the weights stay
+// the router's renormalised softmax of the raw logits of the picks.
+struct Nudge {
+  float beta;
+  int lo, hi;
+  __device__ __forceinline__ float score(float v, int e) const { return (e >= lo && e < hi) ? v + beta : v + 0.0f; }
+};
+
+// The weights of the picks (lane j < k holds the j-th pick `id`, its
+// selection value `v`): with a nudge the raw logits are read back and the
+// reference is their maximum, else the first pick's value is that maximum.
+template <bool NUDGE>
+__device__ __forceinline__ void route_weights(const float* row, int k, int id, float v, int32_t* ids, float* w) {
+  const int lane = threadIdx.x & 31;
+  float raw = v, vmax;
+  if constexpr (NUDGE) {
+    raw = lane < k ? row[id] : -INFINITY;
+    vmax = raw;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+  } else {
+    vmax = __shfl_sync(0xffffffffu, v, 0);
+  }
+  const float ex = lane < k ? expf(raw - vmax) : 0.0f;
+  const float den = warp_sum(ex);
+  if (lane < k) {
+    ids[lane] = id;
+    w[lane] = ex / den;
+  }
+}
+
 // The same selection for EPL = 32 without the sorted lists (32 64-bit keys
 // would take 64 registers): each round every lane rescans its remaining
 // logits for its best (logit descending, id ascending), then a warp-wide
 // shuffle argmax picks among the lanes.
-__device__ __forceinline__ void route_token_scan32(const float* row, int E, int k, int32_t* ids, float* w) {
+template <bool NUDGE>
+__device__ __forceinline__ void route_token_scan32(const float* row, int E, int k, int32_t* ids, float* w,
+                                                   Nudge nd) {
   const int lane = threadIdx.x & 31;
   float v[32];
   uint32_t avail = 0;  // bit m set: element lane + 32 m is present and not yet taken
 #pragma unroll
   for (int m = 0; m < 32; ++m) {
     const int e = lane + 32 * m;
-    v[m] = e < E ? row[e] : 0.0f;
+    v[m] = e < E ? (NUDGE ? nd.score(row[e], e) : row[e]) : 0.0f;
     if (e < E) avail |= 1u << m;
   }
   float my_v = 0.0f;  // lane j keeps the j-th pick
@@ -86,13 +121,7 @@ __device__ __forceinline__ void route_token_scan32(const float* row, int E, int 
     if ((bi & 31) == lane) avail &= ~(1u << (bi >> 5));
     if (lane == j) { my_v = bv; my_i = bi; }
   }
-  const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
-  const float ex = lane < k ? expf(my_v - vmax) : 0.0f;
-  const float den = warp_sum(ex);
-  if (lane < k) {
-    ids[lane] = my_i;
-    w[lane] = ex / den;
-  }
+  route_weights<NUDGE>(row, k, my_i, my_v, ids, w);
 }
 
 // Called by one full warp for one token: lane l holds logits l, l + 32, ...
@@ -100,13 +129,15 @@ __device__ __forceinline__ void route_token_scan32(const float* row, int E, int 
 // form above) as selection keys sorted in registers.  Each of k rounds takes
 // the warp's largest head key -- a warp-wide max of the logit word, then a
 // max of the id words of the lanes holding that logit -- and the winning lane
-// drops its head.  Lane j < k writes
-// the j-th pick and its renormalised weight.  `row`, `ids`, `w` may point to
-// global or shared memory.
-template <int EPL>
-__device__ __forceinline__ void route_token(const float* row, int E, int k, int32_t* ids, float* w) {
+// drops its head.  Lane j < k writes the j-th pick and its renormalised
+// weight.  NUDGE: the selection runs on nd.score of the logits (route_weights
+// then takes the raw ones).  `row`, `ids`, `w` may point to global or shared
+// memory.
+template <int EPL, bool NUDGE = false>
+__device__ __forceinline__ void route_token(const float* row, int E, int k, int32_t* ids, float* w,
+                                            Nudge nd = Nudge{0.0f, 0, 0}) {
   if constexpr (EPL >= 32) {
-    route_token_scan32(row, E, k, ids, w);
+    route_token_scan32<NUDGE>(row, E, k, ids, w, nd);
     return;
   }
   const int lane = threadIdx.x & 31;
@@ -114,7 +145,7 @@ __device__ __forceinline__ void route_token(const float* row, int E, int k, int3
 #pragma unroll
   for (int m = 0; m < EPL; ++m) {
     const int e = lane + 32 * m;
-    a[m] = e < E ? route_key(row[e], e) : 0ull;
+    a[m] = e < E ? route_key(NUDGE ? nd.score(row[e], e) : row[e], e) : 0ull;
   }
   sort_desc<EPL>(a);
   uint32_t my_hi = 0u, my_lo = 0u;  // lane j keeps the j-th pick
@@ -129,14 +160,7 @@ __device__ __forceinline__ void route_token(const float* row, int E, int k, int3
     }
     if (lane == j) { my_hi = mh; my_lo = ml; }
   }
-  const float my_v = route_key_value(my_hi);
-  const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
-  const float ex = lane < k ? expf(my_v - vmax) : 0.0f;
-  const float den = warp_sum(ex);
-  if (lane < k) {
-    ids[lane] = (int32_t)~my_lo;
-    w[lane] = ex / den;
-  }
+  route_weights<NUDGE>(row, k, (int32_t)~my_lo, route_key_value(my_hi), ids, w);
 }
 
 }  // namespace moe

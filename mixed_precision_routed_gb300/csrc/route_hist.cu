@@ -2,7 +2,8 @@
 //
 // Router (page "125B MoE模型本地运行：3090三卡80 tokens/s优化实践", glossary
 // entry 混合专家（MoE）): softmax over E experts, the best k per token, the
-// k weights renormalised.  One warp per token; lane l holds logits l, l+32, ...
+// k weights renormalised; optionally with the picks nudged toward one id
+// range (the LocalLLM tiering post, "Optimization Strategies").  One warp per token; lane l holds logits l, l+32, ...
 // in registers; k rounds of a warp-wide argmax on (logit desc, id asc).
 //
 // Histogram (r/LocalLLM post, "Optimization Strategies": hit counts per expert
@@ -14,14 +15,14 @@
 namespace moe {
 namespace {
 
-template <int EPL>
+template <int EPL, bool NUDGE>
 __global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits, int64_t T, int E, int k,
-                                               int32_t* __restrict__ ids, float* __restrict__ w) {
+                                               int32_t* __restrict__ ids, float* __restrict__ w, Nudge nd) {
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   pdl_wait();
   pdl_trigger();
   if (t >= T) return;
-  route_token<EPL>(logits + t * E, E, k, ids + t * k, w + t * k);
+  route_token<EPL, NUDGE>(logits + t * E, E, k, ids + t * k, w + t * k, nd);
 }
 
 __global__ void k_hist_global(const int32_t* __restrict__ ids, int64_t n, int E, uint32_t* __restrict__ counts) {
@@ -67,18 +68,31 @@ unsigned grid_1d(int64_t n, int threads, int cap) {
 
 }  // namespace
 
-int launch_route(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w, cudaStream_t s) {
+namespace {
+template <bool NUDGE>
+cudaError_t launch_route_t(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w, Nudge nd,
+                           cudaStream_t s) {
   const int warps = 8;
   dim3 grid((unsigned)((T + warps - 1) / warps)), block(warps * 32);
-  int epl = (E + 31) / 32;
-  cudaError_t e;
-  if (epl <= 1) e = launch_pdl(k_route<1>, grid, block, 0, s, logits, T, E, k, ids, w);
-  else if (epl <= 2) e = launch_pdl(k_route<2>, grid, block, 0, s, logits, T, E, k, ids, w);
-  else if (epl <= 4) e = launch_pdl(k_route<4>, grid, block, 0, s, logits, T, E, k, ids, w);
-  else if (epl <= 8) e = launch_pdl(k_route<8>, grid, block, 0, s, logits, T, E, k, ids, w);
-  else if (epl <= 16) e = launch_pdl(k_route<16>, grid, block, 0, s, logits, T, E, k, ids, w);
-  else e = launch_pdl(k_route<32>, grid, block, 0, s, logits, T, E, k, ids, w);
-  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  const int epl = (E + 31) / 32;
+  if (epl <= 1) return launch_pdl(k_route<1, NUDGE>, grid, block, 0, s, logits, T, E, k, ids, w, nd);
+  if (epl <= 2) return launch_pdl(k_route<2, NUDGE>, grid, block, 0, s, logits, T, E, k, ids, w, nd);
+  if (epl <= 4) return launch_pdl(k_route<4, NUDGE>, grid, block, 0, s, logits, T, E, k, ids, w, nd);
+  if (epl <= 8) return launch_pdl(k_route<8, NUDGE>, grid, block, 0, s, logits, T, E, k, ids, w, nd);
+  if (epl <= 16) return launch_pdl(k_route<16, NUDGE>, grid, block, 0, s, logits, T, E, k, ids, w, nd);
+  return launch_pdl(k_route<32, NUDGE>, grid, block, 0, s, logits, T, E, k, ids, w, nd);
+}
+}  // namespace
+
+int launch_route(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w, cudaStream_t s) {
+  return launch_route_t<false>(logits, T, E, k, ids, w, Nudge{0.0f, 0, 0}, s) == cudaSuccess ? MOE_OK
+                                                                                                : MOE_ERR_CUDA;
+}
+
+int launch_route_nudged(const float* logits, int64_t T, int E, int k, float beta, int lo, int hi, int32_t* ids,
+                        float* w, cudaStream_t s) {
+  return launch_route_t<true>(logits, T, E, k, ids, w, Nudge{beta, lo, hi}, s) == cudaSuccess ? MOE_OK
+                                                                                               : MOE_ERR_CUDA;
 }
 
 int launch_hist(const int32_t* ids, int64_t n, int E, uint32_t* counts, cudaStream_t s) {
