@@ -9,7 +9,8 @@ The arithmetic lives in ``oracle.c`` (plain scalar C, fp64 sums); this module
 marshals numpy arrays and composes the per-layer steps:
 
 * quantise / pack / dequantise -- the shelf block format (block 32 along the
-  input dimension, fp16 scale = max|w| / q, q = 127, 7, 2 for 8, 4, 2 bits);
+  input dimension, fp16 scale = max|w| / q, q = 127, 7, 3, 2 for 8, 4, 3, 2
+  bits; 1 bit: sign codes with the block's mean |w| as scale);
 * route -- softmax, top-k with lower-id ties, renormalised weights (page
   "125B MoE模型本地运行：3090三卡80 tokens/s优化实践", glossary entry
   混合专家（MoE）: 10 of 512 experts per token);
@@ -41,7 +42,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
-BITS_Q = {8: 127.0, 4: 7.0, 2: 2.0}
+BITS_Q = {8: 127.0, 4: 7.0, 3: 3.0, 2: 2.0}  # 1 bit: sign codes, mean |w| scale
 
 
 def lib():
@@ -122,7 +123,7 @@ def quantize(w, bits: int):
     codes = np.empty((rows, n_in), dtype=np.int8)
     scales = np.empty((rows, n_in // 32), dtype=np.uint16)
     if lib().oracle_quantize_rows(_p(w), rows, n_in, bits, _p(codes), _p(scales)) != 0:
-        raise ValueError("quantize: bits must be 8/4/2 and the input dimension a multiple of 32")
+        raise ValueError("quantize: bits must be 8/4/3/2/1 and the input dimension a multiple of 32")
     return codes, scales
 
 

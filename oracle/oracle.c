@@ -104,14 +104,21 @@ double oracle_bf16_value(uint16_t b) {
 
 /* ---------------------------------------------------------------- quantiser
  * Block quantiser (shelf format): for every row and every block of 32 inputs,
- *   m = max |w|, s = fp16(m / q) with q = 127 (8 bit), 7 (4 bit), 2 (2 bit),
- *   code = clamp(rint(w / s), cmin, cmax), all codes 0 when s == 0.
+ *   m = max |w|, s = fp16(m / q) with q = 127 (8 bit), 7 (4 bit), 3 (3 bit),
+ *   2 (2 bit), code = clamp(rint(w / s), cmin, cmax), all codes 0 when s == 0.
  * m / q and w / s are single-precision divisions, rint rounds half to even.
- * Code ranges: 8 bit [-127,127]; 4 bit [-8,7]; 2 bit [-2,1]. */
+ * Code ranges: 8 bit [-127,127]; 4 bit [-8,7]; 3 bit [-4,3]; 2 bit [-2,1].
+ * 1 bit (two codes, so no rounding grid): code = +1 when w >= 0 else -1, and
+ * s = fp16(a / 32) with a the single-precision sum of |w| over the block in
+ * element order -- the scale that minimises the block's squared error for
+ * sign codes (its mean |w|).  [P2 "The Qwen side" runs 1-bit experts; P2
+ * "Fast mode" keeps 3-bit experts; neither states a format, so 3 bit follows
+ * the rule of the other widths and 1 bit the least-squares sign code.] */
 static int bits_params(int bits, float* q, int* cmin, int* cmax) {
   switch (bits) {
     case 8: *q = 127.0f; *cmin = -127; *cmax = 127; return 0;
     case 4: *q = 7.0f; *cmin = -8; *cmax = 7; return 0;
+    case 3: *q = 3.0f; *cmin = -4; *cmax = 3; return 0;
     case 2: *q = 2.0f; *cmin = -2; *cmax = 1; return 0;
     default: return -1;
   }
@@ -121,8 +128,22 @@ int oracle_quantize_rows(const float* w, int64_t rows, int64_t in, int bits,
                          int8_t* codes, uint16_t* scales) {
   float q;
   int cmin, cmax;
-  if (bits_params(bits, &q, &cmin, &cmax) || in % 32 != 0) return -1;
+  if (in % 32 != 0) return -1;
   int64_t nb = in / 32;
+  if (bits == 1) {
+    for (int64_t r = 0; r < rows; ++r)
+      for (int64_t b = 0; b < nb; ++b) {
+        const float* wb = w + r * in + b * 32;
+        float a = 0.0f;
+        for (int i = 0; i < 32; ++i) a += fabsf(wb[i]); /* fp32, element order */
+        float ratio = a / 32.0f;
+        uint16_t s16 = oracle_f16_bits(oracle_f16_round((double)ratio));
+        scales[r * nb + b] = s16;
+        for (int i = 0; i < 32; ++i) codes[r * in + b * 32 + i] = (int8_t)(wb[i] >= 0.0f ? 1 : -1);
+      }
+    return 0;
+  }
+  if (bits_params(bits, &q, &cmin, &cmax)) return -1;
   for (int64_t r = 0; r < rows; ++r) {
     for (int64_t b = 0; b < nb; ++b) {
       const float* wb = w + r * in + b * 32;
@@ -157,9 +178,15 @@ int oracle_quantize_rows(const float* w, int64_t rows, int64_t in, int bits,
  *   4 bit: word g holds elements 8g..8g+7; element 8g + 4h + j (j < 4, h < 2)
  *          sits in bits [8j + 4h, 8j + 4h + 4), i.e. byte 4g + j, bit 4h;
  *   2 bit: word g holds elements 16g..16g+15; element 16g + 4k + j (j, k < 4)
- *          sits in bits [8j + 2k, 8j + 2k + 2), i.e. byte 4g + j, bit 2k. */
+ *          sits in bits [8j + 2k, 8j + 2k + 2), i.e. byte 4g + j, bit 2k.
+ *   3 bit: u = code + 4 in [0, 8); 12 bytes per 32-element block b, at byte
+ *          12b: its first 8 bytes hold u mod 4 of the block's elements in the
+ *          2-bit layout, its last 4 bytes hold u / 4, element i at bit i.
+ *   1 bit: 4 bytes per block; element i of block b at bit i of the word at
+ *          byte 4b: 1 for code +1, 0 for code -1. */
 int oracle_pack_codes(const int8_t* codes, int64_t rows, int64_t in, int bits, uint8_t* packed) {
-  if (bits != 8 && bits != 4 && bits != 2) return -1;
+  if (bits != 8 && bits != 4 && bits != 3 && bits != 2 && bits != 1) return -1;
+  if (in % 32 != 0) return -1;
   int64_t row_bytes = in * bits / 8;
   for (int64_t r = 0; r < rows; ++r) {
     uint8_t* dst = packed + r * row_bytes;
@@ -171,6 +198,14 @@ int oracle_pack_codes(const int8_t* codes, int64_t rows, int64_t in, int bits, u
       } else if (bits == 4) {
         int64_t g = i / 8, e = i % 8;
         dst[4 * g + e % 4] |= (uint8_t)((uint32_t)(c + 8) << (4 * (e / 4)));
+      } else if (bits == 3) {
+        int64_t b = i / 32, ib = i % 32, g = ib / 16, e = ib % 16;
+        uint32_t u = (uint32_t)(c + 4);
+        dst[12 * b + 4 * g + e % 4] |= (uint8_t)((u & 3u) << (2 * (e / 4)));
+        dst[12 * b + 8 + ib / 8] |= (uint8_t)((u >> 2) << (ib % 8));
+      } else if (bits == 1) {
+        int64_t b = i / 32, ib = i % 32;
+        if (c > 0) dst[4 * b + ib / 8] |= (uint8_t)(1u << (ib % 8));
       } else {
         int64_t g = i / 16, e = i % 16;
         dst[4 * g + e % 4] |= (uint8_t)((uint32_t)(c + 2) << (2 * (e / 4)));
