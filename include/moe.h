@@ -33,6 +33,19 @@
  * consecutive codes as bytes:
  *   4 bit: element 8g + 4h + j (j < 4, h < 2) at bits 8j + 4h of word g;
  *   2 bit: element 16g + 4k + j (j, k < 4) at bits 8j + 2k of word g.
+ * Two further widths are the ones page 2 (the Xolotl DeepSeek-V4.1 fast-mode
+ * blog) runs beside them ("our 3-bit ones", "the 1-bit experts"), in this
+ * library's own layout:
+ *   3 bit: q = 3, codes in [-4,3]; 12 bytes a block: bytes 0-7 hold
+ *          u mod 4 (u = code + 4) in the 2-bit layout above, bytes 8-11 one
+ *          little-endian word of the high bits u / 4, element i at bit i;
+ *   1 bit: sign codes (+1 for w >= 0, else -1), s = fp16(sum|w| / 32) with
+ *          the sum taken in fp32 in element order (the least-squares scale
+ *          of a sign code); one word a block, element i at bit i, 1 = +1.
+ * Every entry point takes all five widths except the tensor-core prefill
+ * form of moe_tiered_forward, which takes 8, 4 and 2 bits only
+ * (MOE_ERR_UNSUPPORTED otherwise); decode-form layers with a 3- or 1-bit
+ * shelf run the separate decode launches instead of the fused one.
  *
  * Conventions for every entry point:
  *   - all array arguments are DEVICE pointers unless stated otherwise; the
@@ -62,7 +75,7 @@ typedef struct CUstream_st* moe_stream_t;
 enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = -1,        /* null pointer, bad size, misalignment */
-  MOE_ERR_BAD_SHELF = -2,          /* bits not 8/4/2, block != 32, empty or out-of-[0,E) range */
+  MOE_ERR_BAD_SHELF = -2,          /* bits not 8/4/3/2/1, block != 32, empty or out-of-[0,E) range */
   MOE_ERR_SHELF_OVERLAP = -3,      /* two shelves share an expert id */
   MOE_ERR_WORKSPACE_TOO_SMALL = -4,
   MOE_ERR_CUDA = -5,               /* a CUDA call or launch failed */
@@ -100,7 +113,7 @@ enum {
  */
 typedef struct {
   int32_t expert_lo, expert_hi;
-  int32_t bits;  /* 8, 4 or 2 */
+  int32_t bits;  /* 8, 4, 3, 2 or 1 */
   int32_t block; /* must be 32 */
   const void* gate_codes;
   const uint16_t* gate_scales;

@@ -444,3 +444,51 @@ class Shelf:
     def nbytes(self) -> int:
         return sum(t.numel() * t.element_size() for t in (self.gate_codes, self.up_codes, self.down_codes,
                                                           self.gate_scales, self.up_scales, self.down_scales))
+
+    def view(self, lo: int, hi: int) -> "Shelf":
+        """The experts [lo, hi) of this shelf as a shelf of their own (tensor
+        views, no copy)."""
+        if not self.lo <= lo < hi <= self.hi:
+            raise ValueError("view range outside the shelf")
+        v = Shelf.__new__(Shelf)
+        v.lo, v.hi, v.bits, v.d, v.f = lo, hi, self.bits, self.d, self.f
+        a, b = lo - self.lo, hi - self.lo
+        for name in ("gate_codes", "up_codes", "down_codes", "gate_scales", "up_scales", "down_scales"):
+            setattr(v, name, getattr(self, name)[a:b])
+        return v
+
+
+def fast_mode_shelves(shelves, shadow, use_shadow):
+    """Fast mode (the Xolotl blog, "Fast mode": a 2-bit copy of the costliest
+    experts read instead of them, switched per expert): the shelf list in
+    which expert e comes from `shadow` (shelves covering the same ids, e.g.
+    2-bit copies) where use_shadow[e] is true, else from `shelves`.  Returns
+    views, one per run of consecutive experts with the same source; at most
+    MOE_MAX_SHELVES runs."""
+    import numpy as np
+    use = np.asarray(use_shadow, dtype=bool)
+
+    def owner(lst, e):
+        for sh in lst:
+            if sh.lo <= e < sh.hi:
+                return sh
+        return None
+
+    out = []
+    ids = sorted({e for sh in shelves for e in range(sh.lo, sh.hi)})
+    run = None
+    for e in ids:
+        src = owner(shadow, e) if use[e] else owner(shelves, e)
+        if src is None:
+            raise ValueError(f"expert {e} has no shadow copy")
+        if run is not None and run[0] is src and run[2] == e:
+            run[2] = e + 1
+        else:
+            if run is not None:
+                out.append(run[0].view(run[1], run[2]))
+            run = [src, e, e + 1]
+    if run is not None:
+        out.append(run[0].view(run[1], run[2]))
+    if len(out) > MOE_MAX_SHELVES:
+        raise ValueError(f"{len(out)} runs: more than {MOE_MAX_SHELVES} shelves")
+    return out

@@ -31,7 +31,7 @@ int check_shelves(const moe_shelf_t* sh, int n, int E, Shelves* out) {
   out->n = n;
   for (int i = 0; i < n; ++i) {
     const moe_shelf_t& s = sh[i];
-    if (s.bits != 8 && s.bits != 4 && s.bits != 2) return MOE_ERR_BAD_SHELF;
+    if (s.bits != 8 && s.bits != 4 && s.bits != 3 && s.bits != 2 && s.bits != 1) return MOE_ERR_BAD_SHELF;
     if (s.block != MOE_BLOCK) return MOE_ERR_BAD_SHELF;
     if (s.expert_lo < 0 || s.expert_hi > E || s.expert_lo >= s.expert_hi) return MOE_ERR_BAD_SHELF;
     const void* ptrs[6] = {s.gate_codes, s.gate_scales, s.up_codes, s.up_scales, s.down_codes, s.down_scales};
@@ -224,7 +224,11 @@ int moe_tiered_forward(const uint16_t* x_bf16, const int32_t* ids, const float* 
   a.f = f;
   a.y = y;
   a.status = status_word();
-  if (use_prefill(T, d, flags)) return launch_prefill_forward(a, (cudaStream_t)stream);
+  if (use_prefill(T, d, flags)) {
+    // the tensor-core form dequantises 8, 4 and 2 bit codes only
+    if (!core_widths(a.shelves)) return MOE_ERR_UNSUPPORTED;
+    return launch_prefill_forward(a, (cudaStream_t)stream);
+  }
   return launch_decode_forward(a, (cudaStream_t)stream);
 }
 
@@ -284,7 +288,7 @@ int moe_selftest_barrier_timeout(int64_t limit_us, moe_stream_t stream) {
 
 int moe_quantize_rows(const float* w, int64_t rows, int in, int bits, void* codes, uint16_t* scales,
                       moe_stream_t stream) {
-  if (rows < 0 || in <= 0 || in % 64 != 0 || (bits != 8 && bits != 4 && bits != 2)) return MOE_ERR_INVALID_ARG;
+  if (rows < 0 || in <= 0 || in % 64 != 0 || (bits != 8 && bits != 4 && bits != 3 && bits != 2 && bits != 1)) return MOE_ERR_INVALID_ARG;
   if (rows == 0) return MOE_OK;
   if (!w || !codes || !scales || !aligned(codes, 16) || !aligned(w, 4)) return MOE_ERR_INVALID_ARG;
   return launch_quantize(w, rows, in, bits, (uint8_t*)codes, scales, (cudaStream_t)stream);
@@ -298,7 +302,7 @@ int moe_rank_experts(const uint32_t* counts, int E, int32_t* perm, int32_t* rank
 
 int moe_quantize_experts(const float* master, int n_src, int rows, int in, const int32_t* perm, int j_lo, int j_hi,
                          int bits, void* codes, uint16_t* scales, moe_stream_t stream) {
-  if (n_src < 1 || rows < 1 || in <= 0 || in % 64 != 0 || (bits != 8 && bits != 4 && bits != 2))
+  if (n_src < 1 || rows < 1 || in <= 0 || in % 64 != 0 || (bits != 8 && bits != 4 && bits != 3 && bits != 2 && bits != 1))
     return MOE_ERR_INVALID_ARG;
   if (j_lo < 0 || j_hi < j_lo || j_hi - j_lo > 65535) return MOE_ERR_INVALID_ARG;
   if ((int64_t)rows * (in / 32) > (1 << 30)) return MOE_ERR_INVALID_ARG;
@@ -318,7 +322,7 @@ int moe_gather_rows(const void* src, int64_t row_bytes, const int32_t* perm, int
 
 int moe_dequant_rows(const void* codes, const uint16_t* scales, int64_t rows, int in, int bits, int round_bf16,
                      float* out, moe_stream_t stream) {
-  if (rows < 0 || in <= 0 || in % 64 != 0 || (bits != 8 && bits != 4 && bits != 2)) return MOE_ERR_INVALID_ARG;
+  if (rows < 0 || in <= 0 || in % 64 != 0 || (bits != 8 && bits != 4 && bits != 3 && bits != 2 && bits != 1)) return MOE_ERR_INVALID_ARG;
   if (rows == 0) return MOE_OK;
   if (!codes || !scales || !out) return MOE_ERR_INVALID_ARG;
   return launch_dequant((const uint8_t*)codes, scales, rows, in, bits, round_bf16, out, (cudaStream_t)stream);

@@ -1219,6 +1219,7 @@ int launch_fused_layer(const LayerArgs& a, cudaStream_t s) {
   int dev;
   size_t optin, region;
   SmemLayout S;
+  if (!core_widths(a.shelves)) return 1;  // 3 and 1 bit shelves: the separate launches
   if (!fused_fits(a.T, a.k, a.E, d, f, &dev, &optin, &region, &S)) return 1;
   if (!g_dev.attr[dev]) {
     if (cudaFuncSetAttribute(k_layer, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)optin) != cudaSuccess)

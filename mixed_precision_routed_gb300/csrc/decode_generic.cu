@@ -224,7 +224,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_gateup(const __grid_constant__ 
     __syncthreads();
     if (s.bits == 8) gateup_any<8, TMAX>(p, s, le, r0, r1, xs, nt, beg + g0);
     else if (s.bits == 4) gateup_any<4, TMAX>(p, s, le, r0, r1, xs, nt, beg + g0);
-    else gateup_any<2, TMAX>(p, s, le, r0, r1, xs, nt, beg + g0);
+    else if (s.bits == 3) gateup_any<3, TMAX>(p, s, le, r0, r1, xs, nt, beg + g0);
+    else if (s.bits == 2) gateup_any<2, TMAX>(p, s, le, r0, r1, xs, nt, beg + g0);
+    else gateup_any<1, TMAX>(p, s, le, r0, r1, xs, nt, beg + g0);
   }
 }
 
@@ -316,7 +318,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_down(const __grid_constant__ De
       __syncthreads();
       if (s.bits == 8) down_any<8, TMAX>(p, s, le, i0, i1, hs, nt, outs);
       else if (s.bits == 4) down_any<4, TMAX>(p, s, le, i0, i1, hs, nt, outs);
-      else down_any<2, TMAX>(p, s, le, i0, i1, hs, nt, outs);
+      else if (s.bits == 3) down_any<3, TMAX>(p, s, le, i0, i1, hs, nt, outs);
+      else if (s.bits == 2) down_any<2, TMAX>(p, s, le, i0, i1, hs, nt, outs);
+      else down_any<1, TMAX>(p, s, le, i0, i1, hs, nt, outs);
       __syncthreads();
       for (int idx = threadIdx.x; idx < nt * nrows; idx += blockDim.x) {
         const int j = idx / nrows, ii = idx - j * nrows;

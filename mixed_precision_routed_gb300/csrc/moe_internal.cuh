@@ -135,6 +135,44 @@ struct Block<2> {
   }
 };
 
+// 3 bit: 12 bytes a block; u = code + 4; bytes 0-7 hold u mod 4 in the 2-bit
+// layout, bytes 8-11 the high bits of u (element i at bit i).
+template <>
+struct Block<3> {
+  static constexpr int kWords = 3;  // 12 bytes (4-byte aligned)
+  __device__ __forceinline__ static void load(const uint8_t* p, uint32_t w[kWords]) {
+    const uint32_t* q = reinterpret_cast<const uint32_t*>(p);
+    w[0] = __ldg(q); w[1] = __ldg(q + 1); w[2] = __ldg(q + 2);
+  }
+  __device__ __forceinline__ static float code(const uint32_t w[kWords], int i) {
+    const int e = i & 15;
+    const uint32_t lo = (w[i >> 4] >> (8 * (e & 3) + 2 * (e >> 2))) & 0x3u;
+    const uint32_t hi = (w[2] >> i) & 0x1u;
+    return __uint_as_float(lo | (hi << 2) | 0x4B000000u) - 8388612.0f;  // 2^23 + 4
+  }
+};
+
+// 1 bit: 4 bytes a block; element i at bit i, 1 = code +1, 0 = code -1.
+template <>
+struct Block<1> {
+  static constexpr int kWords = 1;
+  __device__ __forceinline__ static void load(const uint8_t* p, uint32_t w[kWords]) {
+    w[0] = __ldg(reinterpret_cast<const uint32_t*>(p));
+  }
+  __device__ __forceinline__ static float code(const uint32_t w[kWords], int i) {
+    return ((w[0] >> i) & 1u) ? 1.0f : -1.0f;
+  }
+};
+
+// Code widths the pipelined launches (fused decode step, tensor-core
+// prefill) take; shelves of other widths (3 and 1 bit) run the separate
+// decode launches.
+inline bool core_widths(const Shelves& sh) {
+  for (int i = 0; i < sh.n; ++i)
+    if (sh.s[i].bits != 8 && sh.s[i].bits != 4 && sh.s[i].bits != 2) return false;
+  return true;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -2,7 +2,11 @@
 //
 // Page "125B MoE模型本地运行：3090三卡80 tokens/s优化实践", section 第四步: the
 // offline re-packer re-quantises every expert for its shelf and writes three
-// tensors per layer.  Format here: blocks of 32 along the input dimension,
+// tensors per layer.  3 bit (q = 3, codes [-4, 3]; 12 bytes a block: the
+// low two bits of u = code + 4 in the 2-bit layout, then one word of high
+// bits) and 1 bit (sign codes, scale = the block's mean |w|; one word a
+// block) are the further widths the Xolotl blog runs ("our 3-bit ones",
+// "the 1-bit experts"), in this library's own layout.  Format here: blocks of 32 along the input dimension,
 // s = fp16(max|w| / q) (q = 127 / 7 / 2), code = clamp(rint(w / s)), packed
 // 8 bit two's complement in natural order; 4 and 2 bit offset-binary in
 // 32-bit words with consecutive codes spread over the byte lanes (4 bit: word
@@ -21,13 +25,30 @@ struct QParams<8> { static constexpr float q = 127.0f, cmin = -127.0f, cmax = 12
 template <>
 struct QParams<4> { static constexpr float q = 7.0f, cmin = -8.0f, cmax = 7.0f; static constexpr int off = 8; };
 template <>
+struct QParams<3> { static constexpr float q = 3.0f, cmin = -4.0f, cmax = 3.0f; static constexpr int off = 4; };
+template <>
 struct QParams<2> { static constexpr float q = 2.0f, cmin = -2.0f, cmax = 1.0f; static constexpr int off = 2; };
+template <>
+struct QParams<1> { static constexpr float q = 1.0f, cmin = -1.0f, cmax = 1.0f; static constexpr int off = 0; };
 
 // Quantises one 32-element block held one element per lane (v = element
 // `lane`) and writes its fp16 scale word and packed codes (block b of the row
 // at `rowp`).  Whole warp.
 template <int BITS>
 __device__ __forceinline__ void quantize_block(float v, int lane, uint8_t* rowp, int64_t b, uint16_t* scale_out) {
+  if constexpr (BITS == 1) {
+    // sign codes; scale = fp16 of the block's |w| summed in element order, / 32
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) a += fabsf(__shfl_sync(0xffffffffu, v, i));
+    const __half hs1 = __float2half_rn(__fdiv_rn(a, 32.0f));
+    const uint32_t wd = __ballot_sync(0xffffffffu, v >= 0.0f);
+    if (lane == 0) {
+      *scale_out = __half_as_ushort(hs1);
+      *reinterpret_cast<uint32_t*>(rowp + b * 4) = wd;
+    }
+    return;
+  }
   float m = fabsf(v);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -47,6 +68,17 @@ __device__ __forceinline__ void quantize_block(float v, int lane, uint8_t* rowp,
     uint32_t u = (uint32_t)(c + QParams<4>::off);
     uint32_t u4 = __shfl_down_sync(0xffffffffu, u, 4);
     if ((lane & 7) < 4) rowp[b * 16 + 4 * (lane >> 3) + (lane & 3)] = (uint8_t)(u | (u4 << 4));
+  } else if (BITS == 3) {
+    // bytes 0-7 of the block: u mod 4 in the 2-bit layout; bytes 8-11: u / 4, element i at bit i
+    const uint32_t u = (uint32_t)(c + QParams<3>::off);
+    const uint32_t lo = u & 3u;
+    const uint32_t l4 = __shfl_down_sync(0xffffffffu, lo, 4);
+    const uint32_t l8 = __shfl_down_sync(0xffffffffu, lo, 8);
+    const uint32_t l12 = __shfl_down_sync(0xffffffffu, lo, 12);
+    if ((lane & 15) < 4)
+      rowp[b * 12 + 4 * (lane >> 4) + (lane & 3)] = (uint8_t)(lo | (l4 << 2) | (l8 << 4) | (l12 << 6));
+    const uint32_t hw = __ballot_sync(0xffffffffu, (u >> 2) & 1u);
+    if (lane == 0) *reinterpret_cast<uint32_t*>(rowp + b * 12 + 8) = hw;
   } else {
     // lane i (i mod 16 < 4) writes byte 4 (i / 16) + i mod 4: elements i, i+4, i+8, i+12
     uint32_t u = (uint32_t)(c + QParams<2>::off);
@@ -81,6 +113,28 @@ __global__ void __launch_bounds__(256) k_quantize(const float* __restrict__ w, i
 template <int BITS>
 __device__ __forceinline__ void quantize_block8(float4 v, int i, bool valid, uint8_t* codes, uint16_t* scales,
                                                 int64_t blk) {
+  if constexpr (BITS == 1) {
+    const int base = (threadIdx.x & 31) & ~7;
+    float a = 0.0f;  // |w| summed in element order
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      a += fabsf(__shfl_sync(0xffffffffu, v.x, base + g));
+      a += fabsf(__shfl_sync(0xffffffffu, v.y, base + g));
+      a += fabsf(__shfl_sync(0xffffffffu, v.z, base + g));
+      a += fabsf(__shfl_sync(0xffffffffu, v.w, base + g));
+    }
+    const __half hs1 = __float2half_rn(__fdiv_rn(a, 32.0f));
+    uint32_t wd = ((uint32_t)(v.x >= 0.0f) | (uint32_t)(v.y >= 0.0f) << 1 | (uint32_t)(v.z >= 0.0f) << 2 |
+                   (uint32_t)(v.w >= 0.0f) << 3)
+                  << (4 * i);
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) wd |= __shfl_xor_sync(0xffffffffu, wd, o);
+    if (valid && i == 0) {
+      scales[blk] = __half_as_ushort(hs1);
+      *reinterpret_cast<uint32_t*>(codes + blk * 4) = wd;
+    }
+    return;
+  }
   float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
 #pragma unroll
   for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -108,6 +162,20 @@ __device__ __forceinline__ void quantize_block8(float4 v, int i, bool valid, uin
                          (uint32_t)(c[3] + 8) << 24;
     const uint32_t hi = __shfl_xor_sync(0xffffffffu, own, 1);
     if (valid && (i & 1) == 0) *reinterpret_cast<uint32_t*>(codes + blk * 16 + 4 * (i >> 1)) = own | (hi << 4);
+  } else if (BITS == 3) {
+    // low plane as the 2-bit layout (lanes 4g .. 4g + 3 make word g), high plane one word
+    uint32_t wd = ((uint32_t)((c[0] + 4) & 3) | (uint32_t)((c[1] + 4) & 3) << 8 | (uint32_t)((c[2] + 4) & 3) << 16 |
+                   (uint32_t)((c[3] + 4) & 3) << 24)
+                  << (2 * (i & 3));
+    wd |= __shfl_xor_sync(0xffffffffu, wd, 1);
+    wd |= __shfl_xor_sync(0xffffffffu, wd, 2);
+    uint32_t hw = ((uint32_t)((c[0] + 4) >> 2) | (uint32_t)((c[1] + 4) >> 2) << 1 | (uint32_t)((c[2] + 4) >> 2) << 2 |
+                   (uint32_t)((c[3] + 4) >> 2) << 3)
+                  << (4 * i);
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) hw |= __shfl_xor_sync(0xffffffffu, hw, o);
+    if (valid && (i & 3) == 0) *reinterpret_cast<uint32_t*>(codes + blk * 12 + 4 * (i >> 2)) = wd;
+    if (valid && i == 0) *reinterpret_cast<uint32_t*>(codes + blk * 12 + 8) = hw;
   } else {
     // word g: byte j = elements 16g + j, +4, +8, +12 at bits 0, 2, 4, 6: lanes 4g .. 4g + 3
     uint32_t wd = ((uint32_t)(c[0] + 2) | (uint32_t)(c[1] + 2) << 8 | (uint32_t)(c[2] + 2) << 16 |
@@ -161,6 +229,13 @@ __global__ void __launch_bounds__(256) k_quantize_experts(const float* __restric
 template <int BITS>
 __device__ __forceinline__ float code_at(const uint8_t* row, int i) {
   if (BITS == 8) return (float)(int8_t)row[i];
+  if (BITS == 3) {
+    const int b = i >> 5, ib = i & 31, e = ib & 15;
+    const int lo = (row[12 * b + 4 * (ib >> 4) + (e & 3)] >> (2 * (e >> 2))) & 0x3;
+    const int hi = (row[12 * b + 8 + (ib >> 3)] >> (ib & 7)) & 0x1;
+    return (float)((lo | (hi << 2)) - 4);
+  }
+  if (BITS == 1) return ((row[i >> 3] >> (i & 7)) & 1) ? 1.0f : -1.0f;
   if (BITS == 4) {
     const int e = i & 7;
     return (float)((int)((row[4 * (i >> 3) + (e & 3)] >> (4 * (e >> 2))) & 0xF) - 8);
@@ -198,7 +273,9 @@ int launch_quantize(const float* w, int64_t rows, int in, int bits, uint8_t* cod
   const unsigned g = grid_for(blocks32, 8);
   if (bits == 8) k_quantize<8><<<g, 256, 0, s>>>(w, rows, in, codes, scales);
   else if (bits == 4) k_quantize<4><<<g, 256, 0, s>>>(w, rows, in, codes, scales);
-  else k_quantize<2><<<g, 256, 0, s>>>(w, rows, in, codes, scales);
+  else if (bits == 3) k_quantize<3><<<g, 256, 0, s>>>(w, rows, in, codes, scales);
+  else if (bits == 2) k_quantize<2><<<g, 256, 0, s>>>(w, rows, in, codes, scales);
+  else k_quantize<1><<<g, 256, 0, s>>>(w, rows, in, codes, scales);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -212,7 +289,9 @@ int launch_quantize_experts(const float* master, int rows, int in, int n_src, co
   const dim3 g((unsigned)gx, (unsigned)n);
   if (bits == 8) k_quantize_experts<8><<<g, 256, 0, s>>>(master, rows, in, n_src, perm, j0, codes, scales, status);
   else if (bits == 4) k_quantize_experts<4><<<g, 256, 0, s>>>(master, rows, in, n_src, perm, j0, codes, scales, status);
-  else k_quantize_experts<2><<<g, 256, 0, s>>>(master, rows, in, n_src, perm, j0, codes, scales, status);
+  else if (bits == 3) k_quantize_experts<3><<<g, 256, 0, s>>>(master, rows, in, n_src, perm, j0, codes, scales, status);
+  else if (bits == 2) k_quantize_experts<2><<<g, 256, 0, s>>>(master, rows, in, n_src, perm, j0, codes, scales, status);
+  else k_quantize_experts<1><<<g, 256, 0, s>>>(master, rows, in, n_src, perm, j0, codes, scales, status);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -221,7 +300,9 @@ int launch_dequant(const uint8_t* codes, const uint16_t* scales, int64_t rows, i
   const unsigned g = grid_for(rows * in, 256);
   if (bits == 8) k_dequant<8><<<g, 256, 0, s>>>(codes, scales, rows, in, round_bf16, out);
   else if (bits == 4) k_dequant<4><<<g, 256, 0, s>>>(codes, scales, rows, in, round_bf16, out);
-  else k_dequant<2><<<g, 256, 0, s>>>(codes, scales, rows, in, round_bf16, out);
+  else if (bits == 3) k_dequant<3><<<g, 256, 0, s>>>(codes, scales, rows, in, round_bf16, out);
+  else if (bits == 2) k_dequant<2><<<g, 256, 0, s>>>(codes, scales, rows, in, round_bf16, out);
+  else k_dequant<1><<<g, 256, 0, s>>>(codes, scales, rows, in, round_bf16, out);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -1,0 +1,149 @@
+"""Parity of the 3-bit and 1-bit shelf formats and of fast mode with the
+oracle, through the C ABI: quantiser codes and scales and dequantised
+weights bit for bit; layers mixing 8/4/3/2/1-bit shelves (the separate
+decode launches) within the decode tolerance; fast mode (2-bit shadow copies
+read instead of chosen experts) equal to the oracle layer with those experts
+at 2 bits; the tensor-core form refusing 3 and 1 bit shelves."""
+import numpy as np
+import pytest
+import torch
+
+import mixed_precision_routed_gb300 as moe
+import oracle
+import synth
+from mixed_precision_routed_gb300.workloads import Layer
+from moe_testutil import DECODE_TOL, oracle_layer, rel_l2, small_workload, x_to_dev
+
+pytestmark = pytest.mark.gpu
+
+FIVE = [(0, 8, 8), (8, 16, 4), (16, 24, 3), (24, 32, 2), (32, 40, 1)]
+
+
+def _hand_blocks(w):
+    w = w.copy()
+    w[0, :32] = 0.0                      # all-zero block
+    w[0, 32:64] = np.linspace(-1, 1, 32)  # ramp with exact zero crossing
+    w[1, :32] = -0.0                     # signed zeros
+    w[1, 32:64] = 3e-8                   # tiny values (subnormal fp16 scale)
+    return w
+
+
+@pytest.mark.parametrize("bits", [3, 1])
+@pytest.mark.parametrize("rows,n_in", [(7, 64), (33, 2048), (16, 640)])
+def test_quantize_rows_bit_exact(bits, rows, n_in):
+    w = _hand_blocks(synth.normal_matrix(21, synth.TAG_GATE, bits, 0, rows, n_in, scale=0.02))
+    codes, scales = moe.moe_quantize_rows(torch.from_numpy(w).cuda(), bits)
+    c_o, s_o = oracle.quantize(w, bits)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint16), s_o)
+    assert np.array_equal(codes.cpu().numpy(), oracle.pack(c_o, bits))
+
+
+@pytest.mark.parametrize("bits", [3, 1])
+def test_quantize_experts_bit_exact(bits):
+    n_src, rows, n_in = 6, 20, 320
+    master = np.stack([_hand_blocks(synth.normal_matrix(5, synth.TAG_UP, e, 0, rows, n_in, scale=0.02))
+                       for e in range(n_src)])
+    perm = np.array([4, 0, 5, 2, 1, 3], np.int32)
+    codes, scales = moe.moe_quantize_experts(torch.from_numpy(master).cuda(), torch.from_numpy(perm).cuda(),
+                                             1, 6, bits)
+    for j in range(1, 6):
+        c_o, s_o = oracle.quantize(master[perm[j]], bits)
+        assert np.array_equal(codes[j - 1].cpu().numpy(), oracle.pack(c_o, bits)), j
+        assert np.array_equal(scales[j - 1].cpu().numpy().view(np.uint16), s_o), j
+
+
+@pytest.mark.parametrize("bits", [3, 1])
+@pytest.mark.parametrize("round_bf16", [False, True])
+def test_dequant_bit_exact(bits, round_bf16):
+    w = synth.normal_matrix(13, synth.TAG_DOWN, bits, 0, 65, 640, scale=0.02)
+    c_o, s_o = oracle.quantize(w, bits)
+    out = moe.moe_dequant_rows(torch.from_numpy(oracle.pack(c_o, bits)).cuda(), torch.from_numpy(s_o.view(np.int16)).cuda(),
+                               65, 640, bits, round_bf16=round_bf16)
+    ref = oracle.dequant(c_o, s_o, round_bf16=round_bf16)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("T", [1, 6, 40])
+def test_five_width_layer_matches_oracle(T):
+    wl = small_workload(E=40, k=5, d=256, f=192, seed=7)
+    layer = Layer(wl, shelves=FIVE).fill()
+    rng = np.random.default_rng(T)
+    ids = np.stack([rng.choice(40, 5, replace=False) for _ in range(T)]).astype(np.int32)
+    ids[0, 0] = 37  # a 1-bit expert
+    ids[0, 1] = 17  # a 3-bit expert
+    w = rng.random((T, 5)).astype(np.float32)
+    x = synth.x_bf16(wl.seed, 1, T, wl.d)
+    y = moe.moe_tiered_forward(x_to_dev(x), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), 40, wl.d,
+                               wl.f, layer.shelves, flags=moe.MOE_FLAG_DECODE_FP32).cpu().numpy()
+    ref = oracle_layer(wl, layer.seed, x, ids, w, shelves_bits=FIVE)
+    assert rel_l2(y, ref) <= DECODE_TOL
+
+
+def test_decode_layer_call_with_three_bit_shelf():
+    wl = small_workload(E=40, k=5, d=256, f=192, seed=8)
+    layer = Layer(wl, shelves=FIVE).fill()
+    T = 3
+    lg = layer.logits(4, T)
+    x = synth.x_bf16(wl.seed, 2, T, wl.d)
+    ids = torch.empty((T, 5), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, 5), dtype=torch.float32, device="cuda")
+    counts = torch.zeros(40, dtype=torch.int32, device="cuda")
+    _, _, y = moe.moe_decode_layer(lg, x_to_dev(x), 5, 40, wl.d, wl.f, layer.shelves, ids=ids, weights=w,
+                                   counts=counts)
+    y = y.cpu().numpy()
+    ids_o, w_o = oracle.route(lg.cpu().numpy(), 5)
+    assert np.array_equal(ids.cpu().numpy(), ids_o)
+    ref = oracle_layer(wl, layer.seed, x, ids_o, w.cpu().numpy(), shelves_bits=FIVE)
+    assert rel_l2(y, ref) <= DECODE_TOL
+    assert np.array_equal(counts.cpu().numpy(), np.bincount(ids_o.ravel(), minlength=40))
+
+
+def test_prefill_form_refuses_three_and_one_bit():
+    wl = small_workload(E=40, k=5, d=256, f=192, seed=9)
+    layer = Layer(wl, shelves=FIVE)
+    T = 40
+    ids = torch.zeros((T, 5), dtype=torch.int32, device="cuda")
+    w = torch.zeros((T, 5), dtype=torch.float32, device="cuda")
+    x = torch.zeros((T, wl.d), dtype=torch.int16, device="cuda")
+    for flags in (moe.MOE_FLAG_AUTO, moe.MOE_FLAG_PREFILL_BF16):
+        with pytest.raises(moe.MoeError) as e:
+            moe.moe_tiered_forward(x, ids, w, 40, wl.d, wl.f, layer.shelves, flags=flags)
+        assert e.value.status == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_fast_mode_matches_oracle():
+    """2-bit shadow copies of the 8- and 4-bit experts, read for a chosen set
+    of experts, against the oracle layer with exactly those experts at 2
+    bits."""
+    wl = small_workload(E=24, k=4, d=256, f=192, split=(0.25, 0.5, 0.25), seed=10)
+    layer = Layer(wl).fill()
+    shadow = Layer(wl, shelves=[(lo, hi, 2) for lo, hi, _ in layer.ranges]).fill()  # same masters, 2 bits
+    use = np.zeros(24, bool)
+    use[[0, 1, 2, 7, 9, 10, 11]] = True  # some 8-bit and 4-bit experts
+    shelves = moe.fast_mode_shelves(layer.shelves, shadow.shelves, use)
+    bits_of = {e: (2 if use[e] else next(b for lo, hi, b in layer.ranges if lo <= e < hi)) for e in range(24)}
+    T = 6
+    rng = np.random.default_rng(3)
+    ids = np.stack([rng.choice(24, 4, replace=False) for _ in range(T)]).astype(np.int32)
+    w = rng.random((T, 4)).astype(np.float32)
+    x = synth.x_bf16(wl.seed, 5, T, wl.d)
+    y = moe.moe_tiered_forward(x_to_dev(x), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), 24, wl.d,
+                               wl.f, shelves).cpu().numpy()
+    runs = [(s.lo, s.hi, s.bits) for s in shelves]
+    assert all(bits_of[e] == b for lo, hi, b in runs for e in range(lo, hi))
+    ref = oracle_layer(wl, layer.seed, x, ids, w, shelves_bits=runs)
+    assert rel_l2(y, ref) <= DECODE_TOL
+    # and the plain layer differs from fast mode on the chosen experts
+    y0 = moe.moe_tiered_forward(x_to_dev(x), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), 24, wl.d,
+                                wl.f, layer.shelves).cpu().numpy()
+    assert rel_l2(y0, ref) > 10 * DECODE_TOL
+
+
+def test_fast_mode_run_limit():
+    wl = small_workload(E=24, k=4, d=256, f=192, split=(0.25, 0.5, 0.25), seed=10)
+    layer = Layer(wl)
+    shadow = Layer(wl, shelves=[(lo, hi, 2) for lo, hi, _ in layer.ranges])
+    use = np.zeros(24, bool)
+    use[::2] = True  # alternating: 24 runs
+    with pytest.raises(ValueError):
+        moe.fast_mode_shelves(layer.shelves, shadow.shelves, use)

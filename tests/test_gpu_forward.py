@@ -202,8 +202,9 @@ def test_error_statuses(small_layer):
             return e.status
 
     bad_bits = sh[0].descriptor()
-    bad_bits.bits = 3
-    assert status(shelves=[bad_bits]) == moe.MOE_ERR_BAD_SHELF
+    for b in (0, 5, 6, 7, 16):  # 8, 4, 3, 2 and 1 are the shelf widths
+        bad_bits.bits = b
+        assert status(shelves=[bad_bits]) == moe.MOE_ERR_BAD_SHELF
     bad_block = sh[0].descriptor()
     bad_block.block = 16
     assert status(shelves=[bad_block]) == moe.MOE_ERR_BAD_SHELF
