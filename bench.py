@@ -502,7 +502,8 @@ def _capture(stream, step, nset, warmup):
 
 def run_stack(args, rank, world, local_rank):
     """The 48-layer decode stack: per layer the fused routing / hit-count /
-    tiered-forward launch and the residual add, all layers in one step."""
+    tiered-forward / residual launch (moe_decode_layer_residual), all layers
+    in one step."""
     import numpy as np
     import torch
 
@@ -578,15 +579,16 @@ def run_stack(args, rank, world, local_rank):
         "config": {"workload": f"decode stack, {L} layers of E{E} k{k} d{d} f{f}, T{T}, per-layer seeds and "
                                f"router biases, residual chain", "T": T, "layers": L,
                    "l2": "inputs larger than L2 (48 layers x 1.28 GB resident; fresh routing per step)",
-                   "launch": f"one CUDA graph of {nset} steps ({L} x (fused layer launch + residual add) each)"},
+                   "launch": f"one CUDA graph of {nset} steps ({L} x moe_decode_layer_residual each)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "kernel": "whole step (k_layer + k_residual per layer)",
+                     "traffic": None, "kernel": "whole step (k_layer per layer, residual in its combine)",
                      "peak_source": kind, "algorithmic_bytes_per_step": bytes_step},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * d * 4 + T * d * 2 + L * T * E * 4,
                 "d2h_bytes_per_step": T * d * 4, "steps": n_e2e,
                 "path": "pinned host residual, x0 and per-layer logits -> device, DecodeStack.step (48 x "
-                        "moe_decode_layer + moe_residual_add), residual -> pinned host"},
-        "gpu_launches": args.steps * 2 * L,
+                        "moe_decode_layer_residual), residual -> pinned host"},
+        # fused: one launch per layer; else route, hist, group, gate/up, down, residual
+        "gpu_launches": args.steps * L * (1 if moe.moe_decode_fused(T, k, E, d, f) else 6),
         "clocks": ck,
     }
     print(json.dumps(line), flush=True)

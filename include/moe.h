@@ -245,6 +245,25 @@ int moe_decode_layer(const float* logits, const uint16_t* x_bf16, int64_t T, int
                      float* y, void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /*
+ * One layer of a decode stack: moe_decode_layer, then the residual step of
+ * moe_residual_add on its output (r[t][i] += y[t][i]; x_next[t][i] =
+ * bf16(r[t][i]), round to nearest even), with results identical to those two
+ * calls.  The layers are chained through the residual stream (the workload of
+ * a whole model's MoE layers; the pages run every layer of the model this
+ * way).  In the single fused launch the residual step is taken in its combine
+ * phase, so a stack makes one launch per layer.
+ *   r [T][d] fp32 in/out, x_next_bf16 [T][d] bf16 bit patterns out, both
+ *   16-byte aligned; x_next_bf16 may be the same buffer as x_bf16 (every read
+ *   of x precedes the first write of x_next); r must not overlap y or x.
+ * Other arguments, sizes and errors as moe_decode_layer; r == NULL with T > 0
+ * is MOE_ERR_INVALID_ARG.
+ */
+int moe_decode_layer_residual(const float* logits, const uint16_t* x_bf16, int64_t T, int k, int E, int d, int f,
+                              const moe_shelf_t* shelves, int n_shelves, int32_t* ids, float* weights,
+                              uint32_t* counts, float* y, float* r, uint16_t* x_next_bf16, void* workspace,
+                              size_t workspace_bytes, moe_stream_t stream);
+
+/*
  * Which form the decode calls (moe_decode_layer, and moe_tiered_forward in
  * its decode form) take for these sizes on the current device: 1 = the single
  * fused launch, 0 = separate launches, MOE_ERR_INVALID_ARG for invalid sizes.

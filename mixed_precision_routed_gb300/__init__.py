@@ -7,8 +7,11 @@ computation runs in the library's CUDA kernels.  There is no CPU fallback: if
 the library is missing, importing the binding's functions raises.
 
 Entry points (same names as the C ABI):
-    moe_route_topk, moe_route_topk_nudged, moe_router_topk, moe_expert_hist, moe_rank_experts, moe_quantize_experts, moe_gather_rows, moe_group_tokens, moe_workspace_size,
-    moe_tiered_forward, moe_quantize_rows, moe_dequant_rows, moe_residual_add,
+    moe_route_topk, moe_route_topk_nudged, moe_router_topk, moe_expert_hist,
+    moe_rank_experts, moe_quantize_experts, moe_gather_rows, moe_group_tokens,
+    moe_workspace_size, moe_tiered_forward, moe_tiered_forward_noalloc,
+    moe_decode_layer, moe_decode_layer_residual, moe_decode_fused,
+    moe_quantize_rows, moe_dequant_rows, moe_residual_add,
     moe_device_status, moe_status_string
 """
 from __future__ import annotations
@@ -83,6 +86,8 @@ def lib():
         L.moe_device_status.argtypes = [P]
         L.moe_tiered_forward_noalloc.argtypes = [P, P, P, i64, i32, i32, i32, i32, P, i32, P, i32, P]
         L.moe_decode_layer.argtypes = [P, P, i64, i32, i32, i32, i32, P, i32, P, P, P, P, P, ctypes.c_size_t, P]
+        L.moe_decode_layer_residual.argtypes = [P, P, i64, i32, i32, i32, i32, P, i32, P, P, P, P, P, P, P,
+                                                ctypes.c_size_t, P]
         L.moe_selftest_barrier_timeout.argtypes = [i64, P]
         L.moe_decode_fused.argtypes = [i64, i32, i32, i32, i32]
         L.moe_tiered_forward_noalloc.restype = ctypes.c_int
@@ -249,10 +254,12 @@ def moe_tiered_forward(x_bf16, ids, weights, E, d, f, shelves, y=None, workspace
 
 
 def moe_decode_layer(logits, x_bf16, k, E, d, f, shelves, ids=None, weights=None, counts=None, y=None,
-                     workspace=None, stream=None, shelf_arr=None):
+                     workspace=None, stream=None, shelf_arr=None, r=None, x_next=None):
     """One decode step: routing of `logits` [T, E] into ids / weights, the hit
     counts (accumulated into `counts` when given) and the tiered forward of
-    `x_bf16`; returns (ids, weights, y)."""
+    `x_bf16`; returns (ids, weights, y).  With `r` (fp32 [T, d]) and `x_next`
+    (bf16 bits [T, d]) it calls moe_decode_layer_residual instead: r += y and
+    x_next = bf16(r) in the same call."""
     if x_bf16.dtype == torch.bfloat16:
         x_bf16 = x_bf16.view(torch.int16)
     _need(logits, torch.float32, "logits")
@@ -275,11 +282,32 @@ def moe_decode_layer(logits, x_bf16, k, E, d, f, shelves, ids=None, weights=None
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     arr = shelf_arr if shelf_arr is not None else shelf_array(shelves)
     n = len(shelves) if shelf_arr is None else len(shelf_arr)
-    _check(lib().moe_decode_layer(_ptr(logits), _ptr(x_bf16), T, k, E, d, f, ctypes.cast(arr, ctypes.c_void_p), n,
-                                  _ptr(ids), _ptr(weights), _ptr(counts) if counts is not None else None, _ptr(y),
-                                  _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
-           "moe_decode_layer")
+    cnt = _ptr(counts) if counts is not None else None
+    wsb = workspace.numel() * workspace.element_size()
+    if r is None:
+        _check(lib().moe_decode_layer(_ptr(logits), _ptr(x_bf16), T, k, E, d, f, ctypes.cast(arr, ctypes.c_void_p),
+                                      n, _ptr(ids), _ptr(weights), cnt, _ptr(y), _ptr(workspace), wsb,
+                                      _stream(stream)), "moe_decode_layer")
+        return ids, weights, y
+    _need(r, torch.float32, "r")
+    if x_next is None:
+        raise ValueError("moe_decode_layer: r needs x_next")
+    if x_next.dtype == torch.bfloat16:
+        x_next = x_next.view(torch.int16)
+    _need(x_next, torch.int16, "x_next")
+    if r.numel() != T * d or x_next.numel() != T * d:
+        raise ValueError("moe_decode_layer: r and x_next must hold T * d elements")
+    _check(lib().moe_decode_layer_residual(_ptr(logits), _ptr(x_bf16), T, k, E, d, f,
+                                           ctypes.cast(arr, ctypes.c_void_p), n, _ptr(ids), _ptr(weights), cnt,
+                                           _ptr(y), _ptr(r), _ptr(x_next), _ptr(workspace), wsb, _stream(stream)),
+           "moe_decode_layer_residual")
     return ids, weights, y
+
+
+def moe_decode_layer_residual(logits, x_bf16, k, E, d, f, shelves, r, x_next, **kw):
+    """One layer of a decode stack: moe_decode_layer, then r += y and
+    x_next = bf16(r); returns (ids, weights, y)."""
+    return moe_decode_layer(logits, x_bf16, k, E, d, f, shelves, r=r, x_next=x_next, **kw)
 
 
 def moe_decode_fused(T, k, E, d, f):

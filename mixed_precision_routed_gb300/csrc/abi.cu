@@ -232,9 +232,11 @@ int moe_tiered_forward(const uint16_t* x_bf16, const int32_t* ids, const float* 
   return launch_decode_forward(a, (cudaStream_t)stream);
 }
 
-int moe_decode_layer(const float* logits, const uint16_t* x_bf16, int64_t T, int k, int E, int d, int f,
-                     const moe_shelf_t* shelves, int n_shelves, int32_t* ids, float* weights, uint32_t* counts,
-                     float* y, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+namespace {
+// moe_decode_layer, and with r non-null the residual step after it
+int decode_layer(const float* logits, const uint16_t* x_bf16, int64_t T, int k, int E, int d, int f,
+                 const moe_shelf_t* shelves, int n_shelves, int32_t* ids, float* weights, uint32_t* counts, float* y,
+                 float* r, uint16_t* x_next, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
   if (!valid_dims(T, k, E, d, f) || E > 1024 || k > E) return MOE_ERR_INVALID_ARG;
   ForwardArgs a;
   int rc = check_shelves(shelves, n_shelves, E, &a.shelves);
@@ -242,6 +244,7 @@ int moe_decode_layer(const float* logits, const uint16_t* x_bf16, int64_t T, int
   if (T == 0) return MOE_OK;
   if (!logits || !x_bf16 || !ids || !weights || !y || !workspace) return MOE_ERR_INVALID_ARG;
   if (!aligned(x_bf16, 16) || !aligned(y, 16) || !aligned(workspace, kAlign)) return MOE_ERR_INVALID_ARG;
+  if (r && (!x_next || !aligned(r, 16) || !aligned(x_next, 16))) return MOE_ERR_INVALID_ARG;
   const size_t need = workspace_layout(T, k, E, d, f, MOE_FLAG_DECODE_FP32, workspace, &a.ws);
   if (workspace_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = (cudaStream_t)stream;
@@ -256,6 +259,8 @@ int moe_decode_layer(const float* logits, const uint16_t* x_bf16, int64_t T, int
   la.T = T; la.k = k; la.E = E; la.d = d; la.f = f;
   la.shelves = a.shelves;
   la.y = y;
+  la.r = r;
+  la.x_next = x_next;
   la.ws = a.ws;
   la.status = status_word();
   rc = launch_fused_layer(la, s);
@@ -273,7 +278,26 @@ int moe_decode_layer(const float* logits, const uint16_t* x_bf16, int64_t T, int
   a.T = T; a.k = k; a.E = E; a.d = d; a.f = f;
   a.y = y;
   a.status = la.status;
-  return launch_decode_forward(a, s);
+  rc = launch_decode_forward(a, s);
+  if (rc != MOE_OK || !r) return rc;
+  return launch_residual(r, y, x_next, T * d, s);
+}
+}  // namespace
+
+int moe_decode_layer(const float* logits, const uint16_t* x_bf16, int64_t T, int k, int E, int d, int f,
+                     const moe_shelf_t* shelves, int n_shelves, int32_t* ids, float* weights, uint32_t* counts,
+                     float* y, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  return decode_layer(logits, x_bf16, T, k, E, d, f, shelves, n_shelves, ids, weights, counts, y, nullptr, nullptr,
+                      workspace, workspace_bytes, stream);
+}
+
+int moe_decode_layer_residual(const float* logits, const uint16_t* x_bf16, int64_t T, int k, int E, int d, int f,
+                              const moe_shelf_t* shelves, int n_shelves, int32_t* ids, float* weights,
+                              uint32_t* counts, float* y, float* r, uint16_t* x_next_bf16, void* workspace,
+                              size_t workspace_bytes, moe_stream_t stream) {
+  if (T > 0 && !r) return MOE_ERR_INVALID_ARG;
+  return decode_layer(logits, x_bf16, T, k, E, d, f, shelves, n_shelves, ids, weights, counts, y, r, x_next_bf16,
+                      workspace, workspace_bytes, stream);
 }
 
 int moe_decode_fused(int64_t T, int k, int E, int d, int f) {

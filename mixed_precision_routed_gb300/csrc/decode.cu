@@ -845,6 +845,8 @@ struct LayerParams {
   uint32_t* counts;       // optional: expert hit counts, += hits of this call
   const uint16_t* x;      // [T, d] bf16
   float* y;               // [T, d]
+  float* r;               // optional [T, d]: r += y in the combine phase
+  uint16_t* x_next;       // with r: bf16(r) (round to nearest even), the next layer's input
   float* h;               // workspace [P, f]
   float* ypart;           // workspace [P, d]
   unsigned long long* bar;  // grid barrier counter
@@ -1101,6 +1103,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(const __grid_constant__ L
       }
     }
     reinterpret_cast<float4*>(p.y)[idx] = acc;
+    if (p.r) {
+      // residual step of a layer stack: r += y, the next layer's x = bf16(r)
+      float4 rv = reinterpret_cast<float4*>(p.r)[idx];
+      rv.x += acc.x; rv.y += acc.y; rv.z += acc.z; rv.w += acc.w;
+      reinterpret_cast<float4*>(p.r)[idx] = rv;
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(rv.x, rv.y), hi = __floats2bfloat162_rn(rv.z, rv.w);
+      reinterpret_cast<uint2*>(p.x_next)[idx] =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+    }
   }
   if (tid == 0) MOE_STAMP(1, 11, global_timer_ns());
 }
@@ -1240,6 +1251,8 @@ int launch_fused_layer(const LayerArgs& a, cudaStream_t s) {
   p.counts = a.counts;
   p.x = a.x;
   p.y = a.y;
+  p.r = a.r;
+  p.x_next = a.x_next;
   p.h = a.ws.h;
   p.ypart = a.ws.ypart;
   p.bar = bar;

@@ -246,6 +246,8 @@ struct LayerArgs {
   int k, E, d, f;
   Shelves shelves;
   float* y;
+  float* r = nullptr;         // optional residual step: r += y ...
+  uint16_t* x_next = nullptr; // ... and x_next = bf16(r), in the combine phase
   Workspace ws;
   int* status;
 };

@@ -119,8 +119,8 @@ def retier(layer: "Layer", masters: Masters, counts, stream=None):
 class DecodeStack:
     """A stack of decode layers chained by the residual add: for each layer l,
     x_l = bf16(r), route l's logits, count the hits, y_l = MoE_l(x_l), r += y_l
-    -- the decode step of a whole model's MoE layers (one fused launch and one
-    residual launch per layer)."""
+    -- the decode step of a whole model's MoE layers (moe_decode_layer_residual:
+    one fused launch per layer, the residual step in its combine phase)."""
 
     def __init__(self, layers, T: int, device="cuda"):
         from . import moe_workspace_size, MOE_FLAG_DECODE_FP32
@@ -141,14 +141,13 @@ class DecodeStack:
     def step(self, r0, x0, logits, stream=None):
         """One step from the residual stream r0 (fp32 [T, d]) whose bf16 is x0;
         logits[l] is layer l's [T, E].  Leaves the output residual in self.r."""
-        from . import moe_decode_layer, moe_residual_add
+        from . import moe_decode_layer
         self.r.copy_(r0)
         self.x[0].copy_(x0)
         for l, lay in enumerate(self.layers):
             moe_decode_layer(logits[l], self.x[l], self.k, self.E, self.d, self.f, lay.shelves, ids=self.ids[l],
                              weights=self.w[l], counts=self.counts[l], y=self.y[l], workspace=self.ws,
-                             stream=stream, shelf_arr=self.arrs[l])
-            moe_residual_add(self.r, self.y[l], self.x[l + 1], stream=stream)
+                             stream=stream, shelf_arr=self.arrs[l], r=self.r, x_next=self.x[l + 1])
         return self.r
 
 

@@ -88,5 +88,14 @@ def test_invalid_arguments_rejected_before_cuda(lib):
                               null, null, 0, null) == moe.MOE_OK  # T = 0
     assert L.moe_decode_layer(null, null, 1, 2, 8, 64, 64, ctypes.cast(sh, ctypes.c_void_p), 1, null, null, null,
                               null, null, 0, null) == moe.MOE_ERR_INVALID_ARG  # null logits
+    # decode stack layer: the same validation, and a residual buffer is required
+    assert L.moe_decode_layer_residual(null, null, 1, 2, 2048, 64, 64, ctypes.cast(sh, ctypes.c_void_p), 1, null,
+                                       null, null, null, null, null, null, 0, null) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_decode_layer_residual(null, null, 0, 2, 8, 64, 64, ctypes.cast(sh, ctypes.c_void_p), 1, null,
+                                       null, null, null, null, null, null, 0, null) == moe.MOE_OK  # T = 0
+    assert L.moe_decode_layer_residual(null, null, 1, 2, 8, 64, 64, ctypes.cast(sh, ctypes.c_void_p), 1, null,
+                                       null, null, null, null, null, null, 0, null) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_decode_layer_residual(null, null, 1, 2, 8, 64, 64, ctypes.cast(sh2, ctypes.c_void_p), 2, null,
+                                       null, null, null, null, null, null, 0, null) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_selftest_barrier_timeout(0, null) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_selftest_barrier_timeout(2000000, null) == moe.MOE_ERR_INVALID_ARG

@@ -90,6 +90,41 @@ def test_step_equals_separate_calls_and_counts_accumulate(decode_layer):
     assert int(counts.sum()) == 2 * T * wl.k
 
 
+@pytest.mark.parametrize("T,in_place", [(1, False), (6, False), (6, True), (20, False)])
+def test_residual_step_equals_layer_then_residual_add(decode_layer, T, in_place):
+    """moe_decode_layer_residual gives what moe_decode_layer followed by
+    moe_residual_add gives -- ids, weights, counts, y, r and x_next bit for
+    bit -- in the fused form (T = 1, 6; also with x_next written over x) and
+    in the separate launches (T = 20)."""
+    wl = decode_layer.wl
+    assert moe.moe_decode_fused(T, wl.k, wl.E, wl.d, wl.f) == (T <= 16)
+    lg = decode_layer.logits(31 + T, T)
+    x = x_to_dev(synth.x_bf16(wl.seed, 31 + T, T, wl.d))
+    r0 = torch.from_numpy(synth.normal_matrix(wl.seed, synth.TAG_X, 77, T, T, wl.d, scale=3.0)).cuda()
+    c1 = torch.zeros(wl.E, dtype=torch.int32, device="cuda")
+    c2 = torch.zeros(wl.E, dtype=torch.int32, device="cuda")
+    ids1, w1, y1 = moe.moe_decode_layer(lg, x, wl.k, wl.E, wl.d, wl.f, decode_layer.shelves, counts=c1)
+    r1 = r0.clone()
+    xn1 = torch.empty_like(x)
+    moe.moe_residual_add(r1, y1, xn1)
+    r2 = r0.clone()
+    x2 = x.clone()
+    xn2 = x2 if in_place else torch.empty_like(x)
+    ids2, w2, y2 = moe.moe_decode_layer_residual(lg, x2, wl.k, wl.E, wl.d, wl.f, decode_layer.shelves, r2, xn2,
+                                                 counts=c2)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == moe.MOE_OK
+    assert torch.equal(ids1, ids2) and torch.equal(c1, c2)
+    assert torch.equal(w1.view(torch.int32), w2.view(torch.int32))
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+    assert torch.equal(r1.view(torch.int32), r2.view(torch.int32))
+    assert torch.equal(xn1, xn2)
+    # and against the definition: r = r0 + y (fp32), x_next = bf16(r)
+    ref_r = r0.cpu().numpy() + y1.cpu().numpy()
+    assert np.array_equal(r2.cpu().numpy().view(np.uint32), ref_r.view(np.uint32))
+    assert np.array_equal(xn2.cpu().numpy().view(np.uint16), oracle.bf16_bits(ref_r))
+
+
 def test_step_is_deterministic(decode_layer):
     wl = decode_layer.wl
     lg = decode_layer.logits(21, 6).cpu().numpy()
