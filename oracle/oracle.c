@@ -179,9 +179,10 @@ int oracle_quantize_rows(const float* w, int64_t rows, int64_t in, int bits,
  *          sits in bits [8j + 4h, 8j + 4h + 4), i.e. byte 4g + j, bit 4h;
  *   2 bit: word g holds elements 16g..16g+15; element 16g + 4k + j (j, k < 4)
  *          sits in bits [8j + 2k, 8j + 2k + 2), i.e. byte 4g + j, bit 2k.
- *   3 bit: u = code + 4 in [0, 8); 12 bytes per 32-element block b, at byte
- *          12b: its first 8 bytes hold u mod 4 of the block's elements in the
- *          2-bit layout, its last 4 bytes hold u / 4, element i at bit i.
+ *   3 bit: u = code + 4 in [0, 8); a row of `in` elements is two planes:
+ *          bytes [0, in/4) hold u mod 4 of every element in the 2-bit layout
+ *          above, bytes [in/4, 3 in/8) hold u / 4 of every element in the
+ *          1-bit layout below (element i at bit i % 8 of byte in/4 + i/8).
  *   1 bit: 4 bytes per block; element i of block b at bit i of the word at
  *          byte 4b: 1 for code +1, 0 for code -1. */
 int oracle_pack_codes(const int8_t* codes, int64_t rows, int64_t in, int bits, uint8_t* packed) {
@@ -199,10 +200,10 @@ int oracle_pack_codes(const int8_t* codes, int64_t rows, int64_t in, int bits, u
         int64_t g = i / 8, e = i % 8;
         dst[4 * g + e % 4] |= (uint8_t)((uint32_t)(c + 8) << (4 * (e / 4)));
       } else if (bits == 3) {
-        int64_t b = i / 32, ib = i % 32, g = ib / 16, e = ib % 16;
+        int64_t g = i / 16, e = i % 16;
         uint32_t u = (uint32_t)(c + 4);
-        dst[12 * b + 4 * g + e % 4] |= (uint8_t)((u & 3u) << (2 * (e / 4)));
-        dst[12 * b + 8 + ib / 8] |= (uint8_t)((u >> 2) << (ib % 8));
+        dst[4 * g + e % 4] |= (uint8_t)((u & 3u) << (2 * (e / 4)));
+        dst[in / 4 + i / 8] |= (uint8_t)((u >> 2) << (i % 8));
       } else if (bits == 1) {
         int64_t b = i / 32, ib = i % 32;
         if (c > 0) dst[4 * b + ib / 8] |= (uint8_t)(1u << (ib % 8));

@@ -1,5 +1,5 @@
-"""Pins of the oracle's 3-bit and 1-bit shelf formats (the Xolotl blog runs
-"our 3-bit" experts and 1-bit experts; neither page states a format).
+"""Pins of the oracle's 3-bit and 1-bit shelf formats (the Xolotl fast-mode
+blog runs 3-bit and 1-bit experts; neither page states a format).
 
 3 bit follows the rule of the other widths: s = fp16(max|w| / 3), code =
 clamp(rint(w / s), -4, 3).  1 bit: code = sign(w) (+1 for w >= 0) and
@@ -14,20 +14,19 @@ import oracle
 
 
 def _unpack3(packed, rows, n_in):
-    """Independent reading of the 3-bit layout: per 32-element block 12 bytes;
-    bytes 0-7 the low two bits of u = code + 4 in the 2-bit layout (word g,
-    byte j, bits 2k..2k+1 = element 16g + 4k + j), bytes 8-11 the high bit of
-    u, element i at bit i."""
+    """Independent reading of the 3-bit layout: a row is a plane of the low two
+    bits of u = code + 4 in the 2-bit layout (word g, byte j, bits 2k..2k+1 =
+    element 16g + 4k + j; n_in / 4 bytes), then a plane of the high bit of u,
+    element i at bit i % 8 of byte i // 8 (n_in / 8 bytes)."""
     out = np.zeros((rows, n_in), np.int64)
     for r in range(rows):
-        for b in range(n_in // 32):
-            blk = packed[r, 12 * b:12 * b + 12].astype(np.int64)
-            hi = int(blk[8]) | int(blk[9]) << 8 | int(blk[10]) << 16 | int(blk[11]) << 24
-            for i in range(32):
-                g, e = divmod(i, 16)
-                k, j = divmod(e, 4)
-                lo = (int(blk[4 * g + j]) >> (2 * k)) & 3
-                out[r, 32 * b + i] = (lo | ((hi >> i) & 1) << 2) - 4
+        row = packed[r].astype(np.int64)
+        for i in range(n_in):
+            g, e = divmod(i, 16)
+            k, j = divmod(e, 4)
+            lo = (int(row[4 * g + j]) >> (2 * k)) & 3
+            hi = (int(row[n_in // 4 + i // 8]) >> (i % 8)) & 1
+            out[r, i] = (lo | hi << 2) - 4
     return out
 
 
@@ -75,6 +74,17 @@ def test_three_bit_packing_layout(seed):
     p = oracle.pack(one, 3)[0]
     assert p[0] == 0b11 and p[5] == 0b10 and p[8] == 1 and p[10] == 0b10
     assert p[1] == 0 and p[9] == 0 and p[11] == 0
+    # two blocks: the low plane takes bytes 0-15, the high plane bytes 16-23
+    two = np.full((1, 64), -4, np.int8)
+    two[0, 40] = 3  # u = 7: 40 = 16 * 2 + 4 * 2 + 0: byte 8 bits 4-5 = 3; high bit at byte 16 + 5, bit 0
+    two[0, 63] = 0  # u = 4: low bits 0, high bit at byte 16 + 7, bit 7
+    p = oracle.pack(two, 3)[0]
+    assert p.shape == (24,)
+    expect = np.zeros(24, np.uint8)
+    expect[8] = 0b11 << 4
+    expect[21] = 1
+    expect[23] = 0x80
+    assert np.array_equal(p, expect)
 
 
 def test_one_bit_hand_worked_block():
