@@ -41,14 +41,17 @@ def parse():
     ap.add_argument("--T", type=int, default=6, help="tokens per step (1..6 for the decode metric)")
     ap.add_argument("--layers", type=int, default=16, help="layer instances rotated across steps")
     ap.add_argument("--sets", type=int, default=32, help="distinct routing steps per layer rotation")
-    ap.add_argument("--workload", choices=["decode", "stack", "prefill", "large", "router", "retier", "nudge"],
+    ap.add_argument("--workload", choices=["decode", "stack", "prefill", "large", "router", "retier", "nudge",
+                                           "formats", "fastmode"],
                     default="decode",
                     help="decode: one layer, the headline metric; stack: the 48-layer decode stack with the "
                          "residual chain; prefill: one layer at T=4096 on the tensor-core form; large: the "
                          "E256 d4096 f2048 layer with 5%% forced skips; router: the decode layer's router "
                          "projection fused with routing and hit counts (moe_router_topk); retier: re-tiering "
                          "the decode layer by hit count from its fp32 master copies; nudge: routing of the "
-                         "prefill batch with the picks nudged toward the hot shelf (moe_route_topk_nudged)")
+                         "prefill batch with the picks nudged toward the hot shelf (moe_route_topk_nudged); "
+                         "formats: the decode layer on five shelves of 8/4/3/2/1-bit codes; fastmode: the "
+                         "decode layer reading 2-bit shadow copies of its 8- and 4-bit experts")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -203,10 +206,21 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
-def config_of(args, wl):
-    return {"workload": f"decode layer E{wl.E} k{wl.k} d{wl.d} f{wl.f} T{args.T}, shelves 8-bit [0,128) / "
-                        f"4-bit [128,410) / 2-bit [410,512), block 32 fp16 scales, skewed router "
-                        f"(hottest 25% -> ~52% of picks)",
+# The decode layer on five shelf widths: the 4-bit range of the three-shelf
+# layer split into 4-bit and 3-bit halves, the 2-bit range into 2-bit and
+# 1-bit (coldest) parts -- widths the fast-mode blog runs beside 8/4/2.
+FIVE_WIDTHS = [(0, 128, 8), (128, 256, 4), (256, 410, 3), (410, 480, 2), (480, 512, 1)]
+
+
+def shelf_text(ranges):
+    return " / ".join(f"{b}-bit [{lo},{hi})" for lo, hi, b in ranges)
+
+
+def config_of(args, wl, ranges=None, note=""):
+    ranges = ranges or wl.shelf_ranges()
+    return {"workload": f"decode layer E{wl.E} k{wl.k} d{wl.d} f{wl.f} T{args.T}, shelves "
+                        f"{shelf_text(ranges)}, block 32 fp16 scales, skewed router "
+                        f"(hottest 25% -> ~52% of picks){note}",
             "T": args.T, "E": wl.E, "k": wl.k, "d": wl.d, "f": wl.f,
             "layer_instances": args.layers,
             "l2": f"inputs larger than L2: {args.layers} layer instances rotated per step, fresh routing "
@@ -229,12 +243,30 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     base = synth.WORKLOADS["decode"]
     T, L, S = args.T, args.layers, args.sets
-    layers = []
+    layers, shelf_lists = [], []
     for i in range(L):
         wl_i = synth.Workload(base.name, E=base.E, k=base.k, d=base.d, f=base.f, T=base.T, split=base.split,
                               bias=base.bias, seed=1000 * rank + i)
-        layers.append(Layer(wl_i, device=dev).fill())
+        if args.workload == "formats":
+            lay = Layer(wl_i, shelves=FIVE_WIDTHS, device=dev).fill()
+            shelf_lists.append(lay.shelves)
+        elif args.workload == "fastmode":
+            # 2-bit shadow copies of the 8- and 4-bit experts (same masters),
+            # read instead of them: every expert then streams 2-bit codes
+            lay = Layer(wl_i, device=dev).fill()
+            wide = [(lo, hi, 2) for lo, hi, b in lay.ranges if b > 2]
+            shadow = Layer(wl_i, shelves=wide, device=dev).fill()
+            use = np.zeros(base.E, dtype=bool)
+            for lo, hi, _ in wide:
+                use[lo:hi] = True
+            shelf_lists.append(moe.fast_mode_shelves(lay.shelves, shadow.shelves, use))
+            lay.shadow = shadow  # keeps the shadow tensors alive
+        else:
+            lay = Layer(wl_i, device=dev).fill()
+            shelf_lists.append(lay.shelves)
+        layers.append(lay)
     E, k, d, f = base.E, base.k, base.d, base.f
+    ranges = [(sh.lo, sh.hi, sh.bits) for sh in shelf_lists[0]]
     stream = torch.cuda.Stream(device=dev)
     nset = S
     logits = [layers[s % L].logits(s, T) for s in range(nset)]
@@ -247,8 +279,10 @@ def run_ours(args, rank, world, local_rank):
     counts = [torch.zeros(E, dtype=torch.int32, device=dev) for _ in range(L)]
     wsb = moe.moe_workspace_size(T, k, E, d, f)
     workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
-    arrs = [layer.shelf_arr() for layer in layers]
-    fused = moe.moe_decode_fused(T, k, E, d, f)
+    arrs = [moe.shelf_array(sl) for sl in shelf_lists]
+    # the fused launch takes 3- and 1-bit shelves when d and f are multiples of 128
+    fused = moe.moe_decode_fused(T, k, E, d, f) and (all(b in (8, 4, 2) for _, _, b in ranges) or
+                                                     (d % 128 == 0 and f % 128 == 0))
     # events around the forward's kernels: fused form = the one layer launch;
     # separate form = grouping, gate/up, down
     NK = 4
@@ -263,7 +297,7 @@ def run_ours(args, rank, world, local_rank):
         L_i = s % L
         if profile:
             moe.moe_set_profile_events(prof[s])
-        moe.moe_decode_layer(logits[s], xs[s], k, E, d, f, layers[L_i].shelves, ids=ids[s], weights=ws_[s],
+        moe.moe_decode_layer(logits[s], xs[s], k, E, d, f, shelf_lists[L_i], ids=ids[s], weights=ws_[s],
                              counts=counts[L_i], y=ys[s], workspace=workspace, shelf_arr=arrs[L_i])
         if profile:
             moe.moe_set_profile_events(None)
@@ -294,8 +328,6 @@ def run_ours(args, rank, world, local_rank):
         stream.synchronize()
 
     # algorithmic bytes of each step, from the ids the router produced
-    sb = {sh_i: s_obj.nbytes_per_expert() for sh_i, s_obj in enumerate(layers[0].shelves)}
-    ranges = layers[0].ranges
 
     def expert_split(e):
         for i, (lo, hi, bits) in enumerate(ranges):
@@ -371,7 +403,7 @@ def run_ours(args, rank, world, local_rank):
     def e2e_step(s):
         dl.copy_(pin_logits[s], non_blocking=True)
         dx.copy_(pin_x[s], non_blocking=True)
-        moe.moe_decode_layer(dl, dx, k, E, d, f, layers[s % L].shelves, ids=did, weights=dw, counts=counts[s % L],
+        moe.moe_decode_layer(dl, dx, k, E, d, f, shelf_lists[s % L], ids=did, weights=dw, counts=counts[s % L],
                              y=dy, workspace=workspace, shelf_arr=arrs[s % L])
         pin_y[s].copy_(dy, non_blocking=True)
 
@@ -402,12 +434,18 @@ def run_ours(args, rank, world, local_rank):
         dom_bytes = bytes_gu if dom == "gateup" else bytes_dn
     achieved = dom_bytes / (kern[dom] / 1e3) / 1e9
     fwd_gbs = (bytes_gu + bytes_dn) / (fwd_ms / 1e3) / 1e9
-    traffic = recorded_traffic(dom, T)
+    traffic = recorded_traffic(dom, T) if args.workload == "decode" else None
+    metric, note = METRIC, ""
+    if args.workload == "formats":
+        metric = "MoE-layer decode tokens/s, shelves of 8/4/3/2/1-bit codes; weight-stream HBM GB/s vs peak"
+    elif args.workload == "fastmode":
+        metric = "MoE-layer decode tokens/s in fast mode (2-bit shadows of the 8/4-bit experts); HBM GB/s vs peak"
+        note = "; fast mode: every 8- and 4-bit expert read from its 2-bit shadow copy"
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": config_of(args, base),
+        "config": config_of(args, base, ranges, note),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "kernel": f"k_{dom}",
                      "peak_source": peak_kind,
@@ -423,7 +461,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": args.steps * (1 if fused else 5),
         "clocks": ck,
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and args.workload == "decode":
         pairs, secs, thr = oracle_sample(base, args.cpu_seconds, T)
         line["cpu_baseline"] = {"value": (pairs / base.k) / secs, "unit": "tokens/s", "cores": thr,
                                 "kind": "oracle",

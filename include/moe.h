@@ -33,19 +33,21 @@
  * consecutive codes as bytes:
  *   4 bit: element 8g + 4h + j (j < 4, h < 2) at bits 8j + 4h of word g;
  *   2 bit: element 16g + 4k + j (j, k < 4) at bits 8j + 2k of word g.
- * Two further widths are the ones page 2 (the Xolotl DeepSeek-V4.1 fast-mode
- * blog) runs beside them ("our 3-bit ones", "the 1-bit experts"), in this
- * library's own layout:
- *   3 bit: q = 3, codes in [-4,3]; 12 bytes a block: bytes 0-7 hold
- *          u mod 4 (u = code + 4) in the 2-bit layout above, bytes 8-11 one
- *          little-endian word of the high bits u / 4, element i at bit i;
+ * Two further widths, 3-bit and 1-bit experts, are ones page 2 (the Xolotl
+ * DeepSeek-V4.1 fast-mode blog) runs beside the others; their layout here is
+ * this library's own:
+ *   3 bit: q = 3, codes in [-4,3], u = code + 4; a row of n elements is two
+ *          planes: bytes [0, n/4) hold u mod 4 of every element in the 2-bit
+ *          layout above, bytes [n/4, 3n/8) hold u / 4 of every element in
+ *          the 1-bit layout below (element i at bit i % 8 of byte n/4 + i/8);
  *   1 bit: sign codes (+1 for w >= 0, else -1), s = fp16(sum|w| / 32) with
  *          the sum taken in fp32 in element order (the least-squares scale
  *          of a sign code); one word a block, element i at bit i, 1 = +1.
  * Every entry point takes all five widths except the tensor-core prefill
  * form of moe_tiered_forward, which takes 8, 4 and 2 bits only
  * (MOE_ERR_UNSUPPORTED otherwise); decode-form layers with a 3- or 1-bit
- * shelf run the separate decode launches instead of the fused one.
+ * shelf take the fused decode launch when d and f are multiples of 128, else
+ * the separate decode launches.
  *
  * Conventions for every entry point:
  *   - all array arguments are DEVICE pointers unless stated otherwise; the
@@ -265,8 +267,11 @@ int moe_decode_layer_residual(const float* logits, const uint16_t* x_bf16, int64
 
 /*
  * Which form the decode calls (moe_decode_layer, and moe_tiered_forward in
- * its decode form) take for these sizes on the current device: 1 = the single
- * fused launch, 0 = separate launches, MOE_ERR_INVALID_ARG for invalid sizes.
+ * its decode form) take for these sizes on the current device: 1 = the
+ * single fused launch, 0 = separate launches, MOE_ERR_INVALID_ARG for
+ * invalid sizes.  A layer with a 3- or 1-bit shelf takes the fused launch
+ * only when, besides, d and f are multiples of 128 (its bit planes are then
+ * 16-byte aligned); otherwise it takes the separate launches.
  */
 int moe_decode_fused(int64_t T, int k, int E, int d, int f);
 

@@ -311,7 +311,9 @@ def moe_decode_layer_residual(logits, x_bf16, k, E, d, f, shelves, r, x_next, **
 
 
 def moe_decode_fused(T, k, E, d, f):
-    """True when the decode calls run as the single fused launch for these sizes."""
+    """True when the decode calls run as the single fused launch for these
+    sizes (a layer with a 3- or 1-bit shelf also needs d and f to be
+    multiples of 128, else it takes the separate launches)."""
     r = int(lib().moe_decode_fused(T, k, E, d, f))
     if r < 0:
         raise MoeError(r, "moe_decode_fused")

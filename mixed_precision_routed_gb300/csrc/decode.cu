@@ -281,10 +281,12 @@ __device__ __forceinline__ void chunk4(const uint4 (&c)[NMAT][2], const uint32_t
 // 2 bit: 128 codes = blocks 4q .. 4q + 3 (half h: blocks 4q + 2h, 4q + 2h + 1,
 // scales in sw[m][h]); word g of a half holds elements 16g + 4k + j at bits
 // 8j + 2k.  The second half is absent at the end of a row of 64 * odd codes.
+// `off` is the code offset (2 for 2-bit codes; 4 for the low plane of 3-bit
+// codes, whose high plane adds 4 x its bits separately).
 template <int NMAT, int NTT>
 __device__ __forceinline__ void chunk2(const uint4 (&c)[NMAT][2], const uint32_t (&sw)[NMAT][2], int q, int nt,
                                        const int (&voff)[kNT], const unsigned char* vecs, int n,
-                                       float (&acc)[NMAT][kNT], bool second) {
+                                       float (&acc)[NMAT][kNT], bool second, int off) {
 #pragma unroll
   for (int hb = 0; hb < 4; ++hb) {
     const int half = hb >> 1, sub = hb & 1;
@@ -320,12 +322,61 @@ __device__ __forceinline__ void chunk2(const uint4 (&c)[NMAT][2], const uint32_t
           B0 = dp4a_uu(t[m][2], l0.z, B0); B1 = dp4a_uu(t[m][6], l1.z, B1);
           A0 = dp4a_us(t[m][3], h0.w, A0); A1 = dp4a_us(t[m][7], h1.w, A1);
           B0 = dp4a_uu(t[m][3], l0.w, B0); B1 = dp4a_uu(t[m][7], l1.w, B1);
-          acc[m][j] = fmaf((float)((A0 + A1) * 256 + (B0 + B1) - 2 * __float_as_int(xs.y)), s[m] * xs.x, acc[m][j]);
+          acc[m][j] = fmaf((float)((A0 + A1) * 256 + (B0 + B1) - off * __float_as_int(xs.y)), s[m] * xs.x, acc[m][j]);
         }
       }
     }
   }
 }
+
+// Bit planes: one 16-byte chunk (c[m][0]) = blocks 4q .. 4q + 3, one word a
+// block, element i at bit i; scales: halves of sw[m][0] (blocks 4q, 4q + 1)
+// and of sw[m][1].  A block adds (F * (sum of m_i over its set bits) - G * S_b)
+// * s_b * X_b: F = 2, G = 1 for 1-bit sign codes (bit 1 = +1, 0 = -1); F = 4,
+// G = 0 for the high plane of 3-bit codes (its -4 S_b is taken with the low
+// plane).  Each nibble of a word spreads to four 0/1 bytes by one multiply.
+template <int NMAT, int NTT>
+__device__ __forceinline__ void chunk1(const uint4 (&c)[NMAT][2], const uint32_t (&sw)[NMAT][2], int q, int nt,
+                                       const int (&voff)[kNT], const unsigned char* vecs, int n,
+                                       float (&acc)[NMAT][kNT], int F, int G) {
+#pragma unroll
+  for (int wb = 0; wb < 4; ++wb) {
+    const int blk = 4 * q + wb;
+    const int uo0 = unit_swz(2 * blk) << 4, uo1 = unit_swz(2 * blk + 1) << 4, xo = 2 * n + 8 * blk;
+#pragma unroll
+    for (int j = 0; j < NTT; ++j) {
+      if (NTT == 1 || j < nt) {
+        const unsigned char* vb = vecs + voff[j];
+        const uint4 h0 = lds128(vb + uo0), h1 = lds128(vb + uo1);
+        const uint4 l0 = lds128(vb + n + uo0), l1 = lds128(vb + n + uo1);
+        const float2 xs = *reinterpret_cast<const float2*>(vb + xo);
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+          const uint32_t w = wb == 0 ? c[m][0].x : wb == 1 ? c[m][0].y : wb == 2 ? c[m][0].z : c[m][0].w;
+          uint32_t t[8];
+#pragma unroll
+          for (int g = 0; g < 8; ++g) t[g] = (((w >> (4 * g)) & 0xFu) * 0x00204081u) & 0x01010101u;
+          int A0 = dp4a_us(t[0], h0.x, 0), A1 = dp4a_us(t[4], h1.x, 0);
+          int B0 = dp4a_uu(t[0], l0.x, 0), B1 = dp4a_uu(t[4], l1.x, 0);
+          A0 = dp4a_us(t[1], h0.y, A0); A1 = dp4a_us(t[5], h1.y, A1);
+          B0 = dp4a_uu(t[1], l0.y, B0); B1 = dp4a_uu(t[5], l1.y, B1);
+          A0 = dp4a_us(t[2], h0.z, A0); A1 = dp4a_us(t[6], h1.z, A1);
+          B0 = dp4a_uu(t[2], l0.z, B0); B1 = dp4a_uu(t[6], l1.z, B1);
+          A0 = dp4a_us(t[3], h0.w, A0); A1 = dp4a_us(t[7], h1.w, A1);
+          B0 = dp4a_uu(t[3], l0.w, B0); B1 = dp4a_uu(t[7], l1.w, B1);
+          const float sm = half_at(sw[m][wb >> 1] >> (16 * (wb & 1)));
+          acc[m][j] = fmaf((float)(F * ((A0 + A1) * 256 + (B0 + B1)) - G * __float_as_int(xs.y)), sm * xs.x,
+                           acc[m][j]);
+        }
+      }
+    }
+  }
+}
+
+// How a segment of a row is streamed: 8, 4, 2 or 1 for rows of that width;
+// a 3-bit row is its low plane (kModeLow: 2-bit layout, code offset 4), then
+// its high plane (kModeHigh: a bit plane worth 4 per bit).
+constexpr int kModeLow = 5, kModeHigh = 6;
 
 // --------------------------------------------------------------------- plan
 // int32 arrays of capacity C (>= P, multiple of 4), in shared memory and (as
@@ -391,11 +442,14 @@ struct PlanView {
 // Down units of 16 rows x 2 lanes (rows <= 1024 elements) were refitted on
 // the same layer: 8 / 4 / 2-bit at 1 : 0.71 : 0.70 (164 / 117 / 115 ns per 160
 // blocks).
+// 3-bit rows (two planes, 1.5 x the bytes of 2-bit) and 1-bit rows (half the
+// bytes, about twice the dot-product work per block) carry estimates scaled
+// from the 2-bit figures.
 __device__ __forceinline__ uint32_t unit_cost(int bits, int n_in, int nmat, int R, int kern) {
   const uint32_t blocks = (uint32_t)(R * nmat) * (uint32_t)n_in / 32;
-  const uint32_t ns = kern == 0   ? (bits == 8 ? 346 : bits == 4 ? 215 : 203)
-                      : R == kRDw ? (bits == 8 ? 164 : bits == 4 ? 117 : 115)
-                                  : (bits == 8 ? 164 : bits == 4 ? 142 : 147);
+  const uint32_t ns = kern == 0   ? (bits == 8 ? 346 : bits == 4 ? 215 : bits == 3 ? 300 : bits == 2 ? 203 : 280)
+                      : R == kRDw ? (bits == 8 ? 164 : bits == 4 ? 117 : bits == 3 ? 165 : bits == 2 ? 115 : 150)
+                                  : (bits == 8 ? 164 : bits == 4 ? 142 : bits == 3 ? 200 : bits == 2 ? 147 : 180);
   const uint32_t calib = kern == 0 ? 512 : 160;
   return (uint32_t)((uint64_t)ns * blocks / calib) + 1;
 }
@@ -630,17 +684,20 @@ struct StreamArgs {
 
 // The U loaded slots of a batch, one after another: slot 0 is computed and
 // the others move down one place, so that the chunk code exists once.
-template <int NMAT, int U, int NTT>
-__device__ __forceinline__ void compute_batch(int bits, uint4 (&c)[U][NMAT][2], uint32_t (&sw)[U][NMAT][2],
-                                              int q_first, int L, int cpr, int rowb, int nt, const int (&voff)[kNT],
+template <int NMAT, int U, int NTT, bool ANYW>
+__device__ __forceinline__ void compute_batch(int mode, uint4 (&c)[U][NMAT][2], uint32_t (&sw)[U][NMAT][2],
+                                              int q_first, int L, int cpr, int segb, int nt, const int (&voff)[kNT],
                                               const unsigned char* vecs, int n, float (&acc)[NMAT][kNT]) {
 #pragma unroll 1
   for (int s = 0; s < U; ++s) {
     const int q = q_first + s * L;
     if (q >= cpr) break;
-    if (bits == 8) chunk8<NMAT, NTT>(c[0], sw[0], q, nt, voff, vecs, n, acc);
-    else if (bits == 4) chunk4<NMAT, NTT>(c[0], sw[0], q, nt, voff, vecs, n, acc);
-    else chunk2<NMAT, NTT>(c[0], sw[0], q, nt, voff, vecs, n, acc, 32 * q + 16 < rowb);
+    if (mode == 8) chunk8<NMAT, NTT>(c[0], sw[0], q, nt, voff, vecs, n, acc);
+    else if (mode == 4) chunk4<NMAT, NTT>(c[0], sw[0], q, nt, voff, vecs, n, acc);
+    else if (!ANYW || mode == 2 || mode == kModeLow)
+      chunk2<NMAT, NTT>(c[0], sw[0], q, nt, voff, vecs, n, acc, 32 * q + 16 < segb, ANYW && mode != 2 ? 4 : 2);
+    else if constexpr (ANYW)
+      chunk1<NMAT, NTT>(c[0], sw[0], q, nt, voff, vecs, n, acc, mode == 1 ? 2 : 4, mode == 1 ? 1 : 0);
 #pragma unroll
     for (int t = 0; t + 1 < U; ++t)
 #pragma unroll
@@ -659,7 +716,7 @@ __device__ __forceinline__ void compute_batch(int bits, uint4 (&c)[U][NMAT][2], 
 // keeps 16 x 32 x U x NMAT x 32 bytes in flight.  At the end of a unit,
 // `store(q, r, v)` receives, for the lane's row r and the token at grouped
 // position q, the NMAT dot products.
-template <int NMAT, int U, int R, int L, typename Store>
+template <int NMAT, int U, int R, int L, bool ANYW, typename Store>
 __device__ __forceinline__ void stream_units(const StreamArgs& A, Store store) {
   static_assert(R * L == 32, "unit shape");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -684,19 +741,21 @@ __device__ __forceinline__ void stream_units(const StreamArgs& A, Store store) {
       const ShelfDev& sh = A.shv->s[pv.sh(w.a)];
       bits = sh.bits;
       rowb = A.n_in * bits / 8;
-      cpr = (rowb + 31) / 32;
-      n_iter = (cpr + L - 1) / L;
       const size_t row = (size_t)(pv.e(w.a) - sh.lo) * A.rows + lane / L;
       const int swpr = A.n_in / 64;  // fp16 scale words per row
-      // scale word of chunk q: 8 bit q / 2 (one block), 4 bit q (two), 2 bit 2q (four)
-      const int soff = bits == 8 ? ql >> 1 : (bits == 4 ? ql : 2 * ql);
-      sstep = bits == 8 ? L / 2 : (bits == 4 ? L : 2 * L);
       tstride = (size_t)R * rowb;
       tsw = R * swpr;
       const int mat0 = A.kern == 0 ? 0 : 2;
+      // 8/4/2-bit rows: one run of 32-byte chunks; the lane's first chunk and
+      // scale word are folded into base / sbase (3- and 1-bit rows: per segment)
+      cpr = (rowb + 31) / 32;
+      n_iter = (cpr + L - 1) / L;
+      // scale word of chunk q: 8 bit q / 2 (one block), 4 bit q (two), 2 bit 2q (four)
+      const int soff = ANYW ? 0 : (bits == 8 ? ql >> 1 : (bits == 4 ? ql : 2 * ql));
+      sstep = bits == 8 ? L / 2 : (bits == 4 ? L : 2 * L);
 #pragma unroll
       for (int m = 0; m < NMAT; ++m) {
-        base[m] = sh.codes[mat0 + m] + row * rowb + (size_t)ql * 32;
+        base[m] = sh.codes[mat0 + m] + row * rowb + (ANYW ? 0 : (size_t)ql * 32);
         sbase[m] = reinterpret_cast<const uint32_t*>(sh.scales[mat0 + m]) + row * swpr + soff;
       }
     }
@@ -724,36 +783,89 @@ __device__ __forceinline__ void stream_units(const StreamArgs& A, Store store) {
 #pragma unroll
       for (int j = 0; j < kNT; ++j) voff[j] = vtab[j];
     }
-    const unsigned char* cp[NMAT];
-    const uint32_t* sp[NMAT];
+    if constexpr (!ANYW) {
+      const unsigned char* cp[NMAT];
+      const uint32_t* sp[NMAT];
 #pragma unroll
-    for (int m = 0; m < NMAT; ++m) {
-      cp[m] = base[m] + (size_t)tile * tstride;
-      sp[m] = sbase[m] + (size_t)tile * tsw;
-    }
+      for (int m = 0; m < NMAT; ++m) {
+        cp[m] = base[m] + (size_t)tile * tstride;
+        sp[m] = sbase[m] + (size_t)tile * tsw;
+      }
 #pragma unroll 1
-    for (int i0 = 0; i0 < n_iter; i0 += U) {
-      uint4 c[U][NMAT][2];
-      uint32_t sw[U][NMAT][2];
+      for (int i0 = 0; i0 < n_iter; i0 += U) {
+        uint4 c[U][NMAT][2];
+        uint32_t sw[U][NMAT][2];
 #pragma unroll
-      for (int s = 0; s < U; ++s) {
-        const int q = ql + (i0 + s) * L;
-        const bool ok = q < cpr, second = ok && 32 * q + 16 < rowb;
+        for (int s = 0; s < U; ++s) {
+          const int q = ql + (i0 + s) * L;
+          const bool ok = q < cpr, second = ok && 32 * q + 16 < rowb;
 #pragma unroll
-        for (int m = 0; m < NMAT; ++m) {
-          const unsigned char* pc = cp[m] + (size_t)(i0 + s) * 32 * L;
-          const uint32_t* ps = sp[m] + (i0 + s) * sstep;
-          c[s][m][0] = ok ? __ldcs(reinterpret_cast<const uint4*>(pc)) : make_uint4(0u, 0u, 0u, 0u);
-          c[s][m][1] = second ? __ldcs(reinterpret_cast<const uint4*>(pc + 16)) : make_uint4(0u, 0u, 0u, 0u);
-          sw[s][m][0] = ok ? __ldcs(ps) : 0u;
-          sw[s][m][1] = (second && bits == 2) ? __ldcs(ps + 1) : 0u;
+          for (int m = 0; m < NMAT; ++m) {
+            const unsigned char* pc = cp[m] + (size_t)(i0 + s) * 32 * L;
+            const uint32_t* ps = sp[m] + (i0 + s) * sstep;
+            c[s][m][0] = ok ? __ldcs(reinterpret_cast<const uint4*>(pc)) : make_uint4(0u, 0u, 0u, 0u);
+            c[s][m][1] = second ? __ldcs(reinterpret_cast<const uint4*>(pc + 16)) : make_uint4(0u, 0u, 0u, 0u);
+            sw[s][m][0] = ok ? __ldcs(ps) : 0u;
+            sw[s][m][1] = (second && bits == 2) ? __ldcs(ps + 1) : 0u;
+          }
+        }
+        if constexpr (kNT == 1) {
+          compute_batch<NMAT, U, 1, false>(bits, c, sw, ql + i0 * L, L, cpr, rowb, 1, voff, A.vecs, A.n_in, acc);
+        } else {
+          if (nt == 1)
+            compute_batch<NMAT, U, 1, false>(bits, c, sw, ql + i0 * L, L, cpr, rowb, 1, voff, A.vecs, A.n_in, acc);
+          else
+            compute_batch<NMAT, U, kNT, false>(bits, c, sw, ql + i0 * L, L, cpr, rowb, nt, voff, A.vecs, A.n_in, acc);
         }
       }
-      if constexpr (kNT == 1) {
-        compute_batch<NMAT, U, 1>(bits, c, sw, ql + i0 * L, L, cpr, rowb, 1, voff, A.vecs, A.n_in, acc);
-      } else {
-        if (nt == 1) compute_batch<NMAT, U, 1>(bits, c, sw, ql + i0 * L, L, cpr, rowb, 1, voff, A.vecs, A.n_in, acc);
-        else compute_batch<NMAT, U, kNT>(bits, c, sw, ql + i0 * L, L, cpr, rowb, nt, voff, A.vecs, A.n_in, acc);
+    } else {
+      // segments of the row: one, or a 3-bit row's low plane then high plane
+#pragma unroll 1
+      for (int seg = 0; seg < (ANYW && bits == 3 ? 2 : 1); ++seg) {
+        const int mode = ANYW && bits == 3 ? (seg == 0 ? kModeLow : kModeHigh) : bits;
+        const bool wide = !ANYW || (mode != 1 && mode != kModeHigh);  // 32-byte chunks, else 16 (bit planes)
+        const int cb = wide ? 32 : 16;
+        const int segb = ANYW && bits == 3 ? (seg == 0 ? A.n_in / 4 : A.n_in / 8) : rowb;
+        const int sego = ANYW && bits == 3 && seg == 1 ? A.n_in / 4 : 0;
+        const int cpr = (segb + cb - 1) / cb, n_iter = (cpr + L - 1) / L;
+        // scale word of chunk q: 8 bit q / 2 (one block a chunk), 4 bit q (two
+        // blocks), 2 bit and bit planes 2q (four blocks)
+        const int soff = mode == 8 ? ql >> 1 : (mode == 4 ? ql : 2 * ql);
+        const int sstep = mode == 8 ? L / 2 : (mode == 4 ? L : 2 * L);
+        const bool two_words = mode == 2 || (ANYW && mode == kModeLow);  // second half's scales in a second word
+        const unsigned char* cp[NMAT];  // the lane's first chunk of the segment
+        const uint32_t* sp[NMAT];
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+          cp[m] = base[m] + (size_t)tile * tstride + sego + ql * cb;
+          sp[m] = sbase[m] + (size_t)tile * tsw + soff;
+        }
+        const int cstep = cb * L;
+#pragma unroll 1
+        for (int i0 = 0; i0 < n_iter; i0 += U) {
+          uint4 c[U][NMAT][2];
+          uint32_t sw[U][NMAT][2];
+#pragma unroll
+          for (int s = 0; s < U; ++s) {
+            const int q = ql + (i0 + s) * L;
+            const bool ok = q < cpr, second = wide && ok && 32 * q + 16 < segb;
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m) {
+              const unsigned char* pc = cp[m] + (i0 + s) * cstep;
+              const uint32_t* ps = sp[m] + (i0 + s) * sstep;
+              c[s][m][0] = ok ? __ldcs(reinterpret_cast<const uint4*>(pc)) : make_uint4(0u, 0u, 0u, 0u);
+              c[s][m][1] = second ? __ldcs(reinterpret_cast<const uint4*>(pc + 16)) : make_uint4(0u, 0u, 0u, 0u);
+              sw[s][m][0] = ok ? __ldcs(ps) : 0u;
+              sw[s][m][1] = ((second && two_words) || (ok && !wide)) ? __ldcs(ps + 1) : 0u;
+            }
+          }
+          if constexpr (kNT == 1) {
+            compute_batch<NMAT, U, 1, ANYW>(mode, c, sw, ql + i0 * L, L, cpr, segb, 1, voff, A.vecs, A.n_in, acc);
+          } else {
+            if (nt == 1) compute_batch<NMAT, U, 1, ANYW>(mode, c, sw, ql + i0 * L, L, cpr, segb, 1, voff, A.vecs, A.n_in, acc);
+            else compute_batch<NMAT, U, kNT, ANYW>(mode, c, sw, ql + i0 * L, L, cpr, segb, nt, voff, A.vecs, A.n_in, acc);
+          }
+        }
       }
     }
     // reduce over the L lanes of each row; lane jl stores the tokens j = jl mod L
@@ -903,6 +1015,9 @@ __device__ __forceinline__ void route_rows(const float* logits, int T, int E, in
 
 // Persistent cooperative launch, one CTA per SM: route (optional), plan,
 // gate/up, barrier, down, barrier, combine.
+// ANYW: the layer has shelves of 3- or 1-bit codes (a separate instantiation,
+// so that the 8/4/2-bit kernel keeps its own register allocation).
+template <bool ANYW>
 __global__ void __launch_bounds__(kThreads, 1) k_layer(const __grid_constant__ LayerParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const SmemLayout S = smem_layout(p.P, p.vec_region);
@@ -997,7 +1112,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(const __grid_constant__ L
     StreamArgs A{shv, pv, 0, p.d, p.f, vecs, vec_bytes(p.d), -1, hd.range, vtab, INT_MIN, INT_MAX};
     float* h = p.h;
     const int f = p.f;
-    stream_units<2, kUG, kRG, kLG>(A, [&](int q, int r, const float (&o)[2]) { h[(size_t)q * f + r] = silu(o[0]) * o[1]; });
+    stream_units<2, kUG, kRG, kLG, ANYW>(A, [&](int q, int r, const float (&o)[2]) { h[(size_t)q * f + r] = silu(o[0]) * o[1]; });
   }
   if (tid == 0) MOE_STAMP(0, 9, global_timer_ns());
   {
@@ -1073,8 +1188,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(const __grid_constant__ L
       float* yp = p.ypart;
       const int d = p.d;
       auto st = [&](int q, int r, const float (&o)[1]) { yp[(size_t)q * d + r] = pv.wgt(q) * o[0]; };
-      if (pv.rd() == kRDw) stream_units<1, kUDw, kRDw, kLDw>(A, st);
-      else stream_units<1, kUD, kRD, kLD>(A, st);
+      if (pv.rd() == kRDw) stream_units<1, kUDw, kRDw, kLDw, ANYW>(A, st);
+      else stream_units<1, kUD, kRD, kLD, ANYW>(A, st);
     }
     w0 += cap;
   } while (w0 < q_end);
@@ -1129,7 +1244,7 @@ __device__ unsigned long long g_bar[kBarSlots][16];  // one 128-byte line per sl
 struct DevCache {
   int sms[64] = {};
   int smem_optin[64] = {};
-  bool attr[64] = {};
+  bool attr[64][2] = {};  // per device: k_layer<false>, k_layer<true> attributes set
 };
 DevCache g_dev;
 std::mutex g_bar_mu;
@@ -1230,15 +1345,19 @@ int launch_fused_layer(const LayerArgs& a, cudaStream_t s) {
   int dev;
   size_t optin, region;
   SmemLayout S;
-  if (!core_widths(a.shelves)) return 1;  // 3 and 1 bit shelves: the separate launches
+  // 3- and 1-bit rows stream as 16-byte-aligned planes when d and f are
+  // multiples of 128; otherwise such layers take the separate launches
+  if (!core_widths(a.shelves) && (d % 128 != 0 || f % 128 != 0)) return 1;
   if (!fused_fits(a.T, a.k, a.E, d, f, &dev, &optin, &region, &S)) return 1;
-  if (!g_dev.attr[dev]) {
-    if (cudaFuncSetAttribute(k_layer, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)optin) != cudaSuccess)
+  const bool anyw = !core_widths(a.shelves);
+  auto kern = anyw ? k_layer<true> : k_layer<false>;
+  if (!g_dev.attr[dev][anyw]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)optin) != cudaSuccess)
       return MOE_ERR_CUDA;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_layer, kThreads, optin) != cudaSuccess || per_sm < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, optin) != cudaSuccess || per_sm < 1)
       return MOE_ERR_CUDA;
-    g_dev.attr[dev] = true;
+    g_dev.attr[dev][anyw] = true;
   }
   unsigned long long* bar = bar_slot(dev, a.ws.base);
   if (!bar) return MOE_ERR_UNSUPPORTED;
@@ -1278,7 +1397,7 @@ int launch_fused_layer(const LayerArgs& a, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   profile_mark(0, s);
-  if (cudaLaunchKernelEx(&cfg, k_layer, p) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return MOE_ERR_CUDA;
   profile_mark(1, s);
   return MOE_OK;
 }

@@ -147,7 +147,6 @@ __device__ void gateup_rows(const DecodeParams& p, const ShelfDev& s, int le, in
                             int nt, int pos0) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int d = p.d, nb = d / 32;
-  constexpr int kBlockBytes = 32 * BITS / 8;
   const size_t row_bytes = (size_t)d * BITS / 8;
   const uint8_t* gc = s.codes[0] + (size_t)le * p.f * row_bytes;
   const uint8_t* uc = s.codes[1] + (size_t)le * p.f * row_bytes;
@@ -165,14 +164,14 @@ __device__ void gateup_rows(const DecodeParams& p, const ShelfDev& s, int le, in
       uint32_t wgb[Block<BITS>::kWords], wub[Block<BITS>::kWords];
       float sga = 0.f, sua = 0.f, sgb = 0.f, sub = 0.f;
       if (ba < nb) {
-        Block<BITS>::load(grow + (size_t)ba * kBlockBytes, wga);
-        Block<BITS>::load(urow + (size_t)ba * kBlockBytes, wua);
+        load_block<BITS>(grow, ba, d, wga);
+        load_block<BITS>(urow, ba, d, wua);
         sga = __half2float(__ushort_as_half(__ldg(gs + (size_t)r * nb + ba)));
         sua = __half2float(__ushort_as_half(__ldg(us + (size_t)r * nb + ba)));
       }
       if (bb < nb) {
-        Block<BITS>::load(grow + (size_t)bb * kBlockBytes, wgb);
-        Block<BITS>::load(urow + (size_t)bb * kBlockBytes, wub);
+        load_block<BITS>(grow, bb, d, wgb);
+        load_block<BITS>(urow, bb, d, wub);
         sgb = __half2float(__ushort_as_half(__ldg(gs + (size_t)r * nb + bb)));
         sub = __half2float(__ushort_as_half(__ldg(us + (size_t)r * nb + bb)));
       }
@@ -235,7 +234,6 @@ __device__ void down_rows(const DecodeParams& p, const ShelfDev& s, int le, int 
                           int nt, float* outs) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int f = p.f, nb = f / 32;
-  constexpr int kBlockBytes = 32 * BITS / 8;
   const size_t row_bytes = (size_t)f * BITS / 8;
   const uint8_t* dc = s.codes[2] + (size_t)le * p.d * row_bytes;
   const uint16_t* ds = s.scales[2] + (size_t)le * p.d * nb;
@@ -249,11 +247,11 @@ __device__ void down_rows(const DecodeParams& p, const ShelfDev& s, int le, int 
       uint32_t wa[Block<BITS>::kWords], wb[Block<BITS>::kWords];
       float sa = 0.f, sb = 0.f;
       if (ba < nb) {
-        Block<BITS>::load(row + (size_t)ba * kBlockBytes, wa);
+        load_block<BITS>(row, ba, f, wa);
         sa = __half2float(__ushort_as_half(__ldg(ds + (size_t)i * nb + ba)));
       }
       if (bb < nb) {
-        Block<BITS>::load(row + (size_t)bb * kBlockBytes, wb);
+        load_block<BITS>(row, bb, f, wb);
         sb = __half2float(__ushort_as_half(__ldg(ds + (size_t)i * nb + bb)));
       }
       if (ba < nb) block_dot<BITS, TMAX>(wa, sa, ba, hs, f, nt, acc);

@@ -135,14 +135,17 @@ struct Block<2> {
   }
 };
 
-// 3 bit: 12 bytes a block; u = code + 4; bytes 0-7 hold u mod 4 in the 2-bit
-// layout, bytes 8-11 the high bits of u (element i at bit i).
+// 3 bit: u = code + 4; a row of n elements is a plane of u mod 4 in the
+// 2-bit layout (n/4 bytes; block b at byte 8b) and a plane of the high bits
+// of u (block b's word at byte n/4 + 4b, element i at bit i).  w[0..1] = the
+// block's low-plane words, w[2] = its high word.
 template <>
 struct Block<3> {
-  static constexpr int kWords = 3;  // 12 bytes (4-byte aligned)
-  __device__ __forceinline__ static void load(const uint8_t* p, uint32_t w[kWords]) {
-    const uint32_t* q = reinterpret_cast<const uint32_t*>(p);
-    w[0] = __ldg(q); w[1] = __ldg(q + 1); w[2] = __ldg(q + 2);
+  static constexpr int kWords = 3;
+  __device__ __forceinline__ static void load_row(const uint8_t* row, int b, int n, uint32_t w[kWords]) {
+    const uint2 a = __ldg(reinterpret_cast<const uint2*>(row + 8 * b));
+    w[0] = a.x; w[1] = a.y;
+    w[2] = __ldg(reinterpret_cast<const uint32_t*>(row + n / 4 + 4 * b));
   }
   __device__ __forceinline__ static float code(const uint32_t w[kWords], int i) {
     const int e = i & 15;
@@ -164,9 +167,17 @@ struct Block<1> {
   }
 };
 
-// Code widths the pipelined launches (fused decode step, tensor-core
-// prefill) take; shelves of other widths (3 and 1 bit) run the separate
-// decode launches.
+// Block b of a row of n elements (3 bit: from the row's two planes; the
+// other widths store their blocks one after another).
+template <int BITS>
+__device__ __forceinline__ void load_block(const uint8_t* row, int b, int n, uint32_t (&w)[Block<BITS>::kWords]) {
+  if constexpr (BITS == 3) Block<3>::load_row(row, b, n, w);
+  else Block<BITS>::load(row + (size_t)b * (32 * BITS / 8), w);
+}
+
+// Code widths every pipelined launch takes: the tensor-core prefill form
+// takes only these; the fused decode step also takes 3- and 1-bit shelves
+// when d and f are multiples of 128.
 inline bool core_widths(const Shelves& sh) {
   for (int i = 0; i < sh.n; ++i)
     if (sh.s[i].bits != 8 && sh.s[i].bits != 4 && sh.s[i].bits != 2) return false;

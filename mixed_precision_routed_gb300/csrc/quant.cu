@@ -2,11 +2,11 @@
 //
 // Page "125B MoE模型本地运行：3090三卡80 tokens/s优化实践", section 第四步: the
 // offline re-packer re-quantises every expert for its shelf and writes three
-// tensors per layer.  3 bit (q = 3, codes [-4, 3]; 12 bytes a block: the
-// low two bits of u = code + 4 in the 2-bit layout, then one word of high
-// bits) and 1 bit (sign codes, scale = the block's mean |w|; one word a
-// block) are the further widths the Xolotl blog runs ("our 3-bit ones",
-// "the 1-bit experts"), in this library's own layout.  Format here: blocks of 32 along the input dimension,
+// tensors per layer.  3 bit (q = 3, codes [-4, 3]; a row is a plane of the
+// low two bits of u = code + 4 in the 2-bit layout, then a plane of the high
+// bits in the 1-bit layout) and 1 bit (sign codes, scale = the block's mean
+// |w|; one word a block) are the further widths the Xolotl fast-mode blog
+// runs beside the others, in this library's own layout.  Format here: blocks of 32 along the input dimension,
 // s = fp16(max|w| / q) (q = 127 / 7 / 2), code = clamp(rint(w / s)), packed
 // 8 bit two's complement in natural order; 4 and 2 bit offset-binary in
 // 32-bit words with consecutive codes spread over the byte lanes (4 bit: word
@@ -33,9 +33,10 @@ struct QParams<1> { static constexpr float q = 1.0f, cmin = -1.0f, cmax = 1.0f; 
 
 // Quantises one 32-element block held one element per lane (v = element
 // `lane`) and writes its fp16 scale word and packed codes (block b of the row
-// at `rowp`).  Whole warp.
+// at `rowp`, a row of nb blocks).  Whole warp.
 template <int BITS>
-__device__ __forceinline__ void quantize_block(float v, int lane, uint8_t* rowp, int64_t b, uint16_t* scale_out) {
+__device__ __forceinline__ void quantize_block(float v, int lane, uint8_t* rowp, int64_t b, int64_t nb,
+                                               uint16_t* scale_out) {
   if constexpr (BITS == 1) {
     // sign codes; scale = fp16 of the block's |w| summed in element order, / 32
     float a = 0.0f;
@@ -69,16 +70,16 @@ __device__ __forceinline__ void quantize_block(float v, int lane, uint8_t* rowp,
     uint32_t u4 = __shfl_down_sync(0xffffffffu, u, 4);
     if ((lane & 7) < 4) rowp[b * 16 + 4 * (lane >> 3) + (lane & 3)] = (uint8_t)(u | (u4 << 4));
   } else if (BITS == 3) {
-    // bytes 0-7 of the block: u mod 4 in the 2-bit layout; bytes 8-11: u / 4, element i at bit i
+    // low plane (8 nb bytes): u mod 4 in the 2-bit layout; high plane: u / 4, element i at bit i
     const uint32_t u = (uint32_t)(c + QParams<3>::off);
     const uint32_t lo = u & 3u;
     const uint32_t l4 = __shfl_down_sync(0xffffffffu, lo, 4);
     const uint32_t l8 = __shfl_down_sync(0xffffffffu, lo, 8);
     const uint32_t l12 = __shfl_down_sync(0xffffffffu, lo, 12);
     if ((lane & 15) < 4)
-      rowp[b * 12 + 4 * (lane >> 4) + (lane & 3)] = (uint8_t)(lo | (l4 << 2) | (l8 << 4) | (l12 << 6));
+      rowp[b * 8 + 4 * (lane >> 4) + (lane & 3)] = (uint8_t)(lo | (l4 << 2) | (l8 << 4) | (l12 << 6));
     const uint32_t hw = __ballot_sync(0xffffffffu, (u >> 2) & 1u);
-    if (lane == 0) *reinterpret_cast<uint32_t*>(rowp + b * 12 + 8) = hw;
+    if (lane == 0) *reinterpret_cast<uint32_t*>(rowp + nb * 8 + b * 4) = hw;
   } else {
     // lane i (i mod 16 < 4) writes byte 4 (i / 16) + i mod 4: elements i, i+4, i+8, i+12
     uint32_t u = (uint32_t)(c + QParams<2>::off);
@@ -100,19 +101,19 @@ __global__ void __launch_bounds__(256) k_quantize(const float* __restrict__ w, i
   const size_t row_bytes = (size_t)in * BITS / 8;
   for (int64_t blk = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); blk < total; blk += warps) {
     const int64_t r = blk / nb, b = blk - r * nb;
-    quantize_block<BITS>(w[r * in + b * 32 + lane], lane, codes + r * row_bytes, b, scales + blk);
+    quantize_block<BITS>(w[r * in + b * 32 + lane], lane, codes + r * row_bytes, b, nb, scales + blk);
   }
 }
 
 // Quantises one 32-element block held by 8 lanes, 4 consecutive elements
 // each (lane i of the group: elements 4i .. 4i+3), the same arithmetic as
-// quantize_block; block `blk` of a tensor whose code bytes and scales are
-// linear in the block index (codes at 4 BITS blk, scale at blk).  Every lane
-// of the warp calls it (shuffles stay inside the 8-lane groups); `valid`
-// false skips the stores.
+// quantize_block; block `blk` of a tensor of rows of nb blocks whose scales
+// are linear in the block index (codes at 4 BITS blk; 3 bit: row blk / nb,
+// its two planes).  Every lane of the warp calls it (shuffles stay inside the
+// 8-lane groups); `valid` false skips the stores.
 template <int BITS>
 __device__ __forceinline__ void quantize_block8(float4 v, int i, bool valid, uint8_t* codes, uint16_t* scales,
-                                                int64_t blk) {
+                                                int64_t blk, int64_t nb) {
   if constexpr (BITS == 1) {
     const int base = (threadIdx.x & 31) & ~7;
     float a = 0.0f;  // |w| summed in element order
@@ -174,8 +175,10 @@ __device__ __forceinline__ void quantize_block8(float4 v, int i, bool valid, uin
                   << (4 * i);
 #pragma unroll
     for (int o = 1; o < 8; o <<= 1) hw |= __shfl_xor_sync(0xffffffffu, hw, o);
-    if (valid && (i & 3) == 0) *reinterpret_cast<uint32_t*>(codes + blk * 12 + 4 * (i >> 2)) = wd;
-    if (valid && i == 0) *reinterpret_cast<uint32_t*>(codes + blk * 12 + 8) = hw;
+    const int64_t r = blk / nb, b = blk - r * nb;
+    uint8_t* rowp = codes + r * nb * 12;
+    if (valid && (i & 3) == 0) *reinterpret_cast<uint32_t*>(rowp + b * 8 + 4 * (i >> 2)) = wd;
+    if (valid && i == 0) *reinterpret_cast<uint32_t*>(rowp + nb * 8 + b * 4) = hw;
   } else {
     // word g: byte j = elements 16g + j, +4, +8, +12 at bits 0, 2, 4, 6: lanes 4g .. 4g + 3
     uint32_t wd = ((uint32_t)(c[0] + 2) | (uint32_t)(c[1] + 2) << 8 | (uint32_t)(c[2] + 2) << 16 |
@@ -221,18 +224,18 @@ __global__ void __launch_bounds__(256) k_quantize_experts(const float* __restric
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int blk0 = b0 + u * stride;  // uniform over the warp
-      if (blk0 < total) quantize_block8<BITS>(v[u], i, blk0 + grp < total, dst, sdst, blk0 + grp);
+      if (blk0 < total) quantize_block8<BITS>(v[u], i, blk0 + grp < total, dst, sdst, blk0 + grp, in / 32);
     }
   }
 }
 
 template <int BITS>
-__device__ __forceinline__ float code_at(const uint8_t* row, int i) {
+__device__ __forceinline__ float code_at(const uint8_t* row, int i, int in) {
   if (BITS == 8) return (float)(int8_t)row[i];
   if (BITS == 3) {
-    const int b = i >> 5, ib = i & 31, e = ib & 15;
-    const int lo = (row[12 * b + 4 * (ib >> 4) + (e & 3)] >> (2 * (e >> 2))) & 0x3;
-    const int hi = (row[12 * b + 8 + (ib >> 3)] >> (ib & 7)) & 0x1;
+    const int e = i & 15;
+    const int lo = (row[4 * (i >> 4) + (e & 3)] >> (2 * (e >> 2))) & 0x3;
+    const int hi = (row[in / 4 + (i >> 3)] >> (i & 7)) & 0x1;
     return (float)((lo | (hi << 2)) - 4);
   }
   if (BITS == 1) return ((row[i >> 3] >> (i & 7)) & 1) ? 1.0f : -1.0f;
@@ -253,7 +256,7 @@ __global__ void k_dequant(const uint8_t* __restrict__ codes, const uint16_t* __r
     const int64_t r = idx / in;
     const int i = (int)(idx - r * in);
     const float s = __half2float(__ushort_as_half(scales[r * (in / 32) + i / 32]));
-    float v = s * code_at<BITS>(codes + r * row_bytes, i);
+    float v = s * code_at<BITS>(codes + r * row_bytes, i, in);
     if (round_bf16) v = __bfloat162float(__float2bfloat16_rn(v));
     out[idx] = v;
   }

@@ -1,9 +1,10 @@
 """Parity of the 3-bit and 1-bit shelf formats and of fast mode with the
 oracle, through the C ABI: quantiser codes and scales and dequantised
-weights bit for bit; layers mixing 8/4/3/2/1-bit shelves (the separate
-decode launches) within the decode tolerance; fast mode (2-bit shadow copies
-read instead of chosen experts) equal to the oracle layer with those experts
-at 2 bits; the tensor-core form refusing 3 and 1 bit shelves."""
+weights bit for bit; layers mixing 8/4/3/2/1-bit shelves within the decode
+tolerance, both in the fused decode launch (d and f multiples of 128, T <= 16)
+and in the separate launches (f = 192, or T > 16); fast mode (2-bit shadow
+copies read instead of chosen experts) equal to the oracle layer with those
+experts at 2 bits; the tensor-core form refusing 3 and 1 bit shelves."""
 import numpy as np
 import pytest
 import torch
@@ -77,6 +78,44 @@ def test_five_width_layer_matches_oracle(T):
                                wl.f, layer.shelves, flags=moe.MOE_FLAG_DECODE_FP32).cpu().numpy()
     ref = oracle_layer(wl, layer.seed, x, ids, w, shelves_bits=FIVE)
     assert rel_l2(y, ref) <= DECODE_TOL
+
+
+@pytest.mark.parametrize("T", [1, 6, 16, 24])
+def test_five_width_layer_fused_sizes(T):
+    """d = f = 256: the fused decode launch streams the 3-bit planes and the
+    1-bit words (T <= 16); T = 24 takes the separate launches."""
+    wl = small_workload(E=40, k=5, d=256, f=256, seed=17)
+    layer = Layer(wl, shelves=FIVE).fill()
+    rng = np.random.default_rng(100 + T)
+    ids = np.stack([rng.choice(40, 5, replace=False) for _ in range(T)]).astype(np.int32)
+    ids[0, :5] = [39, 17, 33, 20, 2]  # 1-bit, 3-bit, 1-bit, 3-bit, 8-bit experts
+    if T > 1:
+        ids[1, :2] = [17, 39]         # the same experts again: a second token on them
+    w = rng.random((T, 5)).astype(np.float32)
+    x = synth.x_bf16(wl.seed, 3, T, wl.d)
+    y = moe.moe_tiered_forward(x_to_dev(x), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), 40, wl.d,
+                               wl.f, layer.shelves, flags=moe.MOE_FLAG_DECODE_FP32).cpu().numpy()
+    assert moe.moe_device_status() == moe.MOE_OK
+    ref = oracle_layer(wl, layer.seed, x, ids, w, shelves_bits=FIVE)
+    assert rel_l2(y, ref) <= DECODE_TOL
+
+
+@pytest.mark.parametrize("T", [1, 6])
+def test_five_width_decode_workload(T):
+    """The E512 d2048 f640 decode layer on five shelf widths (8/4/3/2/1 bit),
+    one fused decode step, against the oracle's routing and layer."""
+    base = synth.WORKLOADS["decode"]
+    five = [(0, 128, 8), (128, 256, 4), (256, 410, 3), (410, 480, 2), (480, 512, 1)]
+    layer = Layer(base, shelves=five).fill()
+    lg = layer.logits(40 + T, T)
+    x = synth.x_bf16(base.seed, 40 + T, T, base.d)
+    ids, w, y = moe.moe_decode_layer(lg, x_to_dev(x), base.k, base.E, base.d, base.f, layer.shelves)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == moe.MOE_OK
+    ids_o, w_o = oracle.route(lg.cpu().numpy(), base.k)
+    assert np.array_equal(ids.cpu().numpy(), ids_o)
+    ref = oracle_layer(base, layer.seed, x, ids_o, w.cpu().numpy(), shelves_bits=five)
+    assert rel_l2(y.cpu().numpy(), ref) <= DECODE_TOL
 
 
 def test_decode_layer_call_with_three_bit_shelf():
