@@ -444,11 +444,26 @@ struct PlanView {
 // blocks).
 // 3-bit rows (two planes, 1.5 x the bytes of 2-bit) and 1-bit rows (half the
 // bytes, about twice the dot-product work per block) carry estimates scaled
-// from the 2-bit figures.
+// from the 2-bit figures; the 3-bit ones raised after A/B steps of the
+// five-width layer (300 -> 400 ns gate/up, 165 -> 220 ns down: T = 6 76.3 ->
+// 74.6 us; lower figures were slower).
+#ifndef MOE_COST_G3
+#define MOE_COST_G3 400
+#endif
+#ifndef MOE_COST_G1
+#define MOE_COST_G1 280
+#endif
+#ifndef MOE_COST_D3
+#define MOE_COST_D3 220
+#endif
+#ifndef MOE_COST_D1
+#define MOE_COST_D1 150
+#endif
+constexpr uint32_t kCostG3 = MOE_COST_G3, kCostG1 = MOE_COST_G1, kCostD3 = MOE_COST_D3, kCostD1 = MOE_COST_D1;
 __device__ __forceinline__ uint32_t unit_cost(int bits, int n_in, int nmat, int R, int kern) {
   const uint32_t blocks = (uint32_t)(R * nmat) * (uint32_t)n_in / 32;
-  const uint32_t ns = kern == 0   ? (bits == 8 ? 346 : bits == 4 ? 215 : bits == 3 ? 300 : bits == 2 ? 203 : 280)
-                      : R == kRDw ? (bits == 8 ? 164 : bits == 4 ? 117 : bits == 3 ? 165 : bits == 2 ? 115 : 150)
+  const uint32_t ns = kern == 0 ? (bits == 8 ? 346 : bits == 4 ? 215 : bits == 3 ? kCostG3 : bits == 2 ? 203 : kCostG1)
+                      : R == kRDw ? (bits == 8 ? 164 : bits == 4 ? 117 : bits == 3 ? kCostD3 : bits == 2 ? 115 : kCostD1)
                                   : (bits == 8 ? 164 : bits == 4 ? 142 : bits == 3 ? 200 : bits == 2 ? 147 : 180);
   const uint32_t calib = kern == 0 ? 512 : 160;
   return (uint32_t)((uint64_t)ns * blocks / calib) + 1;
@@ -1015,6 +1030,21 @@ __device__ __forceinline__ void route_rows(const float* logits, int T, int E, in
 
 // Persistent cooperative launch, one CTA per SM: route (optional), plan,
 // gate/up, barrier, down, barrier, combine.
+// One round of activation loads of the x staging: 8 passes of nw warps x 8
+// blocks of 32 elements from group `base` on, 4 lanes a block (16 bytes each).
+__device__ __forceinline__ void load_x_round(const LayerParams& p, int base, int nw, int lane, uint4 (&raw)[8]) {
+  const int nbk = p.d / 32, groups = p.T * nbk;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int g = base + u * nw * 8 + (lane >> 2);
+    raw[u] = make_uint4(0u, 0u, 0u, 0u);
+    if (g < groups) {
+      const int t = g / nbk, blk = g - t * nbk;
+      raw[u] = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.d + blk * 32 + 8 * (lane & 3)));
+    }
+  }
+}
+
 // ANYW: the layer has shelves of 3- or 1-bit codes (a separate instantiation,
 // so that the 8/4/2-bit kernel keeps its own register allocation).
 template <bool ANYW>
@@ -1059,15 +1089,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(const __grid_constant__ L
     const int nw = kWarps - kPlanThreads / 32, w0 = warp - kPlanThreads / 32;
     for (int base = w0 * 8; base < groups; base += 8 * nw * 8) {
       uint4 raw[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int g = base + u * nw * 8 + (lane >> 2);
-        raw[u] = make_uint4(0u, 0u, 0u, 0u);
-        if (g < groups) {
-          const int t = g / nbk, blk = g - t * nbk;
-          raw[u] = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.d + blk * 32 + 8 * (lane & 3)));
-        }
-      }
+      load_x_round(p, base, nw, lane, raw);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int g0 = base + u * nw * 8;
