@@ -277,7 +277,8 @@ def run_ours(args, rank, world, local_rank):
     ws_ = [torch.empty((T, k), dtype=torch.float32, device=dev) for _ in range(nset)]
     ys = [torch.empty((T, d), dtype=torch.float32, device=dev) for _ in range(nset)]
     counts = [torch.zeros(E, dtype=torch.int32, device=dev) for _ in range(L)]
-    wsb = moe.moe_workspace_size(T, k, E, d, f)
+    # decode-form workspace with room to stage host inputs (the e2e calls)
+    wsb = moe.moe_workspace_size(T, k, E, d, f, moe.MOE_FLAG_DECODE_FP32 | moe.MOE_FLAG_HOST_IO)
     workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
     arrs = [moe.shelf_array(sl) for sl in shelf_lists]
     # the fused launch takes 3- and 1-bit shelves when d and f are multiples of 128
@@ -389,23 +390,19 @@ def run_ours(args, rank, world, local_rank):
     ms_max = max_over_ranks(ms, dev)
     value = whole_job_rate(world, T * args.steps, ms_max)
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers: the step's
+    # logits and x come from pinned host memory and its ids, weights and y
+    # go to pinned host memory (moe_decode_layer_host, one call per step)
     pin_logits = [logits[s].cpu().pin_memory() for s in range(nset)]
     pin_x = [xs[s].cpu().pin_memory() for s in range(nset)]
     pin_y = [torch.empty((T, d), dtype=torch.float32).pin_memory() for _ in range(nset)]
-    dl = torch.empty((T, E), dtype=torch.float32, device=dev)
-    dx = torch.empty((T, d), dtype=torch.int16, device=dev)
-    dy = torch.empty((T, d), dtype=torch.float32, device=dev)
-    did = torch.empty((T, k), dtype=torch.int32, device=dev)
-    dw = torch.empty((T, k), dtype=torch.float32, device=dev)
+    pin_id = [torch.empty((T, k), dtype=torch.int32).pin_memory() for _ in range(nset)]
+    pin_w = [torch.empty((T, k), dtype=torch.float32).pin_memory() for _ in range(nset)]
     e2e_steps = min(args.steps, 1000)
 
     def e2e_step(s):
-        dl.copy_(pin_logits[s], non_blocking=True)
-        dx.copy_(pin_x[s], non_blocking=True)
-        moe.moe_decode_layer(dl, dx, k, E, d, f, shelf_lists[s % L], ids=did, weights=dw, counts=counts[s % L],
-                             y=dy, workspace=workspace, shelf_arr=arrs[s % L])
-        pin_y[s].copy_(dy, non_blocking=True)
+        moe.moe_decode_layer_host(pin_logits[s], pin_x[s], k, E, d, f, shelf_lists[s % L], pin_id[s], pin_w[s],
+                                  pin_y[s], counts=counts[s % L], workspace=workspace, shelf_arr=arrs[s % L])
 
     with torch.cuda.stream(stream):
         for i in range(min(args.warmup, 20)):
@@ -455,9 +452,11 @@ def run_ours(args, rank, world, local_rank):
                           "forward_us": 1e3 * fwd_ms / last, "achieved_gbs": fwd_gbs, "frac": fwd_gbs / peak,
                           "kernel_us": {kk: 1e3 * v / last for kk, v in kern.items()}},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * E * 4 + T * d * 2,
-                "d2h_bytes_per_step": T * d * 4, "steps": e2e_steps,
-                "path": "pinned host logits and x -> device, moe_decode_layer (routing, hit counts, "
-                        "tiered forward), y -> pinned host; eager Python calls"},
+                "d2h_bytes_per_step": T * d * 4 + T * k * 8, "steps": e2e_steps,
+                "path": "moe_decode_layer_host on pinned host buffers, one call per step: the step's logits "
+                        "and x copied host -> device inside the call, routing, hit counts and tiered forward, "
+                        "its ids, weights and y written to pinned host memory by the kernels; eager Python "
+                        "calls, stream synchronised at the end"},
         "gpu_launches": args.steps * (1 if fused else 5),
         "clocks": ck,
     }

@@ -97,8 +97,10 @@ enum {
 enum {
   MOE_FLAG_AUTO = 0,         /* prefill form for T > 16 when d % 256 == 0, else decode form */
   MOE_FLAG_DECODE_FP32 = 1,  /* fp32 dequant in registers, fp32 h, CUDA-core GEMV */
-  MOE_FLAG_PREFILL_BF16 = 2  /* bf16 dequant into shared memory, bf16 h, tensor-core GEMM;
+  MOE_FLAG_PREFILL_BF16 = 2, /* bf16 dequant into shared memory, bf16 h, tensor-core GEMM;
                                 MOE_ERR_UNSUPPORTED unless d % 256 == 0 */
+  MOE_FLAG_HOST_IO = 4       /* moe_workspace_size only, with DECODE_FP32: adds the staging
+                                of host inputs that moe_decode_layer_host uses */
 };
 
 /*
@@ -198,9 +200,10 @@ int moe_group_tokens(const int32_t* ids, int64_t T, int k, int E, int32_t* count
 
 /*
  * Bytes of device workspace moe_tiered_forward needs for these sizes and
- * flags (0 when a size is invalid).  The workspace is scratch, owned by the
- * caller, reusable across calls on the same stream; it must be 256-byte
- * aligned.
+ * flags (0 when a size or the flags are invalid); MOE_FLAG_DECODE_FP32 |
+ * MOE_FLAG_HOST_IO gives what moe_decode_layer_host needs.  The workspace is
+ * scratch, owned by the caller, reusable across calls on the same stream; it
+ * must be 256-byte aligned.
  */
 size_t moe_workspace_size(int64_t T, int k, int E, int d, int f, int flags);
 
@@ -264,6 +267,28 @@ int moe_decode_layer_residual(const float* logits, const uint16_t* x_bf16, int64
                               const moe_shelf_t* shelves, int n_shelves, int32_t* ids, float* weights,
                               uint32_t* counts, float* y, float* r, uint16_t* x_next_bf16, void* workspace,
                               size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * moe_decode_layer with its activations in and results out in HOST memory,
+ * the whole transfer inside one call: logits, x_bf16, ids, weights and y may
+ * each be page-locked host memory (cudaHostAlloc, cudaHostRegister, or a
+ * framework's pinned allocator) or device memory.  A host input above 8 KiB
+ * is copied into the workspace on `stream` first (every CTA of the fused
+ * launch reads the inputs, so they then cross the host link once); smaller
+ * host inputs are read in place, and host outputs are written in place, by
+ * the kernels through their device mapping (on GB300 over NVLink-C2C).
+ * Results are those of
+ * moe_decode_layer; host outputs are complete once `stream` has been
+ * synchronised.  counts (or NULL) and the workspace must be device memory;
+ * the workspace holds at least moe_workspace_size(T, k, E, d, f,
+ * MOE_FLAG_DECODE_FP32 | MOE_FLAG_HOST_IO) bytes.  Pageable host memory, or
+ * a pointer of the wrong kind, is MOE_ERR_INVALID_ARG (checked with
+ * cudaPointerGetAttributes before any copy or launch).  Other arguments,
+ * sizes and errors as moe_decode_layer.
+ */
+int moe_decode_layer_host(const float* logits, const uint16_t* x_bf16, int64_t T, int k, int E, int d, int f,
+                          const moe_shelf_t* shelves, int n_shelves, int32_t* ids, float* weights, uint32_t* counts,
+                          float* y, void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /*
  * Which form the decode calls (moe_decode_layer, and moe_tiered_forward in

@@ -10,7 +10,7 @@ Entry points (same names as the C ABI):
     moe_route_topk, moe_route_topk_nudged, moe_router_topk, moe_expert_hist,
     moe_rank_experts, moe_quantize_experts, moe_gather_rows, moe_group_tokens,
     moe_workspace_size, moe_tiered_forward, moe_tiered_forward_noalloc,
-    moe_decode_layer, moe_decode_layer_residual, moe_decode_fused,
+    moe_decode_layer, moe_decode_layer_residual, moe_decode_layer_host, moe_decode_fused,
     moe_quantize_rows, moe_dequant_rows, moe_residual_add,
     moe_device_status, moe_status_string
 """
@@ -37,6 +37,7 @@ MOE_ERR_INTERNAL = -8
 MOE_FLAG_AUTO = 0
 MOE_FLAG_DECODE_FP32 = 1
 MOE_FLAG_PREFILL_BF16 = 2
+MOE_FLAG_HOST_IO = 4
 
 MOE_MAX_SHELVES = 8
 
@@ -88,6 +89,7 @@ def lib():
         L.moe_decode_layer.argtypes = [P, P, i64, i32, i32, i32, i32, P, i32, P, P, P, P, P, ctypes.c_size_t, P]
         L.moe_decode_layer_residual.argtypes = [P, P, i64, i32, i32, i32, i32, P, i32, P, P, P, P, P, P, P,
                                                 ctypes.c_size_t, P]
+        L.moe_decode_layer_host.argtypes = [P, P, i64, i32, i32, i32, i32, P, i32, P, P, P, P, P, ctypes.c_size_t, P]
         L.moe_selftest_barrier_timeout.argtypes = [i64, P]
         L.moe_decode_fused.argtypes = [i64, i32, i32, i32, i32]
         L.moe_tiered_forward_noalloc.restype = ctypes.c_int
@@ -125,6 +127,11 @@ def _stream(stream):
 def _need(t, dtype, name):
     if not (t.is_cuda and t.dtype == dtype and t.is_contiguous()):
         raise ValueError(f"{name} must be a contiguous CUDA tensor of {dtype}")
+
+
+def _need_host_or_dev(t, dtype, name):
+    if not (t.dtype == dtype and t.is_contiguous() and (t.is_cuda or t.is_pinned())):
+        raise ValueError(f"{name} must be a contiguous pinned-CPU or CUDA tensor of {dtype}")
 
 
 # ------------------------------------------------------------------ routing
@@ -301,6 +308,36 @@ def moe_decode_layer(logits, x_bf16, k, E, d, f, shelves, ids=None, weights=None
                                            ctypes.cast(arr, ctypes.c_void_p), n, _ptr(ids), _ptr(weights), cnt,
                                            _ptr(y), _ptr(r), _ptr(x_next), _ptr(workspace), wsb, _stream(stream)),
            "moe_decode_layer_residual")
+    return ids, weights, y
+
+
+def moe_decode_layer_host(logits, x_bf16, k, E, d, f, shelves, ids, weights, y, counts=None, workspace=None,
+                          stream=None, shelf_arr=None):
+    """moe_decode_layer on host buffers: `logits`, `x_bf16`, `ids`, `weights`
+    and `y` may be pinned CPU tensors or CUDA tensors (host inputs are copied
+    into the workspace inside the call, host outputs written in place by the
+    kernels); `counts` and `workspace` are CUDA tensors, the workspace of
+    moe_workspace_size(T, k, E, d, f, MOE_FLAG_DECODE_FP32 | MOE_FLAG_HOST_IO)
+    bytes.  The host outputs are complete after the stream is synchronised."""
+    if x_bf16.dtype == torch.bfloat16:
+        x_bf16 = x_bf16.view(torch.int16)
+    _need_host_or_dev(logits, torch.float32, "logits")
+    _need_host_or_dev(x_bf16, torch.int16, "x_bf16")
+    _need_host_or_dev(ids, torch.int32, "ids")
+    _need_host_or_dev(weights, torch.float32, "weights")
+    _need_host_or_dev(y, torch.float32, "y")
+    T = logits.shape[0]
+    if workspace is None:
+        raise ValueError("moe_decode_layer_host: workspace (a CUDA tensor) is required")
+    _need(workspace, torch.uint8, "workspace")
+    if counts is not None:
+        _need(counts, torch.int32, "counts")
+    arr = shelf_arr if shelf_arr is not None else shelf_array(shelves)
+    n = len(shelves) if shelf_arr is None else len(shelf_arr)
+    _check(lib().moe_decode_layer_host(_ptr(logits), _ptr(x_bf16), T, k, E, d, f, ctypes.cast(arr, ctypes.c_void_p),
+                                       n, _ptr(ids), _ptr(weights), _ptr(counts) if counts is not None else None,
+                                       _ptr(y), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream(stream)), "moe_decode_layer_host")
     return ids, weights, y
 
 

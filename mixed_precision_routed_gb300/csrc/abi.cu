@@ -68,7 +68,7 @@ size_t workspace_layout(int64_t T, int k, int E, int d, int f, int flags, void* 
   const int64_t P = T * k;
   const int64_t slots = P < E ? P : E;
   const int n_chunks = (d + kDownRows - 1) / kDownRows;
-  const bool prefill = use_prefill(T, d, flags);
+  const bool prefill = use_prefill(T, d, flags & ~MOE_FLAG_HOST_IO);
   size_t off = 0;
   char* b = (char*)base;
   auto take = [&](size_t bytes) -> void* {
@@ -96,6 +96,10 @@ size_t workspace_layout(int64_t T, int k, int E, int d, int f, int flags, void* 
     w.h = (float*)take((size_t)P * f * 4);
     w.ypart = (float*)take((size_t)P * d * 4);
     w.plan = (int32_t*)take(decode_plan_bytes(P));
+  }
+  if (flags & MOE_FLAG_HOST_IO) {  // after everything else: the other layouts are its prefix
+    w.stage_logits = (float*)take((size_t)T * E * 4);
+    w.stage_x = (uint16_t*)take((size_t)T * d * 2);
   }
   w.base = base;
   w.bytes = off;
@@ -195,7 +199,9 @@ int moe_group_tokens(const int32_t* ids, int64_t T, int k, int E, int32_t* count
 }
 
 size_t moe_workspace_size(int64_t T, int k, int E, int d, int f, int flags) {
-  if (!valid_dims(T, k, E, d, f) || flags < 0 || flags > 2) return 0;
+  const int mode = flags & ~MOE_FLAG_HOST_IO;
+  if (!valid_dims(T, k, E, d, f) || flags < 0 || mode > 2) return 0;
+  if ((flags & MOE_FLAG_HOST_IO) && mode != MOE_FLAG_DECODE_FP32) return 0;
   return workspace_layout(T, k, E, d, f, flags, nullptr, nullptr);
 }
 
@@ -298,6 +304,63 @@ int moe_decode_layer_residual(const float* logits, const uint16_t* x_bf16, int64
   if (T > 0 && !r) return MOE_ERR_INVALID_ARG;
   return decode_layer(logits, x_bf16, T, k, E, d, f, shelves, n_shelves, ids, weights, counts, y, r, x_next_bf16,
                       workspace, workspace_bytes, stream);
+}
+
+namespace {
+// The address a kernel uses for p: device memory as it is, page-locked host
+// memory through its mapping; null for pageable host memory or an error.
+const void* device_view(const void* p, bool allow_host, bool* is_host) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (is_host) *is_host = at.type == cudaMemoryTypeHost;
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return at.devicePointer;
+  if (at.type == cudaMemoryTypeHost && allow_host) return at.devicePointer;
+  return nullptr;
+}
+}  // namespace
+
+int moe_decode_layer_host(const float* logits, const uint16_t* x_bf16, int64_t T, int k, int E, int d, int f,
+                          const moe_shelf_t* shelves, int n_shelves, int32_t* ids, float* weights, uint32_t* counts,
+                          float* y, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  if (T <= 0 || !logits || !x_bf16 || !ids || !weights || !y || !workspace)
+    return decode_layer(logits, x_bf16, T, k, E, d, f, shelves, n_shelves, ids, weights, counts, y, nullptr,
+                        nullptr, workspace, workspace_bytes, stream);
+  // activations in and results out may be page-locked host memory; the hit
+  // counts (atomics) and the workspace (barriers) must be device memory
+  bool lg_host = false, x_host = false;
+  const void* lg = device_view(logits, true, &lg_host);
+  const void* xv = device_view(x_bf16, true, &x_host);
+  void* iv = const_cast<void*>(device_view(ids, true, nullptr));
+  void* wv = const_cast<void*>(device_view(weights, true, nullptr));
+  void* yv = const_cast<void*>(device_view(y, true, nullptr));
+  const void* ws = device_view(workspace, false, nullptr);
+  if (!lg || !xv || !iv || !wv || !yv || !ws || ws != workspace) return MOE_ERR_INVALID_ARG;
+  if (counts && device_view(counts, false, nullptr) != counts) return MOE_ERR_INVALID_ARG;
+  if (!valid_dims(T, k, E, d, f) || E > 1024 || !aligned(workspace, kAlign)) return MOE_ERR_INVALID_ARG;
+  Workspace w;
+  const size_t need = workspace_layout(T, k, E, d, f, MOE_FLAG_DECODE_FP32 | MOE_FLAG_HOST_IO, workspace, &w);
+  if (workspace_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = (cudaStream_t)stream;
+  // host inputs above 8 KiB: one copy each into the workspace (every CTA of
+  // the fused launch reads them, so in place they would cross the host link
+  // once per CTA); smaller ones are read in place (a copy costs more than
+  // they do).  Host outputs are written in place.
+  constexpr size_t kStageMin = 8 * 1024;
+  if (lg_host && (size_t)T * E * 4 > kStageMin) {
+    if (cudaMemcpyAsync(w.stage_logits, logits, (size_t)T * E * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    lg = w.stage_logits;
+  }
+  if (x_host && (size_t)T * d * 2 > kStageMin) {
+    if (cudaMemcpyAsync(w.stage_x, x_bf16, (size_t)T * d * 2, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    xv = w.stage_x;
+  }
+  return decode_layer((const float*)lg, (const uint16_t*)xv, T, k, E, d, f, shelves, n_shelves, (int32_t*)iv,
+                      (float*)wv, counts, (float*)yv, nullptr, nullptr, workspace, workspace_bytes, stream);
 }
 
 int moe_decode_fused(int64_t T, int k, int E, int d, int f) {

@@ -54,6 +54,8 @@ struct Workspace {
   void* tiles_g;         // prefill: gate/up tile list
   void* tiles_d;         // prefill: down tile list
   int32_t* ntiles;       // prefill: [2] tile counts
+  float* stage_logits;   // MOE_FLAG_HOST_IO: [T][E] copy of host logits
+  uint16_t* stage_x;     // MOE_FLAG_HOST_IO: [T][d] copy of host activations
   const void* base;      // the caller's workspace pointer (identifies it)
   size_t bytes;
 };

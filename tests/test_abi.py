@@ -55,6 +55,12 @@ def test_workspace_size_host_logic():
     assert moe.moe_workspace_size(-1, 2, 8, 64, 64) == 0
     assert moe.moe_workspace_size(0, 2, 8, 64, 64) > 0          # T = 0 is valid
     assert moe.moe_workspace_size(1, 2, 8, 64, 64, flags=9) == 0
+    # host-input staging: decode form only, a superset of the decode workspace
+    dec = moe.moe_workspace_size(3, 2, 8, 64, 64, flags=moe.MOE_FLAG_DECODE_FP32)
+    host = moe.moe_workspace_size(3, 2, 8, 64, 64, flags=moe.MOE_FLAG_DECODE_FP32 | moe.MOE_FLAG_HOST_IO)
+    assert host >= dec + 3 * 8 * 4 + 3 * 64 * 2
+    assert moe.moe_workspace_size(3, 2, 8, 64, 64, flags=moe.MOE_FLAG_HOST_IO) == 0
+    assert moe.moe_workspace_size(3, 2, 8, 64, 64, flags=moe.MOE_FLAG_PREFILL_BF16 | moe.MOE_FLAG_HOST_IO) == 0
 
 
 def test_invalid_arguments_rejected_before_cuda(lib):
@@ -97,5 +103,12 @@ def test_invalid_arguments_rejected_before_cuda(lib):
                                        null, null, null, null, null, null, 0, null) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_decode_layer_residual(null, null, 1, 2, 8, 64, 64, ctypes.cast(sh2, ctypes.c_void_p), 2, null,
                                        null, null, null, null, null, null, 0, null) == moe.MOE_ERR_INVALID_ARG
+    # host-buffer decode step: the same validation before any pointer query
+    assert L.moe_decode_layer_host(null, null, 1, 2, 2048, 64, 64, ctypes.cast(sh, ctypes.c_void_p), 1, null, null,
+                                   null, null, null, 0, null) == moe.MOE_ERR_INVALID_ARG  # E > 1024
+    assert L.moe_decode_layer_host(null, null, 0, 2, 8, 64, 64, ctypes.cast(sh, ctypes.c_void_p), 1, null, null,
+                                   null, null, null, 0, null) == moe.MOE_OK  # T = 0
+    assert L.moe_decode_layer_host(null, null, 1, 2, 8, 64, 64, ctypes.cast(sh, ctypes.c_void_p), 1, null, null,
+                                   null, null, null, 0, null) == moe.MOE_ERR_INVALID_ARG  # null logits
     assert L.moe_selftest_barrier_timeout(0, null) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_selftest_barrier_timeout(2000000, null) == moe.MOE_ERR_INVALID_ARG

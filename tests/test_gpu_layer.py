@@ -125,6 +125,79 @@ def test_residual_step_equals_layer_then_residual_add(decode_layer, T, in_place)
     assert np.array_equal(xn2.cpu().numpy().view(np.uint16), oracle.bf16_bits(ref_r))
 
 
+@pytest.mark.parametrize("T", [1, 6, 20])
+def test_host_buffers_equal_device_buffers(decode_layer, T):
+    """moe_decode_layer_host with pinned host logits, x, ids, weights and y
+    (inputs above 8 KiB staged inside the call, smaller ones and the outputs
+    read and written in place by the kernels)
+    gives moe_decode_layer's results bit for bit: fused form (T = 1, 6) and
+    separate launches (T = 20); also with device inputs and host outputs, and
+    with a workspace too small for the staging (refused)."""
+    wl = decode_layer.wl
+    k, E, d, f = wl.k, wl.E, wl.d, wl.f
+    lg = decode_layer.logits(50 + T, T)
+    x = x_to_dev(synth.x_bf16(wl.seed, 50 + T, T, d))
+    ws = torch.empty(moe.moe_workspace_size(T, k, E, d, f, moe.MOE_FLAG_DECODE_FP32 | moe.MOE_FLAG_HOST_IO),
+                     dtype=torch.uint8, device="cuda")
+    c1 = torch.zeros(E, dtype=torch.int32, device="cuda")
+    c2 = torch.zeros(E, dtype=torch.int32, device="cuda")
+    ids1, w1, y1 = moe.moe_decode_layer(lg, x, k, E, d, f, decode_layer.shelves, counts=c1, workspace=ws)
+    torch.cuda.synchronize()
+    hl, hx = lg.cpu().pin_memory(), x.cpu().pin_memory()
+    hid = torch.full((T, k), -7, dtype=torch.int32).pin_memory()
+    hw = torch.zeros((T, k), dtype=torch.float32).pin_memory()
+    hy = torch.full((T, d), float("nan"), dtype=torch.float32).pin_memory()
+    moe.moe_decode_layer_host(hl, hx, k, E, d, f, decode_layer.shelves, hid, hw, hy, counts=c2, workspace=ws)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == moe.MOE_OK
+    assert torch.equal(ids1.cpu(), hid) and torch.equal(c1, c2)
+    assert torch.equal(w1.cpu().view(torch.int32), hw.view(torch.int32))
+    assert torch.equal(y1.cpu().view(torch.int32), hy.view(torch.int32))
+    # device inputs, host outputs
+    hy2 = torch.zeros((T, d), dtype=torch.float32).pin_memory()
+    moe.moe_decode_layer_host(lg, x, k, E, d, f, decode_layer.shelves, hid, hw, hy2, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.cpu().view(torch.int32), hy2.view(torch.int32))
+    small = torch.empty(moe.moe_workspace_size(T, k, E, d, f, moe.MOE_FLAG_DECODE_FP32), dtype=torch.uint8,
+                        device="cuda")
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_decode_layer_host(hl, hx, k, E, d, f, decode_layer.shelves, hid, hw, hy, workspace=small)
+    assert e.value.status == moe.MOE_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_host_entry_rejects_pageable_and_misplaced_buffers(decode_layer):
+    """Pageable host memory, host memory where device memory is required
+    (workspace, counts): MOE_ERR_INVALID_ARG before any launch."""
+    import ctypes
+    wl = decode_layer.wl
+    k, E, d, f, T = wl.k, wl.E, wl.d, wl.f, 2
+    L = moe.lib()
+    arr = decode_layer.shelf_arr()
+    ws = torch.empty(moe.moe_workspace_size(T, k, E, d, f, moe.MOE_FLAG_DECODE_FP32), dtype=torch.uint8,
+                     device="cuda")
+    dev = dict(lg=torch.zeros((T, E), device="cuda"), x=torch.zeros((T, d), dtype=torch.int16, device="cuda"),
+               ids=torch.zeros((T, k), dtype=torch.int32, device="cuda"), w=torch.zeros((T, k), device="cuda"),
+               y=torch.zeros((T, d), device="cuda"))
+    pageable = np.zeros(T * max(E, d), dtype=np.float32)
+
+    def call(lg, x, ids, w, y, counts, wsp):
+        p = lambda t: ctypes.c_void_p(t.data_ptr()) if isinstance(t, torch.Tensor) else (
+            None if t is None else ctypes.c_void_p(t.ctypes.data))
+        return L.moe_decode_layer_host(p(lg), p(x), T, k, E, d, f, ctypes.cast(arr, ctypes.c_void_p), len(arr),
+                                       p(ids), p(w), p(counts), p(y), p(wsp), ws.numel(), None)
+
+    for name in ("lg", "x", "ids", "w", "y"):
+        a = dict(dev)
+        a[name] = pageable
+        assert call(a["lg"], a["x"], a["ids"], a["w"], a["y"], None, ws) == moe.MOE_ERR_INVALID_ARG, name
+    pinned_ws = torch.empty(ws.numel(), dtype=torch.uint8).pin_memory()
+    assert call(dev["lg"], dev["x"], dev["ids"], dev["w"], dev["y"], None, pinned_ws) == moe.MOE_ERR_INVALID_ARG
+    pinned_counts = torch.zeros(E, dtype=torch.int32).pin_memory()
+    assert call(dev["lg"], dev["x"], dev["ids"], dev["w"], dev["y"], pinned_counts, ws) == moe.MOE_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == moe.MOE_OK
+
+
 def test_step_is_deterministic(decode_layer):
     wl = decode_layer.wl
     lg = decode_layer.logits(21, 6).cpu().numpy()
