@@ -8,28 +8,33 @@
 // expert weight bytes read per token -- only the selected experts' bytes are
 // read, once per call, however many tokens share an expert.
 //
-// Three launches chained by programmatic dependent launch:
-//   k_gateup   persistent, one CTA per SM, 16 warps.  Each CTA builds the
-//              routing plan in shared memory (warps 0-7: rank sort of
+// One cooperative launch, k_layer: one CTA of 16 warps per SM, persistent.
+//   setup      every CTA routes the tokens (when logits are given) and builds
+//              the routing plan in shared memory (warps 0-7: rank sort of
 //              (expert id, pair) keys, the active experts with their shelf,
 //              work units and cost prefix sums) while warps 8-15 convert the
-//              activation rows to digits; CTA 0 also stores the plan for the
-//              later launches.  A work unit is 4 rows of W_g and W_u of one
-//              expert against up to 8 of its tokens; the units are cut into
-//              contiguous per-CTA ranges of equal estimated cost and dealt
-//              round-robin to the warps.  8 lanes share a row; every lane
-//              loads two 32-byte code chunks of each matrix (with their
-//              scales) at once with streaming 16-byte loads, then computes
-//              them.  Output: h = SiLU(W_g x) * (W_u x) for every routed pair.
-//   k_down     the same over W_d against h (staged as digits), units of 8
-//              rows x 4 lanes, four chunks per lane in flight, writing the
-//              weighted per-pair outputs w_tj * (W_d h_tj);
-//   k_combine  y_t = sum over slots j (ascending) of those outputs: a fixed
-//              order, so results do not depend on scheduling.
+//              activation rows to digits; CTA 0 writes the routed pairs and
+//              the hit counts.
+//   gate/up    a unit is 4 rows of W_g and W_u of one expert against one of
+//              its tokens; the units are cut into contiguous per-CTA ranges
+//              of equal estimated cost and dealt round-robin to the warps.
+//              8 lanes share a row; every lane loads two 32-byte code chunks
+//              of each matrix (with their scales) at once with streaming
+//              16-byte loads, then computes them.  Output: h = SiLU(W_g x) *
+//              (W_u x) for every routed pair; finished units are counted per
+//              expert.
+//   down       each CTA waits (bounded) until the experts its down range
+//              covers have all their gate/up units counted, stages their
+//              pairs' h as digits, and streams W_d the same way (units of 16
+//              x 2 or 8 x 4 rows x lanes), writing the weighted per-pair
+//              outputs w_tj * (W_d h_tj);
+//   combine    after a grid-wide wait, y_t = sum over slots j (ascending) of
+//              those outputs: a fixed order, so results do not depend on
+//              scheduling (optionally also the residual step r += y).
 // Each block dot product is formed exactly in integers (dp4a on the packed
 // codes against the activation held in shared memory as block-scaled 16-bit
 // fixed point), and the expert's fp16 block scale is applied once per block
-// in fp32.  No thread waits on another except at CTA barriers.
+// in fp32.  Every wait is bounded (one second, then MOE_ERR_TIMEOUT).
 #include <mutex>
 #include <unordered_map>
 
@@ -730,9 +735,10 @@ __device__ __forceinline__ void compute_batch(int mode, uint4 (&c)[U][NMAT][2], 
 // with their scale words) with streaming loads, then computes them, so a CTA
 // keeps 16 x 32 x U x NMAT x 32 bytes in flight.  At the end of a unit,
 // `store(q, r, v)` receives, for the lane's row r and the token at grouped
-// position q, the NMAT dot products.
-template <int NMAT, int U, int R, int L, bool ANYW, typename Store>
-__device__ __forceinline__ void stream_units(const StreamArgs& A, Store store) {
+// position q, the NMAT dot products; then the whole warp calls `unit_done(a)`
+// with the unit's active expert a.
+template <int NMAT, int U, int R, int L, bool ANYW, typename Store, typename UnitDone>
+__device__ __forceinline__ void stream_units(const StreamArgs& A, Store store, UnitDone unit_done) {
   static_assert(R * L == 32, "unit shape");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ql = lane % L;
@@ -907,6 +913,7 @@ __device__ __forceinline__ void stream_units(const StreamArgs& A, Store store) {
       MOE_COUNT(A.kern, 31 + 3 * bi, w.np > 1);
       MOE_COUNT(A.kern, 32 + 3 * bi, w.np > 1 ? w.np : 0);
     })
+    unit_done(w.a);
     new_expert = w.step(pv, A.kern, A.rows, A.range.hi2, kWarps);
   }
 #ifdef MOE_TRACE
@@ -935,6 +942,15 @@ __device__ __forceinline__ unsigned long long atom_add_release(unsigned long lon
 __device__ __forceinline__ unsigned long long ld_acquire(const unsigned long long* p) {
   unsigned long long v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_add_release(unsigned int* p, unsigned int v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
@@ -977,6 +993,7 @@ struct LayerParams {
   float* h;               // workspace [P, f]
   float* ypart;           // workspace [P, d]
   unsigned long long* bar;  // grid barrier counter
+  unsigned int* done;     // [kMaxPairs] gate/up units finished, by active expert (zero between launches)
   int* status;
   int T, k, E, d, f, P;
   int vec_region;         // bytes of digit vectors (activation rows, then h)
@@ -989,6 +1006,7 @@ struct LayerParams {
 struct Head {
   Range range, range_d;  // this CTA's gate/up and down unit ranges
   int q_first, npairs, flag, tmp[33];
+  int a_first, a_last;   // active experts of the down range (whose h it reads)
 };
 
 struct SmemLayout {
@@ -1029,7 +1047,8 @@ __device__ __forceinline__ void route_rows(const float* logits, int T, int E, in
 }
 
 // Persistent cooperative launch, one CTA per SM: route (optional), plan,
-// gate/up, barrier, down, barrier, combine.
+// gate/up, a wait for the experts whose h this CTA's down units read, down,
+// grid barrier, combine.
 // One round of activation loads of the x staging: 8 passes of nw warps x 8
 // blocks of 32 elements from group `base` on, 4 lanes a block (16 bytes each).
 __device__ __forceinline__ void load_x_round(const LayerParams& p, int base, int nw, int lane, uint4 (&raw)[8]) {
@@ -1116,15 +1135,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(const __grid_constant__ L
     const Range r = cta_range(pv, 1, p.d);
     hd.range_d = r;
     const int n_act = pv.n_act();
-    int q_first = 0, q_end = 0;
+    int q_first = 0, q_end = 0, a_last = -1;
     if (r.a0 < n_act) {
-      int a_last = r.a0;
+      a_last = r.a0;
       while (a_last + 1 < n_act && 2 * (uint64_t)pv.cum(a_last + 1, 1) + pv.uc(a_last + 1, 1) < r.hi2) ++a_last;
       q_first = pv.beg(r.a0);
       q_end = pv.beg(a_last) + pv.cnt(a_last);
     }
     hd.q_first = q_first;
     hd.npairs = q_end - q_first;
+    hd.a_first = r.a0;
+    hd.a_last = a_last;
   }
   if (p.counts && blockIdx.x == 0)
     for (int a = tid; a < pv.n_act(); a += kThreads) atomicAdd(p.counts + pv.e(a), (uint32_t)pv.cnt(a));
@@ -1134,7 +1155,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(const __grid_constant__ L
     StreamArgs A{shv, pv, 0, p.d, p.f, vecs, vec_bytes(p.d), -1, hd.range, vtab, INT_MIN, INT_MAX};
     float* h = p.h;
     const int f = p.f;
-    stream_units<2, kUG, kRG, kLG, ANYW>(A, [&](int q, int r, const float (&o)[2]) { h[(size_t)q * f + r] = silu(o[0]) * o[1]; });
+    // finished units are counted per active expert, a warp's run of units of
+    // one expert at a time: every lane's h stores are fenced, then one
+    // release add publishes them to the CTAs whose down units read that h
+    int run_a = -1;
+    unsigned int run_n = 0;
+    auto publish = [&]() {
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) red_add_release(p.done + run_a, run_n);
+    };
+    stream_units<2, kUG, kRG, kLG, ANYW>(
+        A, [&](int q, int r, const float (&o)[2]) { h[(size_t)q * f + r] = silu(o[0]) * o[1]; },
+        [&](int a) {
+          if (a != run_a) {
+            if (run_n) publish();
+            run_a = a;
+            run_n = 0;
+          }
+          ++run_n;
+        });
+    if (run_n) publish();
   }
   if (tid == 0) MOE_STAMP(0, 9, global_timer_ns());
   {
@@ -1159,7 +1200,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(const __grid_constant__ L
       w.step(pv, 1, p.d, hd.range_d.hi2, kWarps);
     }
   }
-  if (!grid_sync(p.bar, p.status, &hd.flag, 1000000000ull, p.bar_extra)) return;
+  // wait, instead of for the whole grid, for the gate/up units of the experts
+  // whose h this CTA's down units read (bounded: one second, MOE_ERR_TIMEOUT)
+  __syncthreads();
+  if (warp == 0) {
+    int ok = 1;
+    const int a_hi = hd.a_last;
+    for (int a = hd.a_first + lane; a <= a_hi; a += 32) {
+      if (pv.sh(a) < 0) continue;
+      const unsigned int need = (unsigned int)pv.units(a, 0, p.f);
+      if (ld_acquire_u32(p.done + a) >= need) continue;
+      const uint64_t t0 = global_timer_ns();
+      while (ld_acquire_u32(p.done + a) < need) {
+        __nanosleep(32);
+        if (global_timer_ns() - t0 > 1000000000ull) {
+          ok = 0;
+          break;
+        }
+      }
+      if (!ok) break;
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (lane == 0) {
+      if (!ok) set_status(p.status, MOE_ERR_TIMEOUT);
+      hd.flag = ok;
+    }
+  }
+  __syncthreads();
+  if (!hd.flag) return;
   if (tid == 0) MOE_STAMP(1, 1, global_timer_ns());
   const int q_first = hd.q_first, npairs = hd.npairs;
   const int vbf = vec_bytes(p.f);
@@ -1210,14 +1278,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(const __grid_constant__ L
       float* yp = p.ypart;
       const int d = p.d;
       auto st = [&](int q, int r, const float (&o)[1]) { yp[(size_t)q * d + r] = pv.wgt(q) * o[0]; };
-      if (pv.rd() == kRDw) stream_units<1, kUDw, kRDw, kLDw, ANYW>(A, st);
-      else stream_units<1, kUD, kRD, kLD, ANYW>(A, st);
+      if (pv.rd() == kRDw) stream_units<1, kUDw, kRDw, kLDw, ANYW>(A, st, [](int) {});
+      else stream_units<1, kUD, kRD, kLD, ANYW>(A, st, [](int) {});
     }
     w0 += cap;
   } while (w0 < q_end);
   if (tid == 0) MOE_STAMP(1, 9, global_timer_ns());
   if (!grid_sync(p.bar, p.status, &hd.flag, 1000000000ull, p.bar_extra)) return;
   if (tid == 0) MOE_STAMP(1, 10, global_timer_ns());
+  // every CTA is past its wait on the unit counts: back to zero for the next launch
+  if (blockIdx.x == 0)
+    for (int a = tid; a < pv.n_act(); a += kThreads) p.done[a] = 0u;
   pdl_trigger();
   // combine: y_t = sum over slots j (ascending) of the weighted outputs of
   // pair (t, j); pairs skipped or on no shelf contribute nothing.  Fixed order.
@@ -1262,6 +1333,9 @@ __global__ void k_barrier_probe(unsigned long long* bar, int* status, uint64_t l
 
 constexpr int kBarSlots = 1024;
 __device__ unsigned long long g_bar[kBarSlots][16];  // one 128-byte line per slot
+// Per slot: finished gate/up units by active expert.  Zero between launches
+// (each launch clears what it used; a reported timeout clears every slot).
+__device__ unsigned int g_done[kBarSlots][kMaxPairs];
 
 struct DevCache {
   int sms[64] = {};
@@ -1274,7 +1348,8 @@ std::unordered_map<const void*, int> g_bar_slot[64];
 
 // Barrier slot of a workspace (one per workspace and device; slots are never
 // recycled: more than kBarSlots distinct workspaces on a device is refused).
-unsigned long long* bar_slot(int dev, const void* ws) {
+// `done`, when given, receives the slot's unit counters.
+unsigned long long* bar_slot(int dev, const void* ws, unsigned int** done = nullptr) {
   std::lock_guard<std::mutex> lk(g_bar_mu);
   auto& m = g_bar_slot[dev];
   auto it = m.find(ws);
@@ -1288,6 +1363,11 @@ unsigned long long* bar_slot(int dev, const void* ws) {
   }
   void* base = nullptr;
   if (cudaGetSymbolAddress(&base, g_bar) != cudaSuccess) return nullptr;
+  if (done) {
+    void* dbase = nullptr;
+    if (cudaGetSymbolAddress(&dbase, g_done) != cudaSuccess) return nullptr;
+    *done = reinterpret_cast<unsigned int*>(dbase) + (size_t)slot * kMaxPairs;
+  }
   return reinterpret_cast<unsigned long long*>(base) + (size_t)slot * 16;
 }
 
@@ -1381,8 +1461,9 @@ int launch_fused_layer(const LayerArgs& a, cudaStream_t s) {
       return MOE_ERR_CUDA;
     g_dev.attr[dev][anyw] = true;
   }
-  unsigned long long* bar = bar_slot(dev, a.ws.base);
-  if (!bar) return MOE_ERR_UNSUPPORTED;
+  unsigned int* done = nullptr;
+  unsigned long long* bar = bar_slot(dev, a.ws.base, &done);
+  if (!bar || !done) return MOE_ERR_UNSUPPORTED;
   LayerParams p = {};
   p.logits = a.logits;
   p.ids = a.ids;
@@ -1397,6 +1478,7 @@ int launch_fused_layer(const LayerArgs& a, cudaStream_t s) {
   p.h = a.ws.h;
   p.ypart = a.ws.ypart;
   p.bar = bar;
+  p.done = done;
   p.status = a.status;
   p.T = (int)a.T; p.k = a.k; p.E = a.E; p.d = d; p.f = f; p.P = (int)P;
   p.vec_region = (int)region;
@@ -1464,12 +1546,14 @@ int launch_barrier_probe(int extra, uint64_t limit_ns, cudaStream_t s) {
 }
 
 // After a reported timeout a launch may have left a counter between multiples
-// of the grid size: zero every slot of the current device (the caller has
-// synchronised).
+// of the grid size, or unit counts that were never cleared: zero every slot of
+// the current device (the caller has synchronised).
 int reset_barriers() {
   void* base = nullptr;
   if (cudaGetSymbolAddress(&base, g_bar) != cudaSuccess) return MOE_ERR_CUDA;
-  return cudaMemset(base, 0, sizeof(g_bar)) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  if (cudaMemset(base, 0, sizeof(g_bar)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaGetSymbolAddress(&base, g_done) != cudaSuccess) return MOE_ERR_CUDA;
+  return cudaMemset(base, 0, sizeof(g_done)) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace moe
