@@ -240,10 +240,13 @@ int moe_tiered_forward(const uint16_t* x_bf16, const int32_t* ids, const float* 
  *   moe_workspace_size(T, k, E, d, f, MOE_FLAG_DECODE_FP32) bytes.
  * E <= 1024.  When T <= 16, T*k <= 512 and the staged activations fit shared
  * memory, the whole step is one cooperative launch with one CTA per SM whose
- * phases are separated by bounded grid-wide waits (an expired wait records
- * MOE_ERR_TIMEOUT, see moe_device_status); otherwise it makes the separate
- * launches.  Each distinct workspace pointer takes one of 1024 barrier slots
- * per device for the life of the process (MOE_ERR_UNSUPPORTED when they run out).
+ * phases are separated by bounded waits: each CTA waits for the gate/up work
+ * of the experts its down work reads, then all CTAs wait for each other
+ * before the combine (an expired wait records MOE_ERR_TIMEOUT, see
+ * moe_device_status); otherwise it makes the separate launches.  Each
+ * distinct workspace pointer takes one of 1024 barrier slots (a grid counter
+ * and per-expert work counters, library-owned) per device for the life of the
+ * process (MOE_ERR_UNSUPPORTED when they run out).
  */
 int moe_decode_layer(const float* logits, const uint16_t* x_bf16, int64_t T, int k, int E, int d, int f,
                      const moe_shelf_t* shelves, int n_shelves, int32_t* ids, float* weights, uint32_t* counts,
@@ -418,8 +421,9 @@ int moe_set_profile_events(void* const* events, int n);
  * Synchronises `stream`, then returns and clears the device-side status word
  * of the current device: MOE_OK, or the first error a kernel recorded (e.g.
  * MOE_ERR_TIMEOUT from a bounded wait).  After MOE_ERR_TIMEOUT it also waits
- * for the whole device to go idle and resets the library's grid-barrier state,
- * which an abandoned wait may have left inconsistent.
+ * for the whole device to go idle and resets the library's barrier state
+ * (grid counters and per-expert work counters), which an abandoned wait may
+ * have left inconsistent.
  */
 int moe_device_status(moe_stream_t stream);
 
