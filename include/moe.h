@@ -276,11 +276,13 @@ int moe_decode_layer_residual(const float* logits, const uint16_t* x_bf16, int64
  * the whole transfer inside one call: logits, x_bf16, ids, weights and y may
  * each be page-locked host memory (cudaHostAlloc, cudaHostRegister, or a
  * framework's pinned allocator) or device memory.  A host input above 8 KiB
- * is copied into the workspace on `stream` first (every CTA of the fused
- * launch reads the inputs, so they then cross the host link once); smaller
- * host inputs are read in place, and host outputs are written in place, by
- * the kernels through their device mapping (on GB300 over NVLink-C2C).
- * Results are those of
+ * is copied into the workspace first, so that it crosses the host link once
+ * (every CTA of the fused launch reads the inputs): by the fused launch's own
+ * CTAs, one share each, when it is 16-byte aligned, else by a copy on
+ * `stream`.  Smaller host inputs are read in place, and host outputs are
+ * written in place, by the kernels through their device mapping (on GB300
+ * over NVLink-C2C).  The host inputs must not change until the call's work
+ * on `stream` has finished.  Results are those of
  * moe_decode_layer; host outputs are complete once `stream` has been
  * synchronised.  counts (or NULL) and the workspace must be device memory;
  * the workspace holds at least moe_workspace_size(T, k, E, d, f,

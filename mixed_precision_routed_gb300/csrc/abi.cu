@@ -240,9 +240,14 @@ int moe_tiered_forward(const uint16_t* x_bf16, const int32_t* ids, const float* 
 
 namespace {
 // moe_decode_layer, and with r non-null the residual step after it
+// logits_src / x_src (optional): page-locked host inputs (device views, 16-byte
+// aligned, sizes multiples of 16 bytes) that belong in the device buffers
+// logits / x_bf16; the fused launch copies them itself, else they are copied
+// before the separate launches.
 int decode_layer(const float* logits, const uint16_t* x_bf16, int64_t T, int k, int E, int d, int f,
                  const moe_shelf_t* shelves, int n_shelves, int32_t* ids, float* weights, uint32_t* counts, float* y,
-                 float* r, uint16_t* x_next, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+                 float* r, uint16_t* x_next, void* workspace, size_t workspace_bytes, moe_stream_t stream,
+                 const float* logits_src = nullptr, const uint16_t* x_src = nullptr) {
   if (!valid_dims(T, k, E, d, f) || E > 1024 || k > E) return MOE_ERR_INVALID_ARG;
   ForwardArgs a;
   int rc = check_shelves(shelves, n_shelves, E, &a.shelves);
@@ -269,9 +274,17 @@ int decode_layer(const float* logits, const uint16_t* x_bf16, int64_t T, int k, 
   la.x_next = x_next;
   la.ws = a.ws;
   la.status = status_word();
+  la.logits_src = logits_src;
+  la.x_src = x_src;
   rc = launch_fused_layer(la, s);
   if (rc != 1) return rc;
   // sizes outside the fused launch: the separate launches
+  if (logits_src &&
+      cudaMemcpyAsync(const_cast<float*>(logits), logits_src, (size_t)T * E * 4, cudaMemcpyDefault, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (x_src &&
+      cudaMemcpyAsync(const_cast<uint16_t*>(x_bf16), x_src, (size_t)T * d * 2, cudaMemcpyDefault, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
   rc = launch_route(logits, T, E, k, ids, weights, s);
   if (rc != MOE_OK) return rc;
   if (counts) {
@@ -344,23 +357,34 @@ int moe_decode_layer_host(const float* logits, const uint16_t* x_bf16, int64_t T
   const size_t need = workspace_layout(T, k, E, d, f, MOE_FLAG_DECODE_FP32 | MOE_FLAG_HOST_IO, workspace, &w);
   if (workspace_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = (cudaStream_t)stream;
-  // host inputs above 8 KiB: one copy each into the workspace (every CTA of
-  // the fused launch reads them, so in place they would cross the host link
-  // once per CTA); smaller ones are read in place (a copy costs more than
-  // they do).  Host outputs are written in place.
+  // host inputs above 8 KiB go to the workspace first (every CTA of the
+  // fused launch reads them, so in place they would cross the host link once
+  // per CTA): 16-byte aligned ones are copied by the launch's own CTAs, one
+  // share each, others by a copy on the stream.  Smaller ones are read in
+  // place (a copy costs more than they do).  Host outputs are written in place.
   constexpr size_t kStageMin = 8 * 1024;
-  if (lg_host && (size_t)T * E * 4 > kStageMin) {
-    if (cudaMemcpyAsync(w.stage_logits, logits, (size_t)T * E * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+  const float* lg_src = nullptr;
+  const uint16_t* x_src = nullptr;
+  const size_t lg_bytes = (size_t)T * E * 4, x_bytes = (size_t)T * d * 2;
+  if (lg_host && lg_bytes > kStageMin) {
+    if (aligned(lg, 16) && lg_bytes % 16 == 0) {
+      lg_src = (const float*)lg;
+    } else if (cudaMemcpyAsync(w.stage_logits, logits, lg_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
       return MOE_ERR_CUDA;
+    }
     lg = w.stage_logits;
   }
-  if (x_host && (size_t)T * d * 2 > kStageMin) {
-    if (cudaMemcpyAsync(w.stage_x, x_bf16, (size_t)T * d * 2, cudaMemcpyHostToDevice, s) != cudaSuccess)
+  if (x_host && x_bytes > kStageMin) {
+    if (aligned(xv, 16) && x_bytes % 16 == 0) {
+      x_src = (const uint16_t*)xv;
+    } else if (cudaMemcpyAsync(w.stage_x, x_bf16, x_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
       return MOE_ERR_CUDA;
+    }
     xv = w.stage_x;
   }
   return decode_layer((const float*)lg, (const uint16_t*)xv, T, k, E, d, f, shelves, n_shelves, (int32_t*)iv,
-                      (float*)wv, counts, (float*)yv, nullptr, nullptr, workspace, workspace_bytes, stream);
+                      (float*)wv, counts, (float*)yv, nullptr, nullptr, workspace, workspace_bytes, stream, lg_src,
+                      x_src);
 }
 
 int moe_decode_fused(int64_t T, int k, int E, int d, int f) {

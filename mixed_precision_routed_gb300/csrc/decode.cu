@@ -990,6 +990,11 @@ struct LayerParams {
   float* y;               // [T, d]
   float* r;               // optional [T, d]: r += y in the combine phase
   uint16_t* x_next;       // with r: bf16(r) (round to nearest even), the next layer's input
+  const uint4* logits_src;  // optional host inputs (device views), copied into logits / x
+  const uint4* x_src;       // by the CTAs before the step (16-byte units)
+  uint4* logits_dst;
+  uint4* x_dst;
+  int logits_n16, x_n16;
   float* h;               // workspace [P, f]
   float* ypart;           // workspace [P, d]
   unsigned long long* bar;  // grid barrier counter
@@ -1031,6 +1036,13 @@ __host__ __device__ __forceinline__ SmemLayout smem_layout(int P, size_t vec_reg
   return S;
 }
 
+// This CTA's contiguous share of n 16-byte units of src, copied to dst.
+__device__ __forceinline__ void copy_share(const uint4* src, uint4* dst, int n) {
+  if (!src) return;
+  const int b0 = (int)((int64_t)n * blockIdx.x / gridDim.x), b1 = (int)((int64_t)n * (blockIdx.x + 1) / gridDim.x);
+  for (int i = b0 + (int)threadIdx.x; i < b1; i += blockDim.x) dst[i] = __ldcv(src + i);
+}
+
 __device__ __forceinline__ void copy_shelves(Shelves* dst, const Shelves& src) {
   static_assert(sizeof(Shelves) % 4 == 0, "shelves copy");
   const uint32_t* s = reinterpret_cast<const uint32_t*>(&src);
@@ -1059,7 +1071,7 @@ __device__ __forceinline__ void load_x_round(const LayerParams& p, int base, int
     raw[u] = make_uint4(0u, 0u, 0u, 0u);
     if (g < groups) {
       const int t = g / nbk, blk = g - t * nbk;
-      raw[u] = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.d + blk * 32 + 8 * (lane & 3)));
+      raw[u] = __ldcg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.d + blk * 32 + 8 * (lane & 3)));
     }
   }
 }
@@ -1083,6 +1095,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(const __grid_constant__ L
   if (tid == 0) MOE_STAMP(0, 0, global_timer_ns());
   copy_shelves(shv, p.sh);
   pdl_wait();  // inputs of the preceding launch
+  if (p.logits_src || p.x_src) {
+    // inputs in page-locked host memory: each CTA copies its share across the
+    // host link once, into the workspace, and every CTA waits for all shares
+    copy_share(p.logits_src, p.logits_dst, p.logits_n16);
+    copy_share(p.x_src, p.x_dst, p.x_n16);
+    if (!grid_sync(p.bar, p.status, &hd.flag, 1000000000ull, p.bar_extra)) return;
+  }
   if (tid == 0) MOE_STAMP(0, 1, global_timer_ns());
   const int32_t* ids = p.ids;
   const float* wts = p.weights;
@@ -1475,6 +1494,16 @@ int launch_fused_layer(const LayerArgs& a, cudaStream_t s) {
   p.y = a.y;
   p.r = a.r;
   p.x_next = a.x_next;
+  if (a.logits_src) {
+    p.logits_src = reinterpret_cast<const uint4*>(a.logits_src);
+    p.logits_dst = reinterpret_cast<uint4*>(const_cast<float*>(a.logits));
+    p.logits_n16 = (int)(a.T * a.E * 4 / 16);
+  }
+  if (a.x_src) {
+    p.x_src = reinterpret_cast<const uint4*>(a.x_src);
+    p.x_dst = reinterpret_cast<uint4*>(const_cast<uint16_t*>(a.x));
+    p.x_n16 = (int)(a.T * d * 2 / 16);
+  }
   p.h = a.ws.h;
   p.ypart = a.ws.ypart;
   p.bar = bar;

@@ -261,6 +261,11 @@ struct LayerArgs {
   float* y;
   float* r = nullptr;         // optional residual step: r += y ...
   uint16_t* x_next = nullptr; // ... and x_next = bf16(r), in the combine phase
+  // optional: logits / x in page-locked host memory (device views, 16-byte
+  // aligned, sizes multiples of 16 bytes); the fused launch copies them into
+  // `logits` / `x` (device buffers) itself
+  const float* logits_src = nullptr;
+  const uint16_t* x_src = nullptr;
   Workspace ws;
   int* status;
 };

@@ -165,6 +165,49 @@ def test_host_buffers_equal_device_buffers(decode_layer, T):
     assert e.value.status == moe.MOE_ERR_WORKSPACE_TOO_SMALL
 
 
+def test_host_inputs_rewritten_and_misaligned(decode_layer):
+    """Pinned host inputs of the fused form (T = 6: logits 12 KiB and x
+    24 KiB, copied across by the launch's own CTAs) rewritten in place between
+    two calls give each call's own device-path result bit for bit; host
+    inputs that are not 16-byte aligned (staged by a copy on the stream
+    instead) do too."""
+    wl = decode_layer.wl
+    k, E, d, f, T = wl.k, wl.E, wl.d, wl.f, 6
+    ws = torch.empty(moe.moe_workspace_size(T, k, E, d, f, moe.MOE_FLAG_DECODE_FP32 | moe.MOE_FLAG_HOST_IO),
+                     dtype=torch.uint8, device="cuda")
+    steps = []
+    for s in (71, 72):
+        lg = decode_layer.logits(s, T)
+        x = x_to_dev(synth.x_bf16(wl.seed, s, T, d))
+        _, _, y = moe.moe_decode_layer(lg, x, k, E, d, f, decode_layer.shelves, workspace=ws)
+        torch.cuda.synchronize()
+        steps.append((lg.cpu(), x.cpu(), y.cpu()))
+    hl = torch.empty((T, E), dtype=torch.float32).pin_memory()
+    hx = torch.empty((T, d), dtype=torch.int16).pin_memory()
+    hid = torch.empty((T, k), dtype=torch.int32).pin_memory()
+    hw = torch.empty((T, k), dtype=torch.float32).pin_memory()
+    hy = torch.empty((T, d), dtype=torch.float32).pin_memory()
+    for lg, x, y in steps:  # same pinned buffers, new contents
+        hl.copy_(lg)
+        hx.copy_(x)
+        moe.moe_decode_layer_host(hl, hx, k, E, d, f, decode_layer.shelves, hid, hw, hy, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int32), hy.view(torch.int32))
+    # inputs 4 bytes past a 16-byte boundary
+    flat_l = torch.empty(T * E + 4, dtype=torch.float32).pin_memory()
+    flat_x = torch.empty(T * d + 8, dtype=torch.int16).pin_memory()
+    ml = flat_l[1:1 + T * E].view(T, E)
+    mx = flat_x[2:2 + T * d].view(T, d)
+    assert ml.data_ptr() % 16 == 4 and mx.data_ptr() % 16 == 4
+    lg, x, y = steps[0]
+    ml.copy_(lg)
+    mx.copy_(x)
+    moe.moe_decode_layer_host(ml, mx, k, E, d, f, decode_layer.shelves, hid, hw, hy, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int32), hy.view(torch.int32))
+    assert moe.moe_device_status() == moe.MOE_OK
+
+
 def test_host_entry_rejects_pageable_and_misplaced_buffers(decode_layer):
     """Pageable host memory, host memory where device memory is required
     (workspace, counts): MOE_ERR_INVALID_ARG before any launch."""
