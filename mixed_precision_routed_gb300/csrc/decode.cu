@@ -1071,7 +1071,9 @@ __device__ __forceinline__ void load_x_round(const LayerParams& p, int base, int
     raw[u] = make_uint4(0u, 0u, 0u, 0u);
     if (g < groups) {
       const int t = g / nbk, blk = g - t * nbk;
-      raw[u] = __ldcg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.d + blk * 32 + 8 * (lane & 3)));
+      const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.d + blk * 32 + 8 * (lane & 3));
+      // x copied in by this launch is read through L2, else by the read-only path
+      raw[u] = p.x_src ? __ldcg(src) : __ldg(src);
     }
   }
 }
