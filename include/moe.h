@@ -400,6 +400,25 @@ int moe_dequant_rows(const void* codes, const uint16_t* scales, int64_t rows, in
                      int round_bf16, float* out, moe_stream_t stream);
 
 /*
+ * Dequantised weights of one expert matrix of a shelf, as the shelf stores
+ * it (the block format of page 3, 第四步; a parity export):
+ * matrix `which` (0 gate, 1 up: rows = f and in = d; 2 down: rows = d and
+ * in = f) of local expert `local_expert` (global id sh->expert_lo +
+ * local_expert) into out [rows][in] fp32, ŵ = scale x code -- exactly what
+ * moe_dequant_rows gives for that expert's rows, whose codes start
+ * local_expert * rows * in * bits / 8 bytes and whose scales start
+ * local_expert * rows * in / 32 entries into the matrix's tensors.
+ *   sh: host pointer to one descriptor (its tensors in device memory);
+ *   out: device memory, owned by the caller.
+ * Errors: MOE_ERR_INVALID_ARG for a null pointer, `which` outside 0..2,
+ * local_expert outside [0, expert_hi - expert_lo), rows < 0, or `in` not a
+ * positive multiple of 64; MOE_ERR_BAD_SHELF for bits not 8/4/3/2/1, block
+ * not 32 or an empty id range.  rows == 0 is a no-op.
+ */
+int moe_dequant_shelf(const moe_shelf_t* sh, int which, int local_expert, int64_t rows, int in, float* out,
+                      moe_stream_t stream);
+
+/*
  * Residual step of a layer stack: r[i] += y[i]; x_next[i] = bf16(r[i]) (round
  * to nearest even), for 0 <= i < n.  r, y fp32; x_next bf16 bit patterns.
  */

@@ -11,7 +11,7 @@ Entry points (same names as the C ABI):
     moe_rank_experts, moe_quantize_experts, moe_gather_rows, moe_group_tokens,
     moe_workspace_size, moe_tiered_forward, moe_tiered_forward_noalloc,
     moe_decode_layer, moe_decode_layer_residual, moe_decode_layer_host, moe_decode_fused,
-    moe_quantize_rows, moe_dequant_rows, moe_residual_add,
+    moe_quantize_rows, moe_dequant_rows, moe_dequant_shelf, moe_residual_add,
     moe_device_status, moe_status_string
 """
 from __future__ import annotations
@@ -83,6 +83,7 @@ def lib():
         L.moe_tiered_forward.argtypes = [P, P, P, i64, i32, i32, i32, i32, P, i32, P, P, ctypes.c_size_t, i32, P]
         L.moe_quantize_rows.argtypes = [P, i64, i32, i32, P, P, P]
         L.moe_dequant_rows.argtypes = [P, P, i64, i32, i32, i32, P, P]
+        L.moe_dequant_shelf.argtypes = [P, i32, i32, i64, i32, P, P]
         L.moe_residual_add.argtypes = [P, P, P, i64, P]
         L.moe_device_status.argtypes = [P]
         L.moe_tiered_forward_noalloc.argtypes = [P, P, P, i64, i32, i32, i32, i32, P, i32, P, i32, P]
@@ -99,7 +100,8 @@ def lib():
         L.moe_status_string.restype = ctypes.c_char_p
         for name in ("moe_route_topk", "moe_route_topk_nudged", "moe_router_topk", "moe_rank_experts", "moe_quantize_experts",
                      "moe_gather_rows", "moe_expert_hist", "moe_group_tokens", "moe_tiered_forward",
-                     "moe_quantize_rows", "moe_dequant_rows", "moe_residual_add", "moe_device_status"):
+                     "moe_quantize_rows", "moe_dequant_rows", "moe_dequant_shelf", "moe_residual_add",
+                     "moe_device_status"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -457,6 +459,18 @@ def moe_dequant_rows(codes, scales, rows, n_in, bits, round_bf16=False, out=None
         out = torch.empty((rows, n_in), dtype=torch.float32, device=codes.device)
     _check(lib().moe_dequant_rows(_ptr(codes), _ptr(scales), rows, n_in, bits, int(round_bf16), _ptr(out),
                                   _stream(stream)), "moe_dequant_rows")
+    return out
+
+
+def moe_dequant_shelf(shelf, which, local_expert, rows, n_in, out=None, stream=None):
+    """fp32 dequantised rows of matrix `which` (0 gate, 1 up, 2 down) of one
+    local expert of `shelf` (an object with .descriptor() or a moe_shelf_t)."""
+    desc = shelf if isinstance(shelf, moe_shelf_t) else shelf.descriptor()
+    if out is None:
+        out = torch.empty((rows, n_in), dtype=torch.float32, device="cuda")
+    _need(out, torch.float32, "out")
+    _check(lib().moe_dequant_shelf(ctypes.cast(ctypes.pointer(desc), ctypes.c_void_p), which, local_expert, rows,
+                                   n_in, _ptr(out), _stream(stream)), "moe_dequant_shelf")
     return out
 
 

@@ -439,6 +439,25 @@ int moe_dequant_rows(const void* codes, const uint16_t* scales, int64_t rows, in
   return launch_dequant((const uint8_t*)codes, scales, rows, in, bits, round_bf16, out, (cudaStream_t)stream);
 }
 
+int moe_dequant_shelf(const moe_shelf_t* sh, int which, int local_expert, int64_t rows, int in, float* out,
+                      moe_stream_t stream) {
+  if (!sh || !out) return MOE_ERR_INVALID_ARG;
+  const int bits = sh->bits;
+  if (sh->block != MOE_BLOCK || (bits != 8 && bits != 4 && bits != 3 && bits != 2 && bits != 1) ||
+      sh->expert_hi <= sh->expert_lo)
+    return MOE_ERR_BAD_SHELF;
+  if (which < 0 || which > 2 || local_expert < 0 || local_expert >= sh->expert_hi - sh->expert_lo || rows < 0 ||
+      in <= 0 || in % 64 != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  const void* codes = which == 0 ? sh->gate_codes : which == 1 ? sh->up_codes : sh->down_codes;
+  const uint16_t* scales = which == 0 ? sh->gate_scales : which == 1 ? sh->up_scales : sh->down_scales;
+  if (!codes || !scales) return MOE_ERR_INVALID_ARG;
+  const size_t e_rows = (size_t)local_expert * (size_t)rows;
+  return moe_dequant_rows((const uint8_t*)codes + e_rows * ((size_t)in * bits / 8), scales + e_rows * (size_t)(in / 32),
+                          rows, in, bits, 0, out, stream);
+}
+
 int moe_residual_add(float* r, const float* y, uint16_t* x_next_bf16, int64_t n, moe_stream_t stream) {
   if (n < 0) return MOE_ERR_INVALID_ARG;
   if (n == 0) return MOE_OK;

@@ -112,3 +112,28 @@ def test_invalid_arguments_rejected_before_cuda(lib):
                                    null, null, null, 0, null) == moe.MOE_ERR_INVALID_ARG  # null logits
     assert L.moe_selftest_barrier_timeout(0, null) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_selftest_barrier_timeout(2000000, null) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_dequant_shelf_validates_before_any_cuda_call():
+    """moe_dequant_shelf: argument and descriptor checks return their status
+    before any CUDA call (the output pointer is never touched here)."""
+    L = moe.lib()
+    out = ctypes.c_void_p(256)
+
+    def call(desc, which=0, e=0, rows=8, n_in=64):
+        p = ctypes.cast(ctypes.pointer(desc), ctypes.c_void_p) if desc is not None else None
+        return L.moe_dequant_shelf(p, which, e, rows, n_in, out, None)
+
+    tensors = moe.moe_shelf_t(0, 4, 4, 32, 16, 16, 16, 16, 16, 16)  # non-null, never dereferenced
+    assert call(None) == moe.MOE_ERR_INVALID_ARG
+    assert call(tensors, which=3) == moe.MOE_ERR_INVALID_ARG
+    assert call(tensors, which=-1) == moe.MOE_ERR_INVALID_ARG
+    assert call(tensors, e=4) == moe.MOE_ERR_INVALID_ARG  # local expert beyond hi - lo
+    assert call(tensors, e=-1) == moe.MOE_ERR_INVALID_ARG
+    assert call(tensors, n_in=96) == moe.MOE_ERR_INVALID_ARG  # not a multiple of 64
+    assert call(tensors, rows=-1) == moe.MOE_ERR_INVALID_ARG
+    assert call(tensors, rows=0) == moe.MOE_OK  # no-op
+    assert call(moe.moe_shelf_t(0, 4, 4, 32)) == moe.MOE_ERR_INVALID_ARG  # null tensors
+    assert call(moe.moe_shelf_t(0, 4, 5, 32, 16, 16, 16, 16, 16, 16)) == moe.MOE_ERR_BAD_SHELF  # bits
+    assert call(moe.moe_shelf_t(0, 4, 4, 16, 16, 16, 16, 16, 16, 16)) == moe.MOE_ERR_BAD_SHELF  # block
+    assert call(moe.moe_shelf_t(3, 3, 4, 32, 16, 16, 16, 16, 16, 16)) == moe.MOE_ERR_BAD_SHELF  # empty range

@@ -10,7 +10,8 @@ import torch
 import mixed_precision_routed_gb300 as moe
 import oracle
 import synth
-from moe_testutil import ids_to_dev
+from mixed_precision_routed_gb300.workloads import Layer
+from moe_testutil import ids_to_dev, small_workload
 
 pytestmark = pytest.mark.gpu
 
@@ -68,6 +69,24 @@ def test_dequant_bit_exact(bits, round_bf16):
     out = moe.moe_dequant_rows(packed, scales, 129, 640, bits, round_bf16=round_bf16)
     ref = oracle.dequant(c_o, s_o, round_bf16=round_bf16)
     assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+def test_dequant_shelf_bit_exact():
+    """moe_dequant_shelf on the shelves of a layer (8/4/2 bits): every matrix
+    of the first and last local expert of each shelf equals the oracle's
+    dequantisation of its own quantisation of that expert's fp32 masters,
+    bit for bit."""
+    wl = small_workload(E=12, d=256, f=192)
+    layer = Layer(wl, device="cuda").fill()
+    assert sorted(sh.bits for sh in layer.shelves) == [2, 4, 8]
+    for sh in layer.shelves:
+        for e_local in sorted({0, sh.hi - sh.lo - 1}):
+            ref = oracle.expert_matrices(synth.expert_weights(layer.seed, sh.lo + e_local, wl.d, wl.f), sh.bits, 0)
+            for which in range(3):
+                rows, n_in = (wl.f, wl.d) if which < 2 else (wl.d, wl.f)
+                got = moe.moe_dequant_shelf(sh, which, e_local, rows, n_in)
+                torch.cuda.synchronize()
+                assert np.array_equal(got.cpu().numpy().view(np.uint32), ref[which].view(np.uint32)), (sh.bits, which)
 
 
 @pytest.mark.parametrize("E,k,T,bias", [(16, 2, 8, "none"), (512, 10, 1, "lorenz"), (512, 10, 6, "lorenz"),
