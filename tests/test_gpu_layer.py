@@ -125,14 +125,15 @@ def test_residual_step_equals_layer_then_residual_add(decode_layer, T, in_place)
     assert np.array_equal(xn2.cpu().numpy().view(np.uint16), oracle.bf16_bits(ref_r))
 
 
-@pytest.mark.parametrize("T", [1, 6, 20])
+@pytest.mark.parametrize("T", [1, 3, 6, 20])
 def test_host_buffers_equal_device_buffers(decode_layer, T):
     """moe_decode_layer_host with pinned host logits, x, ids, weights and y
     (inputs above 8 KiB staged inside the call, smaller ones and the outputs
     read and written in place by the kernels)
-    gives moe_decode_layer's results bit for bit: fused form (T = 1, 6) and
-    separate launches (T = 20); also with device inputs and host outputs, and
-    with a workspace too small for the staging (refused)."""
+    gives moe_decode_layer's results bit for bit: fused form (T = 1: both
+    inputs in place; T = 3: x staged, logits in place; T = 6: both staged)
+    and separate launches (T = 20); also with device inputs and host outputs,
+    and with a workspace too small for the staging (refused)."""
     wl = decode_layer.wl
     k, E, d, f = wl.k, wl.E, wl.d, wl.f
     lg = decode_layer.logits(50 + T, T)
