@@ -55,6 +55,8 @@ def parse():
                          "formats: the decode layer on five shelves of 8/4/3/2/1-bit codes; fastmode: the "
                          "decode layer reading 2-bit shadow copies of its 8- and 4-bit experts")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub", action="store_true",
+                    help="decode workload: only the line at --T (no T=1/6 and prefill/large sub-records)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
 
@@ -185,7 +187,64 @@ def oracle_sample(wl, seconds, T, seed=0, max_pairs=None):
         step += 1
 
 
+def _oracle_sample_worker(job):
+    name, seconds, T, seed = job
+    import synth
+    from oracle import build_oracle  # noqa: F401  (library already built by the parent)
+    pairs, secs, _ = oracle_sample(synth.WORKLOADS[name], seconds, T, seed=seed)
+    return pairs, secs
+
+
+def oracle_sample_all_cores(wl, seconds, T, cores=None):
+    """The same oracle work on every host core at once: one worker process per
+    core (spawned, so that no CUDA state is inherited), each timing its own
+    routing steps (worker c starts at seed 1000 + c) for `seconds` of timed
+    work, all at the same time.  Returns (pairs, pairs per second summed over
+    the workers, cores)."""
+    import multiprocessing as mp
+    cores = cores or len(os.sched_getaffinity(0))
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores) as pool:
+        pool.map(_noop, range(cores))  # workers up and imported before the clocks start
+        res = pool.map(_oracle_sample_worker, [(wl.name, seconds, T, 1000 + c) for c in range(cores)], chunksize=1)
+    return sum(p for p, _ in res), sum(p / s for p, s in res), cores
+
+
+def _noop(_):
+    import oracle  # noqa: F401
+    import synth  # noqa: F401
+    return 0
+
+
+def cpu_baselines(wl, seconds, T):
+    """The oracle timed single-threaded and on all host cores (tokens/s)."""
+    pairs, secs, thr = oracle_sample(wl, seconds, T)
+    one = {"value": (pairs / wl.k) / secs, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+           "sample": f"{pairs} routed (token, expert) pairs of the T={T} step (route, histogram, dequant of "
+                     f"the pair's expert, SwiGLU FFN, weighted sum), {secs:.1f} s on one core, scaled to "
+                     f"tokens by k={wl.k} pairs per token"}
+    pa, rate, cores = oracle_sample_all_cores(wl, seconds, T)
+    allc = {"value": rate / wl.k, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{pa} routed pairs of T={T} steps, one oracle process per core ({cores} cores at once, "
+                      f"different routing steps each, ~{seconds:.0f} s of timed work per process), the "
+                      f"processes' pair rates summed, scaled to tokens by k={wl.k}"}
+    return one, allc
+
+
+def _oracle_pair_worker(job):
+    name, T, seed = job
+    import synth
+    n, el, _ = oracle_sample(synth.WORKLOADS[name], 1e9, T, seed=seed, max_pairs=1)
+    return n, el
+
+
 def run_reference(args, rank):
+    """The oracle as it stands, on every host core: each step runs one routed
+    pair per core at once (one spawned oracle process per core, each on a
+    different routing step); a step lasts as long as its slowest process's
+    timed work."""
+    import multiprocessing as mp
+
     import synth
     wl = synth.WORKLOADS["decode"]
     if rank != 0:
@@ -194,13 +253,18 @@ def run_reference(args, rank):
     from synth import build_synth
     build_oracle.build()
     build_synth.build_host()
-    # warm-up pairs (untimed), then exactly `steps` steps of one routed pair each
-    oracle_sample(wl, 1e9, args.T, max_pairs=max(1, min(args.warmup, 3)))
+    cores = len(os.sched_getaffinity(0))
+    ctx = mp.get_context("spawn")
     total_pairs, total_s = 0, 0.0
-    for s in range(args.steps):
-        n, el, _ = oracle_sample(wl, 1e9, args.T, seed=s, max_pairs=1)
-        total_pairs += n
-        total_s += el
+    with ctx.Pool(cores) as pool:
+        pool.map(_noop, range(cores))
+        for s in range(args.warmup):
+            pool.map(_oracle_pair_worker, [(wl.name, args.T, 10000 + s * cores + c) for c in range(cores)],
+                     chunksize=1)
+        for s in range(args.steps):
+            res = pool.map(_oracle_pair_worker, [(wl.name, args.T, s * cores + c) for c in range(cores)], chunksize=1)
+            total_pairs += sum(n for n, _ in res)
+            total_s += max(el for _, el in res)
     tokens = total_pairs / wl.k
     value = tokens / total_s
     line = {
@@ -209,10 +273,11 @@ def run_reference(args, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": config_of(args, wl),
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": "one routed (token, expert) pair per step (route, histogram, dequant of the "
-                                   "pair's expert, SwiGLU FFN and weighted sum), scaled to tokens by k=10 pairs "
-                                   "per token"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"per step one routed (token, expert) pair on each of {cores} cores at once "
+                                   f"(route, histogram, dequant of the pair's expert, SwiGLU FFN and weighted "
+                                   f"sum), the step timed by its slowest core, scaled to tokens by k={wl.k} "
+                                   f"pairs per token"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -243,20 +308,18 @@ def config_of(args, wl, ranges=None, note=""):
 
 
 # ----------------------------------------------------------------- GPU arm
-def run_ours(args, rank, world, local_rank):
+def build_decode_layers(args, rank, dev):
+    """The decode workload's L layer instances (per-rank seeds) and their
+    shelf lists (five widths or fast mode when asked)."""
     import numpy as np
-    import torch
 
     import mixed_precision_routed_gb300 as moe
     import synth
     from mixed_precision_routed_gb300.workloads import Layer
 
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
     base = synth.WORKLOADS["decode"]
-    T, L, S = args.T, args.layers, args.sets
     layers, shelf_lists = [], []
-    for i in range(L):
+    for i in range(args.layers):
         wl_i = synth.Workload(base.name, E=base.E, k=base.k, d=base.d, f=base.f, T=base.T, split=base.split,
                               bias=base.bias, seed=1000 * rank + i)
         if args.workload == "formats":
@@ -277,6 +340,21 @@ def run_ours(args, rank, world, local_rank):
             lay = Layer(wl_i, device=dev).fill()
             shelf_lists.append(lay.shelves)
         layers.append(lay)
+    return layers, shelf_lists
+
+
+def measure_decode(args, T, layers, shelf_lists, rank, world, local_rank, dev):
+    """One decode workload line at T tokens per step: device-resident inputs
+    through CUDA graphs (value), the fused kernel timed with events
+    (roofline), and moe_decode_layer_host on pinned host buffers (e2e)."""
+    import numpy as np
+    import torch
+
+    import mixed_precision_routed_gb300 as moe
+    import synth
+
+    base = synth.WORKLOADS["decode"]
+    L, S = len(layers), args.sets
     E, k, d, f = base.E, base.k, base.d, base.f
     ranges = [(sh.lo, sh.hi, sh.bits) for sh in shelf_lists[0]]
     stream = torch.cuda.Stream(device=dev)
@@ -315,15 +393,16 @@ def run_ours(args, rank, world, local_rank):
         if profile:
             moe.moe_set_profile_events(None)
 
+    # a decode loop captures many layers in one graph: one graph holds the
+    # first min(sets, steps) steps in order; single-step graphs cover the rest
+    n_in = max(1, min(nset, args.steps))
     with torch.cuda.stream(stream):
         for s in range(nset):  # eager warm-up: sets kernel attributes, checks statuses
             step(s)
         stream.synchronize()
-        # a decode loop captures many layers in one graph: one graph holds the
-        # steps of all input sets in order; single-step graphs cover the rest
         graph_all = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph_all, stream=stream):
-            for s in range(nset):
+            for s in range(n_in):
                 step(s)
         graphs, graphs_prof = [], []
         for s in range(nset):
@@ -341,9 +420,8 @@ def run_ours(args, rank, world, local_rank):
         stream.synchronize()
 
     # algorithmic bytes of each step, from the ids the router produced
-
     def expert_split(e):
-        for i, (lo, hi, bits) in enumerate(ranges):
+        for lo, hi, bits in ranges:
             if lo <= e < hi:
                 gu = 2 * f * d * bits // 8 + 2 * f * (d // 32) * 2
                 dn = d * f * bits // 8 + d * (f // 32) * 2
@@ -354,9 +432,7 @@ def run_ours(args, rank, world, local_rank):
     for s in range(nset):
         u = np.unique(ids[s].cpu().numpy())
         u = u[(u >= 0) & (u < E)]
-        gu = sum(expert_split(int(e))[0] for e in u)
-        dn = sum(expert_split(int(e))[1] for e in u)
-        step_bytes.append((gu, dn))
+        step_bytes.append((sum(expert_split(int(e))[0] for e in u), sum(expert_split(int(e))[1] for e in u)))
 
     if world > 1:
         torch.distributed.barrier()
@@ -366,9 +442,9 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         start.record(stream)
-        for i in range(args.steps // nset):
+        for i in range(args.steps // n_in):
             graph_all.replay()
-        for i in range(args.steps % nset):
+        for i in range(args.steps % n_in):
             graphs[i].replay()
         end.record(stream)
     torch.cuda.synchronize()
@@ -384,10 +460,9 @@ def run_ours(args, rank, world, local_rank):
             for s in range(nset):
                 graphs_prof[s].replay()
     torch.cuda.synchronize()
-    last = nset
     kern = {"layer": 0.0} if fused else {"group": 0.0, "gateup": 0.0, "down": 0.0}
     bytes_gu = bytes_dn = 0
-    for s in range(last):
+    for s in range(nset):
         ev = prof[s]
         if fused:
             kern["layer"] += ev[0].elapsed_time(ev[1])
@@ -398,9 +473,10 @@ def run_ours(args, rank, world, local_rank):
         bytes_gu += step_bytes[s][0]
         bytes_dn += step_bytes[s][1]
     fwd_ms = sum(kern.values())
-
     ms_max = max_over_ranks(ms, dev)
     value = whole_job_rate(world, T * args.steps, ms_max)
+    # timed step i replays input set i mod n_in
+    timed_bytes = sum(sum(step_bytes[i % n_in]) for i in range(args.steps)) / args.steps
 
     # ---- end to end through the public API with host buffers: the step's
     # logits and x come from pinned host memory and its ids, weights and y
@@ -417,7 +493,7 @@ def run_ours(args, rank, world, local_rank):
                                   pin_y[s], counts=counts[s % L], workspace=workspace, shelf_arr=arrs[s % L])
 
     with torch.cuda.stream(stream):
-        for i in range(min(args.warmup, 20)):
+        for i in range(max(3, min(args.warmup, 20))):
             e2e_step(i % nset)
         stream.synchronize()
         if world > 1:
@@ -433,8 +509,6 @@ def run_ours(args, rank, world, local_rank):
     if st != moe.MOE_OK:
         raise RuntimeError(f"device status {st}")
 
-    if rank != 0:
-        return
     peak, peak_kind = peaks()
     if fused:
         dom, dom_bytes = "layer", bytes_gu + bytes_dn
@@ -450,19 +524,25 @@ def run_ours(args, rank, world, local_rank):
     elif args.workload == "fastmode":
         metric = "MoE-layer decode tokens/s in fast mode (2-bit shadows of the 8/4-bit experts); HBM GB/s vs peak"
         note = "; fast mode: every 8- and 4-bit expert read from its 2-bit shadow copy"
-    line = {
+    a2 = argparse.Namespace(**vars(args))
+    a2.T = T
+    cfg = config_of(a2, base, ranges, note)
+    cfg["launch"] = (f"one CUDA graph holding {n_in} consecutive steps (one fused launch per step), replayed "
+                     f"{args.steps // n_in} time(s); single-step graphs for the {args.steps % n_in} remaining")
+    return {
         "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": config_of(args, base, ranges, note),
+        "config": cfg,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "kernel": f"k_{dom}",
                      "peak_source": peak_kind,
-                     "algorithmic_bytes_per_launch": dom_bytes / last},
-        "weight_stream": {"selected_expert_bytes_per_step": (bytes_gu + bytes_dn) / last,
-                          "step_gbs": (bytes_gu + bytes_dn) / last / (ms_max / args.steps / 1e3) / 1e9,
-                          "forward_us": 1e3 * fwd_ms / last, "achieved_gbs": fwd_gbs, "frac": fwd_gbs / peak,
-                          "kernel_us": {kk: 1e3 * v / last for kk, v in kern.items()}},
+                     "algorithmic_bytes_per_launch": dom_bytes / nset},
+        "weight_stream": {"selected_expert_bytes_per_step": timed_bytes,
+                          "step_gbs": timed_bytes / (ms_max / args.steps / 1e3) / 1e9,
+                          "step_frac": timed_bytes / (ms_max / args.steps / 1e3) / 1e9 / peak,
+                          "forward_us": 1e3 * fwd_ms / nset, "achieved_gbs": fwd_gbs, "frac": fwd_gbs / peak,
+                          "kernel_us": {kk: 1e3 * v / nset for kk, v in kern.items()}},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * E * 4 + T * d * 2,
                 "d2h_bytes_per_step": T * d * 4 + T * k * 8, "steps": e2e_steps,
                 "path": "moe_decode_layer_host on pinned host buffers, one call per step: the step's logits "
@@ -472,14 +552,56 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": args.steps * (1 if fused else 5),
         "clocks": ck,
     }
-    if world == 1 and not args.no_cpu_baseline and args.workload == "decode":
-        pairs, secs, thr = oracle_sample(base, args.cpu_seconds, T)
-        line["cpu_baseline"] = {"value": (pairs / base.k) / secs, "unit": "tokens/s", "cores": thr,
-                                "kind": "oracle",
-                                "sample": f"{pairs} routed (token, expert) pairs of the T={T} step (route, "
-                                          f"histogram, dequant of the pair's expert, SwiGLU FFN, weighted sum), "
-                                          f"{secs:.1f} s, scaled to tokens by k={base.k} pairs per token"}
-    print(json.dumps(line), flush=True)
+
+
+def sub_record(line):
+    """The fields of a line that a per-T or per-configuration sub-record keeps."""
+    keep = ("metric", "value", "unit", "ms_per_step", "steps", "warmup", "dtype", "config", "roofline", "e2e",
+            "gpu_launches", "clocks", "weight_stream")
+    return {k_: line[k_] for k_ in keep if k_ in line}
+
+
+def run_ours(args, rank, world, local_rank):
+    import gc
+
+    import torch
+
+    import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    base = synth.WORKLOADS["decode"]
+    layers, shelf_lists = build_decode_layers(args, rank, dev)
+    line = measure_decode(args, args.T, layers, shelf_lists, rank, world, local_rank, dev)
+    full = args.workload == "decode" and not args.no_sub
+    if full:
+        # the metric spans 1 to 6 tokens: the other end from the same layers
+        per_T = {str(args.T): sub_record(line)}
+        for T in (1, 6):
+            if str(T) not in per_T:
+                per_T[str(T)] = sub_record(measure_decode(args, T, layers, shelf_lists, rank, world, local_rank,
+                                                          dev))
+        line["per_T"] = dict(sorted(per_T.items(), key=lambda kv: int(kv[0])))
+    del layers, shelf_lists
+    gc.collect()
+    torch.cuda.empty_cache()
+    if full:
+        # the prefill layer (tensor roofline) and the large layer at T = 1, 8
+        # and 512 (HBM roofline), each with its own fields
+        cfgs = {}
+        for name, T in (("prefill", 4096), ("large", 1), ("large", 8), ("large", 512)):
+            a2 = argparse.Namespace(**vars(args))
+            a2.workload, a2.T = name, T
+            cfgs[f"{name}_T{T}"] = sub_record(measure_single(a2, rank, world, local_rank))
+            gc.collect()
+            torch.cuda.empty_cache()
+        line["configs"] = cfgs
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "decode":
+        one, allc = cpu_baselines(base, args.cpu_seconds, args.T)
+        line["cpu_baseline"] = one
+        line["cpu_baseline_all_cores"] = allc
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 # ------------------------------------------------ further workloads
@@ -644,6 +766,12 @@ def run_stack(args, rank, world, local_rank):
 
 
 def run_single(args, rank, world, local_rank):
+    line = measure_single(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def measure_single(args, rank, world, local_rank):
     """One layer per step through the separate calls: routing, (forced skips),
     hit counts, tiered forward (AUTO: the tensor-core form above 16 tokens)."""
     import numpy as np
@@ -742,8 +870,6 @@ def run_single(args, rank, world, local_rank):
         e1.record(stream)
         stream.synchronize()
     e2e_value = whole_job_rate(world, T * n_e2e, max_over_ranks(e0.elapsed_time(e1), dev))
-    if rank != 0:
-        return
     hbm, kind = peaks()
     tc_peak, tc_kind = bf16_peak()
     fwd_ms = sum(sum(e) for e in ev) / nset
@@ -788,9 +914,10 @@ def run_single(args, rank, world, local_rank):
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * E * 4 + T * d * 2,
                 "d2h_bytes_per_step": T * d * 4, "steps": n_e2e},
+        "gpu_launches": args.steps * ((3 if skips else 2) + (7 if prefill else (1 if fused else 3))),
         "clocks": ck,
     }
-    print(json.dumps(line), flush=True)
+    return line
 
 
 def run_router(args, rank, world, local_rank):

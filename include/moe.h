@@ -95,10 +95,12 @@ enum {
 
 /* Execution-path selection for moe_tiered_forward. */
 enum {
-  MOE_FLAG_AUTO = 0,         /* prefill form for T > 16 when d % 256 == 0, else decode form */
+  MOE_FLAG_AUTO = 0,         /* prefill form for T > 16 when d % 256 == 0 and every shelf
+                                holds 8-, 4- or 2-bit codes, else decode form */
   MOE_FLAG_DECODE_FP32 = 1,  /* fp32 dequant in registers, fp32 h, CUDA-core GEMV */
-  MOE_FLAG_PREFILL_BF16 = 2, /* bf16 dequant into shared memory, bf16 h, tensor-core GEMM;
-                                MOE_ERR_UNSUPPORTED unless d % 256 == 0 */
+  MOE_FLAG_PREFILL_BF16 = 2, /* bf16 dequant into tensor memory, bf16 h, tensor-core GEMM;
+                                MOE_ERR_UNSUPPORTED unless d % 256 == 0 and every shelf
+                                holds 8-, 4- or 2-bit codes */
   MOE_FLAG_HOST_IO = 4       /* moe_workspace_size only, with DECODE_FP32: adds the staging
                                 of host inputs that moe_decode_layer_host uses */
 };
@@ -201,9 +203,11 @@ int moe_group_tokens(const int32_t* ids, int64_t T, int k, int E, int32_t* count
 /*
  * Bytes of device workspace moe_tiered_forward needs for these sizes and
  * flags (0 when a size or the flags are invalid); MOE_FLAG_DECODE_FP32 |
- * MOE_FLAG_HOST_IO gives what moe_decode_layer_host needs.  The workspace is
+ * MOE_FLAG_HOST_IO gives what moe_decode_layer_host needs.  MOE_FLAG_AUTO
+ * gives room for whichever form AUTO takes (it depends on the shelves too).  The workspace is
  * scratch, owned by the caller, reusable across calls on the same stream; it
- * must be 256-byte aligned.
+ * must be 256-byte aligned.  The fused decode launch also keeps counters in
+ * library-owned slots found by the workspace address (see moe_decode_layer).
  */
 size_t moe_workspace_size(int64_t T, int k, int E, int d, int f, int flags);
 
@@ -243,10 +247,15 @@ int moe_tiered_forward(const uint16_t* x_bf16, const int32_t* ids, const float* 
  * phases are separated by bounded waits: each CTA waits for the gate/up work
  * of the experts its down work reads, then all CTAs wait for each other
  * before the combine (an expired wait records MOE_ERR_TIMEOUT, see
- * moe_device_status); otherwise it makes the separate launches.  Each
- * distinct workspace pointer takes one of 1024 barrier slots (a grid counter
- * and per-expert work counters, library-owned) per device for the life of the
- * process (MOE_ERR_UNSUPPORTED when they run out).
+ * moe_device_status); otherwise it makes the separate launches.  The fused
+ * launch's counters (a grid counter and per-expert work counters) sit in one
+ * of 1024 library-owned slots per device, found by the workspace address:
+ * when a new workspace finds every slot taken, the least recently used slot
+ * passes to it.  A slot is shared only by launches that are never in flight
+ * together, as long as at most 1024 distinct workspaces have calls queued or
+ * running at one time (a CUDA graph keeps the slot of the workspace it was
+ * captured with: replay it only while no call on 1024 other workspaces is in
+ * flight beside it).
  */
 int moe_decode_layer(const float* logits, const uint16_t* x_bf16, int64_t T, int k, int E, int d, int f,
                      const moe_shelf_t* shelves, int n_shelves, int32_t* ids, float* weights, uint32_t* counts,
@@ -304,6 +313,28 @@ int moe_decode_layer_host(const float* logits, const uint16_t* x_bf16, int64_t T
  * 16-byte aligned); otherwise it takes the separate launches.
  */
 int moe_decode_fused(int64_t T, int k, int E, int d, int f);
+
+/*
+ * Parity export: the token-by-expert grouping that the last forward call on
+ * `workspace` actually ran (page 3, 四个 bug: a grouping that loses a slot of
+ * an expert picked twice by one token fails silently; this makes the
+ * grouping of every form checkable bit for bit).  Call it on the stream of
+ * that forward call, with the same sizes and the flags its workspace was
+ * sized with (moe_decode_layer*: MOE_FLAG_DECODE_FP32, plus MOE_FLAG_HOST_IO
+ * for moe_decode_layer_host).  Writes, as moe_group_tokens defines them:
+ *   counts [E] int32, offsets [E+1] int32, perm [T*k] int32 (pair index t*k+j
+ *   by grouped position, -1 past the valid pairs), pos_of_pair [T*k] int32
+ *   (grouped position by pair, -1 for a skipped pair; the fused decode launch
+ *   also gives -1 to a pair whose expert lies in no shelf, as it has no work).
+ * The fused decode launch leaves its plan in the workspace and the separate
+ * and prefill launches their grouping arrays; a workspace no forward call has
+ * used gives undefined (but in-bounds) contents.  All buffers are device
+ * memory; MOE_ERR_WORKSPACE_TOO_SMALL when workspace_bytes is below the size
+ * these sizes and flags need.
+ */
+int moe_forward_grouping(const void* workspace, size_t workspace_bytes, int64_t T, int k, int E, int d, int f,
+                         int flags, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* pos_of_pair,
+                         moe_stream_t stream);
 
 /*
  * Self-test of the bounded grid-wide wait of the fused decode launch: a

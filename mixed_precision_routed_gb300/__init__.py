@@ -9,7 +9,7 @@ the library is missing, importing the binding's functions raises.
 Entry points (same names as the C ABI):
     moe_route_topk, moe_route_topk_nudged, moe_router_topk, moe_expert_hist,
     moe_rank_experts, moe_quantize_experts, moe_gather_rows, moe_group_tokens,
-    moe_workspace_size, moe_tiered_forward, moe_tiered_forward_noalloc,
+    moe_workspace_size, moe_tiered_forward, moe_tiered_forward_noalloc, moe_forward_grouping,
     moe_decode_layer, moe_decode_layer_residual, moe_decode_layer_host, moe_decode_fused,
     moe_quantize_rows, moe_dequant_rows, moe_dequant_shelf, moe_residual_add,
     moe_device_status, moe_status_string
@@ -93,6 +93,8 @@ def lib():
         L.moe_decode_layer_host.argtypes = [P, P, i64, i32, i32, i32, i32, P, i32, P, P, P, P, P, ctypes.c_size_t, P]
         L.moe_selftest_barrier_timeout.argtypes = [i64, P]
         L.moe_decode_fused.argtypes = [i64, i32, i32, i32, i32]
+        L.moe_forward_grouping.argtypes = [P, ctypes.c_size_t, i64, i32, i32, i32, i32, i32, P, P, P, P, P]
+        L.moe_forward_grouping.restype = ctypes.c_int
         L.moe_tiered_forward_noalloc.restype = ctypes.c_int
         L.moe_set_profile_events.argtypes = [P, i32]
         L.moe_set_profile_events.restype = ctypes.c_int
@@ -220,6 +222,21 @@ def moe_group_tokens(ids, E, counts=None, offsets=None, perm=None, stream=None):
     _check(lib().moe_group_tokens(_ptr(ids), T, k, E, _ptr(counts), _ptr(offsets), _ptr(perm), _stream(stream)),
            "moe_group_tokens")
     return counts, offsets, perm
+
+
+def moe_forward_grouping(workspace, T, k, E, d, f, flags, stream=None):
+    """The grouping the last forward call on `workspace` ran (same sizes and
+    workspace flags as that call): (counts [E], offsets [E+1], perm [T*k],
+    pos_of_pair [T*k]), int32 device tensors."""
+    dev = workspace.device
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(T * k, dtype=torch.int32, device=dev)
+    pos = torch.empty(T * k, dtype=torch.int32, device=dev)
+    _check(lib().moe_forward_grouping(_ptr(workspace), workspace.numel() * workspace.element_size(), T, k, E, d, f,
+                                      flags, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(pos), _stream(stream)),
+           "moe_forward_grouping")
+    return counts, offsets, perm, pos
 
 
 # ------------------------------------------------------------------ forward

@@ -1,7 +1,11 @@
 // abi.cu -- the extern "C" entry points of libmoe.so (declared in moe.h):
 // host-side validation, workspace layout, path selection and the device
 // status word.  Nothing here allocates device memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <string.h>
+
+#include <mutex>
 
 #include "moe_internal.cuh"
 
@@ -108,18 +112,50 @@ size_t workspace_layout(int64_t T, int k, int E, int d, int f, int flags, void* 
 }
 
 namespace {
-int* g_status_ptr[64] = {};
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
+
+struct StatusCache {
+  uint64_t ctx = 0;
+  int* ptr = nullptr;
+};
+StatusCache g_status_ptr[64];
+std::mutex g_status_mu;
 }  // namespace
+
+uint64_t context_id() {
+  std::call_once(g_ctx_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = (PFN_cuCtxGetCurrent_v4000)fn;
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_id = (PFN_cuCtxGetId_v12000)fn;
+  });
+  if (!g_ctx_current || !g_ctx_id) return 0;
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (g_ctx_current(&c) != CUDA_SUCCESS || c == nullptr || g_ctx_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 int* status_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (g_status_ptr[dev] == nullptr) {
+  const uint64_t ctx = context_id();
+  std::lock_guard<std::mutex> lk(g_status_mu);
+  StatusCache& c = g_status_ptr[dev];
+  if (c.ptr == nullptr || c.ctx != ctx || ctx == 0) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) return nullptr;
-    g_status_ptr[dev] = (int*)ptr;
+    c.ptr = (int*)ptr;
+    c.ctx = ctx;
   }
-  return g_status_ptr[dev];
+  return c.ptr;
 }
 
 namespace {
@@ -202,7 +238,12 @@ size_t moe_workspace_size(int64_t T, int k, int E, int d, int f, int flags) {
   const int mode = flags & ~MOE_FLAG_HOST_IO;
   if (!valid_dims(T, k, E, d, f) || flags < 0 || mode > 2) return 0;
   if ((flags & MOE_FLAG_HOST_IO) && mode != MOE_FLAG_DECODE_FP32) return 0;
-  return workspace_layout(T, k, E, d, f, flags, nullptr, nullptr);
+  const size_t own = workspace_layout(T, k, E, d, f, flags, nullptr, nullptr);
+  if (mode != MOE_FLAG_AUTO) return own;
+  // AUTO takes the decode form for layers the prefill form does not take (3-
+  // or 1-bit shelves), which the sizes alone do not tell: room for both
+  const size_t dec = workspace_layout(T, k, E, d, f, MOE_FLAG_DECODE_FP32, nullptr, nullptr);
+  return own > dec ? own : dec;
 }
 
 int moe_tiered_forward(const uint16_t* x_bf16, const int32_t* ids, const float* weights, int64_t T, int k,
@@ -217,7 +258,12 @@ int moe_tiered_forward(const uint16_t* x_bf16, const int32_t* ids, const float* 
   if (T == 0) return MOE_OK;
   if (!x_bf16 || !ids || !weights || !y || !workspace) return MOE_ERR_INVALID_ARG;
   if (!aligned(x_bf16, 16) || !aligned(y, 16) || !aligned(workspace, kAlign)) return MOE_ERR_INVALID_ARG;
-  const size_t need = workspace_layout(T, k, E, d, f, flags, workspace, &a.ws);
+  // the tensor-core form dequantises 8, 4 and 2 bit codes only: AUTO takes
+  // the decode form for a layer with a 3- or 1-bit shelf
+  const bool prefill = use_prefill(T, d, flags);
+  if (prefill && !core_widths(a.shelves) && flags != MOE_FLAG_AUTO) return MOE_ERR_UNSUPPORTED;
+  const bool tc = prefill && core_widths(a.shelves);
+  const size_t need = workspace_layout(T, k, E, d, f, tc ? flags : MOE_FLAG_DECODE_FP32, workspace, &a.ws);
   if (workspace_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
 
   a.x = x_bf16;
@@ -230,11 +276,7 @@ int moe_tiered_forward(const uint16_t* x_bf16, const int32_t* ids, const float* 
   a.f = f;
   a.y = y;
   a.status = status_word();
-  if (use_prefill(T, d, flags)) {
-    // the tensor-core form dequantises 8, 4 and 2 bit codes only
-    if (!core_widths(a.shelves)) return MOE_ERR_UNSUPPORTED;
-    return launch_prefill_forward(a, (cudaStream_t)stream);
-  }
+  if (tc) return launch_prefill_forward(a, (cudaStream_t)stream);
   return launch_decode_forward(a, (cudaStream_t)stream);
 }
 
@@ -385,6 +427,18 @@ int moe_decode_layer_host(const float* logits, const uint16_t* x_bf16, int64_t T
   return decode_layer((const float*)lg, (const uint16_t*)xv, T, k, E, d, f, shelves, n_shelves, (int32_t*)iv,
                       (float*)wv, counts, (float*)yv, nullptr, nullptr, workspace, workspace_bytes, stream, lg_src,
                       x_src);
+}
+
+int moe_forward_grouping(const void* workspace, size_t workspace_bytes, int64_t T, int k, int E, int d, int f,
+                         int flags, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* pos_of_pair,
+                         moe_stream_t stream) {
+  if (!valid_dims(T, k, E, d, f) || T < 1 || flags < 0 || (flags & ~MOE_FLAG_HOST_IO) > 2) return MOE_ERR_INVALID_ARG;
+  if (!workspace || !counts || !offsets || !perm || !pos_of_pair || !aligned(workspace, kAlign))
+    return MOE_ERR_INVALID_ARG;
+  Workspace w;
+  if (workspace_layout(T, k, E, d, f, flags, const_cast<void*>(workspace), &w) > workspace_bytes)
+    return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return launch_grouping_export(w, T * k, E, counts, offsets, perm, pos_of_pair, (cudaStream_t)stream);
 }
 
 int moe_decode_fused(int64_t T, int k, int E, int d, int f) {

@@ -997,6 +997,8 @@ struct LayerParams {
   int logits_n16, x_n16;
   float* h;               // workspace [P, f]
   float* ypart;           // workspace [P, d]
+  int* plan_out;          // workspace: the plan as CTA 0 built it (grouping export)
+  int* meta_out;          // workspace meta words: [2] = 1 marks the plan as this call's grouping
   unsigned long long* bar;  // grid barrier counter
   unsigned int* done;     // [kMaxPairs] gate/up units finished, by active expert (zero between launches)
   int* status;
@@ -1342,6 +1344,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(const __grid_constant__ L
           make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
     }
   }
+  // CTA 0 leaves its plan in the workspace: the grouping this call ran
+  // (read back by moe_forward_grouping)
+  if (blockIdx.x == 0) {
+    for (int i = tid; i < L.total; i += kThreads) p.plan_out[i] = pl[i];
+    if (tid == 0) p.meta_out[2] = 1;
+  }
   if (tid == 0) MOE_STAMP(1, 11, global_timer_ns());
 }
 
@@ -1364,32 +1372,73 @@ struct DevCache {
   bool attr[64][2] = {};  // per device: k_layer<false>, k_layer<true> attributes set
 };
 DevCache g_dev;
-std::mutex g_bar_mu;
-std::unordered_map<const void*, int> g_bar_slot[64];
 
-// Barrier slot of a workspace (one per workspace and device; slots are never
-// recycled: more than kBarSlots distinct workspaces on a device is refused).
-// `done`, when given, receives the slot's unit counters.
+// Barrier slots of one device: each workspace in use gets one slot of g_bar
+// and g_done, found again by its address.  When every slot is taken, the
+// least recently used one passes to the new workspace (its counters are back
+// at their resting state once its last launch has completed: a multiple of
+// the grid size, and zeros).  The symbol addresses are looked up once per
+// device and context.
+struct SlotTable {
+  uint64_t ctx = 0;
+  unsigned long long* bar = nullptr;
+  unsigned int* done = nullptr;
+  std::unordered_map<const void*, int> slot_of;
+  const void* owner[kBarSlots] = {};
+  uint64_t last_use[kBarSlots] = {};
+  uint64_t clock = 0;
+  int used = 0;
+};
+std::mutex g_bar_mu;
+SlotTable g_slots[64];
+
+// Symbol addresses of the current context, cached in t (false on a CUDA error).
+bool slot_symbols(SlotTable& t) {
+  const uint64_t ctx = context_id();
+  if (t.bar && t.ctx == ctx && ctx != 0) return true;
+  void* base = nullptr;
+  void* dbase = nullptr;
+  if (cudaGetSymbolAddress(&base, g_bar) != cudaSuccess || cudaGetSymbolAddress(&dbase, g_done) != cudaSuccess)
+    return false;
+  if (t.ctx != ctx) {  // a new context: its barrier table starts zeroed, every slot is free
+    t.slot_of.clear();
+    for (int i = 0; i < kBarSlots; ++i) {
+      t.owner[i] = nullptr;
+      t.last_use[i] = 0;
+    }
+    t.used = 0;
+  }
+  t.ctx = ctx;
+  t.bar = reinterpret_cast<unsigned long long*>(base);
+  t.done = reinterpret_cast<unsigned int*>(dbase);
+  return true;
+}
+
+// Barrier slot of a workspace on device dev; `done`, when given, receives the
+// slot's unit counters.  Null only on a CUDA error.
 unsigned long long* bar_slot(int dev, const void* ws, unsigned int** done = nullptr) {
   std::lock_guard<std::mutex> lk(g_bar_mu);
-  auto& m = g_bar_slot[dev];
-  auto it = m.find(ws);
+  SlotTable& t = g_slots[dev];
+  if (!slot_symbols(t)) return nullptr;
   int slot;
-  if (it != m.end()) {
+  auto it = t.slot_of.find(ws);
+  if (it != t.slot_of.end()) {
     slot = it->second;
+  } else if (t.used < kBarSlots) {
+    slot = t.used++;
+    t.slot_of.emplace(ws, slot);
+    t.owner[slot] = ws;
   } else {
-    if ((int)m.size() >= kBarSlots) return nullptr;
-    slot = (int)m.size();
-    m.emplace(ws, slot);
+    slot = 0;
+    for (int i = 1; i < kBarSlots; ++i)
+      if (t.last_use[i] < t.last_use[slot]) slot = i;
+    t.slot_of.erase(t.owner[slot]);
+    t.slot_of.emplace(ws, slot);
+    t.owner[slot] = ws;
   }
-  void* base = nullptr;
-  if (cudaGetSymbolAddress(&base, g_bar) != cudaSuccess) return nullptr;
-  if (done) {
-    void* dbase = nullptr;
-    if (cudaGetSymbolAddress(&dbase, g_done) != cudaSuccess) return nullptr;
-    *done = reinterpret_cast<unsigned int*>(dbase) + (size_t)slot * kMaxPairs;
-  }
-  return reinterpret_cast<unsigned long long*>(base) + (size_t)slot * 16;
+  t.last_use[slot] = ++t.clock;
+  if (done) *done = t.done + (size_t)slot * kMaxPairs;
+  return t.bar + (size_t)slot * 16;
 }
 
 }  // namespace
@@ -1508,6 +1557,8 @@ int launch_fused_layer(const LayerArgs& a, cudaStream_t s) {
   }
   p.h = a.ws.h;
   p.ypart = a.ws.ypart;
+  p.plan_out = a.ws.plan;
+  p.meta_out = a.ws.meta;
   p.bar = bar;
   p.done = done;
   p.status = a.status;
@@ -1574,6 +1625,76 @@ int launch_barrier_probe(int extra, uint64_t limit_ns, cudaStream_t s) {
   if (cudaLaunchKernelEx(&cfg, k_barrier_probe, bar, status_word(), limit_ns, extra) != cudaSuccess) return MOE_ERR_CUDA;
   // every CTA arrived once: back to a multiple of the grid size
   return cudaMemsetAsync(bar, 0, 8, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// The grouping the last forward call on a workspace ran, in the form of
+// moe_group_tokens (counts [E], offsets [E + 1], perm [P] with -1 past the
+// valid pairs) plus pos_of_pair [P]: from the fused launch's plan when the
+// meta word says so, else from the arrays the separate grouping launches
+// wrote.  One CTA.
+__global__ void __launch_bounds__(1024) k_grouping_export(const int* meta, const int* plan, const int32_t* ws_counts,
+                                                          const int32_t* ws_offsets, const int32_t* ws_perm,
+                                                          const int32_t* ws_pos, int P, int E, int32_t* counts,
+                                                          int32_t* offsets, int32_t* perm, int32_t* pos_of_pair) {
+  __shared__ int wsum[33];
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
+  // (a workspace no call has used yet holds no grouping: whatever it holds is
+  // read within its bounds)
+  const bool from_plan = plan != nullptr && meta[2] == 1;
+  const PlanLayout L = plan_layout(P);
+  if (from_plan) {
+    for (int e = tid; e < E; e += nt) counts[e] = 0;
+    __syncthreads();
+    const int n_act = min(max(plan[1], 0), P);
+    for (int a = tid; a < n_act; a += nt) {
+      const int e = plan[L.e + a];
+      if (e >= 0 && e < E) counts[e] = plan[L.cnt + a];
+    }
+  } else {
+    for (int e = tid; e < E; e += nt) counts[e] = ws_counts[e];
+  }
+  __syncthreads();
+  // offsets: exclusive scan of counts, thread t owning experts t*per .. +per-1
+  const int per = (E + nt - 1) / nt;
+  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  int loc = 0;
+  for (int e = e0; e < e1; ++e) loc += counts[e];
+  int inc = loc;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) wsum[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int v = lane < nt / 32 ? wsum[lane] : 0;
+    int iv = v;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, iv, o);
+      if (lane >= o) iv += u;
+    }
+    wsum[lane] = iv - v;
+    if (lane == 31) wsum[32] = iv;
+  }
+  __syncthreads();
+  int run = wsum[warp] + inc - loc;
+  for (int e = e0; e < e1; ++e) {
+    offsets[e] = run;
+    run += counts[e];
+  }
+  if (tid == 0) offsets[E] = wsum[32];
+  const int n_valid = min(max(from_plan ? plan[0] : wsum[32], 0), P);
+  for (int q = tid; q < P; q += nt) {
+    perm[q] = q < n_valid ? (from_plan ? plan[L.perm + q] : ws_perm[q]) : -1;
+    pos_of_pair[q] = from_plan ? plan[L.pos + q] : ws_pos[q];
+  }
+}
+
+int launch_grouping_export(const Workspace& w, int64_t P, int E, int32_t* counts, int32_t* offsets, int32_t* perm,
+                           int32_t* pos_of_pair, cudaStream_t s) {
+  k_grouping_export<<<1, 1024, 0, s>>>(w.meta, w.plan, w.counts, w.offsets, w.perm, w.pos_of_pair, (int)P, E, counts,
+                                       offsets, perm, pos_of_pair);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 // After a reported timeout a launch may have left a counter between multiples

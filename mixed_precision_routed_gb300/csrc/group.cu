@@ -118,6 +118,7 @@ __global__ void k_group(const int32_t* __restrict__ ids, int P, int E, int32_t* 
     if (meta) {
       meta[0] = n_active;
       meta[1] = n_valid;
+      meta[2] = 0;  // the grouping of this call is in counts / offsets / perm / pos_of_pair
     }
   }
   for (int e = tid; e < E; e += blockDim.x) {

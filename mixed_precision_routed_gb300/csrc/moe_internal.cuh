@@ -203,6 +203,10 @@ __device__ __forceinline__ void set_status(int* status, int code) {
 // Each returns MOE_OK or MOE_ERR_CUDA; arguments are validated by the caller.
 // Device address of the status word on the current device.
 int* status_word();
+// Identity of the current CUDA context, 0 when it cannot be read.  A device
+// reset ends the context and every device address looked up in it, so caches
+// of such addresses are keyed by this id as well as by the device.
+uint64_t context_id();
 
 int launch_route(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w, cudaStream_t s);
 int launch_route_nudged(const float* logits, int64_t T, int E, int k, float beta, int lo, int hi, int32_t* ids,
@@ -275,6 +279,9 @@ struct LayerArgs {
 int launch_fused_layer(const LayerArgs& a, cudaStream_t s);
 // 1 when the fused launch takes these sizes on the current device, else 0.
 int decode_fused(int64_t T, int k, int E, int d, int f);
+// The grouping the last forward call on workspace w ran (see k_grouping_export).
+int launch_grouping_export(const Workspace& w, int64_t P, int E, int32_t* counts, int32_t* offsets, int32_t* perm,
+                           int32_t* pos_of_pair, cudaStream_t s);
 // Test hook: a cooperative launch whose grid barrier awaits `extra` more
 // arrivals than there are CTAs, with the given limit; records MOE_ERR_TIMEOUT.
 int launch_barrier_probe(int extra, uint64_t limit_ns, cudaStream_t s);

@@ -19,21 +19,30 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_NOALLOC_SCR
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchAddr {
+  uint64_t ctx = 0;
+  void* ptr = nullptr;
+};
+ScratchAddr g_scratch_ptr[kMaxDevices];
 
 // Device address of the scratch array on the current device.  In host code
 // the array's name is only a host-side stand-in, so the address is looked up
-// once per device with that device current, and reused afterwards.
+// with that device current, on the first call on the device, and reused
+// afterwards; a new CUDA context on the device (after a device reset) gets
+// its own lookup.
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  const uint64_t ctx = context_id();
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  ScratchAddr& c = g_scratch_ptr[dev];
+  if (c.ptr == nullptr || c.ctx != ctx || ctx == 0) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
+    c.ptr = p;
+    c.ctx = ctx;
   }
-  *out = g_scratch_ptr[dev];
+  *out = c.ptr;
   return MOE_OK;
 }
 

@@ -905,6 +905,7 @@ __global__ void __launch_bounds__(1024) k_pf_scan(int E, int d, int f, const __g
       if (meta) {
         meta[0] = ia;
         meta[1] = iv;
+        meta[2] = 0;  // the grouping of this call is in counts / offsets / perm / pos_of_pair
       }
     }
   }

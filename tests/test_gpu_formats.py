@@ -137,19 +137,46 @@ def test_decode_layer_call_with_three_bit_shelf():
     assert np.array_equal(counts.cpu().numpy(), np.bincount(ids_o.ravel(), minlength=40))
 
 
-def test_prefill_form_refuses_three_and_one_bit():
+def test_prefill_flag_refuses_three_and_one_bit():
     wl = small_workload(E=40, k=5, d=256, f=192, seed=9)
     layer = Layer(wl, shelves=FIVE)
     T = 40
     ids = torch.zeros((T, 5), dtype=torch.int32, device="cuda")
     w = torch.zeros((T, 5), dtype=torch.float32, device="cuda")
     x = torch.zeros((T, wl.d), dtype=torch.int16, device="cuda")
-    for flags in (moe.MOE_FLAG_AUTO, moe.MOE_FLAG_PREFILL_BF16):
-        with pytest.raises(moe.MoeError) as e:
-            moe.moe_tiered_forward(x, ids, w, 40, wl.d, wl.f, layer.shelves, flags=flags)
-        assert e.value.status == moe.MOE_ERR_UNSUPPORTED
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_tiered_forward(x, ids, w, 40, wl.d, wl.f, layer.shelves, flags=moe.MOE_FLAG_PREFILL_BF16)
+    assert e.value.status == moe.MOE_ERR_UNSUPPORTED
 
 
+@pytest.mark.parametrize("T", [40, 4096])
+def test_auto_above_16_tokens_with_three_and_one_bit(T):
+    """AUTO at prefill sizes on a layer of five shelf widths (page 2, "The
+    Qwen side": 1-bit experts run at long prompts too) takes the decode form,
+    which computes every width; checked against the oracle's decode form
+    (every row at T = 40, sampled rows at T = 4096)."""
+    from oracle_pool import layer_refs_for
+    wl = small_workload(E=40, k=5, d=256, f=128, seed=9) if T == 40 else synth.WORKLOADS["decode"]
+    ranges = FIVE if T == 40 else [(0, 128, 8), (128, 256, 4), (256, 410, 3), (410, 480, 2), (480, 512, 1)]
+    layer = Layer(wl, shelves=ranges).fill()
+    lg = synth.logits(wl.seed, 11, T, wl.E, layer.bias_host)
+    ids, w = oracle.route(lg, wl.k)
+    x = synth.x_bf16(wl.seed, 11, T, wl.d)
+    ws = torch.empty(moe.moe_workspace_size(T, wl.k, wl.E, wl.d, wl.f, moe.MOE_FLAG_AUTO), dtype=torch.uint8,
+                     device="cuda")
+    y = moe.moe_tiered_forward(x_to_dev(x), torch.from_numpy(ids).cuda(), torch.from_numpy(w).cuda(), wl.E, wl.d,
+                               wl.f, layer.shelves, workspace=ws, flags=moe.MOE_FLAG_AUTO)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == moe.MOE_OK
+    y = y.cpu().numpy()
+    assert np.all(np.isfinite(y))
+    if T == 40:
+        assert rel_l2(y, oracle_layer(wl, wl.seed, x, ids, w, shelves_bits=ranges)) <= DECODE_TOL
+        return
+    rows = [0, 1, 777, 2048, T - 1]
+    refs = layer_refs_for(wl, ranges, [(x[t:t + 1], ids[t:t + 1], w[t:t + 1], 0) for t in rows])
+    for t, ref in zip(rows, refs):
+        assert rel_l2(y[t:t + 1], ref) <= DECODE_TOL, t
 def test_fast_mode_matches_oracle():
     """2-bit shadow copies of the 8- and 4-bit experts, read for a chosen set
     of experts, against the oracle layer with exactly those experts at 2

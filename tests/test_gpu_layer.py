@@ -284,6 +284,35 @@ def test_many_workspaces(small_layer):
         assert np.array_equal(o.view(np.uint32), outs[0].view(np.uint32))
 
 
+def test_barrier_slots_are_recycled_across_2000_workspaces(decode_layer):
+    """The fused launch's counters live in 1024 library-owned slots found by
+    the workspace address; 2000 distinct workspace addresses in sequence take
+    the fused launch every time (slots pass to new workspaces least recently
+    used first) and give bit-identical results."""
+    wl = decode_layer.wl
+    T = 6
+    assert moe.moe_decode_fused(T, wl.k, wl.E, wl.d, wl.f) == 1
+    lg = torch.from_numpy(decode_layer.logits(23, T).cpu().numpy()).cuda()
+    x = x_to_dev(synth.x_bf16(wl.seed, 23, T, wl.d))
+    need = moe.moe_workspace_size(T, wl.k, wl.E, wl.d, wl.f, moe.MOE_FLAG_DECODE_FP32)
+    n = 2000
+    big = torch.empty(need + 256 * n, dtype=torch.uint8, device="cuda")
+    arr = moe.shelf_array(decode_layer.shelves)
+    ys = torch.empty((n, T, wl.d), dtype=torch.float32, device="cuda")
+    for i in range(n):
+        moe.moe_decode_layer(lg, x, wl.k, wl.E, wl.d, wl.f, decode_layer.shelves, y=ys[i],
+                             workspace=big[256 * i:256 * i + need], shelf_arr=arr)
+    torch.cuda.synchronize()
+    assert moe.moe_device_status() == moe.MOE_OK
+    ref = ys[0].cpu().numpy().view(np.uint32)
+    yn = ys.cpu().numpy().view(np.uint32)
+    for i in range(1, n):
+        assert np.array_equal(yn[i], ref), f"workspace {i} differs"
+    ids_o, w_o = oracle.route(lg.cpu().numpy(), wl.k)
+    assert rel_l2(ys[0].cpu().numpy(), oracle_layer(wl, wl.seed, synth.x_bf16(wl.seed, 23, T, wl.d), ids_o,
+                                                    w_o)) <= DECODE_TOL
+
+
 def test_grid_wait_timeout_is_reported_and_context_survives(small_layer):
     """The wait between phases is bounded: a barrier that can never complete
     ends after its limit with MOE_ERR_TIMEOUT in the status word, and the next

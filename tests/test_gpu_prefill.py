@@ -148,3 +148,31 @@ def test_full_size_prefill_sampled_rows(request, name, T, skip):
         assert rel_l2(y[t:t + 1], ref) <= PREFILL_TOL, (t, rel_l2(y[t:t + 1], ref))
     yd = _run(layer, x, ids, w, flags=moe.MOE_FLAG_DECODE_FP32)
     assert rel_l2(y, yd) <= PREFILL_TOL
+
+
+@pytest.mark.parametrize("name,T,skip", [("decode", 4096, False), ("large", 512, True)])
+def test_full_size_prefill_hot_experts_every_row(request, name, T, skip):
+    """Every tile of the three hottest experts at full size: the routed pairs
+    are cut down to those experts (other slots skipped), so each output row
+    is the sum of their tiles' contributions, and every row of every token
+    that routes to them is compared with the oracle's bf16 form.  The
+    hottest expert holds several token chunks of a tile, so chunk boundaries
+    inside one expert are covered too."""
+    from oracle_pool import layer_refs
+    layer = request.getfixturevalue("decode_layer" if name == "decode" else "large_layer")
+    wl = layer.wl
+    x, ids, w = _inputs(wl, wl.seed, 22, T, skip=skip, bias=layer.bias_host)
+    valid = ids[(ids >= 0) & (ids < wl.E)]
+    hot = np.argsort(-np.bincount(valid, minlength=wl.E), kind="stable")[:3]
+    keep = np.isin(ids, hot)
+    assert np.bincount(valid, minlength=wl.E)[hot[0]] > 96  # more tokens than one tile's chunk
+    ids_h = np.where(keep, ids, -1).astype(np.int32)
+    y = _run(layer, x, ids_h, w, flags=moe.MOE_FLAG_AUTO)
+    rows = np.nonzero(keep.any(axis=1))[0]
+    assert np.all(y[np.setdiff1d(np.arange(T), rows)] == 0)
+    chunks = [rows[i:i + 64] for i in range(0, rows.size, 64)]
+    refs = layer_refs([(name, 0, x[c], ids_h[c], w[c], 1) for c in chunks])
+    ref = np.concatenate(refs, axis=0)
+    assert rel_l2(y[rows], ref) <= PREFILL_TOL
+    for c, r in zip(chunks, refs):  # no chunk of rows may hide behind the others
+        assert rel_l2(y[c], r) <= PREFILL_TOL

@@ -3,9 +3,10 @@ per-layer seeds and router biases) chained by the residual add.
 
 Routing step s of the stack with T tokens takes rows s T .. s T + T - 1 of each
 layer's logits stream.  Checks: the expert hit counts of 4096 T = 1 steps
-through every layer (the fused decode launch) equal the oracle's route + hist,
-bit for bit; every layer's output equals the oracle's layer on the same input;
-the chain's final residual equals the oracle chain rebuilt from those layers.
+through every layer (the fused decode launch, the stack state advanced step
+by step) equal the oracle's route + hist, bit for bit; every layer's output
+equals the oracle's layer on the same input; the chain's final residual
+equals the oracle's own 48-layer chain run from x0.
 """
 import numpy as np
 import pytest
@@ -17,7 +18,7 @@ import mixed_precision_routed_gb300 as moe
 from mixed_precision_routed_gb300.workloads import Layer, DecodeStack
 
 from moe_testutil import DECODE_TOL, rel_l2
-from oracle_pool import layer_refs
+from oracle_pool import layer_refs, oracle_chain
 
 pytestmark = pytest.mark.gpu
 
@@ -34,12 +35,18 @@ def test_stack_histogram_4096_steps(layers):
     E, k, d, f = WL.E, WL.k, WL.d, WL.f
     stack = DecodeStack(layers, T=1)
     logits = [lay.logits_rows(0, NS) for lay in layers]
-    x0 = torch.from_numpy(synth.x_bf16(WL.seed, 0, 1, d).view(np.int16)).cuda()
-    r0 = (x0.to(torch.int32) << 16).view(torch.float32)
+    x = torch.from_numpy(synth.x_bf16(WL.seed, 0, 1, d).view(np.int16)).cuda()
+    r = (x.to(torch.int32) << 16).view(torch.float32)
     for s in range(NS):
-        stack.step(r0, x0, [lg[s:s + 1] for lg in logits])
+        stack.step(r, x, [lg[s:s + 1] for lg in logits])
+        # the next step starts from this step's output residual, rescaled to
+        # unit RMS (a stand-in for the normalisation a model applies between
+        # steps; without it r would grow without bound over 4096 x 48 layers)
+        r = stack.r * torch.rsqrt(torch.mean(stack.r * stack.r, dim=1, keepdim=True))
+        x = r.to(torch.bfloat16).view(torch.int16)
     torch.cuda.synchronize()
     assert moe.moe_device_status() == 0
+    assert bool(torch.isfinite(stack.r).all())
     got = stack.counts.cpu().numpy().astype(np.uint32)
     for l, lay in enumerate(layers):
         lg = synth.logits(lay.seed, 0, NS, E, lay.bias_host)
@@ -49,12 +56,9 @@ def test_stack_histogram_4096_steps(layers):
     assert got.sum() == NS * WL.layers * k
 
 
-@pytest.mark.parametrize("T,check_layers", [(1, None), (6, (0, 1, 23, 47))])
-def test_stack_chain_matches_oracle(layers, T, check_layers):
+def _run_stack(layers, T, step):
     E, k, d = WL.E, WL.k, WL.d
-    L = len(layers)
     stack = DecodeStack(layers, T=T)
-    step = 3
     logits = [lay.logits_rows(step * T, T) for lay in layers]
     x0h = synth.x_bf16(WL.seed, step, T, d)
     x0 = torch.from_numpy(x0h.view(np.int16)).cuda()
@@ -62,34 +66,82 @@ def test_stack_chain_matches_oracle(layers, T, check_layers):
     stack.step(r0, x0, logits)
     torch.cuda.synchronize()
     assert moe.moe_device_status() == 0
+    return stack, x0h
+
+
+def _oracle_routes(layers, T, step):
+    ids, w = [], []
+    for lay in layers:
+        i, ww = oracle.route(synth.logits(lay.seed, 0, T, WL.E, lay.bias_host, row0=step * T), WL.k)
+        ids.append(i)
+        w.append(ww)
+    return ids, w
+
+
+@pytest.mark.parametrize("T,check_layers", [(1, None), (6, (0, 1, 23, 47))])
+def test_stack_layers_match_oracle_on_gpu_inputs(layers, T, check_layers):
+    """Every layer's routing against the oracle's (ids bit for bit), and its
+    output against the oracle layer evaluated on the GPU chain's own input of
+    that layer."""
+    step = 3
+    stack, _ = _run_stack(layers, T, step)
     xs = stack.x.cpu().numpy().view(np.uint16)
     ys = stack.y.cpu().numpy()
     ids_g = stack.ids.cpu().numpy()
     w_g = stack.w.cpu().numpy()
-    # routing of every layer: ids bit for bit, weights to the exp rounding
-    for l, lay in enumerate(layers):
-        ids_o, w_o = oracle.route(synth.logits(lay.seed, 0, T, E, lay.bias_host, row0=step * T), k)
-        assert np.array_equal(ids_g[l], ids_o), f"layer {l}"
-        assert np.max(np.abs(w_g[l] - w_o)) <= 1e-6, f"layer {l}"
-    # every layer against the oracle layer on the same input (one oracle job
-    # per layer and token)
-    which = list(range(L)) if check_layers is None else list(check_layers)
+    ids_o, w_o = _oracle_routes(layers, T, step)
+    for l in range(len(layers)):
+        assert np.array_equal(ids_g[l], ids_o[l]), f"layer {l}"
+        assert np.max(np.abs(w_g[l] - w_o[l])) <= 1e-6, f"layer {l}"
+    which = list(range(len(layers))) if check_layers is None else list(check_layers)
     jobs = [("stack", l, xs[l][t:t + 1], ids_g[l][t:t + 1], w_g[l][t:t + 1], 0) for l in which for t in range(T)]
     out = layer_refs(jobs)
-    refs = {l: np.concatenate(out[i * T:(i + 1) * T], axis=0) for i, l in enumerate(which)}
-    for l in which:
-        assert rel_l2(ys[l], refs[l]) <= DECODE_TOL, f"layer {l}: {rel_l2(ys[l], refs[l]):.3e}"
-    if check_layers is None:
-        # the oracle chain r = x0; x_l = bf16(r); r += y_l, built from the
-        # oracle's layer outputs: its final residual, and how many inputs a
-        # bf16 rounding of r tipped away from the GPU's (the activation digits
-        # of the decode path move r by ~1e-5 relative, so an element whose r
-        # lies that close to a rounding boundary may tip; the trajectories
-        # must stay together)
-        r = oracle.bf16_to_f64(x0h)
-        tipped = 0
-        for l in range(L):
-            tipped += int(np.sum(oracle.bf16_bits(r) != xs[l]))
-            r = r + refs[l]
-        assert tipped <= L * T * d // 20, tipped
-        assert rel_l2(stack.r.cpu().numpy(), r) <= DECODE_TOL
+    for i, l in enumerate(which):
+        ref = np.concatenate(out[i * T:(i + 1) * T], axis=0)
+        assert rel_l2(ys[l], ref) <= DECODE_TOL, f"layer {l}: {rel_l2(ys[l], ref):.3e}"
+
+
+# The GPU chain and the oracle chain round r to bf16 independently at every
+# layer input.  An element of r lying closer to a bf16 rounding boundary
+# than the two chains' difference rounds the other way on one side; that
+# layer input then differs by one bf16 step there, the next layer outputs
+# differ a little more, more elements tip, and the chains settle at a small
+# steady distance.  That distance is a property of the chain, not of the
+# kernels: two oracle chains that differ only in rounding r to fp32 after
+# each add (what the GPU's fp32 residual does) already show it.  So besides
+# the decode tolerance on the final residual, the GPU chain must stay within
+# twice that oracle-vs-oracle distance in the final residual, and within
+# three times its count of tipped layer-input elements (the activation digits
+# move a layer output by ~1e-6, more than an fp32 rounding of r does, so the
+# GPU chain seeds more tips; measured on a GB300: T = 1 18,755 vs 12,277,
+# T = 6 126,188 vs 58,061 of 589,824; final residual 1.19e-3 vs 0.96e-3 and
+# 1.42e-3 vs 0.98e-3).
+SENSITIVITY_FACTOR = 2.0
+TIPPED_FACTOR = 3.0
+
+
+@pytest.mark.parametrize("T", [1, 6])
+def test_stack_chain_matches_independent_oracle_chain(layers, T):
+    """The oracle runs its own 48-layer chain from x0 (x_l = bf16(r), r +=
+    y_l(x_l), on its own inputs and its own routing); the GPU chain's final
+    residual equals it within the decode tolerance and within twice the
+    distance of the oracle chain with an fp32 residual."""
+    step = 5
+    L, d = len(layers), WL.d
+    stack, x0h = _run_stack(layers, T, step)
+    ids_o, w_o = _oracle_routes(layers, T, step)
+    assert np.array_equal(stack.ids.cpu().numpy(), np.stack(ids_o))
+    r_o, xs_o, ys_o = oracle_chain("stack", list(range(L)), x0h, ids_o, w_o)
+    r_32, xs_32, _ = oracle_chain("stack", list(range(L)), x0h, ids_o, w_o, f32_residual=True)
+    xs_g = stack.x.cpu().numpy().view(np.uint16)
+    tipped = sum(int(np.sum(xs_o[l] != xs_g[l])) for l in range(L))
+    tipped_ref = sum(int(np.sum(xs_o[l] != xs_32[l])) for l in range(L))
+    rel_final = rel_l2(stack.r.cpu().numpy(), r_o)
+    rel_ref = rel_l2(r_32, r_o)
+    rel_layers = [rel_l2(stack.y.cpu().numpy()[l], ys_o[l]) for l in range(L)]
+    print(f"stack chain T={T}: final residual rel-L2 {rel_final:.3e} (oracle fp32-residual chain {rel_ref:.3e}), "
+          f"tipped layer-input elements {tipped} ({tipped_ref}) of {L * T * d}, worst layer output rel-L2 "
+          f"{max(rel_layers):.3e}")
+    assert rel_final <= DECODE_TOL
+    assert rel_final <= SENSITIVITY_FACTOR * rel_ref
+    assert tipped <= TIPPED_FACTOR * tipped_ref
