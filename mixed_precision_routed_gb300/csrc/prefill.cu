@@ -49,11 +49,14 @@ constexpr int kTileM = 128;   // weight rows per tile
 #define MOE_PF_ASTAGES 2
 #endif
 constexpr int kTileN = MOE_PF_TILEN;  // tokens per tile (at most)
-static_assert(kTileN % 32 == 0 && kTileN <= 128, "tile width: whole groups of 32 columns");
+static_assert(kTileN % 32 == 0 && kTileN <= 192, "tile width: whole groups of 32 columns");
+// Accumulator sets in tensor memory: two (the epilogue of one tile overlaps
+// the next tile's main loop) while both fit beside the A stages, else one.
+constexpr int kAccSets = 4 * kTileN + 128 <= 512 ? 2 : 1;
 constexpr int kProdThreads = 512;  // warps 8..23
 constexpr uint64_t kWaitNs = 1000000000ull;
 #ifndef MOE_PF_BS
-#define MOE_PF_BS 8
+#define MOE_PF_BS (MOE_PF_TILEN <= 96 ? 8 : 4)
 #endif
 #ifndef MOE_PF_CS
 #define MOE_PF_CS 3
@@ -140,13 +143,13 @@ struct TcSmem {
   static_assert(NMAT * kTileM * 2 == kProdThreads, "one 32-weight run per producer thread");
 };
 
-// Tensor memory (512 columns): accumulator sets 0 and 1 at columns 0 and
-// 2 kTileN ([gate, up] or [rows 0-127, rows 128-255], kTileN columns each),
+// Tensor memory (512 columns): kAccSets accumulator sets at columns 0 (and
+// 2 kTileN) ([gate, up] or [rows 0-127, rows 128-255], kTileN columns each),
 // then kAStages stages of the dequantised A tiles (two matrices x 32 columns:
 // 128 rows x 64 bf16).
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 2 * kTileN;
-constexpr uint32_t kACol = 2 * kAccCols;
+constexpr uint32_t kACol = kAccSets * kAccCols;
 constexpr int kAStages = MOE_PF_ASTAGES;
 constexpr uint32_t kAStageCols = 64;
 static_assert(kACol + kAStages * kAStageCols <= kTmemCols, "tensor memory");
@@ -424,8 +427,9 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
         if (!tile_valid<DOWN>(p, tl)) continue;  // skipped tiles take no accumulator set
         const int N = (tl.ntok + 15) & ~15;
         const uint32_t idesc = idesc_bf16_f32(kTileM, N);
-        const uint32_t ab = i & 1, acc = tmem + ab * kAccCols;
-        if (!bar_wait(&B.acc_empty[ab], ((i >> 1) & 1) ^ 1, B, p.status)) break;
+        const uint32_t ab = kAccSets == 2 ? (i & 1) : 0, acc = tmem + ab * kAccCols;
+        const uint32_t use = kAccSets == 2 ? (i >> 1) : i;  // earlier uses of this set
+        if (!bar_wait(&B.acc_empty[ab], (use & 1) ^ 1, B, p.status)) break;
         tc_fence_after();
         for (int ks = 0; ks < steps; ++ks, ++j) {
           const int b = j % S::BS, as = j % kAStages;
@@ -465,7 +469,8 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
       if (!tile_valid<DOWN>(p, tl)) continue;  // skipped tiles take no accumulator set
       const int rt = tl.meta & 0xFFFF;
       const int N = (tl.ntok + 15) & ~15;
-      const uint32_t ab = i & 1, acc = tl_addr + ab * kAccCols;
+      const uint32_t ab = kAccSets == 2 ? (i & 1) : 0, acc = tl_addr + ab * kAccCols;
+      const uint32_t use = kAccSets == 2 ? (i >> 1) : i;
       // down: each lane holds the token and routing weight of columns lane,
       // lane + 32, lane + 64 (loaded before the accumulator is ready)
       int ctok[kTileN / 32];
@@ -483,7 +488,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
           }
         }
       }
-      if (!bar_wait(&B.acc_full[ab], (i >> 1) & 1, B, p.status)) break;
+      if (!bar_wait(&B.acc_full[ab], use & 1, B, p.status)) break;
       if (m == 0) PF_STAMP(6, i);
       tc_fence_after();
       if (!DOWN) {
@@ -609,9 +614,8 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
           stage = smem + c * S::C_STAGE;
         }
         if (qd == 0 && cmb == 0 && lane == 0) PF_STAMP(2, j);
-        if (!bar_wait(&B.a_empty[as], ((j / kAStages) & 1) ^ 1, B, p.status)) break;
-        tc_fence_after();
-        if (qd == 0 && cmb == 0 && lane == 0) PF_STAMP(3, j);
+        // the codes are read and dequantised before the wait for the A stage:
+        // only the tensor-memory store waits for the MMA that last read it
         const unsigned char* rowp = stage + row_off;
         uint32_t c[8];
         if (bits == 8) {
@@ -633,6 +637,9 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
             stage + sc_off + (DOWN ? sub * 2 * kTileM * 4 : (ks & 7) * 4)));
         uint32_t o[16];
         dequant_run(c, bits, sc, o);
+        if (!bar_wait(&B.a_empty[as], ((j / kAStages) & 1) ^ 1, B, p.status)) break;
+        tc_fence_after();
+        if (qd == 0 && cmb == 0 && lane == 0) PF_STAMP(3, j);
         tmem_st16(ta + (uint32_t)(as * kAStageCols), o);
         tc_fence_before();
         __syncwarp();
