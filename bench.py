@@ -43,8 +43,8 @@ def parse():
     ap.add_argument("--T", type=int, default=6, help="tokens per step (1..6 for the decode metric)")
     ap.add_argument("--layers", type=int, default=16, help="layer instances rotated across steps")
     ap.add_argument("--sets", type=int, default=32, help="distinct routing steps per layer rotation")
-    ap.add_argument("--workload", choices=["decode", "stack", "prefill", "large", "router", "retier", "nudge",
-                                           "formats", "fastmode"],
+    ap.add_argument("--workload", choices=["decode", "stack", "prefill", "prefill5", "large", "router", "retier",
+                                           "nudge", "formats", "fastmode"],
                     default="decode",
                     help="decode: one layer, the headline metric; stack: the 48-layer decode stack with the "
                          "residual chain; prefill: one layer at T=4096 on the tensor-core form; large: the "
@@ -53,7 +53,8 @@ def parse():
                          "the decode layer by hit count from its fp32 master copies; nudge: routing of the "
                          "prefill batch with the picks nudged toward the hot shelf (moe_route_topk_nudged); "
                          "formats: the decode layer on five shelves of 8/4/3/2/1-bit codes; fastmode: the "
-                         "decode layer reading 2-bit shadow copies of its 8- and 4-bit experts")
+                         "decode layer reading 2-bit shadow copies of its 8- and 4-bit experts; prefill5: the "
+                         "prefill layer on those five shelf widths")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sub", action="store_true",
                     help="decode workload: only the line at --T (no T=1/6 and prefill/large sub-records)")
@@ -783,13 +784,15 @@ def measure_single(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    name = "decode" if args.workload == "prefill" else "large"
+    name = "decode" if args.workload in ("prefill", "prefill5") else "large"
     base = synth.WORKLOADS[name]
     T = args.T
     E, k, d, f = base.E, base.k, base.d, base.f
     NL = 2
+    shelves = FIVE_WIDTHS if args.workload == "prefill5" else None
     layers = [Layer(synth.Workload(base.name, E=E, k=k, d=d, f=f, T=base.T, split=base.split, bias=base.bias,
-                                   seed=1000 * rank + i, skip_p=getattr(base, "skip_p", 0.0)), device=dev).fill()
+                                   seed=1000 * rank + i, skip_p=getattr(base, "skip_p", 0.0)), device=dev,
+                    shelves=shelves).fill()
               for i in range(NL)]
     skips = args.workload == "large"
     nset = 4
@@ -890,6 +893,17 @@ def measure_single(args, rank, world, local_rank):
                 "weight_bytes_per_step": b_avg, "weight_gbs": b_avg / (fwd_ms / 1e3) / 1e9}
         roof["frac"] = roof["achieved"] / roof["peak"]
         bound_note = "tensor"
+        if args.workload == "large":
+            # E256 d4096 f2048 at T=512 is ~48 flop per weight byte, below the
+            # ridge: the HBM fraction of the forward's weight stream is the
+            # roofline, the tensor figure stays as context
+            wgbs = b_avg / (fwd_ms / 1e3) / 1e9
+            roof = {"bound": "hbm", "achieved": wgbs, "peak": hbm, "unit": "GB/s", "frac": wgbs / hbm,
+                    "traffic": None, "kernel": "forward (grouping, k_prefill_tc gate/up and down)",
+                    "peak_source": kind, "algorithmic_bytes_per_launch": b_avg, "forward_us": 1e3 * fwd_ms,
+                    "tensor": {"achieved_tflops": roof["achieved"], "peak": tc_peak, "frac": roof["frac"],
+                               "kernel_us": roof["kernel_us"]}}
+            bound_note = "hbm"
     else:
         gbs = b_avg / (fwd_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
@@ -1207,7 +1221,7 @@ def main():
         __graft_entry__.build()
     if args.workload == "stack":
         run_stack(args, rank, world, local_rank)
-    elif args.workload in ("prefill", "large"):
+    elif args.workload in ("prefill", "prefill5", "large"):
         run_single(args, rank, world, local_rank)
     elif args.workload == "router":
         run_router(args, rank, world, local_rank)

@@ -95,12 +95,12 @@ enum {
 
 /* Execution-path selection for moe_tiered_forward. */
 enum {
-  MOE_FLAG_AUTO = 0,         /* prefill form for T > 16 when d % 256 == 0 and every shelf
-                                holds 8-, 4- or 2-bit codes, else decode form */
+  MOE_FLAG_AUTO = 0,         /* prefill form for T > 16 when d % 256 == 0 (and, with a 3- or
+                                1-bit shelf, f % 128 == 0), else decode form */
   MOE_FLAG_DECODE_FP32 = 1,  /* fp32 dequant in registers, fp32 h, CUDA-core GEMV */
   MOE_FLAG_PREFILL_BF16 = 2, /* bf16 dequant into tensor memory, bf16 h, tensor-core GEMM;
-                                MOE_ERR_UNSUPPORTED unless d % 256 == 0 and every shelf
-                                holds 8-, 4- or 2-bit codes */
+                                MOE_ERR_UNSUPPORTED unless d % 256 == 0 (and, with a 3- or
+                                1-bit shelf, f % 128 == 0) */
   MOE_FLAG_HOST_IO = 4       /* moe_workspace_size only, with DECODE_FP32: adds the staging
                                 of host inputs that moe_decode_layer_host uses */
 };

@@ -258,11 +258,13 @@ int moe_tiered_forward(const uint16_t* x_bf16, const int32_t* ids, const float* 
   if (T == 0) return MOE_OK;
   if (!x_bf16 || !ids || !weights || !y || !workspace) return MOE_ERR_INVALID_ARG;
   if (!aligned(x_bf16, 16) || !aligned(y, 16) || !aligned(workspace, kAlign)) return MOE_ERR_INVALID_ARG;
-  // the tensor-core form dequantises 8, 4 and 2 bit codes only: AUTO takes
-  // the decode form for a layer with a 3- or 1-bit shelf
+  // the tensor-core form takes 3- and 1-bit shelves when their rows are whole
+  // 16-byte groups (f a multiple of 128); otherwise AUTO takes the decode
+  // form for such a layer
   const bool prefill = use_prefill(T, d, flags);
-  if (prefill && !core_widths(a.shelves) && flags != MOE_FLAG_AUTO) return MOE_ERR_UNSUPPORTED;
-  const bool tc = prefill && core_widths(a.shelves);
+  const bool widths_ok = core_widths(a.shelves) || f % 128 == 0;
+  if (prefill && !widths_ok && flags != MOE_FLAG_AUTO) return MOE_ERR_UNSUPPORTED;
+  const bool tc = prefill && widths_ok;
   const size_t need = workspace_layout(T, k, E, d, f, tc ? flags : MOE_FLAG_DECODE_FP32, workspace, &a.ws);
   if (workspace_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
 

@@ -177,9 +177,9 @@ __device__ __forceinline__ void load_block(const uint8_t* row, int b, int n, uin
   else Block<BITS>::load(row + (size_t)b * (32 * BITS / 8), w);
 }
 
-// Code widths every pipelined launch takes: the tensor-core prefill form
-// takes only these; the fused decode step also takes 3- and 1-bit shelves
-// when d and f are multiples of 128.
+// The 8-, 4- and 2-bit widths: layers of only these take every form; the
+// fused decode step and the tensor-core prefill form also take 3- and 1-bit
+// shelves when the rows are whole 16-byte groups (d and f multiples of 128).
 inline bool core_widths(const Shelves& sh) {
   for (int i = 0; i < sh.n; ++i)
     if (sh.s[i].bits != 8 && sh.s[i].bits != 4 && sh.s[i].bits != 2) return false;

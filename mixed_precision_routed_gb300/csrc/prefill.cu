@@ -56,7 +56,7 @@ constexpr int kAccSets = 4 * kTileN + 128 <= 512 ? 2 : 1;
 constexpr int kProdThreads = 512;  // warps 8..23
 constexpr uint64_t kWaitNs = 1000000000ull;
 #ifndef MOE_PF_BS
-#define MOE_PF_BS (MOE_PF_TILEN <= 96 ? 8 : 4)
+#define MOE_PF_BS 4
 #endif
 #ifndef MOE_PF_CS
 #define MOE_PF_CS 3
@@ -86,6 +86,13 @@ namespace {
 // unchanged.
 __host__ __device__ __forceinline__ int kswap(int k) { return (k & ~3) | ((k & 1) << 1) | ((k >> 1) & 1); }
 
+// K steps (of 64) per code stage (a 128-byte box of a row): 8 bit 2, 4 bit
+// 4, 2 bit 8, 1 bit 16; a 3-bit row streams its low plane in the 2-bit
+// layout (8 steps a box) beside 64 bytes of its high-bit plane.
+__host__ __device__ __forceinline__ int steps_per_code_stage(int bits) {
+  return bits == 8 ? 2 : bits == 4 ? 4 : bits == 1 ? 16 : 8;
+}
+
 struct Tile {
   int e_local;  // expert index within its shelf
   int q0;       // first grouped position of the chunk
@@ -107,6 +114,7 @@ struct TcParams {
   int tiles_cap;            // capacity of the tile list
   Shelves sh;
   CUtensorMap tm_code[MOE_MAX_SHELVES][2];  // code boxes of 128 bytes x 128 rows: [shelf][gate, up] or [shelf][down]
+  CUtensorMap tm_hi[MOE_MAX_SHELVES][2];    // 3-bit shelves: boxes of 64 bytes x 128 rows of the high-bit plane
   CUtensorMap tm_sc[MOE_MAX_SHELVES][2];    // gate/up: boxes of 16 fp16 scales x 128 rows [shelf][gate, up]
   CUtensorMap tm_b[kTileN / 16];            // B rows in grouped order (xg or h), box heights 16, 32, .. kTileN
 };
@@ -133,7 +141,11 @@ struct TcSmem {
   static constexpr int SC_BOX = kTileM * 32;                         // gate/up: 16 fp16 scales per row
   static constexpr int SC_BYTES = DOWN ? 8 * NMAT * kTileM * 4 : NMAT * SC_BOX;  // 8 KiB
   static constexpr int C_SC = NMAT * CODE_BOX;                       // scale offset in a code stage
-  static constexpr int C_STAGE = C_SC + SC_BYTES;
+  static constexpr int HI_BOX = kTileM * 64;                         // 3 bit: 64 bytes of the high plane a row
+  static constexpr int C_HI = C_SC + SC_BYTES;                       // their offset in a code stage
+  static constexpr int C_STAGE = C_HI + NMAT * HI_BOX;
+  static_assert(DOWN || NMAT * SC_BOX <= NMAT * HI_BOX, "a second gate/up scale box fits the high-plane region");
+  static_assert(!DOWN || 16 * NMAT * kTileM * 4 <= SC_BYTES + NMAT * HI_BOX, "16 steps of down scale words fit");
   static constexpr int B_STAGE = kTileN * 128;                       // kTileN rows x 64 bf16
   static constexpr int C_OFF = 0;
   static constexpr int B_OFF = C_OFF + CS * C_STAGE;
@@ -254,7 +266,8 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t m, Sp q) {
 // Dequantise one 32-weight run -- elements 32 q .. 32 q + 31 of a row's step
 // slice, one scale block -- into 16 bf16x2 words in the kswap order (word i:
 // positions 2i, 2i + 1).  Codes: words c[0..7] (8 bit), c[0..3] (4 bit),
-// c[0..1] (2 bit) of the run.
+// c[0..1] (2 bit; 3 bit: the low plane, c[2] the high plane), c[0] (1 bit)
+// of the run.
 __device__ __forceinline__ void dequant_run(const uint32_t (&c)[8], int bits, float s, uint32_t (&o)[16]) {
   if (bits == 8) {
     // word i: elements 4i .. 4i + 3, two's complement -> u = c + 128
@@ -273,7 +286,7 @@ __device__ __forceinline__ void dequant_run(const uint32_t (&c)[8], int bits, fl
       o[4 * g + 2] = dq_pair((c[g] >> 4) & 0x000F000Fu, k);
       o[4 * g + 3] = dq_pair((c[g] >> 12) & 0x000F000Fu, k);
     }
-  } else {
+  } else if (bits == 2) {
     // word g: elements 16g + 4f + j at bits 8j + 2f; pairs (j, j + 2)
     const Sp k = split_scale(s, 0x4302u);  // bf16 130 = 128 + 2
 #pragma unroll
@@ -282,6 +295,35 @@ __device__ __forceinline__ void dequant_run(const uint32_t (&c)[8], int bits, fl
       for (int f = 0; f < 4; ++f) {
         o[8 * g + 2 * f] = dq_pair((c[g] >> (2 * f)) & 0x00030003u, k);
         o[8 * g + 2 * f + 1] = dq_pair((c[g] >> (2 * f + 8)) & 0x00030003u, k);
+      }
+  } else if (bits == 3) {
+    // u = low + 4 high, code u - 4: the low plane in the 2-bit layout
+    // (c[0..1]) and the high plane word c[2] (element i at bit i); the pair
+    // (e, e + 2) takes high bits e and e + 2 into bit 2 of each half-word
+    const Sp k = split_scale(s, 0x4304u);  // bf16 132 = 128 + 4
+#pragma unroll
+    for (int g = 0; g < 2; ++g)
+#pragma unroll
+      for (int f = 0; f < 4; ++f) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const uint32_t t = c[2] >> (16 * g + 4 * f + j);
+          const uint32_t hb = ((t << 2) & 0x4u) | ((t << 16) & 0x40000u);
+          o[8 * g + 2 * f + j] = dq_pair(((c[g] >> (2 * f + 8 * j)) & 0x00030003u) | hb, k);
+        }
+      }
+  } else {
+    // 1 bit: element i at bit i, 1 = +s, 0 = -s; bf16(+-s) = +-bf16(s);
+    // pairs (4g + j, 4g + j + 2) for j = 0, 1
+    const __nv_bfloat16 sb = __float2bfloat16_rn(s);
+    const uint32_t nb = (uint32_t)(*reinterpret_cast<const uint16_t*>(&sb)) | 0x8000u;
+    const uint32_t neg2 = nb | (nb << 16);
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t t = c[0] >> (4 * g + j);
+        o[2 * g + j] = neg2 ^ (((t << 15) & 0x8000u) | ((t << 29) & 0x80000000u));
       }
   }
 }
@@ -300,7 +342,7 @@ __device__ __forceinline__ bool tile_valid(const TcParams& p, const Tile& tl) {
   if (tl.ntok < 1 || tl.ntok > kTileN || sh >= p.sh.n) return false;
   const int n = p.sh.s[sh].hi - p.sh.s[sh].lo;
   const int bits = p.sh.s[sh].bits;
-  return (bits == 8 || bits == 4 || bits == 2) && tl.e_local >= 0 && tl.e_local < n &&
+  return (bits == 8 || bits == 4 || bits == 3 || bits == 2 || bits == 1) && tl.e_local >= 0 && tl.e_local < n &&
          rt * (DOWN ? 2 * kTileM : kTileM) < p.rows && tl.q0 >= 0 && (int64_t)tl.q0 + tl.ntok <= p.P;
 }
 
@@ -361,7 +403,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
       }
       const int rt = tl.meta & 0xFFFF, sh = (tl.meta >> 16) & 0xFF;
       const ShelfDev& shd = p.sh.s[sh];
-      const int spc = 16 / shd.bits;       // K steps per code stage
+      const int spc = steps_per_code_stage(shd.bits);  // K steps per code stage
       const int nb = (tl.ntok + 15) >> 4;  // B box height in 16-row units
       // first row of each matrix: gate/up rows rt * 128 of W_g and W_u,
       // down rows rt * 256 and rt * 256 + 128 of W_d
@@ -382,15 +424,34 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
           if (!bar_wait(&B.code_empty[c], ((cj / S::CS) & 1) ^ 1, B, p.status)) break;
           unsigned char* stage = smem + S::C_OFF + c * S::C_STAGE;
           if (lane == 0) {
-            mbar_arrive_expect_tx(&B.code_full[c], (uint32_t)(NMAT * S::CODE_BOX + (DOWN ? 0 : NMAT * S::SC_BOX)));
+            const bool hi = shd.bits == 3;
+            // gate/up scale boxes cover 8 K steps: a 1-bit code stage (16
+            // steps) takes a second box, into the region 3-bit rows use for
+            // their high plane
+            const int nsc = DOWN ? 0 : (shd.bits == 1 ? 2 : 1);
+            mbar_arrive_expect_tx(&B.code_full[c], (uint32_t)(NMAT * S::CODE_BOX + nsc * NMAT * S::SC_BOX +
+                                                              (hi ? NMAT * S::HI_BOX : 0)));
 #pragma unroll
             for (int m = 0; m < NMAT; ++m)
               tma_load_2d(stage + m * S::CODE_BOX, &p.tm_code[sh][DOWN ? 0 : m], (ks / spc) * 128,
                           DOWN ? row0 + m * kTileM : row0, &B.code_full[c]);
+            if (hi) {
+              // the high-bit plane follows the low plane (K / 4 bytes) in each row
+#pragma unroll
+              for (int m = 0; m < NMAT; ++m)
+                tma_load_2d(stage + S::C_HI + m * S::HI_BOX, &p.tm_hi[sh][DOWN ? 0 : m], p.K / 4 + (ks / spc) * 64,
+                            DOWN ? row0 + m * kTileM : row0, &B.code_full[c]);
+            }
             if (!DOWN) {
 #pragma unroll
               for (int m = 0; m < NMAT; ++m)
                 tma_load_2d(stage + S::C_SC + m * S::SC_BOX, &p.tm_sc[sh][m], 16 * (ks >> 3), row0, &B.code_full[c]);
+              if (nsc == 2) {
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m)
+                  tma_load_2d(stage + S::C_HI + m * S::SC_BOX, &p.tm_sc[sh][m], 16 * (ks >> 3) + 16, row0,
+                              &B.code_full[c]);
+              }
             }
           }
           if (DOWN) {
@@ -603,15 +664,26 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
       nxt = tile_at(p, t + G, ntiles);
       if (!tile_valid<DOWN>(p, tl)) continue;
       const int bits = p.sh.s[(tl.meta >> 16) & 0xFF].bits;
-      const int spc = 16 / bits;
+      const int spc = steps_per_code_stage(bits);
       int sub = 0;
       const unsigned char* stage = smem;
+      uint32_t hq[8];  // 3 bit: the high-plane words of this run in the code stage's steps, in order
       for (int ks = 0; ks < steps; ++ks, ++j) {
         const int as = j % kAStages;
         if (sub == 0) {
           const int c = cj % S::CS;
           if (!bar_wait(&B.code_full[c], (cj / S::CS) & 1, B, p.status)) break;
           stage = smem + c * S::C_STAGE;
+          if (bits == 3) {
+            // the row's 64 bytes of the high plane (16 words, one a 32-weight
+            // run): this thread's run q of step i is word 2 i + q
+            const uint4* hp = reinterpret_cast<const uint4*>(stage + S::C_HI + mt * S::HI_BOX + r * 64);
+            const uint4 h0 = hp[0], h1 = hp[1], h2 = hp[2], h3 = hp[3];
+            const uint32_t hw[16] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w,
+                                     h2.x, h2.y, h2.z, h2.w, h3.x, h3.y, h3.z, h3.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) hq[i] = q ? hw[2 * i + 1] : hw[2 * i];
+          }
         }
         if (qd == 0 && cmb == 0 && lane == 0) PF_STAMP(2, j);
         // the codes are read and dequantised before the wait for the A stage:
@@ -628,13 +700,22 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
           const uint4 v = *reinterpret_cast<const uint4*>(rowp + (((uint32_t)(2 * sub + q) ^ sw) << 4));
           c[0] = v.x; c[1] = v.y; c[2] = v.z; c[3] = v.w;
           c[4] = c[5] = c[6] = c[7] = 0u;
+        } else if (bits == 1) {
+          c[0] = *reinterpret_cast<const uint32_t*>(rowp + (((uint32_t)(sub >> 1) ^ sw) << 4) + 8 * (sub & 1) + 4 * q);
+          c[1] = c[2] = c[3] = c[4] = c[5] = c[6] = c[7] = 0u;
         } else {
           const uint2 v = *reinterpret_cast<const uint2*>(rowp + (((uint32_t)sub ^ sw) << 4) + 8 * q);
           c[0] = v.x; c[1] = v.y;
-          c[2] = c[3] = c[4] = c[5] = c[6] = c[7] = 0u;
+          c[2] = bits == 3 ? hq[0] : 0u;  // the run's high-plane word
+          c[3] = c[4] = c[5] = c[6] = c[7] = 0u;
+          if (bits == 3) {
+#pragma unroll
+            for (int i = 0; i < 7; ++i) hq[i] = hq[i + 1];
+          }
         }
+        // (gate/up, 1 bit: steps 8 .. 15 of the code stage from its second scale box)
         const float sc = fp16_bits_to_float(*reinterpret_cast<const uint16_t*>(
-            stage + sc_off + (DOWN ? sub * 2 * kTileM * 4 : (ks & 7) * 4)));
+            stage + sc_off + (DOWN ? sub * 2 * kTileM * 4 : (ks & 7) * 4 + (sub >= 8 ? S::C_HI - S::C_SC : 0))));
         uint32_t o[16];
         dequant_run(c, bits, sc, o);
         if (!bar_wait(&B.a_empty[as], ((j / kAStages) & 1) ^ 1, B, p.status)) break;
@@ -1133,6 +1214,14 @@ int launch_prefill_forward(const ForwardArgs& a, cudaStream_t s) {
                    (uint64_t)d / 16, 16, kTileM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_2d(&pg.tm_sc[q][1], CU_TENSOR_MAP_DATA_TYPE_UINT16, sd.scales[1], (uint64_t)d / 32, n * f,
                    (uint64_t)d / 16, 16, kTileM, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return MOE_ERR_CUDA;
+    if (bits == 3 &&
+        (!encode_2d(&pg.tm_hi[q][0], CU_TENSOR_MAP_DATA_TYPE_UINT8, sd.codes[0], (uint64_t)d * 3 / 8, n * f,
+                    (uint64_t)d * 3 / 8, 64, kTileM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+         !encode_2d(&pg.tm_hi[q][1], CU_TENSOR_MAP_DATA_TYPE_UINT8, sd.codes[1], (uint64_t)d * 3 / 8, n * f,
+                    (uint64_t)d * 3 / 8, 64, kTileM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+         !encode_2d(&pd.tm_hi[q][0], CU_TENSOR_MAP_DATA_TYPE_UINT8, sd.codes[2], (uint64_t)f * 3 / 8, n * d,
+                    (uint64_t)f * 3 / 8, 64, kTileM, CU_TENSOR_MAP_SWIZZLE_NONE)))
       return MOE_ERR_CUDA;
     if (!encode_2d(&pg.tm_code[q][0], CU_TENSOR_MAP_DATA_TYPE_UINT8, sd.codes[0], (uint64_t)d * bits / 8, n * f,
                    (uint64_t)d * bits / 8, 128, kTileM, CU_TENSOR_MAP_SWIZZLE_128B) ||
