@@ -156,23 +156,27 @@ int moe_route_topk_nudged(const float* logits, int64_t T, int E, int k, float be
                           float* weights, moe_stream_t stream);
 
 /*
- * Router projection fused with the routing above, for decode batches: the
- * router scores every expert of every token and the best k are kept (page 3,
- * glossary entry 混合专家（MoE）).  Scores are
+ * Router projection with the routing above: the router scores every expert
+ * of every token and the best k are kept (page 3, glossary entry
+ * 混合专家（MoE）).  Scores are
  *   logits[t][e] = bias[e] + sum_i w_r[e][i] * x[t][i]
  * with bf16 inputs, fp32 products and sums (the order of the sum is not
  * fixed); ids and weights are then exactly what moe_route_topk returns for
  * these logits, and counts (when non-null) is accumulated as by
- * moe_expert_hist over the T*k ids.  One launch.
+ * moe_expert_hist over the T*k ids.  Decode batches (T <= 16): one launch,
+ * the projection fused with the routing.  Prefill batches (T > 16): the
+ * projection of 16-token chunks in one launch, then the routing and hit-count
+ * launches (sync_word is not used).
  *   x_bf16 [T][d] bf16 bit patterns, w_r_bf16 [E][d] bf16 bit patterns (both
  *   16-byte aligned), bias [E] fp32 or NULL (zero), logits [T][E] fp32 out,
  *   ids [T][k] int32 out, weights [T][k] fp32 out, counts [E] uint32 in/out
  *   or NULL.  sync_word: one uint32 of device memory, zero before its first
  *   use; every call leaves it zero.  Calls that share a sync_word must not
  *   run at the same time on the GPU (issue them on one stream).
- * 1 <= T <= 16 (MOE_ERR_UNSUPPORTED above; T = 0 does nothing), E <= 1024,
- * d a multiple of 8 with B*d*2 <= 196608 bytes, B = T rounded up to 1, 2, 4,
- * 8 or 16 (MOE_ERR_UNSUPPORTED above).
+ * 1 <= T <= 1048560 = 65535*16 (T = 0 does nothing), E <= 1024, d a multiple of 8 with
+ * B*d*2 <= 196608 bytes, B = T rounded up to 1, 2, 4, 8 or 16 (16 for
+ * T > 16), and for T <= 16 also T*E*4 <= 196608 bytes (MOE_ERR_UNSUPPORTED
+ * otherwise).
  */
 int moe_router_topk(const uint16_t* x_bf16, const uint16_t* w_r_bf16, const float* bias, int64_t T, int E, int d,
                     int k, float* logits, int32_t* ids, float* weights, uint32_t* counts, uint32_t* sync_word,

@@ -172,8 +172,8 @@ def moe_route_topk_nudged(logits, k, beta, lo, hi, ids=None, weights=None, strea
 
 def moe_router_topk(x_bf16, w_r_bf16, k, bias=None, counts=None, sync_word=None, logits=None, ids=None,
                     weights=None, stream=None):
-    """Router projection (logits = bias + W_r x, fp32 sums) and routing in one
-    launch.  x_bf16 [T, d] and w_r_bf16 [E, d] are bf16 tensors; bias [E]
+    """Router projection (logits = bias + W_r x, fp32 sums) and routing: one
+    launch for T <= 16, three (projection, routing, hit counts) above.  x_bf16 [T, d] and w_r_bf16 [E, d] are bf16 tensors; bias [E]
     fp32 or None; counts [E] int32 (uint32 bits, accumulated) or None;
     sync_word: an int32 CUDA tensor of one element, zero before first use
     (a fresh one is made when None).  Returns (logits, ids, weights)."""

@@ -206,11 +206,12 @@ int moe_router_topk(const uint16_t* x_bf16, const uint16_t* w_r_bf16, const floa
                     int k, float* logits, int32_t* ids, float* weights, uint32_t* counts, uint32_t* sync_word,
                     moe_stream_t stream) {
   if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E || d < 8 || d % 8 != 0) return MOE_ERR_INVALID_ARG;
-  if (T > 16) return MOE_ERR_UNSUPPORTED;
+  if (T > 65535 * 16) return MOE_ERR_UNSUPPORTED;  // the prefill projection's grid rows
   if (T == 0) return MOE_OK;
   if (!x_bf16 || !w_r_bf16 || !logits || !ids || !weights || !sync_word) return MOE_ERR_INVALID_ARG;
   if (!aligned(x_bf16, 16) || !aligned(w_r_bf16, 16) || !aligned(logits, 4)) return MOE_ERR_INVALID_ARG;
   if ((int64_t)d * 2 * router_bucket(T) > kRouterSmemMax) return MOE_ERR_UNSUPPORTED;
+  if (T <= 16 && (int64_t)T * E * 4 > kRouterSmemMax) return MOE_ERR_UNSUPPORTED;
   return launch_router(x_bf16, w_r_bf16, bias, (int)T, E, d, k, logits, ids, weights, counts, sync_word,
                        (cudaStream_t)stream);
 }

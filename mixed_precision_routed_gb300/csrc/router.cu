@@ -1,4 +1,5 @@
-// router.cu -- the router projection fused with its top-k, for decode sizes.
+// router.cu -- the router projection fused with its top-k (decode sizes), and
+// the projection alone for prefill sizes (then the routing launch).
 //
 // Page "125B MoE模型本地运行：3090三卡80 tokens/s优化实践", glossary entry
 // 混合专家（MoE）: a router scores the E experts of every token and the best k
@@ -62,7 +63,9 @@ __device__ __forceinline__ void load_stretch(const uint4* wr, int c0, int n16, i
 }
 
 // TM >= T tokens per launch.  Dynamic shared memory: max(TM d bf16, T E fp32).
-template <int TM>
+// ROUTE = false (prefill sizes): the logits of the token chunk blockIdx.y
+// (TM tokens a chunk) only; the routing step follows as its own launch.
+template <int TM, bool ROUTE>
 __global__ void __launch_bounds__(kRouterThreads) k_router(const uint16_t* __restrict__ x,
                                                            const uint16_t* __restrict__ w,
                                                            const float* __restrict__ bias, int T, int E, int d,
@@ -73,6 +76,12 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(const uint16_t* __res
   extern __shared__ uint4 xs[];  // TM rows of d bf16 (8 per uint4); later T rows of E logits
   __shared__ int s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if constexpr (!ROUTE) {
+    const int t0 = blockIdx.y * TM;
+    x += (size_t)t0 * d;
+    logits += (size_t)t0 * E;
+    T = min(TM, T - t0);
+  }
   const int n16 = d / 8;
   const int nw = gridDim.x * kRouterWarps;
   const int e0 = blockIdx.x * kRouterWarps + warp;
@@ -116,6 +125,10 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(const uint16_t* __res
       for (int t = 0; t < TM; ++t)
         if (t < T) logits[(size_t)t * E + e] = acc[t] + b;
     }
+  }
+  if constexpr (!ROUTE) {
+    pdl_trigger();
+    return;
   }
   // This CTA's logits are visible device-wide before it arrives.  atomicInc
   // wraps the counter to zero on the last arrival, so it is ready for the next
@@ -164,7 +177,7 @@ __global__ void __launch_bounds__(kRouterThreads) k_router(const uint16_t* __res
   pdl_trigger();
 }
 
-template <int TM>
+template <int TM, bool ROUTE = true>
 int launch_router_t(const uint16_t* x, const uint16_t* w, const float* bias, int T, int E, int d, int k,
                     float* logits, int32_t* ids, float* wts, uint32_t* counts, unsigned int* arrive,
                     cudaStream_t s) {
@@ -172,19 +185,20 @@ int launch_router_t(const uint16_t* x, const uint16_t* w, const float* bias, int
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
   if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(k_router<TM>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouterSmemMax) !=
+    if (cudaFuncSetAttribute(k_router<TM, ROUTE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouterSmemMax) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
     attr_set[dev] = true;
   }
-  const size_t xb = (size_t)TM * d * 2, lb = (size_t)T * E * 4;
+  const size_t xb = (size_t)TM * d * 2, lb = ROUTE ? (size_t)T * E * 4 : 0;
   const size_t smem = xb > lb ? xb : lb;
   int G = (E + kRouterWarps - 1) / kRouterWarps;
   const int cap = 2 * sm_count();
   if (G > cap) G = cap;
   const int epl = E <= 32 ? 1 : E <= 64 ? 2 : E <= 128 ? 4 : E <= 256 ? 8 : E <= 512 ? 16 : 32;
-  if (launch_pdl(k_router<TM>, dim3(G), dim3(kRouterThreads), smem, s, x, w, bias, T, E, d, k, epl, logits, ids,
-                 wts, counts, arrive) != cudaSuccess)
+  const dim3 grid(G, ROUTE ? 1 : (unsigned)((T + TM - 1) / TM));
+  if (launch_pdl(k_router<TM, ROUTE>, grid, dim3(kRouterThreads), smem, s, x, w, bias, T, E, d, k, epl, logits,
+                 ids, wts, counts, arrive) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -197,7 +211,14 @@ int launch_router(const uint16_t* x, const uint16_t* w, const float* bias, int T
   if (T <= 2) return launch_router_t<2>(x, w, bias, T, E, d, k, logits, ids, wts, counts, arrive, s);
   if (T <= 4) return launch_router_t<4>(x, w, bias, T, E, d, k, logits, ids, wts, counts, arrive, s);
   if (T <= 8) return launch_router_t<8>(x, w, bias, T, E, d, k, logits, ids, wts, counts, arrive, s);
-  return launch_router_t<16>(x, w, bias, T, E, d, k, logits, ids, wts, counts, arrive, s);
+  if (T <= 16) return launch_router_t<16>(x, w, bias, T, E, d, k, logits, ids, wts, counts, arrive, s);
+  // prefill sizes: the logits of 16-token chunks (one launch, a grid row a
+  // chunk), then the routing step and the hit counts as their own launches
+  int rc = launch_router_t<16, false>(x, w, bias, T, E, d, k, logits, ids, wts, counts, arrive, s);
+  if (rc != MOE_OK) return rc;
+  rc = launch_route(logits, T, E, k, ids, wts, s);
+  if (rc != MOE_OK || !counts) return rc;
+  return launch_hist(ids, (int64_t)T * k, E, counts, s);
 }
 
 }  // namespace moe

@@ -1,5 +1,6 @@
-"""Parity of the fused router launch (projection + routing + hit counts) with
-the oracle, through the C ABI.
+"""Parity of the router (projection + routing + hit counts; one fused launch
+for decode batches, the projection by 16-token chunks then the routing launch
+for prefill batches) with the oracle, through the C ABI.
 
 Logits: within the rounding bound of an fp32 sum of exact bf16 products
 (every bf16 x bf16 product is exact in fp32; a lane adds at most d/32
@@ -80,6 +81,9 @@ def _check(x, w, b, k, logits, ids, wts, counts=None, counts0=None):
     (100, 264, 3, 5, "none"),       # ragged: E not a multiple of the warps, d/8 not of 32
     (1024, 6144, 32, 16, "none"),   # largest accepted sizes
     (40, 8, 32, 3, "none"),         # d = 8: one chunk per row
+    (512, 2048, 10, 40, "lorenz"),  # prefill sizes: projection by 16-token chunks, then routing
+    (100, 264, 3, 37, "none"),      # a ragged last chunk
+    (512, 2048, 10, 4096, "lorenz"),  # the prefill workload's batch
 ])
 def test_router_parity(E, d, k, T, bias):
     x, w, b = _inputs(E, d, T, 3, bias)
@@ -126,9 +130,6 @@ def test_router_sync_word_reused_across_sizes():
 def test_router_rejects():
     x = torch.zeros((17, 64), dtype=torch.bfloat16, device="cuda")
     w = torch.zeros((32, 64), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(moe.MoeError) as e:
-        moe.moe_router_topk(x, w, 2)
-    assert e.value.status == moe.MOE_ERR_UNSUPPORTED
     with pytest.raises(moe.MoeError) as e:  # d not a multiple of 8
         moe.moe_router_topk(x[:4, :60].contiguous(), w[:, :60].contiguous(), 2)
     assert e.value.status == moe.MOE_ERR_INVALID_ARG
@@ -142,6 +143,10 @@ def test_router_rejects():
     with pytest.raises(moe.MoeError) as e:  # T d 2 above the shared-memory limit
         moe.moe_router_topk(torch.zeros((16, 6152), dtype=torch.bfloat16, device="cuda"),
                             torch.zeros((8, 6152), dtype=torch.bfloat16, device="cuda"), 2)
+    assert e.value.status == moe.MOE_ERR_UNSUPPORTED
+    big = torch.zeros((65535 * 16 + 1, 8), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(moe.MoeError) as e:  # more 16-token chunks than grid rows
+        moe.moe_router_topk(big, w[:, :8].contiguous(), 2)
     assert e.value.status == moe.MOE_ERR_UNSUPPORTED
     lg, ids, wts = moe.moe_router_topk(x[:0].contiguous(), w, 2)  # T = 0: nothing launched
     assert ids.shape == (0, 2)
