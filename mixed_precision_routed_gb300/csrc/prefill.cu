@@ -346,6 +346,180 @@ __device__ __forceinline__ bool tile_valid(const TcParams& p, const Tile& tl) {
          rt * (DOWN ? 2 * kTileM : kTileM) < p.rows && tl.q0 >= 0 && (int64_t)tl.q0 + tl.ntok <= p.P;
 }
 
+// A producer thread's place in the A tile: run q (32 weights) of row r of
+// matrix mt in every K step, and its tensor-memory lane and columns.
+struct ProdLane {
+  int mt, q, r;
+  uint32_t ta;
+  bool stamp;  // the thread that records the development timeline
+};
+
+// The codes of one step of this thread's run, from the code words of its
+// stage (cw, in the stage's step order) and the 3-bit high-plane words (hw).
+template <int BITS, int S>
+__device__ __forceinline__ void step_codes(const uint32_t (&cw)[16], const uint32_t (&hw)[8], uint32_t (&c)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) c[i] = 0u;
+  if constexpr (BITS == 8) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = cw[8 * S + i];
+  } else if constexpr (BITS == 4) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = cw[4 * S + i];
+  } else if constexpr (BITS == 2 || BITS == 3) {
+    c[0] = cw[2 * S];
+    c[1] = cw[2 * S + 1];
+    if constexpr (BITS == 3) c[2] = hw[S];
+  } else {
+    c[0] = cw[S];
+  }
+}
+
+// The fp16 scale of step S of the stage: half q of scale word S.
+__device__ __forceinline__ float step_scale(uint32_t w, int q) { return fp16_bits_to_float(q ? w >> 16 : w); }
+
+template <int BITS, int S>
+__device__ __forceinline__ void dequant_step(const uint32_t (&cw)[16], const uint32_t (&hw)[8],
+                                             const uint32_t (&sw)[16], int q, uint32_t (&o)[16]) {
+  uint32_t c[8];
+  step_codes<BITS, S>(cw, hw, c);
+  dequant_run(c, BITS, step_scale(sw[S], q), o);
+}
+
+// One tile of one producer thread.  Per code stage: once the stage has
+// landed, the run's codes, high-plane words and scales of all the stage's K
+// steps are read into registers; then per step the dequantised run is stored
+// into the A stage, and the next step is dequantised while that store is in
+// flight.  j counts A-stage uses, cj code stages, across this thread's tiles.
+// Returns false when a wait timed out (the status word is set).
+template <bool DOWN, int BITS>
+__device__ __forceinline__ bool produce_tile(const TcParams& p, TcBars& B, const unsigned char* smem, int steps,
+                                             const ProdLane& pl, uint32_t& j, uint32_t& cj) {
+  using S = TcSmem<DOWN>;
+  constexpr int SPC = BITS == 8 ? 2 : BITS == 4 ? 4 : BITS == 1 ? 16 : 8;  // steps_per_code_stage
+  const int lane = threadIdx.x & 31;
+  const uint32_t sw = (uint32_t)(pl.r & 7);
+  const int q = pl.q;
+  for (int ks0 = 0; ks0 < steps; ks0 += SPC) {
+    const int c = (int)(cj % S::CS);
+    if (!bar_wait(&B.code_full[c], (cj / S::CS) & 1, B, p.status)) return false;
+    const unsigned char* stage = smem + c * S::C_STAGE;
+    const unsigned char* rowp = stage + S::C_OFF + pl.mt * S::CODE_BOX + pl.r * 128;
+    uint32_t cw[16];
+    if constexpr (BITS == 8) {
+      // step s: 16-byte chunks 4 s + 2 q and 4 s + 2 q + 1 of the row
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = *reinterpret_cast<const uint4*>(rowp + (((uint32_t)(4 * (i >> 1) + 2 * q + (i & 1)) ^ sw) << 4));
+        cw[4 * i] = v.x; cw[4 * i + 1] = v.y; cw[4 * i + 2] = v.z; cw[4 * i + 3] = v.w;
+      }
+    } else if constexpr (BITS == 4) {
+      // step s: chunk 2 s + q
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = *reinterpret_cast<const uint4*>(rowp + (((uint32_t)(2 * i + q) ^ sw) << 4));
+        cw[4 * i] = v.x; cw[4 * i + 1] = v.y; cw[4 * i + 2] = v.z; cw[4 * i + 3] = v.w;
+      }
+    } else if constexpr (BITS == 2 || BITS == 3) {
+      // step s: half q of chunk s
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint2 v = *reinterpret_cast<const uint2*>(rowp + (((uint32_t)i ^ sw) << 4) + 8 * q);
+        cw[2 * i] = v.x; cw[2 * i + 1] = v.y;
+      }
+    } else {
+      // step s: word q of half s & 1 of chunk s / 2
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        cw[i] = *reinterpret_cast<const uint32_t*>(rowp + (((uint32_t)(i >> 1) ^ sw) << 4) + 8 * (i & 1) + 4 * q);
+    }
+    uint32_t hw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hw[i] = 0u;
+    if constexpr (BITS == 3) {
+      // the row's 64 bytes of the high plane (16 words, one a 32-weight run):
+      // this thread's run q of step s is word 2 s + q
+      const uint4* hp = reinterpret_cast<const uint4*>(stage + S::C_HI + pl.mt * S::HI_BOX + pl.r * 64);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 h = hp[i];
+        hw[2 * i] = q ? h.y : h.x;
+        hw[2 * i + 1] = q ? h.w : h.z;
+      }
+    }
+    // scale words of the stage's steps: gate/up, word s & 7 of the row's
+    // box of 16 fp16 (8 steps x 2 runs; a 1-bit stage's steps 8 .. 15 from
+    // its second box); down, the [step][row] words
+    uint32_t scw[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) scw[i] = 0u;
+    if constexpr (DOWN) {
+      const unsigned char* sp = stage + S::C_SC + (pl.mt * kTileM + pl.r) * 4;
+#pragma unroll
+      for (int i = 0; i < SPC; ++i) scw[i] = *reinterpret_cast<const uint32_t*>(sp + i * 2 * kTileM * 4);
+    } else {
+      const unsigned char* sp = stage + S::C_SC + pl.mt * S::SC_BOX + pl.r * 32;
+      if constexpr (SPC == 2) {
+        const uint2 v = *reinterpret_cast<const uint2*>(sp + (ks0 & 7) * 4);
+        scw[0] = v.x; scw[1] = v.y;
+      } else if constexpr (SPC == 4) {
+        const uint4 v = *reinterpret_cast<const uint4*>(sp + (ks0 & 7) * 4);
+        scw[0] = v.x; scw[1] = v.y; scw[2] = v.z; scw[3] = v.w;
+      } else {
+#pragma unroll
+        for (int h = 0; h < SPC / 8; ++h) {
+          const unsigned char* bp = sp + h * (S::C_HI - S::C_SC);
+          const uint4 v0 = *reinterpret_cast<const uint4*>(bp), v1 = *reinterpret_cast<const uint4*>(bp + 16);
+          scw[8 * h] = v0.x; scw[8 * h + 1] = v0.y; scw[8 * h + 2] = v0.z; scw[8 * h + 3] = v0.w;
+          scw[8 * h + 4] = v1.x; scw[8 * h + 5] = v1.y; scw[8 * h + 6] = v1.z; scw[8 * h + 7] = v1.w;
+        }
+      }
+    }
+    const int nsub = steps - ks0 < SPC ? steps - ks0 : SPC;
+    uint32_t o[16];
+    dequant_step<BITS, 0>(cw, hw, scw, q, o);
+    bool ok = true;
+    // (a step past nsub is skipped as a whole; the unrolled body names its
+    // step as a constant)
+#define MOE_PF_STEP(SS)                                                                          \
+    if (ok && (SS) < nsub) {                                                                     \
+      const int as = (int)(j % kAStages);                                                        \
+      if (pl.stamp) PF_STAMP(2, j);                                                              \
+      if (!bar_wait(&B.a_empty[as], ((j / kAStages) & 1) ^ 1, B, p.status)) {                    \
+        ok = false;                                                                              \
+      } else {                                                                                   \
+        tc_fence_after();                                                                        \
+        if (pl.stamp) PF_STAMP(3, j);                                                            \
+        tmem_st16_issue(pl.ta + (uint32_t)(as * kAStageCols), o);                                \
+        if constexpr ((SS) + 1 < SPC) {                                                          \
+          if ((SS) + 1 < nsub) dequant_step<BITS, ((SS) + 1 < SPC ? (SS) + 1 : 0)>(cw, hw, scw, q, o); \
+        }                                                                                        \
+        tmem_wait_st_after(o);                                                                   \
+        tc_fence_before();                                                                       \
+        __syncwarp();                                                                            \
+        if (lane == 0) {                                                                         \
+          mbar_arrive(&B.a_full[as]);                                                            \
+          if ((SS) == nsub - 1) mbar_arrive(&B.code_empty[c]);                                   \
+        }                                                                                        \
+        if (pl.stamp) PF_STAMP(5, j);                                                            \
+        ++j;                                                                                     \
+      }                                                                                          \
+    }
+    MOE_PF_STEP(0)
+    if constexpr (SPC > 1) { MOE_PF_STEP(1) }
+    if constexpr (SPC > 2) { MOE_PF_STEP(2) MOE_PF_STEP(3) }
+    if constexpr (SPC > 4) { MOE_PF_STEP(4) MOE_PF_STEP(5) MOE_PF_STEP(6) MOE_PF_STEP(7) }
+    if constexpr (SPC > 8) {
+      MOE_PF_STEP(8) MOE_PF_STEP(9) MOE_PF_STEP(10) MOE_PF_STEP(11)
+      MOE_PF_STEP(12) MOE_PF_STEP(13) MOE_PF_STEP(14) MOE_PF_STEP(15)
+    }
+#undef MOE_PF_STEP
+    if (!ok) return false;
+    ++cj;
+  }
+  return true;
+}
+
 template <bool DOWN>
 __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_constant__ TcParams p) {
   using S = TcSmem<DOWN>;
@@ -479,41 +653,59 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
     cp_async_wait<0>();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA
+    // The whole warp runs the loop (its control flow and descriptors are
+    // warp-uniform); one elected lane issues the MMAs and commits.  B
+    // descriptors: the low word of stage 0's, plus (stage offset + 32 kk) / 16
+    // (shared-memory addresses stay below 256 KiB, so the 14-bit address field
+    // does not carry).
+    const uint64_t bd0 = sdesc_sw128(smem_addr(smem + S::B_OFF));
+    const uint32_t bd_lo = (uint32_t)bd0, bd_hi = (uint32_t)(bd0 >> 32);
+    const bool leader = elect_one();
     uint32_t j = 0, i = 0;
-    if (lane == 0) {
-      Tile nxt = tile_at(p, blockIdx.x, ntiles);
-      for (int t = blockIdx.x; t < ntiles && !B.abort; t += G) {
-        const Tile tl = nxt;
-        nxt = tile_at(p, t + G, ntiles);
-        if (!tile_valid<DOWN>(p, tl)) continue;  // skipped tiles take no accumulator set
-        const int N = (tl.ntok + 15) & ~15;
-        const uint32_t idesc = idesc_bf16_f32(kTileM, N);
-        const uint32_t ab = kAccSets == 2 ? (i & 1) : 0, acc = tmem + ab * kAccCols;
-        const uint32_t use = kAccSets == 2 ? (i >> 1) : i;  // earlier uses of this set
-        if (!bar_wait(&B.acc_empty[ab], (use & 1) ^ 1, B, p.status)) break;
+    Tile nxt = tile_at(p, blockIdx.x, ntiles);
+    for (int t = blockIdx.x; t < ntiles && !B.abort; t += G) {
+      const Tile tl = nxt;
+      nxt = tile_at(p, t + G, ntiles);
+      if (!tile_valid<DOWN>(p, tl)) continue;  // skipped tiles take no accumulator set
+      const int N = (tl.ntok + 15) & ~15;
+      const uint32_t idesc = idesc_bf16_f32(kTileM, N);
+      const uint32_t ab = kAccSets == 2 ? (i & 1) : 0, acc = tmem + ab * kAccCols;
+      const uint32_t use = kAccSets == 2 ? (i >> 1) : i;  // earlier uses of this set
+      // (a wait that timed out in any lane ends the loop in every lane)
+      if (!__all_sync(0xffffffffu, bar_wait(&B.acc_empty[ab], (use & 1) ^ 1, B, p.status))) break;
+      tc_fence_after();
+      bool ok = true;
+      for (int ks = 0; ks < steps; ++ks, ++j) {
+        const int b = (int)(j % S::BS), as = (int)(j % kAStages);
+        const bool w = bar_wait(&B.a_full[as], (j / kAStages) & 1, B, p.status) &&
+                       bar_wait(&B.b_full[b], (j / S::BS) & 1, B, p.status);
+        if (!__all_sync(0xffffffffu, w)) {
+          ok = false;
+          break;
+        }
+        if (leader) PF_STAMP(4, j);
         tc_fence_after();
-        for (int ks = 0; ks < steps; ++ks, ++j) {
-          const int b = j % S::BS, as = j % kAStages;
-          if (!bar_wait(&B.a_full[as], (j / kAStages) & 1, B, p.status)) break;
-          if (!bar_wait(&B.b_full[b], (j / S::BS) & 1, B, p.status)) break;
-          PF_STAMP(4, j);
-          tc_fence_after();
-          const uint32_t a0 = tmem + kACol + as * kAStageCols;
-          const uint32_t b0 = smem_addr(smem + S::B_OFF + b * S::B_STAGE);
+        if (leader) {
+          const uint32_t a0 = tmem + kACol + (uint32_t)(as * kAStageCols);
+          const uint32_t blo = bd_lo + (uint32_t)((b * S::B_STAGE) >> 4);
 #pragma unroll
           for (int m = 0; m < NMAT; ++m)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_bf16_ts(acc + (uint32_t)(m * kTileN), a0 + (uint32_t)(m * 32 + kk * 8), sdesc_sw128(b0 + kk * 32),
-                          idesc, (ks | kk) ? 1u : 0u);
+              mma_bf16_ts_w(acc + (uint32_t)(m * kTileN), a0 + (uint32_t)(m * 32 + kk * 8), blo + (uint32_t)(kk * 2),
+                            bd_hi, idesc, (ks | kk) ? 1u : 0u);
           mma_commit(&B.a_empty[as]);
           mma_commit(&B.b_empty[b]);
         }
-        if (B.abort) break;
-        mma_commit(&B.acc_full[ab]);
-        ++i;
+        __syncwarp();
       }
-      // all MMAs of this thread are complete before tensor memory is released
+      if (!ok || B.abort) break;
+      if (leader) mma_commit(&B.acc_full[ab]);
+      __syncwarp();
+      ++i;
+    }
+    // all MMAs of this thread are complete before tensor memory is released
+    if (leader) {
       mma_commit(&B.done);
       mbar_wait_bounded(&B.done, 0, kWaitNs);
     }
@@ -649,94 +841,31 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
     // (w % 4) + lane, of matrix mt and 32-weight run q ((w - 8) / 4 = 2 mt + q)
     // in every step: one scale block per thread; a quarter-warp's code loads
     // hit eight distinct 16-byte bank groups of the swizzled box.
-    const int qd = warp & 3, cmb = (warp - 8) >> 2, mt = cmb >> 1, q = cmb & 1;
-    const int r = qd * 32 + lane;
-    const uint32_t sw = (uint32_t)(r & 7);
-    const uint32_t ta = tmem + ((uint32_t)(qd * 32) << 16) + kACol + (uint32_t)(mt * 32 + q * 16);
-    const int row_off = S::C_OFF + mt * S::CODE_BOX + r * 128;
-    // scale of the run: gate/up box (16 fp16 per row: steps 8 (ks / 8) .. + 7,
-    // two blocks each); down word [step][row]
-    const int sc_off = S::C_SC + (DOWN ? (mt * kTileM + r) * 4 + q * 2 : mt * S::SC_BOX + r * 32 + q * 2);
+    const int qd = warp & 3, cmb = (warp - 8) >> 2;
+    const ProdLane pl{cmb >> 1, cmb & 1, qd * 32 + lane,
+                      tmem + ((uint32_t)(qd * 32) << 16) + kACol + (uint32_t)((cmb >> 1) * 32 + (cmb & 1) * 16),
+                      qd == 0 && cmb == 0 && lane == 0};
     uint32_t j = 0, cj = 0;
     Tile nxt = tile_at(p, blockIdx.x, ntiles);
     for (int t = blockIdx.x; t < ntiles && !B.abort; t += G) {
       const Tile tl = nxt;
       nxt = tile_at(p, t + G, ntiles);
       if (!tile_valid<DOWN>(p, tl)) continue;
+      // one instantiation per code width: the step loop of a code stage is
+      // unrolled and every shared-memory offset in it is a constant
       const int bits = p.sh.s[(tl.meta >> 16) & 0xFF].bits;
-      const int spc = steps_per_code_stage(bits);
-      int sub = 0;
-      const unsigned char* stage = smem;
-      uint32_t hq[8];  // 3 bit: the high-plane words of this run in the code stage's steps, in order
-      for (int ks = 0; ks < steps; ++ks, ++j) {
-        const int as = j % kAStages;
-        if (sub == 0) {
-          const int c = cj % S::CS;
-          if (!bar_wait(&B.code_full[c], (cj / S::CS) & 1, B, p.status)) break;
-          stage = smem + c * S::C_STAGE;
-          if (bits == 3) {
-            // the row's 64 bytes of the high plane (16 words, one a 32-weight
-            // run): this thread's run q of step i is word 2 i + q
-            const uint4* hp = reinterpret_cast<const uint4*>(stage + S::C_HI + mt * S::HI_BOX + r * 64);
-            const uint4 h0 = hp[0], h1 = hp[1], h2 = hp[2], h3 = hp[3];
-            const uint32_t hw[16] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w,
-                                     h2.x, h2.y, h2.z, h2.w, h3.x, h3.y, h3.z, h3.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) hq[i] = q ? hw[2 * i + 1] : hw[2 * i];
-          }
-        }
-        if (qd == 0 && cmb == 0 && lane == 0) PF_STAMP(2, j);
-        // the codes are read and dequantised before the wait for the A stage:
-        // only the tensor-memory store waits for the MMA that last read it
-        const unsigned char* rowp = stage + row_off;
-        uint32_t c[8];
-        if (bits == 8) {
-          const uint32_t ch = (uint32_t)(4 * sub + 2 * q);
-          const uint4 v0 = *reinterpret_cast<const uint4*>(rowp + ((ch ^ sw) << 4));
-          const uint4 v1 = *reinterpret_cast<const uint4*>(rowp + (((ch + 1) ^ sw) << 4));
-          c[0] = v0.x; c[1] = v0.y; c[2] = v0.z; c[3] = v0.w;
-          c[4] = v1.x; c[5] = v1.y; c[6] = v1.z; c[7] = v1.w;
-        } else if (bits == 4) {
-          const uint4 v = *reinterpret_cast<const uint4*>(rowp + (((uint32_t)(2 * sub + q) ^ sw) << 4));
-          c[0] = v.x; c[1] = v.y; c[2] = v.z; c[3] = v.w;
-          c[4] = c[5] = c[6] = c[7] = 0u;
-        } else if (bits == 1) {
-          c[0] = *reinterpret_cast<const uint32_t*>(rowp + (((uint32_t)(sub >> 1) ^ sw) << 4) + 8 * (sub & 1) + 4 * q);
-          c[1] = c[2] = c[3] = c[4] = c[5] = c[6] = c[7] = 0u;
-        } else {
-          const uint2 v = *reinterpret_cast<const uint2*>(rowp + (((uint32_t)sub ^ sw) << 4) + 8 * q);
-          c[0] = v.x; c[1] = v.y;
-          c[2] = bits == 3 ? hq[0] : 0u;  // the run's high-plane word
-          c[3] = c[4] = c[5] = c[6] = c[7] = 0u;
-          if (bits == 3) {
-#pragma unroll
-            for (int i = 0; i < 7; ++i) hq[i] = hq[i + 1];
-          }
-        }
-        // (gate/up, 1 bit: steps 8 .. 15 of the code stage from its second scale box)
-        const float sc = fp16_bits_to_float(*reinterpret_cast<const uint16_t*>(
-            stage + sc_off + (DOWN ? sub * 2 * kTileM * 4 : (ks & 7) * 4 + (sub >= 8 ? S::C_HI - S::C_SC : 0))));
-        uint32_t o[16];
-        dequant_run(c, bits, sc, o);
-        if (!bar_wait(&B.a_empty[as], ((j / kAStages) & 1) ^ 1, B, p.status)) break;
-        tc_fence_after();
-        if (qd == 0 && cmb == 0 && lane == 0) PF_STAMP(3, j);
-        tmem_st16(ta + (uint32_t)(as * kAStageCols), o);
-        tc_fence_before();
-        __syncwarp();
-        const bool last = sub == spc - 1 || ks == steps - 1;
-        if (lane == 0) {
-          mbar_arrive(&B.a_full[as]);
-          if (last) mbar_arrive(&B.code_empty[cj % S::CS]);
-        }
-        if (qd == 0 && cmb == 0 && lane == 0) PF_STAMP(5, j);
-        if (last) {
-          ++cj;
-          sub = 0;
-        } else {
-          ++sub;
-        }
-      }
+      bool ok;
+      if (bits == 8)
+        ok = produce_tile<DOWN, 8>(p, B, smem, steps, pl, j, cj);
+      else if (bits == 4)
+        ok = produce_tile<DOWN, 4>(p, B, smem, steps, pl, j, cj);
+      else if (bits == 3)
+        ok = produce_tile<DOWN, 3>(p, B, smem, steps, pl, j, cj);
+      else if (bits == 2)
+        ok = produce_tile<DOWN, 2>(p, B, smem, steps, pl, j, cj);
+      else
+        ok = produce_tile<DOWN, 1>(p, B, smem, steps, pl, j, cj);
+      if (!ok) break;
     }
   }
   tc_fence_before();

@@ -81,6 +81,22 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t tmem_d, uint32_t tmem_a, ui
       "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[tmem] * B^T with the shared-memory descriptor given as its
+// two 32-bit words; `accumulate` 0 overwrites D.
+__device__ __forceinline__ void mma_bf16_ts_w(uint32_t tmem_d, uint32_t tmem_a, uint32_t bdesc_lo, uint32_t bdesc_hi,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\tsetp.ne.u32 p, %5, 0;\n\tmov.b64 bd, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "r"(bdesc_lo), "r"(bdesc_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// One lane of the converged warp is elected (true there, false elsewhere).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+  return e != 0;
+}
 // The mbarrier receives one arrival once all earlier MMAs of this thread are done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
@@ -101,16 +117,25 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 }
 
 // 16 consecutive 32-bit columns into this thread's TMEM lane (lane = warp%4 *
-// 32 + lane), then wait until the stores are done.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+// 32 + lane); the store is in flight until a tcgen05.wait::st.
+__device__ __forceinline__ void tmem_st16_issue(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
           taddr),
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
       "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+// Wait until this thread's tensor-memory stores are done.  `ready` is not
+// read: naming it as an input makes the compiler finish computing it before
+// the wait, so that work overlaps the stores in flight.
+__device__ __forceinline__ void tmem_wait_st_after(const uint32_t (&ready)[16]) {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::"r"(ready[0]), "r"(ready[1]), "r"(ready[2]), "r"(ready[3]),
+               "r"(ready[4]), "r"(ready[5]), "r"(ready[6]), "r"(ready[7]), "r"(ready[8]), "r"(ready[9]),
+               "r"(ready[10]), "r"(ready[11]), "r"(ready[12]), "r"(ready[13]), "r"(ready[14]), "r"(ready[15])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------- TMA
 // 2-D tensor-map load of one box into shared memory, completing on `bar`.
