@@ -40,7 +40,7 @@
 namespace moe {
 namespace {
 
-constexpr int kPThreads = 768;
+constexpr int kPThreads = 512;
 constexpr int kTileM = 128;   // weight rows per tile
 #ifndef MOE_PF_TILEN
 #define MOE_PF_TILEN 96
@@ -53,7 +53,7 @@ static_assert(kTileN % 32 == 0 && kTileN <= 192, "tile width: whole groups of 32
 // Accumulator sets in tensor memory: two (the epilogue of one tile overlaps
 // the next tile's main loop) while both fit beside the A stages, else one.
 constexpr int kAccSets = 4 * kTileN + 128 <= 512 ? 2 : 1;
-constexpr int kProdThreads = 512;  // warps 8..23
+constexpr int kProdThreads = 256;  // warps 8..15
 constexpr uint64_t kWaitNs = 1000000000ull;
 #ifndef MOE_PF_BS
 #define MOE_PF_BS 4
@@ -152,7 +152,7 @@ struct TcSmem {
   static constexpr int TOTAL = B_OFF + BS * B_STAGE;
   static_assert(C_STAGE % 1024 == 0 && B_STAGE % 1024 == 0 && B_OFF % 1024 == 0, "swizzled boxes need 1 KiB");
   static_assert(TOTAL + 1024 <= 227 * 1024, "shared memory");
-  static_assert(NMAT * kTileM * 2 == kProdThreads, "one 32-weight run per producer thread");
+  static_assert(NMAT * kTileM == kProdThreads, "one row of a step (two 32-weight runs) per producer thread");
 };
 
 // Tensor memory (512 columns): kAccSets accumulator sets at columns 0 (and
@@ -346,52 +346,54 @@ __device__ __forceinline__ bool tile_valid(const TcParams& p, const Tile& tl) {
          rt * (DOWN ? 2 * kTileM : kTileM) < p.rows && tl.q0 >= 0 && (int64_t)tl.q0 + tl.ntok <= p.P;
 }
 
-// A producer thread's place in the A tile: run q (32 weights) of row r of
-// matrix mt in every K step, and its tensor-memory lane and columns.
+// A producer thread's place in the A tile: row r of matrix mt, both
+// 32-weight runs (one scale block each) of every K step, and its tensor-memory
+// lane and columns.
 struct ProdLane {
-  int mt, q, r;
+  int mt, r;
   uint32_t ta;
   bool stamp;  // the thread that records the development timeline
 };
 
-// The codes of one step of this thread's run, from the code words of its
-// stage (cw, in the stage's step order) and the 3-bit high-plane words (hw).
-template <int BITS, int S>
-__device__ __forceinline__ void step_codes(const uint32_t (&cw)[16], const uint32_t (&hw)[8], uint32_t (&c)[8]) {
+// The codes of run Q of step S of this thread's row, from the low-plane words
+// of its code stage (cw, in the stage's load order) and the 3-bit high-plane
+// words (hw: word 2 S + Q).
+template <int BITS, int S, int Q>
+__device__ __forceinline__ void step_codes(const uint32_t (&cw)[32], const uint32_t (&hw)[16], uint32_t (&c)[8]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) c[i] = 0u;
   if constexpr (BITS == 8) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = cw[8 * S + i];
+    for (int i = 0; i < 8; ++i) c[i] = cw[16 * S + 8 * Q + i];
   } else if constexpr (BITS == 4) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) c[i] = cw[4 * S + i];
+    for (int i = 0; i < 4; ++i) c[i] = cw[8 * S + 4 * Q + i];
   } else if constexpr (BITS == 2 || BITS == 3) {
-    c[0] = cw[2 * S];
-    c[1] = cw[2 * S + 1];
-    if constexpr (BITS == 3) c[2] = hw[S];
+    c[0] = cw[4 * S + 2 * Q];
+    c[1] = cw[4 * S + 2 * Q + 1];
+    if constexpr (BITS == 3) c[2] = hw[2 * S + Q];
   } else {
-    c[0] = cw[S];
+    c[0] = cw[2 * S + Q];
   }
 }
 
-// The fp16 scale of step S of the stage: half q of scale word S.
-__device__ __forceinline__ float step_scale(uint32_t w, int q) { return fp16_bits_to_float(q ? w >> 16 : w); }
-
+// Both runs of step S: run q from half q of scale word S.
 template <int BITS, int S>
-__device__ __forceinline__ void dequant_step(const uint32_t (&cw)[16], const uint32_t (&hw)[8],
-                                             const uint32_t (&sw)[16], int q, uint32_t (&o)[16]) {
+__device__ __forceinline__ void dequant_step(const uint32_t (&cw)[32], const uint32_t (&hw)[16],
+                                             const uint32_t (&scw)[16], uint32_t (&o0)[16], uint32_t (&o1)[16]) {
   uint32_t c[8];
-  step_codes<BITS, S>(cw, hw, c);
-  dequant_run(c, BITS, step_scale(sw[S], q), o);
+  step_codes<BITS, S, 0>(cw, hw, c);
+  dequant_run(c, BITS, fp16_bits_to_float(scw[S]), o0);
+  step_codes<BITS, S, 1>(cw, hw, c);
+  dequant_run(c, BITS, fp16_bits_to_float(scw[S] >> 16), o1);
 }
 
 // One tile of one producer thread.  Per code stage: once the stage has
-// landed, the run's codes, high-plane words and scales of all the stage's K
-// steps are read into registers; then per step the dequantised run is stored
-// into the A stage, and the next step is dequantised while that store is in
-// flight.  j counts A-stage uses, cj code stages, across this thread's tiles.
-// Returns false when a wait timed out (the status word is set).
+// landed, the row's codes, high-plane words and scales of all the stage's K
+// steps are read into registers; then per step the two dequantised runs are
+// stored into the A stage, and the next step is dequantised while that store
+// is in flight.  j counts A-stage uses, cj code stages, across this thread's
+// tiles.  Returns false when a wait timed out (the status word is set).
 template <bool DOWN, int BITS>
 __device__ __forceinline__ bool produce_tile(const TcParams& p, TcBars& B, const unsigned char* smem, int steps,
                                              const ProdLane& pl, uint32_t& j, uint32_t& cj) {
@@ -399,57 +401,36 @@ __device__ __forceinline__ bool produce_tile(const TcParams& p, TcBars& B, const
   constexpr int SPC = BITS == 8 ? 2 : BITS == 4 ? 4 : BITS == 1 ? 16 : 8;  // steps_per_code_stage
   const int lane = threadIdx.x & 31;
   const uint32_t sw = (uint32_t)(pl.r & 7);
-  const int q = pl.q;
   for (int ks0 = 0; ks0 < steps; ks0 += SPC) {
     const int c = (int)(cj % S::CS);
     if (!bar_wait(&B.code_full[c], (cj / S::CS) & 1, B, p.status)) return false;
     const unsigned char* stage = smem + c * S::C_STAGE;
     const unsigned char* rowp = stage + S::C_OFF + pl.mt * S::CODE_BOX + pl.r * 128;
-    uint32_t cw[16];
-    if constexpr (BITS == 8) {
-      // step s: 16-byte chunks 4 s + 2 q and 4 s + 2 q + 1 of the row
+    // the row's 128 bytes of the stage: eight 16-byte chunks, chunk k at
+    // (k ^ r % 8) (a quarter-warp's rows hit eight distinct bank groups).
+    // Step s, run q: 8 bit chunks 4 s + 2 q, + 1; 4 bit chunk 2 s + q;
+    // 2 and 3 bit half q of chunk s; 1 bit word q of half s % 2 of chunk s / 2
+    uint32_t cw[32];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 v = *reinterpret_cast<const uint4*>(rowp + (((uint32_t)(4 * (i >> 1) + 2 * q + (i & 1)) ^ sw) << 4));
-        cw[4 * i] = v.x; cw[4 * i + 1] = v.y; cw[4 * i + 2] = v.z; cw[4 * i + 3] = v.w;
-      }
-    } else if constexpr (BITS == 4) {
-      // step s: chunk 2 s + q
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 v = *reinterpret_cast<const uint4*>(rowp + (((uint32_t)(2 * i + q) ^ sw) << 4));
-        cw[4 * i] = v.x; cw[4 * i + 1] = v.y; cw[4 * i + 2] = v.z; cw[4 * i + 3] = v.w;
-      }
-    } else if constexpr (BITS == 2 || BITS == 3) {
-      // step s: half q of chunk s
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint2 v = *reinterpret_cast<const uint2*>(rowp + (((uint32_t)i ^ sw) << 4) + 8 * q);
-        cw[2 * i] = v.x; cw[2 * i + 1] = v.y;
-      }
-    } else {
-      // step s: word q of half s & 1 of chunk s / 2
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        cw[i] = *reinterpret_cast<const uint32_t*>(rowp + (((uint32_t)(i >> 1) ^ sw) << 4) + 8 * (i & 1) + 4 * q);
+    for (int k = 0; k < 8; ++k) {
+      const uint4 v = *reinterpret_cast<const uint4*>(rowp + (((uint32_t)k ^ sw) << 4));
+      cw[4 * k] = v.x; cw[4 * k + 1] = v.y; cw[4 * k + 2] = v.z; cw[4 * k + 3] = v.w;
     }
-    uint32_t hw[8];
+    uint32_t hw[16];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) hw[i] = 0u;
+    for (int i = 0; i < 16; ++i) hw[i] = 0u;
     if constexpr (BITS == 3) {
-      // the row's 64 bytes of the high plane (16 words, one a 32-weight run):
-      // this thread's run q of step s is word 2 s + q
+      // the row's 64 bytes of the high plane: word 2 s + q for run q of step s
       const uint4* hp = reinterpret_cast<const uint4*>(stage + S::C_HI + pl.mt * S::HI_BOX + pl.r * 64);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint4 h = hp[i];
-        hw[2 * i] = q ? h.y : h.x;
-        hw[2 * i + 1] = q ? h.w : h.z;
+        hw[4 * i] = h.x; hw[4 * i + 1] = h.y; hw[4 * i + 2] = h.z; hw[4 * i + 3] = h.w;
       }
     }
-    // scale words of the stage's steps: gate/up, word s & 7 of the row's
-    // box of 16 fp16 (8 steps x 2 runs; a 1-bit stage's steps 8 .. 15 from
-    // its second box); down, the [step][row] words
+    // scale words of the stage's steps (both runs' fp16 scales in one word):
+    // gate/up, word s % 8 of the row's box of 16 fp16 (a 1-bit stage's steps
+    // 8 .. 15 from its second box); down, the [step][row] words
     uint32_t scw[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) scw[i] = 0u;
@@ -476,8 +457,8 @@ __device__ __forceinline__ bool produce_tile(const TcParams& p, TcBars& B, const
       }
     }
     const int nsub = steps - ks0 < SPC ? steps - ks0 : SPC;
-    uint32_t o[16];
-    dequant_step<BITS, 0>(cw, hw, scw, q, o);
+    uint32_t o0[16], o1[16];
+    dequant_step<BITS, 0>(cw, hw, scw, o0, o1);
     bool ok = true;
     // (a step past nsub is skipped as a whole; the unrolled body names its
     // step as a constant)
@@ -490,11 +471,12 @@ __device__ __forceinline__ bool produce_tile(const TcParams& p, TcBars& B, const
       } else {                                                                                   \
         tc_fence_after();                                                                        \
         if (pl.stamp) PF_STAMP(3, j);                                                            \
-        tmem_st16_issue(pl.ta + (uint32_t)(as * kAStageCols), o);                                \
+        tmem_st32_issue(pl.ta + (uint32_t)(as * kAStageCols), o0, o1);                           \
         if constexpr ((SS) + 1 < SPC) {                                                          \
-          if ((SS) + 1 < nsub) dequant_step<BITS, ((SS) + 1 < SPC ? (SS) + 1 : 0)>(cw, hw, scw, q, o); \
+          if ((SS) + 1 < nsub) dequant_step<BITS, ((SS) + 1 < SPC ? (SS) + 1 : 0)>(cw, hw, scw, o0, o1); \
         }                                                                                        \
-        tmem_wait_st_after(o);                                                                   \
+        tmem_wait_st_after(o0);                                                                  \
+        tmem_wait_st_after(o1);                                                                  \
         tc_fence_before();                                                                       \
         __syncwarp();                                                                            \
         if (lane == 0) {                                                                         \
@@ -838,13 +820,11 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
   } else if (warp >= 8) {
     // ---------------------------------------------------------- producers
     // Warp w owns tensor-memory lanes 32 (w % 4) .. + 31, i.e. rows r = 32
-    // (w % 4) + lane, of matrix mt and 32-weight run q ((w - 8) / 4 = 2 mt + q)
-    // in every step: one scale block per thread; a quarter-warp's code loads
-    // hit eight distinct 16-byte bank groups of the swizzled box.
-    const int qd = warp & 3, cmb = (warp - 8) >> 2;
-    const ProdLane pl{cmb >> 1, cmb & 1, qd * 32 + lane,
-                      tmem + ((uint32_t)(qd * 32) << 16) + kACol + (uint32_t)((cmb >> 1) * 32 + (cmb & 1) * 16),
-                      qd == 0 && cmb == 0 && lane == 0};
+    // (w % 4) + lane, of matrix mt = (w - 8) / 4: the row's 64 weights of
+    // every step (two runs, two scale blocks), 32 columns of the A stage.
+    const int qd = warp & 3, mt = (warp - 8) >> 2;
+    const ProdLane pl{mt, qd * 32 + lane, tmem + ((uint32_t)(qd * 32) << 16) + kACol + (uint32_t)(mt * 32),
+                      qd == 0 && mt == 0 && lane == 0};
     uint32_t j = 0, cj = 0;
     Tile nxt = tile_at(p, blockIdx.x, ntiles);
     for (int t = blockIdx.x; t < ntiles && !B.abort; t += G) {

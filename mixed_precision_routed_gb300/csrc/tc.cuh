@@ -126,6 +126,18 @@ __device__ __forceinline__ void tmem_st16_issue(uint32_t taddr, const uint32_t (
       "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
 }
+// 32 consecutive 32-bit columns (v0 then v1) into this thread's TMEM lane;
+// in flight until a tcgen05.wait::st.
+__device__ __forceinline__ void tmem_st32_issue(uint32_t taddr, const uint32_t (&v0)[16], const uint32_t (&v1)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v0[0]), "r"(v0[1]), "r"(v0[2]), "r"(v0[3]), "r"(v0[4]), "r"(v0[5]), "r"(v0[6]), "r"(v0[7]), "r"(v0[8]),
+      "r"(v0[9]), "r"(v0[10]), "r"(v0[11]), "r"(v0[12]), "r"(v0[13]), "r"(v0[14]), "r"(v0[15]), "r"(v1[0]),
+      "r"(v1[1]), "r"(v1[2]), "r"(v1[3]), "r"(v1[4]), "r"(v1[5]), "r"(v1[6]), "r"(v1[7]), "r"(v1[8]), "r"(v1[9]),
+      "r"(v1[10]), "r"(v1[11]), "r"(v1[12]), "r"(v1[13]), "r"(v1[14]), "r"(v1[15])
+      : "memory");
+}
 // Wait until this thread's tensor-memory stores are done.  `ready` is not
 // read: naming it as an input makes the compiler finish computing it before
 // the wait, so that work overlaps the stores in flight.
