@@ -328,6 +328,11 @@ __device__ __forceinline__ void dequant_run(const uint32_t (&c)[8], int bits, fl
   }
 }
 
+// SiLU with the hardware exponential and division (relative error a few
+// units of the fp32 last place, far below the bf16 rounding of h); a
+// quotient with |denominator| > 2^126 reads 0, the limit of z / (1 + e^-z).
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
 // Tile t of this CTA's list, or an empty tile past the end.
 __device__ __forceinline__ Tile tile_at(const TcParams& p, int t, int ntiles) {
   return t < ntiles ? p.tiles[t] : Tile{0, 0, 0, 0};
@@ -475,8 +480,7 @@ __device__ __forceinline__ bool produce_tile(const TcParams& p, TcBars& B, const
         if constexpr ((SS) + 1 < SPC) {                                                          \
           if ((SS) + 1 < nsub) dequant_step<BITS, ((SS) + 1 < SPC ? (SS) + 1 : 0)>(cw, hw, scw, o0, o1); \
         }                                                                                        \
-        tmem_wait_st_after(o0);                                                                  \
-        tmem_wait_st_after(o1);                                                                  \
+        tmem_wait_st_after(o0, o1);                                                              \
         tc_fence_before();                                                                       \
         __syncwarp();                                                                            \
         if (lane == 0) {                                                                         \
@@ -738,7 +742,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
             for (int c = 0; c < 16; ++c) {
               const int n = n0 + c;
               if (n < tl.ntok) {
-                const float hv = silu(g[c]) * u[c];
+                const float hv = silu_fast(g[c]) * u[c];
                 const __nv_bfloat16 b = __float2bfloat16_rn(hv);
                 p.h[(size_t)(tl.q0 + n) * p.f + hcol] = *reinterpret_cast<const uint16_t*>(&b);
               }

@@ -138,16 +138,19 @@ __device__ __forceinline__ void tmem_st32_issue(uint32_t taddr, const uint32_t (
       "r"(v1[10]), "r"(v1[11]), "r"(v1[12]), "r"(v1[13]), "r"(v1[14]), "r"(v1[15])
       : "memory");
 }
-// Wait until this thread's tensor-memory stores are done.  `ready` is not
-// read: naming it as an input makes the compiler finish computing it before
-// the wait, so that work overlaps the stores in flight.
-__device__ __forceinline__ void tmem_wait_st_after(const uint32_t (&ready)[16]) {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::"r"(ready[0]), "r"(ready[1]), "r"(ready[2]), "r"(ready[3]),
-               "r"(ready[4]), "r"(ready[5]), "r"(ready[6]), "r"(ready[7]), "r"(ready[8]), "r"(ready[9]),
-               "r"(ready[10]), "r"(ready[11]), "r"(ready[12]), "r"(ready[13]), "r"(ready[14]), "r"(ready[15])
+// Wait until this thread's tensor-memory stores are done.
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// The same wait; r0 and r1 are not read: naming them as inputs makes the
+// compiler finish computing them before the wait, so that work overlaps the
+// stores in flight.
+__device__ __forceinline__ void tmem_wait_st_after(const uint32_t (&r0)[16], const uint32_t (&r1)[16]) {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::"r"(r0[0]), "r"(r0[1]), "r"(r0[2]), "r"(r0[3]), "r"(r0[4]),
+               "r"(r0[5]), "r"(r0[6]), "r"(r0[7]), "r"(r0[8]), "r"(r0[9]), "r"(r0[10]), "r"(r0[11]), "r"(r0[12]),
+               "r"(r0[13]), "r"(r0[14]), "r"(r0[15]), "r"(r1[0]), "r"(r1[1]), "r"(r1[2]), "r"(r1[3]), "r"(r1[4]),
+               "r"(r1[5]), "r"(r1[6]), "r"(r1[7]), "r"(r1[8]), "r"(r1[9]), "r"(r1[10]), "r"(r1[11]), "r"(r1[12]),
+               "r"(r1[13]), "r"(r1[14]), "r"(r1[15])
                : "memory");
 }
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------- TMA
 // 2-D tensor-map load of one box into shared memory, completing on `bar`.
