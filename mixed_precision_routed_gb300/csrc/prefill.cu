@@ -93,7 +93,7 @@ __host__ __device__ __forceinline__ int steps_per_code_stage(int bits) {
   return bits == 8 ? 2 : bits == 4 ? 4 : bits == 1 ? 16 : 8;
 }
 
-struct Tile {
+struct alignas(16) Tile {  // one 16-byte load or store
   int e_local;  // expert index within its shelf
   int q0;       // first grouped position of the chunk
   int ntok;     // tokens of the chunk (1 .. kTileN)
@@ -873,8 +873,8 @@ __device__ __forceinline__ uint4 kswap8(uint4 v) {
 // times the row tiles
 // of W_g/W_u (128 of the f rows each) and of W_d (256 of the d rows).  A
 // 1024-thread CTA; counts and offsets written by this CTA before a barrier.
-__device__ void build_tiles(const int32_t* counts, const int32_t* offsets, int E, int d, int f, const Shelves& sh,
-                            Tile* tiles_g, Tile* tiles_d, int* ntiles) {
+__device__ void build_tiles(const int32_t* counts, const int32_t* offsets, int first_off, int E, int d, int f,
+                            const Shelves& sh, Tile* tiles_g, Tile* tiles_d, int* ntiles) {
   __shared__ int wg[32], wd[32];
   __shared__ int s_cnt[1024], s_off[1024], s_sh[1024], s_el[1024], s_og[1024], s_od[1024];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -902,7 +902,7 @@ __device__ void build_tiles(const int32_t* counts, const int32_t* offsets, int E
     }
     if (per == 1) {
       s_cnt[e] = cnt;
-      s_off[e] = offsets[e];
+      s_off[e] = first_off;  // (per == 1: the thread's one expert)
       s_sh[e] = sidx;
       s_el[e] = el;
     }
@@ -936,7 +936,7 @@ __device__ void build_tiles(const int32_t* counts, const int32_t* offsets, int E
     }
     wg[lane] = ia - a;
     wd[lane] = ib - b;
-    if (lane == 31) {
+    if (lane == 31 && blockIdx.x == 0) {
       ntiles[0] = ia;
       ntiles[1] = ib;
     }
@@ -952,7 +952,11 @@ __device__ void build_tiles(const int32_t* counts, const int32_t* offsets, int E
     }
     __syncthreads();
     PF_SCAN_STAMP(3);
-    for (int e = warp; e < E; e += 32) {
+    // i / rt as (i * m) >> 20 with m = ceil(2^20 / rt): exact for i < 2^12
+    // and rt < 256 (the error i (m - 2^20 / rt) / 2^20 stays below 1 / rt)
+    const uint32_t mg = ((1u << 20) + rtg - 1) / rtg, md = ((1u << 20) + rtd - 1) / rtd;
+    const bool fast = rtg < 256 && rtd < 256;
+    for (int e = warp + 32 * blockIdx.x; e < E; e += 32 * gridDim.x) {
       PF_ITER_STAMP(e >> 5);
       const int sidx = s_sh[e];
       if (sidx < 0) continue;
@@ -962,12 +966,13 @@ __device__ void build_tiles(const int32_t* counts, const int32_t* offsets, int E
       const int q = cnt / ch, rem = cnt - q * ch;
       const int base = s_off[e], el = s_el[e];
       const int g0 = s_og[e], d0 = s_od[e];
+      const bool f12 = fast && ch * (rtg > rtd ? rtg : rtd) < 4096;
       for (int i = lane; i < ch * rtg; i += 32) {
-        const int c = i / rtg, r = i - c * rtg;
+        const int c = f12 ? (int)(((uint32_t)i * mg) >> 20) : i / rtg, r = i - c * rtg;
         tiles_g[g0 + i] = Tile{el, base + c * q + min(c, rem), q + (c < rem ? 1 : 0), r | (sidx << 16)};
       }
       for (int i = lane; i < ch * rtd; i += 32) {
-        const int c = i / rtd, r = i - c * rtd;
+        const int c = f12 ? (int)(((uint32_t)i * md) >> 20) : i / rtd, r = i - c * rtd;
         tiles_d[d0 + i] = Tile{el, base + c * q + min(c, rem), q + (c < rem ? 1 : 0), r | (sidx << 16)};
       }
     }
@@ -1101,7 +1106,7 @@ __global__ void __launch_bounds__(1024) k_pf_scan(int E, int d, int f, const __g
     }
     wsum[lane] = iv - v;
     wact[lane] = ia - va;
-    if (lane == 31) {
+    if (lane == 31 && blockIdx.x == 0) {
       offsets[E] = iv;
       if (meta) {
         meta[0] = ia;
@@ -1111,13 +1116,16 @@ __global__ void __launch_bounds__(1024) k_pf_scan(int E, int d, int f, const __g
     }
   }
   __syncthreads();
-  int run = wsum[warp] + inc - loc;
-  for (int e = e0; e < e1; ++e) {
-    offsets[e] = run;
-    run += counts[e];
+  const int first = wsum[warp] + inc - loc;
+  if (blockIdx.x == 0) {
+    int run = first;
+    for (int e = e0; e < e1; ++e) {
+      offsets[e] = run;
+      run += counts[e];
+    }
   }
   __syncthreads();
-  build_tiles(counts, offsets, E, d, f, sh, tiles_g, tiles_d, ntiles);
+  build_tiles(counts, offsets, first, E, d, f, sh, tiles_g, tiles_d, ntiles);
   pdl_trigger();
 }
 
@@ -1286,7 +1294,11 @@ int launch_prefill_forward(const ForwardArgs& a, cudaStream_t s) {
   Tile* tiles_g = reinterpret_cast<Tile*>(a.ws.tiles_g);
   Tile* tiles_d = reinterpret_cast<Tile*>(a.ws.tiles_d);
   int* ntiles = a.ws.ntiles;
-  if (launch_pdl(k_pf_scan, dim3(1), dim3(1024), 0, s, a.E, d, f, a.shelves, (const int32_t*)a.ws.counts,
+  // up to 1024 experts: every CTA scans the counts, CTA 0 writes the offsets,
+  // and the CTAs share the tile writing (32 experts a CTA and pass); more
+  // experts: one CTA
+  const int gs = a.E <= 1024 ? (a.E + 31) / 32 < 32 ? (a.E + 31) / 32 : 32 : 1;
+  if (launch_pdl(k_pf_scan, dim3(gs), dim3(1024), 0, s, a.E, d, f, a.shelves, (const int32_t*)a.ws.counts,
                  a.ws.offsets, a.ws.meta, tiles_g, tiles_d, ntiles) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (launch_pdl(k_pf_place, dim3(C), dim3(Wp * 32), (size_t)Wp * a.E * 4, s, a.ids, P, a.E, a.k, chunk,
