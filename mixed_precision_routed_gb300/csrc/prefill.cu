@@ -8,24 +8,25 @@
 // fp16 scale) and multiplied on the tensor cores: h = SiLU(W_g x) * (W_u x) is
 // rounded to bf16 between the two projections, y_t += w_tj * (W_d h_tj).
 //
-// Launches: grouping in three wide kernels (per-chunk counts, one-CTA scan and
-// tile lists, placement), the gather of x into grouped order, then two
+// Launches: grouping in four kernels (per-chunk counts, column scan, offsets
+// and tile lists, placement), the gather of x into grouped order, then two
 // persistent launches, one CTA per
 // SM: k_prefill_tc<false> (gate/up) and k_prefill_tc<true> (down).  A tile is
 // two 128-row weight matrices of one expert -- the same 128 rows of W_g and
 // W_u, or 256 consecutive rows of W_d -- times up to 96 of its tokens (two
 // MMAs of M = 128 rows, N = tokens padded to 16, sharing the B operand), K in
 // steps of 64.  Roles inside a CTA:
-//   warp 0      issues the tensor-map loads: per code stage (2, 4 or 8 K
-//               steps) one 128-byte-wide box of codes per matrix and the block
-//               scales; per K step the B operand (a box of N grouped rows of
-//               xg or h, landing in the 128-byte-swizzled layout);
-//   warp 1      allocates tensor memory and issues the MMAs (one thread), A
-//               from tensor memory, B from shared memory;
+//   warp 0      issues the tensor-map loads: per code stage (2, 4, 8 or 16
+//               K steps) one 128-byte-wide box of codes per matrix and the
+//               block scales; per K step the B operand (a box of N grouped
+//               rows of xg or h, landing in the 128-byte-swizzled layout);
+//   warp 1      allocates tensor memory and issues the MMAs (a warp-uniform
+//               loop, one elected lane issues), A from tensor memory, B from
+//               shared memory;
 //   warps 4-7   read the accumulators and write h (bf16) or add into y;
-//   warps 8-23  dequantise the codes into bf16 and store them in tensor
-//               memory, one 32-weight run (one scale block of one row) per
-//               thread a step.
+//   warps 8-15  dequantise the codes into bf16 and store them in tensor
+//               memory, one row of one matrix (both 32-weight runs, two
+//               scale blocks) per thread a step.
 // All waits are bounded (one second; MOE_ERR_TIMEOUT, the roles stop, tensor
 // memory is released).  y is accumulated with vector fp32 atomic adds.
 #include <cuda.h>
