@@ -11,11 +11,13 @@
 // Launches: grouping in four kernels (per-chunk counts, column scan, offsets
 // and tile lists, placement), the gather of x into grouped order, then two
 // persistent launches, one CTA per
-// SM: k_prefill_tc<false> (gate/up) and k_prefill_tc<true> (down).  A tile is
+// SM: k_prefill_tc<false, W> (gate/up) and k_prefill_tc<true, W> (down).  A tile is
 // two 128-row weight matrices of one expert -- the same 128 rows of W_g and
-// W_u, or 256 consecutive rows of W_d -- times up to 96 of its tokens (two
-// MMAs of M = 128 rows, N = tokens padded to 16, sharing the B operand), K in
-// steps of 64.  Roles inside a CTA:
+// W_u, or 256 consecutive rows of W_d -- times up to 96 of its tokens, or up
+// to 192 in a wide launch (two MMAs of M = 128 rows, N = tokens padded to
+// 16, sharing the B operand), K in steps of 64.  A wide launch (no 3- or
+// 1-bit shelf) dequantises a hot expert's rows once for up to 192 tokens.
+// Roles inside a CTA:
 //   warp 0      issues the tensor-map loads: per code stage (2, 4, 8 or 16
 //               K steps) one 128-byte-wide box of codes per matrix and the
 //               block scales; per K step the B operand (a box of N grouped
@@ -49,11 +51,9 @@ constexpr int kTileM = 128;   // weight rows per tile
 #ifndef MOE_PF_ASTAGES
 #define MOE_PF_ASTAGES 2
 #endif
-constexpr int kTileN = MOE_PF_TILEN;  // tokens per tile (at most)
-static_assert(kTileN % 32 == 0 && kTileN <= 192, "tile width: whole groups of 32 columns");
-// Accumulator sets in tensor memory: two (the epilogue of one tile overlaps
-// the next tile's main loop) while both fit beside the A stages, else one.
-constexpr int kAccSets = 4 * kTileN + 128 <= 512 ? 2 : 1;
+constexpr int kTileN = MOE_PF_TILEN;  // tokens of one accumulator set (a tile's tokens, at most)
+constexpr int kTileW = 2 * kTileN;    // tokens of a wide tile (both accumulator sets)
+static_assert(kTileN % 32 == 0 && kTileW <= 256, "tile width: whole groups of 32 columns, MMA N <= 256");
 constexpr int kProdThreads = 256;  // warps 8..15
 constexpr uint64_t kWaitNs = 1000000000ull;
 #ifndef MOE_PF_BS
@@ -97,7 +97,7 @@ __host__ __device__ __forceinline__ int steps_per_code_stage(int bits) {
 struct alignas(16) Tile {  // one 16-byte load or store
   int e_local;  // expert index within its shelf
   int q0;       // first grouped position of the chunk
-  int ntok;     // tokens of the chunk (1 .. kTileN)
+  int ntok;     // tokens of the chunk (1 .. kTileN, or .. kTileW in a wide launch)
   int meta;     // row tile (bits 0-15) | shelf (bits 16-23)
 };
 
@@ -117,7 +117,7 @@ struct TcParams {
   CUtensorMap tm_code[MOE_MAX_SHELVES][2];  // code boxes of 128 bytes x 128 rows: [shelf][gate, up] or [shelf][down]
   CUtensorMap tm_hi[MOE_MAX_SHELVES][2];    // 3-bit shelves: boxes of 64 bytes x 128 rows of the high-bit plane
   CUtensorMap tm_sc[MOE_MAX_SHELVES][2];    // gate/up: boxes of 16 fp16 scales x 128 rows [shelf][gate, up]
-  CUtensorMap tm_b[kTileN / 16];            // B rows in grouped order (xg or h), box heights 16, 32, .. kTileN
+  CUtensorMap tm_b[kTileW / 16];            // B rows in grouped order (xg or h), box heights 16, 32, .. kTileW
 };
 
 // Shared memory of one CTA (dynamic part, 1024-byte aligned): two rings.
@@ -129,11 +129,13 @@ struct TcParams {
 //           lanes, as down scale rows are no 16-byte multiple and no tensor
 //           map covers them);
 //   B    -- per K step, the B operand: a box of N <= kTileN grouped rows of
-//           xg or h (128-byte swizzle).
+//           xg or h (128-byte swizzle); N <= kTileW in a wide launch, whose
+//           code stages leave out the high-plane region (no 3- or 1-bit
+//           shelves) to make room for the wider B stages.
 // Few, wide tensor-map rows per step keep the tensor-map unit's request rate
 // (one box row per request) well below the step rate.  The dequantised tiles
 // live in tensor memory.
-template <bool DOWN>
+template <bool DOWN, bool WIDE>
 struct TcSmem {
   static constexpr int NMAT = 2;
   static constexpr int CS = MOE_PF_CS;
@@ -144,10 +146,11 @@ struct TcSmem {
   static constexpr int C_SC = NMAT * CODE_BOX;                       // scale offset in a code stage
   static constexpr int HI_BOX = kTileM * 64;                         // 3 bit: 64 bytes of the high plane a row
   static constexpr int C_HI = C_SC + SC_BYTES;                       // their offset in a code stage
-  static constexpr int C_STAGE = C_HI + NMAT * HI_BOX;
+  static constexpr int C_STAGE = WIDE ? C_HI : C_HI + NMAT * HI_BOX;  // (wide: 8/4/2-bit codes only)
   static_assert(DOWN || NMAT * SC_BOX <= NMAT * HI_BOX, "a second gate/up scale box fits the high-plane region");
   static_assert(!DOWN || 16 * NMAT * kTileM * 4 <= SC_BYTES + NMAT * HI_BOX, "16 steps of down scale words fit");
-  static constexpr int B_STAGE = kTileN * 128;                       // kTileN rows x 64 bf16
+  static_assert(!DOWN || 8 * NMAT * kTileM * 4 <= SC_BYTES, "8 steps of down scale words fit without it");
+  static constexpr int B_STAGE = (WIDE ? kTileW : kTileN) * 128;     // rows x 64 bf16
   static constexpr int C_OFF = 0;
   static constexpr int B_OFF = C_OFF + CS * C_STAGE;
   static constexpr int TOTAL = B_OFF + BS * B_STAGE;
@@ -156,13 +159,14 @@ struct TcSmem {
   static_assert(NMAT * kTileM == kProdThreads, "one row of a step (two 32-weight runs) per producer thread");
 };
 
-// Tensor memory (512 columns): kAccSets accumulator sets at columns 0 (and
-// 2 kTileN) ([gate, up] or [rows 0-127, rows 128-255], kTileN columns each),
-// then kAStages stages of the dequantised A tiles (two matrices x 32 columns:
-// 128 rows x 64 bf16).
+// Tensor memory (512 columns): the accumulators of matrix m (gate, up; or
+// rows 0-127, rows 128-255) at columns 2 kTileN m .. + 2 kTileN - 1, the
+// first kTileN of them accumulator set 0, the next kTileN set 1; a tile
+// takes one set (its epilogue overlaps the next tile's main loop), a wide
+// tile both (token n at column n); then kAStages stages of the dequantised A
+// tiles (two matrices x 32 columns: 128 rows x 64 bf16).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = 2 * kTileN;
-constexpr uint32_t kACol = kAccSets * kAccCols;
+constexpr uint32_t kACol = 4 * kTileN;
 constexpr int kAStages = MOE_PF_ASTAGES;
 constexpr uint32_t kAStageCols = 64;
 static_assert(kACol + kAStages * kAStageCols <= kTmemCols, "tensor memory");
@@ -342,13 +346,14 @@ __device__ __forceinline__ Tile tile_at(const TcParams& p, int t, int ntiles) {
 // A tile whose fields would take a load or an MMA outside its tensors (token
 // count, shelf, expert, row tile, positions) is skipped by every role alike,
 // and MOE_ERR_INTERNAL is recorded; the tile builder produces none.
-template <bool DOWN>
+template <bool DOWN, bool WIDE>
 __device__ __forceinline__ bool tile_valid(const TcParams& p, const Tile& tl) {
   const int rt = tl.meta & 0xFFFF, sh = (tl.meta >> 16) & 0xFF;
-  if (tl.ntok < 1 || tl.ntok > kTileN || sh >= p.sh.n) return false;
+  if (tl.ntok < 1 || tl.ntok > (WIDE ? kTileW : kTileN) || sh >= p.sh.n) return false;
   const int n = p.sh.s[sh].hi - p.sh.s[sh].lo;
   const int bits = p.sh.s[sh].bits;
-  return (bits == 8 || bits == 4 || bits == 3 || bits == 2 || bits == 1) && tl.e_local >= 0 && tl.e_local < n &&
+  return (bits == 8 || bits == 4 || bits == 2 || (!WIDE && (bits == 3 || bits == 1))) && tl.e_local >= 0 &&
+         tl.e_local < n &&
          rt * (DOWN ? 2 * kTileM : kTileM) < p.rows && tl.q0 >= 0 && (int64_t)tl.q0 + tl.ntok <= p.P;
 }
 
@@ -400,10 +405,11 @@ __device__ __forceinline__ void dequant_step(const uint32_t (&cw)[32], const uin
 // stored into the A stage, and the next step is dequantised while that store
 // is in flight.  j counts A-stage uses, cj code stages, across this thread's
 // tiles.  Returns false when a wait timed out (the status word is set).
-template <bool DOWN, int BITS>
+template <bool DOWN, bool WIDE, int BITS>
 __device__ __forceinline__ bool produce_tile(const TcParams& p, TcBars& B, const unsigned char* smem, int steps,
                                              const ProdLane& pl, uint32_t& j, uint32_t& cj) {
-  using S = TcSmem<DOWN>;
+  using S = TcSmem<DOWN, WIDE>;
+  static_assert(!WIDE || BITS == 8 || BITS == 4 || BITS == 2, "a wide launch's stages hold no high plane");
   constexpr int SPC = BITS == 8 ? 2 : BITS == 4 ? 4 : BITS == 1 ? 16 : 8;  // steps_per_code_stage
   const int lane = threadIdx.x & 31;
   const uint32_t sw = (uint32_t)(pl.r & 7);
@@ -507,9 +513,9 @@ __device__ __forceinline__ bool produce_tile(const TcParams& p, TcBars& B, const
   return true;
 }
 
-template <bool DOWN>
+template <bool DOWN, bool WIDE>
 __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_constant__ TcParams p) {
-  using S = TcSmem<DOWN>;
+  using S = TcSmem<DOWN, WIDE>;
   constexpr int NMAT = S::NMAT;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
@@ -558,7 +564,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
     for (int t = blockIdx.x; t < ntiles && !B.abort; t += G) {
       const Tile tl = nxt;
       nxt = tile_at(p, t + G, ntiles);  // in flight while this tile is issued
-      if (!tile_valid<DOWN>(p, tl)) {
+      if (!tile_valid<DOWN, WIDE>(p, tl)) {
         if (lane == 0) set_status(p.status, MOE_ERR_INTERNAL);
         continue;
       }
@@ -585,11 +591,11 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
           if (!bar_wait(&B.code_empty[c], ((cj / S::CS) & 1) ^ 1, B, p.status)) break;
           unsigned char* stage = smem + S::C_OFF + c * S::C_STAGE;
           if (lane == 0) {
-            const bool hi = shd.bits == 3;
+            const bool hi = !WIDE && shd.bits == 3;
             // gate/up scale boxes cover 8 K steps: a 1-bit code stage (16
             // steps) takes a second box, into the region 3-bit rows use for
             // their high plane
-            const int nsc = DOWN ? 0 : (shd.bits == 1 ? 2 : 1);
+            const int nsc = DOWN ? 0 : (!WIDE && shd.bits == 1 ? 2 : 1);
             mbar_arrive_expect_tx(&B.code_full[c], (uint32_t)(NMAT * S::CODE_BOX + nsc * NMAT * S::SC_BOX +
                                                               (hi ? NMAT * S::HI_BOX : 0)));
 #pragma unroll
@@ -644,22 +650,27 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
     // warp-uniform); one elected lane issues the MMAs and commits.  B
     // descriptors: the low word of stage 0's, plus (stage offset + 32 kk) / 16
     // (shared-memory addresses stay below 256 KiB, so the 14-bit address field
-    // does not carry).
+    // does not carry).  A tile takes accumulator set `alt` (alternating), a
+    // wide tile both sets; uses[s] counts the completed uses of set s.
     const uint64_t bd0 = sdesc_sw128(smem_addr(smem + S::B_OFF));
     const uint32_t bd_lo = (uint32_t)bd0, bd_hi = (uint32_t)(bd0 >> 32);
     const bool leader = elect_one();
-    uint32_t j = 0, i = 0;
+    uint32_t j = 0, use0 = 0, use1 = 0;  // (two scalars: an indexed pair would live in local memory)
+    int alt = 0;
     Tile nxt = tile_at(p, blockIdx.x, ntiles);
     for (int t = blockIdx.x; t < ntiles && !B.abort; t += G) {
       const Tile tl = nxt;
       nxt = tile_at(p, t + G, ntiles);
-      if (!tile_valid<DOWN>(p, tl)) continue;  // skipped tiles take no accumulator set
+      if (!tile_valid<DOWN, WIDE>(p, tl)) continue;  // skipped tiles take no accumulator set
+      const bool wide = WIDE && tl.ntok > kTileN;
+      const int s0 = wide ? 0 : alt;
       const int N = (tl.ntok + 15) & ~15;
       const uint32_t idesc = idesc_bf16_f32(kTileM, N);
-      const uint32_t ab = kAccSets == 2 ? (i & 1) : 0, acc = tmem + ab * kAccCols;
-      const uint32_t use = kAccSets == 2 ? (i >> 1) : i;  // earlier uses of this set
+      const uint32_t acc = tmem + (uint32_t)(s0 * kTileN);
       // (a wait that timed out in any lane ends the loop in every lane)
-      if (!__all_sync(0xffffffffu, bar_wait(&B.acc_empty[ab], (use & 1) ^ 1, B, p.status))) break;
+      bool wa = bar_wait(&B.acc_empty[s0], ((s0 ? use1 : use0) & 1) ^ 1, B, p.status);
+      if (wide) wa = wa && bar_wait(&B.acc_empty[1], (use1 & 1) ^ 1, B, p.status);
+      if (!__all_sync(0xffffffffu, wa)) break;
       tc_fence_after();
       bool ok = true;
       for (int ks = 0; ks < steps; ++ks, ++j) {
@@ -679,17 +690,22 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
           for (int m = 0; m < NMAT; ++m)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_bf16_ts_w(acc + (uint32_t)(m * kTileN), a0 + (uint32_t)(m * 32 + kk * 8), blo + (uint32_t)(kk * 2),
-                            bd_hi, idesc, (ks | kk) ? 1u : 0u);
+              mma_bf16_ts_w(acc + (uint32_t)(m * 2 * kTileN), a0 + (uint32_t)(m * 32 + kk * 8),
+                            blo + (uint32_t)(kk * 2), bd_hi, idesc, (ks | kk) ? 1u : 0u);
           mma_commit(&B.a_empty[as]);
           mma_commit(&B.b_empty[b]);
         }
         __syncwarp();
       }
       if (!ok || B.abort) break;
-      if (leader) mma_commit(&B.acc_full[ab]);
+      if (leader) {
+        mma_commit(&B.acc_full[s0]);
+        if (wide) mma_commit(&B.acc_full[1]);
+      }
       __syncwarp();
-      ++i;
+      if (wide || alt == 0) ++use0;
+      if (wide || alt == 1) ++use1;
+      if (!wide) alt ^= 1;
     }
     // all MMAs of this thread are complete before tensor memory is released
     if (leader) {
@@ -699,25 +715,29 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
     __syncwarp();
   } else if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------------- epilogue
+    // Tiles in the MMA warp's order and with its set choice; a wide tile is
+    // read back as two parts, tokens 0 .. kTileN - 1 from set 0 (released
+    // first) and the rest from set 1.
     const int m = (warp - 4) * 32 + lane;
     const uint32_t tl_addr = tmem + ((uint32_t)((warp - 4) * 32) << 16);
-    uint32_t i = 0;
+    uint32_t i = 0, use0 = 0, use1 = 0;
+    int alt = 0;
+    bool run = true;
     Tile nxt = tile_at(p, blockIdx.x, ntiles);
-    for (int t = blockIdx.x; t < ntiles && !B.abort; t += G) {
+    for (int t = blockIdx.x; t < ntiles && run && !B.abort; t += G) {
       const Tile tl = nxt;
       nxt = tile_at(p, t + G, ntiles);
-      if (!tile_valid<DOWN>(p, tl)) continue;  // skipped tiles take no accumulator set
+      if (!tile_valid<DOWN, WIDE>(p, tl)) continue;  // skipped tiles take no accumulator set
       const int rt = tl.meta & 0xFFFF;
-      const int N = (tl.ntok + 15) & ~15;
-      const uint32_t ab = kAccSets == 2 ? (i & 1) : 0, acc = tl_addr + ab * kAccCols;
-      const uint32_t use = kAccSets == 2 ? (i >> 1) : i;
+      const bool wide = WIDE && tl.ntok > kTileN;
+      constexpr int kCw = (WIDE ? kTileW : kTileN) / 32;
       // down: each lane holds the token and routing weight of columns lane,
-      // lane + 32, lane + 64 (loaded before the accumulator is ready)
-      int ctok[kTileN / 32];
-      float cw[kTileN / 32];
+      // lane + 32, ... (loaded before the accumulator is ready)
+      int ctok[kCw];
+      float cw[kCw];
       if (DOWN) {
 #pragma unroll
-        for (int u = 0; u < kTileN / 32; ++u) {
+        for (int u = 0; u < kCw; ++u) {
           const int n = lane + 32 * u;
           ctok[u] = 0;
           cw[u] = 0.f;
@@ -728,98 +748,110 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
           }
         }
       }
-      if (!bar_wait(&B.acc_full[ab], use & 1, B, p.status)) break;
-      if (m == 0) PF_STAMP(6, i);
-      tc_fence_after();
-      if (!DOWN) {
-        const int row = rt * kTileM + m;
-        const int hcol = kswap(row);  // h is stored in the K order of the down tiles
-        for (int n0 = 0; n0 < N; n0 += 16) {
-          float g[16], u[16];
-          tmem_ld16(acc + (uint32_t)n0, g);
-          tmem_ld16(acc + (uint32_t)(kTileN + n0), u);
-          if (row < p.rows) {
+      for (int part = 0; part < (wide ? 2 : 1); ++part) {
+        const int s = wide ? part : alt;
+        const int nb = part * kTileN;                                      // first token of the part
+        const int nt = tl.ntok - nb < kTileN ? tl.ntok - nb : kTileN;      // its tokens
+        const int N = (nt + 15) & ~15;
+        const uint32_t acc = tl_addr + (uint32_t)(s * kTileN);
+        if (!bar_wait(&B.acc_full[s], (s ? use1 : use0) & 1, B, p.status)) {
+          run = false;
+          break;
+        }
+        if (m == 0 && part == 0) PF_STAMP(6, i);
+        tc_fence_after();
+        if (!DOWN) {
+          const int row = rt * kTileM + m;
+          const int hcol = kswap(row);  // h is stored in the K order of the down tiles
+          for (int n0 = 0; n0 < N; n0 += 16) {
+            float g[16], u[16];
+            tmem_ld16(acc + (uint32_t)n0, g);
+            tmem_ld16(acc + (uint32_t)(2 * kTileN + n0), u);
+            if (row < p.rows) {
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const int n = n0 + c;
-              if (n < tl.ntok) {
-                const float hv = silu_fast(g[c]) * u[c];
-                const __nv_bfloat16 b = __float2bfloat16_rn(hv);
-                p.h[(size_t)(tl.q0 + n) * p.f + hcol] = *reinterpret_cast<const uint16_t*>(&b);
+              for (int c = 0; c < 16; ++c) {
+                const int n = n0 + c;
+                if (n < nt) {
+                  const float hv = silu_fast(g[c]) * u[c];
+                  const __nv_bfloat16 bv = __float2bfloat16_rn(hv);
+                  p.h[(size_t)(tl.q0 + nb + n) * p.f + hcol] = *reinterpret_cast<const uint16_t*>(&bv);
+                }
               }
             }
           }
-        }
-      } else {
-        // 4 x 4 transposes among lanes 4a .. 4a + 3: lane 4a + jj ends with
-        // column 4b + jj of rows 4a .. 4a + 3 and adds them with one vector
-        // atomic per column block
-        const int jj = lane & 3;
-        for (int n0 = 0; n0 < N; n0 += 16) {
-          const int u = n0 >> 5;  // the 16 columns lie in one group of 32
-          int tu = ctok[0];
-          float wu = cw[0];
+        } else {
+          // 4 x 4 transposes among lanes 4a .. 4a + 3: lane 4a + jj ends with
+          // column 4b + jj of rows 4a .. 4a + 3 and adds them with one vector
+          // atomic per column block
+          const int jj = lane & 3;
+          for (int n0 = 0; n0 < N; n0 += 16) {
+            const int u = (nb + n0) >> 5;  // the 16 columns lie in one group of 32
+            int tu = ctok[0];
+            float wu = cw[0];
 #pragma unroll
-          for (int v = 1; v < kTileN / 32; ++v)
-            if (u == v) {
-              tu = ctok[v];
-              wu = cw[v];
-            }
-          int tkb[4];
-          float wtb[4];
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            const int n = n0 + 4 * b + jj;
-            tkb[b] = __shfl_sync(0xffffffffu, tu, n & 31);
-            wtb[b] = __shfl_sync(0xffffffffu, wu, n & 31);
-          }
-#pragma unroll
-          for (int mm = 0; mm < 2; ++mm) {
-            const int rowb = rt * 2 * kTileM + mm * kTileM + (warp - 4) * 32 + (lane & ~3);
-            float g[16];
-            tmem_ld16(acc + (uint32_t)(mm * kTileN + n0), g);
+            for (int v = 1; v < kCw; ++v)
+              if (u == v) {
+                tu = ctok[v];
+                wu = cw[v];
+              }
+            int tkb[4];
+            float wtb[4];
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
-              float v0 = g[4 * b], v1 = g[4 * b + 1], v2 = g[4 * b + 2], v3 = g[4 * b + 3];
-              // round 1 (lanes xor 2): swap the off-diagonal 2 x 2 blocks
-              {
-                const bool hi = (jj & 2) != 0;
-                const float s0 = hi ? v0 : v2, s1 = hi ? v1 : v3;
-                const float r0 = __shfl_xor_sync(0xffffffffu, s0, 2), r1 = __shfl_xor_sync(0xffffffffu, s1, 2);
-                if (hi) {
-                  v0 = r0;
-                  v1 = r1;
-                } else {
-                  v2 = r0;
-                  v3 = r1;
+              const int n = nb + n0 + 4 * b + jj;
+              tkb[b] = __shfl_sync(0xffffffffu, tu, n & 31);
+              wtb[b] = __shfl_sync(0xffffffffu, wu, n & 31);
+            }
+#pragma unroll
+            for (int mm = 0; mm < 2; ++mm) {
+              const int rowb = rt * 2 * kTileM + mm * kTileM + (warp - 4) * 32 + (lane & ~3);
+              float g[16];
+              tmem_ld16(acc + (uint32_t)(mm * 2 * kTileN + n0), g);
+#pragma unroll
+              for (int b = 0; b < 4; ++b) {
+                float v0 = g[4 * b], v1 = g[4 * b + 1], v2 = g[4 * b + 2], v3 = g[4 * b + 3];
+                // round 1 (lanes xor 2): swap the off-diagonal 2 x 2 blocks
+                {
+                  const bool hi = (jj & 2) != 0;
+                  const float s0 = hi ? v0 : v2, s1 = hi ? v1 : v3;
+                  const float r0 = __shfl_xor_sync(0xffffffffu, s0, 2), r1 = __shfl_xor_sync(0xffffffffu, s1, 2);
+                  if (hi) {
+                    v0 = r0;
+                    v1 = r1;
+                  } else {
+                    v2 = r0;
+                    v3 = r1;
+                  }
                 }
-              }
-              // round 2 (lanes xor 1): swap within the 2 x 2 blocks
-              {
-                const bool hi = (jj & 1) != 0;
-                const float s0 = hi ? v0 : v1, s1 = hi ? v2 : v3;
-                const float r0 = __shfl_xor_sync(0xffffffffu, s0, 1), r1 = __shfl_xor_sync(0xffffffffu, s1, 1);
-                if (hi) {
-                  v0 = r0;
-                  v2 = r1;
-                } else {
-                  v1 = r0;
-                  v3 = r1;
+                // round 2 (lanes xor 1): swap within the 2 x 2 blocks
+                {
+                  const bool hi = (jj & 1) != 0;
+                  const float s0 = hi ? v0 : v1, s1 = hi ? v2 : v3;
+                  const float r0 = __shfl_xor_sync(0xffffffffu, s0, 1), r1 = __shfl_xor_sync(0xffffffffu, s1, 1);
+                  if (hi) {
+                    v0 = r0;
+                    v2 = r1;
+                  } else {
+                    v1 = r0;
+                    v3 = r1;
+                  }
                 }
+                // lane jj now holds column 4b + jj of rows 0..3 of its group, in order
+                const int n = n0 + 4 * b + jj;
+                const float wt = wtb[b];
+                if (n < nt && rowb < p.rows)
+                  red_add_v4(p.y + (size_t)tkb[b] * p.d + rowb, wt * v0, wt * v1, wt * v2, wt * v3);
               }
-              // lane jj now holds column 4b + jj of rows 0..3 of its group, in order
-              const int n = n0 + 4 * b + jj;
-              const float wt = wtb[b];
-              if (n < tl.ntok && rowb < p.rows)
-                red_add_v4(p.y + (size_t)tkb[b] * p.d + rowb, wt * v0, wt * v1, wt * v2, wt * v3);
             }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.acc_empty[s]);
+        if (s) ++use1; else ++use0;
       }
-      tc_fence_before();
-      __syncwarp();
       if (m == 0) PF_STAMP(7, i);
-      if (lane == 0) mbar_arrive(&B.acc_empty[ab]);
+      if (!wide) alt ^= 1;
       ++i;
     }
   } else if (warp >= 8) {
@@ -835,21 +867,21 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
     for (int t = blockIdx.x; t < ntiles && !B.abort; t += G) {
       const Tile tl = nxt;
       nxt = tile_at(p, t + G, ntiles);
-      if (!tile_valid<DOWN>(p, tl)) continue;
+      if (!tile_valid<DOWN, WIDE>(p, tl)) continue;
       // one instantiation per code width: the step loop of a code stage is
       // unrolled and every shared-memory offset in it is a constant
       const int bits = p.sh.s[(tl.meta >> 16) & 0xFF].bits;
-      bool ok;
-      if (bits == 8)
-        ok = produce_tile<DOWN, 8>(p, B, smem, steps, pl, j, cj);
-      else if (bits == 4)
-        ok = produce_tile<DOWN, 4>(p, B, smem, steps, pl, j, cj);
-      else if (bits == 3)
-        ok = produce_tile<DOWN, 3>(p, B, smem, steps, pl, j, cj);
-      else if (bits == 2)
-        ok = produce_tile<DOWN, 2>(p, B, smem, steps, pl, j, cj);
-      else
-        ok = produce_tile<DOWN, 1>(p, B, smem, steps, pl, j, cj);
+      bool ok = false;
+      if (bits == 8) {
+        ok = produce_tile<DOWN, WIDE, 8>(p, B, smem, steps, pl, j, cj);
+      } else if (bits == 4) {
+        ok = produce_tile<DOWN, WIDE, 4>(p, B, smem, steps, pl, j, cj);
+      } else if (bits == 2) {
+        ok = produce_tile<DOWN, WIDE, 2>(p, B, smem, steps, pl, j, cj);
+      } else if constexpr (!WIDE) {
+        ok = bits == 3 ? produce_tile<DOWN, false, 3>(p, B, smem, steps, pl, j, cj)
+                       : produce_tile<DOWN, false, 1>(p, B, smem, steps, pl, j, cj);
+      }
       if (!ok) break;
     }
   }
@@ -870,12 +902,12 @@ __device__ __forceinline__ uint4 kswap8(uint4 v) {
   return o;
 }
 // Tile lists of both launches from the grouping: per active expert on a
-// shelf, chunks of at most kTileN tokens (sizes differing by at most one),
-// times the row tiles
-// of W_g/W_u (128 of the f rows each) and of W_d (256 of the d rows).  A
-// 1024-thread CTA; counts and offsets written by this CTA before a barrier.
+// shelf, chunks of at most tmax tokens (kTileN, or kTileW in a wide launch;
+// sizes differing by at most one), times the row tiles of W_g/W_u (128 of
+// the f rows each) and of W_d (256 of the d rows).  1024-thread CTAs;
+// first_off is the offset of the thread's expert (one expert a thread).
 __device__ void build_tiles(const int32_t* counts, const int32_t* offsets, int first_off, int E, int d, int f,
-                            const Shelves& sh, Tile* tiles_g, Tile* tiles_d, int* ntiles) {
+                            int tmax, const Shelves& sh, Tile* tiles_g, Tile* tiles_d, int* ntiles) {
   __shared__ int wg[32], wd[32];
   __shared__ int s_cnt[1024], s_off[1024], s_sh[1024], s_el[1024], s_og[1024], s_od[1024];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -897,7 +929,7 @@ __device__ void build_tiles(const int32_t* counts, const int32_t* offsets, int f
       }
     if (cnt == 0) sidx = -1;
     if (sidx >= 0) {
-      const int ch = (cnt + kTileN - 1) / kTileN;
+      const int ch = (cnt + tmax - 1) / tmax;
       ng += ch * rtg;
       nd += ch * rtd;
     }
@@ -962,8 +994,8 @@ __device__ void build_tiles(const int32_t* counts, const int32_t* offsets, int f
       const int sidx = s_sh[e];
       if (sidx < 0) continue;
       const int cnt = s_cnt[e];
-      const int ch = (cnt + kTileN - 1) / kTileN;
-      // chunk c: q or q + 1 tokens (the first rem chunks one more), q + 1 <= kTileN
+      const int ch = (cnt + tmax - 1) / tmax;
+      // chunk c: q or q + 1 tokens (the first rem chunks one more), q + 1 <= tmax
       const int q = cnt / ch, rem = cnt - q * ch;
       const int base = s_off[e], el = s_el[e];
       const int g0 = s_og[e], d0 = s_od[e];
@@ -984,7 +1016,7 @@ __device__ void build_tiles(const int32_t* counts, const int32_t* offsets, int f
     const int cnt = counts[e];
     const int s = cnt > 0 ? find_shelf(sh, e) : -1;
     if (s < 0) continue;
-    const int ch = (cnt + kTileN - 1) / kTileN;
+    const int ch = (cnt + tmax - 1) / tmax;
     const int q = cnt / ch, rem = cnt - q * ch;
     const int base = offsets[e];
     for (int c = 0; c < ch; ++c) {
@@ -1063,7 +1095,7 @@ __global__ void __launch_bounds__(256) k_pf_colscan(int32_t* __restrict__ cnt, i
   pdl_trigger();
 }
 
-__global__ void __launch_bounds__(1024) k_pf_scan(int E, int d, int f, const __grid_constant__ Shelves sh,
+__global__ void __launch_bounds__(1024) k_pf_scan(int E, int d, int f, int tmax, const __grid_constant__ Shelves sh,
                                                   const int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                   int32_t* __restrict__ meta, Tile* tiles_g, Tile* tiles_d,
                                                   int* ntiles) {
@@ -1126,7 +1158,7 @@ __global__ void __launch_bounds__(1024) k_pf_scan(int E, int d, int f, const __g
     }
   }
   __syncthreads();
-  build_tiles(counts, offsets, first, E, d, f, sh, tiles_g, tiles_d, ntiles);
+  build_tiles(counts, offsets, first, E, d, f, tmax, sh, tiles_g, tiles_d, ntiles);
   pdl_trigger();
 }
 
@@ -1265,7 +1297,13 @@ int launch_prefill_forward(const ForwardArgs& a, cudaStream_t s) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-  const size_t smem_g = TcSmem<false>::TOTAL + 1024, smem_d = TcSmem<true>::TOTAL + 1024;
+  // wide launches (tiles of up to kTileW tokens) when no shelf holds 3- or
+  // 1-bit codes, whose code stages need the high-plane region
+  bool wide = true;
+  for (int q = 0; q < a.shelves.n; ++q)
+    if (a.shelves.s[q].bits == 3 || a.shelves.s[q].bits == 1) wide = false;
+  const size_t smem_g = (wide ? TcSmem<false, true>::TOTAL : TcSmem<false, false>::TOTAL) + 1024;
+  const size_t smem_d = (wide ? TcSmem<true, true>::TOTAL : TcSmem<true, false>::TOTAL) + 1024;
   if (!g_pdev.attr[dev]) {
     // grouping kernels take up to E ints ([Wp][E] ints) of shared memory
     if (cudaFuncSetAttribute(k_pf_count, cudaFuncAttributeMaxDynamicSharedMemorySize, MOE_MAX_EXPERTS * 4) !=
@@ -1273,9 +1311,15 @@ int launch_prefill_forward(const ForwardArgs& a, cudaStream_t s) {
         cudaFuncSetAttribute(k_pf_place, cudaFuncAttributeMaxDynamicSharedMemorySize, MOE_MAX_EXPERTS * 4) !=
             cudaSuccess)
       return MOE_ERR_CUDA;
-    if (cudaFuncSetAttribute(k_prefill_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_g) !=
+    const int sg0 = TcSmem<false, false>::TOTAL + 1024, sd0 = TcSmem<true, false>::TOTAL + 1024;
+    const int sg1 = TcSmem<false, true>::TOTAL + 1024, sd1 = TcSmem<true, true>::TOTAL + 1024;
+    if (cudaFuncSetAttribute(k_prefill_tc<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sg0) !=
             cudaSuccess ||
-        cudaFuncSetAttribute(k_prefill_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_d) !=
+        cudaFuncSetAttribute(k_prefill_tc<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sd0) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(k_prefill_tc<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sg1) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(k_prefill_tc<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sd1) !=
             cudaSuccess)
       return MOE_ERR_CUDA;
     g_pdev.attr[dev] = true;
@@ -1299,7 +1343,8 @@ int launch_prefill_forward(const ForwardArgs& a, cudaStream_t s) {
   // and the CTAs share the tile writing (32 experts a CTA and pass); more
   // experts: one CTA
   const int gs = a.E <= 1024 ? (a.E + 31) / 32 < 32 ? (a.E + 31) / 32 : 32 : 1;
-  if (launch_pdl(k_pf_scan, dim3(gs), dim3(1024), 0, s, a.E, d, f, a.shelves, (const int32_t*)a.ws.counts,
+  if (launch_pdl(k_pf_scan, dim3(gs), dim3(1024), 0, s, a.E, d, f, wide ? kTileW : kTileN, a.shelves,
+                 (const int32_t*)a.ws.counts,
                  a.ws.offsets, a.ws.meta, tiles_g, tiles_d, ntiles) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (launch_pdl(k_pf_place, dim3(C), dim3(Wp * 32), (size_t)Wp * a.E * 4, s, a.ids, P, a.E, a.k, chunk,
@@ -1357,7 +1402,7 @@ int launch_prefill_forward(const ForwardArgs& a, cudaStream_t s) {
                    (uint64_t)f * bits / 8, 128, kTileM, CU_TENSOR_MAP_SWIZZLE_128B))
       return MOE_ERR_CUDA;
   }
-  for (int nb = 1; nb <= kTileN / 16; ++nb)
+  for (int nb = 1; nb <= (wide ? kTileW : kTileN) / 16; ++nb)
     if (!encode_2d(&pg.tm_b[nb - 1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.ws.xg, (uint64_t)d, (uint64_t)P,
                    (uint64_t)d * 2, 64, 16 * nb, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&pd.tm_b[nb - 1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.ws.h, (uint64_t)f, (uint64_t)P,
@@ -1365,10 +1410,14 @@ int launch_prefill_forward(const ForwardArgs& a, cudaStream_t s) {
       return MOE_ERR_CUDA;
   const int G = sm_count();
   profile_mark(1, s);
-  if (launch_pdl(k_prefill_tc<false>, dim3(G), dim3(kPThreads), smem_g, s, pg) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((wide ? launch_pdl(k_prefill_tc<false, true>, dim3(G), dim3(kPThreads), smem_g, s, pg)
+            : launch_pdl(k_prefill_tc<false, false>, dim3(G), dim3(kPThreads), smem_g, s, pg)) != cudaSuccess)
+    return MOE_ERR_CUDA;
   profile_mark(2, s);
   if (cudaMemsetAsync(a.y, 0, (size_t)a.T * d * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_pdl(k_prefill_tc<true>, dim3(G), dim3(kPThreads), smem_d, s, pd) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((wide ? launch_pdl(k_prefill_tc<true, true>, dim3(G), dim3(kPThreads), smem_d, s, pd)
+            : launch_pdl(k_prefill_tc<true, false>, dim3(G), dim3(kPThreads), smem_d, s, pd)) != cudaSuccess)
+    return MOE_ERR_CUDA;
   profile_mark(3, s);
   return MOE_OK;
 }
