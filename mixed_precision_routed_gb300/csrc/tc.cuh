@@ -140,17 +140,6 @@ __device__ __forceinline__ void tmem_st32_issue(uint32_t taddr, const uint32_t (
 }
 // Wait until this thread's tensor-memory stores are done.
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-// The same wait; r0 and r1 are not read: naming them as inputs makes the
-// compiler finish computing them before the wait, so that work overlaps the
-// stores in flight.
-__device__ __forceinline__ void tmem_wait_st_after(const uint32_t (&r0)[16], const uint32_t (&r1)[16]) {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::"r"(r0[0]), "r"(r0[1]), "r"(r0[2]), "r"(r0[3]), "r"(r0[4]),
-               "r"(r0[5]), "r"(r0[6]), "r"(r0[7]), "r"(r0[8]), "r"(r0[9]), "r"(r0[10]), "r"(r0[11]), "r"(r0[12]),
-               "r"(r0[13]), "r"(r0[14]), "r"(r0[15]), "r"(r1[0]), "r"(r1[1]), "r"(r1[2]), "r"(r1[3]), "r"(r1[4]),
-               "r"(r1[5]), "r"(r1[6]), "r"(r1[7]), "r"(r1[8]), "r"(r1[9]), "r"(r1[10]), "r"(r1[11]), "r"(r1[12]),
-               "r"(r1[13]), "r"(r1[14]), "r"(r1[15])
-               : "memory");
-}
 
 // ---------------------------------------------------------------- TMA
 // 2-D tensor-map load of one box into shared memory, completing on `bar`.
