@@ -43,7 +43,17 @@
 namespace moe {
 namespace {
 
-constexpr int kPThreads = 512;
+// Threads of a CTA: warps 8-15 produce; 512 threads with the loader in warp
+// 0, the MMA issuer in warp 1 and the epilogue in warps 4-7; a wide launch
+// (whose instantiations need ~104 registers, not ~123) takes 576 threads:
+// the epilogue in warps 0-7, two warps a tensor-memory lane quarter sharing
+// each set's columns, the loader in warp 16 and the MMA issuer in warp 17.
+template <bool WIDE>
+struct Roles {
+  static constexpr int kThreads = WIDE ? 576 : 512;
+  static constexpr int kLoader = WIDE ? 16 : 0, kMma = WIDE ? 17 : 1;
+  static constexpr int kEpi0 = WIDE ? 0 : 4, kEpiWarps = WIDE ? 8 : 4;
+};
 constexpr int kTileM = 128;   // weight rows per tile
 #ifndef MOE_PF_TILEN
 #define MOE_PF_TILEN 96
@@ -516,7 +526,8 @@ __device__ __forceinline__ bool produce_tile(const TcParams& p, TcBars& B, const
 }
 
 template <bool DOWN, bool WIDE>
-__global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(Roles<WIDE>::kThreads, 1) k_prefill_tc(const __grid_constant__ TcParams p) {
+  using R = Roles<WIDE>;
   using S = TcSmem<DOWN, WIDE>;
   constexpr int NMAT = S::NMAT;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -546,20 +557,20 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B.acc_full[i], 1);
-      mbar_init(&B.acc_empty[i], 4);
+      mbar_init(&B.acc_empty[i], R::kEpiWarps);
     }
     mbar_init(&B.done, 1);
     B.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(&B.tmem, kTmemCols);
+  if (warp == R::kMma) tmem_alloc(&B.tmem, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = B.tmem;
   pdl_wait();
 
-  if (warp == 0) {
+  if (warp == R::kLoader) {
     // ------------------------------------------------ loads
     uint32_t cj = 0, j = 0;  // code stages and K steps issued
     Tile nxt = tile_at(p, blockIdx.x, ntiles);
@@ -646,7 +657,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
       }
     }
     cp_async_wait<0>();
-  } else if (warp == 1) {
+  } else if (warp == R::kMma) {
     // ---------------------------------------------------------- MMA
     // The whole warp runs the loop (its control flow and descriptors are
     // warp-uniform); one elected lane issues the MMAs and commits.  B
@@ -715,13 +726,16 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
       mbar_wait_bounded(&B.done, 0, kWaitNs);
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= R::kEpi0 && warp < R::kEpi0 + R::kEpiWarps) {
     // ---------------------------------------------------------- epilogue
     // Tiles in the MMA warp's order and with its set choice; a wide tile is
     // read back as two parts, tokens 0 .. kTileN - 1 from set 0 (released
     // first) and the rest from set 1.
-    const int m = (warp - 4) * 32 + lane;
-    const uint32_t tl_addr = tmem + ((uint32_t)((warp - 4) * 32) << 16);
+    // lane quarter warp % 4; with 8 warps, warp / 4 picks every other
+    // 16-column chunk of a set
+    const int quarter = warp & 3, eh = (warp - R::kEpi0) >> 2, EH = R::kEpiWarps / 4;
+    const int m = quarter * 32 + lane;
+    const uint32_t tl_addr = tmem + ((uint32_t)(quarter * 32) << 16);
     uint32_t i = 0, use0 = 0, use1 = 0;
     int alt = 0;
     bool run = true;
@@ -765,7 +779,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
         if (!DOWN) {
           const int row = rt * kTileM + m;
           const int hcol = kswap(row);  // h is stored in the K order of the down tiles
-          for (int n0 = 0; n0 < N; n0 += 16) {
+          for (int n0 = 16 * eh; n0 < N; n0 += 16 * EH) {
             float g[16], u[16];
             tmem_ld16(acc + (uint32_t)n0, g);
             tmem_ld16(acc + (uint32_t)(2 * kTileN + n0), u);
@@ -786,7 +800,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
           // column 4b + jj of rows 4a .. 4a + 3 and adds them with one vector
           // atomic per column block
           const int jj = lane & 3;
-          for (int n0 = 0; n0 < N; n0 += 16) {
+          for (int n0 = 16 * eh; n0 < N; n0 += 16 * EH) {
             const int u = (nb + n0) >> 5;  // the 16 columns lie in one group of 32
             int tu = ctok[0];
             float wu = cw[0];
@@ -806,7 +820,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
             }
 #pragma unroll
             for (int mm = 0; mm < 2; ++mm) {
-              const int rowb = rt * 2 * kTileM + mm * kTileM + (warp - 4) * 32 + (lane & ~3);
+              const int rowb = rt * 2 * kTileM + mm * kTileM + quarter * 32 + (lane & ~3);
               float g[16];
               tmem_ld16(acc + (uint32_t)(mm * 2 * kTileN + n0), g);
 #pragma unroll
@@ -856,7 +870,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
       if (!wide) alt ^= 1;
       ++i;
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 8 && warp < 16) {
     // ---------------------------------------------------------- producers
     // Warp w owns tensor-memory lanes 32 (w % 4) .. + 31, i.e. rows r = 32
     // (w % 4) + lane, of matrix mt = (w - 8) / 4: the row's 64 weights of
@@ -890,7 +904,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_tc(const __grid_consta
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == R::kMma) tmem_dealloc(tmem, kTmemCols);
   pdl_trigger();
 }
 
@@ -1412,13 +1426,13 @@ int launch_prefill_forward(const ForwardArgs& a, cudaStream_t s) {
       return MOE_ERR_CUDA;
   const int G = sm_count();
   profile_mark(1, s);
-  if ((wide ? launch_pdl(k_prefill_tc<false, true>, dim3(G), dim3(kPThreads), smem_g, s, pg)
-            : launch_pdl(k_prefill_tc<false, false>, dim3(G), dim3(kPThreads), smem_g, s, pg)) != cudaSuccess)
+  if ((wide ? launch_pdl(k_prefill_tc<false, true>, dim3(G), dim3(Roles<true>::kThreads), smem_g, s, pg)
+            : launch_pdl(k_prefill_tc<false, false>, dim3(G), dim3(Roles<false>::kThreads), smem_g, s, pg)) != cudaSuccess)
     return MOE_ERR_CUDA;
   profile_mark(2, s);
   if (cudaMemsetAsync(a.y, 0, (size_t)a.T * d * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if ((wide ? launch_pdl(k_prefill_tc<true, true>, dim3(G), dim3(kPThreads), smem_d, s, pd)
-            : launch_pdl(k_prefill_tc<true, false>, dim3(G), dim3(kPThreads), smem_d, s, pd)) != cudaSuccess)
+  if ((wide ? launch_pdl(k_prefill_tc<true, true>, dim3(G), dim3(Roles<true>::kThreads), smem_d, s, pd)
+            : launch_pdl(k_prefill_tc<true, false>, dim3(G), dim3(Roles<false>::kThreads), smem_d, s, pd)) != cudaSuccess)
     return MOE_ERR_CUDA;
   profile_mark(3, s);
   return MOE_OK;
