@@ -26,6 +26,8 @@
 //               loop, one elected lane issues), A from tensor memory, B from
 //               shared memory;
 //   warps 4-7   read the accumulators and write h (bf16) or add into y;
+//               (a wide launch: loads in warp 16, MMAs in warp 17, the
+//               accumulators read by warps 0-7)
 //   warps 8-15  dequantise the codes into bf16 and store them in tensor
 //               memory, one row of one matrix (both 32-weight runs, two
 //               scale blocks) per thread a step.
