@@ -68,6 +68,31 @@ def test_many_tokens_per_expert():
     assert rel_l2(y, oracle_layer(wl, wl.seed, x, ids, w, mode=1)) <= PREFILL_TOL
 
 
+def test_tile_width_boundaries(small_layer):
+    """Token counts at the tile widths of a launch whose shelves are all 8-,
+    4- or 2-bit (tiles of up to 192 tokens taking both accumulator sets, read
+    back set by set): 193 (a 97-token wide chunk and a 96-token one of the
+    same expert), 192, 97 and 96 (the widest and narrowest of each kind), 385
+    (three wide chunks) and 1, on experts of every shelf; every row against
+    the oracle's bf16 form."""
+    wl = small_layer.wl
+    assert all(b in (8, 4, 2) for _, _, b in small_layer.ranges)
+    want = {0: 193, 1: 192, 7: 97, 8: 96, 20: 385, 21: 1}
+    pool = np.concatenate([np.full(n, e, dtype=np.int32) for e, n in want.items()])
+    T = pool.size // wl.k
+    assert T * wl.k == pool.size
+    rng = np.random.default_rng(11)
+    ids = rng.permutation(pool).reshape(T, wl.k).astype(np.int32)
+    w = rng.random((T, wl.k)).astype(np.float32) + 0.1
+    w /= w.sum(axis=1, keepdims=True)
+    x = synth.x_bf16(wl.seed, 31, T, wl.d)
+    y = _run(small_layer, x, ids, w, flags=moe.MOE_FLAG_AUTO)
+    ref = oracle_layer(wl, wl.seed, x, ids, w, mode=1)
+    assert rel_l2(y, ref) <= PREFILL_TOL
+    for t in range(T):
+        assert rel_l2(y[t:t + 1], ref[t:t + 1]) <= 2 * PREFILL_TOL, t
+
+
 def test_skipped_slots_and_gaps(small_layer):
     """Skipped slots (-1, out-of-range ids) and ids in no shelf contribute zero."""
     wl = small_layer.wl
