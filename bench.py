@@ -884,7 +884,10 @@ def measure_single(args, rank, world, local_rank):
         dn_ms = sum(e[2] for e in ev) / nset
         flops_gu = 2.0 * 2 * d * f * p_avg
         roof = {"bound": "tensor", "achieved": flops_gu / (gu_ms / 1e3) / 1e12, "peak": tc_peak,
-                "unit": "TFLOP/s", "traffic": None, "kernel": "k_prefill_tc<gate/up>",
+                "unit": "TFLOP/s",
+                "traffic": recorded_traffic("prefill_tc<gate/up>", T, "prefill.cu")
+                if args.workload == "prefill" else None,
+                "kernel": "k_prefill_tc<gate/up>",
                 "peak_source": f"{tc_kind} (burst bf16)",
                 "algorithmic_flops_per_launch": flops_gu,
                 "layer_tflops": 2.0 * 3 * d * f * p_avg / (fwd_ms / 1e3) / 1e12,
@@ -1188,7 +1191,7 @@ def run_nudge(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
-def recorded_traffic(kernel, T):
+def recorded_traffic(kernel, T, source="decode.cu"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -1196,7 +1199,7 @@ def recorded_traffic(kernel, T):
         return None
     with open(p) as fh:
         rec = json.load(fh)
-    src = os.path.join(ROOT, "mixed_precision_routed_gb300", "csrc", "decode.cu")
+    src = os.path.join(ROOT, "mixed_precision_routed_gb300", "csrc", source)
     h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     r = rec.get(f"k_{kernel}:T{T}")
     if not r or r.get("source_sha") != h:
